@@ -1,0 +1,306 @@
+/*
+ * tp_block.h -- C ABI of the Megatron column/row tensor-parallel block with
+ * N logical shards on one GPU (sm_103a).
+ *
+ * Sources, by page title and section:
+ *  [RT]  "feat: multi-GPU tensor-parallel runtime with per-rank device
+ *        placement and cross-GPU collectives": Problem (ranks run on one
+ *        device and their partial outputs are summed locally), Design /
+ *        Forward execution (replicated residual stream; reductions after
+ *        o_proj and after down_proj), Collective backend abstraction
+ *        (copy-and-reduce), Acceptance criteria (clear errors, no silent
+ *        wrong results).
+ *  [GA]  "Gather tensor-parallel sharded parameters on read in a trace":
+ *        Change (shard-dim rule, replicated tensors, vocab padding dropped to
+ *        org_vocab_size, fused rows grouped by rank, gathered tensor is a
+ *        copy).
+ *  [MG]  "Multi-GPU & Multi-Node": How tensor parallelism works (steps 1-3,
+ *        replicated norms), Supported architectures (expert slicing with a
+ *        replicated router), Requirements & constraints (divisibility).
+ *
+ * Conventions for every call:
+ *  - All tensor arguments are plain pointers to DEVICE memory on the current
+ *    CUDA device unless stated otherwise; the caller owns them. No call keeps
+ *    a pointer after it returns, and no call frees caller memory.
+ *  - Matrices are row-major [out, in] (y = x @ W^T). Storage type of weight
+ *    matrices and KV caches is the plan's dtype; 1-D parameters (norm gamma,
+ *    biases), hidden states, router logits and partial sums are float32.
+ *  - `stream` is a cudaStream_t passed as void* (NULL: legacy default
+ *    stream). Calls that launch work are asynchronous on that stream.
+ *  - Every call validates its arguments on the host before any launch and
+ *    returns TP_OK (0) or a negative tp_status; nothing aborts, prints or
+ *    falls back to the CPU. tp_last_error() gives a message for the last
+ *    failing call on the calling thread.
+ *  - Launching calls require the current device to be compute capability
+ *    10.3 (sm_103a); otherwise they return TP_ERR_UNSUPPORTED.
+ */
+#ifndef TP_BLOCK_H
+#define TP_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TP_MAX_SHARDS 8
+#define TP_ABI_VERSION 1
+
+typedef enum tp_status {
+    TP_OK = 0,
+    TP_ERR_INVALID_ARG = -1,   /* bad size, mode or enum value */
+    TP_ERR_INDIVISIBLE = -2,   /* heads / kv heads / FFN not divisible by tp */
+    TP_ERR_UNSUPPORTED = -3,   /* device is not sm_103, or shape outside the kernels' range */
+    TP_ERR_NULL = -4,          /* a required pointer is NULL */
+    TP_ERR_ALIGN = -5,         /* a pointer is not 16-byte aligned */
+    TP_ERR_SHAPE = -6,         /* sizes inconsistent with the plan */
+    TP_ERR_CAPACITY = -7,      /* position + new tokens exceeds max_kv, or workspace too small */
+    TP_ERR_CUDA = -8,          /* a CUDA runtime call or launch failed */
+    TP_ERR_TIMEOUT = -9        /* a bounded device-side wait gave up */
+} tp_status;
+
+typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+
+typedef enum tp_mode {
+    TP_MODE_DECODE = 0,   /* one new token per sequence at pos[b] */
+    TP_MODE_PREFILL = 1,  /* T_per_seq new tokens per sequence at pos[b].. (causal) */
+    TP_MODE_MOE_FFN = 2   /* feed-forward half only, expert-sliced MoE */
+} tp_mode;
+
+/* Kinds of sharded parameter ([GA] Change): which dim is split and how the
+ * gather reassembles it. */
+typedef enum tp_param_kind {
+    TP_PARAM_REPLICATED = 0,      /* no shard stamp: every shard holds the whole tensor */
+    TP_PARAM_COLWISE = 1,         /* column-parallel: output dim (dim 0) split */
+    TP_PARAM_ROWWISE = 2,         /* row-parallel: input dim (dim 1) split */
+    TP_PARAM_FUSED_QKV = 3,       /* [q_r; k_r; v_r] per shard; gathers rank-grouped */
+    TP_PARAM_FUSED_GATE_UP = 4,   /* [gate_r; up_r] per shard; gathers rank-grouped */
+    TP_PARAM_PACKED_COLWISE = 5,  /* any stacked segments, per-shard slices stacked */
+    TP_PARAM_VOCAB_PARALLEL = 6   /* rows padded to a multiple of 64*tp, split; gather cuts to org_vocab */
+} tp_param_kind;
+
+/* Shape of one block. Attention fields may be 0 for an MoE-only block
+ * (TP_MODE_MOE_FFN); expert fields are 0 for a dense block. */
+typedef struct tp_model_desc {
+    int64_t hidden;        /* H */
+    int64_t n_heads;       /* Hq */
+    int64_t n_kv_heads;    /* Hkv */
+    int64_t head_dim;      /* d */
+    int64_t ffn;           /* F (dense SwiGLU intermediate) */
+    int64_t n_experts;     /* E (0: dense) */
+    int64_t top_k;         /* experts per token */
+    int64_t expert_ffn;    /* Fe */
+    int64_t org_vocab;     /* lm_head rows before padding (0: no head) */
+    double eps;            /* RMSNorm epsilon */
+    double rope_theta;     /* rotary base */
+    int32_t dtype;         /* tp_dtype of weight matrices and KV caches */
+    int32_t has_qkv_bias;  /* 1: q/k/v biases present */
+    int64_t max_batch;     /* sequences per call */
+    int64_t max_tokens;    /* B * T_per_seq per call */
+    int64_t max_kv;        /* KV cache capacity (positions) per sequence */
+} tp_model_desc;
+
+typedef struct tp_plan_s* tp_plan_t;
+
+/* Sizes derived by tp_plan. Row counts are per shard; *_bytes are per shard. */
+typedef struct tp_plan_info {
+    int32_t tp;
+    int32_t reduce_points;       /* row-parallel reductions per block: 2 dense, 1 MoE-only */
+    int64_t hq_shard;            /* Hq' = Hq/tp */
+    int64_t hkv_shard;           /* Hkv' */
+    int64_t ffn_shard;           /* F' */
+    int64_t expert_ffn_shard;    /* Fe' */
+    int64_t qkv_rows;            /* (Hq' + 2 Hkv') d */
+    int64_t vocab_padded;        /* org_vocab rounded up to a multiple of 64*tp */
+    int64_t vocab_rows_shard;    /* vocab_padded / tp */
+    int64_t wqkv_bytes, bqkv_bytes, wo_bytes, wgu_bytes, wd_bytes, gamma_bytes;
+    int64_t egu_bytes, ed_bytes;
+    int64_t kv_cache_bytes;      /* one of K or V: [max_batch][Hkv'][max_kv][d] */
+    int64_t lm_head_bytes;       /* [vocab_rows_shard][H] */
+    int64_t workspace_bytes;     /* scratch for tp_block_forward, any mode */
+    int64_t weight_bytes_shard;  /* all matrices of one shard */
+    int64_t weight_bytes_total;  /* all shards */
+} tp_plan_info;
+
+/* Full (unsharded) block weights, caller-owned device memory. */
+typedef struct tp_block_weights {
+    const void* wq;          /* [Hq d, H] */
+    const void* wk;          /* [Hkv d, H] */
+    const void* wv;          /* [Hkv d, H] */
+    const float* bq;         /* [Hq d] or NULL */
+    const float* bk;         /* [Hkv d] or NULL */
+    const float* bv;         /* [Hkv d] or NULL */
+    const void* wo;          /* [H, Hq d] */
+    const void* w_gate;      /* [F, H] */
+    const void* w_up;        /* [F, H] */
+    const void* w_down;      /* [H, F] */
+    const float* gamma_attn; /* [H] */
+    const float* gamma_ffn;  /* [H] */
+    const void* e_gate;      /* [E, Fe, H] */
+    const void* e_up;        /* [E, Fe, H] */
+    const void* e_down;      /* [E, H, Fe] */
+} tp_block_weights;
+
+/* Per-shard tensors, caller-allocated with the sizes in tp_plan_info. */
+typedef struct tp_shard_set {
+    void* wqkv[TP_MAX_SHARDS];        /* [qkv_rows, H]: rows q_r, then k_r, then v_r */
+    float* bqkv[TP_MAX_SHARDS];       /* [qkv_rows] or NULL */
+    void* wo[TP_MAX_SHARDS];          /* [H, Hq' d]: columns r*Hq'd.. of o_proj */
+    void* wgu[TP_MAX_SHARDS];         /* [2F', H]: gate_r rows then up_r rows */
+    void* wd[TP_MAX_SHARDS];          /* [H, F']: columns r*F'.. of down_proj */
+    float* gamma_attn[TP_MAX_SHARDS]; /* [H] replicated copy */
+    float* gamma_ffn[TP_MAX_SHARDS];  /* [H] replicated copy */
+    void* egu[TP_MAX_SHARDS];         /* [E, 2Fe', H]: per expert gate_r then up_r rows */
+    void* ed[TP_MAX_SHARDS];          /* [E, H, Fe']: per expert columns r*Fe'.. of down */
+} tp_shard_set;
+
+/* Per-shard KV caches: shard r owns KV heads [r Hkv', (r+1) Hkv').
+ * Layout [max_batch][Hkv'][max_kv][d] in the plan dtype; keys are stored
+ * after the rotary embedding. */
+typedef struct tp_kv_set {
+    void* k[TP_MAX_SHARDS];
+    void* v[TP_MAX_SHARDS];
+} tp_kv_set;
+
+/* ---------------------------------------------------------------- plan */
+
+/* Validates `d` for `tp` logical shards and builds a host-only plan
+ * ([MG] Requirements & constraints: heads, KV heads and the FFN width must
+ * divide by the degree; [RT] Design: the reduction points after o_proj and
+ * down_proj). Makes no CUDA call. The plan is owned by the caller and freed
+ * with tp_plan_destroy.
+ * Errors: TP_ERR_NULL (d or out NULL), TP_ERR_INVALID_ARG (tp outside
+ * 1..TP_MAX_SHARDS, non-positive sizes, Hq % Hkv != 0, unknown dtype),
+ * TP_ERR_INDIVISIBLE (Hq, Hkv, F or Fe not divisible by tp),
+ * TP_ERR_UNSUPPORTED (sizes outside what the kernels handle: head_dim not 64
+ * or 128, H or per-shard widths not multiples of 64). */
+tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out);
+
+/* Frees a plan. NULL is accepted. */
+void tp_plan_destroy(tp_plan_t plan);
+
+/* Copies the derived sizes into `out` (host memory). */
+tp_status tp_plan_get_info(tp_plan_t plan, tp_plan_info* out);
+
+/* Writes a one-line text description (per-shard bytes and shapes, showing
+ * that each shard holds about 1/tp of the weights, [RT] Acceptance
+ * criteria) into `buf` (host, `n` bytes, NUL-terminated, truncated). */
+tp_status tp_plan_describe(tp_plan_t plan, char* buf, size_t n);
+
+/* ----------------------------------------------------- shard and gather */
+
+/* Builds every shard's tensors from the full block weights ([MG] How tensor
+ * parallelism works: QKV and gate/up split their output dim, o_proj and
+ * down_proj their input dim; norms replicated; [MG] Supported architectures:
+ * each shard holds 1/tp of every expert). Bit-exact copies, asynchronous on
+ * `stream`. Pointers in `full` that the block does not use may be NULL.
+ * Errors: TP_ERR_NULL, TP_ERR_ALIGN (matrix pointers must be 16-byte
+ * aligned), TP_ERR_UNSUPPORTED, TP_ERR_CUDA. */
+tp_status tp_shard_weights(tp_plan_t plan, const tp_block_weights* full,
+                           const tp_shard_set* out, void* stream);
+
+/* Shards one tensor of kind `k`. `full` is [rows, cols] of `dtype`
+ * (TP_F32 or TP_BF16); `shards_out` is a HOST array of tp device pointers,
+ * each sized for one shard. Fused kinds take `segments` (host array of
+ * `n_segments` row counts summing to `rows`); for FUSED_QKV and
+ * FUSED_GATE_UP a NULL `segments` means the plan's (Hq d, Hkv d, Hkv d) or
+ * (F, F). VOCAB_PARALLEL takes rows = org_vocab and writes padding rows of
+ * zeros at the tail of the last shard. REPLICATED copies to every shard.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE (a dim not divisible as required),
+ * TP_ERR_INVALID_ARG, TP_ERR_CUDA. */
+tp_status tp_shard_param(tp_plan_t plan, int32_t k, const void* full,
+                         int64_t rows, int64_t cols, int32_t dtype,
+                         const int64_t* segments, int32_t n_segments,
+                         void* const* shards_out, void* stream);
+
+/* All-gathers a sharded parameter into `out` ([GA] Change):
+ *  REPLICATED: out = shard 0 ([rows, cols]);
+ *  COLWISE / FUSED_QKV / FUSED_GATE_UP / PACKED_COLWISE: shards stacked on
+ *    dim 0 in rank order ([tp*rows, cols]); fused rows therefore come back
+ *    grouped by rank, the layout whose x @ W^T equals the concatenated shard
+ *    outputs;
+ *  ROWWISE: shards concatenated on dim 1 ([rows, tp*cols]);
+ *  VOCAB_PARALLEL: shards stacked, rows >= org_vocab dropped
+ *    ([org_vocab, cols]).
+ * `shards` is a HOST array of tp device pointers, each [rows, cols] of
+ * `dtype`. `out` is caller-allocated at the full size. The result is a copy;
+ * the shards are read only. Bit-exact. Uses 16-byte vector copies when rows
+ * are 16-byte aligned, element copies otherwise (no error).
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE (e.g. org_vocab > tp*rows),
+ * TP_ERR_INVALID_ARG, TP_ERR_CUDA. */
+tp_status tp_gather_param(tp_plan_t plan, int32_t k, const void* const* shards,
+                          int64_t rows_per_shard, int64_t cols_per_shard,
+                          int32_t dtype, void* out, void* stream);
+
+/* ------------------------------------------------------------- forward */
+
+/* Zeroes the control words (completion counters, status) at the start of a
+ * workspace. Call once after allocating a workspace and before its first
+ * tp_block_forward; the kernels leave the counters at zero after each
+ * call. `bytes` >= tp_plan_info.workspace_bytes. */
+tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t bytes, void* stream);
+
+/* One tensor-parallel block over all tp logical shards ([MG] How tensor
+ * parallelism works, steps 1-3; [RT] Design / Forward execution):
+ *   DECODE / PREFILL:  h = x + sum_r Attn_r(RMSNorm(x)) Wo_r^T,
+ *                      y = h + sum_r SwiGLU_r(RMSNorm(h)) Wd_r^T,
+ *     column-parallel QKV and gate/up per shard, rotate-half RoPE, K/V
+ *     appended to each shard's cache at positions pos[b]..pos[b]+T_per_seq-1,
+ *     grouped-query attention over the shard's own heads (causal), and the
+ *     row-parallel partials summed in rank order (((p0 + p1) + p2) + ...)
+ *     in float32 before the residual is added.
+ *   MOE_FFN: y = x + sum_r sum_j w_tj SwiGLU_{e_tj, r}(RMSNorm(x)_t), with
+ *     softmax top-k routing of `router_logits` ([T, E] float32), ties to the
+ *     lower expert id, weights renormalised; j-order then rank-order sums.
+ * x and y are float32 [B*T_per_seq, H], rows sequence-major, y != x. pos is
+ * DEVICE int32 [B]. `workspace` holds `workspace_bytes` >= the plan's
+ * workspace_bytes and was set up by tp_workspace_init. Results are
+ * deterministic (byte-identical across calls on the same inputs).
+ * Positions past max_kv are not written; the kernels record
+ * TP_ERR_CAPACITY in the workspace status word (tp_get_device_status).
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE (B or tokens above the plan's maxima,
+ * T_per_seq != 1 in DECODE), TP_ERR_CAPACITY (workspace too small),
+ * TP_ERR_INVALID_ARG (mode not valid for the plan), TP_ERR_UNSUPPORTED,
+ * TP_ERR_CUDA. */
+tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
+                           const float* x, float* y, const int32_t* pos,
+                           int32_t B, int32_t T_per_seq, int32_t mode,
+                           const float* router_logits,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Standalone rank-order reduction ([RT] Collective backend abstraction,
+ * copy-and-reduce; [MG] Local TP: the add after the copies):
+ *   out[m, :] = residual[m, :] + (((p_0 + p_1) + p_2) + ... + p_{tp-1})[m, :] + bias
+ * partials is float32 [tp][M][H] (contiguous), residual float32 [M, H] or
+ * NULL, bias float32 [H] or NULL (a row-parallel bias is replicated and
+ * added once, after the sum), out float32 [M, H]. out may alias residual.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE (M < 0), TP_ERR_CUDA. */
+tp_status tp_reduce_partials(tp_plan_t plan, const float* partials, const float* residual,
+                             const float* bias, float* out, int64_t M, void* stream);
+
+/* Reads the workspace status word (TP_OK or the first device-detected error
+ * since tp_workspace_init) into *out (host). Synchronises `stream`. */
+tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);
+
+/* Measurement hook: while set, tp_block_forward records events[i]
+ * (cudaEvent_t values passed as void*, created by the caller) on its stream
+ * before launching stage i and events[n_events-1] after the last stage, so
+ * a caller can time each kernel. Decode has 5 stages (qkv+rope, attention,
+ * o_proj+reduce, gate_up+swiglu, down+reduce): pass 6 events. n_events = 0
+ * or events = NULL clears the hook. The array is copied. */
+tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int32_t n_events);
+
+/* ----------------------------------------------------------------- misc */
+
+/* Message for the last failing call on this thread ("" if none). Never fails. */
+const char* tp_last_error(void);
+
+/* TP_ABI_VERSION. */
+int32_t tp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_BLOCK_H */

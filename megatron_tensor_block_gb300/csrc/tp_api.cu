@@ -1,0 +1,686 @@
+// C ABI of the tensor-parallel block library: plan validation and sizes,
+// workspace layout, argument checks, and the launch sequence of each call.
+// Every step of the block runs in the kernels of this library; there is no
+// host-side or CPU fallback path.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "tp_internal.h"
+
+using namespace tpk;
+
+// ---------------------------------------------------------------- errors
+
+static thread_local char g_err[512];
+
+static tp_status fail(tp_status code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static tp_status ok() {
+    g_err[0] = '\0';
+    return TP_OK;
+}
+
+static tp_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(TP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define TP_CUDA(call, what)                              \
+    do {                                                 \
+        cudaError_t e_ = (call);                         \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+// ---------------------------------------------------------------- plan
+
+struct tp_plan_s {
+    tp_model_desc d;
+    int N = 1;
+    tp_plan_info info{};
+    bool dense = false, moe = false;
+    size_t esz = 4;                     // bytes per stored weight/KV element
+    // decode launch shapes
+    GemvShape g_qkv, g_o, g_gu, g_down;
+    int attn_chunks = 0, attn_groups = 0;
+    // workspace layout (byte offsets)
+    size_t off_status = 0, off_cnt_qkv = 0, off_cnt_attn = 0, off_cnt_o = 0, off_cnt_gu = 0,
+           off_cnt_down = 0, ctrl_bytes = 0;
+    size_t off_q = 0, off_attn_part = 0, off_attn_out = 0, off_h = 0, off_act = 0;
+    size_t off_part_qkv = 0, off_part_o = 0, off_part_gu = 0, off_part_down = 0;
+    size_t ws_bytes = 0;
+    // measurement hook (tp_profile_stages)
+    cudaEvent_t stage_ev[16] = {};
+    int n_stage_ev = 0;
+};
+
+static void stage_mark(tp_plan_t P, int i, cudaStream_t s) {
+    if (i < P->n_stage_ev && P->stage_ev[i]) cudaEventRecord(P->stage_ev[i], s);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Smallest number of reduction chunks per shard such that the launch has at
+// least `target` work units, with chunk lengths that are whole 64-element
+// steps, at least two steps (both k-halves of a CTA busy) and at most
+// `max_steps` steps (shared-memory bound).
+static int pick_chunks(int steps, long units_per_chunk, int max_steps, long target) {
+    int best = -1;
+    for (int C = 1; C <= steps; ++C) {
+        if (steps % C) continue;
+        const int len = steps / C;
+        if (len > max_steps) continue;
+        if (len < 2 && steps >= 2) continue;
+        best = C;
+        if (units_per_chunk * C >= target) return C;
+    }
+    return best > 0 ? best : steps;
+}
+
+static GemvShape make_shape(int groups, int shards_per_group, int K, size_t esz) {
+    GemvShape s;
+    s.groups = groups;
+    s.shards_per_group = shards_per_group;
+    const int steps = K / kKStep;
+    const int max_steps = (esz == 2 ? 2048 : 1024) / kKStep;
+    s.chunks = pick_chunks(steps, (long)groups * shards_per_group, max_steps, 4L * kSMs);
+    s.kc = K / s.chunks;
+    return s;
+}
+
+extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out) {
+    if (!d || !out) return fail(TP_ERR_NULL, "tp_plan: desc and out must not be NULL");
+    *out = nullptr;
+    if (tp < 1 || tp > TP_MAX_SHARDS)
+        return fail(TP_ERR_INVALID_ARG, "tp_plan: tp=%d outside 1..%d", tp, TP_MAX_SHARDS);
+    if (d->dtype != TP_F32 && d->dtype != TP_BF16)
+        return fail(TP_ERR_INVALID_ARG, "tp_plan: unknown dtype %d", d->dtype);
+    if (d->hidden <= 0) return fail(TP_ERR_INVALID_ARG, "tp_plan: hidden must be positive");
+    const bool dense = d->n_heads > 0;
+    const bool moe = d->n_experts > 0;
+    if (!dense && !moe) return fail(TP_ERR_INVALID_ARG, "tp_plan: neither attention heads nor experts given");
+    if (d->max_batch <= 0 || d->max_tokens <= 0)
+        return fail(TP_ERR_INVALID_ARG, "tp_plan: max_batch and max_tokens must be positive");
+    if (d->org_vocab < 0) return fail(TP_ERR_INVALID_ARG, "tp_plan: org_vocab must be >= 0");
+    if (!(d->eps >= 0.0)) return fail(TP_ERR_INVALID_ARG, "tp_plan: eps must be >= 0");
+    if (dense) {
+        if (d->n_kv_heads <= 0 || d->head_dim <= 0 || d->ffn <= 0 || d->max_kv <= 0)
+            return fail(TP_ERR_INVALID_ARG, "tp_plan: n_kv_heads, head_dim, ffn and max_kv must be positive");
+        if (d->n_heads % d->n_kv_heads)
+            return fail(TP_ERR_INVALID_ARG, "tp_plan: n_heads=%lld not a multiple of n_kv_heads=%lld",
+                        (long long)d->n_heads, (long long)d->n_kv_heads);
+        if (!(d->rope_theta > 0.0)) return fail(TP_ERR_INVALID_ARG, "tp_plan: rope_theta must be positive");
+        if (d->n_heads % tp)
+            return fail(TP_ERR_INDIVISIBLE, "tp_plan: n_heads=%lld not divisible by tp=%d", (long long)d->n_heads, tp);
+        if (d->n_kv_heads % tp)
+            return fail(TP_ERR_INDIVISIBLE, "tp_plan: n_kv_heads=%lld not divisible by tp=%d", (long long)d->n_kv_heads, tp);
+        if (d->ffn % tp)
+            return fail(TP_ERR_INDIVISIBLE, "tp_plan: ffn=%lld not divisible by tp=%d", (long long)d->ffn, tp);
+    }
+    if (moe) {
+        if (d->top_k < 1 || d->top_k > d->n_experts || d->expert_ffn <= 0)
+            return fail(TP_ERR_INVALID_ARG, "tp_plan: need 1 <= top_k <= n_experts and expert_ffn > 0");
+        if (d->expert_ffn % tp)
+            return fail(TP_ERR_INDIVISIBLE, "tp_plan: expert_ffn=%lld not divisible by tp=%d", (long long)d->expert_ffn, tp);
+    }
+    // ranges the kernels handle
+    if (d->hidden % 64) return fail(TP_ERR_UNSUPPORTED, "tp_plan: hidden must be a multiple of 64");
+    if (dense) {
+        if (d->head_dim != 64 && d->head_dim != 128)
+            return fail(TP_ERR_UNSUPPORTED, "tp_plan: head_dim must be 64 or 128");
+        if ((d->ffn / tp) % 64) return fail(TP_ERR_UNSUPPORTED, "tp_plan: ffn/tp must be a multiple of 64");
+        if (d->n_heads / d->n_kv_heads > 8)
+            return fail(TP_ERR_UNSUPPORTED, "tp_plan: more than 8 query heads per KV head");
+    }
+    if (moe && (d->expert_ffn / tp) % 64)
+        return fail(TP_ERR_UNSUPPORTED, "tp_plan: expert_ffn/tp must be a multiple of 64");
+
+    tp_plan_s* P = new (std::nothrow) tp_plan_s();
+    if (!P) return fail(TP_ERR_INVALID_ARG, "tp_plan: out of host memory");
+    P->d = *d;
+    P->N = tp;
+    P->dense = dense;
+    P->moe = moe;
+    P->esz = d->dtype == TP_BF16 ? 2 : 4;
+    const int64_t N = tp, H = d->hidden, esz = (int64_t)P->esz;
+    tp_plan_info& I = P->info;
+    I.tp = tp;
+    I.reduce_points = dense ? 2 : 1;
+    if (dense) {
+        I.hq_shard = d->n_heads / N;
+        I.hkv_shard = d->n_kv_heads / N;
+        I.ffn_shard = d->ffn / N;
+        I.qkv_rows = (I.hq_shard + 2 * I.hkv_shard) * d->head_dim;
+        I.wqkv_bytes = I.qkv_rows * H * esz;
+        I.bqkv_bytes = d->has_qkv_bias ? I.qkv_rows * 4 : 0;
+        I.wo_bytes = H * I.hq_shard * d->head_dim * esz;
+        I.wgu_bytes = 2 * I.ffn_shard * H * esz;
+        I.wd_bytes = H * I.ffn_shard * esz;
+        I.kv_cache_bytes = d->max_batch * I.hkv_shard * d->max_kv * d->head_dim * esz;
+    }
+    I.gamma_bytes = H * 4;
+    if (moe) {
+        I.expert_ffn_shard = d->expert_ffn / N;
+        I.egu_bytes = d->n_experts * 2 * I.expert_ffn_shard * H * esz;
+        I.ed_bytes = d->n_experts * H * I.expert_ffn_shard * esz;
+    }
+    if (d->org_vocab > 0) {
+        const int64_t m = 64 * N;
+        I.vocab_padded = (d->org_vocab + m - 1) / m * m;
+        I.vocab_rows_shard = I.vocab_padded / N;
+        I.lm_head_bytes = I.vocab_rows_shard * H * esz;
+    }
+    I.weight_bytes_shard = I.wqkv_bytes + I.wo_bytes + I.wgu_bytes + I.wd_bytes + I.egu_bytes + I.ed_bytes;
+    I.weight_bytes_total = I.weight_bytes_shard * N;
+
+    // ---- workspace layout: control words first, then the data buffers
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    P->off_status = take(sizeof(int));
+    if (dense) {
+        const int hd = (int)d->head_dim;
+        P->g_qkv = make_shape((int)(N * I.qkv_rows / kTileRows), 1, (int)H, P->esz);
+        P->g_o = make_shape((int)(H / kTileRows), (int)N, (int)(I.hq_shard * hd), P->esz);
+        P->g_gu = make_shape((int)(N * I.ffn_shard / 32), 1, (int)H, P->esz);
+        P->g_down = make_shape((int)(H / kTileRows), (int)N, (int)I.ffn_shard, P->esz);
+        P->attn_chunks = (int)((d->max_kv + kAttnChunk - 1) / kAttnChunk);
+        P->attn_groups = (int)(N * (d->max_batch < kTMax ? d->max_batch : kTMax) * I.hkv_shard);
+        P->off_cnt_qkv = take(sizeof(unsigned) * P->g_qkv.groups);
+        P->off_cnt_attn = take(sizeof(unsigned) * P->attn_groups);
+        P->off_cnt_o = take(sizeof(unsigned) * P->g_o.groups);
+        P->off_cnt_gu = take(sizeof(unsigned) * P->g_gu.groups);
+        P->off_cnt_down = take(sizeof(unsigned) * P->g_down.groups);
+    }
+    P->ctrl_bytes = off;
+    if (dense) {
+        const int64_t hd = d->head_dim, G = d->n_heads / d->n_kv_heads;
+        P->off_q = take((size_t)kTMax * d->n_heads * hd * 4);
+        P->off_attn_part = take((size_t)P->attn_groups * P->attn_chunks * G * (hd + 2) * 4);
+        P->off_attn_out = take((size_t)kTMax * d->n_heads * hd * esz);
+        P->off_h = take((size_t)kTMax * H * 4);
+        P->off_act = take((size_t)kTMax * d->ffn * esz);
+        P->off_part_qkv = take((size_t)P->g_qkv.units() * kPartStride * 4);
+        P->off_part_o = take((size_t)P->g_o.units() * kPartStride * 4);
+        P->off_part_gu = take((size_t)P->g_gu.units() * kPartStride * 4);
+        P->off_part_down = take((size_t)P->g_down.units() * kPartStride * 4);
+    }
+    P->ws_bytes = off;
+    I.workspace_bytes = (int64_t)P->ws_bytes;
+    *out = P;
+    return ok();
+}
+
+extern "C" void tp_plan_destroy(tp_plan_t plan) { delete plan; }
+
+extern "C" tp_status tp_plan_get_info(tp_plan_t plan, tp_plan_info* out) {
+    if (!plan || !out) return fail(TP_ERR_NULL, "tp_plan_get_info: NULL argument");
+    *out = plan->info;
+    return ok();
+}
+
+extern "C" tp_status tp_plan_describe(tp_plan_t plan, char* buf, size_t n) {
+    if (!plan || !buf || n == 0) return fail(TP_ERR_NULL, "tp_plan_describe: NULL argument");
+    const tp_plan_info& I = plan->info;
+    const double total = (double)I.weight_bytes_total, shard = (double)I.weight_bytes_shard;
+    snprintf(buf, n,
+             "tensor parallelism: %d logical shards on one GPU; per shard: qkv [%lld x %lld], "
+             "o [%lld x %lld], gate_up [%lld x %lld], down [%lld x %lld], experts %lld x [%lld x %lld]; "
+             "weights %.3f MB per shard = %.4f of %.3f MB total; %d reductions per block; workspace %lld bytes",
+             I.tp, (long long)I.qkv_rows, (long long)plan->d.hidden, (long long)plan->d.hidden,
+             (long long)(I.hq_shard * plan->d.head_dim), (long long)(2 * I.ffn_shard), (long long)plan->d.hidden,
+             (long long)plan->d.hidden, (long long)I.ffn_shard, (long long)plan->d.n_experts,
+             (long long)(2 * I.expert_ffn_shard), (long long)plan->d.hidden, shard / 1e6,
+             total > 0 ? shard / total : 0.0, total / 1e6, I.reduce_points, (long long)I.workspace_bytes);
+    return ok();
+}
+
+// ---------------------------------------------------------------- device checks
+
+static tp_status check_device() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(TP_ERR_UNSUPPORTED, "no usable CUDA device: %s", cudaGetErrorString(e));
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(TP_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    return TP_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ---------------------------------------------------------------- shard / gather
+
+namespace {
+struct Batcher {
+    CopyBatch b{};
+    cudaStream_t s;
+    cudaError_t err = cudaSuccess;
+    explicit Batcher(cudaStream_t st) : s(st) { b.n = 0; }
+    void add(const void* src, void* dst, int64_t rows, int64_t row_bytes, int64_t sp, int64_t dp) {
+        if (rows <= 0 || row_bytes <= 0) return;
+        if (b.n == kMaxCopyDescs) flush();
+        b.d[b.n++] = CopyDesc{src, dst, rows, row_bytes, sp, dp};
+    }
+    void flush() {
+        if (b.n && err == cudaSuccess) err = launch_copy_batch(b, s);
+        b.n = 0;
+    }
+};
+const char* cptr(const void* p, int64_t off) { return static_cast<const char*>(p) + off; }
+char* mptr(void* p, int64_t off) { return static_cast<char*>(p) + off; }
+}  // namespace
+
+extern "C" tp_status tp_shard_weights(tp_plan_t plan, const tp_block_weights* full,
+                                      const tp_shard_set* out, void* stream) {
+    if (!plan || !full || !out) return fail(TP_ERR_NULL, "tp_shard_weights: NULL argument");
+    tp_status st = check_device();
+    if (st) return st;
+    const tp_model_desc& d = plan->d;
+    const int N = plan->N;
+    const tp_plan_info& I = plan->info;
+    const int64_t H = d.hidden, es = (int64_t)plan->esz;
+    if (!full->gamma_attn && plan->dense) return fail(TP_ERR_NULL, "tp_shard_weights: gamma_attn is NULL");
+    if (!full->gamma_ffn) return fail(TP_ERR_NULL, "tp_shard_weights: gamma_ffn is NULL");
+    for (int r = 0; r < N; ++r)
+        if (!out->gamma_ffn[r] || (plan->dense && !out->gamma_attn[r]))
+            return fail(TP_ERR_NULL, "tp_shard_weights: shard %d gamma buffer is NULL", r);
+    Batcher B(static_cast<cudaStream_t>(stream));
+    if (plan->dense) {
+        const void* need[] = {full->wq, full->wk, full->wv, full->wo, full->w_gate, full->w_up, full->w_down};
+        for (const void* p : need) {
+            if (!p) return fail(TP_ERR_NULL, "tp_shard_weights: a dense weight pointer is NULL");
+            if (!aligned16(p)) return fail(TP_ERR_ALIGN, "tp_shard_weights: weight pointers must be 16-byte aligned");
+        }
+        if (d.has_qkv_bias && (!full->bq || !full->bk || !full->bv))
+            return fail(TP_ERR_NULL, "tp_shard_weights: plan has q/k/v biases but a bias pointer is NULL");
+        const int64_t hd = d.head_dim, qr = I.hq_shard * hd, kr = I.hkv_shard * hd, Fs = I.ffn_shard;
+        for (int r = 0; r < N; ++r) {
+            if (!out->wqkv[r] || !out->wo[r] || !out->wgu[r] || !out->wd[r] || (d.has_qkv_bias && !out->bqkv[r]))
+                return fail(TP_ERR_NULL, "tp_shard_weights: shard %d output buffer is NULL", r);
+            const int64_t row = H * es;
+            // fused [q_r; k_r; v_r]
+            B.add(cptr(full->wq, r * qr * row), mptr(out->wqkv[r], 0), qr, row, row, row);
+            B.add(cptr(full->wk, r * kr * row), mptr(out->wqkv[r], qr * row), kr, row, row, row);
+            B.add(cptr(full->wv, r * kr * row), mptr(out->wqkv[r], (qr + kr) * row), kr, row, row, row);
+            if (d.has_qkv_bias) {
+                B.add(cptr(full->bq, r * qr * 4), mptr(out->bqkv[r], 0), 1, qr * 4, qr * 4, qr * 4);
+                B.add(cptr(full->bk, r * kr * 4), mptr(out->bqkv[r], qr * 4), 1, kr * 4, kr * 4, kr * 4);
+                B.add(cptr(full->bv, r * kr * 4), mptr(out->bqkv[r], (qr + kr) * 4), 1, kr * 4, kr * 4, kr * 4);
+            }
+            // o_proj: columns [r*Hq'd, (r+1)*Hq'd)
+            B.add(cptr(full->wo, r * qr * es), out->wo[r], H, qr * es, d.n_heads * hd * es, qr * es);
+            // fused [gate_r; up_r]
+            B.add(cptr(full->w_gate, r * Fs * row), mptr(out->wgu[r], 0), Fs, row, row, row);
+            B.add(cptr(full->w_up, r * Fs * row), mptr(out->wgu[r], Fs * row), Fs, row, row, row);
+            // down_proj: columns [r*F', (r+1)*F')
+            B.add(cptr(full->w_down, r * Fs * es), out->wd[r], H, Fs * es, d.ffn * es, Fs * es);
+            B.add(full->gamma_attn, out->gamma_attn[r], 1, H * 4, H * 4, H * 4);
+        }
+    }
+    if (plan->moe) {
+        if (!full->e_gate || !full->e_up || !full->e_down)
+            return fail(TP_ERR_NULL, "tp_shard_weights: expert weight pointer is NULL");
+        const int64_t E = d.n_experts, Fe = d.expert_ffn, Fs = I.expert_ffn_shard, row = H * es;
+        for (int r = 0; r < N; ++r) {
+            if (!out->egu[r] || !out->ed[r]) return fail(TP_ERR_NULL, "tp_shard_weights: shard %d expert buffer is NULL", r);
+            // every expert: gate rows and up rows [r*Fe', (r+1)*Fe') -> [E][2Fe'][H]
+            B.add(cptr(full->e_gate, r * Fs * row), mptr(out->egu[r], 0), E, Fs * row, Fe * row, 2 * Fs * row);
+            B.add(cptr(full->e_up, r * Fs * row), mptr(out->egu[r], Fs * row), E, Fs * row, Fe * row, 2 * Fs * row);
+            // down columns [r*Fe', (r+1)*Fe') of every [H, Fe] -> [E][H][Fe']
+            B.add(cptr(full->e_down, r * Fs * es), out->ed[r], E * H, Fs * es, Fe * es, Fs * es);
+        }
+    }
+    for (int r = 0; r < N; ++r) B.add(full->gamma_ffn, out->gamma_ffn[r], 1, H * 4, H * 4, H * 4);
+    B.flush();
+    if (B.err != cudaSuccess) return cuda_fail(B.err, "tp_shard_weights: copy launch");
+    return ok();
+}
+
+static tp_status default_segments(tp_plan_t plan, int32_t k, const int64_t* segments, int32_t nseg,
+                                  int64_t rows, int64_t* seg, int* ns) {
+    if (segments && nseg > 0) {
+        if (nseg > 16) return fail(TP_ERR_INVALID_ARG, "at most 16 segments");
+        for (int i = 0; i < nseg; ++i) seg[i] = segments[i];
+        *ns = nseg;
+    } else if (k == TP_PARAM_FUSED_QKV && plan->dense) {
+        seg[0] = plan->d.n_heads * plan->d.head_dim;
+        seg[1] = seg[2] = plan->d.n_kv_heads * plan->d.head_dim;
+        *ns = 3;
+    } else if (k == TP_PARAM_FUSED_GATE_UP && plan->dense) {
+        seg[0] = seg[1] = plan->d.ffn;
+        *ns = 2;
+    } else {
+        return fail(TP_ERR_INVALID_ARG, "fused/packed kind needs segment row counts");
+    }
+    int64_t sum = 0;
+    for (int i = 0; i < *ns; ++i) {
+        if (seg[i] <= 0 || seg[i] % plan->N) return fail(TP_ERR_SHAPE, "segment %d rows %lld not divisible by tp=%d", i, (long long)seg[i], plan->N);
+        sum += seg[i];
+    }
+    if (sum != rows) return fail(TP_ERR_SHAPE, "segments sum to %lld rows, tensor has %lld", (long long)sum, (long long)rows);
+    return TP_OK;
+}
+
+extern "C" tp_status tp_shard_param(tp_plan_t plan, int32_t k, const void* full, int64_t rows,
+                                    int64_t cols, int32_t dtype, const int64_t* segments,
+                                    int32_t n_segments, void* const* shards_out, void* stream) {
+    if (!plan || !full || !shards_out) return fail(TP_ERR_NULL, "tp_shard_param: NULL argument");
+    if (dtype != TP_F32 && dtype != TP_BF16) return fail(TP_ERR_INVALID_ARG, "tp_shard_param: unknown dtype");
+    if (rows <= 0 || cols <= 0) return fail(TP_ERR_SHAPE, "tp_shard_param: rows and cols must be positive");
+    const int N = plan->N;
+    for (int r = 0; r < N; ++r)
+        if (!shards_out[r]) return fail(TP_ERR_NULL, "tp_shard_param: shard %d pointer is NULL", r);
+    tp_status st = check_device();
+    if (st) return st;
+    const int64_t es = dtype == TP_BF16 ? 2 : 4, row = cols * es;
+    Batcher B(static_cast<cudaStream_t>(stream));
+    switch (k) {
+        case TP_PARAM_REPLICATED:
+            for (int r = 0; r < N; ++r) B.add(full, shards_out[r], rows, row, row, row);
+            break;
+        case TP_PARAM_COLWISE: {
+            if (rows % N) return fail(TP_ERR_SHAPE, "tp_shard_param: rows %lld not divisible by tp", (long long)rows);
+            const int64_t R = rows / N;
+            for (int r = 0; r < N; ++r) B.add(cptr(full, r * R * row), shards_out[r], R, row, row, row);
+            break;
+        }
+        case TP_PARAM_ROWWISE: {
+            if (cols % N) return fail(TP_ERR_SHAPE, "tp_shard_param: cols %lld not divisible by tp", (long long)cols);
+            const int64_t C = cols / N;
+            for (int r = 0; r < N; ++r) B.add(cptr(full, r * C * es), shards_out[r], rows, C * es, row, C * es);
+            break;
+        }
+        case TP_PARAM_FUSED_QKV:
+        case TP_PARAM_FUSED_GATE_UP:
+        case TP_PARAM_PACKED_COLWISE: {
+            int64_t seg[16];
+            int ns = 0;
+            st = default_segments(plan, k, segments, n_segments, rows, seg, &ns);
+            if (st) return st;
+            for (int r = 0; r < N; ++r) {
+                int64_t src0 = 0, dst0 = 0;
+                for (int i = 0; i < ns; ++i) {
+                    const int64_t R = seg[i] / N;
+                    B.add(cptr(full, (src0 + r * R) * row), mptr(shards_out[r], dst0 * row), R, row, row, row);
+                    src0 += seg[i];
+                    dst0 += R;
+                }
+            }
+            break;
+        }
+        case TP_PARAM_VOCAB_PARALLEL: {
+            const int64_t m = 64 * (int64_t)N, padded = (rows + m - 1) / m * m, R = padded / N;
+            for (int r = 0; r < N; ++r) {
+                int64_t have = rows - r * R;
+                have = have < 0 ? 0 : (have > R ? R : have);
+                B.add(cptr(full, r * R * row), shards_out[r], have, row, row, row);
+                B.add(nullptr, mptr(shards_out[r], have * row), R - have, row, row, row);
+            }
+            break;
+        }
+        default:
+            return fail(TP_ERR_INVALID_ARG, "tp_shard_param: unknown kind %d", k);
+    }
+    B.flush();
+    if (B.err != cudaSuccess) return cuda_fail(B.err, "tp_shard_param: copy launch");
+    return ok();
+}
+
+extern "C" tp_status tp_gather_param(tp_plan_t plan, int32_t k, const void* const* shards,
+                                     int64_t rows_per_shard, int64_t cols_per_shard, int32_t dtype,
+                                     void* out, void* stream) {
+    if (!plan || !shards || !out) return fail(TP_ERR_NULL, "tp_gather_param: NULL argument");
+    if (dtype != TP_F32 && dtype != TP_BF16) return fail(TP_ERR_INVALID_ARG, "tp_gather_param: unknown dtype");
+    if (rows_per_shard <= 0 || cols_per_shard <= 0)
+        return fail(TP_ERR_SHAPE, "tp_gather_param: rows and cols must be positive");
+    const int N = plan->N;
+    for (int r = 0; r < N; ++r)
+        if (!shards[r]) return fail(TP_ERR_NULL, "tp_gather_param: shard %d pointer is NULL", r);
+    if (k < TP_PARAM_REPLICATED || k > TP_PARAM_VOCAB_PARALLEL)
+        return fail(TP_ERR_INVALID_ARG, "tp_gather_param: unknown kind %d", k);
+    const int64_t org = plan->d.org_vocab;
+    if (k == TP_PARAM_VOCAB_PARALLEL && (org <= 0 || org > N * rows_per_shard))
+        return fail(TP_ERR_SHAPE, "tp_gather_param: org_vocab=%lld outside 1..%lld", (long long)org,
+                    (long long)(N * rows_per_shard));
+    tp_status st = check_device();
+    if (st) return st;
+    const int64_t es = dtype == TP_BF16 ? 2 : 4, R = rows_per_shard, C = cols_per_shard, row = C * es;
+    Batcher B(static_cast<cudaStream_t>(stream));
+    if (k == TP_PARAM_REPLICATED) {
+        B.add(shards[0], out, R, row, row, row);
+    } else if (k == TP_PARAM_ROWWISE) {
+        for (int r = 0; r < N; ++r) B.add(shards[r], mptr(out, r * row), R, row, row, N * row);
+    } else {
+        for (int r = 0; r < N; ++r) {
+            int64_t n = R;
+            if (k == TP_PARAM_VOCAB_PARALLEL) {
+                n = org - r * R;
+                n = n < 0 ? 0 : (n > R ? R : n);
+            }
+            B.add(shards[r], mptr(out, r * R * row), n, row, row, row);
+        }
+    }
+    B.flush();
+    if (B.err != cudaSuccess) return cuda_fail(B.err, "tp_gather_param: copy launch");
+    return ok();
+}
+
+// ---------------------------------------------------------------- forward
+
+extern "C" tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t bytes, void* stream) {
+    if (!plan || !workspace) return fail(TP_ERR_NULL, "tp_workspace_init: NULL argument");
+    if (bytes < plan->ws_bytes)
+        return fail(TP_ERR_CAPACITY, "tp_workspace_init: workspace %zu bytes < required %zu", bytes, plan->ws_bytes);
+    if (!aligned16(workspace)) return fail(TP_ERR_ALIGN, "tp_workspace_init: workspace must be 16-byte aligned");
+    tp_status st = check_device();
+    if (st) return st;
+    TP_CUDA(cudaMemsetAsync(workspace, 0, plan->ctrl_bytes, static_cast<cudaStream_t>(stream)),
+            "tp_workspace_init: memset");
+    return ok();
+}
+
+static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_set* kv, const float* x,
+                                float* y, const int32_t* pos, int B, char* ws, cudaStream_t s) {
+    const tp_model_desc& d = P->d;
+    const tp_plan_info& I = P->info;
+    const int N = P->N, T = B;
+    for (int r = 0; r < N; ++r) {
+        if (!w->wqkv[r] || !w->wo[r] || !w->wgu[r] || !w->wd[r] || !w->gamma_attn[r] || !w->gamma_ffn[r])
+            return fail(TP_ERR_NULL, "tp_block_forward: shard %d weight pointer is NULL", r);
+        if (d.has_qkv_bias && !w->bqkv[r]) return fail(TP_ERR_NULL, "tp_block_forward: shard %d bias is NULL", r);
+        if (!kv->k[r] || !kv->v[r]) return fail(TP_ERR_NULL, "tp_block_forward: shard %d KV cache is NULL", r);
+        const void* al[] = {w->wqkv[r], w->wo[r], w->wgu[r], w->wd[r], w->gamma_attn[r], w->gamma_ffn[r]};
+        for (const void* p : al)
+            if (!aligned16(p)) return fail(TP_ERR_ALIGN, "tp_block_forward: shard %d pointer not 16-byte aligned", r);
+    }
+    int* status = reinterpret_cast<int*>(ws + P->off_status);
+    const size_t es = P->esz;
+    const int hd = (int)d.head_dim;
+
+    GemvParams q{};
+    q.n_shards = N;
+    q.rows = (int)I.qkv_rows;
+    q.K = (int)d.hidden;
+    q.T = T;
+    q.shape = P->g_qkv;
+    q.x = x;
+    q.eps = (float)d.eps;
+    q.part = reinterpret_cast<float*>(ws + P->off_part_qkv);
+    q.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_qkv);
+    q.status = status;
+    q.q_out = reinterpret_cast<float*>(ws + P->off_q);
+    q.pos = pos;
+    q.hq_s = (int)I.hq_shard;
+    q.hkv_s = (int)I.hkv_shard;
+    q.head_dim = hd;
+    q.max_kv = (int)d.max_kv;
+    q.log2_theta = std::log2(d.rope_theta);
+    for (int r = 0; r < N; ++r) {
+        q.W[r] = w->wqkv[r];
+        q.gamma[r] = w->gamma_attn[r];
+        q.bias[r] = d.has_qkv_bias ? w->bqkv[r] : nullptr;
+        q.kcache[r] = kv->k[r];
+        q.vcache[r] = kv->v[r];
+    }
+    stage_mark(P, 0, s);
+    cudaError_t e = launch_gemv(q, EPI_QKV_ROPE, d.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: qkv launch");
+
+    AttnDecodeParams a{};
+    a.q = q.q_out;
+    for (int r = 0; r < N; ++r) {
+        a.kcache[r] = kv->k[r];
+        a.vcache[r] = kv->v[r];
+    }
+    a.pos = pos;
+    a.N = N;
+    a.B = B;
+    a.hq_s = (int)I.hq_shard;
+    a.hkv_s = (int)I.hkv_shard;
+    a.d = hd;
+    a.max_kv = (int)d.max_kv;
+    a.max_batch = (int)d.max_batch;
+    a.n_chunks = P->attn_chunks;
+    a.scale = (float)(1.0 / std::sqrt((double)hd));
+    a.part = reinterpret_cast<float*>(ws + P->off_attn_part);
+    a.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_attn);
+    a.out = ws + P->off_attn_out;
+    a.status = status;
+    stage_mark(P, 1, s);
+    e = launch_attn_decode(a, d.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: attention launch");
+
+    float* h = reinterpret_cast<float*>(ws + P->off_h);
+    GemvParams o{};
+    o.n_shards = N;
+    o.rows = (int)d.hidden;
+    o.K = (int)(I.hq_shard * hd);
+    o.T = T;
+    o.shape = P->g_o;
+    o.part = reinterpret_cast<float*>(ws + P->off_part_o);
+    o.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_o);
+    o.status = status;
+    o.resid = x;
+    o.y = h;
+    for (int r = 0; r < N; ++r) {
+        o.W[r] = w->wo[r];
+        o.act[r] = ws + P->off_attn_out + (size_t)r * T * o.K * es;
+    }
+    stage_mark(P, 2, s);
+    e = launch_gemv(o, EPI_ROWPAR, d.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: o_proj launch");
+
+    GemvParams g{};
+    g.n_shards = N;
+    g.rows = (int)(2 * I.ffn_shard);
+    g.K = (int)d.hidden;
+    g.T = T;
+    g.shape = P->g_gu;
+    g.x = h;
+    g.eps = (float)d.eps;
+    g.part = reinterpret_cast<float*>(ws + P->off_part_gu);
+    g.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_gu);
+    g.status = status;
+    g.act_out = ws + P->off_act;
+    g.ffn_s = (int)I.ffn_shard;
+    for (int r = 0; r < N; ++r) {
+        g.W[r] = w->wgu[r];
+        g.gamma[r] = w->gamma_ffn[r];
+    }
+    stage_mark(P, 3, s);
+    e = launch_gemv(g, EPI_SWIGLU, d.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: gate_up launch");
+
+    GemvParams dn{};
+    dn.n_shards = N;
+    dn.rows = (int)d.hidden;
+    dn.K = (int)I.ffn_shard;
+    dn.T = T;
+    dn.shape = P->g_down;
+    dn.part = reinterpret_cast<float*>(ws + P->off_part_down);
+    dn.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_down);
+    dn.status = status;
+    dn.resid = h;
+    dn.y = y;
+    for (int r = 0; r < N; ++r) {
+        dn.W[r] = w->wd[r];
+        dn.act[r] = ws + P->off_act + (size_t)r * T * dn.K * es;
+    }
+    stage_mark(P, 4, s);
+    e = launch_gemv(dn, EPI_ROWPAR, d.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: down launch");
+    stage_mark(P, 5, s);
+    return ok();
+}
+
+extern "C" tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
+                                      const float* x, float* y, const int32_t* pos, int32_t B,
+                                      int32_t T_per_seq, int32_t mode, const float* router_logits,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    if (!plan || !w || !x || !y || !workspace) return fail(TP_ERR_NULL, "tp_block_forward: NULL argument");
+    if (x == y) return fail(TP_ERR_INVALID_ARG, "tp_block_forward: y must not alias x");
+    if (B < 1 || T_per_seq < 1) return fail(TP_ERR_SHAPE, "tp_block_forward: B and T_per_seq must be >= 1");
+    if (B > plan->d.max_batch || (int64_t)B * T_per_seq > plan->d.max_tokens)
+        return fail(TP_ERR_SHAPE, "tp_block_forward: B=%d x T=%d exceeds the plan's max_batch/max_tokens", B, T_per_seq);
+    if (workspace_bytes < plan->ws_bytes)
+        return fail(TP_ERR_CAPACITY, "tp_block_forward: workspace %zu bytes < required %zu", workspace_bytes,
+                    plan->ws_bytes);
+    if (!aligned16(workspace) || !aligned16(x) || !aligned16(y))
+        return fail(TP_ERR_ALIGN, "tp_block_forward: x, y and workspace must be 16-byte aligned");
+    tp_status st = check_device();
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    (void)router_logits;
+    if (mode == TP_MODE_DECODE) {
+        if (!plan->dense) return fail(TP_ERR_INVALID_ARG, "tp_block_forward: DECODE needs an attention block");
+        if (!kv || !pos) return fail(TP_ERR_NULL, "tp_block_forward: DECODE needs kv and pos");
+        if (T_per_seq != 1) return fail(TP_ERR_SHAPE, "tp_block_forward: DECODE takes T_per_seq == 1");
+        if (B > kTMax) return fail(TP_ERR_SHAPE, "tp_block_forward: DECODE handles at most %d sequences", kTMax);
+        return forward_decode(plan, w, kv, x, y, pos, B, ws, s);
+    }
+    if (mode == TP_MODE_PREFILL || mode == TP_MODE_MOE_FFN)
+        return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: mode %d not available in this build", mode);
+    return fail(TP_ERR_INVALID_ARG, "tp_block_forward: unknown mode %d", mode);
+}
+
+extern "C" tp_status tp_reduce_partials(tp_plan_t plan, const float* partials, const float* residual,
+                                        const float* bias, float* out, int64_t M, void* stream) {
+    if (!plan || !partials || !out) return fail(TP_ERR_NULL, "tp_reduce_partials: NULL argument");
+    if (M < 0) return fail(TP_ERR_SHAPE, "tp_reduce_partials: M must be >= 0");
+    tp_status st = check_device();
+    if (st) return st;
+    cudaError_t e = launch_reduce_partials(partials, residual, bias, out, plan->N, M, plan->d.hidden,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tp_reduce_partials: launch");
+    return ok();
+}
+
+extern "C" tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream) {
+    if (!workspace || !out) return fail(TP_ERR_NULL, "tp_get_device_status: NULL argument");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TP_CUDA(cudaMemcpyAsync(out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s), "tp_get_device_status: copy");
+    TP_CUDA(cudaStreamSynchronize(s), "tp_get_device_status: sync");
+    return ok();
+}
+
+extern "C" tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int32_t n_events) {
+    if (!plan) return fail(TP_ERR_NULL, "tp_profile_stages: plan is NULL");
+    if (n_events < 0 || n_events > 16) return fail(TP_ERR_INVALID_ARG, "tp_profile_stages: 0..16 events");
+    plan->n_stage_ev = events ? n_events : 0;
+    for (int i = 0; i < plan->n_stage_ev; ++i) plan->stage_ev[i] = static_cast<cudaEvent_t>(events[i]);
+    return ok();
+}
+
+extern "C" const char* tp_last_error(void) { return g_err; }
+
+extern "C" int32_t tp_version(void) { return TP_ABI_VERSION; }

@@ -1,0 +1,108 @@
+// Internal declarations shared by the C-ABI layer (tp_api.cu) and the kernel
+// translation units. Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tp_block.h"
+
+namespace tpk {
+
+constexpr int kTileRows = 64;     // output rows per skinny-GEMM work unit
+constexpr int kTMax = 8;          // tokens per decode step handled in one pass
+constexpr int kKStep = 64;        // reduction elements per warp step
+constexpr int kSMs = 152;         // GB300 streaming multiprocessors
+constexpr int kAttnChunk = 256;   // keys per split-KV work unit (decode)
+constexpr int kPartStride = kTileRows * kTMax + kTMax;   // floats per unit partial
+
+// Shape of one skinny-GEMM launch: `groups` output tiles, each reduced from
+// `units_per_group` work units (`shards_per_group` shards x `chunks` chunks).
+struct GemvShape {
+    int groups = 0;
+    int shards_per_group = 1;
+    int chunks = 1;
+    int kc = 0;                 // reduction elements per unit
+#ifdef __CUDACC__
+    __host__ __device__
+#endif
+    int units() const { return groups * shards_per_group * chunks; }
+#ifdef __CUDACC__
+    __host__ __device__
+#endif
+    int units_per_group() const { return shards_per_group * chunks; }
+};
+
+enum Epi : int { EPI_QKV_ROPE = 0, EPI_SWIGLU = 1, EPI_ROWPAR = 2 };
+
+// Parameters of one skinny-GEMM launch (decode projections). One struct for
+// all epilogues; fields an epilogue does not use are ignored.
+struct GemvParams {
+    const void* W[TP_MAX_SHARDS];      // per-shard weight [rows, K]
+    int n_shards;
+    int rows;                          // rows per shard (column-par) or H (row-par)
+    int K;                             // reduction length per shard
+    int T;                             // tokens (<= kTMax)
+    GemvShape shape;
+    // activation: normalised input (column-parallel) ...
+    const float* x;                    // [T, K] float32 (residual stream)
+    const float* gamma[TP_MAX_SHARDS]; // per-shard replicated norm weight [K]
+    float eps;
+    // ... or per-shard activation (row-parallel), storage type of W
+    const void* act[TP_MAX_SHARDS];    // [T, K]
+    // workspace
+    float* part;                       // [units][kPartStride]
+    unsigned* cnt;                     // [groups]
+    int* status;
+    // EPI_QKV_ROPE
+    const float* bias[TP_MAX_SHARDS];  // [rows] or NULL
+    float* q_out;                      // [N][T][Hq' d]
+    void* kcache[TP_MAX_SHARDS];
+    void* vcache[TP_MAX_SHARDS];
+    const int* pos;                    // [B]
+    int hq_s, hkv_s, head_dim, max_kv;
+    double log2_theta;
+    // EPI_SWIGLU
+    void* act_out;                     // [N][T][F']
+    int ffn_s;
+    // EPI_ROWPAR
+    const float* resid;                // [T][rows]
+    float* y;                          // [T][rows]
+};
+
+struct AttnDecodeParams {
+    const float* q;                    // [N][T][Hq' d] rotated queries
+    const void* kcache[TP_MAX_SHARDS]; // [Bmax][Hkv'][max_kv][d]
+    const void* vcache[TP_MAX_SHARDS];
+    const int* pos;                    // [B]
+    int N, B, hq_s, hkv_s, d, max_kv, max_batch, n_chunks;
+    float scale;                       // 1/sqrt(d)
+    float* part;                       // [groups][n_chunks][G*(d+2)]
+    unsigned* cnt;                     // [groups]
+    void* out;                         // [N][T][Hq' d] storage type
+    int* status;
+};
+
+struct CopyDesc {
+    const void* src;    // NULL: fill zeros
+    void* dst;
+    int64_t rows;
+    int64_t row_bytes;
+    int64_t src_pitch;  // bytes
+    int64_t dst_pitch;  // bytes
+};
+constexpr int kMaxCopyDescs = 48;
+struct CopyBatch {
+    CopyDesc d[kMaxCopyDescs];
+    int n;
+};
+
+// launchers (return the launch's cudaError_t)
+cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_copy_batch(const CopyBatch& b, cudaStream_t s);
+cudaError_t launch_reduce_partials(const float* partials, const float* resid, const float* bias,
+                                   float* out, int N, int64_t M, int64_t H, cudaStream_t s);
+
+}  // namespace tpk
