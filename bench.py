@@ -288,6 +288,10 @@ def run_ours(args, world, rank, local):
     # ---- per-kernel durations: stage events around each launch over K' steps
     n_prof = min(args.steps, 2000)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n_prof)]
+    for row in evs:          # torch creates events lazily: record once so the raw handles exist
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
     with torch.cuda.stream(stream):
         for i in range(n_prof):
             tb.tp_profile_stages(model.plan, evs[i])
