@@ -269,6 +269,41 @@ tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_se
                            const float* router_logits,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the library-owned scratch array used by tp_block_forward_noalloc,
+ * per device: 16 MiB. */
+#define TP_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/* DECODE forward (same computation, kernels and results as tp_block_forward
+ * with TP_MODE_DECODE, T_per_seq = 1) for callers that must not allocate
+ * device memory: code that runs while a CUDA graph is being captured, where
+ * an allocation is not allowed; plug-ins inside a host program that owns all
+ * device memory through its own pool; and latency-bound loops that cannot
+ * afford the synchronisation an allocation may cause. Instead of a caller
+ * workspace it uses one static device array of TP_NOALLOC_SCRATCH_BYTES that
+ * each GPU loading this library holds until the process exits. The pages have
+ * no counterpart of this entry point; it is an interface convenience.
+ *  - The caller still passes every input and output (weights, caches, x, y,
+ *    pos, as for tp_block_forward). The call allocates nothing: no cudaMalloc,
+ *    no cudaFree, no allocating library routine.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture. Later calls only enqueue work.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents; each call clears the counters and status word it needs on
+ *    `stream` before its kernels run. Calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race on the array and give wrong
+ *    results: issue them on one stream, or serialise them.
+ *  - Plans whose decode scratch exceeds TP_NOALLOC_SCRATCH_BYTES are rejected
+ *    with TP_ERR_CAPACITY before any GPU work (the Llama-3-8B-shaped block at
+ *    tp 4, batch 8, KV 2049 needs about 10 MB). Positions past max_kv are
+ *    skipped as in tp_block_forward, but the status word is not readable here.
+ * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no attention block, y == x),
+ * TP_ERR_SHAPE (B outside 1..min(max_batch, 8)), TP_ERR_CAPACITY,
+ * TP_ERR_ALIGN, TP_ERR_UNSUPPORTED, TP_ERR_CUDA. */
+tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
+                                   const float* x, float* y, const int32_t* pos, int32_t B,
+                                   void* stream);
+
 /* Standalone rank-order reduction ([RT] Collective backend abstraction,
  * copy-and-reduce; [MG] Local TP: the add after the copies):
  *   out[m, :] = residual[m, :] + (((p_0 + p_1) + p_2) + ... + p_{tp-1})[m, :] + bias

@@ -100,6 +100,8 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_workspace_init": (I32, [P, VP, C.c_size_t, VP]),
         "tp_block_forward": (I32, [P, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), VP, VP, VP, I32, I32,
                                    I32, VP, VP, C.c_size_t, VP]),
+        "tp_block_forward_noalloc": (I32, [P, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), VP, VP, VP, I32,
+                                           VP]),
         "tp_reduce_partials": (I32, [P, VP, VP, VP, VP, I64, VP]),
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
         "tp_profile_stages": (I32, [P, C.POINTER(VP), I32]),
@@ -218,6 +220,14 @@ def tp_block_forward(plan: Plan, shards: dict, kv: tuple, x, y, pos, B: int, T_p
                                    C.byref(kvs) if kvs is not None else None, _ptr(x), _ptr(y), _ptr(pos),
                                    B, T_per_seq, mode, _ptr(router_logits), _ptr(workspace), nbytes,
                                    _stream(stream)))
+
+
+def tp_block_forward_noalloc(plan: Plan, shards: dict, kv: tuple, x, y, pos, B: int, stream=None) -> None:
+    """Decode forward using the library's static scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    kvs = _kv_set(*kv)
+    _check(load().tp_block_forward_noalloc(plan.handle, C.byref(_shard_set(shards)), C.byref(kvs), _ptr(x),
+                                           _ptr(y), _ptr(pos), B, _stream(stream)))
 
 
 def tp_reduce_partials(plan: Plan, partials, residual, bias, out, M: int, stream=None) -> None:

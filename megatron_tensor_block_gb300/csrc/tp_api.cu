@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "tp_internal.h"
@@ -56,6 +57,7 @@ struct tp_plan_s {
     size_t off_q = 0, off_attn_part = 0, off_attn_out = 0, off_h = 0, off_act = 0;
     size_t off_part_qkv = 0, off_part_o = 0, off_part_gu = 0, off_part_down = 0;
     size_t ws_bytes = 0;
+    size_t ws_decode_end = 0;           // end of the decode buffers (control words included)
     // measurement hook (tp_profile_stages)
     cudaEvent_t stage_ev[16] = {};
     int n_stage_ev = 0;
@@ -210,6 +212,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_part_o = take((size_t)P->g_o.units() * kPartStride * 4);
         P->off_part_gu = take((size_t)P->g_gu.units() * kPartStride * 4);
         P->off_part_down = take((size_t)P->g_down.units() * kPartStride * 4);
+        P->ws_decode_end = off;
     }
     P->ws_bytes = off;
     I.workspace_bytes = (int64_t)P->ws_bytes;
@@ -684,3 +687,61 @@ extern "C" tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int3
 extern "C" const char* tp_last_error(void) { return g_err; }
 
 extern "C" int32_t tp_version(void) { return TP_ABI_VERSION; }
+
+// ---------------------------------------------------------------- decode with library-owned scratch
+
+// Scratch of tp_block_forward_noalloc: one array in device global memory per
+// GPU that loads this library, held until the process exits. Host code must
+// not use the array's name as an address (on the host it only stands for the
+// symbol); its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current) and remembered.
+static tp_status noalloc_scratch(void** out) {
+    int dev = 0;
+    TP_CUDA(cudaGetDevice(&dev), "tp_block_forward_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(TP_ERR_UNSUPPORTED, "tp_block_forward_noalloc: device index %d above %d", dev, kMaxDevices - 1);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward_noalloc: cudaGetSymbolAddress");
+        if (!p) return fail(TP_ERR_CUDA, "tp_block_forward_noalloc: no device address for the scratch array");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return TP_OK;
+}
+
+extern "C" tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
+                                              const float* x, float* y, const int32_t* pos, int32_t B,
+                                              void* stream) {
+    if (!plan || !w || !kv || !x || !y || !pos) return fail(TP_ERR_NULL, "tp_block_forward_noalloc: NULL argument");
+    if (!plan->dense) return fail(TP_ERR_INVALID_ARG, "tp_block_forward_noalloc: the plan has no attention block");
+    if (x == y) return fail(TP_ERR_INVALID_ARG, "tp_block_forward_noalloc: y must not alias x");
+    if (B < 1 || B > plan->d.max_batch || B > kTMax)
+        return fail(TP_ERR_SHAPE, "tp_block_forward_noalloc: B=%d outside 1..min(max_batch, %d)", B, kTMax);
+    if (plan->ws_decode_end > (size_t)TP_NOALLOC_SCRATCH_BYTES)
+        return fail(TP_ERR_CAPACITY,
+                    "tp_block_forward_noalloc: this plan's decode needs %zu bytes of scratch; the static array "
+                    "holds %lld (use tp_block_forward with a caller workspace)",
+                    plan->ws_decode_end, (long long)TP_NOALLOC_SCRATCH_BYTES);
+    if (!aligned16(x) || !aligned16(y)) return fail(TP_ERR_ALIGN, "tp_block_forward_noalloc: x and y must be 16-byte aligned");
+    tp_status st = check_device();
+    if (st) return st;
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents: counters and status start at zero
+    TP_CUDA(cudaMemsetAsync(scratch, 0, plan->ctrl_bytes, s), "tp_block_forward_noalloc: clearing counters");
+    return forward_decode(plan, w, kv, x, y, pos, B, static_cast<char*>(scratch), s);
+}
