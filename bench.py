@@ -352,7 +352,7 @@ def run_ours(args, world, rank, local):
                      "traffic": kernel_traffic("gemv_swiglu")},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x_host.numel() * 4 + pos_host.numel() * 4,
                 "d2h_bytes_per_step": y_host.numel() * 4, "path": "tp_block_forward via the ctypes binding"},
-        "gpu_launches": len(STAGES) * args.steps,
+        "gpu_launches": (9 if w.dtype == "bf16" else 5) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -56,6 +56,7 @@ struct tp_plan_s {
            off_cnt_down = 0, ctrl_bytes = 0;
     size_t off_q = 0, off_attn_part = 0, off_attn_out = 0, off_h = 0, off_act = 0;
     size_t off_part_qkv = 0, off_part_o = 0, off_part_gu = 0, off_part_down = 0;
+    size_t off_xg = 0, off_ss = 0, off_hg = 0, off_ss_tiles = 0;   // bf16 normalised operands
     size_t ws_bytes = 0;
     size_t ws_decode_end = 0;           // end of the decode buffers (control words included)
     // measurement hook (tp_profile_stages)
@@ -73,9 +74,9 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // least `target` work units, with chunk lengths that are whole 64-element
 // steps, at least two steps (both k-halves of a CTA busy) and at most
 // `max_steps` steps (shared-memory bound).
-static int pick_chunks(int steps, long units_per_chunk, int max_steps, long target) {
+static int pick_chunks(int steps, long units_per_chunk, int max_steps, long target, int max_chunks) {
     int best = -1;
-    for (int C = 1; C <= steps; ++C) {
+    for (int C = 1; C <= steps && C <= max_chunks; ++C) {
         if (steps % C) continue;
         const int len = steps / C;
         if (len > max_steps) continue;
@@ -88,11 +89,35 @@ static int pick_chunks(int steps, long units_per_chunk, int max_steps, long targ
 
 static GemvShape make_shape(int groups, int shards_per_group, int K, size_t esz) {
     GemvShape s;
+    if (esz == 2) {
+        // bf16: persistent tensor-map kernel. Column-parallel tiles take the whole
+        // reduction (no cross-CTA partials); row-parallel tiles split each shard's
+        // reduction into whole 256-element stages until there are >= 3 units per SM.
+        s.groups = groups;
+        s.shards_per_group = shards_per_group;
+        s.chunks = 1;
+        const int stages = (K + 255) / 256;
+        if (shards_per_group > 1) {
+            for (int C = 1; C <= stages && shards_per_group * C <= kMaxGroupUnits; ++C) {
+                if (stages % C) continue;
+                s.chunks = C;
+                if ((long)groups * shards_per_group * C >= 3L * kSMs) break;
+            }
+            if (K % (s.chunks * 64) || (K / s.chunks) % 64) s.chunks = 1;
+        }
+        s.kc = K / s.chunks;
+        return s;
+    }
     s.groups = groups;
     s.shards_per_group = shards_per_group;
     const int steps = K / kKStep;
-    const int max_steps = (esz == 2 ? 2048 : 1024) / kKStep;
-    s.chunks = pick_chunks(steps, (long)groups * shards_per_group, max_steps, 4L * kSMs);
+    // bf16 runs on the persistent streaming kernel (one CTA per SM walking its
+    // units round-robin): ~6 units per CTA keeps the tail short. fp32 runs
+    // one CTA per unit.
+    const int max_steps = (esz == 2 ? kMaxKcTma : 1024) / kKStep;
+    const long target = esz == 2 ? 3L * kSMs : 4L * kSMs;
+    s.chunks = pick_chunks(steps, (long)groups * shards_per_group, max_steps, target,
+                           kMaxGroupUnits / shards_per_group);
     s.kc = K / s.chunks;
     return s;
 }
@@ -212,6 +237,10 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_part_o = take((size_t)P->g_o.units() * kPartStride * 4);
         P->off_part_gu = take((size_t)P->g_gu.units() * kPartStride * 4);
         P->off_part_down = take((size_t)P->g_down.units() * kPartStride * 4);
+        P->off_xg = take((size_t)N * kTMax * H * 2);
+        P->off_ss = take((size_t)kTMax * 4);
+        P->off_hg = take((size_t)N * kTMax * H * 2);
+        P->off_ss_tiles = take((size_t)(H / kTileRows) * kTMax * 4);
         P->ws_decode_end = off;
     }
     P->ws_bytes = off;
@@ -534,8 +563,26 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         q.kcache[r] = kv->k[r];
         q.vcache[r] = kv->v[r];
     }
+    const bool bf = d.dtype == TP_BF16;
+    cudaError_t e;
     stage_mark(P, 0, s);
-    cudaError_t e = launch_gemv(q, EPI_QKV_ROPE, d.dtype, s);
+    if (bf) {
+        // bf16 projections take their RMSNorm operands pre-scaled:
+        // x * gamma_r for every shard, and sum(x^2) per token
+        NormPrepParams np{};
+        np.x = x;
+        for (int r = 0; r < N; ++r) np.gamma[r] = w->gamma_attn[r];
+        np.N = N;
+        np.T = T;
+        np.H = (int)d.hidden;
+        np.xg = ws + P->off_xg;
+        np.ss = reinterpret_cast<float*>(ws + P->off_ss);
+        e = launch_norm_prep(np, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: norm prep launch");
+        q.xact = ws + P->off_xg;
+        q.ss_in = np.ss;
+    }
+    e = launch_gemv(q, EPI_QKV_ROPE, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: qkv launch");
 
     AttnDecodeParams a{};
@@ -561,6 +608,10 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     stage_mark(P, 1, s);
     e = launch_attn_decode(a, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: attention launch");
+    if (bf) {
+        e = launch_attn_combine(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: attention combine launch");
+    }
 
     float* h = reinterpret_cast<float*>(ws + P->off_h);
     GemvParams o{};
@@ -576,10 +627,17 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     o.y = h;
     for (int r = 0; r < N; ++r) {
         o.W[r] = w->wo[r];
-        o.act[r] = ws + P->off_attn_out + (size_t)r * T * o.K * es;
+        o.act[r] = ws + P->off_attn_out + (size_t)r * kTMax * o.K * es;
+        o.gamma2[r] = w->gamma_ffn[r];
+    }
+    if (bf) {
+        o.xact = ws + P->off_attn_out;
+        o.norm_out = ws + P->off_hg;
+        o.ss_tiles_out = reinterpret_cast<float*>(ws + P->off_ss_tiles);
     }
     stage_mark(P, 2, s);
     e = launch_gemv(o, EPI_ROWPAR, d.dtype, s);
+    if (e == cudaSuccess && bf) e = launch_rowpar_reduce(o, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: o_proj launch");
 
     GemvParams g{};
@@ -599,6 +657,11 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         g.W[r] = w->wgu[r];
         g.gamma[r] = w->gamma_ffn[r];
     }
+    if (bf) {
+        g.xact = ws + P->off_hg;
+        g.ss_tiles = reinterpret_cast<const float*>(ws + P->off_ss_tiles);
+        g.n_ss_tiles = (int)(d.hidden / kTileRows);
+    }
     stage_mark(P, 3, s);
     e = launch_gemv(g, EPI_SWIGLU, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: gate_up launch");
@@ -616,10 +679,12 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     dn.y = y;
     for (int r = 0; r < N; ++r) {
         dn.W[r] = w->wd[r];
-        dn.act[r] = ws + P->off_act + (size_t)r * T * dn.K * es;
+        dn.act[r] = ws + P->off_act + (size_t)r * kTMax * dn.K * es;
     }
+    if (bf) dn.xact = ws + P->off_act;
     stage_mark(P, 4, s);
     e = launch_gemv(dn, EPI_ROWPAR, d.dtype, s);
+    if (e == cudaSuccess && bf) e = launch_rowpar_reduce(dn, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: down launch");
     stage_mark(P, 5, s);
     return ok();

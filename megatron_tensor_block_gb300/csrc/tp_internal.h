@@ -16,6 +16,8 @@ constexpr int kKStep = 64;        // reduction elements per warp step
 constexpr int kSMs = 152;         // GB300 streaming multiprocessors
 constexpr int kAttnChunk = 256;   // keys per split-KV work unit (decode)
 constexpr int kPartStride = kTileRows * kTMax + kTMax;   // floats per unit partial
+constexpr int kMaxKcTma = 512;
+constexpr int kMaxGroupUnits = 16;  // partials reduced by one finisher (register-resident)    // reduction chunk bound of the tensor-map projection kernel
 
 // Shape of one skinny-GEMM launch: `groups` output tiles, each reduced from
 // `units_per_group` work units (`shards_per_group` shards x `chunks` chunks).
@@ -69,6 +71,24 @@ struct GemvParams {
     // EPI_ROWPAR
     const float* resid;                // [T][rows]
     float* y;                          // [T][rows]
+    // tensor-map (bf16) kernel: activations arrive through the copy pipeline
+    const void* xact;                  // [N * kTMax][K] bf16 operand rows (shard r at row r*kTMax)
+    const float* ss_in;                // QKV: [kTMax] sums of squares of x
+    const float* ss_tiles;             // gate/up: [rows of h / 64][kTMax] per-tile sums of squares
+    int n_ss_tiles;
+    void* norm_out;                    // o_proj: [N][kTMax][H] bf16(h * gamma_ffn_r), or NULL
+    float* ss_tiles_out;               // o_proj: [H / 64][kTMax]
+    const float* gamma2[TP_MAX_SHARDS];
+};
+
+// RMSNorm operand preparation: xg[r][t][k] = bf16(x[t][k] * gamma_r[k]),
+// ss[t] = sum_k x[t][k]^2 (rows t >= T are zero).
+struct NormPrepParams {
+    const float* x;
+    const float* gamma[TP_MAX_SHARDS];
+    int N, T, H;
+    void* xg;
+    float* ss;
 };
 
 struct AttnDecodeParams {
@@ -102,6 +122,9 @@ struct CopyBatch {
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_copy_batch(const CopyBatch& b, cudaStream_t s);
+cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s);
+cudaError_t launch_rowpar_reduce(const GemvParams& p, cudaStream_t s);
+cudaError_t launch_attn_combine(const AttnDecodeParams& p, cudaStream_t s);
 cudaError_t launch_reduce_partials(const float* partials, const float* resid, const float* bias,
                                    float* out, int N, int64_t M, int64_t H, cudaStream_t s);
 
