@@ -750,6 +750,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const __
         for (int st = 0; st < spu; ++st, ++it) {
             const int sl = it % kGemvStages;
             mbar_wait(&R.full[sl], (it / kGemvStages) & 1, R.abort, p.status);
+            __syncwarp();   // lanes leave the wait loop independently
             const int steps_here = min(kBoxK / kKStep, (kc - st * kBoxK) / kKStep);
             const unsigned char* stage = ring + sl * kGemvStageBytes;
             const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
@@ -1025,6 +1026,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
             const int keys = min(SK, n - k0);
             const int sl = it % kStages;
             mbar_wait(&R.full[sl], (it / kStages) & 1, R.abort, p.status);
+            __syncwarp();
             const bf16* Kt = reinterpret_cast<const bf16*>(ring + sl * kAttnStageBytes);
             for (int kk = 0; kk < SK; kk += KPP) {       // uniform trip count (shuffles below)
                 const int key = kk + ks;
@@ -1089,6 +1091,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
             const int keys = min(SK, n - k0);
             const int sl = it % kStages;
             mbar_wait(&R.full[sl], (it / kStages) & 1, R.abort, p.status);
+            __syncwarp();
             const bf16* Vt = reinterpret_cast<const bf16*>(ring + sl * kAttnStageBytes);
             for (int key = ks; key < keys; key += KPP) {
                 const uint4 w = *reinterpret_cast<const uint4*>(Vt + key * D + li * 8);
@@ -1214,6 +1217,9 @@ static cudaError_t launch_gemv_t(const GemvParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+static bool g_pdl = true;
+void set_pdl(bool on) { g_pdl = on; }
+
 static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -1224,7 +1230,7 @@ static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 1 : 0;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -1305,7 +1311,7 @@ cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 1 : 0;
     void* args[] = {const_cast<NormPrepParams*>(&p)};
     cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(norm_prep_kernel), args);
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -1371,7 +1377,7 @@ static cudaError_t launch_small_pdl(const void* fn, void** args, int grid, int t
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 1 : 0;
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

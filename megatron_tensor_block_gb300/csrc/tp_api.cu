@@ -536,6 +536,9 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     }
     int* status = reinterpret_cast<int*>(ws + P->off_status);
     const size_t es = P->esz;
+    // with per-stage events recorded between the launches, launch without
+    // programmatic overlap so each event brackets exactly one stage
+    set_pdl(P->n_stage_ev == 0);
     const int hd = (int)d.head_dim;
 
     GemvParams q{};
@@ -605,6 +608,7 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     a.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_attn);
     a.out = ws + P->off_attn_out;
     a.status = status;
+    a.part_units = (unsigned)(P->attn_groups * P->attn_chunks);
     stage_mark(P, 1, s);
     e = launch_attn_decode(a, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: attention launch");

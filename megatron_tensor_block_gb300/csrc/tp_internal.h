@@ -100,8 +100,9 @@ struct AttnDecodeParams {
     float scale;                       // 1/sqrt(d)
     float* part;                       // [groups][n_chunks][G*(d+2)]
     unsigned* cnt;                     // [groups]
-    void* out;                         // [N][T][Hq' d] storage type
+    void* out;                         // [N][kTMax][Hq' d] storage type
     int* status;
+    unsigned part_units;               // capacity of `part` in chunk partials
 };
 
 struct CopyDesc {
@@ -120,6 +121,7 @@ struct CopyBatch {
 
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
+void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_copy_batch(const CopyBatch& b, cudaStream_t s);
 cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s);
