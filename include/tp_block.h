@@ -121,6 +121,10 @@ typedef struct tp_plan_info {
     int64_t workspace_bytes;     /* scratch for tp_block_forward, any mode */
     int64_t weight_bytes_shard;  /* all matrices of one shard */
     int64_t weight_bytes_total;  /* all shards */
+    /* MoE routing tables inside the workspace (byte offsets, for inspection
+     * after a MOE_FFN call): chosen expert ids int32 [T*top_k], bucket starts
+     * int32 [E+1], slot -> choice index int32 [T*top_k]. -1 without experts. */
+    int64_t moe_ids_offset, moe_bucket_offset, moe_perm_offset;
 } tp_plan_info;
 
 /* Full (unsharded) block weights, caller-owned device memory. */

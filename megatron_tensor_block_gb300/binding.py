@@ -52,7 +52,8 @@ class tp_plan_info(C.Structure):
             "hq_shard", "hkv_shard", "ffn_shard", "expert_ffn_shard", "qkv_rows", "vocab_padded",
             "vocab_rows_shard", "wqkv_bytes", "bqkv_bytes", "wo_bytes", "wgu_bytes", "wd_bytes",
             "gamma_bytes", "egu_bytes", "ed_bytes", "kv_cache_bytes", "lm_head_bytes", "workspace_bytes",
-            "weight_bytes_shard", "weight_bytes_total")]
+            "weight_bytes_shard", "weight_bytes_total", "moe_ids_offset", "moe_bucket_offset",
+            "moe_perm_offset")]
 
 
 class tp_block_weights(C.Structure):

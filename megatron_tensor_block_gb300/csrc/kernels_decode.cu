@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "stream.cuh"
 #include "tp_internal.h"
 
 namespace tpk {
@@ -546,50 +547,6 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnDecodeParams
 // the preceding kernel does not write while that kernel is still running.
 // ---------------------------------------------------------------------------
 
-constexpr int kStages = 4;                 // ring depth
-constexpr int kConsumers = 256;            // eight consumer warps
-constexpr int kStreamThreads = kConsumers + 32;
-constexpr int kBoxK = 256;                 // reduction elements per tensor-map box
-constexpr int kBoxBytes = kBoxK * 32 * 2;  // one box: 32 rows x 256 bf16 = 16 KB
-constexpr int kXBoxBytes = kBoxK * kTMax * 2;   // activation box: 8 token rows x 256 bf16 = 4 KB
-constexpr int kGemvStageBytes = 2 * kBoxBytes + kXBoxBytes;
-constexpr int kGemvStages = 3;             // projection ring depth (96 KB)
-constexpr int kAttnStageBytes = 16384;     // one contiguous run of K or V rows
-constexpr int kCtrlBytes = 128;            // barriers and flags at the start of shared memory
-
-struct Ring {
-    uint64_t* full;
-    uint64_t* empty;
-    volatile int* abort;
-    unsigned* s_flag;
-};
-
-__device__ __forceinline__ Ring ring_setup(unsigned char* smem, int stages = kStages) {
-    Ring R;
-    R.full = reinterpret_cast<uint64_t*>(smem);
-    R.empty = R.full + kStages;
-    R.abort = reinterpret_cast<volatile int*>(smem + 16 * kStages);
-    R.s_flag = reinterpret_cast<unsigned*>(smem + 16 * kStages + 4);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < stages; ++i) {
-            mbar_init(&R.full[i], 1);
-            mbar_init(&R.empty[i], kConsumers / 32);
-        }
-        *R.abort = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-    return R;
-}
-
-// After an aborted wait the producer must not leave copies writing into
-// shared memory of an exited CTA: wait (bounded) for every stage issued.
-__device__ __forceinline__ void producer_drain(const Ring& R, uint32_t issued, int stages = kStages) {
-    volatile int no_abort = 0;
-    const uint32_t first = issued > (uint32_t)stages ? issued - stages : 0u;
-    for (uint32_t k = first; k < issued; ++k) mbar_wait(&R.full[k % stages], (k / stages) & 1, &no_abort, nullptr);
-}
-
 __device__ __forceinline__ void decode_unit(const GemvParams& p, int epi, int u, int& gi, int& r, int& tb,
                                             int& chunk) {
     const int upg = p.shape.units_per_group();
@@ -614,23 +571,6 @@ struct TmaGemvArgs {
     CUtensorMap tmx;                 // activation operand rows, boxes of kBoxK x 8 rows
     GemvParams p;
 };
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_keep(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
 
 // Each stage carries, for 64 rows x 256 reduction elements: the two weight
 // boxes (rows 0-31 and 32-63 of the tile) and the matching activation box
@@ -1220,10 +1160,10 @@ static cudaError_t launch_gemv_t(const GemvParams& p, cudaStream_t s) {
 static bool g_pdl = true;
 void set_pdl(bool on) { g_pdl = on; }
 
-static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s, int threads) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kStreamThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1241,15 +1181,17 @@ size_t gemv_stream_smem(int kc) {
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library), encoded once per (weight, shape) and cached.
-static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap* out, int box_rows = 32) {
+// against the driver library); each distinct map is encoded once and cached.
+cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner, int box_rows, int swizzle128,
+                          CUtensorMap* out) {
     static std::mutex mu;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    struct Entry { const void* w; int K, rows, box_rows; CUtensorMap tm; };
+    struct Entry { const void* w; long inner, rows; int bi, br, sw; CUtensorMap tm; };
     static std::vector<Entry> cache;
     std::lock_guard<std::mutex> lock(mu);
     for (const Entry& e : cache)
-        if (e.w == W && e.K == K && e.rows == rows && e.box_rows == box_rows) {
+        if (e.w == base && e.inner == inner && e.rows == rows && e.bi == box_inner && e.br == box_rows &&
+            e.sw == swizzle128) {
             *out = e.tm;
             return cudaSuccess;
         }
@@ -1259,19 +1201,24 @@ static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap
                                                          12000, cudaEnableDefault, &q);
         if (e != cudaSuccess || !encode) return e != cudaSuccess ? e : cudaErrorNotSupported;
     }
-    cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBoxK, (cuuint32_t)box_rows};
+    cuuint64_t gdim[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
     cuuint32_t estride[2] = {1u, 1u};
-    Entry ent{W, K, rows, box_rows, {}};
-    CUresult r = encode(&ent.tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride, box, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    Entry ent{base, inner, rows, box_inner, box_rows, swizzle128, {}};
+    CUresult r = encode(&ent.tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (cache.size() > 4096) cache.clear();
     cache.push_back(ent);
     *out = ent.tm;
     return cudaSuccess;
+}
+
+static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap* out, int box_rows = 32) {
+    return tensor_map_2d(W, K, rows, kBoxK, box_rows, 0, out);
 }
 
 template <int EPI>
@@ -1298,7 +1245,7 @@ static cudaError_t launch_gemv_stream(const GemvParams& p, cudaStream_t s) {
     if (ex != cudaSuccess) return ex;
     const int grid = p.shape.units() < kSMs ? p.shape.units() : kSMs;
     void* args[] = {&A};
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(gemv_stream_kernel<EPI>), args, grid, smem, s);
+    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(gemv_stream_kernel<EPI>), args, grid, smem, s, kStreamThreads);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1364,7 +1311,7 @@ static cudaError_t launch_attn_stream(const AttnDecodeParams& p, cudaStream_t s)
     const int U = p.N * p.B * p.hkv_s * p.n_chunks;
     const int grid = U < kSMs ? U : kSMs;
     void* args[] = {const_cast<AttnDecodeParams*>(&p)};
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_stream_kernel<D>), args, grid, smem, s);
+    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_stream_kernel<D>), args, grid, smem, s, kStreamThreads);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

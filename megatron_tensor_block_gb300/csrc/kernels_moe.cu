@@ -1,0 +1,436 @@
+// Expert-sliced MoE feed-forward block ("Multi-GPU & Multi-Node", Supported
+// architectures: each shard holds 1/tp of every expert's weights and the
+// router is replicated, so the load stays balanced whichever experts a token
+// picks). Decode-sized token counts, bf16 weights, fp32 accumulation.
+//
+//   route   : softmax top-k per token (chosen by logit, ties to the lower id),
+//             weights renormalised over the chosen experts
+//   bucket  : stable counting sort of the (token, choice) slots by expert
+//   prep    : x_t * gamma_r (bf16) for every slot and shard, 1/rms per slot
+//   gate/up : per shard and expert, streaming grouped GEMM over the expert's
+//             slots, SwiGLU epilogue
+//   down    : per shard and expert, streaming grouped GEMM -> slot outputs
+//   combine : y_t = x_t + sum_r ( sum_j w_tj * o[r][slot(t, j)] ), j then r
+#include <cuda.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "stream.cuh"
+#include "tp_internal.h"
+
+namespace tpk {
+
+constexpr int kMoeTokPass = 32;                        // slots per pass of a unit (4 MMA column groups)
+constexpr int kMoeGroups = kMoeTokPass / 8;
+constexpr int kMoeXBytes = kMoeGroups * kBoxK * 8 * 2; // 4 activation boxes of 8 rows x 256
+constexpr int kMoeStageBytes = 2 * kBoxBytes + kMoeXBytes;
+constexpr int kMoeStages = 3;
+constexpr int kMaxExperts = 256;         // router
+constexpr int kMaxBucketExperts = 64;    // bucketing (per-warp count table)
+
+struct MoeArgs {
+    CUtensorMap tw[TP_MAX_SHARDS];   // weights of the launch (egu or ed), boxes 256 x 32
+    CUtensorMap tx[TP_MAX_SHARDS];   // activations in slot order (xs or act), boxes 256 x 8
+    MoeParams p;
+    int down;                        // 0: gate/up, 1: down
+};
+
+// ---------------------------------------------------------------- route
+
+__global__ void __launch_bounds__(256) moe_route_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= p.T) return;
+    const float* lg = p.logits + (size_t)t * p.E;
+    constexpr int kPer = kMaxExperts / 32;
+    float v[kPer];
+    bool taken[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int e = lane + 32 * q;
+        v[q] = e < p.E ? lg[e] : -INFINITY;
+        taken[q] = e >= p.E;
+    }
+    int sel[8];
+    float sl[8];
+    for (int j = 0; j < p.top_k; ++j) {
+        float best = -INFINITY;
+        int bi = 0x7fffffff;
+        #pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = lane + 32 * q;
+            if (!taken[q] && (v[q] > best || (v[q] == best && e < bi))) {
+                best = v[q];
+                bi = e;
+            }
+        }
+        // warp arg-max, ties to the lower expert id
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ob > best || (ob == best && oi < bi)) {
+                best = ob;
+                bi = oi;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+            if (lane + 32 * q == bi) taken[q] = true;
+        sel[j] = bi;
+        sl[j] = best;
+    }
+    if (lane == 0) {
+        // softmax restricted to the chosen experts == renormalised top-k softmax
+        float den = 0.f;
+        for (int j = 0; j < p.top_k; ++j) den += expf(sl[j] - sl[0]);
+        for (int j = 0; j < p.top_k; ++j) {
+            p.ids[t * p.top_k + j] = sel[j];
+            p.wts[t * p.top_k + j] = expf(sl[j] - sl[0]) / den;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- bucket (one CTA, 1024 threads)
+
+__global__ void __launch_bounds__(1024) moe_bucket_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int cnt[kMaxExperts];
+    __shared__ int base[kMaxExperts];
+    __shared__ int wcnt[32][kMaxBucketExperts];    // per-warp counts of a 1024-slot chunk
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = p.T * p.top_k, E = p.E;
+    for (int e = tid; e < E; e += 1024) cnt[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += 1024) atomicAdd(&cnt[p.ids[i]], 1);
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            base[e] = run;
+            p.offsets[e] = run;
+            run += cnt[e];
+        }
+        p.offsets[E] = run;
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < n; c0 += 1024) {
+        for (int q = tid; q < 32 * E; q += 1024) wcnt[q / E][q % E] = 0;
+        __syncthreads();
+        const int i = c0 + tid;
+        const int e = i < n ? p.ids[i] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & lt);
+        if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(same);
+        __syncthreads();
+        if (tid < E) {                       // exclusive prefix over warps, in warp order
+            int run = 0;
+            for (int w = 0; w < 32; ++w) {
+                const int c = wcnt[w][tid];
+                wcnt[w][tid] = run;
+                run += c;
+            }
+            cnt[tid] = run;                  // this chunk's count of expert tid
+        }
+        __syncthreads();
+        if (e >= 0) {
+            const int pos = base[e] + wcnt[warp][e] + rank;
+            p.perm[pos] = i;
+            p.slot_of[i] = pos;
+        }
+        __syncthreads();
+        if (tid < E) base[tid] += cnt[tid];
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- prep (one CTA per slot)
+
+__global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float wsum[8];
+    const int s = blockIdx.x, tid = threadIdx.x;
+    const int t = p.perm[s] / p.top_k;
+    const float* x = p.x + (size_t)t * p.H;
+    float a = 0.f;
+    for (int k = tid * 4; k < p.H; k += 1024) {
+        const float4 v = *reinterpret_cast<const float4*>(x + k);
+        a = fmaf(v.x, v.x, a);
+        a = fmaf(v.y, v.y, a);
+        a = fmaf(v.z, v.z, a);
+        a = fmaf(v.w, v.w, a);
+        for (int r = 0; r < p.N; ++r) {
+            const float4 g = *reinterpret_cast<const float4*>(p.gamma[r] + k);
+            uint2 pk;
+            pk.x = pack_bf16x2(v.x * g.x, v.y * g.y);
+            pk.y = pack_bf16x2(v.z * g.z, v.w * g.w);
+            const size_t row = (size_t)r * p.T * p.top_k + s;
+            *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xs) + row * p.H + k) = pk;
+        }
+    }
+    a = warp_sum(a);
+    if ((tid & 31) == 0) wsum[tid >> 5] = a;
+    __syncthreads();
+    if (tid == 0) {
+        float ss = 0.f;
+        for (int w = 0; w < 8; ++w) ss += wsum[w];
+        p.rinv[s] = 1.0f / sqrtf(ss / (float)p.H + p.eps);
+    }
+}
+
+// ---------------------------------------------------------------- grouped streaming GEMM
+//
+// Unit = (shard r, expert e, 64-row tile). Gate/up: rows are 32 gate + the
+// matching 32 up rows of the expert's shard slice, K = H. Down: 64 rows of H,
+// K = Fs. The expert's slots are processed in passes of 32 (four 8-column MMA
+// groups); each stage carries the weight boxes and up to four activation boxes.
+
+__global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeArgs A) {
+    const MoeParams& p = A.p;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const Ring R = ring_setup(smem, kMoeStages);
+    unsigned char* ring = smem + kCtrlBytes;
+    float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [64][32]
+    int* s_off = reinterpret_cast<int*>(tile + kTileRows * kMoeTokPass);          // [E+1]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool down = A.down != 0;
+    const int nslot = p.T * p.top_k;
+    const int tiles = down ? p.H / kTileRows : (2 * p.Fs) / kTileRows;
+    const int K = down ? p.Fs : p.H;
+    const int spu = (K + kBoxK - 1) / kBoxK;
+    const int U = p.N * p.E * tiles;
+
+    if (warp == kConsumers / 32) {                     // ---- producer
+        if (lane == 0) {
+            pdl_wait();                                // routing and activations come from earlier kernels
+            const uint64_t pol = l2_evict_first_policy();
+            uint32_t it = 0;
+            bool ok = (smem_u32(ring) & 127u) == 0;
+            if (!ok) {
+                *R.abort = 1;
+                set_status(p.status, TP_ERR_ALIGN);
+            }
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const int tb = u % tiles, e = (u / tiles) % p.E, r = u / (tiles * p.E);
+                const int off = p.offsets[e], cnt = p.offsets[e + 1] - off;
+                int rowa, rowb;
+                if (down) {
+                    rowa = e * p.H + tb * kTileRows;
+                    rowb = rowa + 32;
+                } else {
+                    rowa = e * 2 * p.Fs + tb * 32;
+                    rowb = rowa + p.Fs;
+                }
+                for (int ps = 0; ps < cnt && ok; ps += kMoeTokPass) {
+                    const int ng = min(kMoeGroups, (cnt - ps + 7) / 8);
+                    for (int st = 0; st < spu; ++st, ++it) {
+                        const int sl = it % kMoeStages;
+                        if (!mbar_wait(&R.empty[sl], ((it / kMoeStages) & 1) ^ 1, R.abort, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&R.full[sl], 2u * kBoxBytes + (uint32_t)ng * kBoxK * 8 * 2);
+                        unsigned char* dst = ring + sl * kMoeStageBytes;
+                        tma_load_2d(dst, &A.tw[r], st * kBoxK, rowa, &R.full[sl], pol);
+                        tma_load_2d(dst + kBoxBytes, &A.tw[r], st * kBoxK, rowb, &R.full[sl], pol);
+                        for (int g = 0; g < ng; ++g)
+                            tma_load_2d_keep(dst + 2 * kBoxBytes + g * kBoxK * 8 * 2, &A.tx[r], st * kBoxK,
+                                             off + ps + 8 * g, &R.full[sl]);
+                    }
+                }
+            }
+            pdl_trigger();
+            if (!ok || *R.abort) producer_drain(R, it, kMoeStages);
+        }
+        return;
+    }
+
+    // ---- consumers
+    pdl_wait();
+    for (int i = tid; i <= p.E; i += kConsumers) s_off[i] = p.offsets[i];
+    consumer_sync(kConsumers);
+    const int wm = warp & 3, wk = warp >> 2;
+    const int g = lane >> 2, tq = lane & 3;
+    const int box = wm >> 1, brow = 16 * (wm & 1) + g;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        const int tb = u % tiles, e = (u / tiles) % p.E, r = u / (tiles * p.E);
+        const int off = s_off[e], cnt = s_off[e + 1] - off;
+        for (int ps = 0; ps < cnt; ps += kMoeTokPass) {
+            const int ng = min(kMoeGroups, (cnt - ps + 7) / 8);
+            float c[kMoeGroups][4];
+#pragma unroll
+            for (int q = 0; q < kMoeGroups; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
+            for (int st = 0; st < spu; ++st, ++it) {
+                const int sl = it % kMoeStages;
+                mbar_wait(&R.full[sl], (it / kMoeStages) & 1, R.abort, p.status);
+                __syncwarp();
+                const int steps_here = min(kBoxK / kKStep, (K - st * kBoxK) / kKStep);
+                const unsigned char* stage = ring + sl * kMoeStageBytes;
+                const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
+                const unsigned char* wB = wA + 8 * (kBoxK * 2);
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    const int step = wk + 2 * s2;
+                    if (step < steps_here) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
+                            const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
+#pragma unroll
+                            for (int q = 0; q < kMoeGroups; ++q) {
+                                if (q < ng) {
+                                    const uint4 xv = *reinterpret_cast<const uint4*>(
+                                        stage + 2 * kBoxBytes + q * kBoxK * 16 + g * (kBoxK * 2) + tq * 16 +
+                                        step * 128 + h * 64);
+                                    mma_bf16_16816(c[q], a.x, b.x, a.y, b.y, xv.x, xv.y);
+                                    mma_bf16_16816(c[q], a.z, b.z, a.w, b.w, xv.z, xv.w);
+                                }
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&R.empty[sl]);
+            }
+            // tile[row][slot] = half 0 + half 1
+#pragma unroll
+            for (int q = 0; q < kMoeGroups; ++q) {
+                const int c0 = 8 * q + 2 * tq;
+                const int i0 = (16 * wm + g) * kMoeTokPass + c0, i1 = (16 * wm + g + 8) * kMoeTokPass + c0;
+                if (wk == 0) {
+                    tile[i0] = c[q][0];
+                    tile[i0 + 1] = c[q][1];
+                    tile[i1] = c[q][2];
+                    tile[i1 + 1] = c[q][3];
+                }
+            }
+            consumer_sync(kConsumers);
+#pragma unroll
+            for (int q = 0; q < kMoeGroups; ++q) {
+                const int c0 = 8 * q + 2 * tq;
+                const int i0 = (16 * wm + g) * kMoeTokPass + c0, i1 = (16 * wm + g + 8) * kMoeTokPass + c0;
+                if (wk == 1) {
+                    tile[i0] += c[q][0];
+                    tile[i0 + 1] += c[q][1];
+                    tile[i1] += c[q][2];
+                    tile[i1 + 1] += c[q][3];
+                }
+            }
+            consumer_sync(kConsumers);
+            const int nt = min(kMoeTokPass, cnt - ps);
+            if (down) {
+                // expert output rows for this pass's slots
+                for (int i = tid; i < kTileRows * nt; i += kConsumers) {
+                    const int j = i / nt, q = i - j * nt;
+                    const int slot = off + ps + q;
+                    p.o[((size_t)r * nslot + slot) * p.H + tb * kTileRows + j] = tile[j * kMoeTokPass + q];
+                }
+            } else {
+                bf16* act = reinterpret_cast<bf16*>(p.act);
+                for (int i = tid; i < 32 * nt; i += kConsumers) {
+                    const int j = i / nt, q = i - j * nt;
+                    const int slot = off + ps + q;
+                    const float rv = p.rinv[slot];
+                    const float gt = tile[j * kMoeTokPass + q] * rv;
+                    const float up = tile[(j + 32) * kMoeTokPass + q] * rv;
+                    act[((size_t)r * nslot + slot) * p.Fs + tb * 32 + j] =
+                        __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                }
+            }
+            consumer_sync(kConsumers);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- combine (one CTA per token)
+
+__global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
+    const int t = blockIdx.x, nslot = p.T * p.top_k;
+    for (int h = threadIdx.x * 4; h < p.H; h += 1024) {
+        float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < p.N; ++r) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < p.top_k; ++j) {
+                const int f = t * p.top_k + j;
+                const float w = p.wts[f];
+                const float4 v = *reinterpret_cast<const float4*>(p.o + ((size_t)r * nslot + p.slot_of[f]) * p.H + h);
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+            if (r == 0) total = acc;
+            else { total.x += acc.x; total.y += acc.y; total.z += acc.z; total.w += acc.w; }
+        }
+        const float4 xv = *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + h);
+        *reinterpret_cast<float4*>(p.y + (size_t)t * p.H + h) =
+            make_float4(xv.x + total.x, xv.y + total.y, xv.z + total.z, xv.w + total.w);
+    }
+}
+
+// ---------------------------------------------------------------- launch sequence
+
+static size_t moe_gemm_smem(int E) {
+    return kCtrlBytes + (size_t)kMoeStages * kMoeStageBytes + (size_t)kTileRows * kMoeTokPass * 4 +
+           (size_t)(E + 1) * 4 + 16;
+}
+
+static cudaError_t launch_small(const void* fn, void* arg, int grid, int threads, cudaStream_t s) {
+    void* args[] = {arg};
+    return launch_pdl(fn, args, grid, 0, s, threads);
+}
+
+cudaError_t launch_moe(const MoeParams& p, cudaStream_t s) {
+    MoeParams q = p;
+    cudaError_t e = launch_small(reinterpret_cast<const void*>(moe_route_kernel), &q, (p.T + 7) / 8, 256, s);
+    if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_bucket_kernel), &q, 1, 1024, s);
+    if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_prep_kernel), &q, p.T * p.top_k, 256, s);
+    if (e != cudaSuccess) return e;
+    const size_t smem = moe_gemm_smem(p.E);
+    static int set_bytes = -1;
+    if ((int)smem > set_bytes) {
+        e = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        set_bytes = (int)smem;
+    }
+    const long nslot = (long)p.T * p.top_k;
+    for (int down = 0; down < 2; ++down) {
+        MoeArgs A;
+        memset(&A, 0, sizeof A);
+        A.p = p;
+        A.down = down;
+        for (int r = 0; r < p.N; ++r) {
+            if (down) {
+                e = tensor_map_2d(p.ed[r], p.Fs, (long)p.E * p.H, kBoxK, 32, 0, &A.tw[r]);
+                if (e == cudaSuccess)
+                    e = tensor_map_2d(static_cast<const bf16*>(p.act) + (size_t)r * nslot * p.Fs, p.Fs, nslot, kBoxK, 8,
+                                      0, &A.tx[r]);
+            } else {
+                e = tensor_map_2d(p.egu[r], p.H, (long)p.E * 2 * p.Fs, kBoxK, 32, 0, &A.tw[r]);
+                if (e == cudaSuccess)
+                    e = tensor_map_2d(static_cast<const bf16*>(p.xs) + (size_t)r * nslot * p.H, p.H, nslot, kBoxK, 8, 0,
+                                      &A.tx[r]);
+            }
+            if (e != cudaSuccess) return e;
+        }
+        const int tiles = down ? p.H / kTileRows : 2 * p.Fs / kTileRows;
+        const int U = p.N * p.E * tiles;
+        void* args[] = {&A};
+        e = launch_pdl(reinterpret_cast<const void*>(moe_gemm_kernel), args, U < kSMs ? U : kSMs, smem, s,
+                       kStreamThreads);
+        if (e != cudaSuccess) return e;
+    }
+    e = launch_small(reinterpret_cast<const void*>(moe_combine_kernel), &q, p.T, 256, s);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace tpk

@@ -57,6 +57,9 @@ struct tp_plan_s {
     size_t off_q = 0, off_attn_part = 0, off_attn_out = 0, off_h = 0, off_act = 0;
     size_t off_part_qkv = 0, off_part_o = 0, off_part_gu = 0, off_part_down = 0;
     size_t off_xg = 0, off_ss = 0, off_hg = 0, off_ss_tiles = 0;   // bf16 normalised operands
+    // MoE buffers (share the data region with the decode buffers)
+    size_t off_m_ids = 0, off_m_wts = 0, off_m_off = 0, off_m_perm = 0, off_m_slot = 0, off_m_rinv = 0,
+           off_m_xs = 0, off_m_act = 0, off_m_o = 0, ws_moe_end = 0;
     size_t ws_bytes = 0;
     size_t ws_decode_end = 0;           // end of the decode buffers (control words included)
     // measurement hook (tp_profile_stages)
@@ -168,6 +171,8 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
     }
     if (moe && (d->expert_ffn / tp) % 64)
         return fail(TP_ERR_UNSUPPORTED, "tp_plan: expert_ffn/tp must be a multiple of 64");
+    if (moe && (d->n_experts > 64 || d->top_k > 8))
+        return fail(TP_ERR_UNSUPPORTED, "tp_plan: MoE supports up to 64 experts and top_k <= 8");
 
     tp_plan_s* P = new (std::nothrow) tp_plan_s();
     if (!P) return fail(TP_ERR_INVALID_ARG, "tp_plan: out of host memory");
@@ -243,7 +248,27 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_ss_tiles = take((size_t)(H / kTileRows) * kTMax * 4);
         P->ws_decode_end = off;
     }
-    P->ws_bytes = off;
+    if (moe) {
+        off = P->ctrl_bytes;
+        const int64_t ns = d->max_tokens * d->top_k, Fs = I.expert_ffn_shard;
+        P->off_m_ids = take((size_t)ns * 4);
+        P->off_m_wts = take((size_t)ns * 4);
+        P->off_m_off = take((size_t)(d->n_experts + 1) * 4);
+        P->off_m_perm = take((size_t)ns * 4);
+        P->off_m_slot = take((size_t)ns * 4);
+        P->off_m_rinv = take((size_t)ns * 4);
+        P->off_m_xs = take((size_t)N * ns * H * 2);
+        P->off_m_act = take((size_t)N * ns * Fs * 2);
+        P->off_m_o = take((size_t)N * ns * H * 4);
+        P->ws_moe_end = off;
+        I.moe_ids_offset = (int64_t)P->off_m_ids;
+        I.moe_bucket_offset = (int64_t)P->off_m_off;
+        I.moe_perm_offset = (int64_t)P->off_m_perm;
+    } else {
+        I.moe_ids_offset = I.moe_bucket_offset = I.moe_perm_offset = -1;
+    }
+    P->ws_bytes = P->ws_decode_end > P->ws_moe_end ? P->ws_decode_end : P->ws_moe_end;
+    if (P->ws_bytes < P->ctrl_bytes) P->ws_bytes = P->ctrl_bytes;
     I.workspace_bytes = (int64_t)P->ws_bytes;
     *out = P;
     return ok();
@@ -694,6 +719,51 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     return ok();
 }
 
+static tp_status forward_moe(tp_plan_t P, const tp_shard_set* w, const float* x, float* y, const float* logits,
+                             int T, char* ws, cudaStream_t s) {
+    const tp_model_desc& d = P->d;
+    const int N = P->N;
+    for (int r = 0; r < N; ++r) {
+        if (!w->egu[r] || !w->ed[r] || !w->gamma_ffn[r])
+            return fail(TP_ERR_NULL, "tp_block_forward: shard %d expert weights or gamma_ffn NULL", r);
+        if (!aligned16(w->egu[r]) || !aligned16(w->ed[r]) || !aligned16(w->gamma_ffn[r]))
+            return fail(TP_ERR_ALIGN, "tp_block_forward: shard %d expert pointer not 16-byte aligned", r);
+    }
+    if (!aligned16(logits)) return fail(TP_ERR_ALIGN, "tp_block_forward: router_logits not 16-byte aligned");
+    MoeParams m{};
+    m.N = N;
+    m.T = T;
+    m.H = (int)d.hidden;
+    m.E = (int)d.n_experts;
+    m.top_k = (int)d.top_k;
+    m.Fs = (int)P->info.expert_ffn_shard;
+    m.eps = (float)d.eps;
+    m.x = x;
+    m.logits = logits;
+    for (int r = 0; r < N; ++r) {
+        m.gamma[r] = w->gamma_ffn[r];
+        m.egu[r] = w->egu[r];
+        m.ed[r] = w->ed[r];
+    }
+    m.ids = reinterpret_cast<int*>(ws + P->off_m_ids);
+    m.wts = reinterpret_cast<float*>(ws + P->off_m_wts);
+    m.offsets = reinterpret_cast<int*>(ws + P->off_m_off);
+    m.perm = reinterpret_cast<int*>(ws + P->off_m_perm);
+    m.slot_of = reinterpret_cast<int*>(ws + P->off_m_slot);
+    m.rinv = reinterpret_cast<float*>(ws + P->off_m_rinv);
+    m.xs = ws + P->off_m_xs;
+    m.act = ws + P->off_m_act;
+    m.o = reinterpret_cast<float*>(ws + P->off_m_o);
+    m.y = y;
+    m.status = reinterpret_cast<int*>(ws + P->off_status);
+    set_pdl(P->n_stage_ev == 0);
+    stage_mark(P, 0, s);
+    cudaError_t e = launch_moe(m, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: MoE launch");
+    stage_mark(P, 1, s);
+    return ok();
+}
+
 extern "C" tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
                                       const float* x, float* y, const int32_t* pos, int32_t B,
                                       int32_t T_per_seq, int32_t mode, const float* router_logits,
@@ -720,7 +790,15 @@ extern "C" tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, con
         if (B > kTMax) return fail(TP_ERR_SHAPE, "tp_block_forward: DECODE handles at most %d sequences", kTMax);
         return forward_decode(plan, w, kv, x, y, pos, B, ws, s);
     }
-    if (mode == TP_MODE_PREFILL || mode == TP_MODE_MOE_FFN)
+    if (mode == TP_MODE_MOE_FFN) {
+        if (!plan->moe) return fail(TP_ERR_INVALID_ARG, "tp_block_forward: MOE_FFN needs a plan with experts");
+        if (!router_logits) return fail(TP_ERR_NULL, "tp_block_forward: MOE_FFN needs router_logits");
+        if (plan->d.dtype != TP_BF16) return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: MOE_FFN runs on bf16 weights");
+        if (plan->d.hidden % 256 || plan->info.expert_ffn_shard % 256)
+            return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: MOE_FFN needs hidden and expert_ffn/tp multiples of 256");
+        return forward_moe(plan, w, x, y, router_logits, B * T_per_seq, ws, s);
+    }
+    if (mode == TP_MODE_PREFILL)
         return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: mode %d not available in this build", mode);
     return fail(TP_ERR_INVALID_ARG, "tp_block_forward: unknown mode %d", mode);
 }

@@ -2,6 +2,7 @@
 // translation units. Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -119,9 +120,38 @@ struct CopyBatch {
     int n;
 };
 
+// Expert-sliced MoE feed-forward block (bf16), slots = (token, choice) pairs.
+struct MoeParams {
+    int N, T, H, E, top_k, Fs;             // Fs: expert FFN width per shard
+    float eps;
+    const float* x;                        // [T][H]
+    const float* logits;                   // [T][E]
+    const float* gamma[TP_MAX_SHARDS];     // [H] per shard
+    const void* egu[TP_MAX_SHARDS];        // [E][2Fs][H]: gate rows then up rows per expert
+    const void* ed[TP_MAX_SHARDS];         // [E][H][Fs]
+    int* ids;                              // [T*k] chosen experts, descending logit
+    float* wts;                            // [T*k] renormalised routing weights
+    int* offsets;                          // [E+1] bucket starts (slot order)
+    int* perm;                             // [T*k] slot -> flat choice index t*k + j
+    int* slot_of;                          // [T*k] flat choice index -> slot
+    float* rinv;                           // [T*k] 1/rms of each slot's token
+    void* xs;                              // [N][T*k][H] bf16: x_t * gamma_r in slot order
+    void* act;                             // [N][T*k][Fs] bf16: SwiGLU outputs per slot
+    float* o;                              // [N][T*k][H] expert outputs per slot
+    float* y;                              // [T][H]
+    int* status;
+};
+cudaError_t launch_moe(const MoeParams& p, cudaStream_t s);
+
+// 2-D bf16 tensor map [rows, inner] with boxes box_inner x box_rows (cached).
+cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner, int box_rows, int swizzle128,
+                          CUtensorMap* out);
+
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)
+// Launch with the programmatic-stream-serialisation attribute (unless switched off).
+cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s, int threads);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_copy_batch(const CopyBatch& b, cudaStream_t s);
 cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s);
