@@ -667,11 +667,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const __
     float* s_bias = ss + 2 * kTMax;                                   // [64]
     // values every unit of this CTA needs, loaded once: the sums of squares
     // of the normalised input and the token positions
-    if (EPI == EPI_QKV_ROPE && tid < kTMax) {
-        ss[tid] = tid < T ? p.ss_in[tid] : 0.f;
-        s_pos[tid] = tid < T ? p.pos[tid] : 0;
-    }
-    if (EPI == EPI_SWIGLU) {
+    if (EPI == EPI_QKV_ROPE && tid < kTMax) s_pos[tid] = tid < T ? p.pos[tid] : 0;
+    if (EPI != EPI_ROWPAR) {
         float a = 0.f;                                                // warp t: token t
         if (warp < T)
             for (int q = lane; q < p.n_ss_tiles; q += 32) a += p.ss_tiles[q * kTMax + warp];
@@ -835,40 +832,36 @@ __global__ void __launch_bounds__(512) rowpar_reduce_kernel(const GemvParams p) 
     }
 }
 
-// RMSNorm operand preparation (one CTA per token row, 256 threads).
-__global__ void __launch_bounds__(256) norm_prep_kernel(const NormPrepParams p) {
+// RMSNorm operand preparation: CTA (t, kb) writes x[t, kb*256 .. +256) * gamma_r
+// as bf16 for every shard and that block's sum of squares ss[kb][t] (rows t >= T
+// are zero). 64 threads x 4 elements.
+__global__ void __launch_bounds__(64) norm_prep_kernel(const NormPrepParams p) {
     pdl_trigger();                                     // the next kernel may start streaming weights
     pdl_wait();
-    __shared__ float wsum[8];
-    const int t = blockIdx.x, tid = threadIdx.x;
-    const bool live = t < p.T;
-    float a = 0.f;
-    for (int k = tid * 4; k < p.H; k += 256 * 4) {
-        const float4 v = live ? *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + k)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        a = fmaf(v.x, v.x, a);
-        a = fmaf(v.y, v.y, a);
-        a = fmaf(v.z, v.z, a);
-        a = fmaf(v.w, v.w, a);
-        for (int r = 0; r < p.N; ++r) {
-            const float4 gm = *reinterpret_cast<const float4*>(p.gamma[r] + k);
-            uint2 pk;
-            pk.x = pack_bf16x2(v.x * gm.x, v.y * gm.y);
-            pk.y = pack_bf16x2(v.z * gm.z, v.w * gm.w);
-            *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xg) + ((size_t)r * kTMax + t) * p.H + k) = pk;
-        }
+    __shared__ float wsum[2];
+    const int t = blockIdx.x, kb = blockIdx.y, tid = threadIdx.x;
+    const int k = kb * 256 + tid * 4;
+    const bool in = k < p.H;                           // the last block may be ragged (H % 256 != 0)
+    const float4 v = (t < p.T && in) ? *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + k)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < p.N && in; ++r) {
+        const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma[r] + k));
+        uint2 pk;
+        pk.x = pack_bf16x2(v.x * gm.x, v.y * gm.y);
+        pk.y = pack_bf16x2(v.z * gm.z, v.w * gm.w);
+        *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xg) + ((size_t)r * kTMax + t) * p.H + k) = pk;
     }
+    float a = v.x * v.x;
+    a = fmaf(v.y, v.y, a);
+    a = fmaf(v.z, v.z, a);
+    a = fmaf(v.w, v.w, a);
     a = warp_sum(a);
     if ((tid & 31) == 0) wsum[tid >> 5] = a;
     __syncthreads();
-    if (tid == 0) {
-        float s = 0.f;
-        for (int w = 0; w < 8; ++w) s += wsum[w];
-        p.ss[t] = s;
-    }
+    if (tid == 0) p.ss[kb * kTMax + t] = wsum[0] + wsum[1];
 }
 
-template <int D>
+template <int D, int G>
 __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const AttnDecodeParams p) {
     constexpr int SK = kAttnStageBytes / (D * 2);      // keys per stage
     constexpr int LPK = D / 8;                          // lanes per key
@@ -883,8 +876,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
     float* s_l = s_m + kMaxGroup;                                             // [8]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = p.hq_s / p.hkv_s;
-    const int T = p.B;
+
     const int U = p.N * p.B * p.hkv_s * p.n_chunks;
 
     if (warp == kConsumers / 32) {                     // ---- producer
@@ -960,6 +952,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
         }
         consumer_sync(kConsumers);
         if (u + (int)gridDim.x < U) q_load(u + gridDim.x);
+        float qr[G][8];                                  // this thread's slice of every query of the group
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qr[g][e] = qs[g * D + li * 8 + e];
 
         // scores s[g][j] = (q_g / sqrt(d)) . k_j, one K stage at a time
         for (int k0 = 0; k0 < n; k0 += SK, ++it) {
@@ -968,6 +965,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
             mbar_wait(&R.full[sl], (it / kStages) & 1, R.abort, p.status);
             __syncwarp();
             const bf16* Kt = reinterpret_cast<const bf16*>(ring + sl * kAttnStageBytes);
+#pragma unroll
             for (int kk = 0; kk < SK; kk += KPP) {       // uniform trip count (shuffles below)
                 const int key = kk + ks;
                 float kv[8];
@@ -981,17 +979,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
 #pragma unroll
                     for (int e = 0; e < 8; ++e) kv[e] = 0.f;
                 }
+#pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float4 q0 = *reinterpret_cast<const float4*>(qs + g * D + li * 8);
-                    const float4 q1 = *reinterpret_cast<const float4*>(qs + g * D + li * 8 + 4);
-                    float dot = q0.x * kv[0];
-                    dot = fmaf(q0.y, kv[1], dot);
-                    dot = fmaf(q0.z, kv[2], dot);
-                    dot = fmaf(q0.w, kv[3], dot);
-                    dot = fmaf(q1.x, kv[4], dot);
-                    dot = fmaf(q1.y, kv[5], dot);
-                    dot = fmaf(q1.z, kv[6], dot);
-                    dot = fmaf(q1.w, kv[7], dot);
+                    // four independent partial products, then a short tree
+                    float d0 = qr[g][0] * kv[0], d1 = qr[g][1] * kv[1], d2 = qr[g][2] * kv[2], d3 = qr[g][3] * kv[3];
+                    d0 = fmaf(qr[g][4], kv[4], d0);
+                    d1 = fmaf(qr[g][5], kv[5], d1);
+                    d2 = fmaf(qr[g][6], kv[6], d2);
+                    d3 = fmaf(qr[g][7], kv[7], d3);
+                    float dot = (d0 + d1) + (d2 + d3);
 #pragma unroll
                     for (int o = LPK / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
                     if (li == 0 && key < keys) sc[g * kAttnChunk + k0 + key] = dot;
@@ -1022,9 +1018,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
         consumer_sync(kConsumers);
 
         // unnormalised output o[g] = sum_j e[g][j] v_j, one V stage at a time
-        float acc[kMaxGroup][8];
+        float acc[G][8];
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g)
+        for (int g = 0; g < G; ++g)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
         for (int k0 = 0; k0 < n; k0 += SK, ++it) {
@@ -1041,12 +1037,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
                 v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y;
                 v[4] = a2.x; v[5] = a2.y; v[6] = a3.x; v[7] = a3.y;
 #pragma unroll
-                for (int g = 0; g < kMaxGroup; ++g) {
-                    if (g < G) {
-                        const float e = sc[g * kAttnChunk + k0 + key];
+                for (int g = 0; g < G; ++g) {
+                    const float e = sc[g * kAttnChunk + k0 + key];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[g][q] = fmaf(e, v[q], acc[g][q]);
-                    }
+                    for (int q = 0; q < 8; ++q) acc[g][q] = fmaf(e, v[q], acc[g][q]);
                 }
             }
             __syncwarp();
@@ -1056,15 +1050,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
 #pragma unroll
         for (int o = LPK; o < 32; o <<= 1)
 #pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g)
+            for (int g = 0; g < G; ++g)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) acc[g][q] += __shfl_xor_sync(0xffffffffu, acc[g][q], o);
         if (lane < LPK) {
 #pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g)
-                if (g < G)
+            for (int g = 0; g < G; ++g)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) red[(warp * kMaxGroup + g) * D + li * 8 + q] = acc[g][q];
+                for (int q = 0; q < 8; ++q) red[(warp * kMaxGroup + g) * D + li * 8 + q] = acc[g][q];
         }
         consumer_sync(kConsumers);
         // this chunk's partial (unnormalised output, max, sum); combined later
@@ -1090,25 +1083,31 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnDecodeParams p) {
     pdl_trigger();
     pdl_wait();
-    __shared__ float s_w[64][kMaxGroup];     // per-chunk weight exp(m_c - M) (first 64 chunks)
+    constexpr int kMaxC = 128;                          // chunk statistics held in shared memory
+    __shared__ float s_m[kMaxC][kMaxGroup], s_l[kMaxC][kMaxGroup];
     __shared__ float s_den[kMaxGroup], s_M[kMaxGroup];
     const int gi = blockIdx.x, tid = threadIdx.x;
     const int G = p.hq_s / p.hkv_s, pstride = G * (D + 2);
     const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
     const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
-    const int nc = p.n_chunks;
+    const int nc = min(p.n_chunks, kMaxC);
+    if (p.n_chunks > kMaxC) set_status(p.status, TP_ERR_UNSUPPORTED);
+    // all chunks' (max, sum) in one parallel pass
+    for (int i = tid; i < nc * 2 * G; i += 256) {
+        const int cc = i / (2 * G), q = i - cc * 2 * G;
+        const float v = base[(size_t)cc * pstride + G * D + q];
+        if (q < G) s_m[cc][q] = v; else s_l[cc][q - G] = v;
+    }
+    __syncthreads();
     if (tid < G) {
         float M = -INFINITY;
-        for (int cc = 0; cc < nc; ++cc) {
-            const float l = base[(size_t)cc * pstride + G * D + G + tid];
-            if (l > 0.f) M = fmaxf(M, base[(size_t)cc * pstride + G * D + tid]);
-        }
+        for (int cc = 0; cc < nc; ++cc)
+            if (s_l[cc][tid] > 0.f) M = fmaxf(M, s_m[cc][tid]);
         float den = 0.f;
         for (int cc = 0; cc < nc; ++cc) {
-            const float l = base[(size_t)cc * pstride + G * D + G + tid];
-            const float w = l > 0.f ? expf(base[(size_t)cc * pstride + G * D + tid] - M) : 0.f;
-            if (cc < 64) s_w[cc][tid] = w;
-            den = fmaf(l, w, den);
+            const float w = s_l[cc][tid] > 0.f ? expf(s_m[cc][tid] - M) : 0.f;
+            s_m[cc][tid] = w;                           // reuse as the chunk weight
+            den = fmaf(s_l[cc][tid], w, den);
         }
         s_den[tid] = den;
         s_M[tid] = M;
@@ -1119,16 +1118,15 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnDecodeParam
     for (int i = tid; i < G * D; i += 256) {
         const int g = i / D;
         float num = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-            float w;
-            if (cc < 64) {
-                w = s_w[cc][g];
-            } else {
-                const float l = base[(size_t)cc * pstride + G * D + G + g];
-                w = l > 0.f ? expf(base[(size_t)cc * pstride + G * D + g] - s_M[g]) : 0.f;
-            }
-            num = fmaf(base[(size_t)cc * pstride + i], w, num);
+        int cc = 0;
+        for (; cc + 8 <= nc; cc += 8) {                  // eight independent loads in flight
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = base[(size_t)(cc + q) * pstride + i];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) num = fmaf(v[q], s_m[cc + q][g], num);
         }
+        for (; cc < nc; ++cc) num = fmaf(base[(size_t)cc * pstride + i], s_m[cc][g], num);
         out[i] = __float2bfloat16_rn(num / s_den[g]);
     }
 }
@@ -1251,8 +1249,8 @@ static cudaError_t launch_gemv_stream(const GemvParams& p, cudaStream_t s) {
 
 cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kTMax);
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3(kTMax, (p.H + 255) / 256);
+    cfg.blockDim = dim3(64);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1296,23 +1294,38 @@ size_t attn_stream_smem(int d) {
            (size_t)(kMaxGroup * d + kMaxGroup * kAttnChunk + 8 * kMaxGroup * d + 2 * kMaxGroup + kTMax) * 4;
 }
 
-template <int D>
+template <int D, int G>
 static cudaError_t launch_attn_stream(const AttnDecodeParams& p, cudaStream_t s) {
     const size_t smem = attn_stream_smem(D);
     static bool set = false;
     if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_stream_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        e = cudaFuncSetAttribute(attn_stream_kernel<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         set = true;
     }
     const int U = p.N * p.B * p.hkv_s * p.n_chunks;
-    const int grid = U < kSMs ? U : kSMs;
+    const int grid = U < 2 * kSMs ? U : 2 * kSMs;       // two CTAs per SM: more warps to hide latency
     void* args[] = {const_cast<AttnDecodeParams*>(&p)};
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_stream_kernel<D>), args, grid, smem, s, kStreamThreads);
+    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_stream_kernel<D, G>), args, grid, smem, s,
+                               kStreamThreads);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_attn_stream_g(const AttnDecodeParams& p, cudaStream_t s) {
+    switch (p.hq_s / p.hkv_s) {
+        case 1: return launch_attn_stream<D, 1>(p, s);
+        case 2: return launch_attn_stream<D, 2>(p, s);
+        case 3: return launch_attn_stream<D, 3>(p, s);
+        case 4: return launch_attn_stream<D, 4>(p, s);
+        case 5: return launch_attn_stream<D, 5>(p, s);
+        case 6: return launch_attn_stream<D, 6>(p, s);
+        case 7: return launch_attn_stream<D, 7>(p, s);
+        default: return launch_attn_stream<D, 8>(p, s);
+    }
 }
 
 static cudaError_t launch_small_pdl(const void* fn, void** args, int grid, int threads, cudaStream_t s) {
@@ -1343,7 +1356,7 @@ cudaError_t launch_attn_combine(const AttnDecodeParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s) {
-    if (dtype == TP_BF16) return p.d == 64 ? launch_attn_stream<64>(p, s) : launch_attn_stream<128>(p, s);
+    if (dtype == TP_BF16) return p.d == 64 ? launch_attn_stream_g<64>(p, s) : launch_attn_stream_g<128>(p, s);
     return p.d == 64 ? launch_attn_t<float, 64>(p, s) : launch_attn_t<float, 128>(p, s);
 }
 

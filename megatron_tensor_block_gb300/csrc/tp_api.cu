@@ -243,7 +243,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_part_gu = take((size_t)P->g_gu.units() * kPartStride * 4);
         P->off_part_down = take((size_t)P->g_down.units() * kPartStride * 4);
         P->off_xg = take((size_t)N * kTMax * H * 2);
-        P->off_ss = take((size_t)kTMax * 4);
+        P->off_ss = take((size_t)(H / 256 + 1) * kTMax * 4);
         P->off_hg = take((size_t)N * kTMax * H * 2);
         P->off_ss_tiles = take((size_t)(H / kTileRows) * kTMax * 4);
         P->ws_decode_end = off;
@@ -608,7 +608,8 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         e = launch_norm_prep(np, s);
         if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: norm prep launch");
         q.xact = ws + P->off_xg;
-        q.ss_in = np.ss;
+        q.ss_tiles = np.ss;
+        q.n_ss_tiles = (int)((d.hidden + 255) / 256);
     }
     e = launch_gemv(q, EPI_QKV_ROPE, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: qkv launch");
