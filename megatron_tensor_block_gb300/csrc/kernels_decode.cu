@@ -576,7 +576,7 @@ struct TmaGemvArgs {
 // boxes (rows 0-31 and 32-63 of the tile) and the matching activation box
 // (the shard's 8 token rows). Consumers touch only shared memory.
 template <int EPI>
-__global__ void __launch_bounds__(kStreamThreads, 1) gemv_stream_kernel(const __grid_constant__ TmaGemvArgs A) {
+__global__ void __launch_bounds__(kStreamThreads, 2) gemv_stream_kernel(const __grid_constant__ TmaGemvArgs A) {
     const GemvParams& p = A.p;
     extern __shared__ __align__(1024) unsigned char smem[];
     const Ring R = ring_setup(smem, kGemvStages);
@@ -1241,7 +1241,7 @@ static cudaError_t launch_gemv_stream(const GemvParams& p, cudaStream_t s) {
     }
     cudaError_t ex = weight_tensor_map(p.xact, p.K, p.n_shards * kTMax, &A.tmx, kTMax);
     if (ex != cudaSuccess) return ex;
-    const int grid = p.shape.units() < kSMs ? p.shape.units() : kSMs;
+    const int grid = p.shape.units() < 2 * kSMs ? p.shape.units() : 2 * kSMs;   // two CTAs per SM
     void* args[] = {&A};
     cudaError_t e = launch_pdl(reinterpret_cast<const void*>(gemv_stream_kernel<EPI>), args, grid, smem, s, kStreamThreads);
     return e != cudaSuccess ? e : cudaGetLastError();

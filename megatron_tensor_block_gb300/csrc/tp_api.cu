@@ -104,7 +104,7 @@ static GemvShape make_shape(int groups, int shards_per_group, int K, size_t esz)
             for (int C = 1; C <= stages && shards_per_group * C <= kMaxGroupUnits; ++C) {
                 if (stages % C) continue;
                 s.chunks = C;
-                if ((long)groups * shards_per_group * C >= 3L * kSMs) break;
+                if ((long)groups * shards_per_group * C >= 6L * kSMs) break;
             }
             if (K % (s.chunks * 64) || (K / s.chunks) % 64) s.chunks = 1;
         }
