@@ -318,6 +318,18 @@ tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set* w, const 
 tp_status tp_reduce_partials(tp_plan_t plan, const float* partials, const float* residual,
                              const float* bias, float* out, int64_t M, void* stream);
 
+/* Tensor-core GEMM, the primitive of the prefill-regime projections:
+ *   C[M, N] = A[M, K] * B[N, K]^T
+ * A and B are bf16, row-major with K contiguous (B in the [out, in] weight
+ * layout), C is float32 row-major; accumulation in float32 on the tcgen05
+ * tensor cores. Requires M % 128 == 0, N % 256 == 0, K % 64 == 0 and
+ * 16-byte aligned pointers. `device_status` is a DEVICE int32 (or NULL) that
+ * receives TP_ERR_TIMEOUT / TP_ERR_ALIGN if a bounded device wait gives up.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_ALIGN, TP_ERR_UNSUPPORTED,
+ * TP_ERR_CUDA. */
+tp_status tp_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                       int32_t* device_status, void* stream);
+
 /* Reads the workspace status word (TP_OK or the first device-detected error
  * since tp_workspace_init) into *out (host). Synchronises `stream`. */
 tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);

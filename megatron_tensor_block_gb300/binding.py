@@ -105,6 +105,7 @@ def load(path: str | None = None) -> C.CDLL:
                                            VP]),
         "tp_reduce_partials": (I32, [P, VP, VP, VP, VP, I64, VP]),
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
+        "tp_gemm_bf16": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
         "tp_profile_stages": (I32, [P, C.POINTER(VP), I32]),
         "tp_last_error": (C.c_char_p, []),
         "tp_version": (I32, []),
@@ -234,6 +235,11 @@ def tp_block_forward_noalloc(plan: Plan, shards: dict, kv: tuple, x, y, pos, B: 
 def tp_reduce_partials(plan: Plan, partials, residual, bias, out, M: int, stream=None) -> None:
     _check(load().tp_reduce_partials(plan.handle, _ptr(partials), _ptr(residual), _ptr(bias), _ptr(out), M,
                                      _stream(stream)))
+
+
+def tp_gemm_bf16(A, B, C, M: int, N: int, K: int, device_status=None, stream=None) -> None:
+    """C[M, N] = A[M, K] @ B[N, K].T on the tensor cores (bf16 in, float32 out)."""
+    _check(load().tp_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, _ptr(device_status), _stream(stream)))
 
 
 def tp_get_device_status(workspace, stream=None) -> int:

@@ -2,6 +2,7 @@
 // workspace layout, argument checks, and the launch sequence of each call.
 // Every step of the block runs in the kernels of this library; there is no
 // host-side or CPU fallback path.
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -813,6 +814,20 @@ extern "C" tp_status tp_reduce_partials(tp_plan_t plan, const float* partials, c
     cudaError_t e = launch_reduce_partials(partials, residual, bias, out, plan->N, M, plan->d.hidden,
                                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tp_reduce_partials: launch");
+    return ok();
+}
+
+extern "C" tp_status tp_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                                  int32_t* device_status, void* stream) {
+    if (!A || !B || !C) return fail(TP_ERR_NULL, "tp_gemm_bf16: NULL operand");
+    if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 256 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return fail(TP_ERR_SHAPE, "tp_gemm_bf16: need M %% 128 == 0, N %% 256 == 0, K %% 64 == 0 (got %lld, %lld, %lld)",
+                    (long long)M, (long long)N, (long long)K);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return fail(TP_ERR_ALIGN, "tp_gemm_bf16: pointers must be 16-byte aligned");
+    tp_status st = check_device();
+    if (st) return st;
+    cudaError_t e = launch_tc_gemm_plain(A, B, C, (int)M, (int)N, (int)K, device_status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tp_gemm_bf16: launch");
     return ok();
 }
 

@@ -147,6 +147,11 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s);
 cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner, int box_rows, int swizzle128,
                           CUtensorMap* out);
 
+// tcgen05 GEMM, C[M, N] (fp32) = A[M, K] * B[N, K]^T (bf16, K-major),
+// M % 128 == 0, N % 256 == 0, K % 64 == 0.
+cudaError_t launch_tc_gemm_plain(const void* A, const void* B, float* C, int M, int N, int K, int* status,
+                                 cudaStream_t s);
+
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)
