@@ -263,9 +263,16 @@ tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t bytes, void*
  * deterministic (byte-identical across calls on the same inputs).
  * Positions past max_kv are not written; the kernels record
  * TP_ERR_CAPACITY in the workspace status word (tp_get_device_status).
+ * PREFILL runs on bf16 plans only. It normalises once per distinct gamma
+ * pointer: shards that point at one replicated gamma tensor share one
+ * normalised copy of the activations (same values either way). Its
+ * activations between stages are stored as bf16 (normalised inputs, q,
+ * attention output, SwiGLU output) and accumulated in float32; the
+ * row-parallel partials and the residual stream stay float32.
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE (B or tokens above the plan's maxima,
- * T_per_seq != 1 in DECODE), TP_ERR_CAPACITY (workspace too small),
- * TP_ERR_INVALID_ARG (mode not valid for the plan), TP_ERR_UNSUPPORTED,
+ * T_per_seq != 1 in DECODE), TP_ERR_CAPACITY (workspace too small,
+ * T_per_seq > max_kv), TP_ERR_INVALID_ARG (mode not valid for the plan),
+ * TP_ERR_UNSUPPORTED (PREFILL or MOE_FFN on an fp32 plan), TP_ERR_ALIGN,
  * TP_ERR_CUDA. */
 tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
                            const float* x, float* y, const int32_t* pos,

@@ -156,3 +156,721 @@ cudaError_t launch_tc_gemm_plain(const void* A, const void* B, float* C, int M, 
 }
 
 }  // namespace tpk
+
+namespace tpk {
+
+// ---------------------------------------------------------------------------
+// shared pieces of the fused projections
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tc_setup(unsigned char* smem, int nfull, int nempty, uint32_t tmem_cols,
+                                         int* status, uint64_t*& full, uint64_t*& empty, uint64_t*& extra,
+                                         uint32_t*& tmem_slot, volatile int*& abort_flag, int n_extra,
+                                         const uint32_t* extra_counts) {
+    full = reinterpret_cast<uint64_t*>(smem);
+    empty = full + nfull;
+    extra = empty + nempty;
+    tmem_slot = reinterpret_cast<uint32_t*>(extra + n_extra);
+    abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nfull; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < nempty; ++i) mbar_init(&empty[i], 1);
+        for (int i = 0; i < n_extra; ++i) mbar_init(&extra[i], extra_counts[i]);
+        *abort_flag = (smem_u32(smem + 1024) & 1023u) ? 1 : 0;
+        if (*abort_flag) set_status(status, TP_ERR_ALIGN);
+        fence_mbar_init();
+    }
+    if ((threadIdx.x >> 5) == 1) tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+__device__ __forceinline__ void tc_teardown(uint64_t* done_bar, uint32_t done_parity, uint32_t tmem,
+                                            uint32_t cols) {
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 1) {
+        volatile int no_abort = 0;
+        if (done_bar) mbar_wait(done_bar, done_parity, &no_abort, nullptr);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, cols);
+        tmem_relinquish();
+    }
+}
+
+__device__ __forceinline__ float fbits(uint32_t u) { return __uint_as_float(u); }
+
+// ---------------------------------------------------------------------------
+// column-parallel projection with fused epilogue (QKV + RoPE + KV append, or
+// gate/up + SwiGLU), one 128-token x 256-column tile of one shard per CTA
+// ---------------------------------------------------------------------------
+
+enum TcMode : int { TC_QKV = 0, TC_GATEUP = 1 };
+
+struct TcColArgs {
+    CUtensorMap ta;                       // normalised activations [T, K], boxes 64 x 128
+    CUtensorMap tb[TP_MAX_SHARDS];        // QKV: [qkv_rows, K] boxes 64 x 256; gate/up: [2F', K] boxes 64 x 128
+    int T, K, S;                          // tokens, reduction length, tokens per sequence
+    int a_row_stride;                     // first A row of shard r = r * a_row_stride (0: shared copy)
+    int hq_s, hkv_s, d, max_kv, ffn_s;
+    const float* bias[TP_MAX_SHARDS];
+    const int* pos;                       // [B] first new position of each sequence
+    const float2* rope;                   // [max_kv][d/2] (cos, sin)
+    bf16* q_out;                          // [N][T][hq_s * d]
+    void* kcache[TP_MAX_SHARDS];
+    void* vcache[TP_MAX_SHARDS];
+    bf16* act;                            // [N][T][F']
+    int* status;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_col_kernel(const __grid_constant__ TcColArgs g) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *full, *empty, *extra;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    const uint32_t one = 1;
+    tc_setup(smem, kTcStages, kTcStages, 256, g.status, full, empty, extra, tmem_slot, abort_flag, 1, &one);
+    uint64_t* accum = extra;
+    const uint32_t tmem = *tmem_slot;
+    unsigned char* stages = smem + 1024;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTcBM, nt = blockIdx.y, r = blockIdx.z;
+    const int nk = g.K / kTcBK;
+
+    if (warp == 0) {
+        if (lane == 0 && !*abort_flag) {
+            int kb = 0;
+            for (; kb < nk; ++kb) {
+                const int s = kb % kTcStages;
+                if (!mbar_wait(&empty[s], ((kb / kTcStages) & 1) ^ 1, abort_flag, g.status)) break;
+                mbar_arrive_expect_tx(&full[s], kTcStageBytes);
+                unsigned char* st = stages + s * kTcStageBytes;
+                tma_load_2d_keep(st, &g.ta, kb * kTcBK, r * g.a_row_stride + m0, &full[s]);
+                if (MODE == TC_QKV) {
+                    tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, nt * kTcBN, &full[s]);
+                } else {   // 128 gate rows, then the matching 128 up rows
+                    tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, nt * 128, &full[s]);
+                    tma_load_2d_keep(st + kTcABytes + kTcBBytes / 2, &g.tb[r], kb * kTcBK, g.ffn_s + nt * 128,
+                                     &full[s]);
+                }
+            }
+            volatile int no_abort = 0;
+            for (int k = kb > kTcStages ? kb - kTcStages : 0; k < kb; ++k)
+                mbar_wait(&full[k % kTcStages], (k / kTcStages) & 1, &no_abort, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
+            for (int kb = 0; kb < nk && !*abort_flag; ++kb) {
+                const int s = kb % kTcStages;
+                if (!mbar_wait(&full[s], (kb / kTcStages) & 1, abort_flag, g.status)) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(stages + s * kTcStageBytes), b0 = a0 + kTcABytes;
+#pragma unroll
+                for (int k = 0; k < kTcBK / 16; ++k)
+                    tc_mma(tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+                tc_commit(smem_u32(&empty[s]));
+            }
+            tc_commit(smem_u32(accum));
+        }
+    } else {
+        const int q = warp & 3;
+        const bool ok = mbar_wait(accum, 0, abort_flag, g.status);
+        tc_fence_after();
+        const int t = m0 + 32 * q + lane;
+        const bool live = ok && t < g.T;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        if (MODE == TC_GATEUP) {
+            for (int c = 0; c < 4; ++c) {
+                if (nt * 128 + 32 * c >= g.ffn_s) break;     // ragged last tile (warp-uniform)
+                uint32_t gv[32], uv[32];
+                tmem_ld32(tmem + lane_off + 32 * c, gv);
+                tmem_ld32(tmem + lane_off + 128 + 32 * c, uv);
+                tmem_wait_ld();
+                if (live) {
+                    bf16* dst = g.act + ((size_t)r * g.T + t) * g.ffn_s + nt * 128 + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float g0 = fbits(gv[i]), g1 = fbits(gv[i + 1]);
+                        const float a0 = g0 / (1.0f + expf(-g0)) * fbits(uv[i]);
+                        const float a1 = g1 / (1.0f + expf(-g1)) * fbits(uv[i + 1]);
+                        *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(a0, a1);
+                    }
+                }
+            }
+        } else {
+            const int d = g.d, half = d >> 1;
+            const int b = t / g.S, sidx = t - b * g.S;
+            const int p = live ? g.pos[b] + sidx : 0;
+            const bool in_cache = p >= 0 && p < g.max_kv;
+            if (live && !in_cache) set_status(g.status, TP_ERR_CAPACITY);
+            const int pr = in_cache ? p : 0;                 // rotary table row (in range on every path)
+            const int n_heads = g.hq_s + 2 * g.hkv_s;
+            for (int hh = 0; hh < kTcBN / d; ++hh) {
+                const int head = (nt * kTcBN) / d + hh;
+                if (head >= n_heads) break;                   // ragged last tile (warp-uniform)
+                for (int c = 0; c < half / 32; ++c) {
+                    uint32_t lo[32], hi[32];
+                    tmem_ld32(tmem + lane_off + hh * d + 32 * c, lo);
+                    tmem_ld32(tmem + lane_off + hh * d + half + 32 * c, hi);
+                    tmem_wait_ld();
+                    if (!live) continue;
+                    const float* bias = g.bias[r];
+                    const bool rot = head < g.hq_s + g.hkv_s;
+                    bf16* qdst = g.q_out + ((size_t)r * g.T + t) * g.hq_s * d + head * d + 32 * c;
+                    const bool is_q = head < g.hq_s;
+                    const bool is_k = !is_q && head < g.hq_s + g.hkv_s;
+                    bf16* cdst = nullptr;
+                    if (!is_q && in_cache) {
+                        const int kvh = is_k ? head - g.hq_s : head - g.hq_s - g.hkv_s;
+                        bf16* cache = reinterpret_cast<bf16*>(is_k ? g.kcache[r] : g.vcache[r]);
+                        cdst = cache + (((size_t)b * g.hkv_s + kvh) * g.max_kv + p) * d + 32 * c;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float va0 = fbits(lo[i]), va1 = fbits(lo[i + 1]);
+                        float vb0 = fbits(hi[i]), vb1 = fbits(hi[i + 1]);
+                        if (bias) {
+                            const int col = head * d + 32 * c + i;
+                            va0 += bias[col]; va1 += bias[col + 1];
+                            vb0 += bias[col + half]; vb1 += bias[col + half + 1];
+                        }
+                        if (rot) {
+                            const float2 cs0 = g.rope[(size_t)pr * half + 32 * c + i];
+                            const float2 cs1 = g.rope[(size_t)pr * half + 32 * c + i + 1];
+                            const float ra0 = va0 * cs0.x - vb0 * cs0.y, rb0 = va0 * cs0.y + vb0 * cs0.x;
+                            const float ra1 = va1 * cs1.x - vb1 * cs1.y, rb1 = va1 * cs1.y + vb1 * cs1.x;
+                            va0 = ra0; vb0 = rb0; va1 = ra1; vb1 = rb1;
+                        }
+                        if (is_q) {
+                            *reinterpret_cast<uint32_t*>(qdst + i) = pack_bf16x2(va0, va1);
+                            *reinterpret_cast<uint32_t*>(qdst + half + i) = pack_bf16x2(vb0, vb1);
+                        } else if (cdst) {
+                            *reinterpret_cast<uint32_t*>(cdst + i) = pack_bf16x2(va0, va1);
+                            *reinterpret_cast<uint32_t*>(cdst + half + i) = pack_bf16x2(vb0, vb1);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_teardown(accum, 0, tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// row-parallel projection with the rank-ordered reduction in tensor memory:
+// for one 128-token x 128-column output tile, shard r's partial product is
+// accumulated in its own TMEM buffer (two buffers alternate), then added to
+// the running sum in rank order: sum = ((p0 + p1) + p2) + ...; the residual is
+// added last.
+// ---------------------------------------------------------------------------
+
+constexpr int kRowBN = 128;
+constexpr int kRowStages = 6;
+constexpr int kRowStageBytes = kTcABytes + kRowBN * kTcBK * 2;   // 32 KB
+constexpr int kRowSmem = 1024 + kRowStages * kRowStageBytes;
+
+struct TcRowArgs {
+    CUtensorMap ta;                       // per-shard activations stacked [N * T, Kr], boxes 64 x 128
+    CUtensorMap tb[TP_MAX_SHARDS];        // shard weights [H, Kr], boxes 64 x 128
+    int T, Kr, N, H;
+    const float* resid;                   // [T][H]
+    float* out;                           // [T][H]
+    int* status;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_row_kernel(const __grid_constant__ TcRowArgs g) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *full, *empty, *extra;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+    const uint32_t counts[5] = {1, 1, 4, 4, 1};   // partial full x2, partial empty x2, done
+    tc_setup(smem, kRowStages, kRowStages, 512, g.status, full, empty, extra, tmem_slot, abort_flag, 5, counts);
+    uint64_t* pfull = extra;
+    uint64_t* pempty = extra + 2;
+    uint64_t* done = extra + 4;
+    const uint32_t tmem = *tmem_slot;
+    unsigned char* stages = smem + 1024;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * kRowBN;
+    const int nk = g.Kr / kTcBK;
+
+    if (warp == 0) {
+        if (lane == 0 && !*abort_flag) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int r = 0; r < g.N && ok; ++r)
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kRowStages;
+                    if (!mbar_wait(&empty[s], ((it / kRowStages) & 1) ^ 1, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], kRowStageBytes);
+                    unsigned char* st = stages + s * kRowStageBytes;
+                    tma_load_2d_keep(st, &g.ta, kb * kTcBK, r * g.T + m0, &full[s]);
+                    tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, n0, &full[s]);
+                }
+            volatile int no_abort = 0;
+            for (uint32_t k = it > (uint32_t)kRowStages ? it - kRowStages : 0; k < it; ++k)
+                mbar_wait(&full[k % kRowStages], (k / kRowStages) & 1, &no_abort, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kTcBM, kRowBN);
+            uint32_t it = 0;
+            bool ok = !*abort_flag;
+            for (int r = 0; r < g.N && ok; ++r) {
+                const int buf = r & 1;
+                if (!mbar_wait(&pempty[buf], ((r >> 1) & 1) ^ 1, abort_flag, g.status)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem + 128 + 128 * buf;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kRowStages;
+                    if (!mbar_wait(&full[s], (it / kRowStages) & 1, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(stages + s * kRowStageBytes), b0 = a0 + kTcABytes;
+#pragma unroll
+                    for (int k = 0; k < kTcBK / 16; ++k)
+                        tc_mma(dt, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+                    tc_commit(smem_u32(&empty[s]));
+                }
+                tc_commit(smem_u32(&pfull[buf]));
+            }
+            tc_commit(smem_u32(done));
+        }
+    } else {
+        const int q = warp & 3;
+        const int t = m0 + 32 * q + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        for (int r = 0; r < g.N; ++r) {
+            const int buf = r & 1;
+            const bool ok = mbar_wait(&pfull[buf], (r >> 1) & 1, abort_flag, g.status);
+            tc_fence_after();
+            for (int c = 0; c < kRowBN / 32; ++c) {
+                uint32_t pv[32], sv[32];
+                tmem_ld32(tmem + lane_off + 128 + 128 * buf + 32 * c, pv);
+                if (r > 0) tmem_ld32(tmem + lane_off + 32 * c, sv);
+                tmem_wait_ld();
+                if (r > 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pv[i] = __float_as_uint(fbits(sv[i]) + fbits(pv[i]));
+                }
+                if (r + 1 < g.N) {
+                    tmem_st32(tmem + lane_off + 32 * c, pv);
+                } else if (ok && t < g.T && n0 + 32 * c < g.H) {
+                    const size_t o = (size_t)t * g.H + n0 + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 rv = *reinterpret_cast<const float4*>(g.resid + o + i);
+                        *reinterpret_cast<float4*>(g.out + o + i) =
+                            make_float4(rv.x + fbits(pv[i]), rv.y + fbits(pv[i + 1]), rv.z + fbits(pv[i + 2]),
+                                        rv.w + fbits(pv[i + 3]));
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[buf]);
+        }
+    }
+    tc_teardown(done, 0, tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm (bf16 output, fully normalised) and the rotary table
+// ---------------------------------------------------------------------------
+
+struct NormCopies {
+    const float* gamma[TP_MAX_SHARDS];
+    int n;
+};
+
+// One token per CTA: 1/rms once, then one bf16 copy per distinct gamma,
+// copy c at out + c * T * H.
+__global__ void __launch_bounds__(256) prefill_norm_kernel(const float* __restrict__ x, const NormCopies gc,
+                                                           bf16* __restrict__ out, int T, int H, float eps) {
+    __shared__ float wsum[8];
+    __shared__ float s_rinv;
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const float* xr = x + (size_t)t * H;
+    float a = 0.f;
+    for (int k = tid * 4; k < H; k += 1024) {
+        const float4 v = *reinterpret_cast<const float4*>(xr + k);
+        a = fmaf(v.x, v.x, a);
+        a = fmaf(v.y, v.y, a);
+        a = fmaf(v.z, v.z, a);
+        a = fmaf(v.w, v.w, a);
+    }
+    a = warp_sum(a);
+    if ((tid & 31) == 0) wsum[tid >> 5] = a;
+    __syncthreads();
+    if (tid == 0) {
+        float ss = 0.f;
+        for (int w = 0; w < 8; ++w) ss += wsum[w];
+        s_rinv = 1.0f / sqrtf(ss / (float)H + eps);
+    }
+    __syncthreads();
+    const float ri = s_rinv;
+    for (int k = tid * 4; k < H; k += 1024) {
+        const float4 v = *reinterpret_cast<const float4*>(xr + k);
+        for (int c = 0; c < gc.n; ++c) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gc.gamma[c] + k);
+            uint2 pk;
+            pk.x = pack_bf16x2(v.x * ri * g4.x, v.y * ri * g4.y);
+            pk.y = pack_bf16x2(v.z * ri * g4.z, v.w * ri * g4.w);
+            *reinterpret_cast<uint2*>(out + ((size_t)c * T + t) * H + k) = pk;
+        }
+    }
+}
+
+__global__ void rope_table_kernel(float2* tab, int max_pos, int half, int d, float log2_theta) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= max_pos * half) return;
+    const int p = i / half, j = i - p * half;
+    float sn, cs;
+    sincosf((float)p * exp2f(-(2.0f * j / d) * log2_theta), &sn, &cs);
+    tab[i] = make_float2(cs, sn);
+}
+
+// ---------------------------------------------------------------------------
+// causal prefill attention (FlashAttention-2 style on mma.sync): one CTA per
+// 64 queries of one head of one sequence of one shard; K/V tiles of 64 keys in
+// padded shared memory (conflict-free ldmatrix), online softmax in registers.
+// ---------------------------------------------------------------------------
+
+struct FlashArgs {
+    const bf16* q;                        // [N][T][hq_s * D]
+    const void* kcache[TP_MAX_SHARDS];    // [Bmax][hkv_s][max_kv][D]
+    const void* vcache[TP_MAX_SHARDS];
+    bf16* out;                            // [N][T][hq_s * D]
+    const int* pos;
+    int N, B, S, T, hq_s, hkv_s, max_kv;
+    float scale;
+    int* status;
+};
+
+constexpr int kFaQ = 64, kFaK = 64;
+
+template <int D>
+struct FaShape {
+    static constexpr int kPitch = D + 8;                                  // bf16 per shared row
+    static constexpr int kTile = kFaK * kPitch;                           // one K or V tile
+    static constexpr int kSmem = (kFaQ * kPitch + 4 * kTile) * 2;         // Q + 2 x (K, V)
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+    const int n = pred ? 16 : 0;                   // 0: fill 16 zero bytes, read nothing
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+
+// Each of the 4 warps owns 16 query rows; lane (g = lane/4, tq = lane%4)
+// holds rows g and g+8 of the score and output fragments.
+template <int D>
+__global__ void __launch_bounds__(128) flash_prefill_kernel(const FlashArgs f) {
+    using Sh = FaShape<D>;
+    constexpr int P = Sh::kPitch, KS = D / 16, NO = D / 8;
+    extern __shared__ __align__(16) unsigned char fa_smem[];
+    bf16* sq = reinterpret_cast<bf16*>(fa_smem);
+    bf16* sk = sq + kFaQ * P;                      // [2][kFaK * P]
+    bf16* sv = sk + 2 * Sh::kTile;                 // [2][kFaK * P]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;
+    const int nqb = (f.S + kFaQ - 1) / kFaQ;
+    // heaviest query blocks first (causal work grows with the block index)
+    int idx = blockIdx.x;
+    const int qb = nqb - 1 - idx % nqb;
+    idx /= nqb;
+    const int h = idx % f.hq_s;
+    idx /= f.hq_s;
+    const int b = idx % f.B;
+    const int r = idx / f.B;
+    const int G = f.hq_s / f.hkv_s, kvh = h / G;
+    const int p0 = f.pos[b];
+    const int rows = min(kFaQ, f.S - qb * kFaQ);         // valid queries in this block
+    const int q_first = p0 + qb * kFaQ;                   // position of the block's first query
+    const int nkeys = max(0, min(q_first + rows, f.max_kv));   // keys 0 .. last query position
+    const int ntiles = (nkeys + kFaK - 1) / kFaK;
+    const int t0 = b * f.S + qb * kFaQ;                   // token row of the block's first query
+    const size_t qstride = (size_t)f.hq_s * D;
+    const bf16* qsrc = f.q + ((size_t)r * f.T + t0) * qstride + h * D;
+    const bf16* kbase = reinterpret_cast<const bf16*>(f.kcache[r]) + ((size_t)b * f.hkv_s + kvh) * f.max_kv * D;
+    const bf16* vbase = reinterpret_cast<const bf16*>(f.vcache[r]) + ((size_t)b * f.hkv_s + kvh) * f.max_kv * D;
+
+    for (int i = tid; i < kFaQ * D / 8; i += 128) {
+        const int row = i / (D / 8), c = i - row * (D / 8);
+        const bool in = row < rows;
+        cp_async16(smem_u32(sq + row * P + c * 8), qsrc + (size_t)(in ? row : 0) * qstride + c * 8, in);
+    }
+    auto load_kv = [&](int kt, int buf) {
+        for (int i = tid; i < kFaK * D / 8; i += 128) {
+            const int row = i / (D / 8), c = i - row * (D / 8);
+            const int key = kt * kFaK + row;
+            const bool in = key < nkeys;
+            const size_t off = (size_t)(in ? key : 0) * D + c * 8;
+            cp_async16(smem_u32(sk + buf * Sh::kTile + row * P + c * 8), kbase + off, in);
+            cp_async16(smem_u32(sv + buf * Sh::kTile + row * P + c * 8), vbase + off, in);
+        }
+    };
+    if (ntiles > 0) load_kv(0, 0);
+    cp_async_commit();
+
+    float o[NO][4];
+#pragma unroll
+    for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qa[KS][4];
+    const int mi = lane >> 3, rr = lane & 7;
+    const int qpos0 = q_first + 16 * warp + g, qpos1 = qpos0 + 8;
+
+    for (int kt = 0; kt < ntiles; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < ntiles) load_kv(kt + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const bf16* kt_s = sk + buf * Sh::kTile;
+        const bf16* vt_s = sv + buf * Sh::kTile;
+        if (kt == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+                ldsm4(smem_u32(sq + (16 * warp + (mi & 1) * 8 + rr) * P + ks * 16 + (mi >> 1) * 8), qa[ks][0],
+                      qa[ks][1], qa[ks][2], qa[ks][3]);
+        }
+        float s[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int np = 0; np < 4; ++np)
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t b0, b1, b2, b3;
+                ldsm4(smem_u32(kt_s + (16 * np + (mi >> 1) * 8 + rr) * P + ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
+                mma_bf16_16816(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+                mma_bf16_16816(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+            }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            const int key = kt * kFaK + 8 * n + 2 * tq;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float v0 = s[n][e] * f.scale, v1 = s[n][2 + e] * f.scale;
+                if (key + e > qpos0 || key + e >= nkeys) v0 = -INFINITY;
+                if (key + e > qpos1 || key + e >= nkeys) v1 = -INFINITY;
+                s[n][e] = v0;
+                s[n][2 + e] = v1;
+                mx0 = fmaxf(mx0, v0);
+                mx1 = fmaxf(mx1, v1);
+            }
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = (mn0 == -INFINITY) ? 1.f : expf(m0 - mn0);
+        const float al1 = (mn1 == -INFINITY) ? 1.f : expf(m1 - mn1);
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float e0 = (s[n][e] == -INFINITY) ? 0.f : expf(s[n][e] - mn0);
+                const float e1 = (s[n][2 + e] == -INFINITY) ? 0.f : expf(s[n][2 + e] - mn1);
+                s[n][e] = e0;
+                s[n][2 + e] = e1;
+                ps0 += e0;
+                ps1 += e1;
+            }
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int n = 0; n < NO; ++n) {
+            o[n][0] *= al0;
+            o[n][1] *= al0;
+            o[n][2] *= al1;
+            o[n][3] *= al1;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {          // 16 keys per step
+            const uint32_t a0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+            const uint32_t a1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+            const uint32_t a2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            const uint32_t a3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                uint32_t b0, b1, b2, b3;
+                ldsm4t(smem_u32(vt_s + (16 * kk + (mi & 1) * 8 + rr) * P + 16 * np + (mi >> 1) * 8), b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncthreads();                           // this buffer is refilled two tiles later
+    }
+    cp_async_wait<0>();
+    const float inv0 = l0 > 0.f ? 1.0f / l0 : 0.f, inv1 = l1 > 0.f ? 1.0f / l1 : 0.f;
+    const int row0 = 16 * warp + g, row1 = row0 + 8;
+    bf16* dst0 = f.out + ((size_t)r * f.T + t0 + row0) * qstride + h * D;
+    bf16* dst1 = f.out + ((size_t)r * f.T + t0 + row1) * qstride + h * D;
+#pragma unroll
+    for (int n = 0; n < NO; ++n) {
+        if (row0 < rows)
+            *reinterpret_cast<uint32_t*>(dst0 + 8 * n + 2 * tq) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+        if (row1 < rows)
+            *reinterpret_cast<uint32_t*>(dst1 + 8 * n + 2 * tq) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_prefill_norm(const float* x, const float* const* gammas, int n_copies, void* out, int T, int H,
+                                float eps, cudaStream_t s) {
+    if (n_copies < 1 || n_copies > TP_MAX_SHARDS) return cudaErrorInvalidValue;
+    NormCopies gc;
+    memset(&gc, 0, sizeof gc);
+    for (int c = 0; c < n_copies; ++c) gc.gamma[c] = gammas[c];
+    gc.n = n_copies;
+    if (T > 0) prefill_norm_kernel<<<T, 256, 0, s>>>(x, gc, static_cast<bf16*>(out), T, H, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* tab, int max_pos, int d, double log2_theta, cudaStream_t s) {
+    const int n = max_pos * (d / 2);
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(tab, max_pos, d / 2, d, (float)log2_theta);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_col(int mode, const PrefillColParams& p, cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    TcColArgs g;
+    memset(&g, 0, sizeof g);
+    const int copies = p.a_copies > 1 ? p.N : 1;
+    cudaError_t e = tensor_map_2d(p.A, p.K, (long)copies * p.T, kTcBK, kTcBM, 1, &g.ta);
+    for (int r = 0; r < p.N && e == cudaSuccess; ++r)
+        e = tensor_map_2d(p.W[r], p.K, p.rows, kTcBK, mode == TC_QKV ? kTcBN : 128, 1, &g.tb[r]);
+    if (e != cudaSuccess) return e;
+    g.a_row_stride = copies > 1 ? p.T : 0;
+    g.T = p.T;
+    g.K = p.K;
+    g.S = p.S;
+    g.hq_s = p.hq_s;
+    g.hkv_s = p.hkv_s;
+    g.d = p.d;
+    g.max_kv = p.max_kv;
+    g.ffn_s = p.ffn_s;
+    for (int r = 0; r < p.N; ++r) {
+        g.bias[r] = p.bias[r];
+        g.kcache[r] = p.kcache[r];
+        g.vcache[r] = p.vcache[r];
+    }
+    g.pos = p.pos;
+    g.rope = p.rope;
+    g.q_out = static_cast<bf16*>(p.q_out);
+    g.act = static_cast<bf16*>(p.act);
+    g.status = p.status;
+    static bool set[2] = {false, false};
+    const void* fn = mode == TC_QKV ? reinterpret_cast<const void*>(tc_col_kernel<TC_QKV>)
+                                    : reinterpret_cast<const void*>(tc_col_kernel<TC_GATEUP>);
+    if (!set[mode]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        if (e != cudaSuccess) return e;
+        set[mode] = true;
+    }
+    const int ntiles = mode == TC_QKV ? (p.rows + kTcBN - 1) / kTcBN : (p.ffn_s + 127) / 128;
+    dim3 grid((p.T + kTcBM - 1) / kTcBM, ntiles, p.N);
+    void* args[] = {&g};
+    e = cudaLaunchKernel(fn, grid, dim3(kTcThreads), args, kTcSmem, s);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    TcRowArgs g;
+    memset(&g, 0, sizeof g);
+    cudaError_t e = tensor_map_2d(p.A, p.Kr, (long)p.N * p.T, kTcBK, kTcBM, 1, &g.ta);
+    for (int r = 0; r < p.N && e == cudaSuccess; ++r) e = tensor_map_2d(p.W[r], p.Kr, p.H, kTcBK, kRowBN, 1, &g.tb[r]);
+    if (e != cudaSuccess) return e;
+    g.T = p.T;
+    g.Kr = p.Kr;
+    g.N = p.N;
+    g.H = p.H;
+    g.resid = p.resid;
+    g.out = p.out;
+    g.status = p.status;
+    static bool set = false;
+    if (!set) {
+        e = cudaFuncSetAttribute(tc_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem);
+        if (e != cudaSuccess) return e;
+        set = true;
+    }
+    dim3 grid((p.T + kTcBM - 1) / kTcBM, (p.H + kRowBN - 1) / kRowBN);
+    tc_row_kernel<<<grid, kTcThreads, kRowSmem, s>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s) {
+    FlashArgs f;
+    memset(&f, 0, sizeof f);
+    f.q = static_cast<const bf16*>(p.q);
+    for (int r = 0; r < p.N; ++r) {
+        f.kcache[r] = p.kcache[r];
+        f.vcache[r] = p.vcache[r];
+    }
+    f.out = static_cast<bf16*>(p.out);
+    f.pos = p.pos;
+    f.N = p.N;
+    f.B = p.B;
+    f.S = p.S;
+    f.T = p.T;
+    f.hq_s = p.hq_s;
+    f.hkv_s = p.hkv_s;
+    f.max_kv = p.max_kv;
+    f.scale = p.scale;
+    f.status = p.status;
+    const long grid = (long)p.N * p.B * p.hq_s * ((p.S + kFaQ - 1) / kFaQ);
+    if (grid == 0) return cudaSuccess;
+    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+    static bool set[2] = {false, false};
+    const int which = p.d == 128 ? 1 : 0;
+    const void* fn = which ? reinterpret_cast<const void*>(flash_prefill_kernel<128>)
+                           : reinterpret_cast<const void*>(flash_prefill_kernel<64>);
+    const int smem = which ? FaShape<128>::kSmem : FaShape<64>::kSmem;
+    if (!set[which]) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        set[which] = true;
+    }
+    void* args[] = {&f};
+    cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(128), args, smem, s);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace tpk

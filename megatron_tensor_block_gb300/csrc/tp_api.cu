@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <new>
 
@@ -61,6 +62,8 @@ struct tp_plan_s {
     // MoE buffers (share the data region with the decode buffers)
     size_t off_m_ids = 0, off_m_wts = 0, off_m_off = 0, off_m_perm = 0, off_m_slot = 0, off_m_rinv = 0,
            off_m_xs = 0, off_m_act = 0, off_m_o = 0, ws_moe_end = 0;
+    // prefill buffers (share the data region with the decode and MoE buffers)
+    size_t off_p_xn = 0, off_p_q = 0, off_p_ao = 0, off_p_h = 0, off_p_act = 0, off_p_rope = 0, ws_prefill_end = 0;
     size_t ws_bytes = 0;
     size_t ws_decode_end = 0;           // end of the decode buffers (control words included)
     // measurement hook (tp_profile_stages)
@@ -249,6 +252,17 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_ss_tiles = take((size_t)(H / kTileRows) * kTMax * 4);
         P->ws_decode_end = off;
     }
+    if (dense && d->dtype == TP_BF16) {
+        off = P->ctrl_bytes;
+        const int64_t Tm = d->max_tokens, hd = d->head_dim;
+        P->off_p_xn = take((size_t)N * Tm * H * 2);              // one bf16 copy per distinct gamma
+        P->off_p_q = take((size_t)Tm * d->n_heads * hd * 2);     // [N][T][Hq' d]
+        P->off_p_ao = take((size_t)Tm * d->n_heads * hd * 2);
+        P->off_p_h = take((size_t)Tm * H * 4);
+        P->off_p_act = take((size_t)Tm * d->ffn * 2);            // [N][T][F']
+        P->off_p_rope = take((size_t)d->max_kv * (hd / 2) * 8);  // (cos, sin) per position and pair
+        P->ws_prefill_end = off;
+    }
     if (moe) {
         off = P->ctrl_bytes;
         const int64_t ns = d->max_tokens * d->top_k, Fs = I.expert_ffn_shard;
@@ -268,7 +282,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
     } else {
         I.moe_ids_offset = I.moe_bucket_offset = I.moe_perm_offset = -1;
     }
-    P->ws_bytes = P->ws_decode_end > P->ws_moe_end ? P->ws_decode_end : P->ws_moe_end;
+    P->ws_bytes = std::max(P->ws_decode_end, std::max(P->ws_moe_end, P->ws_prefill_end));
     if (P->ws_bytes < P->ctrl_bytes) P->ws_bytes = P->ctrl_bytes;
     I.workspace_bytes = (int64_t)P->ws_bytes;
     *out = P;
@@ -766,6 +780,137 @@ static tp_status forward_moe(tp_plan_t P, const tp_shard_set* w, const float* x,
     return ok();
 }
 
+// Prefill: B sequences of S new tokens each (T = B*S rows, sequence-major).
+// Stages: RMSNorm -> column-parallel QKV + RoPE + KV append (tensor cores)
+// -> causal attention per shard -> row-parallel o_proj with the rank-ordered
+// reduction and residual -> RMSNorm -> column-parallel gate/up + SwiGLU ->
+// row-parallel down + reduction + residual.
+static tp_status forward_prefill(tp_plan_t P, const tp_shard_set* w, const tp_kv_set* kv, const float* x, float* y,
+                                 const int32_t* pos, int B, int S, char* ws, cudaStream_t s) {
+    const tp_model_desc& d = P->d;
+    const tp_plan_info& I = P->info;
+    const int N = P->N, T = B * S, H = (int)d.hidden, hd = (int)d.head_dim;
+    for (int r = 0; r < N; ++r) {
+        if (!w->wqkv[r] || !w->wo[r] || !w->wgu[r] || !w->wd[r] || !w->gamma_attn[r] || !w->gamma_ffn[r])
+            return fail(TP_ERR_NULL, "tp_block_forward: shard %d weight pointer is NULL", r);
+        if (d.has_qkv_bias && !w->bqkv[r]) return fail(TP_ERR_NULL, "tp_block_forward: shard %d bias is NULL", r);
+        if (!kv->k[r] || !kv->v[r]) return fail(TP_ERR_NULL, "tp_block_forward: shard %d KV cache is NULL", r);
+        const void* al[] = {w->wqkv[r], w->wo[r], w->wgu[r], w->wd[r], w->gamma_attn[r], w->gamma_ffn[r],
+                            kv->k[r], kv->v[r]};
+        for (const void* p : al)
+            if (!aligned16(p)) return fail(TP_ERR_ALIGN, "tp_block_forward: shard %d pointer not 16-byte aligned", r);
+    }
+    int* status = reinterpret_cast<int*>(ws + P->off_status);
+    void* xn = ws + P->off_p_xn;
+    void* q = ws + P->off_p_q;
+    void* ao = ws + P->off_p_ao;
+    float* h = reinterpret_cast<float*>(ws + P->off_p_h);
+    void* act = ws + P->off_p_act;
+    float2* rope = reinterpret_cast<float2*>(ws + P->off_p_rope);
+    // the gamma of a replicated norm is one tensor: shards that point at the
+    // same gamma share one normalised copy
+    auto distinct = [&](const float* const* g) {
+        for (int r = 1; r < N; ++r)
+            if (g[r] != g[0]) return N;
+        return 1;
+    };
+    const int na = distinct(w->gamma_attn), nf = distinct(w->gamma_ffn);
+    cudaError_t e;
+    const double log2_theta = std::log2(d.rope_theta);
+    stage_mark(P, 0, s);
+    e = launch_rope_table(rope, (int)d.max_kv, hd, log2_theta, s);
+    if (e == cudaSuccess) e = launch_prefill_norm(x, w->gamma_attn, na, xn, T, H, (float)d.eps, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill norm launch");
+
+    PrefillColParams c{};
+    c.A = xn;
+    c.a_copies = na;
+    c.N = N;
+    c.T = T;
+    c.K = H;
+    c.rows = (int)I.qkv_rows;
+    c.S = S;
+    c.hq_s = (int)I.hq_shard;
+    c.hkv_s = (int)I.hkv_shard;
+    c.d = hd;
+    c.max_kv = (int)d.max_kv;
+    c.ffn_s = (int)I.ffn_shard;
+    for (int r = 0; r < N; ++r) {
+        c.W[r] = w->wqkv[r];
+        c.bias[r] = d.has_qkv_bias ? w->bqkv[r] : nullptr;
+        c.kcache[r] = kv->k[r];
+        c.vcache[r] = kv->v[r];
+    }
+    c.pos = pos;
+    c.rope = rope;
+    c.q_out = q;
+    c.act = act;
+    c.status = status;
+    e = launch_tc_col(0, c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill QKV launch");
+    stage_mark(P, 1, s);
+
+    FlashParams f{};
+    f.q = q;
+    for (int r = 0; r < N; ++r) {
+        f.kcache[r] = kv->k[r];
+        f.vcache[r] = kv->v[r];
+    }
+    f.out = ao;
+    f.pos = pos;
+    f.N = N;
+    f.B = B;
+    f.S = S;
+    f.T = T;
+    f.hq_s = (int)I.hq_shard;
+    f.hkv_s = (int)I.hkv_shard;
+    f.max_kv = (int)d.max_kv;
+    f.d = hd;
+    f.scale = (float)(1.0 / std::sqrt((double)hd));
+    f.status = status;
+    e = launch_flash_prefill(f, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill attention launch");
+    stage_mark(P, 2, s);
+
+    PrefillRowParams o{};
+    o.A = ao;
+    o.N = N;
+    o.T = T;
+    o.Kr = (int)(I.hq_shard * hd);
+    o.H = H;
+    for (int r = 0; r < N; ++r) o.W[r] = w->wo[r];
+    o.resid = x;
+    o.out = h;
+    o.status = status;
+    e = launch_tc_row(o, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill o_proj launch");
+    stage_mark(P, 3, s);
+
+    e = launch_prefill_norm(h, w->gamma_ffn, nf, xn, T, H, (float)d.eps, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill norm launch");
+    c.a_copies = nf;
+    c.rows = (int)(2 * I.ffn_shard);
+    for (int r = 0; r < N; ++r) c.W[r] = w->wgu[r];
+    e = launch_tc_col(1, c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill gate/up launch");
+    stage_mark(P, 4, s);
+
+    PrefillRowParams dn{};
+    dn.A = act;
+    dn.N = N;
+    dn.T = T;
+    dn.Kr = (int)I.ffn_shard;
+    dn.H = H;
+    for (int r = 0; r < N; ++r) dn.W[r] = w->wd[r];
+    dn.resid = h;
+    dn.out = y;
+    dn.status = status;
+    e = launch_tc_row(dn, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: prefill down launch");
+    stage_mark(P, 5, s);
+    return ok();
+}
+
 extern "C" tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
                                       const float* x, float* y, const int32_t* pos, int32_t B,
                                       int32_t T_per_seq, int32_t mode, const float* router_logits,
@@ -800,8 +945,16 @@ extern "C" tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, con
             return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: MOE_FFN needs hidden and expert_ffn/tp multiples of 256");
         return forward_moe(plan, w, x, y, router_logits, B * T_per_seq, ws, s);
     }
-    if (mode == TP_MODE_PREFILL)
-        return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: mode %d not available in this build", mode);
+    if (mode == TP_MODE_PREFILL) {
+        if (!plan->dense) return fail(TP_ERR_INVALID_ARG, "tp_block_forward: PREFILL needs an attention block");
+        if (!kv || !pos) return fail(TP_ERR_NULL, "tp_block_forward: PREFILL needs kv and pos");
+        if (plan->d.dtype != TP_BF16)
+            return fail(TP_ERR_UNSUPPORTED, "tp_block_forward: PREFILL runs on bf16 weights (fp32 plans: DECODE)");
+        if ((int64_t)T_per_seq > plan->d.max_kv)
+            return fail(TP_ERR_CAPACITY, "tp_block_forward: T_per_seq=%d exceeds max_kv=%lld", T_per_seq,
+                        (long long)plan->d.max_kv);
+        return forward_prefill(plan, w, kv, x, y, pos, B, T_per_seq, ws, s);
+    }
     return fail(TP_ERR_INVALID_ARG, "tp_block_forward: unknown mode %d", mode);
 }
 

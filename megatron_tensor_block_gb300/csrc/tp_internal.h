@@ -152,6 +152,48 @@ cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner
 cudaError_t launch_tc_gemm_plain(const void* A, const void* B, float* C, int M, int N, int K, int* status,
                                  cudaStream_t s);
 
+// Prefill (tcgen05) projections and attention.
+struct PrefillColParams {
+    const void* A;                        // normalised activations [a_copies][T, K] bf16
+    int a_copies;                         // 1: every shard reads copy 0; N: shard r reads copy r
+    const void* W[TP_MAX_SHARDS];         // QKV: [qkv_rows, K]; gate/up: [2F', K]
+    int N, T, K, rows, S;
+    int hq_s, hkv_s, d, max_kv, ffn_s;
+    const float* bias[TP_MAX_SHARDS];
+    const int* pos;
+    const float2* rope;
+    void* q_out;                          // [N][T][hq_s d] bf16
+    void* kcache[TP_MAX_SHARDS];
+    void* vcache[TP_MAX_SHARDS];
+    void* act;                            // [N][T][F'] bf16
+    int* status;
+};
+struct PrefillRowParams {
+    const void* A;                        // [N][T][Kr] bf16 (shard activations stacked)
+    const void* W[TP_MAX_SHARDS];         // [H, Kr] bf16
+    int N, T, Kr, H;
+    const float* resid;
+    float* out;
+    int* status;
+};
+struct FlashParams {
+    const void* q;
+    void* kcache[TP_MAX_SHARDS];
+    void* vcache[TP_MAX_SHARDS];
+    void* out;
+    const int* pos;
+    int N, B, S, T, hq_s, hkv_s, max_kv, d;   // d: head_dim, 64 or 128
+    float scale;
+    int* status;
+};
+// bf16 RMSNorm of x [T, H]: n_copies outputs (one per gamma), copy c at out + c*T*H
+cudaError_t launch_prefill_norm(const float* x, const float* const* gammas, int n_copies, void* out, int T, int H,
+                                float eps, cudaStream_t s);
+cudaError_t launch_rope_table(float2* tab, int max_pos, int d, double log2_theta, cudaStream_t s);
+cudaError_t launch_tc_col(int mode, const PrefillColParams& p, cudaStream_t s);   // 0: QKV, 1: gate/up
+cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s);
+cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s);
+
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)

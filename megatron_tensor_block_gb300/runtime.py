@@ -114,7 +114,12 @@ class KVCache:
 class Model:
     """A stack of tensor-parallel blocks of one workload on one device."""
 
-    def __init__(self, inputs: dict, device="cuda", max_kv: int | None = None, keep_full: bool = False):
+    def __init__(self, inputs: dict, device="cuda", max_kv: int | None = None, keep_full: bool = False,
+                 share_norm: bool = False):
+        """``share_norm``: point every shard at shard 0's copy of each
+        replicated norm gamma (the copies hold the same values), so that the
+        prefill path forms one normalised copy of the activations instead of
+        one per shard."""
         torch = _torch()
         w = inputs["workload"]
         self.w = w
@@ -134,6 +139,11 @@ class Model:
                 self.caches.append(KVCache(w, inputs["k_cache"][i], inputs["v_cache"][i], self.max_kv,
                                            self.max_batch, device))
             self.pos = torch.from_numpy(inputs["pos"]).to(device)
+        if share_norm:
+            for l in self.layers:
+                for k in ("gamma_attn", "gamma_ffn"):
+                    if l.shards.get(k):
+                        l.shards[k] = [l.shards[k][0]] * len(l.shards[k])
         if not keep_full:
             for l in self.layers:
                 l.drop_full()

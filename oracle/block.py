@@ -358,6 +358,50 @@ def block_tpN(shards, x, k_caches, v_caches, pos, S, cfg, N):
     return ffn_half_tpN(shards, h, cfg, N)
 
 
+def block_rows_tpN(shards, x, k_caches, v_caches, pos, S, cfg, N, rows):
+    """Selected rows of ``block_tpN``'s output, computing only what they
+    depend on, for checks at sizes where the whole block is too slow here.
+
+    Row ``t`` belongs to sequence ``b = t // S`` at position
+    ``pos[b] + t % S``; causal attention makes it depend on the cached prefix
+    of that sequence and on the keys and values of the sequence's new tokens
+    up to ``t`` only. Per shard the operations are those of ``attn_half_tpN``
+    (norm, projection, bias, rotation, attention, o_proj partial) restricted
+    to those tokens, followed by the rank-ordered reduce, the residual and
+    ``ffn_half_tpN`` on the selected rows. The caches passed in are not
+    modified. Returns ``(y_rows [len(rows), H], rows)`` with rows sorted.
+    """
+    rows = np.array(sorted(set(int(t) for t in rows)), dtype=np.int64)
+    Hq_s, Hkv_s, d = cfg.n_heads // N, cfg.n_kv_heads // N, cfg.head_dim
+    P = _positions(pos, S)
+    h_rows = np.empty((rows.size, x.shape[1]))
+    for b in sorted(set((rows // S).tolist())):
+        sel = np.nonzero(rows // S == b)[0]
+        local = rows[sel] - b * S                       # token indices within the sequence
+        upto = int(local.max()) + 1
+        toks = slice(b * S, b * S + upto)
+        Pb = P[b, :upto]
+        partials = []
+        for r in range(N):
+            Sr = shards[r]
+            n = rmsnorm(x[toks], Sr["gamma_attn"], cfg.eps)
+            qkv = n @ Sr["wqkv"].T
+            if Sr["bqkv"] is not None:
+                qkv = qkv + Sr["bqkv"]
+            q = rope(qkv[local, :Hq_s * d].reshape(local.size, Hq_s, d), Pb[local], cfg.rope_theta)
+            k = rope(qkv[:, Hq_s * d:(Hq_s + Hkv_s) * d].reshape(upto, Hkv_s, d), Pb, cfg.rope_theta)
+            v = qkv[:, (Hq_s + Hkv_s) * d:].reshape(upto, Hkv_s, d)
+            kc = k_caches[r][b].copy()
+            vc = v_caches[r][b].copy()
+            kc[:, Pb, :] = k.transpose(1, 0, 2)
+            vc[:, Pb, :] = v.transpose(1, 0, 2)
+            Lk = int(Pb[-1]) + 1
+            o = attention(q, kc[:, :Lk].transpose(1, 0, 2), vc[:, :Lk].transpose(1, 0, 2), Pb[local])
+            partials.append(o.reshape(local.size, Hq_s * d) @ Sr["wo"].T)
+        h_rows[sel] = x[rows[sel]] + reduce_rank_order(partials)
+    return ffn_half_tpN(shards, h_rows, cfg, N), rows
+
+
 # ---------------------------------------------------------------------------
 # MoE feed-forward block with expert slicing ("Multi-GPU & Multi-Node",
 # Supported architectures: each shard holds 1/tp of every expert, the router

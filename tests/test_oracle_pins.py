@@ -319,6 +319,31 @@ def test_block_tpN_equals_tp1(N, S):
     assert np.allclose(np.concatenate(vs, axis=1), v1, atol=1e-12)
 
 
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_block_rows_tpN_matches_torch_assembly_on_selected_rows(N):
+    # The row-sampled form used for checks at full size: the rows it returns
+    # must be the torch library block's rows (causal prefill with a cached
+    # prefix, rows from both sequences, first and last tokens included), and
+    # the caches it is given must stay untouched.
+    cfg = TINY
+    S, B = 6, 2
+    L = _tiny_inputs(cfg, 80 + N, True)
+    Lmax = cfg.kv_len + S
+    kc = rng(81).standard_normal((B, cfg.n_kv_heads, Lmax, cfg.head_dim))
+    vc = rng(82).standard_normal((B, cfg.n_kv_heads, Lmax, cfg.head_dim))
+    pos = np.array([cfg.kv_len, 2], dtype=np.int32)
+    x = rng(83).standard_normal((B * S, cfg.hidden))
+    want, _, _ = _torch_block(L, x, kc, vc, pos, S, cfg)
+    shards = O.shard_layer(L, cfg, N)
+    ks, vs = O.shard_kv_cache(kc, N), O.shard_kv_cache(vc, N)
+    ks0, vs0 = [k.copy() for k in ks], [v.copy() for v in vs]
+    rows = [11, 0, 3, 6, 7, 5, 3]
+    got, order = O.block_rows_tpN(shards, x, ks, vs, pos, S, cfg, N, rows)
+    assert order.tolist() == sorted(set(rows))
+    assert np.allclose(got, want[order], rtol=1e-12, atol=1e-12)
+    assert all(np.array_equal(a, b) for a, b in zip(ks + vs, ks0 + vs0))
+
+
 def test_block_tpN_detects_a_wrong_shard_index():
     # A plausible mistake -- a shard using its neighbour's o_proj slice -- must
     # change the answer (the invariant above would catch it).
