@@ -1,17 +1,23 @@
-"""Benchmark of the tensor-parallel block decode step on GB300.
+"""Benchmark of the tensor-parallel block on GB300.
 
-Workload (default): Llama-3-8B-shaped block, bf16 weights, 4 logical
+Workload (default): Llama-3-8B-shaped block decode, bf16 weights, 4 logical
 tensor-parallel shards, batch 8, KV length 2048 -- one step is one pass of the
 whole block (fused RMSNorm + column-parallel QKV + RoPE + KV append,
 split-KV GQA attention, row-parallel o_proj with rank-ordered reduction,
 RMSNorm + column-parallel gate/up + SwiGLU, row-parallel down_proj with
 rank-ordered reduction) for the 8 new tokens.
 
-`python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]`
-prints one JSON line (rank 0). Under torchrun every rank runs an independent
-replica on its own GPU (the path has no cross-GPU exchange); the timed region
-is bracketed by a barrier and device synchronisation and the slowest rank's
-time is reported. `--impl reference` times the CPU oracle on the host.
+Other workloads (`--workload`): the Llama-3-8B-shaped tp=8 prefill of 4 x
+2048 tokens (tensor-core bound: reported in TFLOP/s against the bf16 peak),
+the 24-layer Qwen2.5-0.5B-shaped decode, and the expert-sliced MoE
+feed-forward block (256 tokens, 64 experts, top-4).
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+[--workload NAME]` prints one JSON line (rank 0). Under torchrun every rank
+runs an independent replica on its own GPU (the path has no cross-GPU
+exchange); the timed region is bracketed by a barrier and device
+synchronisation and the slowest rank's time is reported. `--impl reference`
+times the CPU oracle on the host.
 """
 from __future__ import annotations
 
@@ -35,9 +41,25 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "TP-block decode tokens/s + HBM GB/s (% of ~8 TB/s peak) on 1 GB300"
+METRICS = {
+    "decode": METRIC,
+    "prefill": "TP-block prefill tokens/s + bf16 tensor TFLOP/s (% of dense peak) on 1 GB300",
+    "moe": "MoE expert-sliced FFN tokens/s + HBM GB/s on 1 GB300",
+}
 DEFAULT_WORKLOAD = "llama3_8b_decode_tp4"
-STAGES = ["qkv_rope", "attention", "o_proj_reduce", "gate_up_swiglu", "down_reduce"]
-DOMINANT = "gate_up_swiglu"
+WORKLOAD_KIND = {"llama3_8b_decode_tp4": "decode", "qwen25_05b_decode_tp2": "decode",
+                 "llama3_8b_prefill_tp8": "prefill", "moe_expert_slice_tp4": "moe"}
+STAGES = {
+    "decode": ["qkv_rope", "attention", "o_proj_reduce", "gate_up_swiglu", "down_reduce"],
+    "prefill": ["qkv_rope", "attention", "o_proj_reduce", "gate_up_swiglu", "down_reduce"],
+    "moe": ["route_bucket", "expert_gate_up", "expert_down", "combine"],
+}
+DOMINANT = {"decode": "gate_up_swiglu", "prefill": "gate_up_swiglu", "moe": "expert_gate_up"}
+# the committed ncu summary of each dominant kernel and the source it was taken on
+PROFILE = {"decode": ("gemv_swiglu_llama3_8b_decode.md", "kernels_decode.cu"),
+           "prefill": ("tc_gateup_llama3_8b_prefill.md", "kernels_prefill.cu"),
+           "moe": ("moe_gemm_expert_slice.md", "kernels_moe.cu")}
+LAUNCHES_PER_LAYER = {"decode": 9, "prefill": 8, "moe": 6}
 L2_BYTES = 129e6
 
 
@@ -58,26 +80,57 @@ def stage_bytes(w) -> dict:
 
 
 def step_bytes(w) -> int:
-    """Bytes the method must move per step: weights + KV read once."""
+    """Bytes the method must move per decode step: weights + KV read once."""
     es = 2 if w.dtype == "bf16" else 4
     H, Hq, Hkv, d, F = w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.ffn
     weights = (H * (Hq + 2 * Hkv) * d + H * Hq * d + 3 * H * F) * es
     kv = 2 * w.batch * Hkv * (w.kv_len + 1) * d * es
-    return weights + kv
+    return weights * w.n_layers + kv * w.n_layers
+
+
+def prefill_flops(w) -> dict:
+    """Algorithmic FLOPs per launch of each prefill stage (2 per multiply-add;
+    causal attention counts each query's visible keys only)."""
+    H, Hq, Hkv, d, F, T, S = w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.ffn, w.tokens, w.tokens_per_seq
+    L = w.kv_len
+    keys = w.batch * (S * L + S * (S + 1) // 2)          # sum over queries of visible keys
+    return {
+        "qkv_rope": 2 * T * H * (Hq + 2 * Hkv) * d,
+        "attention": 4 * d * Hq * keys,
+        "o_proj_reduce": 2 * T * Hq * d * H,
+        "gate_up_swiglu": 2 * T * H * 2 * F,
+        "down_reduce": 2 * T * F * H,
+    }
+
+
+def moe_bytes(inputs) -> dict:
+    """Algorithmic HBM bytes of the expert GEMMs: the weights of every expert
+    that receives at least one token, read once, plus the routed activations
+    (top-k of the logits; ties to the lower expert id, as the router does)."""
+    w = inputs["workload"]
+    lg = np.asarray(inputs["router_logits"])
+    ids = np.argsort(-lg, axis=1, kind="stable")[:, :w.top_k]
+    hit = np.unique(ids).size
+    es, H, Fe, ns = 2, w.hidden, w.expert_ffn, w.tokens * w.top_k
+    return {"expert_gate_up": hit * 2 * Fe * H * es + w.tp * ns * H * es + ns * Fe * es,
+            "expert_down": hit * H * Fe * es + ns * Fe * es + w.tp * ns * H * 4,
+            "experts_hit": hit}
 
 
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         j = json.load(open(p))
-        return float(j["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return {"hbm": float(j["hbm_gbs"]), "tensor_burst": float(j["bf16_tflops"]),
+                "tensor_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "kind": "measured"}
+    return {"hbm": 6800.0, "tensor_burst": 1900.0, "tensor_sustained": 1700.0, "kind": "fallback"}
 
 
-def kernel_traffic(name: str):
+def kernel_traffic(kind: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    f = os.path.join(ROOT, "profiles", f"{name}_llama3_8b_decode.md")
+    name, src_name = PROFILE[kind]
+    f = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(f):
         return None
     txt = open(f).read()
@@ -85,7 +138,7 @@ def kernel_traffic(name: str):
     m2 = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
     if not (m1 and m2):
         return None
-    src = os.path.join(ROOT, "megatron_tensor_block_gb300", "csrc", "kernels_decode.cu")
+    src = os.path.join(ROOT, "megatron_tensor_block_gb300", "csrc", src_name)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     return float(m1.group(1)) if sha.startswith(m2.group(1)) else None
 
@@ -162,73 +215,122 @@ def max_over_ranks(v: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 
 
-def oracle_setup(inputs):
-    """Untimed setup of the oracle: float64 shards and caches."""
-    import oracle as O
-    w = inputs["workload"]
-    L = inputs["layers"][0]
-    shards = O.shard_layer(O.layer_f64(L), w, w.tp)
-    kc = np.zeros((w.batch, w.n_kv_heads, w.max_kv, w.head_dim))
-    vc = np.zeros_like(kc)
-    kc[:, :, :w.kv_len] = O.to_f64(inputs["k_cache"][0])
-    vc[:, :, :w.kv_len] = O.to_f64(inputs["v_cache"][0])
-    return shards, O.shard_kv_cache(kc, w.tp), O.shard_kv_cache(vc, w.tp)
+class OracleLeg:
+    """The CPU oracle on a bounded sample of a workload. Setup (float64
+    shards and caches) is untimed; `step()` processes one sample unit and
+    returns the tokens it covered."""
 
+    def __init__(self, inputs):
+        import oracle as O
+        self.O = O
+        self.inputs = inputs
+        w = self.w = inputs["workload"]
+        self.kind = WORKLOAD_KIND.get(w.name, "decode")
+        self.i = 0
+        if self.kind == "moe":
+            eg, eu, ed = (O.to_f64(inputs[k]) for k in ("e_gate", "e_up", "e_down"))
+            self.shards = O.shard_experts(eg, eu, ed, w.tp)
+            self.gammas = [O.to_f64(inputs["gamma_ffn"])] * w.tp
+            self.x = np.asarray(inputs["x"], dtype=np.float64)
+            self.chunk = 16
+            return
+        self.layers = [O.shard_layer(O.layer_f64(L), w, w.tp) for L in inputs["layers"]]
+        kc = np.zeros((w.batch, w.n_kv_heads, w.max_kv, w.head_dim))
+        vc = np.zeros_like(kc)
+        self.caches = []
+        for li in range(len(inputs["layers"])):
+            k, v = kc.copy(), vc.copy()
+            k[:, :, :w.kv_len] = O.to_f64(inputs["k_cache"][li])
+            v[:, :, :w.kv_len] = O.to_f64(inputs["v_cache"][li])
+            self.caches.append((O.shard_kv_cache(k, w.tp), O.shard_kv_cache(v, w.tp)))
+        self.x = np.asarray(inputs["x"], dtype=np.float64)
+        self.chunk = 64 if self.kind == "prefill" else 1
 
-def oracle_step(inputs, setup, b: int):
-    """One decode token of sequence b through the oracle's sharded block."""
-    import oracle as O
-    w = inputs["workload"]
-    shards, ks, vs = setup
-    x = np.asarray(inputs["x"][b:b + 1], dtype=np.float64)
-    pos = inputs["pos"][b:b + 1]
-    kb = [k[b:b + 1] for k in ks]
-    vb = [v[b:b + 1] for v in vs]
-    return O.block_tpN(shards, x, kb, vb, pos, 1, w, w.tp)
+    def describe(self) -> str:
+        if self.kind == "moe":
+            return (f"{self.chunk}-token slices of the {self.w.tokens} routed tokens through the float64 numpy "
+                    f"oracle's expert-sliced MoE block (tp={self.w.tp})")
+        if self.kind == "prefill":
+            return (f"the first {self.chunk} prompt tokens (positions 0..{self.chunk - 1}) of one sequence through "
+                    f"the float64 numpy oracle's sharded block (tp={self.w.tp}), repeated; the full workload is "
+                    f"{self.w.batch} x {self.w.tokens_per_seq} tokens with longer causal spans")
+        return (f"single-token decode steps (one sequence each, round-robin over the batch of {self.w.batch}) "
+                f"through the float64 numpy oracle's sharded block ({self.w.n_layers} layer(s))")
+
+    def step(self) -> int:
+        O, w = self.O, self.w
+        if self.kind == "moe":
+            t0 = (self.i * self.chunk) % w.tokens
+            self.i += 1
+            sl = slice(t0, t0 + self.chunk)
+            O.moe_ffn_tpN(self.shards, self.gammas, self.x[sl], self.inputs["router_logits"][sl], w.eps, w.top_k,
+                          w.tp)
+            return self.chunk
+        if self.kind == "prefill":
+            x = self.x[:self.chunk]
+            pos = np.zeros(1, dtype=np.int32)
+            for shards, (ks, vs) in zip(self.layers, self.caches):
+                x = O.block_tpN(shards, x, [k[:1] for k in ks], [v[:1] for v in vs], pos, self.chunk, w, w.tp)
+            return self.chunk
+        b = self.i % w.batch
+        self.i += 1
+        x = self.x[b:b + 1]
+        pos = self.inputs["pos"][b:b + 1]
+        for shards, (ks, vs) in zip(self.layers, self.caches):
+            x = O.block_tpN(shards, x, [k[b:b + 1] for k in ks], [v[b:b + 1] for v in vs], pos, 1, w, w.tp)
+        return 1
 
 
 def cpu_baseline(inputs, budget_s: float = 20.0) -> dict:
-    setup = oracle_setup(inputs)
-    oracle_step(inputs, setup, 0)                        # warm
-    n, t0 = 0, time.perf_counter()
+    leg = OracleLeg(inputs)
+    leg.step()                                           # warm
+    n, tok, t0 = 0, 0, time.perf_counter()
     while True:
-        oracle_step(inputs, setup, n % inputs["workload"].batch)
+        tok += leg.step()
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s or n >= 4096:
             break
-    return {"value": n / el, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
-            "sample": f"{n} single-token decode steps (one sequence each, round-robin over the batch) of the "
-                      f"float64 numpy oracle's sharded block, weights pre-sharded to float64 outside the timing"}
+    return {"value": tok / el, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+            "sample": f"{n} x " + leg.describe() + "; weights pre-sharded to float64 outside the timing"}
+
+
+def config_of(w) -> dict:
+    kind = WORKLOAD_KIND[w.name]
+    c = {"workload": w.name, "tp_logical_shards": w.tp, "hidden": w.hidden}
+    if kind == "moe":
+        c.update(tokens=w.tokens, experts=w.n_experts, top_k=w.top_k, expert_ffn=w.expert_ffn)
+    else:
+        c.update(batch=w.batch, tokens_per_seq=w.tokens_per_seq, kv_len=w.kv_len, layers=w.n_layers,
+                 heads=[w.n_heads, w.n_kv_heads], head_dim=w.head_dim, ffn=w.ffn)
+    return c
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
+    kind = WORKLOAD_KIND[w.name]
     inputs = synth.make_inputs(w, with_head=False)
-    setup = oracle_setup(inputs)
-    for i in range(args.warmup):
-        oracle_step(inputs, setup, i % w.batch)
+    leg = OracleLeg(inputs)
+    for _ in range(args.warmup):
+        leg.step()
     budget = 120.0
     t0 = time.perf_counter()
-    n = 0
-    for i in range(args.steps):
-        oracle_step(inputs, setup, i % w.batch)
+    n, tok = 0, 0
+    for _ in range(args.steps):
+        tok += leg.step()
         n += 1
         if time.perf_counter() - t0 > budget:
             break
     el = time.perf_counter() - t0
-    value = n / el
+    value = tok / el
     cores = int(os.environ["OMP_NUM_THREADS"])
-    sample = (f"each step is one decode token of one sequence (round-robin over the batch of {w.batch}) through the "
-              f"float64 numpy oracle's sharded block; {n} of {args.steps} requested steps fit the {budget:.0f} s bound")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    sample = (f"each step is {leg.describe()}; {n} of {args.steps} requested steps fit the {budget:.0f} s bound")
+    line = {"impl": "reference", "metric": METRICS[kind], "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": n, "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(n, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tp_logical_shards": w.tp, "batch": w.batch, "kv_len": w.kv_len,
-                       "hidden": w.hidden, "heads": [w.n_heads, w.n_kv_heads], "head_dim": w.head_dim,
-                       "ffn": w.ffn},
+            "config": config_of(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -246,19 +348,23 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     w = synth.WORKLOADS[args.workload]
+    kind = WORKLOAD_KIND[w.name]
+    stages = STAGES[kind]
     inputs = synth.make_inputs(w, with_head=False)
-    model = Model(inputs)
+    # replicated norm gammas: one tensor shared by the shards (prefill forms
+    # one normalised copy; decode reads it per shard either way)
+    model = Model(inputs, share_norm=(kind == "prefill"))
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
     # ---- device-resident timing: one step = one forward, replayed from a CUDA graph
     with torch.cuda.stream(stream):
         for _ in range(3):
-            model.forward()
+            model.forward(stream=stream)
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        model.forward()
+        model.forward(stream=stream)
     for _ in range(max(args.warmup, 3)):
         graph.replay()
     torch.cuda.synchronize()
@@ -285,9 +391,9 @@ def run_ours(args, world, rank, local):
     tokens_step = w.tokens
     value = tokens_step * args.steps * world / (t_ms / 1e3)
 
-    # ---- per-kernel durations: stage events around each launch over K' steps
-    n_prof = min(args.steps, 2000)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(n_prof)]
+    # ---- per-kernel durations: stage events around each launch, on the launching stream
+    n_prof = max(1, min(args.steps, 2000 if kind != "prefill" else 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(n_prof)]
     for row in evs:          # torch creates events lazily: record once so the raw handles exist
         for e in row:
             e.record(stream)
@@ -299,60 +405,103 @@ def run_ours(args, world, rank, local):
         tb.tp_profile_stages(model.plan, None)
     torch.cuda.synchronize()
     stage_ms = {}
-    for j, name in enumerate(STAGES):
+    for j, name in enumerate(stages):
         ts = [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_prof)]
         stage_ms[name] = statistics.mean(ts)
-    sb = stage_bytes(w)
-    peak, peak_kind = peaks()
-    dom_ms = stage_ms[DOMINANT]
-    achieved = sb[DOMINANT] / (dom_ms / 1e3) / 1e9
-    step_gbs = step_bytes(w) / (ms_step / 1e3) / 1e9
+    pk = peaks()
+    dom = DOMINANT[kind]
+    dom_ms = stage_ms[dom]
+    extra = {}
+    if kind == "prefill":
+        fl = prefill_flops(w)
+        achieved = fl[dom] / (dom_ms / 1e3) / 1e12
+        peak = pk["tensor_sustained"]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": pk["kind"] + " bf16 dense, sustained (kernel timed inside "
+                "a long loop of steps)", "algorithmic_flops": fl[dom], "traffic": kernel_traffic(kind)}
+        step_tf = sum(fl.values()) / (ms_step / 1e3) / 1e12
+        extra["tensor"] = {"step_flops": sum(fl.values()), "step_tflops": step_tf, "frac_of_peak": step_tf / peak,
+                           "peak_tflops": peak, "stage_tflops": {k: fl[k] / (stage_ms[k] / 1e3) / 1e12
+                                                                 for k in stages}}
+        l2_note = f"inputs larger than L2 ({w.tokens * w.hidden * 4 / 1e6:.0f} MB activations, weights " \
+                  f"{(sum(fl.values()) - fl['attention']) / (2 * w.tokens) * 2 / 1e6:.0f} MB per step vs 129 MB L2)"
+    elif kind == "moe":
+        mb = moe_bytes(inputs)
+        achieved = mb[dom] / (dom_ms / 1e3) / 1e9
+        peak = pk["hbm"]
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": pk["kind"], "algorithmic_bytes": mb[dom],
+                "traffic": kernel_traffic(kind)}
+        sb = mb["expert_gate_up"] + mb["expert_down"]
+        step_gbs = sb / (ms_step / 1e3) / 1e9
+        extra["hbm"] = {"step_bytes": sb, "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak, "peak_gbs": peak,
+                        "experts_hit": mb["experts_hit"]}
+        l2_note = f"inputs larger than L2 ({sb / 1e6:.0f} MB of expert weights read per step vs 129 MB L2)"
+    else:
+        sb = stage_bytes(w)
+        achieved = sb[dom] / (dom_ms / 1e3) / 1e9
+        peak = pk["hbm"]
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": pk["kind"], "algorithmic_bytes": sb[dom],
+                "traffic": kernel_traffic(kind)}
+        if w.n_layers > 1:
+            roof["note"] = "stage times of the last layer of each step"
+        step_gbs = step_bytes(w) / (ms_step / 1e3) / 1e9
+        extra["hbm"] = {"step_bytes": step_bytes(w), "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak,
+                        "frac_of_8000": step_gbs / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
+        l2_note = f"inputs larger than L2 ({step_bytes(w) / 1e6:.1f} MB read per step vs 129 MB L2)"
 
-    # ---- end to end through the public API: pinned host x -> device, forward, y -> pinned host
+    # ---- end to end through the public API: pinned host inputs -> device, forward, y -> pinned host
     x_host = torch.from_numpy(np.ascontiguousarray(inputs["x"])).pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
-    pos_host = torch.from_numpy(inputs["pos"]).pin_memory()
+    extra_in = []
+    if kind == "moe":
+        extra_in.append((model.router_logits,
+                         torch.from_numpy(np.ascontiguousarray(inputs["router_logits"])).pin_memory()))
+    else:
+        extra_in.append((model.pos, torch.from_numpy(inputs["pos"]).pin_memory()))
+
+    def e2e_step():
+        model.x.copy_(x_host, non_blocking=True)
+        for dev, host in extra_in:
+            dev.copy_(host, non_blocking=True)
+        model.forward(stream=stream)
+        y_host.copy_(model.y, non_blocking=True)
+
     with torch.cuda.stream(stream):
         for _ in range(3):
-            model.x.copy_(x_host, non_blocking=True)
-            model.pos.copy_(pos_host, non_blocking=True)
-            model.forward(stream=stream)
-            y_host.copy_(model.y, non_blocking=True)
+            e2e_step()
     stream.synchronize()
     barrier(world)
+    e2e_steps = args.steps if kind != "prefill" else max(1, min(args.steps, 100))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps):
-            model.x.copy_(x_host, non_blocking=True)
-            model.pos.copy_(pos_host, non_blocking=True)
-            model.forward(stream=stream)
-            y_host.copy_(model.y, non_blocking=True)
+        for _ in range(e2e_steps):
+            e2e_step()
         e1.record(stream)
     e1.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = tokens_step * args.steps * world / (e2e_ms / 1e3)
+    e2e_value = tokens_step * e2e_steps * world / (e2e_ms / 1e3)
     assert model.ws.status() == 0
 
+    config = config_of(w)
+    config.update({"parallelism": f"{w.tp} logical TP shards per GPU; replicas across GPUs", "l2": l2_note,
+                   "launch": "CUDA graph of one forward, replayed per step"})
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRICS[kind], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "tp_logical_shards": w.tp, "batch": w.batch, "kv_len": w.kv_len,
-                   "hidden": w.hidden, "heads": [w.n_heads, w.n_kv_heads], "head_dim": w.head_dim, "ffn": w.ffn,
-                   "parallelism": f"{w.tp} logical TP shards per GPU; replicas across GPUs",
-                   "l2": f"inputs larger than L2 ({step_bytes(w) / 1e6:.1f} MB read per step vs 129 MB L2)",
-                   "launch": "CUDA graph of one forward, replayed per step"},
-        "hbm": {"step_bytes": step_bytes(w), "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak,
-                "frac_of_8000": step_gbs / 8000.0, "peak_gbs": peak, "peak_kind": peak_kind},
+        "config": config,
+        **extra,
         "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},
-        "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "algorithmic_bytes": sb[DOMINANT],
-                     "traffic": kernel_traffic("gemv_swiglu")},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x_host.numel() * 4 + pos_host.numel() * 4,
-                "d2h_bytes_per_step": y_host.numel() * 4, "path": "tp_block_forward via the ctypes binding"},
-        "gpu_launches": (9 if w.dtype == "bf16" else 5) * args.steps,
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * 4 + sum(h.numel() * h.element_size() for _, h in extra_in),
+                "d2h_bytes_per_step": y_host.numel() * 4, "steps": e2e_steps,
+                "path": "tp_block_forward via the ctypes binding"},
+        "gpu_launches": (LAUNCHES_PER_LAYER[kind] if w.dtype == "bf16" else 5) * max(w.n_layers, 1) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -367,7 +516,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=["llama3_8b_decode_tp4"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_KIND))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_setup()

@@ -344,9 +344,13 @@ tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);
 /* Measurement hook: while set, tp_block_forward records events[i]
  * (cudaEvent_t values passed as void*, created by the caller) on its stream
  * before launching stage i and events[n_events-1] after the last stage, so
- * a caller can time each kernel. Decode has 5 stages (qkv+rope, attention,
- * o_proj+reduce, gate_up+swiglu, down+reduce): pass 6 events. n_events = 0
- * or events = NULL clears the hook. The array is copied. */
+ * a caller can time each kernel. DECODE and PREFILL have 5 stages
+ * (norm+qkv+rope+KV append, attention, o_proj+reduce, norm+gate_up+swiglu,
+ * down+reduce): pass 6 events. MOE_FFN has 4 (routing and bucketing, expert
+ * gate/up, expert down, weighted combine): pass 5. While the hook is set,
+ * DECODE and MOE_FFN launch without programmatic dependent launch, so each
+ * event pair brackets its own kernels only. n_events = 0 or events = NULL
+ * clears the hook. The array is copied. */
 tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int32_t n_events);
 
 /* ----------------------------------------------------------------- misc */

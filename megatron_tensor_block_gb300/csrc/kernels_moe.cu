@@ -389,12 +389,17 @@ static cudaError_t launch_small(const void* fn, void* arg, int grid, int threads
     return launch_pdl(fn, args, grid, 0, s, threads);
 }
 
-cudaError_t launch_moe(const MoeParams& p, cudaStream_t s) {
+cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* marks, int n_marks) {
     MoeParams q = p;
+    auto mark = [&](int i) {
+        if (i < n_marks && marks[i]) cudaEventRecord(marks[i], s);
+    };
+    mark(0);
     cudaError_t e = launch_small(reinterpret_cast<const void*>(moe_route_kernel), &q, (p.T + 7) / 8, 256, s);
     if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_bucket_kernel), &q, 1, 1024, s);
     if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_prep_kernel), &q, p.T * p.top_k, 256, s);
     if (e != cudaSuccess) return e;
+    mark(1);
     const size_t smem = moe_gemm_smem(p.E);
     static int set_bytes = -1;
     if ((int)smem > set_bytes) {
@@ -428,8 +433,10 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s) {
         e = launch_pdl(reinterpret_cast<const void*>(moe_gemm_kernel), args, U < kSMs ? U : kSMs, smem, s,
                        kStreamThreads);
         if (e != cudaSuccess) return e;
+        mark(2 + down);
     }
     e = launch_small(reinterpret_cast<const void*>(moe_combine_kernel), &q, p.T, 256, s);
+    mark(4);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

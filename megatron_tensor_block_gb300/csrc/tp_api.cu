@@ -773,10 +773,8 @@ static tp_status forward_moe(tp_plan_t P, const tp_shard_set* w, const float* x,
     m.y = y;
     m.status = reinterpret_cast<int*>(ws + P->off_status);
     set_pdl(P->n_stage_ev == 0);
-    stage_mark(P, 0, s);
-    cudaError_t e = launch_moe(m, s);
+    cudaError_t e = launch_moe(m, s, P->stage_ev, P->n_stage_ev < 5 ? P->n_stage_ev : 5);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: MoE launch");
-    stage_mark(P, 1, s);
     return ok();
 }
 

@@ -141,7 +141,9 @@ struct MoeParams {
     float* y;                              // [T][H]
     int* status;
 };
-cudaError_t launch_moe(const MoeParams& p, cudaStream_t s);
+// marks: optional events recorded before routing, after the routing kernels,
+// after each expert GEMM and after the combine (n_marks <= 5)
+cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* marks = nullptr, int n_marks = 0);
 
 // 2-D bf16 tensor map [rows, inner] with boxes box_inner x box_rows (cached).
 cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner, int box_rows, int swizzle128,
