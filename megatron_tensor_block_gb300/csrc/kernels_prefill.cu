@@ -204,16 +204,20 @@ __device__ __forceinline__ float fbits(uint32_t u) { return __uint_as_float(u); 
 
 // ---------------------------------------------------------------------------
 // column-parallel projection with fused epilogue (QKV + RoPE + KV append, or
-// gate/up + SwiGLU), one 128-token x 256-column tile of one shard per CTA
+// gate/up + SwiGLU). Persistent: one CTA per SM walks the 128-token x
+// 256-column tiles of every shard; two accumulators in tensor memory
+// (2 x 256 columns) let the epilogue of one tile run while the MMAs of the
+// next are issued, and the TMA producer runs ahead across tile boundaries.
 // ---------------------------------------------------------------------------
 
 enum TcMode : int { TC_QKV = 0, TC_GATEUP = 1 };
 
 struct TcColArgs {
-    CUtensorMap ta;                       // normalised activations [T, K], boxes 64 x 128
+    CUtensorMap ta;                       // normalised activations [copies * T, K], boxes 64 x 128
     CUtensorMap tb[TP_MAX_SHARDS];        // QKV: [qkv_rows, K] boxes 64 x 256; gate/up: [2F', K] boxes 64 x 128
     int T, K, S;                          // tokens, reduction length, tokens per sequence
     int a_row_stride;                     // first A row of shard r = r * a_row_stride (0: shared copy)
+    int n_mt, n_nt, N;                    // tiles: token tiles, column tiles per shard, shards
     int hq_s, hkv_s, d, max_kv, ffn_s;
     const float* bias[TP_MAX_SHARDS];
     const int* pos;                       // [B] first new position of each sequence
@@ -225,169 +229,242 @@ struct TcColArgs {
     int* status;
 };
 
+// tile -> (token tile, column tile, shard); token tiles vary fastest so that
+// the CTAs resident at one time share the weight tiles they stream
+__device__ __forceinline__ void col_tile(const TcColArgs& g, int tile, int& mt, int& nt, int& r) {
+    mt = tile % g.n_mt;
+    const int rest = tile / g.n_mt;
+    nt = rest % g.n_nt;
+    r = rest / g.n_nt;
+}
+
+template <int MODE>
+__device__ __forceinline__ void col_epilogue(const TcColArgs& g, uint32_t acc, int mt, int nt, int r, int q, int lane,
+                                             bool ok) {
+    const int t = mt * kTcBM + 32 * q + lane;
+    const bool live = ok && t < g.T;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    if (MODE == TC_GATEUP) {
+        for (int c = 0; c < 4; ++c) {
+            if (nt * 128 + 32 * c >= g.ffn_s) break;      // ragged last tile (warp-uniform)
+            uint32_t gv[32], uv[32];
+            tmem_ld32(acc + lane_off + 32 * c, gv);
+            tmem_ld32(acc + lane_off + 128 + 32 * c, uv);
+            tmem_wait_ld();
+            if (live) {
+                bf16* dst = g.act + ((size_t)r * g.T + t) * g.ffn_s + nt * 128 + 32 * c;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 pk;
+                    uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {
+                        const float g0 = fbits(gv[i + j]), g1 = fbits(gv[i + j + 1]);
+                        const float a0 = g0 / (1.0f + expf(-g0)) * fbits(uv[i + j]);
+                        const float a1 = g1 / (1.0f + expf(-g1)) * fbits(uv[i + j + 1]);
+                        w[j / 2] = pack_bf16x2(a0, a1);
+                    }
+                    *reinterpret_cast<uint4*>(dst + i) = pk;
+                }
+            }
+        }
+        return;
+    }
+    const int d = g.d, half = d >> 1;
+    const int b = t / g.S, sidx = t - b * g.S;
+    const int p = live ? g.pos[b] + sidx : 0;
+    const bool in_cache = p >= 0 && p < g.max_kv;
+    if (live && !in_cache) set_status(g.status, TP_ERR_CAPACITY);
+    const int pr = in_cache ? p : 0;                     // rotary table row (in range on every path)
+    const int n_heads = g.hq_s + 2 * g.hkv_s;
+    for (int hh = 0; hh < kTcBN / d; ++hh) {
+        const int head = (nt * kTcBN) / d + hh;
+        if (head >= n_heads) break;                       // ragged last tile (warp-uniform)
+        const bool is_q = head < g.hq_s;
+        const bool is_k = !is_q && head < g.hq_s + g.hkv_s;
+        const bool rot = is_q || is_k;
+        bf16* qdst = g.q_out + ((size_t)r * g.T + t) * g.hq_s * d + head * d;
+        bf16* cdst = nullptr;
+        if (!is_q && in_cache && live) {
+            const int kvh = is_k ? head - g.hq_s : head - g.hq_s - g.hkv_s;
+            bf16* cache = reinterpret_cast<bf16*>(is_k ? g.kcache[r] : g.vcache[r]);
+            cdst = cache + (((size_t)b * g.hkv_s + kvh) * g.max_kv + p) * d;
+        }
+        const float* bias = g.bias[r];
+        for (int c = 0; c < half / 32; ++c) {
+            uint32_t lo[32], hi[32];
+            tmem_ld32(acc + lane_off + hh * d + 32 * c, lo);
+            tmem_ld32(acc + lane_off + hh * d + half + 32 * c, hi);
+            tmem_wait_ld();
+            if (!live) continue;
+            uint32_t plo[16], phi[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float va0 = fbits(lo[i]), va1 = fbits(lo[i + 1]);
+                float vb0 = fbits(hi[i]), vb1 = fbits(hi[i + 1]);
+                if (bias) {
+                    const int col = head * d + 32 * c + i;
+                    va0 += bias[col];
+                    va1 += bias[col + 1];
+                    vb0 += bias[col + half];
+                    vb1 += bias[col + half + 1];
+                }
+                if (rot) {
+                    const float2 cs0 = g.rope[(size_t)pr * half + 32 * c + i];
+                    const float2 cs1 = g.rope[(size_t)pr * half + 32 * c + i + 1];
+                    const float ra0 = va0 * cs0.x - vb0 * cs0.y, rb0 = va0 * cs0.y + vb0 * cs0.x;
+                    const float ra1 = va1 * cs1.x - vb1 * cs1.y, rb1 = va1 * cs1.y + vb1 * cs1.x;
+                    va0 = ra0;
+                    vb0 = rb0;
+                    va1 = ra1;
+                    vb1 = rb1;
+                }
+                plo[i / 2] = pack_bf16x2(va0, va1);
+                phi[i / 2] = pack_bf16x2(vb0, vb1);
+            }
+            bf16* dst = is_q ? qdst : cdst;
+            if (dst) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                    *reinterpret_cast<uint4*>(dst + 32 * c + 2 * i) = make_uint4(plo[i], plo[i + 1], plo[i + 2], plo[i + 3]);
+                    *reinterpret_cast<uint4*>(dst + half + 32 * c + 2 * i) =
+                        make_uint4(phi[i], phi[i + 1], phi[i + 2], phi[i + 3]);
+                }
+            }
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_col_kernel(const __grid_constant__ TcColArgs g) {
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full, *empty, *extra;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
-    const uint32_t one = 1;
-    tc_setup(smem, kTcStages, kTcStages, 256, g.status, full, empty, extra, tmem_slot, abort_flag, 1, &one);
-    uint64_t* accum = extra;
+    const uint32_t counts[5] = {1, 1, 4, 4, 1};   // acc full x2, acc empty x2 (epilogue warps), done
+    tc_setup(smem, kTcStages, kTcStages, 512, g.status, full, empty, extra, tmem_slot, abort_flag, 5, counts);
+    uint64_t* acc_full = extra;
+    uint64_t* acc_empty = extra + 2;
+    uint64_t* done = extra + 4;
     const uint32_t tmem = *tmem_slot;
     unsigned char* stages = smem + 1024;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kTcBM, nt = blockIdx.y, r = blockIdx.z;
     const int nk = g.K / kTcBK;
+    const int ntiles = g.n_mt * g.n_nt * g.N;
 
     if (warp == 0) {
         if (lane == 0 && !*abort_flag) {
-            int kb = 0;
-            for (; kb < nk; ++kb) {
-                const int s = kb % kTcStages;
-                if (!mbar_wait(&empty[s], ((kb / kTcStages) & 1) ^ 1, abort_flag, g.status)) break;
-                mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-                unsigned char* st = stages + s * kTcStageBytes;
-                tma_load_2d_keep(st, &g.ta, kb * kTcBK, r * g.a_row_stride + m0, &full[s]);
-                if (MODE == TC_QKV) {
-                    tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, nt * kTcBN, &full[s]);
-                } else {   // 128 gate rows, then the matching 128 up rows
-                    tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, nt * 128, &full[s]);
-                    tma_load_2d_keep(st + kTcABytes + kTcBBytes / 2, &g.tb[r], kb * kTcBK, g.ffn_s + nt * 128,
-                                     &full[s]);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                int mt, nt, r;
+                col_tile(g, tile, mt, nt, r);
+                const int arow = r * g.a_row_stride + mt * kTcBM;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kTcStages;
+                    if (!mbar_wait(&empty[s], ((it / kTcStages) & 1) ^ 1, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], kTcStageBytes);
+                    unsigned char* st = stages + s * kTcStageBytes;
+                    tma_load_2d_keep(st, &g.ta, kb * kTcBK, arow, &full[s]);
+                    if (MODE == TC_QKV) {
+                        tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, nt * kTcBN, &full[s]);
+                    } else {   // 128 gate rows, then the matching 128 up rows
+                        tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, nt * 128, &full[s]);
+                        tma_load_2d_keep(st + kTcABytes + kTcBBytes / 2, &g.tb[r], kb * kTcBK, g.ffn_s + nt * 128,
+                                         &full[s]);
+                    }
                 }
             }
-            volatile int no_abort = 0;
-            for (int k = kb > kTcStages ? kb - kTcStages : 0; k < kb; ++k)
+            volatile int no_abort = 0;         // no copy may still be landing when the CTA exits
+            for (uint32_t k = it > (uint32_t)kTcStages ? it - kTcStages : 0; k < it; ++k)
                 mbar_wait(&full[k % kTcStages], (k / kTcStages) & 1, &no_abort, nullptr);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
-            for (int kb = 0; kb < nk && !*abort_flag; ++kb) {
-                const int s = kb % kTcStages;
-                if (!mbar_wait(&full[s], (kb / kTcStages) & 1, abort_flag, g.status)) break;
+            uint32_t it = 0;
+            bool ok = !*abort_flag;
+            int li = 0;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++li) {
+                const int buf = li & 1;
+                if (!mbar_wait(&acc_empty[buf], ((li >> 1) & 1) ^ 1, abort_flag, g.status)) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(stages + s * kTcStageBytes), b0 = a0 + kTcABytes;
+                const uint32_t acc = tmem + 256 * buf;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kTcStages;
+                    if (!mbar_wait(&full[s], (it / kTcStages) & 1, abort_flag, g.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(stages + s * kTcStageBytes), b0 = a0 + kTcABytes;
 #pragma unroll
-                for (int k = 0; k < kTcBK / 16; ++k)
-                    tc_mma(tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-                tc_commit(smem_u32(&empty[s]));
+                    for (int k = 0; k < kTcBK / 16; ++k)
+                        tc_mma(acc, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
+                    tc_commit(smem_u32(&empty[s]));
+                }
+                if (ok) tc_commit(smem_u32(&acc_full[buf]));
             }
-            tc_commit(smem_u32(accum));
+            tc_commit(smem_u32(done));                // fires when every issued MMA has completed
         }
     } else {
-        const int q = warp & 3;
-        const bool ok = mbar_wait(accum, 0, abort_flag, g.status);
-        tc_fence_after();
-        const int t = m0 + 32 * q + lane;
-        const bool live = ok && t < g.T;
-        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        if (MODE == TC_GATEUP) {
-            for (int c = 0; c < 4; ++c) {
-                if (nt * 128 + 32 * c >= g.ffn_s) break;     // ragged last tile (warp-uniform)
-                uint32_t gv[32], uv[32];
-                tmem_ld32(tmem + lane_off + 32 * c, gv);
-                tmem_ld32(tmem + lane_off + 128 + 32 * c, uv);
-                tmem_wait_ld();
-                if (live) {
-                    bf16* dst = g.act + ((size_t)r * g.T + t) * g.ffn_s + nt * 128 + 32 * c;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float g0 = fbits(gv[i]), g1 = fbits(gv[i + 1]);
-                        const float a0 = g0 / (1.0f + expf(-g0)) * fbits(uv[i]);
-                        const float a1 = g1 / (1.0f + expf(-g1)) * fbits(uv[i + 1]);
-                        *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(a0, a1);
-                    }
-                }
+        const int q = warp & 3;                        // warps 2..5 -> tensor-memory lane quarters 2,3,0,1
+        int li = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++li) {
+            const int buf = li & 1;
+            bool ok = mbar_wait(&acc_full[buf], (li >> 1) & 1, abort_flag, g.status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            if (ok) {
+                int mt, nt, r;
+                col_tile(g, tile, mt, nt, r);
+                col_epilogue<MODE>(g, tmem + 256 * buf, mt, nt, r, q, lane, true);
             }
-        } else {
-            const int d = g.d, half = d >> 1;
-            const int b = t / g.S, sidx = t - b * g.S;
-            const int p = live ? g.pos[b] + sidx : 0;
-            const bool in_cache = p >= 0 && p < g.max_kv;
-            if (live && !in_cache) set_status(g.status, TP_ERR_CAPACITY);
-            const int pr = in_cache ? p : 0;                 // rotary table row (in range on every path)
-            const int n_heads = g.hq_s + 2 * g.hkv_s;
-            for (int hh = 0; hh < kTcBN / d; ++hh) {
-                const int head = (nt * kTcBN) / d + hh;
-                if (head >= n_heads) break;                   // ragged last tile (warp-uniform)
-                for (int c = 0; c < half / 32; ++c) {
-                    uint32_t lo[32], hi[32];
-                    tmem_ld32(tmem + lane_off + hh * d + 32 * c, lo);
-                    tmem_ld32(tmem + lane_off + hh * d + half + 32 * c, hi);
-                    tmem_wait_ld();
-                    if (!live) continue;
-                    const float* bias = g.bias[r];
-                    const bool rot = head < g.hq_s + g.hkv_s;
-                    bf16* qdst = g.q_out + ((size_t)r * g.T + t) * g.hq_s * d + head * d + 32 * c;
-                    const bool is_q = head < g.hq_s;
-                    const bool is_k = !is_q && head < g.hq_s + g.hkv_s;
-                    bf16* cdst = nullptr;
-                    if (!is_q && in_cache) {
-                        const int kvh = is_k ? head - g.hq_s : head - g.hq_s - g.hkv_s;
-                        bf16* cache = reinterpret_cast<bf16*>(is_k ? g.kcache[r] : g.vcache[r]);
-                        cdst = cache + (((size_t)b * g.hkv_s + kvh) * g.max_kv + p) * d + 32 * c;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float va0 = fbits(lo[i]), va1 = fbits(lo[i + 1]);
-                        float vb0 = fbits(hi[i]), vb1 = fbits(hi[i + 1]);
-                        if (bias) {
-                            const int col = head * d + 32 * c + i;
-                            va0 += bias[col]; va1 += bias[col + 1];
-                            vb0 += bias[col + half]; vb1 += bias[col + half + 1];
-                        }
-                        if (rot) {
-                            const float2 cs0 = g.rope[(size_t)pr * half + 32 * c + i];
-                            const float2 cs1 = g.rope[(size_t)pr * half + 32 * c + i + 1];
-                            const float ra0 = va0 * cs0.x - vb0 * cs0.y, rb0 = va0 * cs0.y + vb0 * cs0.x;
-                            const float ra1 = va1 * cs1.x - vb1 * cs1.y, rb1 = va1 * cs1.y + vb1 * cs1.x;
-                            va0 = ra0; vb0 = rb0; va1 = ra1; vb1 = rb1;
-                        }
-                        if (is_q) {
-                            *reinterpret_cast<uint32_t*>(qdst + i) = pack_bf16x2(va0, va1);
-                            *reinterpret_cast<uint32_t*>(qdst + half + i) = pack_bf16x2(vb0, vb1);
-                        } else if (cdst) {
-                            *reinterpret_cast<uint32_t*>(cdst + i) = pack_bf16x2(va0, va1);
-                            *reinterpret_cast<uint32_t*>(cdst + half + i) = pack_bf16x2(vb0, vb1);
-                        }
-                    }
-                }
-            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            if (!ok) break;
         }
     }
-    tc_teardown(accum, 0, tmem, 256);
+    tc_teardown(done, 0, tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
-// row-parallel projection with the rank-ordered reduction in tensor memory:
-// for one 128-token x 128-column output tile, shard r's partial product is
-// accumulated in its own TMEM buffer (two buffers alternate), then added to
-// the running sum in rank order: sum = ((p0 + p1) + p2) + ...; the residual is
-// added last.
+// row-parallel projection with the rank-ordered reduction: for one
+// 128-token x 256-column output tile, shard r's partial product is
+// accumulated in its own tensor-memory buffer (two buffers alternate, so the
+// MMAs of shard r+1 run while shard r's partial is read), and the epilogue
+// warps add the partials into a running sum held in registers in rank
+// order, sum = ((p0 + p1) + p2) + ...; the residual is added last.
+// Persistent over the output tiles; 8 epilogue warps, two per lane quarter,
+// each holding 128 of the tile's 256 columns for its 32 rows.
 // ---------------------------------------------------------------------------
 
-constexpr int kRowBN = 128;
-constexpr int kRowStages = 6;
-constexpr int kRowStageBytes = kTcABytes + kRowBN * kTcBK * 2;   // 32 KB
+constexpr int kRowBN = 256;
+constexpr int kRowStages = 4;
+constexpr int kRowStageBytes = kTcABytes + kRowBN * kTcBK * 2;   // 48 KB
 constexpr int kRowSmem = 1024 + kRowStages * kRowStageBytes;
+constexpr int kRowThreads = 320;
 
 struct TcRowArgs {
     CUtensorMap ta;                       // per-shard activations stacked [N * T, Kr], boxes 64 x 128
-    CUtensorMap tb[TP_MAX_SHARDS];        // shard weights [H, Kr], boxes 64 x 128
+    CUtensorMap tb[TP_MAX_SHARDS];        // shard weights [H, Kr], boxes 64 x 256
     int T, Kr, N, H;
+    int n_mt, n_nt;
     const float* resid;                   // [T][H]
     float* out;                           // [T][H]
     int* status;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1) tc_row_kernel(const __grid_constant__ TcRowArgs g) {
+__global__ void __launch_bounds__(kRowThreads, 1) tc_row_kernel(const __grid_constant__ TcRowArgs g) {
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full, *empty, *extra;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
-    const uint32_t counts[5] = {1, 1, 4, 4, 1};   // partial full x2, partial empty x2, done
+    const uint32_t counts[5] = {1, 1, 8, 8, 1};   // partial full x2, partial empty x2 (epilogue warps), done
     tc_setup(smem, kRowStages, kRowStages, 512, g.status, full, empty, extra, tmem_slot, abort_flag, 5, counts);
     uint64_t* pfull = extra;
     uint64_t* pempty = extra + 2;
@@ -395,25 +472,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_row_kernel(const __grid_cons
     const uint32_t tmem = *tmem_slot;
     unsigned char* stages = smem + 1024;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * kRowBN;
     const int nk = g.Kr / kTcBK;
+    const int ntiles = g.n_mt * g.n_nt;
 
     if (warp == 0) {
         if (lane == 0 && !*abort_flag) {
             uint32_t it = 0;
             bool ok = true;
-            for (int r = 0; r < g.N && ok; ++r)
-                for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int s = it % kRowStages;
-                    if (!mbar_wait(&empty[s], ((it / kRowStages) & 1) ^ 1, abort_flag, g.status)) {
-                        ok = false;
-                        break;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % g.n_mt) * kTcBM, n0 = (tile / g.n_mt) * kRowBN;
+                for (int r = 0; r < g.N && ok; ++r)
+                    for (int kb = 0; kb < nk; ++kb, ++it) {
+                        const int s = it % kRowStages;
+                        if (!mbar_wait(&empty[s], ((it / kRowStages) & 1) ^ 1, abort_flag, g.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[s], kRowStageBytes);
+                        unsigned char* st = stages + s * kRowStageBytes;
+                        tma_load_2d_keep(st, &g.ta, kb * kTcBK, r * g.T + m0, &full[s]);
+                        tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, n0, &full[s]);
                     }
-                    mbar_arrive_expect_tx(&full[s], kRowStageBytes);
-                    unsigned char* st = stages + s * kRowStageBytes;
-                    tma_load_2d_keep(st, &g.ta, kb * kTcBK, r * g.T + m0, &full[s]);
-                    tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, n0, &full[s]);
-                }
+            }
             volatile int no_abort = 0;
             for (uint32_t k = it > (uint32_t)kRowStages ? it - kRowStages : 0; k < it; ++k)
                 mbar_wait(&full[k % kRowStages], (k / kRowStages) & 1, &no_abort, nullptr);
@@ -421,64 +501,80 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_row_kernel(const __grid_cons
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kTcBM, kRowBN);
-            uint32_t it = 0;
+            uint32_t it = 0, pi = 0;
             bool ok = !*abort_flag;
-            for (int r = 0; r < g.N && ok; ++r) {
-                const int buf = r & 1;
-                if (!mbar_wait(&pempty[buf], ((r >> 1) & 1) ^ 1, abort_flag, g.status)) break;
-                tc_fence_after();
-                const uint32_t dt = tmem + 128 + 128 * buf;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
-                    const int s = it % kRowStages;
-                    if (!mbar_wait(&full[s], (it / kRowStages) & 1, abort_flag, g.status)) {
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x)
+                for (int r = 0; r < g.N && ok; ++r, ++pi) {
+                    const int buf = pi & 1;
+                    if (!mbar_wait(&pempty[buf], ((pi >> 1) & 1) ^ 1, abort_flag, g.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(stages + s * kRowStageBytes), b0 = a0 + kTcABytes;
+                    const uint32_t dt = tmem + 256 * buf;
+                    for (int kb = 0; kb < nk; ++kb, ++it) {
+                        const int s = it % kRowStages;
+                        if (!mbar_wait(&full[s], (it / kRowStages) & 1, abort_flag, g.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(stages + s * kRowStageBytes), b0 = a0 + kTcABytes;
 #pragma unroll
-                    for (int k = 0; k < kTcBK / 16; ++k)
-                        tc_mma(dt, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-                    tc_commit(smem_u32(&empty[s]));
+                        for (int k = 0; k < kTcBK / 16; ++k)
+                            tc_mma(dt, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
+                                   (kb | k) != 0);
+                        tc_commit(smem_u32(&empty[s]));
+                    }
+                    if (ok) tc_commit(smem_u32(&pfull[buf]));
                 }
-                tc_commit(smem_u32(&pfull[buf]));
-            }
             tc_commit(smem_u32(done));
         }
     } else {
-        const int q = warp & 3;
-        const int t = m0 + 32 * q + lane;
+        const int q = warp & 3;                      // warps 2..9 -> lane quarters 2,3,0,1,2,3,0,1
+        const int hf = (warp - 2) >> 2;              // which 128 of the 256 columns
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        for (int r = 0; r < g.N; ++r) {
-            const int buf = r & 1;
-            const bool ok = mbar_wait(&pfull[buf], (r >> 1) & 1, abort_flag, g.status);
-            tc_fence_after();
-            for (int c = 0; c < kRowBN / 32; ++c) {
-                uint32_t pv[32], sv[32];
-                tmem_ld32(tmem + lane_off + 128 + 128 * buf + 32 * c, pv);
-                if (r > 0) tmem_ld32(tmem + lane_off + 32 * c, sv);
-                tmem_wait_ld();
-                if (r > 0) {
+        uint32_t pi = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const int m0 = (tile % g.n_mt) * kTcBM, n0 = (tile / g.n_mt) * kRowBN;
+            float sum[128];
+            for (int r = 0; r < g.N; ++r, ++pi) {
+                const int buf = pi & 1;
+                ok = mbar_wait(&pfull[buf], (pi >> 1) & 1, abort_flag, g.status);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                if (ok) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) pv[i] = __float_as_uint(fbits(sv[i]) + fbits(pv[i]));
-                }
-                if (r + 1 < g.N) {
-                    tmem_st32(tmem + lane_off + 32 * c, pv);
-                } else if (ok && t < g.T && n0 + 32 * c < g.H) {
-                    const size_t o = (size_t)t * g.H + n0 + 32 * c;
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_off + 256 * buf + 128 * hf + 32 * c, v);
+                        tmem_wait_ld();
+                        if (r == 0) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 rv = *reinterpret_cast<const float4*>(g.resid + o + i);
-                        *reinterpret_cast<float4*>(g.out + o + i) =
-                            make_float4(rv.x + fbits(pv[i]), rv.y + fbits(pv[i + 1]), rv.z + fbits(pv[i + 2]),
-                                        rv.w + fbits(pv[i + 3]));
+                            for (int i = 0; i < 32; ++i) sum[32 * c + i] = fbits(v[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) sum[32 * c + i] += fbits(v[i]);
+                        }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pempty[buf]);
+                if (!ok) break;
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pempty[buf]);
+            const int t = m0 + 32 * q + lane;
+            const int n = n0 + 128 * hf;
+            if (ok && t < g.T && n < g.H) {
+                const size_t o = (size_t)t * g.H + n;
+#pragma unroll
+                for (int i = 0; i < 128; i += 4) {
+                    const float4 rv = *reinterpret_cast<const float4*>(g.resid + o + i);
+                    *reinterpret_cast<float4*>(g.out + o + i) =
+                        make_float4(rv.x + sum[i], rv.y + sum[i + 1], rv.z + sum[i + 2], rv.w + sum[i + 3]);
+                }
+            }
         }
     }
     tc_teardown(done, 0, tmem, 512);
@@ -804,10 +900,14 @@ cudaError_t launch_tc_col(int mode, const PrefillColParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         set[mode] = true;
     }
-    const int ntiles = mode == TC_QKV ? (p.rows + kTcBN - 1) / kTcBN : (p.ffn_s + 127) / 128;
-    dim3 grid((p.T + kTcBM - 1) / kTcBM, ntiles, p.N);
+    g.n_mt = (p.T + kTcBM - 1) / kTcBM;
+    g.n_nt = mode == TC_QKV ? (p.rows + kTcBN - 1) / kTcBN : (p.ffn_s + 127) / 128;
+    g.N = p.N;
+    const long tiles = (long)g.n_mt * g.n_nt * g.N;
+    if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const int grid = tiles < kSMs ? (int)tiles : kSMs;
     void* args[] = {&g};
-    e = cudaLaunchKernel(fn, grid, dim3(kTcThreads), args, kTcSmem, s);
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(kTcThreads), args, kTcSmem, s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -831,8 +931,12 @@ cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         set = true;
     }
-    dim3 grid((p.T + kTcBM - 1) / kTcBM, (p.H + kRowBN - 1) / kRowBN);
-    tc_row_kernel<<<grid, kTcThreads, kRowSmem, s>>>(g);
+    g.n_mt = (p.T + kTcBM - 1) / kTcBM;
+    g.n_nt = (p.H + kRowBN - 1) / kRowBN;
+    const long tiles = (long)g.n_mt * g.n_nt;
+    if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const int grid = tiles < kSMs ? (int)tiles : kSMs;
+    tc_row_kernel<<<grid, kRowThreads, kRowSmem, s>>>(g);
     return cudaGetLastError();
 }
 
