@@ -385,12 +385,18 @@ def block_rows_tpN(shards, x, k_caches, v_caches, pos, S, cfg, N, rows):
         for r in range(N):
             Sr = shards[r]
             n = rmsnorm(x[toks], Sr["gamma_attn"], cfg.eps)
-            qkv = n @ Sr["wqkv"].T
-            if Sr["bqkv"] is not None:
-                qkv = qkv + Sr["bqkv"]
-            q = rope(qkv[local, :Hq_s * d].reshape(local.size, Hq_s, d), Pb[local], cfg.rope_theta)
-            k = rope(qkv[:, Hq_s * d:(Hq_s + Hkv_s) * d].reshape(upto, Hkv_s, d), Pb, cfg.rope_theta)
-            v = qkv[:, (Hq_s + Hkv_s) * d:].reshape(upto, Hkv_s, d)
+            # the q rows of the fused projection only for the selected tokens,
+            # the k and v rows for every token up to the last selected one
+            W, bias = Sr["wqkv"], Sr["bqkv"]
+            nq = Hq_s * d
+            q = n[local] @ W[:nq].T
+            kv = n @ W[nq:].T
+            if bias is not None:
+                q = q + bias[:nq]
+                kv = kv + bias[nq:]
+            q = rope(q.reshape(local.size, Hq_s, d), Pb[local], cfg.rope_theta)
+            k = rope(kv[:, :Hkv_s * d].reshape(upto, Hkv_s, d), Pb, cfg.rope_theta)
+            v = kv[:, Hkv_s * d:].reshape(upto, Hkv_s, d)
             kc = k_caches[r][b].copy()
             vc = v_caches[r][b].copy()
             kc[:, Pb, :] = k.transpose(1, 0, 2)

@@ -123,7 +123,9 @@ def test_full_llama3_8b_prefill_tp8_sampled_rows(gpu_lib):
     inputs = synth.make_inputs(w, with_head=False)
     m, y = _run(inputs, share_norm=True)
     S = w.tokens_per_seq
-    rows = [0, 1, 63, 64, 127, 128, 1000, S - 1, 3 * S, 3 * S + 129, 4 * S - 2, 4 * S - 1]
+    # every sequence's last token, tile and query-block edges, and 64 seeded-random rows
+    rows = [b * S + S - 1 for b in range(w.batch)] + [0, 1, 63, 64, 127, 128, 3 * S, 3 * S + 129, 4 * S - 2]
+    rows += np.random.Generator(np.random.PCG64(2024)).integers(0, w.tokens, 64).tolist()
     L = O.layer_f64(inputs["layers"][0])
     shards = O.shard_layer(L, w, w.tp)
     ks = O.shard_kv_cache(R.full_cache(inputs["k_cache"][0], m.max_kv), w.tp)
