@@ -55,11 +55,14 @@ STAGES = {
     "moe": ["route_bucket", "expert_gate_up", "expert_down", "combine"],
 }
 DOMINANT = {"decode": "gate_up_swiglu", "prefill": "gate_up_swiglu", "moe": "expert_gate_up"}
+# phases of the one-launch bf16 decode step (tp_profile_phases)
+STEP_PHASES = ["norm", "qkv_rope", "attention", "combine", "o_proj", "reduce_o", "gate_up_swiglu", "down",
+               "reduce_down"]
 # the committed ncu summary of each dominant kernel and the source it was taken on
-PROFILE = {"decode": ("gemv_swiglu_llama3_8b_decode.md", "kernels_decode.cu"),
+PROFILE = {"decode": ("decode_step_llama3_8b_decode.md", "kernels_decode.cu"),
            "prefill": ("tc_gateup_llama3_8b_prefill.md", "kernels_prefill.cu"),
            "moe": ("moe_gemm_expert_slice.md", "kernels_moe.cu")}
-LAUNCHES_PER_LAYER = {"decode": 9, "prefill": 8, "moe": 6}
+LAUNCHES_PER_LAYER = {"decode": 1, "prefill": 8, "moe": 6}
 L2_BYTES = 129e6
 
 
@@ -391,28 +394,52 @@ def run_ours(args, world, rank, local):
     tokens_step = w.tokens
     value = tokens_step * args.steps * world / (t_ms / 1e3)
 
-    # ---- per-kernel durations: stage events around each launch, on the launching stream
+    # ---- per-kernel durations: events around each launch, on the launching stream
+    step_kernel = kind == "decode" and w.dtype == "bf16"     # the whole step is one persistent launch
     n_prof = max(1, min(args.steps, 2000 if kind != "prefill" else 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(n_prof)]
+    n_ev = 2 if step_kernel else len(stages) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_prof)]
     for row in evs:          # torch creates events lazily: record once so the raw handles exist
         for e in row:
             e.record(stream)
     stream.synchronize()
+    phases = []
     with torch.cuda.stream(stream):
         for i in range(n_prof):
             tb.tp_profile_stages(model.plan, evs[i])
             model.forward(stream=stream)
+            if step_kernel and i % 10 == 0:
+                phases.append(tb.tp_profile_phases(model.plan, len(STEP_PHASES), stream))
         tb.tp_profile_stages(model.plan, None)
     torch.cuda.synchronize()
     stage_ms = {}
-    for j, name in enumerate(stages):
-        ts = [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_prof)]
-        stage_ms[name] = statistics.mean(ts)
+    if step_kernel:
+        stages = STEP_PHASES
+        for j, name in enumerate(stages):
+            stage_ms[name] = statistics.mean(ph[j] for ph in phases) / 1e3
+        kernel_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof))
+    else:
+        for j, name in enumerate(stages):
+            ts = [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_prof)]
+            stage_ms[name] = statistics.mean(ts)
     pk = peaks()
     dom = DOMINANT[kind]
-    dom_ms = stage_ms[dom]
+    dom_ms = stage_ms.get(dom)
     extra = {}
-    if kind == "prefill":
+    if step_kernel:
+        sb = step_bytes(w) // max(w.n_layers, 1)            # one launch = one layer
+        achieved = sb / (kernel_ms / 1e3) / 1e9
+        peak = pk["hbm"]
+        roof = {"bound": "hbm", "kernel": "decode_step_kernel (one persistent launch per layer)", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": pk["kind"] + " copy bandwidth",
+                "algorithmic_bytes": sb, "launch_us": kernel_ms * 1e3, "traffic": kernel_traffic(kind)}
+        if w.n_layers > 1:
+            roof["note"] = "phase times of the last layer of each profiled step"
+        step_gbs = step_bytes(w) / (ms_step / 1e3) / 1e9
+        extra["hbm"] = {"step_bytes": step_bytes(w), "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak,
+                        "frac_of_8000": step_gbs / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
+        l2_note = f"inputs larger than L2 ({step_bytes(w) / 1e6:.1f} MB read per step vs 129 MB L2)"
+    elif kind == "prefill":
         fl = prefill_flops(w)
         achieved = fl[dom] / (dom_ms / 1e3) / 1e12
         peak = pk["tensor_sustained"]
@@ -437,7 +464,7 @@ def run_ours(args, world, rank, local):
         extra["hbm"] = {"step_bytes": sb, "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak, "peak_gbs": peak,
                         "experts_hit": mb["experts_hit"]}
         l2_note = f"inputs larger than L2 ({sb / 1e6:.0f} MB of expert weights read per step vs 129 MB L2)"
-    else:
+    else:                                   # fp32 decode: separate launches
         sb = stage_bytes(w)
         achieved = sb[dom] / (dom_ms / 1e3) / 1e9
         peak = pk["hbm"]

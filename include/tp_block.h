@@ -353,6 +353,20 @@ tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);
  * clears the hook. The array is copied. */
 tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int32_t n_events);
 
+/* bf16 DECODE runs the whole block as one persistent launch whose phases
+ * are: RMSNorm operands, QKV (+RoPE, KV append), attention, split-KV
+ * combine, o_proj, rank-ordered reduce (+ next norm operands), gate/up
+ * (+SwiGLU), down, rank-ordered reduce. While the hook above is set, that
+ * launch also records per-CTA device timestamps at its start, at each of its
+ * 8 grid barriers and at its end, and events[0] / events[n_events-1] bracket
+ * the launch. This call reads the timestamps of the last such step and
+ * writes the duration of the first `n` (1..9) phases in microseconds to
+ * out_us (host), each measured from the latest arrival at the previous
+ * barrier (the first from the earliest start) to the latest arrival at its
+ * own. Synchronises `stream`. Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no
+ * profiled bf16 decode step yet), TP_ERR_CUDA. */
+tp_status tp_profile_phases(tp_plan_t plan, double* out_us, int32_t n, void* stream);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Message for the last failing call on this thread ("" if none). Never fails. */

@@ -107,6 +107,7 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
         "tp_gemm_bf16": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
         "tp_profile_stages": (I32, [P, C.POINTER(VP), I32]),
+        "tp_profile_phases": (I32, [P, C.POINTER(C.c_double), I32, VP]),
         "tp_last_error": (C.c_char_p, []),
         "tp_version": (I32, []),
     }
@@ -256,6 +257,13 @@ def tp_profile_stages(plan: Plan, events) -> None:
     raw = [e if isinstance(e, int) else e.cuda_event for e in events]
     arr = (C.c_void_p * len(raw))(*raw)
     _check(load().tp_profile_stages(plan.handle, arr, len(raw)))
+
+
+def tp_profile_phases(plan: Plan, n: int = 9, stream=None) -> list:
+    """Phase durations (us) of the last profiled bf16 decode step."""
+    arr = (C.c_double * n)()
+    _check(load().tp_profile_phases(plan.handle, arr, n, _stream(stream)))
+    return list(arr)
 
 
 def tp_last_error() -> str:

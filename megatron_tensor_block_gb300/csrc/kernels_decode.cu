@@ -1077,6 +1077,343 @@ __global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const At
     }
 }
 
+// ---------------------------------------------------------------------------
+// tensor-core split-KV decode attention (bf16 caches). The keys are the MMA
+// rows: S^T = K Q^T with K from shared memory (M = 16 keys per warp) and the
+// group's queries as the 8 columns, so no query padding is needed; then
+// O^T = V^T P^T with P^T moved into operand form by movmatrix. K and V of 64
+// keys arrive per stage as 2-D tensor-map boxes 72 elements wide (head_dim
+// 128), which pads every shared row to 144 bytes: ldmatrix reads are free of
+// bank conflicts without a swizzle. Rows past the chunk's valid keys (stale
+// cache, other groups, or zero fill) are masked in registers (scores to -inf,
+// value operands to zero), so the consumers never write the stages.
+// Warps 0-3 take the even 64-key blocks of a chunk, warps 4-7 the odd ones;
+// each warp keeps a running max, sum and output for its 16 keys per block;
+// the eight are merged at the end of the chunk in a fixed tree order.
+// ---------------------------------------------------------------------------
+
+constexpr int kAtKeys = 64;                   // keys per stage
+constexpr int kAtRing = 5;
+constexpr int kAtMaxStage = 4 * kAtKeys * 72 * 2;   // K and V, two column halves each (head_dim 128)
+constexpr int kAtSlot = 1024;                 // floats per merge slot (G * head_dim <= 1024)
+
+template <int D>
+struct AtShape {
+    static constexpr int NB = D / 64;                     // 64-element column halves per row
+    static constexpr int PT = D == 128 ? 72 : 64;         // elements per shared row (box width)
+    static constexpr int BOX = kAtKeys * PT * 2;          // bytes per box
+    static constexpr int STAGE = 2 * NB * BOX;            // K boxes, then V boxes
+};
+
+struct TmaAttnArgs {
+    CUtensorMap tk[TP_MAX_SHARDS];
+    CUtensorMap tv[TP_MAX_SHARDS];
+    AttnDecodeParams p;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// transpose of an 8x8 bf16 matrix held as one 32-bit fragment register per lane
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// shared address of the 8-element chunk `chunk` of key row `key` in a part
+// (K or V) of a stage made of 64-element-wide boxes
+template <int D>
+__device__ __forceinline__ uint32_t at_addr(uint32_t part, int key, int chunk) {
+    using S = AtShape<D>;
+    return part + (chunk >> 3) * S::BOX + key * (S::PT * 2) + (chunk & 7) * 16;
+}
+
+size_t attn_tc_smem() {
+    return 1024 + (size_t)kAtRing * kAtMaxStage + (size_t)(4 * kAtSlot + 8 * kMaxGroup * 2 + kTMax) * 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kStreamThreads, 1) attn_tc_kernel(const __grid_constant__ TmaAttnArgs A) {
+    using S = AtShape<D>;
+    constexpr int KS = D / 16;
+    const AttnDecodeParams& p = A.p;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kAtRing;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kAtRing);
+    unsigned char* ring = smem + 1024;
+    float* red = reinterpret_cast<float*>(ring + kAtRing * kAtMaxStage);       // [4][kAtSlot]
+    float* s_ml = red + 4 * kAtSlot;                                           // [8 warps][8 queries][m, l]
+    int* s_pos = reinterpret_cast<int*>(s_ml + 8 * kMaxGroup * 2);             // [8]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.hq_s / p.hkv_s;
+    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
+    if (tid == 0) {
+        for (int i = 0; i < kAtRing; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);           // the four warps of one group release a stage
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumers / 32) {             // ---- producer
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            uint32_t it = 0;
+            bool ok = (smem_u32(ring) & 127u) == 0, waited = false;
+            if (!ok) {
+                *abort_flag = 1;
+                set_status(p.status, TP_ERR_ALIGN);
+            }
+            int posv[kTMax];
+            for (int b = 0; b < kTMax; ++b) posv[b] = b < p.B ? p.pos[b] : 0;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const int c = u % p.n_chunks, gi = u / p.n_chunks;
+                const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+                int pos = posv[0];
+#pragma unroll
+                for (int bb = 1; bb < kTMax; ++bb)
+                    if (bb == b) pos = posv[bb];
+                const int Lk = min(pos + 1, p.max_kv);
+                const int j0 = c * kAttnChunk;
+                const int n = max(0, min(Lk - j0, kAttnChunk));
+                const int row0 = (b * p.hkv_s + kh) * p.max_kv + j0;
+                for (int k0 = 0; k0 < n; k0 += kAtKeys, ++it) {
+                    if (!waited && j0 + k0 + kAtKeys > pos) {   // holds the position just written
+                        pdl_wait();
+                        waited = true;
+                    }
+                    const int sl = it % kAtRing;
+                    if (!mbar_wait(&empty[sl], ((it / kAtRing) & 1) ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[sl], (uint32_t)S::STAGE);
+                    unsigned char* st = ring + sl * kAtMaxStage;
+#pragma unroll
+                    for (int h = 0; h < S::NB; ++h) {
+                        tma_load_2d(st + h * S::BOX, &A.tk[r], h * 64, row0 + k0, &full[sl], pol);
+                        tma_load_2d(st + (S::NB + h) * S::BOX, &A.tv[r], h * 64, row0 + k0, &full[sl], pol);
+                    }
+                }
+            }
+            pdl_trigger();
+            if (!ok || *abort_flag) {
+                volatile int no_abort = 0;
+                const uint32_t first = it > (uint32_t)kAtRing ? it - kAtRing : 0u;
+                for (uint32_t k = first; k < it; ++k)
+                    mbar_wait(&full[k % kAtRing], (k / kAtRing) & 1, &no_abort, nullptr);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers
+    pdl_wait();
+    const int grp = warp >> 2, wq = warp & 3;
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;
+    if (tid < kTMax) s_pos[tid] = tid < p.B ? p.pos[tid] : 0;
+    consumer_sync(kConsumers);
+    const uint32_t ring_u32 = smem_u32(ring);
+    const int q0 = 2 * t, q1 = 2 * t + 1;                 // the two queries of this lane's fragments
+    uint32_t it_unit = 0;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        const int c = u % p.n_chunks, gi = u / p.n_chunks;
+        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+        const int pos = s_pos[b];
+        const int Lk = min(pos + 1, p.max_kv);
+        const int j0 = c * kAttnChunk;
+        const int n = max(0, min(Lk - j0, kAttnChunk));
+        const int nblk = (n + kAtKeys - 1) / kAtKeys;
+
+        // B operand of S^T = K Q^T: query g, head-dim pairs (16ks + 2t, +1) and (16ks + 8 + 2t, +1)
+        uint32_t qb[KS][2];
+        {
+            const float* qp = p.q + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (g < G) {
+                    const float2 a = *reinterpret_cast<const float2*>(qp + 16 * ks + 2 * t);
+                    const float2 c2 = *reinterpret_cast<const float2*>(qp + 16 * ks + 8 + 2 * t);
+                    qb[ks][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+                    qb[ks][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
+                } else {
+                    qb[ks][0] = qb[ks][1] = 0u;
+                }
+            }
+        }
+        float o[KS][4];
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        for (int blk = grp; blk < nblk; blk += 2) {
+            const uint32_t it = it_unit + blk;
+            const int sl = it % kAtRing;
+            mbar_wait(&full[sl], (it / kAtRing) & 1, abort_flag, p.status);
+            __syncwarp();                        // lanes leave the wait loop independently
+            const uint32_t kpart = ring_u32 + sl * kAtMaxStage, vpart = kpart + S::NB * S::BOX;
+            const int kb = blk * kAtKeys + 16 * wq;          // this warp's first key, relative to the chunk
+            // ---- S^T for 16 keys x 8 queries
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(at_addr<D>(kpart, 16 * wq + rr + 8 * (mi & 1), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            }
+            // ---- online softmax per query over this warp's keys (rows g and g + 8)
+            const bool v0 = kb + g < n, v1 = kb + g + 8 < n;
+            const float x00 = v0 ? sc[0] : -INFINITY, x01 = v0 ? sc[1] : -INFINITY;
+            const float x10 = v1 ? sc[2] : -INFINITY, x11 = v1 ? sc[3] : -INFINITY;
+            float mq0 = fmaxf(x00, x10), mq1 = fmaxf(x01, x11);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mq0 = fmaxf(mq0, __shfl_xor_sync(0xffffffffu, mq0, off));
+                mq1 = fmaxf(mq1, __shfl_xor_sync(0xffffffffu, mq1, off));
+            }
+            const float n0 = fmaxf(m0, mq0), n1 = fmaxf(m1, mq1);
+            const float al0 = (n0 == -INFINITY) ? 1.f : expf(m0 - n0);
+            const float al1 = (n1 == -INFINITY) ? 1.f : expf(m1 - n1);
+            const float p00 = (x00 == -INFINITY) ? 0.f : expf(x00 - n0);
+            const float p10 = (x10 == -INFINITY) ? 0.f : expf(x10 - n0);
+            const float p01 = (x01 == -INFINITY) ? 0.f : expf(x01 - n1);
+            const float p11 = (x11 == -INFINITY) ? 0.f : expf(x11 - n1);
+            float ps0 = p00 + p10, ps1 = p01 + p11;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+                ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+            }
+            l0 = l0 * al0 + ps0;
+            l1 = l1 * al1 + ps1;
+            m0 = n0;
+            m1 = n1;
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+                o[dt][0] *= al0;
+                o[dt][1] *= al1;
+                o[dt][2] *= al0;
+                o[dt][3] *= al1;
+            }
+            // ---- O^T += V^T P^T; P^T fragments: (keys 2t, 2t+1 | 8+2t, 9+2t ; query g)
+            const uint32_t pb0 = movmatrix_t(pack_bf16x2(p00, p01));
+            const uint32_t pb1 = movmatrix_t(pack_bf16x2(p10, p11));
+            const uint32_t mlo = (kb + 2 * t < n ? 0x0000FFFFu : 0u) | (kb + 2 * t + 1 < n ? 0xFFFF0000u : 0u);
+            const uint32_t mhi = (kb + 8 + 2 * t < n ? 0x0000FFFFu : 0u) | (kb + 9 + 2 * t < n ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(at_addr<D>(vpart, 16 * wq + rr + 8 * (mi >> 1), 2 * dt + (mi & 1)), a0, a1, a2, a3);
+                mma_bf16_16816(o[dt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sl]);
+        }
+        it_unit += nblk;
+
+        // ---- merge the eight warps: common max, then a fixed tree of sums
+        if (g == 0) {
+            s_ml[(warp * kMaxGroup + q0) * 2] = m0;
+            s_ml[(warp * kMaxGroup + q0) * 2 + 1] = l0;
+            s_ml[(warp * kMaxGroup + q1) * 2] = m1;
+            s_ml[(warp * kMaxGroup + q1) * 2 + 1] = l1;
+        }
+        consumer_sync(kConsumers);
+        float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            M0 = fmaxf(M0, s_ml[(w * kMaxGroup + q0) * 2]);
+            M1 = fmaxf(M1, s_ml[(w * kMaxGroup + q1) * 2]);
+        }
+        const float c0 = (m0 == -INFINITY) ? 0.f : expf(m0 - M0);
+        const float c1 = (m1 == -INFINITY) ? 0.f : expf(m1 - M1);
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) {
+            o[dt][0] *= c0;
+            o[dt][1] *= c1;
+            o[dt][2] *= c0;
+            o[dt][3] *= c1;
+        }
+        // round 1: warps 4-7 -> 0-3; round 2: 2,3 -> 0,1; round 3: 1 -> 0
+        for (int half = 4; half >= 1; half >>= 1) {
+            if (warp >= half && warp < 2 * half) {
+                float* dst = red + (warp - half) * kAtSlot;
+#pragma unroll
+                for (int dt = 0; dt < KS; ++dt) {
+                    if (q0 < G) {
+                        dst[q0 * D + 16 * dt + g] = o[dt][0];
+                        dst[q0 * D + 16 * dt + g + 8] = o[dt][2];
+                    }
+                    if (q1 < G) {
+                        dst[q1 * D + 16 * dt + g] = o[dt][1];
+                        dst[q1 * D + 16 * dt + g + 8] = o[dt][3];
+                    }
+                }
+            }
+            consumer_sync(kConsumers);
+            if (warp < half) {
+                const float* src = red + warp * kAtSlot;
+#pragma unroll
+                for (int dt = 0; dt < KS; ++dt) {
+                    if (q0 < G) {
+                        o[dt][0] += src[q0 * D + 16 * dt + g];
+                        o[dt][2] += src[q0 * D + 16 * dt + g + 8];
+                    }
+                    if (q1 < G) {
+                        o[dt][1] += src[q1 * D + 16 * dt + g];
+                        o[dt][3] += src[q1 * D + 16 * dt + g + 8];
+                    }
+                }
+            }
+            consumer_sync(kConsumers);
+        }
+        if (warp == 0 && (unsigned)u < p.part_units) {
+            float* mine = p.part + (size_t)u * G * (D + 2);
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+                if (q0 < G) {
+                    mine[q0 * D + 16 * dt + g] = o[dt][0];
+                    mine[q0 * D + 16 * dt + g + 8] = o[dt][2];
+                }
+                if (q1 < G) {
+                    mine[q1 * D + 16 * dt + g] = o[dt][1];
+                    mine[q1 * D + 16 * dt + g + 8] = o[dt][3];
+                }
+            }
+            if (g == 0) {
+                float L0 = 0.f, L1 = 0.f;
+                for (int w = 0; w < 8; ++w) {
+                    const float mw0 = s_ml[(w * kMaxGroup + q0) * 2], mw1 = s_ml[(w * kMaxGroup + q1) * 2];
+                    if (mw0 != -INFINITY) L0 += s_ml[(w * kMaxGroup + q0) * 2 + 1] * expf(mw0 - M0);
+                    if (mw1 != -INFINITY) L1 += s_ml[(w * kMaxGroup + q1) * 2 + 1] * expf(mw1 - M1);
+                }
+                if (q0 < G) {
+                    mine[G * D + q0] = M0;
+                    mine[G * D + G + q0] = L0;
+                }
+                if (q1 < G) {
+                    mine[G * D + q1] = M1;
+                    mine[G * D + G + q1] = L1;
+                }
+            }
+        }
+        consumer_sync(kConsumers);               // s_ml and red are reused by the next unit
+    }
+}
+
 // Combines the split-KV chunk partials of one (shard, sequence, KV head)
 // group in chunk order with log-sum-exp weights; one CTA per group.
 template <int D>
@@ -1355,9 +1692,844 @@ cudaError_t launch_attn_combine(const AttnDecodeParams& p, cudaStream_t s) {
     return launch_small_pdl(fn, args, p.N * p.B * p.hkv_s, 256, s);
 }
 
+template <int D>
+static cudaError_t launch_attn_tc(const AttnDecodeParams& p, cudaStream_t s) {
+    using S = AtShape<D>;
+    const size_t smem = attn_tc_smem();
+    static bool set = false;
+    if (!set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        set = true;
+    }
+    if ((p.hq_s / p.hkv_s) * D > kAtSlot) return cudaErrorInvalidValue;
+    TmaAttnArgs A;
+    memset(&A, 0, sizeof A);
+    A.p = p;
+    const long rows = (long)p.max_batch * p.hkv_s * p.max_kv;
+    for (int r = 0; r < p.N; ++r) {
+        cudaError_t e = tensor_map_2d(p.kcache[r], D, rows, S::PT, kAtKeys, 0, &A.tk[r]);
+        if (e == cudaSuccess) e = tensor_map_2d(p.vcache[r], D, rows, S::PT, kAtKeys, 0, &A.tv[r]);
+        if (e != cudaSuccess) return e;
+    }
+    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
+    const int grid = U < kSMs ? U : kSMs;
+    void* args[] = {&A};
+    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_tc_kernel<D>), args, grid, smem, s, kStreamThreads);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s) {
-    if (dtype == TP_BF16) return p.d == 64 ? launch_attn_stream_g<64>(p, s) : launch_attn_stream_g<128>(p, s);
+    if (dtype == TP_BF16) return p.d == 64 ? launch_attn_tc<64>(p, s) : launch_attn_tc<128>(p, s);
     return p.d == 64 ? launch_attn_t<float, 64>(p, s) : launch_attn_t<float, 128>(p, s);
+}
+
+
+// ===========================================================================
+// The whole decode step in one persistent launch (bf16).
+//
+// One CTA per SM runs every stage of the block as a phase:
+//   NORM -> QKV (+RoPE, KV append) -> ATTN (split-KV partials) -> COMBINE
+//   -> O_PROJ (partials) -> REDUCE (h, next norm operands) -> GATE_UP
+//   (+SwiGLU) -> DOWN (partials) -> REDUCE (y)
+// separated by grid barriers (a sense-reversing counter in the workspace,
+// every wait bounded). The producer thread streams the data of later
+// phases that does not depend on earlier ones -- every weight box, and every
+// K/V block except the one holding the new position -- through the same
+// 5-stage ring while the consumers are still in an earlier phase or waiting
+// at a barrier; only the activation boxes (and the new K/V rows) wait for
+// the barrier that publishes them. So HBM keeps streaming across phase
+// boundaries and no kernel boundary, launch gap or ramp remains inside the
+// step. The phases compute exactly what the separate kernels compute.
+// ===========================================================================
+
+namespace {
+constexpr int kSkRing = 5;
+constexpr int kSkStage = kGemvStageBytes;               // 36 KB: 2 weight boxes + activation box, or K+V of 64 keys
+constexpr int kSkPhases = 8;                            // barriers inside a step
+constexpr int kSkMaxPend = kSkRing;
+static_assert(kGemvStageBytes == kAtMaxStage, "the two stage formats share one slot size");
+}  // namespace
+
+struct StepArgs {
+    CUtensorMap wm[4][TP_MAX_SHARDS];       // weights of qkv, o, gate_up, down (boxes kBoxK x 32)
+    CUtensorMap xm[4];                      // their activation operands (boxes kBoxK x 8)
+    CUtensorMap tk[TP_MAX_SHARDS];          // K / V caches (boxes 72 or 64 x 64 keys)
+    CUtensorMap tv[TP_MAX_SHARDS];
+    GemvParams g[4];                        // qkv, o, gate_up, down
+    AttnDecodeParams a;
+    NormPrepParams np;
+    unsigned long long* bar;                // grid-barrier arrival counter (only grows)
+    unsigned long long* stamps;             // optional [grid][kStepStamps]: start, 8 barrier arrivals, end (ns)
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier k of a step has passed once the arrival counter reaches
+// base + k * gridDim.x. The counter only grows (by kSkPhases * gridDim.x per
+// step, every CTA arriving at every barrier even after an error), so `base`
+// is the multiple of that amount at or below the value read at the start.
+__device__ __forceinline__ bool sk_passed(const unsigned long long* bar, unsigned long long base, unsigned k) {
+    return ld_acquire_u64(bar) >= base + (unsigned long long)k * gridDim.x;
+}
+
+__device__ __forceinline__ bool sk_wait_gen(const unsigned long long* bar, unsigned long long base, unsigned k,
+                                            volatile int* abort, int* status) {
+    if (sk_passed(bar, base, k)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (sk_passed(bar, base, k)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            set_status(status, TP_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Consumer side of grid barrier k: every consumer thread of the CTA has
+// finished the phase; thread 0 arrives with a release reduction (no reply
+// to wait for) and polls the counter with acquire loads.
+__device__ __forceinline__ void sk_barrier(unsigned long long* bar, unsigned long long base, unsigned k,
+                                           volatile int* abort, int* status, unsigned long long* stamp) {
+    consumer_sync(kConsumers);
+    if (threadIdx.x == 0) {
+        if (stamp) *stamp = global_ns();
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+        sk_wait_gen(bar, base, k, abort, status);
+    }
+    consumer_sync(kConsumers);
+}
+
+// ---- producer helpers -------------------------------------------------------
+
+// Stages whose activation box waits for a barrier, oldest first.
+struct SkPend {
+    int n;
+    uint32_t stage[kSkMaxPend];
+    int slot[kSkMaxPend], x[kSkMaxPend], y[kSkMaxPend], map[kSkMaxPend];
+    unsigned need[kSkMaxPend];
+};
+
+// Issues every pending activation box whose barrier has passed, waiting for
+// the barriers in order (oldest first).
+__device__ __forceinline__ bool sk_flush(SkPend& pd, const StepArgs& A, unsigned char* ring, uint64_t* full,
+                                         unsigned long long gen0, volatile int* abort, int* status) {
+    bool ok = true;
+    for (int i = 0; i < pd.n; ++i) {
+        if (ok) ok = sk_wait_gen(A.bar, gen0, pd.need[i], abort, status);
+        // the activations were written by other CTAs' ordinary stores
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        // issued even after a failed wait: the stage's byte count must complete
+        tma_load_2d_keep(ring + pd.slot[i] * kSkStage + 2 * kBoxBytes, &A.xm[pd.map[i]], pd.x[i], pd.y[i],
+                         &full[pd.slot[i]]);
+    }
+    pd.n = 0;
+    return ok;
+}
+
+// Before the producer reuses the slot of stage `it` (last held by stage
+// it - kSkRing): if that stage is still pending, its consumers cannot release
+// the slot until its activation box is issued.
+__device__ __forceinline__ void sk_before_reuse(SkPend& pd, uint32_t it, const StepArgs& A, unsigned char* ring,
+                                                uint64_t* full, unsigned long long gen0, volatile int* abort,
+                                                int* status) {
+    if (pd.n > 0 && pd.stage[0] + kSkRing <= it) sk_flush(pd, A, ring, full, gen0, abort, status);
+}
+
+// Producer of one projection phase: weight boxes at once, the activation box
+// once barrier `need` has passed.
+__device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, const StepArgs& A, unsigned char* ring,
+                                                uint64_t* full, uint64_t* empty, uint32_t& it, SkPend& pd,
+                                                unsigned long long gen0, volatile int* abort, uint64_t pol) {
+    const GemvParams& p = A.g[wi];
+    const int U = p.shape.units();
+    const int kc = p.shape.kc;
+    const int spu = (kc + kBoxK - 1) / kBoxK;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        int gi, r, tb, chunk;
+        decode_unit(p, epi, u, gi, r, tb, chunk);
+        const int rowa = tile_row(epi, tb, 0, p.head_dim, p.ffn_s);
+        const int rowb = tile_row(epi, tb, 32, p.head_dim, p.ffn_s);
+        const int k0 = chunk * kc;
+        for (int st = 0; st < spu; ++st, ++it) {
+            const int sl = it % kSkRing;
+            sk_before_reuse(pd, it, A, ring, full, gen0, abort, p.status);
+            if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
+            mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
+            unsigned char* dst = ring + sl * kSkStage;
+            tma_load_2d(dst, &A.wm[wi][r], k0 + st * kBoxK, rowa, &full[sl], pol);
+            tma_load_2d(dst + kBoxBytes, &A.wm[wi][r], k0 + st * kBoxK, rowb, &full[sl], pol);
+            if (pd.n == 0 && sk_passed(A.bar, gen0, need)) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                tma_load_2d_keep(dst + 2 * kBoxBytes, &A.xm[wi], k0 + st * kBoxK, r * kTMax, &full[sl]);
+            } else {
+                pd.stage[pd.n] = it;
+                pd.slot[pd.n] = sl;
+                pd.x[pd.n] = k0 + st * kBoxK;
+                pd.y[pd.n] = r * kTMax;
+                pd.map[pd.n] = wi;
+                pd.need[pd.n] = need;
+                ++pd.n;
+            }
+        }
+    }
+    return true;
+}
+
+template <int D>
+__device__ __forceinline__ bool sk_produce_attn(unsigned need, const StepArgs& A, unsigned char* ring, uint64_t* full,
+                                                uint64_t* empty, uint32_t& it, SkPend& pd, unsigned long long gen0,
+                                                volatile int* abort, uint64_t pol, const int* posv) {
+    using S = AtShape<D>;
+    const AttnDecodeParams& p = A.a;
+    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
+    bool passed = false;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        const int c = u % p.n_chunks, gi = u / p.n_chunks;
+        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+        const int pos = posv[b];
+        const int Lk = min(pos + 1, p.max_kv);
+        const int j0 = c * kAttnChunk;
+        const int n = max(0, min(Lk - j0, kAttnChunk));
+        const int row0 = (b * p.hkv_s + kh) * p.max_kv + j0;
+        for (int k0 = 0; k0 < n; k0 += kAtKeys, ++it) {
+            // the block holding the new position is written by the QKV phase
+            if (!passed && j0 + k0 + kAtKeys > pos) {
+                sk_flush(pd, A, ring, full, gen0, abort, p.status);
+                sk_wait_gen(A.bar, gen0, need, abort, p.status);
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                passed = true;
+            }
+            const int sl = it % kSkRing;
+            sk_before_reuse(pd, it, A, ring, full, gen0, abort, p.status);
+            if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
+            mbar_arrive_expect_tx(&full[sl], (uint32_t)S::STAGE);
+            unsigned char* st = ring + sl * kSkStage;
+#pragma unroll
+            for (int h = 0; h < S::NB; ++h) {
+                tma_load_2d(st + h * S::BOX, &A.tk[r], h * 64, row0 + k0, &full[sl], pol);
+                tma_load_2d(st + (S::NB + h) * S::BOX, &A.tv[r], h * 64, row0 + k0, &full[sl], pol);
+            }
+        }
+    }
+    return true;
+}
+
+// ---- consumer phases ---------------------------------------------------------
+
+// RMSNorm operands: x * gamma_r (bf16) for every shard and per-256-block
+// sums of squares; one (token, 256-block) item per warp, all SMs.
+__device__ __forceinline__ void sk_norm(const NormPrepParams& p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nkb = (p.H + 255) / 256;
+    const int items = kTMax * nkb;
+    for (int item = blockIdx.x * 8 + warp; item < items; item += gridDim.x * 8) {
+        const int t = item / nkb, kb = item - t * nkb;
+        float a = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = kb * 256 + h * 128 + lane * 4;
+            const bool in = k < p.H;
+            const float4 v = (t < p.T && in) ? *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + k)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < p.N && in; ++r) {
+                const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma[r] + k));
+                uint2 pk;
+                pk.x = pack_bf16x2(v.x * gm.x, v.y * gm.y);
+                pk.y = pack_bf16x2(v.z * gm.z, v.w * gm.w);
+                *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xg) + ((size_t)r * kTMax + t) * p.H + k) = pk;
+            }
+            a = fmaf(v.x, v.x, a);
+            a = fmaf(v.y, v.y, a);
+            a = fmaf(v.z, v.z, a);
+            a = fmaf(v.w, v.w, a);
+        }
+        a = warp_sum(a);
+        if (lane == 0) p.ss[kb * kTMax + t] = a;
+    }
+}
+
+// One projection phase on the consumer side (the units of this CTA).
+template <int EPI>
+__device__ __forceinline__ void sk_gemv(const GemvParams& p, unsigned char* ring, uint64_t* full, uint64_t* empty,
+                                        volatile int* abort, uint32_t& it, float* tile, float* ss, int* s_pos,
+                                        float* s_bias) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int U = p.shape.units();
+    const int kc = p.shape.kc;
+    const int spu = (kc + kBoxK - 1) / kBoxK;
+    const int wm = warp & 3, wk = warp >> 2;
+    const int g = lane >> 2, tq = lane & 3;
+    const int box = wm >> 1, brow = 16 * (wm & 1) + g;
+    const int T = p.T;
+    if ((int)blockIdx.x >= U) return;
+    if (EPI == EPI_QKV_ROPE && tid < kTMax) s_pos[tid] = tid < T ? p.pos[tid] : 0;
+    if (EPI != EPI_ROWPAR) {
+        float a = 0.f;                                 // warp t: token t
+        if (warp < T)
+            for (int q = lane; q < p.n_ss_tiles; q += 32) a += p.ss_tiles[q * kTMax + warp];
+        a = warp_sum(a);
+        if (lane == 0) ss[warp] = a;
+    }
+    consumer_sync(kConsumers);
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        int gi, r, tb, chunk;
+        decode_unit(p, EPI, u, gi, r, tb, chunk);
+        float bias_v = 0.f;
+        if (EPI == EPI_QKV_ROPE && tid < kTileRows && p.bias[r])
+            bias_v = p.bias[r][tile_row(EPI_QKV_ROPE, tb, tid, p.head_dim, 0)];
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int st = 0; st < spu; ++st, ++it) {
+            const int sl = it % kSkRing;
+            mbar_wait(&full[sl], (it / kSkRing) & 1, abort, p.status);
+            __syncwarp();
+            const int steps_here = min(kBoxK / kKStep, (kc - st * kBoxK) / kKStep);
+            const unsigned char* stage = ring + sl * kSkStage;
+            const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
+            const unsigned char* wB = wA + 8 * (kBoxK * 2);
+            const unsigned char* px = stage + 2 * kBoxBytes + g * (kBoxK * 2) + tq * 16;
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int step = wk + 2 * s2;
+                if (step < steps_here) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
+                        const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
+                        const uint4 xv = *reinterpret_cast<const uint4*>(px + step * 128 + h * 64);
+                        mma_bf16_16816(c, a.x, b.x, a.y, b.y, xv.x, xv.y);
+                        mma_bf16_16816(c, a.z, b.z, a.w, b.w, xv.z, xv.w);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sl]);
+        }
+        const int i0 = (16 * wm + g) * kTMax + 2 * tq, i1 = (16 * wm + g + 8) * kTMax + 2 * tq;
+        if (wk == 0) {
+            tile[i0] = c[0];
+            tile[i0 + 1] = c[1];
+            tile[i1] = c[2];
+            tile[i1 + 1] = c[3];
+        }
+        if (EPI == EPI_QKV_ROPE && tid < kTileRows) s_bias[tid] = bias_v;
+        consumer_sync(kConsumers);
+        if (wk == 1) {
+            tile[i0] += c[0];
+            tile[i0 + 1] += c[1];
+            tile[i1] += c[2];
+            tile[i1 + 1] += c[3];
+        }
+        consumer_sync(kConsumers);
+        if (EPI == EPI_ROWPAR) {
+            float* mine = p.part + (size_t)u * kPartStride;
+            for (int i = tid * 4; i < kTileRows * kTMax; i += kConsumers * 4)
+                *reinterpret_cast<float4*>(mine + i) = *reinterpret_cast<const float4*>(tile + i);
+        } else if (EPI == EPI_SWIGLU) {
+            bf16* out = reinterpret_cast<bf16*>(p.act_out);
+            const float inv_k = 1.0f / (float)p.K;
+            for (int i = tid; i < 32 * T; i += kConsumers) {
+                const int t = i >> 5, j = i & 31;
+                const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
+                const float gt = tile[j * kTMax + t] * rinv;
+                const float up = tile[(j + 32) * kTMax + t] * rinv;
+                out[((size_t)r * kTMax + t) * p.ffn_s + tb * 32 + j] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+            }
+        } else {
+            const int d = p.head_dim, half = d >> 1;
+            const float inv_k = 1.0f / (float)p.K;
+            for (int i = tid; i < 32 * T; i += kConsumers) {
+                const int t = i >> 5, j = i & 31;
+                const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
+                const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
+                const int head = rowA / d, ii = rowA - head * d;
+                float va = tile[j * kTMax + t] * rinv + s_bias[j];
+                float vb = tile[(j + 32) * kTMax + t] * rinv + s_bias[j + 32];
+                const int pos = s_pos[t];
+                if (head < p.hq_s + p.hkv_s) {
+                    float cs, sn;
+                    sincosf((float)pos * exp2f(-(2.0f * ii / d) * (float)p.log2_theta), &sn, &cs);
+                    const float ra = va * cs - vb * sn, rb = va * sn + vb * cs;
+                    va = ra;
+                    vb = rb;
+                }
+                if (head < p.hq_s) {
+                    float* q = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
+                    q[0] = va;
+                    q[half] = vb;
+                } else {
+                    const bool is_k = head < p.hq_s + p.hkv_s;
+                    const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
+                    if (pos < 0 || pos >= p.max_kv) {
+                        set_status(p.status, TP_ERR_CAPACITY);
+                        continue;
+                    }
+                    bf16* cache = reinterpret_cast<bf16*>(is_k ? p.kcache[r] : p.vcache[r]);
+                    bf16* dst = cache + (((size_t)t * p.hkv_s + kvh) * p.max_kv + pos) * d + ii;
+                    dst[0] = __float2bfloat16_rn(va);
+                    dst[half] = __float2bfloat16_rn(vb);
+                }
+            }
+        }
+        consumer_sync(kConsumers);
+    }
+}
+
+// Attention phase on the consumer side: the units of attn_tc_kernel, with
+// every warp waiting for and releasing every stage (the ring is shared with
+// the projection phases, whose stages all eight warps release).
+template <int D>
+__device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char* ring, uint64_t* full,
+                                        uint64_t* empty, volatile int* abort, uint32_t& it_unit, float* red,
+                                        float* s_ml, const int* s_pos) {
+    using S = AtShape<D>;
+    constexpr int KS = D / 16;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.hq_s / p.hkv_s;
+    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
+    const int grp = warp >> 2, wq = warp & 3;
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t ring_u32 = smem_u32(ring);
+    const int q0 = 2 * t, q1 = 2 * t + 1;
+    (void)tid;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        const int c = u % p.n_chunks, gi = u / p.n_chunks;
+        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+        const int pos = s_pos[b];
+        const int Lk = min(pos + 1, p.max_kv);
+        const int j0 = c * kAttnChunk;
+        const int n = max(0, min(Lk - j0, kAttnChunk));
+        const int nblk = (n + kAtKeys - 1) / kAtKeys;
+        uint32_t qb[KS][2];
+        {
+            const float* qp = p.q + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (g < G) {
+                    const float2 a = *reinterpret_cast<const float2*>(qp + 16 * ks + 2 * t);
+                    const float2 c2 = *reinterpret_cast<const float2*>(qp + 16 * ks + 8 + 2 * t);
+                    qb[ks][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+                    qb[ks][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
+                } else {
+                    qb[ks][0] = qb[ks][1] = 0u;
+                }
+            }
+        }
+        float o[KS][4];
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        for (int blk = 0; blk < nblk; ++blk) {
+            const uint32_t it = it_unit + blk;
+            const int sl = it % kSkRing;
+            mbar_wait(&full[sl], (it / kSkRing) & 1, abort, p.status);
+            __syncwarp();
+            if ((blk & 1) == grp) {
+                const uint32_t kpart = ring_u32 + sl * kSkStage, vpart = kpart + S::NB * S::BOX;
+                const int kb = blk * kAtKeys + 16 * wq;
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(at_addr<D>(kpart, 16 * wq + rr + 8 * (mi & 1), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                    mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+                const bool v0 = kb + g < n, v1 = kb + g + 8 < n;
+                const float x00 = v0 ? sc[0] : -INFINITY, x01 = v0 ? sc[1] : -INFINITY;
+                const float x10 = v1 ? sc[2] : -INFINITY, x11 = v1 ? sc[3] : -INFINITY;
+                float mq0 = fmaxf(x00, x10), mq1 = fmaxf(x01, x11);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mq0 = fmaxf(mq0, __shfl_xor_sync(0xffffffffu, mq0, off));
+                    mq1 = fmaxf(mq1, __shfl_xor_sync(0xffffffffu, mq1, off));
+                }
+                const float n0 = fmaxf(m0, mq0), n1 = fmaxf(m1, mq1);
+                const float al0 = (n0 == -INFINITY) ? 1.f : expf(m0 - n0);
+                const float al1 = (n1 == -INFINITY) ? 1.f : expf(m1 - n1);
+                const float p00 = (x00 == -INFINITY) ? 0.f : expf(x00 - n0);
+                const float p10 = (x10 == -INFINITY) ? 0.f : expf(x10 - n0);
+                const float p01 = (x01 == -INFINITY) ? 0.f : expf(x01 - n1);
+                const float p11 = (x11 == -INFINITY) ? 0.f : expf(x11 - n1);
+                float ps0 = p00 + p10, ps1 = p01 + p11;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+                    ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+                }
+                l0 = l0 * al0 + ps0;
+                l1 = l1 * al1 + ps1;
+                m0 = n0;
+                m1 = n1;
+#pragma unroll
+                for (int dt = 0; dt < KS; ++dt) {
+                    o[dt][0] *= al0;
+                    o[dt][1] *= al1;
+                    o[dt][2] *= al0;
+                    o[dt][3] *= al1;
+                }
+                const uint32_t pb0 = movmatrix_t(pack_bf16x2(p00, p01));
+                const uint32_t pb1 = movmatrix_t(pack_bf16x2(p10, p11));
+                const uint32_t mlo = (kb + 2 * t < n ? 0x0000FFFFu : 0u) | (kb + 2 * t + 1 < n ? 0xFFFF0000u : 0u);
+                const uint32_t mhi = (kb + 8 + 2 * t < n ? 0x0000FFFFu : 0u) | (kb + 9 + 2 * t < n ? 0xFFFF0000u : 0u);
+#pragma unroll
+                for (int dt = 0; dt < KS; ++dt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(at_addr<D>(vpart, 16 * wq + rr + 8 * (mi >> 1), 2 * dt + (mi & 1)), a0, a1, a2, a3);
+                    mma_bf16_16816(o[dt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sl]);
+        }
+        it_unit += nblk;
+        if (g == 0) {
+            s_ml[(warp * kMaxGroup + q0) * 2] = m0;
+            s_ml[(warp * kMaxGroup + q0) * 2 + 1] = l0;
+            s_ml[(warp * kMaxGroup + q1) * 2] = m1;
+            s_ml[(warp * kMaxGroup + q1) * 2 + 1] = l1;
+        }
+        consumer_sync(kConsumers);
+        float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            M0 = fmaxf(M0, s_ml[(w * kMaxGroup + q0) * 2]);
+            M1 = fmaxf(M1, s_ml[(w * kMaxGroup + q1) * 2]);
+        }
+        const float c0 = (m0 == -INFINITY) ? 0.f : expf(m0 - M0);
+        const float c1 = (m1 == -INFINITY) ? 0.f : expf(m1 - M1);
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) {
+            o[dt][0] *= c0;
+            o[dt][1] *= c1;
+            o[dt][2] *= c0;
+            o[dt][3] *= c1;
+        }
+        for (int half = 4; half >= 1; half >>= 1) {
+            if (warp >= half && warp < 2 * half) {
+                float* dst = red + (warp - half) * kAtSlot;
+#pragma unroll
+                for (int dt = 0; dt < KS; ++dt) {
+                    if (q0 < G) {
+                        dst[q0 * D + 16 * dt + g] = o[dt][0];
+                        dst[q0 * D + 16 * dt + g + 8] = o[dt][2];
+                    }
+                    if (q1 < G) {
+                        dst[q1 * D + 16 * dt + g] = o[dt][1];
+                        dst[q1 * D + 16 * dt + g + 8] = o[dt][3];
+                    }
+                }
+            }
+            consumer_sync(kConsumers);
+            if (warp < half) {
+                const float* src = red + warp * kAtSlot;
+#pragma unroll
+                for (int dt = 0; dt < KS; ++dt) {
+                    if (q0 < G) {
+                        o[dt][0] += src[q0 * D + 16 * dt + g];
+                        o[dt][2] += src[q0 * D + 16 * dt + g + 8];
+                    }
+                    if (q1 < G) {
+                        o[dt][1] += src[q1 * D + 16 * dt + g];
+                        o[dt][3] += src[q1 * D + 16 * dt + g + 8];
+                    }
+                }
+            }
+            consumer_sync(kConsumers);
+        }
+        if (warp == 0 && (unsigned)u < p.part_units) {
+            float* mine = p.part + (size_t)u * G * (D + 2);
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+                if (q0 < G) {
+                    mine[q0 * D + 16 * dt + g] = o[dt][0];
+                    mine[q0 * D + 16 * dt + g + 8] = o[dt][2];
+                }
+                if (q1 < G) {
+                    mine[q1 * D + 16 * dt + g] = o[dt][1];
+                    mine[q1 * D + 16 * dt + g + 8] = o[dt][3];
+                }
+            }
+            if (g == 0) {
+                float L0 = 0.f, L1 = 0.f;
+                for (int w = 0; w < 8; ++w) {
+                    const float mw0 = s_ml[(w * kMaxGroup + q0) * 2], mw1 = s_ml[(w * kMaxGroup + q1) * 2];
+                    if (mw0 != -INFINITY) L0 += s_ml[(w * kMaxGroup + q0) * 2 + 1] * expf(mw0 - M0);
+                    if (mw1 != -INFINITY) L1 += s_ml[(w * kMaxGroup + q1) * 2 + 1] * expf(mw1 - M1);
+                }
+                if (q0 < G) {
+                    mine[G * D + q0] = M0;
+                    mine[G * D + G + q0] = L0;
+                }
+                if (q1 < G) {
+                    mine[G * D + q1] = M1;
+                    mine[G * D + G + q1] = L1;
+                }
+            }
+        }
+        consumer_sync(kConsumers);
+    }
+}
+
+// Split-KV combine: one (group, query head) item per warp, all SMs. Lanes
+// hold the chunk statistics (chunk = lane, lane + 32, ...), the warp forms
+// the common maximum and denominator, then each lane combines four output
+// elements at a time in chunk order.
+template <int D>
+__device__ __forceinline__ void sk_combine(const AttnDecodeParams& p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.hq_s / p.hkv_s, pstride = G * (D + 2);
+    const int n_groups = p.N * p.B * p.hkv_s;
+    const int nc = p.n_chunks;
+    for (int item = blockIdx.x * 8 + warp; item < n_groups * G; item += gridDim.x * 8) {
+        const int gi = item / G, gq = item - gi * G;
+        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+        const float* base = p.part + (size_t)gi * nc * pstride;
+        float M = -INFINITY;
+        for (int cc = lane; cc < nc; cc += 32) {
+            const float l = base[(size_t)cc * pstride + G * D + G + gq];
+            if (l > 0.f) M = fmaxf(M, base[(size_t)cc * pstride + G * D + gq]);
+        }
+        M = warp_max(M);
+        float den = 0.f;
+        for (int cc = lane; cc < nc; cc += 32) {
+            const float l = base[(size_t)cc * pstride + G * D + G + gq];
+            if (l > 0.f) den = fmaf(l, expf(base[(size_t)cc * pstride + G * D + gq] - M), den);
+        }
+        den = warp_sum(den);
+        const float inv = den > 0.f ? 1.0f / den : 0.f;
+        bf16* out = reinterpret_cast<bf16*>(p.out) + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + gq) * D;
+        for (int d0 = lane * 4; d0 < D; d0 += 128) {
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cc = 0; cc < nc; ++cc) {
+                const float* pc = base + (size_t)cc * pstride;
+                const float l = pc[G * D + G + gq];
+                const float w = l > 0.f ? expf(pc[G * D + gq] - M) : 0.f;
+                // the partial stride G*(D+2) floats need not be a multiple of 4: scalar loads
+                const float* pv = pc + gq * D + d0;
+                num.x = fmaf(pv[0], w, num.x);
+                num.y = fmaf(pv[1], w, num.y);
+                num.z = fmaf(pv[2], w, num.z);
+                num.w = fmaf(pv[3], w, num.w);
+            }
+            uint2 pk;
+            pk.x = pack_bf16x2(num.x * inv, num.y * inv);
+            pk.y = pack_bf16x2(num.z * inv, num.w * inv);
+            *reinterpret_cast<uint2*>(out + d0) = pk;
+        }
+    }
+}
+
+// Rank-ordered reduction of a row-parallel phase's partials: one 8-row slice
+// of a 64-row tile per warp, all SMs; lane = (row, token pair). Chunks are
+// summed in order within each rank, then ranks in order, then the residual.
+// With norm_out it writes the next norm's operands (y * gamma_r, bf16, every
+// shard) and per-(8-row slice, token) sums of squares.
+__device__ __forceinline__ void sk_reduce(const GemvParams& p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int upg = p.shape.units_per_group(), C = p.shape.chunks;
+    const int j8 = lane >> 2, tp = lane & 3;
+    for (int item = blockIdx.x * 8 + warp; item < p.shape.groups * 8; item += gridDim.x * 8) {
+        const int tb = item >> 3, sl = item & 7;
+        const int j = sl * 8 + j8;                     // row within the tile
+        const float* base = p.part + (size_t)tb * upg * kPartStride + j * kTMax + 2 * tp;
+        float2 v[kMaxGroupUnits];
+#pragma unroll
+        for (int q = 0; q < kMaxGroupUnits; ++q)
+            if (q < upg) v[q] = *reinterpret_cast<const float2*>(base + (size_t)q * kPartStride);
+        float2 total = make_float2(0.f, 0.f), pr = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kMaxGroupUnits; ++q) {
+            if (q < upg) {
+                const int cc = q % C;
+                pr = (cc == 0) ? v[q] : make_float2(pr.x + v[q].x, pr.y + v[q].y);
+                if (cc == C - 1) total = (q < C) ? pr : make_float2(total.x + pr.x, total.y + pr.y);
+            }
+        }
+        const int row = tb * kTileRows + j;
+        float sq[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = 2 * tp + e;
+            float yv = 0.f;
+            if (t < p.T) {
+                const size_t o = (size_t)t * p.rows + row;
+                yv = p.resid[o] + (e ? total.y : total.x);
+                p.y[o] = yv;
+                if (p.norm_out) {
+                    bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
+                    for (int r2 = 0; r2 < p.n_shards; ++r2)
+                        nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
+                }
+            }
+            sq[e] = yv * yv;
+        }
+        if (p.norm_out) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
+                sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
+            }
+            if (j8 == 0) {
+                p.ss_tiles_out[(size_t)item * kTMax + 2 * tp] = sq[0];
+                p.ss_tiles_out[(size_t)item * kTMax + 2 * tp + 1] = sq[1];
+            }
+        }
+    }
+}
+
+size_t decode_step_smem() {
+    // ring | red [4][kAtSlot] | s_ml [8][8][2] | tile [64][8] | ss, pos, bias, wsum
+    return 1024 + (size_t)kSkRing * kSkStage +
+           (size_t)(4 * kAtSlot + 8 * kMaxGroup * 2 + kTileRows * kTMax + kTMax + kTMax + 96 + 8) * 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kStreamThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs A) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kSkRing;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kSkRing);
+    unsigned long long* s_gen0 = reinterpret_cast<unsigned long long*>(smem + 16 * kSkRing + 8);
+    unsigned char* ring = smem + 1024;
+    float* red = reinterpret_cast<float*>(ring + kSkRing * kSkStage);
+    float* s_ml = red + 4 * kAtSlot;
+    float* tile = s_ml + 8 * kMaxGroup * 2;
+    float* ss = tile + kTileRows * kTMax;
+    int* s_pos = reinterpret_cast<int*>(ss + kTMax);
+    float* s_bias = reinterpret_cast<float*>(s_pos + kTMax);
+    float* wsum = s_bias + 96;
+    int* status = A.a.status;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < kSkRing; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumers / 32);
+        }
+        *abort_flag = (smem_u32(ring) & 127u) ? 1 : 0;
+        if (*abort_flag) set_status(status, TP_ERR_ALIGN);
+        // read before this CTA arrives anywhere: fewer than gridDim.x arrivals of
+        // this step can precede it
+        const unsigned long long per_step = (unsigned long long)kSkPhases * gridDim.x;
+        const unsigned long long c = ld_acquire_u64(A.bar);
+        *s_gen0 = c - c % per_step;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const unsigned long long gen0 = *s_gen0;
+
+    if (warp == kConsumers / 32) {                     // ---- producer
+        if (lane == 0 && !*abort_flag) {
+            const uint64_t pol = l2_evict_first_policy();
+            uint32_t it = 0;
+            SkPend pd;
+            pd.n = 0;
+            int posv[kTMax];
+            for (int b = 0; b < kTMax; ++b) posv[b] = b < A.a.B ? A.a.pos[b] : 0;
+            bool ok = sk_produce_gemv(EPI_QKV_ROPE, 0, 1, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            if (ok) ok = sk_produce_attn<D>(2, A, ring, full, empty, it, pd, gen0, abort_flag, pol, posv);
+            if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 1, 4, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            if (ok) ok = sk_produce_gemv(EPI_SWIGLU, 2, 6, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 3, 7, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            sk_flush(pd, A, ring, full, gen0, abort_flag, status);
+            // no copy may still be landing when the CTA exits
+            volatile int no_abort = 0;
+            const uint32_t first = it > (uint32_t)kSkRing ? it - kSkRing : 0u;
+            for (uint32_t k = first; k < it; ++k) mbar_wait(&full[k % kSkRing], (k / kSkRing) & 1, &no_abort, nullptr);
+        }
+        return;
+    }
+
+    // ---- consumers
+    unsigned long long* st = A.stamps && blockIdx.x < kMaxStepCtas ? A.stamps + (size_t)blockIdx.x * kStepStamps : nullptr;
+    if (st && tid == 0) st[0] = global_ns();
+    if (tid < kTMax) s_pos[tid] = tid < A.a.B ? A.a.pos[tid] : 0;
+    uint32_t it = 0;
+    sk_norm(A.np);
+    sk_barrier(A.bar, gen0, 1, abort_flag, status, st ? st + 1 : nullptr);
+    sk_gemv<EPI_QKV_ROPE>(A.g[0], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
+    sk_barrier(A.bar, gen0, 2, abort_flag, status, st ? st + 2 : nullptr);
+    if (tid < kTMax) s_pos[tid] = tid < A.a.B ? A.a.pos[tid] : 0;
+    consumer_sync(kConsumers);
+    sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_pos);
+    sk_barrier(A.bar, gen0, 3, abort_flag, status, st ? st + 3 : nullptr);
+    sk_combine<D>(A.a);
+    sk_barrier(A.bar, gen0, 4, abort_flag, status, st ? st + 4 : nullptr);
+    sk_gemv<EPI_ROWPAR>(A.g[1], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
+    sk_barrier(A.bar, gen0, 5, abort_flag, status, st ? st + 5 : nullptr);
+    sk_reduce(A.g[1]);
+    sk_barrier(A.bar, gen0, 6, abort_flag, status, st ? st + 6 : nullptr);
+    sk_gemv<EPI_SWIGLU>(A.g[2], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
+    sk_barrier(A.bar, gen0, 7, abort_flag, status, st ? st + 7 : nullptr);
+    sk_gemv<EPI_ROWPAR>(A.g[3], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
+    sk_barrier(A.bar, gen0, 8, abort_flag, status, st ? st + 8 : nullptr);
+    sk_reduce(A.g[3]);
+    if (st && tid == 0) st[kStepStamps - 1] = global_ns();
+}
+
+cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
+    const size_t smem = decode_step_smem();
+    const int D = P.a.d;
+    const void* fn = D == 64 ? reinterpret_cast<const void*>(decode_step_kernel<64>)
+                             : reinterpret_cast<const void*>(decode_step_kernel<128>);
+    static int grid_sz[2] = {0, 0};
+    const int which = D == 64 ? 0 : 1;
+    if (!grid_sz[which]) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 0, per_sm = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStreamThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        grid_sz[which] = sms;                          // one CTA per SM
+    }
+    StepArgs A;
+    memset(&A, 0, sizeof A);
+    const int epis[4] = {EPI_QKV_ROPE, EPI_ROWPAR, EPI_SWIGLU, EPI_ROWPAR};
+    (void)epis;
+    for (int i = 0; i < 4; ++i) {
+        const GemvParams& p = P.g[i];
+        A.g[i] = p;
+        for (int r = 0; r < p.n_shards; ++r) {
+            cudaError_t e = weight_tensor_map(p.W[r], p.K, p.rows, &A.wm[i][r]);
+            if (e != cudaSuccess) return e;
+        }
+        cudaError_t e = weight_tensor_map(p.xact, p.K, p.n_shards * kTMax, &A.xm[i], kTMax);
+        if (e != cudaSuccess) return e;
+    }
+    A.a = P.a;
+    A.np = P.np;
+    const long rows = (long)P.a.max_batch * P.a.hkv_s * P.a.max_kv;
+    for (int r = 0; r < P.a.N; ++r) {
+        const int pt = D == 128 ? AtShape<128>::PT : AtShape<64>::PT;
+        cudaError_t e = tensor_map_2d(P.a.kcache[r], D, rows, pt, kAtKeys, 0, &A.tk[r]);
+        if (e == cudaSuccess) e = tensor_map_2d(P.a.vcache[r], D, rows, pt, kAtKeys, 0, &A.tv[r]);
+        if (e != cudaSuccess) return e;
+    }
+    A.bar = P.bar;
+    A.stamps = P.stamps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_sz[which]);
+    cfg.blockDim = dim3(kStreamThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[] = {&A};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace tpk

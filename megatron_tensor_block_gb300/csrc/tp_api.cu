@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "tp_internal.h"
 
@@ -55,7 +56,8 @@ struct tp_plan_s {
     int attn_chunks = 0, attn_groups = 0;
     // workspace layout (byte offsets)
     size_t off_status = 0, off_cnt_qkv = 0, off_cnt_attn = 0, off_cnt_o = 0, off_cnt_gu = 0,
-           off_cnt_down = 0, ctrl_bytes = 0;
+           off_cnt_down = 0, off_step_bar = 0, ctrl_bytes = 0;
+    size_t off_stamps = 0;              // per-CTA phase end times of the decode step (profiling)
     size_t off_q = 0, off_attn_part = 0, off_attn_out = 0, off_h = 0, off_act = 0;
     size_t off_part_qkv = 0, off_part_o = 0, off_part_gu = 0, off_part_down = 0;
     size_t off_xg = 0, off_ss = 0, off_hg = 0, off_ss_tiles = 0;   // bf16 normalised operands
@@ -69,6 +71,7 @@ struct tp_plan_s {
     // measurement hook (tp_profile_stages)
     cudaEvent_t stage_ev[16] = {};
     int n_stage_ev = 0;
+    char* last_stamps_ws = nullptr;     // workspace of the last profiled decode step
 };
 
 static void stage_mark(tp_plan_t P, int i, cudaStream_t s) {
@@ -233,6 +236,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_cnt_o = take(sizeof(unsigned) * P->g_o.groups);
         P->off_cnt_gu = take(sizeof(unsigned) * P->g_gu.groups);
         P->off_cnt_down = take(sizeof(unsigned) * P->g_down.groups);
+        P->off_step_bar = take(sizeof(unsigned long long));
     }
     P->ctrl_bytes = off;
     if (dense) {
@@ -249,7 +253,8 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_xg = take((size_t)N * kTMax * H * 2);
         P->off_ss = take((size_t)(H / 256 + 1) * kTMax * 4);
         P->off_hg = take((size_t)N * kTMax * H * 2);
-        P->off_ss_tiles = take((size_t)(H / kTileRows) * kTMax * 4);
+        P->off_ss_tiles = take((size_t)(H / 8) * kTMax * 4);
+        P->off_stamps = take((size_t)kMaxStepCtas * kStepStamps * 8);
         P->ws_decode_end = off;
     }
     if (dense && d->dtype == TP_BF16) {
@@ -560,6 +565,102 @@ extern "C" tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t b
     return ok();
 }
 
+// bf16 decode: every stage in one persistent launch (the launch sequence of
+// the separate fp32 kernels below, as phases of one kernel).
+static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_kv_set* kv, const float* x, float* y,
+                                  const int32_t* pos, int B, char* ws, cudaStream_t s, const GemvParams& q,
+                                  const NormPrepParams& np) {
+    const tp_model_desc& d = P->d;
+    const tp_plan_info& I = P->info;
+    const int N = P->N, T = B, hd = (int)d.head_dim;
+    int* status = reinterpret_cast<int*>(ws + P->off_status);
+    DecodeStepParams st{};
+    st.np = np;
+    st.g[0] = q;
+
+    AttnDecodeParams& a = st.a;
+    a.q = q.q_out;
+    for (int r = 0; r < N; ++r) {
+        a.kcache[r] = kv->k[r];
+        a.vcache[r] = kv->v[r];
+    }
+    a.pos = pos;
+    a.N = N;
+    a.B = B;
+    a.hq_s = (int)I.hq_shard;
+    a.hkv_s = (int)I.hkv_shard;
+    a.d = hd;
+    a.max_kv = (int)d.max_kv;
+    a.max_batch = (int)d.max_batch;
+    a.n_chunks = P->attn_chunks;
+    a.scale = (float)(1.0 / std::sqrt((double)hd));
+    a.part = reinterpret_cast<float*>(ws + P->off_attn_part);
+    a.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_attn);
+    a.out = ws + P->off_attn_out;
+    a.status = status;
+    a.part_units = (unsigned)(P->attn_groups * P->attn_chunks);
+
+    float* h = reinterpret_cast<float*>(ws + P->off_h);
+    GemvParams& o = st.g[1];
+    o.n_shards = N;
+    o.rows = (int)d.hidden;
+    o.K = (int)(I.hq_shard * hd);
+    o.T = T;
+    o.shape = P->g_o;
+    o.part = reinterpret_cast<float*>(ws + P->off_part_o);
+    o.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_o);
+    o.status = status;
+    o.resid = x;
+    o.y = h;
+    for (int r = 0; r < N; ++r) {
+        o.W[r] = w->wo[r];
+        o.gamma2[r] = w->gamma_ffn[r];
+    }
+    o.xact = ws + P->off_attn_out;
+    o.norm_out = ws + P->off_hg;
+    o.ss_tiles_out = reinterpret_cast<float*>(ws + P->off_ss_tiles);
+
+    GemvParams& g = st.g[2];
+    g.n_shards = N;
+    g.rows = (int)(2 * I.ffn_shard);
+    g.K = (int)d.hidden;
+    g.T = T;
+    g.shape = P->g_gu;
+    g.eps = (float)d.eps;
+    g.status = status;
+    g.act_out = ws + P->off_act;
+    g.ffn_s = (int)I.ffn_shard;
+    for (int r = 0; r < N; ++r) {
+        g.W[r] = w->wgu[r];
+        g.gamma[r] = w->gamma_ffn[r];
+    }
+    g.xact = ws + P->off_hg;
+    g.ss_tiles = reinterpret_cast<const float*>(ws + P->off_ss_tiles);
+    g.n_ss_tiles = (int)(d.hidden / 8);                 // per 8-row slice (the step's reduce phase)
+
+    GemvParams& dn = st.g[3];
+    dn.n_shards = N;
+    dn.rows = (int)d.hidden;
+    dn.K = (int)I.ffn_shard;
+    dn.T = T;
+    dn.shape = P->g_down;
+    dn.part = reinterpret_cast<float*>(ws + P->off_part_down);
+    dn.status = status;
+    dn.resid = h;
+    dn.y = y;
+    for (int r = 0; r < N; ++r) dn.W[r] = w->wd[r];
+    dn.xact = ws + P->off_act;
+
+    st.bar = reinterpret_cast<unsigned long long*>(ws + P->off_step_bar);
+    st.stamps = P->n_stage_ev > 0 ? reinterpret_cast<unsigned long long*>(ws + P->off_stamps) : nullptr;
+    P->last_stamps_ws = st.stamps ? ws : nullptr;
+    stage_mark(P, 0, s);
+    cudaError_t e = launch_decode_step(st, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: decode step launch");
+    for (int i = 1; i < P->n_stage_ev; ++i) stage_mark(P, i, s);
+    return ok();
+}
+
 static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_set* kv, const float* x,
                                 float* y, const int32_t* pos, int B, char* ws, cudaStream_t s) {
     const tp_model_desc& d = P->d;
@@ -608,7 +709,7 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     }
     const bool bf = d.dtype == TP_BF16;
     cudaError_t e;
-    stage_mark(P, 0, s);
+    if (!bf) stage_mark(P, 0, s);
     if (bf) {
         // bf16 projections take their RMSNorm operands pre-scaled:
         // x * gamma_r for every shard, and sum(x^2) per token
@@ -620,11 +721,10 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         np.H = (int)d.hidden;
         np.xg = ws + P->off_xg;
         np.ss = reinterpret_cast<float*>(ws + P->off_ss);
-        e = launch_norm_prep(np, s);
-        if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: norm prep launch");
         q.xact = ws + P->off_xg;
         q.ss_tiles = np.ss;
         q.n_ss_tiles = (int)((d.hidden + 255) / 256);
+        return decode_step_bf16(P, w, kv, x, y, pos, B, ws, s, q, np);
     }
     e = launch_gemv(q, EPI_QKV_ROPE, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: qkv launch");
@@ -995,6 +1095,32 @@ extern "C" tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int3
     if (n_events < 0 || n_events > 16) return fail(TP_ERR_INVALID_ARG, "tp_profile_stages: 0..16 events");
     plan->n_stage_ev = events ? n_events : 0;
     for (int i = 0; i < plan->n_stage_ev; ++i) plan->stage_ev[i] = static_cast<cudaEvent_t>(events[i]);
+    return ok();
+}
+
+extern "C" tp_status tp_profile_phases(tp_plan_t plan, double* out_us, int32_t n, void* stream) {
+    if (!plan || !out_us) return fail(TP_ERR_NULL, "tp_profile_phases: NULL argument");
+    if (n < 1 || n > kStepStamps - 1) return fail(TP_ERR_INVALID_ARG, "tp_profile_phases: n must be 1..%d", kStepStamps - 1);
+    if (!plan->last_stamps_ws)
+        return fail(TP_ERR_INVALID_ARG, "tp_profile_phases: no bf16 DECODE step ran while tp_profile_stages was set");
+    int dev = 0, sms = 0;
+    TP_CUDA(cudaGetDevice(&dev), "tp_profile_phases: cudaGetDevice");
+    TP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "tp_profile_phases: SM count");
+    const int rows = sms < kMaxStepCtas ? sms : kMaxStepCtas;
+    std::vector<unsigned long long> h((size_t)rows * kStepStamps);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TP_CUDA(cudaMemcpyAsync(h.data(), plan->last_stamps_ws + plan->off_stamps, h.size() * 8, cudaMemcpyDeviceToHost, s),
+            "tp_profile_phases: copy");
+    TP_CUDA(cudaStreamSynchronize(s), "tp_profile_phases: sync");
+    // phase i ends when its barrier completes, i.e. at the latest arrival
+    unsigned long long prev = ~0ull;
+    for (int c = 0; c < rows; ++c) prev = std::min(prev, h[(size_t)c * kStepStamps]);
+    for (int i = 0; i < n; ++i) {
+        unsigned long long end = 0;
+        for (int c = 0; c < rows; ++c) end = std::max(end, h[(size_t)c * kStepStamps + i + 1]);
+        out_us[i] = end >= prev ? (double)(end - prev) * 1e-3 : 0.0;
+        prev = end;
+    }
     return ok();
 }
 

@@ -196,6 +196,18 @@ cudaError_t launch_tc_col(int mode, const PrefillColParams& p, cudaStream_t s); 
 cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s);
 cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s);
 
+// The whole bf16 decode step in one persistent cooperative launch.
+struct DecodeStepParams {
+    GemvParams g[4];                      // qkv, o, gate_up, down (as for the separate launches)
+    AttnDecodeParams a;
+    NormPrepParams np;
+    unsigned long long* bar;              // grid-barrier arrival counter in the workspace (zero-initialised)
+    unsigned long long* stamps;           // optional per-CTA phase end times
+};
+cudaError_t launch_decode_step(const DecodeStepParams& p, cudaStream_t s);
+constexpr int kMaxStepCtas = 256;        // stamp rows reserved in the workspace
+constexpr int kStepStamps = 10;          // per CTA: start, 8 barrier arrivals, end
+
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)
