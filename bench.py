@@ -56,8 +56,9 @@ STAGES = {
 }
 DOMINANT = {"decode": "gate_up_swiglu", "prefill": "gate_up_swiglu", "moe": "expert_gate_up"}
 # phases of the one-launch bf16 decode step (tp_profile_phases)
-STEP_PHASES = ["norm", "qkv_rope", "attention", "combine", "o_proj", "reduce_o", "gate_up_swiglu", "down",
-               "reduce_down"]
+STEP_PHASES = ["norm", "qkv_rope", "attention_combine", "o_proj_reduce", "gate_up_swiglu", "down_reduce"]
+# each phase is reported as its streaming part and its finishing part (finishes + barrier)
+STEP_INTERVALS = [f"{ph}{part}" for ph in STEP_PHASES for part in ("", "/finish")]
 # the committed ncu summary of each dominant kernel and the source it was taken on
 PROFILE = {"decode": ("decode_step_llama3_8b_decode.md", "kernels_decode.cu"),
            "prefill": ("tc_gateup_llama3_8b_prefill.md", "kernels_prefill.cu"),
@@ -409,14 +410,15 @@ def run_ours(args, world, rank, local):
             tb.tp_profile_stages(model.plan, evs[i])
             model.forward(stream=stream)
             if step_kernel and i % 10 == 0:
-                phases.append(tb.tp_profile_phases(model.plan, len(STEP_PHASES), stream))
+                phases.append(tb.tp_profile_phases(model.plan, len(STEP_INTERVALS), stream, median=True))
         tb.tp_profile_stages(model.plan, None)
     torch.cuda.synchronize()
     stage_ms = {}
     if step_kernel:
-        stages = STEP_PHASES
+        stages = STEP_INTERVALS
         for j, name in enumerate(stages):
-            stage_ms[name] = statistics.mean(ph[j] for ph in phases) / 1e3
+            stage_ms[name] = statistics.mean(ph[0][j] for ph in phases) / 1e3
+        median_us = {name: statistics.mean(ph[1][j] for ph in phases) for j, name in enumerate(stages)}
         kernel_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof))
     else:
         for j, name in enumerate(stages):
@@ -438,6 +440,7 @@ def run_ours(args, world, rank, local):
         step_gbs = step_bytes(w) / (ms_step / 1e3) / 1e9
         extra["hbm"] = {"step_bytes": step_bytes(w), "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak,
                         "frac_of_8000": step_gbs / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
+        extra["phase_median_arrival_us"] = median_us
         l2_note = f"inputs larger than L2 ({step_bytes(w) / 1e6:.1f} MB read per step vs 129 MB L2)"
     elif kind == "prefill":
         fl = prefill_flops(w)

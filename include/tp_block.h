@@ -354,18 +354,26 @@ tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);
 tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int32_t n_events);
 
 /* bf16 DECODE runs the whole block as one persistent launch whose phases
- * are: RMSNorm operands, QKV (+RoPE, KV append), attention, split-KV
- * combine, o_proj, rank-ordered reduce (+ next norm operands), gate/up
- * (+SwiGLU), down, rank-ordered reduce. While the hook above is set, that
- * launch also records per-CTA device timestamps at its start, at each of its
- * 8 grid barriers and at its end, and events[0] / events[n_events-1] bracket
- * the launch. This call reads the timestamps of the last such step and
- * writes the duration of the first `n` (1..9) phases in microseconds to
- * out_us (host), each measured from the latest arrival at the previous
- * barrier (the first from the earliest start) to the latest arrival at its
- * own. Synchronises `stream`. Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no
- * profiled bf16 decode step yet), TP_ERR_CUDA. */
-tp_status tp_profile_phases(tp_plan_t plan, double* out_us, int32_t n, void* stream);
+ * are: RMSNorm operands; QKV (+RoPE, KV append); attention (+split-KV
+ * combine); o_proj (+rank-ordered reduce, next norm operands); gate/up
+ * (+SwiGLU); down (+rank-ordered reduce). While the hook above is set, that
+ * launch also records per-CTA device timestamps at its start and, for each
+ * of its 6 phases, when the CTA's own streaming work of the phase is done
+ * and when it arrives at the phase's grid barrier (or ends), and events[0] /
+ * events[n_events-1] bracket the launch. This call reads the timestamps of
+ * the last such step and writes the first `n` (1..12) intervals in
+ * microseconds to out_us (host): for phase i, out_us[2i] = streaming (latest
+ * previous arrival to latest streaming done) and out_us[2i+1] = finishing
+ * (latest streaming done to latest arrival). `median_us` (nullable) receives
+ * the same intervals measured to the median CTA instead of the latest (the
+ * gap is load imbalance). Synchronises `stream`. Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG
+ * (no profiled bf16 decode step yet), TP_ERR_CUDA. */
+tp_status tp_profile_phases(tp_plan_t plan, double* out_us, double* median_us, int32_t n, void* stream);
+
+/* The raw timestamps behind tp_profile_phases: `rows` CTAs (one per SM, in
+ * launch order) x 13 values (start; then per phase: streaming done, barrier
+ * arrival or end), %globaltimer nanoseconds, copied to `out` (host). */
+tp_status tp_profile_phase_stamps(tp_plan_t plan, uint64_t* out, int32_t rows, void* stream);
 
 /* ----------------------------------------------------------------- misc */
 

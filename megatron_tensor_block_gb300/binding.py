@@ -107,7 +107,8 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
         "tp_gemm_bf16": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
         "tp_profile_stages": (I32, [P, C.POINTER(VP), I32]),
-        "tp_profile_phases": (I32, [P, C.POINTER(C.c_double), I32, VP]),
+        "tp_profile_phases": (I32, [P, C.POINTER(C.c_double), C.POINTER(C.c_double), I32, VP]),
+        "tp_profile_phase_stamps": (I32, [P, C.POINTER(C.c_uint64), I32, VP]),
         "tp_last_error": (C.c_char_p, []),
         "tp_version": (I32, []),
     }
@@ -259,11 +260,20 @@ def tp_profile_stages(plan: Plan, events) -> None:
     _check(load().tp_profile_stages(plan.handle, arr, len(raw)))
 
 
-def tp_profile_phases(plan: Plan, n: int = 9, stream=None) -> list:
-    """Phase durations (us) of the last profiled bf16 decode step."""
+def tp_profile_phase_stamps(plan: Plan, rows: int, stream=None) -> list:
+    """Raw per-CTA timestamps (ns) of the last profiled bf16 decode step: rows x 13."""
+    arr = (C.c_uint64 * (rows * 13))()
+    _check(load().tp_profile_phase_stamps(plan.handle, arr, rows, _stream(stream)))
+    return [list(arr[i * 13:(i + 1) * 13]) for i in range(rows)]
+
+
+def tp_profile_phases(plan: Plan, n: int = 9, stream=None, median: bool = False):
+    """Phase durations (us) of the last profiled bf16 decode step; with
+    ``median`` also the durations to the median CTA's arrival."""
     arr = (C.c_double * n)()
-    _check(load().tp_profile_phases(plan.handle, arr, n, _stream(stream)))
-    return list(arr)
+    med = (C.c_double * n)() if median else None
+    _check(load().tp_profile_phases(plan.handle, arr, med, n, _stream(stream)))
+    return (list(arr), list(med)) if median else list(arr)
 
 
 def tp_last_error() -> str:

@@ -539,14 +539,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(const AttnDecodeParams
     }
 }
 
-// ---------------------------------------------------------------------------
-// persistent warp-specialised kernels (bf16): one producer thread streams the
-// weights (or KV tiles) with bulk asynchronous copies into a ring of shared
-// memory stages; eight consumer warps compute from shared memory. Launched
-// with programmatic dependent launch: the producer starts streaming data that
-// the preceding kernel does not write while that kernel is still running.
-// ---------------------------------------------------------------------------
-
+// Unit u of a projection -> (group, shard, 64-row tile, reduction chunk).
 __device__ __forceinline__ void decode_unit(const GemvParams& p, int epi, int u, int& gi, int& r, int& tb,
                                             int& chunk) {
     const int upg = p.shape.units_per_group();
@@ -561,519 +554,6 @@ __device__ __forceinline__ void decode_unit(const GemvParams& p, int epi, int u,
         r = gi / rb;
         tb = gi - r * rb;
         chunk = rem;
-    }
-}
-
-// Tensor-map arguments of one projection launch: a map per shard weight,
-// boxes of kBoxK x 32 rows (row-major [rows, K] bf16, no swizzle).
-struct TmaGemvArgs {
-    CUtensorMap tm[TP_MAX_SHARDS];   // weights, boxes of kBoxK x 32 rows
-    CUtensorMap tmx;                 // activation operand rows, boxes of kBoxK x 8 rows
-    GemvParams p;
-};
-
-// Each stage carries, for 64 rows x 256 reduction elements: the two weight
-// boxes (rows 0-31 and 32-63 of the tile) and the matching activation box
-// (the shard's 8 token rows). Consumers touch only shared memory.
-template <int EPI>
-__global__ void __launch_bounds__(kStreamThreads, 2) gemv_stream_kernel(const __grid_constant__ TmaGemvArgs A) {
-    const GemvParams& p = A.p;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    const Ring R = ring_setup(smem, kGemvStages);
-    unsigned char* ring = smem + kCtrlBytes;
-    float* tile = reinterpret_cast<float*>(ring + kGemvStages * kGemvStageBytes);   // [64][8]
-    float* ss = tile + kTileRows * kTMax;                                            // [8] (+pad)
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int U = p.shape.units();
-    const int kc = p.shape.kc;
-    const int spu = (kc + kBoxK - 1) / kBoxK;
-
-    if (warp == kConsumers / 32) {                     // ---- producer
-        if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            uint32_t it = 0;
-            bool ok = (smem_u32(ring) & 127u) == 0;    // tensor copies need 128-byte aligned destinations
-            if (!ok) {
-                *R.abort = 1;
-                set_status(p.status, TP_ERR_ALIGN);
-            }
-            // Weights do not depend on the preceding kernel: the first ring's worth
-            // of weight boxes is issued before waiting for it; the activation
-            // boxes of those stages follow once it has completed.
-            const int my_units = ((int)blockIdx.x < U) ? (U - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-            const uint32_t total = (uint32_t)(my_units * spu);
-            bool waited = false;
-            int npend = 0;
-            int pend_x[kGemvStages], pend_y[kGemvStages];
-            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                int gi, r, tb, chunk;
-                decode_unit(p, EPI, u, gi, r, tb, chunk);
-                const int rowa = tile_row(EPI, tb, 0, p.head_dim, p.ffn_s);
-                const int rowb = tile_row(EPI, tb, 32, p.head_dim, p.ffn_s);
-                const int k0 = chunk * kc;
-                for (int st = 0; st < spu; ++st, ++it) {
-                    const int sl = it % kGemvStages;
-                    if (!mbar_wait(&R.empty[sl], ((it / kGemvStages) & 1) ^ 1, R.abort, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&R.full[sl], 2u * kBoxBytes + kXBoxBytes);
-                    unsigned char* dst = ring + sl * kGemvStageBytes;
-                    tma_load_2d(dst, &A.tm[r], k0 + st * kBoxK, rowa, &R.full[sl], pol);
-                    tma_load_2d(dst + kBoxBytes, &A.tm[r], k0 + st * kBoxK, rowb, &R.full[sl], pol);
-                    if (waited) {
-                        tma_load_2d_keep(dst + 2 * kBoxBytes, &A.tmx, k0 + st * kBoxK, r * kTMax, &R.full[sl]);
-                    } else {
-                        pend_x[npend] = k0 + st * kBoxK;
-                        pend_y[npend] = r * kTMax;
-                        ++npend;
-                        if (npend == kGemvStages || it + 1 == total) {
-                            pdl_wait();                // activations are written by the preceding kernel
-                            waited = true;
-                            for (int q = 0; q < npend; ++q) {
-                                const uint32_t iq = it + 1 - npend + q;
-                                const int sq = iq % kGemvStages;
-                                tma_load_2d_keep(ring + sq * kGemvStageBytes + 2 * kBoxBytes, &A.tmx, pend_x[q],
-                                                 pend_y[q], &R.full[sq]);
-                            }
-                            npend = 0;
-                        }
-                    }
-                }
-            }
-            if (!waited && npend > 0) {                // aborted before the flush: complete the stages' bytes
-                pdl_wait();
-                for (int q = 0; q < npend; ++q) {
-                    const uint32_t iq = it - npend + q;
-                    const int sq = iq % kGemvStages;
-                    tma_load_2d_keep(ring + sq * kGemvStageBytes + 2 * kBoxBytes, &A.tmx, pend_x[q], pend_y[q],
-                                     &R.full[sq]);
-                }
-            }
-            pdl_trigger();
-            if (!ok || *R.abort) producer_drain(R, it, kGemvStages);
-        }
-        return;
-    }
-
-    // ---- consumers
-    pdl_wait();
-    const int wm = warp & 3, wk = warp >> 2;
-    const int g = lane >> 2, tq = lane & 3;
-    const int box = wm >> 1, brow = 16 * (wm & 1) + g;
-    const int T = p.T;
-    int* s_pos = reinterpret_cast<int*>(ss + kTMax);                  // [8]
-    float* s_bias = ss + 2 * kTMax;                                   // [64]
-    // values every unit of this CTA needs, loaded once: the sums of squares
-    // of the normalised input and the token positions
-    if (EPI == EPI_QKV_ROPE && tid < kTMax) s_pos[tid] = tid < T ? p.pos[tid] : 0;
-    if (EPI != EPI_ROWPAR) {
-        float a = 0.f;                                                // warp t: token t
-        if (warp < T)
-            for (int q = lane; q < p.n_ss_tiles; q += 32) a += p.ss_tiles[q * kTMax + warp];
-        a = warp_sum(a);
-        if (lane == 0) ss[warp] = a;
-    }
-    consumer_sync(kConsumers);
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        int gi, r, tb, chunk;
-        decode_unit(p, EPI, u, gi, r, tb, chunk);
-        float bias_v = 0.f;                                           // in flight during the stages
-        if (EPI == EPI_QKV_ROPE && tid < kTileRows && p.bias[r])
-            bias_v = p.bias[r][tile_row(EPI_QKV_ROPE, tb, tid, p.head_dim, 0)];
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int st = 0; st < spu; ++st, ++it) {
-            const int sl = it % kGemvStages;
-            mbar_wait(&R.full[sl], (it / kGemvStages) & 1, R.abort, p.status);
-            __syncwarp();   // lanes leave the wait loop independently
-            const int steps_here = min(kBoxK / kKStep, (kc - st * kBoxK) / kKStep);
-            const unsigned char* stage = ring + sl * kGemvStageBytes;
-            const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
-            const unsigned char* wB = wA + 8 * (kBoxK * 2);
-            const unsigned char* px = stage + 2 * kBoxBytes + g * (kBoxK * 2) + tq * 16;
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int step = wk + 2 * s2;
-                if (step < steps_here) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
-                        const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
-                        const uint4 xv = *reinterpret_cast<const uint4*>(px + step * 128 + h * 64);
-                        mma_bf16_16816(c, a.x, b.x, a.y, b.y, xv.x, xv.y);
-                        mma_bf16_16816(c, a.z, b.z, a.w, b.w, xv.z, xv.w);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&R.empty[sl]);
-        }
-        // combine the two reduction halves in a fixed order: (half 0) + (half 1)
-        const int i0 = (16 * wm + g) * kTMax + 2 * tq, i1 = (16 * wm + g + 8) * kTMax + 2 * tq;
-        if (wk == 0) {
-            tile[i0] = c[0];
-            tile[i0 + 1] = c[1];
-            tile[i1] = c[2];
-            tile[i1 + 1] = c[3];
-        }
-        if (EPI == EPI_QKV_ROPE && tid < kTileRows) s_bias[tid] = bias_v;
-        consumer_sync(kConsumers);
-        if (wk == 1) {
-            tile[i0] += c[0];
-            tile[i0 + 1] += c[1];
-            tile[i1] += c[2];
-            tile[i1 + 1] += c[3];
-        }
-        consumer_sync(kConsumers);
-        if (EPI == EPI_ROWPAR) {
-            // this unit's partial sum; the rank-ordered reduction runs in a later kernel
-            float* mine = p.part + (size_t)u * kPartStride;
-            for (int i = tid * 4; i < kTileRows * kTMax; i += kConsumers * 4)
-                *reinterpret_cast<float4*>(mine + i) = *reinterpret_cast<const float4*>(tile + i);
-        } else if (EPI == EPI_SWIGLU) {
-            bf16* out = reinterpret_cast<bf16*>(p.act_out);
-            const float inv_k = 1.0f / (float)p.K;
-            for (int i = tid; i < 32 * T; i += kConsumers) {
-                const int t = i >> 5, j = i & 31;
-                const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
-                const float gt = tile[j * kTMax + t] * rinv;
-                const float up = tile[(j + 32) * kTMax + t] * rinv;
-                out[((size_t)r * kTMax + t) * p.ffn_s + tb * 32 + j] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
-            }
-        } else {
-            const int d = p.head_dim, half = d >> 1;
-            const float inv_k = 1.0f / (float)p.K;
-            for (int i = tid; i < 32 * T; i += kConsumers) {
-                const int t = i >> 5, j = i & 31;
-                const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
-                const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
-                const int head = rowA / d, ii = rowA - head * d;
-                float va = tile[j * kTMax + t] * rinv + s_bias[j];
-                float vb = tile[(j + 32) * kTMax + t] * rinv + s_bias[j + 32];
-                const int pos = s_pos[t];
-                if (head < p.hq_s + p.hkv_s) {
-                    float cs, sn;
-                    sincosf((float)pos * exp2f(-(2.0f * ii / d) * (float)p.log2_theta), &sn, &cs);
-                    const float ra = va * cs - vb * sn, rb = va * sn + vb * cs;
-                    va = ra;
-                    vb = rb;
-                }
-                if (head < p.hq_s) {
-                    float* q = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
-                    q[0] = va;
-                    q[half] = vb;
-                } else {
-                    const bool is_k = head < p.hq_s + p.hkv_s;
-                    const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
-                    if (pos < 0 || pos >= p.max_kv) {
-                        set_status(p.status, TP_ERR_CAPACITY);
-                        continue;
-                    }
-                    bf16* cache = reinterpret_cast<bf16*>(is_k ? p.kcache[r] : p.vcache[r]);
-                    bf16* dst = cache + (((size_t)t * p.hkv_s + kvh) * p.max_kv + pos) * d + ii;
-                    dst[0] = __float2bfloat16_rn(va);
-                    dst[half] = __float2bfloat16_rn(vb);
-                }
-            }
-        }
-        consumer_sync(kConsumers);
-    }
-}
-
-// Rank-ordered reduction of a row-parallel projection's unit partials (the
-// single-device all-reduce), one CTA per 64-row tile, thread = (row, token):
-//   y = resid + sum_r (sum_c part[tile][r][c])   -- chunks, then ranks, in order
-// With norm_out set it also writes the next RMSNorm's operands (y * gamma_r
-// for every shard, bf16) and the tile's per-token sums of squares of y.
-__global__ void __launch_bounds__(512) rowpar_reduce_kernel(const GemvParams p) {
-    pdl_trigger();
-    pdl_wait();
-    __shared__ float sq[kTileRows][kTMax];
-    const int tb = blockIdx.x, tid = threadIdx.x;
-    const int j = tid / kTMax, t = tid - j * kTMax;
-    const int upg = p.shape.units_per_group(), C = p.shape.chunks;
-    const float* base = p.part + (size_t)tb * upg * kPartStride + j * kTMax + t;
-    float v[kMaxGroupUnits];
-#pragma unroll
-    for (int q = 0; q < kMaxGroupUnits; ++q)
-        if (q < upg) v[q] = base[(size_t)q * kPartStride];
-    // chunks in order within each rank, then ranks in order
-    float total = 0.f, pr = 0.f;
-#pragma unroll
-    for (int q = 0; q < kMaxGroupUnits; ++q) {
-        if (q < upg) {
-            const int cc = q % C;
-            pr = (cc == 0) ? v[q] : pr + v[q];
-            if (cc == C - 1) total = (q < C) ? pr : total + pr;
-        }
-    }
-    const int row = tb * kTileRows + j;
-    float yv = 0.f;
-    if (t < p.T) {
-        const size_t o = (size_t)t * p.rows + row;
-        yv = p.resid[o] + total;
-        p.y[o] = yv;
-        if (p.norm_out) {
-            bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
-            for (int r2 = 0; r2 < p.n_shards; ++r2)
-                nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
-        }
-    }
-    if (p.norm_out) {
-        sq[j][t] = yv * yv;
-        __syncthreads();
-        if (tid < kTMax) {
-            float a = 0.f;
-            for (int jj = 0; jj < kTileRows; ++jj) a += sq[jj][tid];
-            p.ss_tiles_out[tb * kTMax + tid] = a;
-        }
-    }
-}
-
-// RMSNorm operand preparation: CTA (t, kb) writes x[t, kb*256 .. +256) * gamma_r
-// as bf16 for every shard and that block's sum of squares ss[kb][t] (rows t >= T
-// are zero). 64 threads x 4 elements.
-__global__ void __launch_bounds__(64) norm_prep_kernel(const NormPrepParams p) {
-    pdl_trigger();                                     // the next kernel may start streaming weights
-    pdl_wait();
-    __shared__ float wsum[2];
-    const int t = blockIdx.x, kb = blockIdx.y, tid = threadIdx.x;
-    const int k = kb * 256 + tid * 4;
-    const bool in = k < p.H;                           // the last block may be ragged (H % 256 != 0)
-    const float4 v = (t < p.T && in) ? *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + k)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < p.N && in; ++r) {
-        const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma[r] + k));
-        uint2 pk;
-        pk.x = pack_bf16x2(v.x * gm.x, v.y * gm.y);
-        pk.y = pack_bf16x2(v.z * gm.z, v.w * gm.w);
-        *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xg) + ((size_t)r * kTMax + t) * p.H + k) = pk;
-    }
-    float a = v.x * v.x;
-    a = fmaf(v.y, v.y, a);
-    a = fmaf(v.z, v.z, a);
-    a = fmaf(v.w, v.w, a);
-    a = warp_sum(a);
-    if ((tid & 31) == 0) wsum[tid >> 5] = a;
-    __syncthreads();
-    if (tid == 0) p.ss[kb * kTMax + t] = wsum[0] + wsum[1];
-}
-
-template <int D, int G>
-__global__ void __launch_bounds__(kStreamThreads, 2) attn_stream_kernel(const AttnDecodeParams p) {
-    constexpr int SK = kAttnStageBytes / (D * 2);      // keys per stage
-    constexpr int LPK = D / 8;                          // lanes per key
-    constexpr int KPP = kConsumers / LPK;               // keys per pass
-    extern __shared__ __align__(1024) unsigned char smem[];
-    const Ring R = ring_setup(smem);
-    unsigned char* ring = smem + kCtrlBytes;
-    float* qs = reinterpret_cast<float*>(ring + kStages * kAttnStageBytes);   // [8][D]
-    float* sc = qs + kMaxGroup * D;                                           // [8][chunk]
-    float* red = sc + kMaxGroup * kAttnChunk;                                 // [8 warps][8][D]
-    float* s_m = red + 8 * kMaxGroup * D;                                     // [8]
-    float* s_l = s_m + kMaxGroup;                                             // [8]
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
-
-    if (warp == kConsumers / 32) {                     // ---- producer
-        if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            uint32_t it = 0;
-            bool ok = true, waited = false;
-            int posv[kTMax];
-            for (int b = 0; b < kTMax; ++b) posv[b] = b < p.B ? p.pos[b] : 0;
-            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const int c = u % p.n_chunks, gi = u / p.n_chunks;
-                const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-                int pos = posv[0];
-#pragma unroll
-                for (int bb = 1; bb < kTMax; ++bb)
-                    if (bb == b) pos = posv[bb];
-                const int Lk = min(pos + 1, p.max_kv);
-                const int j0 = c * kAttnChunk;
-                const int n = max(0, min(Lk - j0, kAttnChunk));
-                const size_t off = (((size_t)b * p.hkv_s + kh) * p.max_kv + j0) * D;
-                for (int half = 0; half < 2 && ok; ++half) {
-                    const bf16* src = reinterpret_cast<const bf16*>(half ? p.vcache[r] : p.kcache[r]) + off;
-                    for (int k0 = 0; k0 < n; k0 += SK, ++it) {
-                        const int keys = min(SK, n - k0);
-                        // the tile holding the new position is written by the preceding kernel
-                        if (!waited && j0 + k0 + keys > pos) {
-                            pdl_wait();
-                            waited = true;
-                        }
-                        const int sl = it % kStages;
-                        if (!mbar_wait(&R.empty[sl], ((it / kStages) & 1) ^ 1, R.abort, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t bytes = (uint32_t)keys * D * 2u;
-                        mbar_arrive_expect_tx(&R.full[sl], bytes);
-                        bulk_g2s(ring + sl * kAttnStageBytes, src + (size_t)k0 * D, bytes, &R.full[sl], pol);
-                    }
-                }
-            }
-            pdl_trigger();
-            if (!ok || *R.abort) producer_drain(R, it);
-        }
-        return;
-    }
-
-    // ---- consumers
-    pdl_wait();
-    const int ks = tid / LPK, li = tid % LPK;
-    int* s_pos = reinterpret_cast<int*>(s_l + kMaxGroup);
-    if (tid < kTMax) s_pos[tid] = tid < p.B ? p.pos[tid] : 0;
-    // the first unit's queries; later units' are loaded during the previous unit
-    float4 qn = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto q_load = [&](int u) {
-        const int gi = u / p.n_chunks, kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-        const size_t qoff = ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)kh * G * D;
-        if (tid * 4 < G * D) qn = *reinterpret_cast<const float4*>(p.q + qoff + tid * 4);
-    };
-    if ((int)blockIdx.x < U) q_load(blockIdx.x);
-    consumer_sync(kConsumers);
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int c = u % p.n_chunks;
-        const int b = (u / p.n_chunks / p.hkv_s) % p.B;
-        const int pos = s_pos[b];
-        const int Lk = min(pos + 1, p.max_kv);
-        const int j0 = c * kAttnChunk;
-        const int n = max(0, min(Lk - j0, kAttnChunk));
-        if (tid * 4 < G * D) {
-            float4 v = qn;
-            v.x *= p.scale; v.y *= p.scale; v.z *= p.scale; v.w *= p.scale;
-            *reinterpret_cast<float4*>(qs + tid * 4) = v;
-        }
-        consumer_sync(kConsumers);
-        if (u + (int)gridDim.x < U) q_load(u + gridDim.x);
-        float qr[G][8];                                  // this thread's slice of every query of the group
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qr[g][e] = qs[g * D + li * 8 + e];
-
-        // scores s[g][j] = (q_g / sqrt(d)) . k_j, one K stage at a time
-        for (int k0 = 0; k0 < n; k0 += SK, ++it) {
-            const int keys = min(SK, n - k0);
-            const int sl = it % kStages;
-            mbar_wait(&R.full[sl], (it / kStages) & 1, R.abort, p.status);
-            __syncwarp();
-            const bf16* Kt = reinterpret_cast<const bf16*>(ring + sl * kAttnStageBytes);
-#pragma unroll
-            for (int kk = 0; kk < SK; kk += KPP) {       // uniform trip count (shuffles below)
-                const int key = kk + ks;
-                float kv[8];
-                if (key < keys) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(Kt + key * D + li * 8);
-                    const float2 a0 = unpack_bf16x2(w.x), a1 = unpack_bf16x2(w.y), a2 = unpack_bf16x2(w.z),
-                                 a3 = unpack_bf16x2(w.w);
-                    kv[0] = a0.x; kv[1] = a0.y; kv[2] = a1.x; kv[3] = a1.y;
-                    kv[4] = a2.x; kv[5] = a2.y; kv[6] = a3.x; kv[7] = a3.y;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) kv[e] = 0.f;
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    // four independent partial products, then a short tree
-                    float d0 = qr[g][0] * kv[0], d1 = qr[g][1] * kv[1], d2 = qr[g][2] * kv[2], d3 = qr[g][3] * kv[3];
-                    d0 = fmaf(qr[g][4], kv[4], d0);
-                    d1 = fmaf(qr[g][5], kv[5], d1);
-                    d2 = fmaf(qr[g][6], kv[6], d2);
-                    d3 = fmaf(qr[g][7], kv[7], d3);
-                    float dot = (d0 + d1) + (d2 + d3);
-#pragma unroll
-                    for (int o = LPK / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                    if (li == 0 && key < keys) sc[g * kAttnChunk + k0 + key] = dot;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&R.empty[sl]);
-        }
-        consumer_sync(kConsumers);
-
-        // chunk-local softmax statistics per head
-        for (int g = warp; g < G; g += kConsumers / 32) {
-            float m = -INFINITY;
-            for (int j = lane; j < n; j += 32) m = fmaxf(m, sc[g * kAttnChunk + j]);
-            m = warp_max(m);
-            float l = 0.f;
-            for (int j = lane; j < n; j += 32) {
-                const float e = expf(sc[g * kAttnChunk + j] - m);
-                sc[g * kAttnChunk + j] = e;
-                l += e;
-            }
-            l = warp_sum(l);
-            if (lane == 0) {
-                s_m[g] = m;
-                s_l[g] = l;
-            }
-        }
-        consumer_sync(kConsumers);
-
-        // unnormalised output o[g] = sum_j e[g][j] v_j, one V stage at a time
-        float acc[G][8];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-        for (int k0 = 0; k0 < n; k0 += SK, ++it) {
-            const int keys = min(SK, n - k0);
-            const int sl = it % kStages;
-            mbar_wait(&R.full[sl], (it / kStages) & 1, R.abort, p.status);
-            __syncwarp();
-            const bf16* Vt = reinterpret_cast<const bf16*>(ring + sl * kAttnStageBytes);
-            for (int key = ks; key < keys; key += KPP) {
-                const uint4 w = *reinterpret_cast<const uint4*>(Vt + key * D + li * 8);
-                float v[8];
-                const float2 a0 = unpack_bf16x2(w.x), a1 = unpack_bf16x2(w.y), a2 = unpack_bf16x2(w.z),
-                             a3 = unpack_bf16x2(w.w);
-                v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y;
-                v[4] = a2.x; v[5] = a2.y; v[6] = a3.x; v[7] = a3.y;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float e = sc[g * kAttnChunk + k0 + key];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[g][q] = fmaf(e, v[q], acc[g][q]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&R.empty[sl]);
-        }
-        // reduce over the key slots: first within the warp, then across warps
-#pragma unroll
-        for (int o = LPK; o < 32; o <<= 1)
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[g][q] += __shfl_xor_sync(0xffffffffu, acc[g][q], o);
-        if (lane < LPK) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) red[(warp * kMaxGroup + g) * D + li * 8 + q] = acc[g][q];
-        }
-        consumer_sync(kConsumers);
-        // this chunk's partial (unnormalised output, max, sum); combined later
-        const int pstride = G * (D + 2);
-        float* mine = p.part + (size_t)u * pstride;
-        for (int i = tid; i < G * D; i += kConsumers) {
-            const int g = i / D, dd = i - g * D;
-            float o = red[g * D + dd];
-            for (int w = 1; w < kConsumers / 32; ++w) o += red[(w * kMaxGroup + g) * D + dd];
-            mine[i] = o;
-        }
-        if (tid < G) {
-            mine[G * D + tid] = s_m[tid];
-            mine[G * D + G + tid] = s_l[tid];
-        }
-        consumer_sync(kConsumers);
     }
 }
 
@@ -1105,12 +585,6 @@ struct AtShape {
     static constexpr int STAGE = 2 * NB * BOX;            // K boxes, then V boxes
 };
 
-struct TmaAttnArgs {
-    CUtensorMap tk[TP_MAX_SHARDS];
-    CUtensorMap tv[TP_MAX_SHARDS];
-    AttnDecodeParams p;
-};
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -1134,338 +608,6 @@ template <int D>
 __device__ __forceinline__ uint32_t at_addr(uint32_t part, int key, int chunk) {
     using S = AtShape<D>;
     return part + (chunk >> 3) * S::BOX + key * (S::PT * 2) + (chunk & 7) * 16;
-}
-
-size_t attn_tc_smem() {
-    return 1024 + (size_t)kAtRing * kAtMaxStage + (size_t)(4 * kAtSlot + 8 * kMaxGroup * 2 + kTMax) * 4;
-}
-
-template <int D>
-__global__ void __launch_bounds__(kStreamThreads, 1) attn_tc_kernel(const __grid_constant__ TmaAttnArgs A) {
-    using S = AtShape<D>;
-    constexpr int KS = D / 16;
-    const AttnDecodeParams& p = A.p;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + kAtRing;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kAtRing);
-    unsigned char* ring = smem + 1024;
-    float* red = reinterpret_cast<float*>(ring + kAtRing * kAtMaxStage);       // [4][kAtSlot]
-    float* s_ml = red + 4 * kAtSlot;                                           // [8 warps][8 queries][m, l]
-    int* s_pos = reinterpret_cast<int*>(s_ml + 8 * kMaxGroup * 2);             // [8]
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = p.hq_s / p.hkv_s;
-    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
-    if (tid == 0) {
-        for (int i = 0; i < kAtRing; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 4);           // the four warps of one group release a stage
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == kConsumers / 32) {             // ---- producer
-        if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            uint32_t it = 0;
-            bool ok = (smem_u32(ring) & 127u) == 0, waited = false;
-            if (!ok) {
-                *abort_flag = 1;
-                set_status(p.status, TP_ERR_ALIGN);
-            }
-            int posv[kTMax];
-            for (int b = 0; b < kTMax; ++b) posv[b] = b < p.B ? p.pos[b] : 0;
-            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const int c = u % p.n_chunks, gi = u / p.n_chunks;
-                const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-                int pos = posv[0];
-#pragma unroll
-                for (int bb = 1; bb < kTMax; ++bb)
-                    if (bb == b) pos = posv[bb];
-                const int Lk = min(pos + 1, p.max_kv);
-                const int j0 = c * kAttnChunk;
-                const int n = max(0, min(Lk - j0, kAttnChunk));
-                const int row0 = (b * p.hkv_s + kh) * p.max_kv + j0;
-                for (int k0 = 0; k0 < n; k0 += kAtKeys, ++it) {
-                    if (!waited && j0 + k0 + kAtKeys > pos) {   // holds the position just written
-                        pdl_wait();
-                        waited = true;
-                    }
-                    const int sl = it % kAtRing;
-                    if (!mbar_wait(&empty[sl], ((it / kAtRing) & 1) ^ 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[sl], (uint32_t)S::STAGE);
-                    unsigned char* st = ring + sl * kAtMaxStage;
-#pragma unroll
-                    for (int h = 0; h < S::NB; ++h) {
-                        tma_load_2d(st + h * S::BOX, &A.tk[r], h * 64, row0 + k0, &full[sl], pol);
-                        tma_load_2d(st + (S::NB + h) * S::BOX, &A.tv[r], h * 64, row0 + k0, &full[sl], pol);
-                    }
-                }
-            }
-            pdl_trigger();
-            if (!ok || *abort_flag) {
-                volatile int no_abort = 0;
-                const uint32_t first = it > (uint32_t)kAtRing ? it - kAtRing : 0u;
-                for (uint32_t k = first; k < it; ++k)
-                    mbar_wait(&full[k % kAtRing], (k / kAtRing) & 1, &no_abort, nullptr);
-            }
-        }
-        return;
-    }
-
-    // ---- consumers
-    pdl_wait();
-    const int grp = warp >> 2, wq = warp & 3;
-    const int g = lane >> 2, t = lane & 3;
-    const int mi = lane >> 3, rr = lane & 7;
-    if (tid < kTMax) s_pos[tid] = tid < p.B ? p.pos[tid] : 0;
-    consumer_sync(kConsumers);
-    const uint32_t ring_u32 = smem_u32(ring);
-    const int q0 = 2 * t, q1 = 2 * t + 1;                 // the two queries of this lane's fragments
-    uint32_t it_unit = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int c = u % p.n_chunks, gi = u / p.n_chunks;
-        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-        const int pos = s_pos[b];
-        const int Lk = min(pos + 1, p.max_kv);
-        const int j0 = c * kAttnChunk;
-        const int n = max(0, min(Lk - j0, kAttnChunk));
-        const int nblk = (n + kAtKeys - 1) / kAtKeys;
-
-        // B operand of S^T = K Q^T: query g, head-dim pairs (16ks + 2t, +1) and (16ks + 8 + 2t, +1)
-        uint32_t qb[KS][2];
-        {
-            const float* qp = p.q + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                if (g < G) {
-                    const float2 a = *reinterpret_cast<const float2*>(qp + 16 * ks + 2 * t);
-                    const float2 c2 = *reinterpret_cast<const float2*>(qp + 16 * ks + 8 + 2 * t);
-                    qb[ks][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
-                    qb[ks][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
-                } else {
-                    qb[ks][0] = qb[ks][1] = 0u;
-                }
-            }
-        }
-        float o[KS][4];
-#pragma unroll
-        for (int dt = 0; dt < KS; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-        for (int blk = grp; blk < nblk; blk += 2) {
-            const uint32_t it = it_unit + blk;
-            const int sl = it % kAtRing;
-            mbar_wait(&full[sl], (it / kAtRing) & 1, abort_flag, p.status);
-            __syncwarp();                        // lanes leave the wait loop independently
-            const uint32_t kpart = ring_u32 + sl * kAtMaxStage, vpart = kpart + S::NB * S::BOX;
-            const int kb = blk * kAtKeys + 16 * wq;          // this warp's first key, relative to the chunk
-            // ---- S^T for 16 keys x 8 queries
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(at_addr<D>(kpart, 16 * wq + rr + 8 * (mi & 1), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            }
-            // ---- online softmax per query over this warp's keys (rows g and g + 8)
-            const bool v0 = kb + g < n, v1 = kb + g + 8 < n;
-            const float x00 = v0 ? sc[0] : -INFINITY, x01 = v0 ? sc[1] : -INFINITY;
-            const float x10 = v1 ? sc[2] : -INFINITY, x11 = v1 ? sc[3] : -INFINITY;
-            float mq0 = fmaxf(x00, x10), mq1 = fmaxf(x01, x11);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mq0 = fmaxf(mq0, __shfl_xor_sync(0xffffffffu, mq0, off));
-                mq1 = fmaxf(mq1, __shfl_xor_sync(0xffffffffu, mq1, off));
-            }
-            const float n0 = fmaxf(m0, mq0), n1 = fmaxf(m1, mq1);
-            const float al0 = (n0 == -INFINITY) ? 1.f : expf(m0 - n0);
-            const float al1 = (n1 == -INFINITY) ? 1.f : expf(m1 - n1);
-            const float p00 = (x00 == -INFINITY) ? 0.f : expf(x00 - n0);
-            const float p10 = (x10 == -INFINITY) ? 0.f : expf(x10 - n0);
-            const float p01 = (x01 == -INFINITY) ? 0.f : expf(x01 - n1);
-            const float p11 = (x11 == -INFINITY) ? 0.f : expf(x11 - n1);
-            float ps0 = p00 + p10, ps1 = p01 + p11;
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
-                ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
-            }
-            l0 = l0 * al0 + ps0;
-            l1 = l1 * al1 + ps1;
-            m0 = n0;
-            m1 = n1;
-#pragma unroll
-            for (int dt = 0; dt < KS; ++dt) {
-                o[dt][0] *= al0;
-                o[dt][1] *= al1;
-                o[dt][2] *= al0;
-                o[dt][3] *= al1;
-            }
-            // ---- O^T += V^T P^T; P^T fragments: (keys 2t, 2t+1 | 8+2t, 9+2t ; query g)
-            const uint32_t pb0 = movmatrix_t(pack_bf16x2(p00, p01));
-            const uint32_t pb1 = movmatrix_t(pack_bf16x2(p10, p11));
-            const uint32_t mlo = (kb + 2 * t < n ? 0x0000FFFFu : 0u) | (kb + 2 * t + 1 < n ? 0xFFFF0000u : 0u);
-            const uint32_t mhi = (kb + 8 + 2 * t < n ? 0x0000FFFFu : 0u) | (kb + 9 + 2 * t < n ? 0xFFFF0000u : 0u);
-#pragma unroll
-            for (int dt = 0; dt < KS; ++dt) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(at_addr<D>(vpart, 16 * wq + rr + 8 * (mi >> 1), 2 * dt + (mi & 1)), a0, a1, a2, a3);
-                mma_bf16_16816(o[dt], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[sl]);
-        }
-        it_unit += nblk;
-
-        // ---- merge the eight warps: common max, then a fixed tree of sums
-        if (g == 0) {
-            s_ml[(warp * kMaxGroup + q0) * 2] = m0;
-            s_ml[(warp * kMaxGroup + q0) * 2 + 1] = l0;
-            s_ml[(warp * kMaxGroup + q1) * 2] = m1;
-            s_ml[(warp * kMaxGroup + q1) * 2 + 1] = l1;
-        }
-        consumer_sync(kConsumers);
-        float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            M0 = fmaxf(M0, s_ml[(w * kMaxGroup + q0) * 2]);
-            M1 = fmaxf(M1, s_ml[(w * kMaxGroup + q1) * 2]);
-        }
-        const float c0 = (m0 == -INFINITY) ? 0.f : expf(m0 - M0);
-        const float c1 = (m1 == -INFINITY) ? 0.f : expf(m1 - M1);
-#pragma unroll
-        for (int dt = 0; dt < KS; ++dt) {
-            o[dt][0] *= c0;
-            o[dt][1] *= c1;
-            o[dt][2] *= c0;
-            o[dt][3] *= c1;
-        }
-        // round 1: warps 4-7 -> 0-3; round 2: 2,3 -> 0,1; round 3: 1 -> 0
-        for (int half = 4; half >= 1; half >>= 1) {
-            if (warp >= half && warp < 2 * half) {
-                float* dst = red + (warp - half) * kAtSlot;
-#pragma unroll
-                for (int dt = 0; dt < KS; ++dt) {
-                    if (q0 < G) {
-                        dst[q0 * D + 16 * dt + g] = o[dt][0];
-                        dst[q0 * D + 16 * dt + g + 8] = o[dt][2];
-                    }
-                    if (q1 < G) {
-                        dst[q1 * D + 16 * dt + g] = o[dt][1];
-                        dst[q1 * D + 16 * dt + g + 8] = o[dt][3];
-                    }
-                }
-            }
-            consumer_sync(kConsumers);
-            if (warp < half) {
-                const float* src = red + warp * kAtSlot;
-#pragma unroll
-                for (int dt = 0; dt < KS; ++dt) {
-                    if (q0 < G) {
-                        o[dt][0] += src[q0 * D + 16 * dt + g];
-                        o[dt][2] += src[q0 * D + 16 * dt + g + 8];
-                    }
-                    if (q1 < G) {
-                        o[dt][1] += src[q1 * D + 16 * dt + g];
-                        o[dt][3] += src[q1 * D + 16 * dt + g + 8];
-                    }
-                }
-            }
-            consumer_sync(kConsumers);
-        }
-        if (warp == 0 && (unsigned)u < p.part_units) {
-            float* mine = p.part + (size_t)u * G * (D + 2);
-#pragma unroll
-            for (int dt = 0; dt < KS; ++dt) {
-                if (q0 < G) {
-                    mine[q0 * D + 16 * dt + g] = o[dt][0];
-                    mine[q0 * D + 16 * dt + g + 8] = o[dt][2];
-                }
-                if (q1 < G) {
-                    mine[q1 * D + 16 * dt + g] = o[dt][1];
-                    mine[q1 * D + 16 * dt + g + 8] = o[dt][3];
-                }
-            }
-            if (g == 0) {
-                float L0 = 0.f, L1 = 0.f;
-                for (int w = 0; w < 8; ++w) {
-                    const float mw0 = s_ml[(w * kMaxGroup + q0) * 2], mw1 = s_ml[(w * kMaxGroup + q1) * 2];
-                    if (mw0 != -INFINITY) L0 += s_ml[(w * kMaxGroup + q0) * 2 + 1] * expf(mw0 - M0);
-                    if (mw1 != -INFINITY) L1 += s_ml[(w * kMaxGroup + q1) * 2 + 1] * expf(mw1 - M1);
-                }
-                if (q0 < G) {
-                    mine[G * D + q0] = M0;
-                    mine[G * D + G + q0] = L0;
-                }
-                if (q1 < G) {
-                    mine[G * D + q1] = M1;
-                    mine[G * D + G + q1] = L1;
-                }
-            }
-        }
-        consumer_sync(kConsumers);               // s_ml and red are reused by the next unit
-    }
-}
-
-// Combines the split-KV chunk partials of one (shard, sequence, KV head)
-// group in chunk order with log-sum-exp weights; one CTA per group.
-template <int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnDecodeParams p) {
-    pdl_trigger();
-    pdl_wait();
-    constexpr int kMaxC = 128;                          // chunk statistics held in shared memory
-    __shared__ float s_m[kMaxC][kMaxGroup], s_l[kMaxC][kMaxGroup];
-    __shared__ float s_den[kMaxGroup], s_M[kMaxGroup];
-    const int gi = blockIdx.x, tid = threadIdx.x;
-    const int G = p.hq_s / p.hkv_s, pstride = G * (D + 2);
-    const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-    const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
-    const int nc = min(p.n_chunks, kMaxC);
-    if (p.n_chunks > kMaxC) set_status(p.status, TP_ERR_UNSUPPORTED);
-    // all chunks' (max, sum) in one parallel pass
-    for (int i = tid; i < nc * 2 * G; i += 256) {
-        const int cc = i / (2 * G), q = i - cc * 2 * G;
-        const float v = base[(size_t)cc * pstride + G * D + q];
-        if (q < G) s_m[cc][q] = v; else s_l[cc][q - G] = v;
-    }
-    __syncthreads();
-    if (tid < G) {
-        float M = -INFINITY;
-        for (int cc = 0; cc < nc; ++cc)
-            if (s_l[cc][tid] > 0.f) M = fmaxf(M, s_m[cc][tid]);
-        float den = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-            const float w = s_l[cc][tid] > 0.f ? expf(s_m[cc][tid] - M) : 0.f;
-            s_m[cc][tid] = w;                           // reuse as the chunk weight
-            den = fmaf(s_l[cc][tid], w, den);
-        }
-        s_den[tid] = den;
-        s_M[tid] = M;
-    }
-    __syncthreads();
-    const size_t qoff = ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)kh * G * D;
-    bf16* out = reinterpret_cast<bf16*>(p.out) + qoff;
-    for (int i = tid; i < G * D; i += 256) {
-        const int g = i / D;
-        float num = 0.f;
-        int cc = 0;
-        for (; cc + 8 <= nc; cc += 8) {                  // eight independent loads in flight
-            float v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = base[(size_t)(cc + q) * pstride + i];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) num = fmaf(v[q], s_m[cc + q][g], num);
-        }
-        for (; cc < nc; ++cc) num = fmaf(base[(size_t)cc * pstride + i], s_m[cc][g], num);
-        out[i] = __float2bfloat16_rn(num / s_den[g]);
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1509,12 +651,6 @@ cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaS
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-size_t gemv_stream_smem(int kc) {
-    (void)kc;
-    // ring | tile [64][8] | ss [8], positions [8], bias [64] (+pad)
-    return kCtrlBytes + (size_t)kGemvStages * kGemvStageBytes + (size_t)(kTileRows * kTMax + 96) * 4;
-}
-
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against the driver library); each distinct map is encoded once and cached.
 cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner, int box_rows, int swizzle128,
@@ -1556,55 +692,9 @@ static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap
     return tensor_map_2d(W, K, rows, kBoxK, box_rows, 0, out);
 }
 
-template <int EPI>
-static cudaError_t launch_gemv_stream(const GemvParams& p, cudaStream_t s) {
-    const size_t smem = gemv_stream_smem(p.shape.kc);
-    static int set_bytes = -1;
-    if ((int)smem > set_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        // full shared-memory carveout, so a CTA of the next kernel fits beside this one
-        e = cudaFuncSetAttribute(gemv_stream_kernel<EPI>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        set_bytes = (int)smem;
-    }
-    TmaGemvArgs A;
-    memset(&A, 0, sizeof A);
-    A.p = p;
-    for (int r = 0; r < p.n_shards; ++r) {
-        cudaError_t e = weight_tensor_map(p.W[r], p.K, p.rows, &A.tm[r]);
-        if (e != cudaSuccess) return e;
-    }
-    cudaError_t ex = weight_tensor_map(p.xact, p.K, p.n_shards * kTMax, &A.tmx, kTMax);
-    if (ex != cudaSuccess) return ex;
-    const int grid = p.shape.units() < 2 * kSMs ? p.shape.units() : 2 * kSMs;   // two CTAs per SM
-    void* args[] = {&A};
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(gemv_stream_kernel<EPI>), args, grid, smem, s, kStreamThreads);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kTMax, (p.H + 255) / 256);
-    cfg.blockDim = dim3(64);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = g_pdl ? 1 : 0;
-    void* args[] = {const_cast<NormPrepParams*>(&p)};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(norm_prep_kernel), args);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
+// fp32 projections (bf16 decode runs as one launch: launch_decode_step)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s) {
-    if (dtype == TP_BF16) {
-        if (epi == EPI_QKV_ROPE) return launch_gemv_stream<EPI_QKV_ROPE>(p, s);
-        if (epi == EPI_SWIGLU) return launch_gemv_stream<EPI_SWIGLU>(p, s);
-        return launch_gemv_stream<EPI_ROWPAR>(p, s);
-    }
+    if (dtype != TP_F32) return cudaErrorInvalidValue;
     if (epi == EPI_QKV_ROPE) return launch_gemv_t<float, EPI_QKV_ROPE>(p, s);
     if (epi == EPI_SWIGLU) return launch_gemv_t<float, EPI_SWIGLU>(p, s);
     return launch_gemv_t<float, EPI_ROWPAR>(p, s);
@@ -1626,101 +716,8 @@ static cudaError_t launch_attn_t(const AttnDecodeParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-size_t attn_stream_smem(int d) {
-    return kCtrlBytes + (size_t)kStages * kAttnStageBytes +
-           (size_t)(kMaxGroup * d + kMaxGroup * kAttnChunk + 8 * kMaxGroup * d + 2 * kMaxGroup + kTMax) * 4;
-}
-
-template <int D, int G>
-static cudaError_t launch_attn_stream(const AttnDecodeParams& p, cudaStream_t s) {
-    const size_t smem = attn_stream_smem(D);
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_stream_kernel<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
-    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
-    const int grid = U < 2 * kSMs ? U : 2 * kSMs;       // two CTAs per SM: more warps to hide latency
-    void* args[] = {const_cast<AttnDecodeParams*>(&p)};
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_stream_kernel<D, G>), args, grid, smem, s,
-                               kStreamThreads);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-template <int D>
-static cudaError_t launch_attn_stream_g(const AttnDecodeParams& p, cudaStream_t s) {
-    switch (p.hq_s / p.hkv_s) {
-        case 1: return launch_attn_stream<D, 1>(p, s);
-        case 2: return launch_attn_stream<D, 2>(p, s);
-        case 3: return launch_attn_stream<D, 3>(p, s);
-        case 4: return launch_attn_stream<D, 4>(p, s);
-        case 5: return launch_attn_stream<D, 5>(p, s);
-        case 6: return launch_attn_stream<D, 6>(p, s);
-        case 7: return launch_attn_stream<D, 7>(p, s);
-        default: return launch_attn_stream<D, 8>(p, s);
-    }
-}
-
-static cudaError_t launch_small_pdl(const void* fn, void** args, int grid, int threads, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(threads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = g_pdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-cudaError_t launch_rowpar_reduce(const GemvParams& p, cudaStream_t s) {
-    void* args[] = {const_cast<GemvParams*>(&p)};
-    return launch_small_pdl(reinterpret_cast<const void*>(rowpar_reduce_kernel), args, p.shape.groups,
-                            kTileRows * kTMax, s);
-}
-
-cudaError_t launch_attn_combine(const AttnDecodeParams& p, cudaStream_t s) {
-    void* args[] = {const_cast<AttnDecodeParams*>(&p)};
-    const void* fn = p.d == 64 ? reinterpret_cast<const void*>(attn_combine_kernel<64>)
-                               : reinterpret_cast<const void*>(attn_combine_kernel<128>);
-    return launch_small_pdl(fn, args, p.N * p.B * p.hkv_s, 256, s);
-}
-
-template <int D>
-static cudaError_t launch_attn_tc(const AttnDecodeParams& p, cudaStream_t s) {
-    using S = AtShape<D>;
-    const size_t smem = attn_tc_smem();
-    static bool set = false;
-    if (!set) {
-        cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        set = true;
-    }
-    if ((p.hq_s / p.hkv_s) * D > kAtSlot) return cudaErrorInvalidValue;
-    TmaAttnArgs A;
-    memset(&A, 0, sizeof A);
-    A.p = p;
-    const long rows = (long)p.max_batch * p.hkv_s * p.max_kv;
-    for (int r = 0; r < p.N; ++r) {
-        cudaError_t e = tensor_map_2d(p.kcache[r], D, rows, S::PT, kAtKeys, 0, &A.tk[r]);
-        if (e == cudaSuccess) e = tensor_map_2d(p.vcache[r], D, rows, S::PT, kAtKeys, 0, &A.tv[r]);
-        if (e != cudaSuccess) return e;
-    }
-    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
-    const int grid = U < kSMs ? U : kSMs;
-    void* args[] = {&A};
-    cudaError_t e = launch_pdl(reinterpret_cast<const void*>(attn_tc_kernel<D>), args, grid, smem, s, kStreamThreads);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s) {
-    if (dtype == TP_BF16) return p.d == 64 ? launch_attn_tc<64>(p, s) : launch_attn_tc<128>(p, s);
+    if (dtype != TP_F32) return cudaErrorInvalidValue;
     return p.d == 64 ? launch_attn_t<float, 64>(p, s) : launch_attn_t<float, 128>(p, s);
 }
 
@@ -1729,26 +726,31 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_
 // The whole decode step in one persistent launch (bf16).
 //
 // One CTA per SM runs every stage of the block as a phase:
-//   NORM -> QKV (+RoPE, KV append) -> ATTN (split-KV partials) -> COMBINE
-//   -> O_PROJ (partials) -> REDUCE (h, next norm operands) -> GATE_UP
-//   (+SwiGLU) -> DOWN (partials) -> REDUCE (y)
-// separated by grid barriers (a sense-reversing counter in the workspace,
-// every wait bounded). The producer thread streams the data of later
-// phases that does not depend on earlier ones -- every weight box, and every
-// K/V block except the one holding the new position -- through the same
-// 5-stage ring while the consumers are still in an earlier phase or waiting
-// at a barrier; only the activation boxes (and the new K/V rows) wait for
-// the barrier that publishes them. So HBM keeps streaming across phase
-// boundaries and no kernel boundary, launch gap or ramp remains inside the
-// step. The phases compute exactly what the separate kernels compute.
+//   NORM | QKV (+RoPE, KV append) | ATTN (+split-KV combine) |
+//   O_PROJ (+rank-ordered reduce, next norm operands) | GATE_UP (+SwiGLU) |
+//   DOWN (+rank-ordered reduce)
+// separated by five grid barriers (a monotonic arrival counter in the
+// workspace; every wait bounded). Each phase's work -- 256-element reduction
+// stages of the projections, or keys of the attention -- is laid out in one
+// flattened order and split evenly into one contiguous range per CTA, so
+// every SM streams the same number of bytes. A 64-row tile (or KV group)
+// whose range straddles two CTAs gets one fp32 partial per CTA; the CTA that
+// finishes last (a per-tile arrival counter) sums them in CTA order and runs
+// the epilogue, so results are deterministic and no extra phase is needed.
+// The producer thread streams the data of later phases that does not depend
+// on earlier ones -- every weight box, and every K/V block except the one
+// holding the new position -- through the same 5-stage ring while the
+// consumers are still busy or at a barrier; only the activation boxes (and
+// the new K/V rows) wait for the barrier that publishes them.
 // ===========================================================================
 
 namespace {
 constexpr int kSkRing = 5;
 constexpr int kSkStage = kGemvStageBytes;               // 36 KB: 2 weight boxes + activation box, or K+V of 64 keys
-constexpr int kSkPhases = 8;                            // barriers inside a step
+constexpr int kSkBarriers = 5;                          // grid barriers inside a step
 constexpr int kSkMaxPend = kSkRing;
 static_assert(kGemvStageBytes == kAtMaxStage, "the two stage formats share one slot size");
+static_assert(kStepStamps == 2 * (kSkBarriers + 1) + 1, "stamps: start, per phase streaming done + arrival");
 }  // namespace
 
 struct StepArgs {
@@ -1756,11 +758,11 @@ struct StepArgs {
     CUtensorMap xm[4];                      // their activation operands (boxes kBoxK x 8)
     CUtensorMap tk[TP_MAX_SHARDS];          // K / V caches (boxes 72 or 64 x 64 keys)
     CUtensorMap tv[TP_MAX_SHARDS];
-    GemvParams g[4];                        // qkv, o, gate_up, down
-    AttnDecodeParams a;
+    GemvParams g[4];                        // qkv, o, gate_up, down; shape.chunks = partial slots per tile
+    AttnDecodeParams a;                     // n_chunks = partial slots per KV group
     NormPrepParams np;
     unsigned long long* bar;                // grid-barrier arrival counter (only grows)
-    unsigned long long* stamps;             // optional [grid][kStepStamps]: start, 8 barrier arrivals, end (ns)
+    unsigned long long* stamps;             // optional [grid][kStepStamps]: start, barrier arrivals, end (ns)
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -1770,7 +772,7 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 }
 
 // Grid barrier k of a step has passed once the arrival counter reaches
-// base + k * gridDim.x. The counter only grows (by kSkPhases * gridDim.x per
+// base + k * gridDim.x. The counter only grows (by kSkBarriers * gridDim.x per
 // step, every CTA arriving at every barrier even after an error), so `base`
 // is the multiple of that amount at or below the value read at the start.
 __device__ __forceinline__ bool sk_passed(const unsigned long long* bar, unsigned long long base, unsigned k) {
@@ -1792,18 +794,135 @@ __device__ __forceinline__ bool sk_wait_gen(const unsigned long long* bar, unsig
     }
 }
 
-// Consumer side of grid barrier k: every consumer thread of the CTA has
-// finished the phase; thread 0 arrives with a release reduction (no reply
-// to wait for) and polls the counter with acquire loads.
-__device__ __forceinline__ void sk_barrier(unsigned long long* bar, unsigned long long base, unsigned k,
-                                           volatile int* abort, int* status, unsigned long long* stamp) {
-    consumer_sync(kConsumers);
-    if (threadIdx.x == 0) {
-        if (stamp) *stamp = global_ns();
-        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
-        sk_wait_gen(bar, base, k, abort, status);
+// ---- flattened work split ------------------------------------------------------
+
+// Per-CTA share of W work items (at least `min_r`, so partial slots per tile
+// stay bounded for any grid size up to kMaxStepCtas).
+__device__ __forceinline__ int sk_share(int W, int min_r) {
+    const int r = (W + (int)gridDim.x - 1) / (int)gridDim.x;
+    return r > min_r ? r : min_r;
+}
+
+// Projection tiles ("segments"): column-parallel -- one 64-row tile of one
+// shard per group (decode_unit with one unit per group); row-parallel -- the
+// shards of 64-row output tile tb are segments tb*N .. tb*N + N-1. Each has
+// S = ceil(K / 256) stages; stage f of the phase is stage f % S of segment f / S.
+__device__ __forceinline__ void sk_segment(const GemvParams& p, int epi, int seg, int& r, int& tb) {
+    if (epi == EPI_ROWPAR) {
+        tb = seg / p.n_shards;
+        r = seg - tb * p.n_shards;
+    } else {
+        const int rb = p.shape.groups / p.n_shards;
+        r = seg / rb;
+        tb = seg - r * rb;
     }
-    consumer_sync(kConsumers);
+}
+
+__device__ __forceinline__ int sk_nseg(const GemvParams& p, int epi) {
+    return epi == EPI_ROWPAR ? p.shape.groups * p.n_shards : p.shape.groups;
+}
+
+// Stages per CTA of a projection phase. Column-parallel phases take whole
+// tiles (a tile split over CTAs would need a cross-CTA finish before its
+// epilogue, which costs more than the imbalance). A row-parallel phase either
+// gives each CTA whole output tiles -- every shard's piece, reduced in rank
+// order inside the CTA (whole_tiles) -- or is split evenly, its pieces then
+// reduced by the CTA that finishes last.
+__device__ __forceinline__ int sk_phase_share(const GemvParams& p, int epi, int S) {
+    const int nseg = sk_nseg(p, epi);
+    if (epi != EPI_ROWPAR) return S * ((nseg + (int)gridDim.x - 1) / (int)gridDim.x);
+    if (p.whole_tiles)                                  // every shard of an output tile in one CTA
+        return S * p.n_shards * ((p.shape.groups + (int)gridDim.x - 1) / (int)gridDim.x);
+    const int W = nseg * S;
+    return sk_share(W, (W + kMaxStepCtas - 1) / kMaxStepCtas);
+}
+
+// CTAs that own stages of segment `seg`: first .. last.
+__device__ __forceinline__ void sk_owners(int seg, int S, int R, int& first, int& last) {
+    first = (seg * S) / R;
+    last = (seg * S + S - 1) / R;
+}
+
+// ---- attention key space -------------------------------------------------------
+
+// Groups (shard r, sequence b, KV head kh) in order ((r * B + b) * Hkv' + kh),
+// each holding len_b = min(pos_b + 1, max_kv) keys, laid end to end.
+struct KeySpace {
+    int len[kTMax];
+    int pre[kTMax + 1];      // keys of sequences before b, times Hkv'
+    int per_r;               // keys of one shard
+    int total;
+};
+
+__device__ __forceinline__ KeySpace sk_keyspace(const AttnDecodeParams& p, const int* posv) {
+    KeySpace ks;
+    ks.pre[0] = 0;
+#pragma unroll
+    for (int b = 0; b < kTMax; ++b) {
+        const int l = b < p.B ? min(max(posv[b] + 1, 0), p.max_kv) : 0;
+        ks.len[b] = l;
+        ks.pre[b + 1] = ks.pre[b] + l * p.hkv_s;
+    }
+    ks.per_r = ks.pre[kTMax];
+    ks.total = ks.per_r * p.N;
+    return ks;
+}
+
+// Group holding flattened key k, the key's offset in it, and the group's
+// first flattened key.
+__device__ __forceinline__ void sk_locate(const KeySpace& ks, const AttnDecodeParams& p, int k, int& gi, int& b,
+                                          int& off, int& gstart) {
+    const int r = k / ks.per_r;
+    const int rem = k - r * ks.per_r;
+    b = 0;
+#pragma unroll
+    for (int bb = 1; bb < kTMax; ++bb)
+        if (bb < p.B && ks.pre[bb] <= rem) b = bb;
+    const int rem2 = rem - ks.pre[b];
+    const int kh = rem2 / ks.len[b];
+    off = rem2 - kh * ks.len[b];
+    gi = (r * p.B + b) * p.hkv_s + kh;
+    gstart = r * ks.per_r + ks.pre[b] + kh * ks.len[b];
+}
+
+// ---- finisher warp ----------------------------------------------------------------
+//
+// The consumer warps never wait for another CTA. When a piece of a tile (or
+// KV group) that other CTAs share is stored, or a phase is done, consumer
+// thread 0 posts a job to a small shared-memory queue and the consumers go
+// on streaming. A tenth warp takes the jobs in order: it publishes the
+// CTA's stores, counts the arrival for the tile, and if this CTA arrived last
+// it sums the pieces in CTA order and runs the epilogue; a phase-end job is
+// the CTA's arrival at the grid barrier, after every earlier job is done.
+
+constexpr int kJobs = 8;
+enum SkJobType : int { JOB_COL = 0, JOB_ROW = 1, JOB_ATTN = 2, JOB_PHASE = 3, JOB_END = 4 };
+struct SkJob {
+    int type, pi, idx;
+    unsigned expected;
+};
+constexpr int kMaxFin = 16;             // finishes one CTA can owe in a phase
+struct SkQueue {
+    SkJob job[kJobs];
+    uint64_t full[kJobs];
+    uint64_t empty[kJobs];
+    uint64_t drained;                   // the finisher has taken every job up to a phase end
+    SkJob fin[kMaxFin];                 // tiles / groups this CTA arrived last on, this phase
+    int n_fin;
+};
+
+// Consumer thread 0 only: the stores the job covers were made before a
+// consumer_sync; the mbarrier arrival orders them before the finisher's wait.
+__device__ __forceinline__ void sk_post(SkQueue* qu, uint32_t& jn, int type, int pi, int idx, unsigned expected,
+                                        volatile int* abort, int* status) {
+    const int sl = jn % kJobs;
+    mbar_wait(&qu->empty[sl], ((jn / kJobs) & 1) ^ 1, abort, status);
+    qu->job[sl].type = type;
+    qu->job[sl].pi = pi;
+    qu->job[sl].idx = idx;
+    qu->job[sl].expected = expected;
+    mbar_arrive(&qu->full[sl]);
+    ++jn;
 }
 
 // ---- producer helpers -------------------------------------------------------
@@ -1816,8 +935,7 @@ struct SkPend {
     unsigned need[kSkMaxPend];
 };
 
-// Issues every pending activation box whose barrier has passed, waiting for
-// the barriers in order (oldest first).
+// Issues every pending activation box, waiting for the barriers in order.
 __device__ __forceinline__ bool sk_flush(SkPend& pd, const StepArgs& A, unsigned char* ring, uint64_t* full,
                                          unsigned long long gen0, volatile int* abort, int* status) {
     bool ok = true;
@@ -1848,35 +966,34 @@ __device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, 
                                                 uint64_t* full, uint64_t* empty, uint32_t& it, SkPend& pd,
                                                 unsigned long long gen0, volatile int* abort, uint64_t pol) {
     const GemvParams& p = A.g[wi];
-    const int U = p.shape.units();
-    const int kc = p.shape.kc;
-    const int spu = (kc + kBoxK - 1) / kBoxK;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        int gi, r, tb, chunk;
-        decode_unit(p, epi, u, gi, r, tb, chunk);
+    const int S = (p.K + kBoxK - 1) / kBoxK;
+    const int W = sk_nseg(p, epi) * S;
+    const int R = sk_phase_share(p, epi, S);
+    const int f0 = min((int)blockIdx.x * R, W), f1 = min(f0 + R, W);
+    for (int f = f0; f < f1; ++f, ++it) {
+        const int seg = f / S, st = f - seg * S;
+        int r, tb;
+        sk_segment(p, epi, seg, r, tb);
         const int rowa = tile_row(epi, tb, 0, p.head_dim, p.ffn_s);
         const int rowb = tile_row(epi, tb, 32, p.head_dim, p.ffn_s);
-        const int k0 = chunk * kc;
-        for (int st = 0; st < spu; ++st, ++it) {
-            const int sl = it % kSkRing;
-            sk_before_reuse(pd, it, A, ring, full, gen0, abort, p.status);
-            if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
-            mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
-            unsigned char* dst = ring + sl * kSkStage;
-            tma_load_2d(dst, &A.wm[wi][r], k0 + st * kBoxK, rowa, &full[sl], pol);
-            tma_load_2d(dst + kBoxBytes, &A.wm[wi][r], k0 + st * kBoxK, rowb, &full[sl], pol);
-            if (pd.n == 0 && sk_passed(A.bar, gen0, need)) {
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                tma_load_2d_keep(dst + 2 * kBoxBytes, &A.xm[wi], k0 + st * kBoxK, r * kTMax, &full[sl]);
-            } else {
-                pd.stage[pd.n] = it;
-                pd.slot[pd.n] = sl;
-                pd.x[pd.n] = k0 + st * kBoxK;
-                pd.y[pd.n] = r * kTMax;
-                pd.map[pd.n] = wi;
-                pd.need[pd.n] = need;
-                ++pd.n;
-            }
+        const int sl = it % kSkRing;
+        sk_before_reuse(pd, it, A, ring, full, gen0, abort, p.status);
+        if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
+        mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
+        unsigned char* dst = ring + sl * kSkStage;
+        tma_load_2d(dst, &A.wm[wi][r], st * kBoxK, rowa, &full[sl], pol);
+        tma_load_2d(dst + kBoxBytes, &A.wm[wi][r], st * kBoxK, rowb, &full[sl], pol);
+        if (pd.n == 0 && sk_passed(A.bar, gen0, need)) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            tma_load_2d_keep(dst + 2 * kBoxBytes, &A.xm[wi], st * kBoxK, r * kTMax, &full[sl]);
+        } else {
+            pd.stage[pd.n] = it;
+            pd.slot[pd.n] = sl;
+            pd.x[pd.n] = st * kBoxK;
+            pd.y[pd.n] = r * kTMax;
+            pd.map[pd.n] = wi;
+            pd.need[pd.n] = need;
+            ++pd.n;
         }
     }
     return true;
@@ -1888,19 +1005,26 @@ __device__ __forceinline__ bool sk_produce_attn(unsigned need, const StepArgs& A
                                                 volatile int* abort, uint64_t pol, const int* posv) {
     using S = AtShape<D>;
     const AttnDecodeParams& p = A.a;
-    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
+    pdl_wait();                                         // cache rows and positions of the preceding step
+    const KeySpace ks = sk_keyspace(p, posv);
+    const int R = sk_share(ks.total, step_min_keys(p.max_kv));
+    const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
     bool passed = false;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int c = u % p.n_chunks, gi = u / p.n_chunks;
-        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+    // segments in reverse order: a block holding a new position (a group's last
+    // keys) comes last in the CTA's range, so everything before it can stream
+    // while the QKV phase is still running
+    for (int ke = k1; ke > k0;) {
+        int gi, b, off, gstart;
+        sk_locate(ks, p, ke - 1, gi, b, off, gstart);
+        const int k = max(k0, gstart);
+        sk_locate(ks, p, k, gi, b, off, gstart);
+        const int seg_len = ke - k;
+        const int kh = gi % p.hkv_s, r = gi / (p.hkv_s * p.B);
+        const int row0 = (b * p.hkv_s + kh) * p.max_kv + off;
         const int pos = posv[b];
-        const int Lk = min(pos + 1, p.max_kv);
-        const int j0 = c * kAttnChunk;
-        const int n = max(0, min(Lk - j0, kAttnChunk));
-        const int row0 = (b * p.hkv_s + kh) * p.max_kv + j0;
-        for (int k0 = 0; k0 < n; k0 += kAtKeys, ++it) {
+        for (int j = 0; j < seg_len; j += kAtKeys, ++it) {
             // the block holding the new position is written by the QKV phase
-            if (!passed && j0 + k0 + kAtKeys > pos) {
+            if (!passed && off + j + kAtKeys > pos) {
                 sk_flush(pd, A, ring, full, gen0, abort, p.status);
                 sk_wait_gen(A.bar, gen0, need, abort, p.status);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -1913,10 +1037,11 @@ __device__ __forceinline__ bool sk_produce_attn(unsigned need, const StepArgs& A
             unsigned char* st = ring + sl * kSkStage;
 #pragma unroll
             for (int h = 0; h < S::NB; ++h) {
-                tma_load_2d(st + h * S::BOX, &A.tk[r], h * 64, row0 + k0, &full[sl], pol);
-                tma_load_2d(st + (S::NB + h) * S::BOX, &A.tv[r], h * 64, row0 + k0, &full[sl], pol);
+                tma_load_2d(st + h * S::BOX, &A.tk[r], h * 64, row0 + j, &full[sl], pol);
+                tma_load_2d(st + (S::NB + h) * S::BOX, &A.tv[r], h * 64, row0 + j, &full[sl], pol);
             }
         }
+        ke = k;
     }
     return true;
 }
@@ -1955,41 +1080,320 @@ __device__ __forceinline__ void sk_norm(const NormPrepParams& p) {
     }
 }
 
-// One projection phase on the consumer side (the units of this CTA).
+// Epilogue of a column-parallel tile whose full sum is in `tile` ([64][8]).
+// Threads tid0, tid0 + nthr, ... of the caller share the outputs. The bias of
+// the tile's rows comes from s_bias (shared) or, when null, from global memory.
 template <int EPI>
-__device__ __forceinline__ void sk_gemv(const GemvParams& p, unsigned char* ring, uint64_t* full, uint64_t* empty,
-                                        volatile int* abort, uint32_t& it, float* tile, float* ss, int* s_pos,
-                                        float* s_bias) {
+__device__ __forceinline__ void sk_col_epilogue(const GemvParams& p, int r, int tb, const float* tile, const float* ss,
+                                                const int* s_pos, const float* s_bias, int tid0 = -1,
+                                                int nthr = kConsumers) {
+    const int tid = tid0 < 0 ? (int)threadIdx.x : tid0, T = p.T;
+    if (EPI == EPI_SWIGLU) {
+        bf16* out = reinterpret_cast<bf16*>(p.act_out);
+        const float inv_k = 1.0f / (float)p.K;
+        for (int i = tid; i < 32 * T; i += nthr) {
+            const int t = i >> 5, j = i & 31;
+            const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
+            const float gt = tile[j * kTMax + t] * rinv;
+            const float up = tile[(j + 32) * kTMax + t] * rinv;
+            out[((size_t)r * kTMax + t) * p.ffn_s + tb * 32 + j] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+        }
+    } else {
+        const int d = p.head_dim, half = d >> 1;
+        const float inv_k = 1.0f / (float)p.K;
+        for (int i = tid; i < 32 * T; i += nthr) {
+            const int t = i >> 5, j = i & 31;
+            const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
+            const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
+            const int head = rowA / d, ii = rowA - head * d;
+            float ba = 0.f, bb = 0.f;
+            if (s_bias) {
+                ba = s_bias[j];
+                bb = s_bias[j + 32];
+            } else if (p.bias[r]) {
+                ba = p.bias[r][rowA];
+                bb = p.bias[r][rowA + half];
+            }
+            float va = tile[j * kTMax + t] * rinv + ba;
+            float vb = tile[(j + 32) * kTMax + t] * rinv + bb;
+            const int pos = s_pos[t];
+            if (head < p.hq_s + p.hkv_s) {
+                float cs, sn;
+                sincosf((float)pos * exp2f(-(2.0f * ii / d) * (float)p.log2_theta), &sn, &cs);
+                const float ra = va * cs - vb * sn, rb = va * sn + vb * cs;
+                va = ra;
+                vb = rb;
+            }
+            if (head < p.hq_s) {
+                float* q = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
+                q[0] = va;
+                q[half] = vb;
+            } else {
+                const bool is_k = head < p.hq_s + p.hkv_s;
+                const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
+                if (pos < 0 || pos >= p.max_kv) {
+                    set_status(p.status, TP_ERR_CAPACITY);
+                    continue;
+                }
+                bf16* cache = reinterpret_cast<bf16*>(is_k ? p.kcache[r] : p.vcache[r]);
+                bf16* dst = cache + (((size_t)t * p.hkv_s + kvh) * p.max_kv + pos) * d + ii;
+                dst[0] = __float2bfloat16_rn(va);
+                dst[half] = __float2bfloat16_rn(vb);
+            }
+        }
+    }
+}
+
+// ---- finishing tiles and groups shared by several CTAs -----------------------
+
+// Finisher warp: publishes the CTA's stores covered by the job and counts its
+// arrival for the tile or group; true in the CTA that arrived last (which
+// resets the counter and will read every piece).
+__device__ __forceinline__ bool fin_arrive(unsigned* cnt, unsigned expected) {
+    unsigned last = 0;
+    if ((threadIdx.x & 31) == 0) {
+        __threadfence();
+        const unsigned old = atomicAdd(cnt, 1u);
+        last = old + 1 == expected;
+        if (last) {
+            *cnt = 0u;
+            __threadfence();
+        }
+    }
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
+}
+
+// Consumers: column-parallel tile `seg` -- the pieces summed in CTA order into
+// `tile`, then the epilogue (the tile's bias read from global memory).
+template <int EPI>
+__device__ __forceinline__ void sk_col_finish(const GemvParams& p, int seg, int np, float* tile, const float* ss,
+                                              const int* s_pos) {
+    const int tid = threadIdx.x;
+    constexpr int kMaxSplit = 8;
+    const int nsplit = p.shape.chunks;
+    for (int i = tid * 2; i < kTileRows * kTMax; i += kConsumers * 2) {
+        float2 v[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+            if (q < np) v[q] = __ldcg(reinterpret_cast<const float2*>(p.part + ((size_t)seg * nsplit + q) * kPartStride + i));
+        float2 acc = v[0];
+#pragma unroll
+        for (int q = 1; q < kMaxSplit; ++q)
+            if (q < np) acc = make_float2(acc.x + v[q].x, acc.y + v[q].y);
+        for (int q = kMaxSplit; q < np; ++q) {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(p.part + ((size_t)seg * nsplit + q) * kPartStride + i));
+            acc = make_float2(acc.x + x.x, acc.y + x.y);
+        }
+        *reinterpret_cast<float2*>(tile + i) = acc;
+    }
+    consumer_sync(kConsumers);
+    int r, tb;
+    sk_segment(p, EPI, seg, r, tb);
+    sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, nullptr);
+    consumer_sync(kConsumers);
+}
+
+// Consumers: row-parallel output tile tb -- pieces (CTA order) within each
+// rank, then ranks in order, then the residual; with norm_out also the next
+// norm's operands and per-(8-row slice, token) sums of squares. One 8-row
+// slice per warp; lane = (row, token pair).
+__device__ __forceinline__ void sk_row_finish(const GemvParams& p, int tb, int S, int R) {
+    constexpr int kPer = 2;                            // pieces per shard held in registers
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j8 = lane >> 2, tp = lane & 3;
+    const int j = warp * 8 + j8;
+    const int nsplit = p.shape.chunks;
+    auto piece = [&](int r, int c) {
+        return reinterpret_cast<const float2*>(p.part + ((size_t)(tb * p.n_shards + r) * nsplit + c) * kPartStride +
+                                               j * kTMax + 2 * tp);
+    };
+    int cnt_r[TP_MAX_SHARDS];
+    float2 v[TP_MAX_SHARDS][kPer];
+#pragma unroll
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        cnt_r[r] = 0;
+        if (r < p.n_shards) {
+            int first, last;
+            sk_owners(tb * p.n_shards + r, S, R, first, last);
+            cnt_r[r] = last - first + 1;
+#pragma unroll
+            for (int c = 0; c < kPer; ++c)
+                if (c < cnt_r[r]) v[r][c] = __ldcg(piece(r, c));
+        }
+    }
+    float2 total = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        if (r < p.n_shards) {
+            float2 pr = v[r][0];
+#pragma unroll
+            for (int c = 1; c < kPer; ++c)
+                if (c < cnt_r[r]) pr = make_float2(pr.x + v[r][c].x, pr.y + v[r][c].y);
+            for (int c = kPer; c < cnt_r[r]; ++c) {
+                const float2 x = __ldcg(piece(r, c));
+                pr = make_float2(pr.x + x.x, pr.y + x.y);
+            }
+            total = r == 0 ? pr : make_float2(total.x + pr.x, total.y + pr.y);
+        }
+    }
+    const int row = tb * kTileRows + j;
+    float sq[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int t = 2 * tp + e;
+        float yv = 0.f;
+        if (t < p.T) {
+            const size_t o = (size_t)t * p.rows + row;
+            yv = p.resid[o] + (e ? total.y : total.x);
+            p.y[o] = yv;
+            if (p.norm_out) {
+                bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
+                for (int r2 = 0; r2 < p.n_shards; ++r2)
+                    nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
+            }
+        }
+        sq[e] = yv * yv;
+    }
+    if (p.norm_out) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
+            sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
+        }
+        if (j8 == 0) {
+            const size_t item = (size_t)tb * 8 + warp;
+            p.ss_tiles_out[item * kTMax + 2 * tp] = sq[0];
+            p.ss_tiles_out[item * kTMax + 2 * tp + 1] = sq[1];
+        }
+    }
+}
+
+// Consumers: output tile tb of a row-parallel phase whose rank-ordered sum
+// over the shards is in `acc` ([64][8]): residual, next norm operands, sums of
+// squares (layout as in sk_row_finish).
+__device__ __forceinline__ void sk_row_epilogue(const GemvParams& p, int tb, const float* acc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j8 = lane >> 2, tp = lane & 3;
+    const int j = warp * 8 + j8;
+    const int row = tb * kTileRows + j;
+    float sq[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int t = 2 * tp + e;
+        float yv = 0.f;
+        if (t < p.T) {
+            const size_t o = (size_t)t * p.rows + row;
+            yv = p.resid[o] + acc[j * kTMax + t];
+            p.y[o] = yv;
+            if (p.norm_out) {
+                bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
+                for (int r2 = 0; r2 < p.n_shards; ++r2)
+                    nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
+            }
+        }
+        sq[e] = yv * yv;
+    }
+    if (p.norm_out) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
+            sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
+        }
+        if (j8 == 0) {
+            const size_t item = (size_t)tb * 8 + warp;
+            p.ss_tiles_out[item * kTMax + 2 * tp] = sq[0];
+            p.ss_tiles_out[item * kTMax + 2 * tp + 1] = sq[1];
+        }
+    }
+}
+
+// Consumers: KV group gi -- the pieces' (max, sum, unnormalised output)
+// combined with log-sum-exp weights in CTA order. `wgt` holds [pieces][8]
+// weights, `lsum` the same for the sums, `s_inv` 8 reciprocals.
+template <int D>
+__device__ __forceinline__ void sk_attn_finish(const AttnDecodeParams& p, int gi, int nc, float* wgt, float* lsum,
+                                               float* s_inv) {
+    const int tid = threadIdx.x;
+    const int G = p.hq_s / p.hkv_s, pstride = G * (D + 2);
+    const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
+    for (int i = tid; i < nc * G; i += kConsumers) {
+        const int cc = i / G, q = i - cc * G;
+        wgt[cc * kMaxGroup + q] = __ldcg(base + (size_t)cc * pstride + G * D + q);
+        lsum[cc * kMaxGroup + q] = __ldcg(base + (size_t)cc * pstride + G * D + G + q);
+    }
+    consumer_sync(kConsumers);
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int cc = 0; cc < nc; ++cc)
+            if (lsum[cc * kMaxGroup + tid] > 0.f) M = fmaxf(M, wgt[cc * kMaxGroup + tid]);
+        float den = 0.f;
+        for (int cc = 0; cc < nc; ++cc) {
+            const float l = lsum[cc * kMaxGroup + tid];
+            const float w = l > 0.f ? expf(wgt[cc * kMaxGroup + tid] - M) : 0.f;
+            wgt[cc * kMaxGroup + tid] = w;
+            den = fmaf(l, w, den);
+        }
+        s_inv[tid] = den > 0.f ? 1.0f / den : 0.f;
+    }
+    consumer_sync(kConsumers);
+    const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
+    bf16* out = reinterpret_cast<bf16*>(p.out) + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)kh * G * D;
+    constexpr int kMaxSplit = 8;
+    for (int i = tid; i < G * D; i += kConsumers) {
+        const int gq = i / D;
+        float v[kMaxSplit];
+#pragma unroll
+        for (int cc = 0; cc < kMaxSplit; ++cc)
+            if (cc < nc) v[cc] = __ldcg(base + (size_t)cc * pstride + i);
+        float num = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kMaxSplit; ++cc)
+            if (cc < nc) num = fmaf(v[cc], wgt[cc * kMaxGroup + gq], num);
+        for (int cc = kMaxSplit; cc < nc; ++cc)
+            num = fmaf(__ldcg(base + (size_t)cc * pstride + i), wgt[cc * kMaxGroup + gq], num);
+        out[i] = __float2bfloat16_rn(num * s_inv[gq]);
+    }
+    consumer_sync(kConsumers);
+}
+
+// One projection phase on the consumer side: this CTA's stage range, one
+// segment (tile of one shard) at a time.
+template <int EPI>
+__device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned char* ring, uint64_t* full,
+                                        uint64_t* empty, volatile int* abort, uint32_t& it, float* tile, float* acc,
+                                        float* ss, int* s_pos, float* s_bias, SkQueue* qu, uint32_t& jn) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int U = p.shape.units();
-    const int kc = p.shape.kc;
-    const int spu = (kc + kBoxK - 1) / kBoxK;
+    const int S = (p.K + kBoxK - 1) / kBoxK;
+    const int W = sk_nseg(p, EPI) * S;
+    const int R = sk_phase_share(p, EPI, S);
+    const int f0 = min((int)blockIdx.x * R, W), f1 = min(f0 + R, W);
     const int wm = warp & 3, wk = warp >> 2;
     const int g = lane >> 2, tq = lane & 3;
     const int box = wm >> 1, brow = 16 * (wm & 1) + g;
-    const int T = p.T;
-    if ((int)blockIdx.x >= U) return;
-    if (EPI == EPI_QKV_ROPE && tid < kTMax) s_pos[tid] = tid < T ? p.pos[tid] : 0;
+    if (f0 >= f1) return;
+    if (EPI == EPI_QKV_ROPE && tid < kTMax) s_pos[tid] = tid < p.T ? p.pos[tid] : 0;
     if (EPI != EPI_ROWPAR) {
         float a = 0.f;                                 // warp t: token t
-        if (warp < T)
+        if (warp < p.T)
             for (int q = lane; q < p.n_ss_tiles; q += 32) a += p.ss_tiles[q * kTMax + warp];
         a = warp_sum(a);
         if (lane == 0) ss[warp] = a;
     }
     consumer_sync(kConsumers);
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        int gi, r, tb, chunk;
-        decode_unit(p, EPI, u, gi, r, tb, chunk);
+    for (int f = f0; f < f1;) {
+        const int seg = f / S, st0 = f - seg * S;
+        const int st1 = min(S, st0 + (f1 - f));       // this CTA's stages of the segment: [st0, st1)
+        int r, tb;
+        sk_segment(p, EPI, seg, r, tb);
         float bias_v = 0.f;
         if (EPI == EPI_QKV_ROPE && tid < kTileRows && p.bias[r])
             bias_v = p.bias[r][tile_row(EPI_QKV_ROPE, tb, tid, p.head_dim, 0)];
         float c[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int st = 0; st < spu; ++st, ++it) {
+        for (int st = st0; st < st1; ++st, ++it) {
             const int sl = it % kSkRing;
             mbar_wait(&full[sl], (it / kSkRing) & 1, abort, p.status);
             __syncwarp();
-            const int steps_here = min(kBoxK / kKStep, (kc - st * kBoxK) / kKStep);
+            const int steps_here = min(kBoxK / kKStep, (p.K - st * kBoxK) / kKStep);
             const unsigned char* stage = ring + sl * kSkStage;
             const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
             const unsigned char* wB = wA + 8 * (kBoxK * 2);
@@ -2011,6 +1415,8 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, unsigned char* ring
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[sl]);
         }
+        f += st1 - st0;
+        // this CTA's sum over its stages of the segment: (half 0) + (half 1)
         const int i0 = (16 * wm + g) * kTMax + 2 * tq, i1 = (16 * wm + g + 8) * kTMax + 2 * tq;
         if (wk == 0) {
             tile[i0] = c[0];
@@ -2027,98 +1433,90 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, unsigned char* ring
             tile[i1 + 1] += c[3];
         }
         consumer_sync(kConsumers);
-        if (EPI == EPI_ROWPAR) {
-            float* mine = p.part + (size_t)u * kPartStride;
-            for (int i = tid * 4; i < kTileRows * kTMax; i += kConsumers * 4)
-                *reinterpret_cast<float4*>(mine + i) = *reinterpret_cast<const float4*>(tile + i);
-        } else if (EPI == EPI_SWIGLU) {
-            bf16* out = reinterpret_cast<bf16*>(p.act_out);
-            const float inv_k = 1.0f / (float)p.K;
-            for (int i = tid; i < 32 * T; i += kConsumers) {
-                const int t = i >> 5, j = i & 31;
-                const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
-                const float gt = tile[j * kTMax + t] * rinv;
-                const float up = tile[(j + 32) * kTMax + t] * rinv;
-                out[((size_t)r * kTMax + t) * p.ffn_s + tb * 32 + j] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+        int first, last;
+        sk_owners(seg, S, R, first, last);
+        const int nsplit = p.shape.chunks;
+        if (EPI == EPI_ROWPAR && p.whole_tiles) {       // this CTA holds every shard of output tile tb
+            for (int i = tid; i < kTileRows * kTMax; i += kConsumers)
+                acc[i] = r == 0 ? tile[i] : acc[i] + tile[i];   // ((p0 + p1) + p2) + ...
+            consumer_sync(kConsumers);
+            if (r == p.n_shards - 1) {
+                sk_row_epilogue(p, tb, acc);
+                consumer_sync(kConsumers);
             }
-        } else {
-            const int d = p.head_dim, half = d >> 1;
-            const float inv_k = 1.0f / (float)p.K;
-            for (int i = tid; i < 32 * T; i += kConsumers) {
-                const int t = i >> 5, j = i & 31;
-                const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
-                const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
-                const int head = rowA / d, ii = rowA - head * d;
-                float va = tile[j * kTMax + t] * rinv + s_bias[j];
-                float vb = tile[(j + 32) * kTMax + t] * rinv + s_bias[j + 32];
-                const int pos = s_pos[t];
-                if (head < p.hq_s + p.hkv_s) {
-                    float cs, sn;
-                    sincosf((float)pos * exp2f(-(2.0f * ii / d) * (float)p.log2_theta), &sn, &cs);
-                    const float ra = va * cs - vb * sn, rb = va * sn + vb * cs;
-                    va = ra;
-                    vb = rb;
+            continue;
+        }
+        if (EPI != EPI_ROWPAR && first == last) {      // the whole tile was this CTA's
+            sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, s_bias);
+            consumer_sync(kConsumers);
+            continue;
+        }
+        float* mine = p.part + ((size_t)seg * nsplit + ((int)blockIdx.x - first)) * kPartStride;
+        for (int i = tid * 4; i < kTileRows * kTMax; i += kConsumers * 4)
+            *reinterpret_cast<float4*>(mine + i) = *reinterpret_cast<const float4*>(tile + i);
+        consumer_sync(kConsumers);                      // the piece is stored; `tile` may be reused
+        if (tid == 0) {
+            if (EPI == EPI_ROWPAR) {
+                // the last piece of output tile tb posts the job that counts the tile's arrivals
+                unsigned expected = 0;
+                for (int r2 = 0; r2 < p.n_shards; ++r2) {
+                    int a1, a2;
+                    sk_owners(tb * p.n_shards + r2, S, R, a1, a2);
+                    expected += (unsigned)(a2 - a1 + 1);
                 }
-                if (head < p.hq_s) {
-                    float* q = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
-                    q[0] = va;
-                    q[half] = vb;
-                } else {
-                    const bool is_k = head < p.hq_s + p.hkv_s;
-                    const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
-                    if (pos < 0 || pos >= p.max_kv) {
-                        set_status(p.status, TP_ERR_CAPACITY);
-                        continue;
-                    }
-                    bf16* cache = reinterpret_cast<bf16*>(is_k ? p.kcache[r] : p.vcache[r]);
-                    bf16* dst = cache + (((size_t)t * p.hkv_s + kvh) * p.max_kv + pos) * d + ii;
-                    dst[0] = __float2bfloat16_rn(va);
-                    dst[half] = __float2bfloat16_rn(vb);
-                }
+                sk_post(qu, jn, JOB_ROW, pi, tb, expected, abort, p.status);
+            } else {
+                sk_post(qu, jn, JOB_COL, pi, seg, (unsigned)(last - first + 1), abort, p.status);
             }
         }
-        consumer_sync(kConsumers);
     }
 }
 
-// Attention phase on the consumer side: the units of attn_tc_kernel, with
-// every warp waiting for and releasing every stage (the ring is shared with
-// the projection phases, whose stages all eight warps release).
+// Attention phase on the consumer side: this CTA's key range, one group
+// segment at a time (every warp waits for and releases every stage; the
+// 64-key blocks of a segment alternate between warps 0-3 and 4-7). A segment
+// holding a whole group writes the normalised output directly; otherwise
+// the CTA stores (max, sum, unnormalised output) and the last of the group's
+// CTAs combines them in CTA order.
 template <int D>
 __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char* ring, uint64_t* full,
-                                        uint64_t* empty, volatile int* abort, uint32_t& it_unit, float* red,
-                                        float* s_ml, const int* s_pos) {
+                                        uint64_t* empty, volatile int* abort, uint32_t& it, float* red,
+                                        float* s_ml2, float* s_cmb, const int* s_pos, SkQueue* qu, uint32_t& jn) {
     using S = AtShape<D>;
     constexpr int KS = D / 16;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.hq_s / p.hkv_s;
-    const int U = p.N * p.B * p.hkv_s * p.n_chunks;
     const int grp = warp >> 2, wq = warp & 3;
     const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;
     const uint32_t ring_u32 = smem_u32(ring);
     const int q0 = 2 * t, q1 = 2 * t + 1;
-    (void)tid;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int c = u % p.n_chunks, gi = u / p.n_chunks;
-        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-        const int pos = s_pos[b];
-        const int Lk = min(pos + 1, p.max_kv);
-        const int j0 = c * kAttnChunk;
-        const int n = max(0, min(Lk - j0, kAttnChunk));
+    const int pstride = G * (D + 2);
+    const KeySpace ks = sk_keyspace(p, s_pos);
+    const int R = sk_share(ks.total, step_min_keys(p.max_kv));
+    const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
+    int ui = 0;
+    for (int ke = k1; ke > k0; ++ui) {                  // segments in reverse order (as the producer)
+        int gi, b, off, gstart;
+        sk_locate(ks, p, ke - 1, gi, b, off, gstart);
+        const int k = max(k0, gstart);
+        const int len = ks.len[b];
+        const int n = ke - k;                           // keys of this segment
+        ke = k;
+        const int kh = gi % p.hkv_s, r = gi / (p.hkv_s * p.B);
         const int nblk = (n + kAtKeys - 1) / kAtKeys;
         uint32_t qb[KS][2];
         {
             const float* qp = p.q + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
+            for (int kk = 0; kk < KS; ++kk) {
                 if (g < G) {
-                    const float2 a = *reinterpret_cast<const float2*>(qp + 16 * ks + 2 * t);
-                    const float2 c2 = *reinterpret_cast<const float2*>(qp + 16 * ks + 8 + 2 * t);
-                    qb[ks][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
-                    qb[ks][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
+                    const float2 a = *reinterpret_cast<const float2*>(qp + 16 * kk + 2 * t);
+                    const float2 c2 = *reinterpret_cast<const float2*>(qp + 16 * kk + 8 + 2 * t);
+                    qb[kk][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+                    qb[kk][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
                 } else {
-                    qb[ks][0] = qb[ks][1] = 0u;
+                    qb[kk][0] = qb[kk][1] = 0u;
                 }
             }
         }
@@ -2126,29 +1524,28 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
 #pragma unroll
         for (int dt = 0; dt < KS; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        for (int blk = 0; blk < nblk; ++blk) {
-            const uint32_t it = it_unit + blk;
+        for (int blk = 0; blk < nblk; ++blk, ++it) {
             const int sl = it % kSkRing;
             mbar_wait(&full[sl], (it / kSkRing) & 1, abort, p.status);
             __syncwarp();
             if ((blk & 1) == grp) {
                 const uint32_t kpart = ring_u32 + sl * kSkStage, vpart = kpart + S::NB * S::BOX;
-                const int kb = blk * kAtKeys + 16 * wq;
+                const int kb = blk * kAtKeys + 16 * wq;          // relative to the segment
                 float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
+                for (int kk = 0; kk < KS; ++kk) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(at_addr<D>(kpart, 16 * wq + rr + 8 * (mi & 1), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                    mma_bf16_16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    ldsm_x4(at_addr<D>(kpart, 16 * wq + rr + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+                    mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
                 }
                 const bool v0 = kb + g < n, v1 = kb + g + 8 < n;
                 const float x00 = v0 ? sc[0] : -INFINITY, x01 = v0 ? sc[1] : -INFINITY;
                 const float x10 = v1 ? sc[2] : -INFINITY, x11 = v1 ? sc[3] : -INFINITY;
                 float mq0 = fmaxf(x00, x10), mq1 = fmaxf(x01, x11);
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mq0 = fmaxf(mq0, __shfl_xor_sync(0xffffffffu, mq0, off));
-                    mq1 = fmaxf(mq1, __shfl_xor_sync(0xffffffffu, mq1, off));
+                for (int sh = 4; sh < 32; sh <<= 1) {
+                    mq0 = fmaxf(mq0, __shfl_xor_sync(0xffffffffu, mq0, sh));
+                    mq1 = fmaxf(mq1, __shfl_xor_sync(0xffffffffu, mq1, sh));
                 }
                 const float n0 = fmaxf(m0, mq0), n1 = fmaxf(m1, mq1);
                 const float al0 = (n0 == -INFINITY) ? 1.f : expf(m0 - n0);
@@ -2159,9 +1556,9 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
                 const float p11 = (x11 == -INFINITY) ? 0.f : expf(x11 - n1);
                 float ps0 = p00 + p10, ps1 = p01 + p11;
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
-                    ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+                for (int sh = 4; sh < 32; sh <<= 1) {
+                    ps0 += __shfl_xor_sync(0xffffffffu, ps0, sh);
+                    ps1 += __shfl_xor_sync(0xffffffffu, ps1, sh);
                 }
                 l0 = l0 * al0 + ps0;
                 l1 = l1 * al1 + ps1;
@@ -2188,7 +1585,10 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[sl]);
         }
-        it_unit += nblk;
+
+        // ---- merge the eight warps: common max per query, every warp's rescaled
+        // output into its slot, then all threads sum the slots in warp order
+        float* s_ml = s_ml2 + (ui & 1) * (8 * kMaxGroup * 2);   // double-buffered across segments
         if (g == 0) {
             s_ml[(warp * kMaxGroup + q0) * 2] = m0;
             s_ml[(warp * kMaxGroup + q0) * 2 + 1] = l0;
@@ -2204,194 +1604,140 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
         }
         const float c0 = (m0 == -INFINITY) ? 0.f : expf(m0 - M0);
         const float c1 = (m1 == -INFINITY) ? 0.f : expf(m1 - M1);
+        float* dst = red + warp * kAtSlot;
 #pragma unroll
         for (int dt = 0; dt < KS; ++dt) {
-            o[dt][0] *= c0;
-            o[dt][1] *= c1;
-            o[dt][2] *= c0;
-            o[dt][3] *= c1;
+            if (q0 < G) {
+                dst[q0 * D + 16 * dt + g] = o[dt][0] * c0;
+                dst[q0 * D + 16 * dt + g + 8] = o[dt][2] * c0;
+            }
+            if (q1 < G) {
+                dst[q1 * D + 16 * dt + g] = o[dt][1] * c1;
+                dst[q1 * D + 16 * dt + g + 8] = o[dt][3] * c1;
+            }
         }
-        for (int half = 4; half >= 1; half >>= 1) {
-            if (warp >= half && warp < 2 * half) {
-                float* dst = red + (warp - half) * kAtSlot;
-#pragma unroll
-                for (int dt = 0; dt < KS; ++dt) {
-                    if (q0 < G) {
-                        dst[q0 * D + 16 * dt + g] = o[dt][0];
-                        dst[q0 * D + 16 * dt + g + 8] = o[dt][2];
-                    }
-                    if (q1 < G) {
-                        dst[q1 * D + 16 * dt + g] = o[dt][1];
-                        dst[q1 * D + 16 * dt + g + 8] = o[dt][3];
-                    }
-                }
+        if (tid < G) {                                  // this segment's (max, sum) per query
+            float M = -INFINITY;
+            for (int w = 0; w < 8; ++w) M = fmaxf(M, s_ml[(w * kMaxGroup + tid) * 2]);
+            float L = 0.f;
+            for (int w = 0; w < 8; ++w) {
+                const float mw = s_ml[(w * kMaxGroup + tid) * 2];
+                if (mw != -INFINITY) L += s_ml[(w * kMaxGroup + tid) * 2 + 1] * expf(mw - M);
             }
-            consumer_sync(kConsumers);
-            if (warp < half) {
-                const float* src = red + warp * kAtSlot;
-#pragma unroll
-                for (int dt = 0; dt < KS; ++dt) {
-                    if (q0 < G) {
-                        o[dt][0] += src[q0 * D + 16 * dt + g];
-                        o[dt][2] += src[q0 * D + 16 * dt + g + 8];
-                    }
-                    if (q1 < G) {
-                        o[dt][1] += src[q1 * D + 16 * dt + g];
-                        o[dt][3] += src[q1 * D + 16 * dt + g + 8];
-                    }
-                }
-            }
-            consumer_sync(kConsumers);
-        }
-        if (warp == 0 && (unsigned)u < p.part_units) {
-            float* mine = p.part + (size_t)u * G * (D + 2);
-#pragma unroll
-            for (int dt = 0; dt < KS; ++dt) {
-                if (q0 < G) {
-                    mine[q0 * D + 16 * dt + g] = o[dt][0];
-                    mine[q0 * D + 16 * dt + g + 8] = o[dt][2];
-                }
-                if (q1 < G) {
-                    mine[q1 * D + 16 * dt + g] = o[dt][1];
-                    mine[q1 * D + 16 * dt + g + 8] = o[dt][3];
-                }
-            }
-            if (g == 0) {
-                float L0 = 0.f, L1 = 0.f;
-                for (int w = 0; w < 8; ++w) {
-                    const float mw0 = s_ml[(w * kMaxGroup + q0) * 2], mw1 = s_ml[(w * kMaxGroup + q1) * 2];
-                    if (mw0 != -INFINITY) L0 += s_ml[(w * kMaxGroup + q0) * 2 + 1] * expf(mw0 - M0);
-                    if (mw1 != -INFINITY) L1 += s_ml[(w * kMaxGroup + q1) * 2 + 1] * expf(mw1 - M1);
-                }
-                if (q0 < G) {
-                    mine[G * D + q0] = M0;
-                    mine[G * D + G + q0] = L0;
-                }
-                if (q1 < G) {
-                    mine[G * D + q1] = M1;
-                    mine[G * D + G + q1] = L1;
-                }
-            }
+            s_cmb[tid] = M;
+            s_cmb[kMaxGroup + tid] = L;
         }
         consumer_sync(kConsumers);
+        const int first = gstart / R, last = (gstart + len - 1) / R;
+        bf16* out = reinterpret_cast<bf16*>(p.out) + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)kh * G * D;
+        if (first == last) {                            // the whole group: normalise and store
+            for (int i = tid; i < G * D; i += kConsumers) {
+                float acc = red[i];
+#pragma unroll
+                for (int w = 1; w < 8; ++w) acc += red[w * kAtSlot + i];
+                const float L = s_cmb[kMaxGroup + i / D];
+                out[i] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+            }
+            continue;                                   // slots are rewritten after the next segment's first barrier
+        }
+        float* mine = p.part + ((size_t)gi * p.n_chunks + ((int)blockIdx.x - first)) * pstride;
+        for (int i = tid; i < G * D; i += kConsumers) {
+            float acc = red[i];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) acc += red[w * kAtSlot + i];
+            mine[i] = acc;
+        }
+        if (tid < G) {
+            mine[G * D + tid] = s_cmb[tid];
+            mine[G * D + G + tid] = s_cmb[kMaxGroup + tid];
+        }
+        consumer_sync(kConsumers);                      // the piece is stored; the slots may be reused
+        if (tid == 0) sk_post(qu, jn, JOB_ATTN, 0, gi, (unsigned)(last - first + 1), abort, p.status);
     }
 }
 
-// Split-KV combine: one (group, query head) item per warp, all SMs. Lanes
-// hold the chunk statistics (chunk = lane, lane + 32, ...), the warp forms
-// the common maximum and denominator, then each lane combines four output
-// elements at a time in chunk order.
-template <int D>
-__device__ __forceinline__ void sk_combine(const AttnDecodeParams& p) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = p.hq_s / p.hkv_s, pstride = G * (D + 2);
-    const int n_groups = p.N * p.B * p.hkv_s;
-    const int nc = p.n_chunks;
-    for (int item = blockIdx.x * 8 + warp; item < n_groups * G; item += gridDim.x * 8) {
-        const int gi = item / G, gq = item - gi * G;
-        const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-        const float* base = p.part + (size_t)gi * nc * pstride;
-        float M = -INFINITY;
-        for (int cc = lane; cc < nc; cc += 32) {
-            const float l = base[(size_t)cc * pstride + G * D + G + gq];
-            if (l > 0.f) M = fmaxf(M, base[(size_t)cc * pstride + G * D + gq]);
-        }
-        M = warp_max(M);
-        float den = 0.f;
-        for (int cc = lane; cc < nc; cc += 32) {
-            const float l = base[(size_t)cc * pstride + G * D + G + gq];
-            if (l > 0.f) den = fmaf(l, expf(base[(size_t)cc * pstride + G * D + gq] - M), den);
-        }
-        den = warp_sum(den);
-        const float inv = den > 0.f ? 1.0f / den : 0.f;
-        bf16* out = reinterpret_cast<bf16*>(p.out) + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + gq) * D;
-        for (int d0 = lane * 4; d0 < D; d0 += 128) {
-            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc = 0; cc < nc; ++cc) {
-                const float* pc = base + (size_t)cc * pstride;
-                const float l = pc[G * D + G + gq];
-                const float w = l > 0.f ? expf(pc[G * D + gq] - M) : 0.f;
-                // the partial stride G*(D+2) floats need not be a multiple of 4: scalar loads
-                const float* pv = pc + gq * D + d0;
-                num.x = fmaf(pv[0], w, num.x);
-                num.y = fmaf(pv[1], w, num.y);
-                num.z = fmaf(pv[2], w, num.z);
-                num.w = fmaf(pv[3], w, num.w);
-            }
-            uint2 pk;
-            pk.x = pack_bf16x2(num.x * inv, num.y * inv);
-            pk.y = pack_bf16x2(num.z * inv, num.w * inv);
-            *reinterpret_cast<uint2*>(out + d0) = pk;
-        }
-    }
-}
-
-// Rank-ordered reduction of a row-parallel phase's partials: one 8-row slice
-// of a 64-row tile per warp, all SMs; lane = (row, token pair). Chunks are
-// summed in order within each rank, then ranks in order, then the residual.
-// With norm_out it writes the next norm's operands (y * gamma_r, bf16, every
-// shard) and per-(8-row slice, token) sums of squares.
-__device__ __forceinline__ void sk_reduce(const GemvParams& p) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int upg = p.shape.units_per_group(), C = p.shape.chunks;
-    const int j8 = lane >> 2, tp = lane & 3;
-    for (int item = blockIdx.x * 8 + warp; item < p.shape.groups * 8; item += gridDim.x * 8) {
-        const int tb = item >> 3, sl = item & 7;
-        const int j = sl * 8 + j8;                     // row within the tile
-        const float* base = p.part + (size_t)tb * upg * kPartStride + j * kTMax + 2 * tp;
-        float2 v[kMaxGroupUnits];
-#pragma unroll
-        for (int q = 0; q < kMaxGroupUnits; ++q)
-            if (q < upg) v[q] = *reinterpret_cast<const float2*>(base + (size_t)q * kPartStride);
-        float2 total = make_float2(0.f, 0.f), pr = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < kMaxGroupUnits; ++q) {
-            if (q < upg) {
-                const int cc = q % C;
-                pr = (cc == 0) ? v[q] : make_float2(pr.x + v[q].x, pr.y + v[q].y);
-                if (cc == C - 1) total = (q < C) ? pr : make_float2(total.x + pr.x, total.y + pr.y);
-            }
-        }
-        const int row = tb * kTileRows + j;
-        float sq[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int t = 2 * tp + e;
-            float yv = 0.f;
-            if (t < p.T) {
-                const size_t o = (size_t)t * p.rows + row;
-                yv = p.resid[o] + (e ? total.y : total.x);
-                p.y[o] = yv;
-                if (p.norm_out) {
-                    bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
-                    for (int r2 = 0; r2 < p.n_shards; ++r2)
-                        nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
-                }
-            }
-            sq[e] = yv * yv;
-        }
-        if (p.norm_out) {
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
-                sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
-            }
-            if (j8 == 0) {
-                p.ss_tiles_out[(size_t)item * kTMax + 2 * tp] = sq[0];
-                p.ss_tiles_out[(size_t)item * kTMax + 2 * tp + 1] = sq[1];
-            }
-        }
-    }
-}
+constexpr int kStepThreads = kStreamThreads + 32;       // + the finisher warp
 
 size_t decode_step_smem() {
-    // ring | red [4][kAtSlot] | s_ml [8][8][2] | tile [64][8] | ss, pos, bias, wsum
+    // ring | red [8][kAtSlot] | s_ml [2][8][8][2] | tile [64][8] | ss, pos, bias | s_cmb | ftile [64][8] | queue
     return 1024 + (size_t)kSkRing * kSkStage +
-           (size_t)(4 * kAtSlot + 8 * kMaxGroup * 2 + kTileRows * kTMax + kTMax + kTMax + 96 + 8) * 4;
+           (size_t)(8 * kAtSlot + 2 * 8 * kMaxGroup * 2 + kTileRows * kTMax + kTMax + kTMax + 96 + 2 * kMaxGroup +
+                    kTileRows * kTMax) * 4 +
+           sizeof(SkQueue);
+}
+
+// The finisher warp: the jobs of the consumers, in order. Piece jobs are
+// counted for their tile or group; a tile or group this CTA arrived last on
+// goes to the CTA's finish list. A phase-end job releases the consumers, who
+// run the finish list with all their threads.
+__device__ __forceinline__ void sk_finisher(const StepArgs& A, SkQueue* qu, volatile int* abort) {
+    const int lane = threadIdx.x & 31;
+    int* status = A.a.status;
+    for (uint32_t fj = 0;; ++fj) {
+        const int sl = fj % kJobs;
+        const bool ok = mbar_wait(&qu->full[sl], (fj / kJobs) & 1, abort, status);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, ok)) return;       // the consumers stopped posting (error already set)
+        const SkJob j = qu->job[sl];
+        if (j.type == JOB_COL || j.type == JOB_ROW || j.type == JOB_ATTN) {
+            unsigned* cnt = j.type == JOB_ATTN ? A.a.cnt : A.g[j.pi].cnt;
+            if (fin_arrive(cnt + j.idx, j.expected) && lane == 0) {
+                if (qu->n_fin < kMaxFin) qu->fin[qu->n_fin++] = j;
+                else set_status(status, TP_ERR_UNSUPPORTED);
+            }
+        } else if (lane == 0) {
+            mbar_arrive(&qu->drained);                   // every earlier job is done
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qu->empty[sl]);
+        if (j.type == JOB_END) return;
+    }
+}
+
+// Consumers at the end of phase k (k = 1..kSkBarriers; k = kSkBarriers + 1 is
+// the last phase, which has no barrier): hand the phase end to the finisher,
+// run the finishes this CTA owes, then arrive at grid barrier k and wait.
+template <int D>
+__device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long long base, unsigned k,
+                                             volatile int* abort, SkQueue* qu, uint32_t& jn, float* tile,
+                                             const float* ss, const int* s_pos, float* red, float* s_inv,
+                                             unsigned long long* st) {
+    int* status = A.a.status;
+    consumer_sync(kConsumers);
+    if (threadIdx.x == 0) {
+        if (st) st[2 * k - 1] = global_ns();
+        sk_post(qu, jn, k > kSkBarriers ? JOB_END : JOB_PHASE, 0, (int)k, 0u, abort, status);
+    }
+    mbar_wait(&qu->drained, (k - 1) & 1, abort, status);
+    const int nf = *reinterpret_cast<volatile int*>(&qu->n_fin);
+    for (int f = 0; f < nf; ++f) {
+        const SkJob j = qu->fin[f];
+        if (j.type == JOB_COL) {
+            if (j.pi == 0) sk_col_finish<EPI_QKV_ROPE>(A.g[0], j.idx, (int)j.expected, tile, ss, s_pos);
+            else sk_col_finish<EPI_SWIGLU>(A.g[2], j.idx, (int)j.expected, tile, ss, s_pos);
+        } else if (j.type == JOB_ROW) {
+            const GemvParams& p = A.g[j.pi];
+            const int S = (p.K + kBoxK - 1) / kBoxK;
+            sk_row_finish(p, j.idx, S, sk_phase_share(p, EPI_ROWPAR, S));
+        } else {
+            sk_attn_finish<D>(A.a, j.idx, (int)j.expected, red, red + 32 * kMaxGroup, s_inv);
+        }
+    }
+    consumer_sync(kConsumers);
+    if (threadIdx.x == 0) {
+        qu->n_fin = 0;
+        if (st) st[2 * k] = global_ns();
+        if (k <= kSkBarriers) {
+            asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(A.bar) : "memory");
+            sk_wait_gen(A.bar, base, k, abort, status);
+            __threadfence();
+        }
+    }
+    consumer_sync(kConsumers);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kStreamThreads, 1) decode_step_kernel(const __grid_constant__ StepArgs A) {
+__global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ StepArgs A) {
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kSkRing;
@@ -2399,12 +1745,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_step_kernel(const __
     unsigned long long* s_gen0 = reinterpret_cast<unsigned long long*>(smem + 16 * kSkRing + 8);
     unsigned char* ring = smem + 1024;
     float* red = reinterpret_cast<float*>(ring + kSkRing * kSkStage);
-    float* s_ml = red + 4 * kAtSlot;
-    float* tile = s_ml + 8 * kMaxGroup * 2;
+    float* s_ml = red + 8 * kAtSlot;
+    float* tile = s_ml + 2 * 8 * kMaxGroup * 2;
     float* ss = tile + kTileRows * kTMax;
     int* s_pos = reinterpret_cast<int*>(ss + kTMax);
     float* s_bias = reinterpret_cast<float*>(s_pos + kTMax);
-    float* wsum = s_bias + 96;
+    float* s_cmb = s_bias + 96;
+    float* ftile = s_cmb + 2 * kMaxGroup;
+    SkQueue* qu = reinterpret_cast<SkQueue*>(ftile + kTileRows * kTMax);
     int* status = A.a.status;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -2413,17 +1761,25 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_step_kernel(const __
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumers / 32);
         }
+        for (int i = 0; i < kJobs; ++i) {
+            mbar_init(&qu->full[i], 1);
+            mbar_init(&qu->empty[i], 1);
+        }
+        mbar_init(&qu->drained, 1);
+        qu->n_fin = 0;
         *abort_flag = (smem_u32(ring) & 127u) ? 1 : 0;
         if (*abort_flag) set_status(status, TP_ERR_ALIGN);
         // read before this CTA arrives anywhere: fewer than gridDim.x arrivals of
         // this step can precede it
-        const unsigned long long per_step = (unsigned long long)kSkPhases * gridDim.x;
+        const unsigned long long per_step = (unsigned long long)kSkBarriers * gridDim.x;
         const unsigned long long c = ld_acquire_u64(A.bar);
         *s_gen0 = c - c % per_step;
         fence_mbar_init();
     }
     __syncthreads();
     const unsigned long long gen0 = *s_gen0;
+    unsigned long long* st =
+        A.stamps && blockIdx.x < kMaxStepCtas ? A.stamps + (size_t)blockIdx.x * kStepStamps : nullptr;
 
     if (warp == kConsumers / 32) {                     // ---- producer
         if (lane == 0 && !*abort_flag) {
@@ -2431,13 +1787,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_step_kernel(const __
             uint32_t it = 0;
             SkPend pd;
             pd.n = 0;
+            // weights do not depend on the preceding step: QKV streams at once; the
+            // activation boxes wait for barrier 1, which follows the consumers' wait
+            bool ok = sk_produce_gemv(EPI_QKV_ROPE, 0, 1, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            pdl_wait();
             int posv[kTMax];
             for (int b = 0; b < kTMax; ++b) posv[b] = b < A.a.B ? A.a.pos[b] : 0;
-            bool ok = sk_produce_gemv(EPI_QKV_ROPE, 0, 1, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
             if (ok) ok = sk_produce_attn<D>(2, A, ring, full, empty, it, pd, gen0, abort_flag, pol, posv);
-            if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 1, 4, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
-            if (ok) ok = sk_produce_gemv(EPI_SWIGLU, 2, 6, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
-            if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 3, 7, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 1, 3, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            if (ok) ok = sk_produce_gemv(EPI_SWIGLU, 2, 4, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
+            if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 3, 5, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
             sk_flush(pd, A, ring, full, gen0, abort_flag, status);
             // no copy may still be landing when the CTA exits
             volatile int no_abort = 0;
@@ -2446,32 +1805,30 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_step_kernel(const __
         }
         return;
     }
+    if (warp == kConsumers / 32 + 1) {                 // ---- finisher
+        sk_finisher(A, qu, abort_flag);
+        return;
+    }
 
     // ---- consumers
-    unsigned long long* st = A.stamps && blockIdx.x < kMaxStepCtas ? A.stamps + (size_t)blockIdx.x * kStepStamps : nullptr;
     if (st && tid == 0) st[0] = global_ns();
-    if (tid < kTMax) s_pos[tid] = tid < A.a.B ? A.a.pos[tid] : 0;
-    uint32_t it = 0;
-    sk_norm(A.np);
-    sk_barrier(A.bar, gen0, 1, abort_flag, status, st ? st + 1 : nullptr);
-    sk_gemv<EPI_QKV_ROPE>(A.g[0], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
-    sk_barrier(A.bar, gen0, 2, abort_flag, status, st ? st + 2 : nullptr);
+    pdl_wait();                                         // x, positions and caches of the preceding step
     if (tid < kTMax) s_pos[tid] = tid < A.a.B ? A.a.pos[tid] : 0;
     consumer_sync(kConsumers);
-    sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_pos);
-    sk_barrier(A.bar, gen0, 3, abort_flag, status, st ? st + 3 : nullptr);
-    sk_combine<D>(A.a);
-    sk_barrier(A.bar, gen0, 4, abort_flag, status, st ? st + 4 : nullptr);
-    sk_gemv<EPI_ROWPAR>(A.g[1], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
-    sk_barrier(A.bar, gen0, 5, abort_flag, status, st ? st + 5 : nullptr);
-    sk_reduce(A.g[1]);
-    sk_barrier(A.bar, gen0, 6, abort_flag, status, st ? st + 6 : nullptr);
-    sk_gemv<EPI_SWIGLU>(A.g[2], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
-    sk_barrier(A.bar, gen0, 7, abort_flag, status, st ? st + 7 : nullptr);
-    sk_gemv<EPI_ROWPAR>(A.g[3], ring, full, empty, abort_flag, it, tile, ss, s_pos, s_bias);
-    sk_barrier(A.bar, gen0, 8, abort_flag, status, st ? st + 8 : nullptr);
-    sk_reduce(A.g[3]);
-    if (st && tid == 0) st[kStepStamps - 1] = global_ns();
+    uint32_t it = 0, jn = 0;
+    sk_norm(A.np);
+    sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qu, jn);
+    sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    pdl_trigger();                                      // the next launch may start streaming its weights
+    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
 }
 
 cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
@@ -2487,15 +1844,13 @@ cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
         int dev = 0, sms = 0, per_sm = 0;
         e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStreamThreads, smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStepThreads, smem);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        grid_sz[which] = sms;                          // one CTA per SM
+        grid_sz[which] = sms < kMaxStepCtas ? sms : kMaxStepCtas;   // one CTA per SM
     }
     StepArgs A;
     memset(&A, 0, sizeof A);
-    const int epis[4] = {EPI_QKV_ROPE, EPI_ROWPAR, EPI_SWIGLU, EPI_ROWPAR};
-    (void)epis;
     for (int i = 0; i < 4; ++i) {
         const GemvParams& p = P.g[i];
         A.g[i] = p;
@@ -2519,14 +1874,19 @@ cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
     A.stamps = P.stamps;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_sz[which]);
-    cfg.blockDim = dim3(kStreamThreads);
+    cfg.blockDim = dim3(kStepThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    // One CTA per SM and every SM taken: once the preceding kernel's CTAs have
+    // left, all of this grid is resident (the grid barriers rely on it; their
+    // waits are bounded, so a grid that could not become resident would end
+    // with TP_ERR_TIMEOUT, not hang). Programmatic serialization lets CTAs start
+    // streaming weights on SMs the preceding step has already left.
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl ? 1 : 0;
     void* args[] = {&A};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -53,7 +53,9 @@ struct tp_plan_s {
     size_t esz = 4;                     // bytes per stored weight/KV element
     // decode launch shapes
     GemvShape g_qkv, g_o, g_gu, g_down;
-    int attn_chunks = 0, attn_groups = 0;
+    int attn_chunks = 0, attn_groups = 0, step_chunks = 0;
+    int step_split[4] = {0, 0, 0, 0};   // partial slots per tile of each projection phase (one-launch step)
+    size_t off_step_part = 0;           // their partials (one region, reused phase after phase)
     // workspace layout (byte offsets)
     size_t off_status = 0, off_cnt_qkv = 0, off_cnt_attn = 0, off_cnt_o = 0, off_cnt_gu = 0,
            off_cnt_down = 0, off_step_bar = 0, ctrl_bytes = 0;
@@ -230,6 +232,11 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->g_gu = make_shape((int)(N * I.ffn_shard / 32), 1, (int)H, P->esz);
         P->g_down = make_shape((int)(H / kTileRows), (int)N, (int)I.ffn_shard, P->esz);
         P->attn_chunks = (int)((d->max_kv + kAttnChunk - 1) / kAttnChunk);
+        // one-launch step: a KV group is split over at most ceil(max_kv / keys per CTA) + 1 <= 32 CTAs
+        {
+            const int mk = step_min_keys((int)d->max_kv);
+            P->step_chunks = (int)((d->max_kv + mk - 1) / mk) + 1;
+        }
         P->attn_groups = (int)(N * (d->max_batch < kTMax ? d->max_batch : kTMax) * I.hkv_shard);
         P->off_cnt_qkv = take(sizeof(unsigned) * P->g_qkv.groups);
         P->off_cnt_attn = take(sizeof(unsigned) * P->attn_groups);
@@ -242,7 +249,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
     if (dense) {
         const int64_t hd = d->head_dim, G = d->n_heads / d->n_kv_heads;
         P->off_q = take((size_t)kTMax * d->n_heads * hd * 4);
-        P->off_attn_part = take((size_t)P->attn_groups * P->attn_chunks * G * (hd + 2) * 4);
+        P->off_attn_part = take((size_t)P->attn_groups * std::max(P->attn_chunks, P->step_chunks) * G * (hd + 2) * 4);
         P->off_attn_out = take((size_t)kTMax * d->n_heads * hd * esz);
         P->off_h = take((size_t)kTMax * H * 4);
         P->off_act = take((size_t)kTMax * d->ffn * esz);
@@ -255,6 +262,20 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_hg = take((size_t)N * kTMax * H * 2);
         P->off_ss_tiles = take((size_t)(H / 8) * kTMax * 4);
         P->off_stamps = take((size_t)kMaxStepCtas * kStepStamps * 8);
+        {
+            // projection phases of the one-launch step: segments x stages, split
+            // evenly over at most kMaxStepCtas CTAs (each CTA takes >= W / kMaxStepCtas)
+            const int64_t segs[4] = {P->g_qkv.groups, P->g_o.groups * N, P->g_gu.groups, P->g_down.groups * N};
+            const int64_t Ks[4] = {H, I.hq_shard * hd, H, I.ffn_shard};
+            size_t need = 0;
+            for (int i = 0; i < 4; ++i) {
+                const int64_t S = (Ks[i] + 255) / 256, W = segs[i] * S;
+                const int64_t rmin = (W + kMaxStepCtas - 1) / kMaxStepCtas;
+                P->step_split[i] = (int)((S + rmin - 1) / rmin + 1);
+                need = std::max(need, (size_t)segs[i] * P->step_split[i] * kPartStride * 4);
+            }
+            P->off_step_part = take(need);
+        }
         P->ws_decode_end = off;
     }
     if (dense && d->dtype == TP_BF16) {
@@ -577,6 +598,9 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     DecodeStepParams st{};
     st.np = np;
     st.g[0] = q;
+    float* part = reinterpret_cast<float*>(ws + P->off_step_part);
+    st.g[0].part = part;
+    st.g[0].shape.chunks = P->step_split[0];
 
     AttnDecodeParams& a = st.a;
     a.q = q.q_out;
@@ -592,13 +616,13 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     a.d = hd;
     a.max_kv = (int)d.max_kv;
     a.max_batch = (int)d.max_batch;
-    a.n_chunks = P->attn_chunks;
+    a.n_chunks = P->step_chunks;
     a.scale = (float)(1.0 / std::sqrt((double)hd));
     a.part = reinterpret_cast<float*>(ws + P->off_attn_part);
     a.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_attn);
     a.out = ws + P->off_attn_out;
     a.status = status;
-    a.part_units = (unsigned)(P->attn_groups * P->attn_chunks);
+    a.part_units = (unsigned)(P->attn_groups * P->step_chunks);
 
     float* h = reinterpret_cast<float*>(ws + P->off_h);
     GemvParams& o = st.g[1];
@@ -607,7 +631,9 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     o.K = (int)(I.hq_shard * hd);
     o.T = T;
     o.shape = P->g_o;
-    o.part = reinterpret_cast<float*>(ws + P->off_part_o);
+    o.shape.chunks = P->step_split[1];
+    o.part = part;
+    o.whole_tiles = 1;                                  // 64 output tiles x every shard: reduced inside each CTA
     o.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_o);
     o.status = status;
     o.resid = x;
@@ -626,6 +652,9 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     g.K = (int)d.hidden;
     g.T = T;
     g.shape = P->g_gu;
+    g.shape.chunks = P->step_split[2];
+    g.part = part;
+    g.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_gu);
     g.eps = (float)d.eps;
     g.status = status;
     g.act_out = ws + P->off_act;
@@ -644,7 +673,9 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     dn.K = (int)I.ffn_shard;
     dn.T = T;
     dn.shape = P->g_down;
-    dn.part = reinterpret_cast<float*>(ws + P->off_part_down);
+    dn.shape.chunks = P->step_split[3];
+    dn.part = part;
+    dn.cnt = reinterpret_cast<unsigned*>(ws + P->off_cnt_down);
     dn.status = status;
     dn.resid = h;
     dn.y = y;
@@ -654,6 +685,8 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     st.bar = reinterpret_cast<unsigned long long*>(ws + P->off_step_bar);
     st.stamps = P->n_stage_ev > 0 ? reinterpret_cast<unsigned long long*>(ws + P->off_stamps) : nullptr;
     P->last_stamps_ws = st.stamps ? ws : nullptr;
+    // with per-step events recorded around the launch, launch without programmatic overlap
+    set_pdl(P->n_stage_ev == 0);
     stage_mark(P, 0, s);
     cudaError_t e = launch_decode_step(st, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: decode step launch");
@@ -709,7 +742,6 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     }
     const bool bf = d.dtype == TP_BF16;
     cudaError_t e;
-    if (!bf) stage_mark(P, 0, s);
     if (bf) {
         // bf16 projections take their RMSNorm operands pre-scaled:
         // x * gamma_r for every shard, and sum(x^2) per token
@@ -726,6 +758,8 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         q.n_ss_tiles = (int)((d.hidden + 255) / 256);
         return decode_step_bf16(P, w, kv, x, y, pos, B, ws, s, q, np);
     }
+    // fp32: one launch per stage
+    stage_mark(P, 0, s);
     e = launch_gemv(q, EPI_QKV_ROPE, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: qkv launch");
 
@@ -753,10 +787,6 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     stage_mark(P, 1, s);
     e = launch_attn_decode(a, d.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: attention launch");
-    if (bf) {
-        e = launch_attn_combine(a, s);
-        if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: attention combine launch");
-    }
 
     float* h = reinterpret_cast<float*>(ws + P->off_h);
     GemvParams o{};
@@ -775,14 +805,8 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         o.act[r] = ws + P->off_attn_out + (size_t)r * kTMax * o.K * es;
         o.gamma2[r] = w->gamma_ffn[r];
     }
-    if (bf) {
-        o.xact = ws + P->off_attn_out;
-        o.norm_out = ws + P->off_hg;
-        o.ss_tiles_out = reinterpret_cast<float*>(ws + P->off_ss_tiles);
-    }
     stage_mark(P, 2, s);
     e = launch_gemv(o, EPI_ROWPAR, d.dtype, s);
-    if (e == cudaSuccess && bf) e = launch_rowpar_reduce(o, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: o_proj launch");
 
     GemvParams g{};
@@ -801,11 +825,6 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
     for (int r = 0; r < N; ++r) {
         g.W[r] = w->wgu[r];
         g.gamma[r] = w->gamma_ffn[r];
-    }
-    if (bf) {
-        g.xact = ws + P->off_hg;
-        g.ss_tiles = reinterpret_cast<const float*>(ws + P->off_ss_tiles);
-        g.n_ss_tiles = (int)(d.hidden / kTileRows);
     }
     stage_mark(P, 3, s);
     e = launch_gemv(g, EPI_SWIGLU, d.dtype, s);
@@ -826,10 +845,8 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         dn.W[r] = w->wd[r];
         dn.act[r] = ws + P->off_act + (size_t)r * kTMax * dn.K * es;
     }
-    if (bf) dn.xact = ws + P->off_act;
     stage_mark(P, 4, s);
     e = launch_gemv(dn, EPI_ROWPAR, d.dtype, s);
-    if (e == cudaSuccess && bf) e = launch_rowpar_reduce(dn, s);
     if (e != cudaSuccess) return cuda_fail(e, "tp_block_forward: down launch");
     stage_mark(P, 5, s);
     return ok();
@@ -1098,7 +1115,8 @@ extern "C" tp_status tp_profile_stages(tp_plan_t plan, void* const* events, int3
     return ok();
 }
 
-extern "C" tp_status tp_profile_phases(tp_plan_t plan, double* out_us, int32_t n, void* stream) {
+extern "C" tp_status tp_profile_phases(tp_plan_t plan, double* out_us, double* median_us, int32_t n,
+                                       void* stream) {
     if (!plan || !out_us) return fail(TP_ERR_NULL, "tp_profile_phases: NULL argument");
     if (n < 1 || n > kStepStamps - 1) return fail(TP_ERR_INVALID_ARG, "tp_profile_phases: n must be 1..%d", kStepStamps - 1);
     if (!plan->last_stamps_ws)
@@ -1115,12 +1133,33 @@ extern "C" tp_status tp_profile_phases(tp_plan_t plan, double* out_us, int32_t n
     // phase i ends when its barrier completes, i.e. at the latest arrival
     unsigned long long prev = ~0ull;
     for (int c = 0; c < rows; ++c) prev = std::min(prev, h[(size_t)c * kStepStamps]);
+    std::vector<unsigned long long> arr(rows);
     for (int i = 0; i < n; ++i) {
         unsigned long long end = 0;
-        for (int c = 0; c < rows; ++c) end = std::max(end, h[(size_t)c * kStepStamps + i + 1]);
+        for (int c = 0; c < rows; ++c) {
+            arr[c] = h[(size_t)c * kStepStamps + i + 1];
+            end = std::max(end, arr[c]);
+        }
         out_us[i] = end >= prev ? (double)(end - prev) * 1e-3 : 0.0;
+        if (median_us) {
+            std::nth_element(arr.begin(), arr.begin() + rows / 2, arr.end());
+            const unsigned long long med = arr[rows / 2];
+            median_us[i] = med >= prev ? (double)(med - prev) * 1e-3 : 0.0;
+        }
         prev = end;
     }
+    return ok();
+}
+
+extern "C" tp_status tp_profile_phase_stamps(tp_plan_t plan, uint64_t* out, int32_t rows, void* stream) {
+    if (!plan || !out) return fail(TP_ERR_NULL, "tp_profile_phase_stamps: NULL argument");
+    if (rows < 1 || rows > kMaxStepCtas) return fail(TP_ERR_INVALID_ARG, "tp_profile_phase_stamps: rows 1..%d", kMaxStepCtas);
+    if (!plan->last_stamps_ws)
+        return fail(TP_ERR_INVALID_ARG, "tp_profile_phase_stamps: no bf16 DECODE step ran while tp_profile_stages was set");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    TP_CUDA(cudaMemcpyAsync(out, plan->last_stamps_ws + plan->off_stamps, (size_t)rows * kStepStamps * 8,
+                            cudaMemcpyDeviceToHost, s), "tp_profile_phase_stamps: copy");
+    TP_CUDA(cudaStreamSynchronize(s), "tp_profile_phase_stamps: sync");
     return ok();
 }
 

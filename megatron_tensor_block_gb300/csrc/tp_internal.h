@@ -15,7 +15,8 @@ constexpr int kTileRows = 64;     // output rows per skinny-GEMM work unit
 constexpr int kTMax = 8;          // tokens per decode step handled in one pass
 constexpr int kKStep = 64;        // reduction elements per warp step
 constexpr int kSMs = 152;         // GB300 streaming multiprocessors
-constexpr int kAttnChunk = 256;   // keys per split-KV work unit (decode)
+constexpr int kAttnChunk = 256;   // keys per split-KV work unit (fp32 decode)
+constexpr int kStepChunk = 128;   // keys per split-KV work unit of the one-launch bf16 decode step
 constexpr int kPartStride = kTileRows * kTMax + kTMax;   // floats per unit partial
 constexpr int kMaxKcTma = 512;
 constexpr int kMaxGroupUnits = 16;  // partials reduced by one finisher (register-resident)    // reduction chunk bound of the tensor-map projection kernel
@@ -75,11 +76,12 @@ struct GemvParams {
     // tensor-map (bf16) kernel: activations arrive through the copy pipeline
     const void* xact;                  // [N * kTMax][K] bf16 operand rows (shard r at row r*kTMax)
     const float* ss_in;                // QKV: [kTMax] sums of squares of x
-    const float* ss_tiles;             // gate/up: [rows of h / 64][kTMax] per-tile sums of squares
+    const float* ss_tiles;             // gate/up: [n_ss_tiles][kTMax] partial sums of squares of h
     int n_ss_tiles;
     void* norm_out;                    // o_proj: [N][kTMax][H] bf16(h * gamma_ffn_r), or NULL
-    float* ss_tiles_out;               // o_proj: [H / 64][kTMax]
+    float* ss_tiles_out;               // o_proj: [H / 8][kTMax] per-8-row sums of squares
     const float* gamma2[TP_MAX_SHARDS];
+    int whole_tiles;                   // one-launch step, row-parallel: each CTA takes every shard of its output tiles
 };
 
 // RMSNorm operand preparation: xg[r][t][k] = bf16(x[t][k] * gamma_r[k]),
@@ -206,7 +208,17 @@ struct DecodeStepParams {
 };
 cudaError_t launch_decode_step(const DecodeStepParams& p, cudaStream_t s);
 constexpr int kMaxStepCtas = 256;        // stamp rows reserved in the workspace
-constexpr int kStepStamps = 10;          // per CTA: start, 8 barrier arrivals, end
+constexpr int kStepMinKeys = 128;        // smallest key range per CTA in the step's attention phase
+// Key range per CTA at least kStepMinKeys and large enough that a KV group of
+// max_kv keys is split over at most 32 CTAs.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int step_min_keys(int max_kv) {
+    const int m = (max_kv + 30) / 31;
+    return m > kStepMinKeys ? m : kStepMinKeys;
+}
+constexpr int kStepStamps = 13;          // per CTA: start, then per phase: streaming done, arrival (or end)
 
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
@@ -215,9 +227,6 @@ void set_pdl(bool on);   // programmatic dependent launch between the kernels of
 cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s, int threads);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_copy_batch(const CopyBatch& b, cudaStream_t s);
-cudaError_t launch_norm_prep(const NormPrepParams& p, cudaStream_t s);
-cudaError_t launch_rowpar_reduce(const GemvParams& p, cudaStream_t s);
-cudaError_t launch_attn_combine(const AttnDecodeParams& p, cudaStream_t s);
 cudaError_t launch_reduce_partials(const float* partials, const float* resid, const float* bias,
                                    float* out, int N, int64_t M, int64_t H, cudaStream_t s);
 
