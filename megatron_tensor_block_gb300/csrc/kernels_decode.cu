@@ -970,6 +970,11 @@ __device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, 
     const int W = sk_nseg(p, epi) * S;
     const int R = sk_phase_share(p, epi, S);
     const int f0 = min((int)blockIdx.x * R, W), f1 = min(f0 + R, W);
+    // the barrier is polled once per phase (an acquire load is an L2 round trip
+    // the producer would otherwise pay per stage); once pending boxes have been
+    // flushed, the barrier is known to have passed
+    bool passed = f0 < f1 && sk_passed(A.bar, gen0, need);
+    if (passed) asm volatile("fence.proxy.async.global;" ::: "memory");   // activations written by ordinary stores
     for (int f = f0; f < f1; ++f, ++it) {
         const int seg = f / S, st = f - seg * S;
         int r, tb;
@@ -977,14 +982,16 @@ __device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, 
         const int rowa = tile_row(epi, tb, 0, p.head_dim, p.ffn_s);
         const int rowb = tile_row(epi, tb, 32, p.head_dim, p.ffn_s);
         const int sl = it % kSkRing;
-        sk_before_reuse(pd, it, A, ring, full, gen0, abort, p.status);
+        if (pd.n > 0 && pd.stage[0] + kSkRing <= it) {
+            sk_flush(pd, A, ring, full, gen0, abort, p.status);
+            passed = true;
+        }
         if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
         mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
         unsigned char* dst = ring + sl * kSkStage;
         tma_load_2d(dst, &A.wm[wi][r], st * kBoxK, rowa, &full[sl], pol);
         tma_load_2d(dst + kBoxBytes, &A.wm[wi][r], st * kBoxK, rowb, &full[sl], pol);
-        if (pd.n == 0 && sk_passed(A.bar, gen0, need)) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (pd.n == 0 && passed) {
             tma_load_2d_keep(dst + 2 * kBoxBytes, &A.xm[wi], st * kBoxK, r * kTMax, &full[sl]);
         } else {
             pd.stage[pd.n] = it;
@@ -1388,7 +1395,11 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
         float bias_v = 0.f;
         if (EPI == EPI_QKV_ROPE && tid < kTileRows && p.bias[r])
             bias_v = p.bias[r][tile_row(EPI_QKV_ROPE, tb, tid, p.head_dim, 0)];
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // four independent accumulators (per 64-element step half and 16-byte
+        // half) so the tensor-core ops of a stage do not form one dependent chain
+        float ca[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ca[q][0] = ca[q][1] = ca[q][2] = ca[q][3] = 0.f;
         for (int st = st0; st < st1; ++st, ++it) {
             const int sl = it % kSkRing;
             mbar_wait(&full[sl], (it / kSkRing) & 1, abort, p.status);
@@ -1398,23 +1409,37 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
             const unsigned char* wB = wA + 8 * (kBoxK * 2);
             const unsigned char* px = stage + 2 * kBoxBytes + g * (kBoxK * 2) + tq * 16;
+            uint4 fa[2][2], fb[2][2], fx[2][2];
 #pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-                const int step = wk + 2 * s2;
-                if (step < steps_here) {
+            for (int s2 = 0; s2 < 2; ++s2)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
-                        const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
-                        const uint4 xv = *reinterpret_cast<const uint4*>(px + step * 128 + h * 64);
-                        mma_bf16_16816(c, a.x, b.x, a.y, b.y, xv.x, xv.y);
-                        mma_bf16_16816(c, a.z, b.z, a.w, b.w, xv.z, xv.w);
+                for (int h = 0; h < 2; ++h) {
+                    const int step = wk + 2 * s2;
+                    if (step < steps_here) {
+                        fa[s2][h] = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
+                        fb[s2][h] = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
+                        fx[s2][h] = *reinterpret_cast<const uint4*>(px + step * 128 + h * 64);
                     }
                 }
-            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[sl]);
+            if (lane == 0) mbar_arrive(&empty[sl]);       // the fragments are in registers
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (wk + 2 * s2 < steps_here) {
+                        float* cq = ca[2 * s2 + h];
+                        float(&cc)[4] = *reinterpret_cast<float(*)[4]>(cq);
+                        mma_bf16_16816(cc, fa[s2][h].x, fb[s2][h].x, fa[s2][h].y, fb[s2][h].y, fx[s2][h].x,
+                                       fx[s2][h].y);
+                        mma_bf16_16816(cc, fa[s2][h].z, fb[s2][h].z, fa[s2][h].w, fb[s2][h].w, fx[s2][h].z,
+                                       fx[s2][h].w);
+                    }
+                }
         }
+        float c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[e] = (ca[0][e] + ca[1][e]) + (ca[2][e] + ca[3][e]);
         f += st1 - st0;
         // this CTA's sum over its stages of the segment: (half 0) + (half 1)
         const int i0 = (16 * wm + g) * kTMax + 2 * tq, i1 = (16 * wm + g + 8) * kTMax + 2 * tq;
