@@ -337,6 +337,12 @@ tp_status tp_reduce_partials(tp_plan_t plan, const float* partials, const float*
 tp_status tp_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
                        int32_t* device_status, void* stream);
 
+/* As tp_gemm_bf16 with B given as [K, N] row-major bf16 (N contiguous), so
+ * C = A @ B: the tensor cores read B through its MN-major operand form (the
+ * form the prefill attention uses for P @ V). Same shape rules and errors. */
+tp_status tp_gemm_bf16_kn(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                          int32_t* device_status, void* stream);
+
 /* Reads the workspace status word (TP_OK or the first device-detected error
  * since tp_workspace_init) into *out (host). Synchronises `stream`. */
 tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);

@@ -106,6 +106,7 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_reduce_partials": (I32, [P, VP, VP, VP, VP, I64, VP]),
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
         "tp_gemm_bf16": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
+        "tp_gemm_bf16_kn": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
         "tp_profile_stages": (I32, [P, C.POINTER(VP), I32]),
         "tp_profile_phases": (I32, [P, C.POINTER(C.c_double), C.POINTER(C.c_double), I32, VP]),
         "tp_profile_phase_stamps": (I32, [P, C.POINTER(C.c_uint64), I32, VP]),
@@ -242,6 +243,11 @@ def tp_reduce_partials(plan: Plan, partials, residual, bias, out, M: int, stream
 def tp_gemm_bf16(A, B, C, M: int, N: int, K: int, device_status=None, stream=None) -> None:
     """C[M, N] = A[M, K] @ B[N, K].T on the tensor cores (bf16 in, float32 out)."""
     _check(load().tp_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, _ptr(device_status), _stream(stream)))
+
+
+def tp_gemm_bf16_kn(A, B, C, M: int, N: int, K: int, device_status=None, stream=None) -> None:
+    """C[M, N] = A[M, K] @ B[K, N] on the tensor cores (B N-contiguous)."""
+    _check(load().tp_gemm_bf16_kn(_ptr(A), _ptr(B), _ptr(C), M, N, K, _ptr(device_status), _stream(stream)))
 
 
 def tp_get_device_status(workspace, stream=None) -> int:

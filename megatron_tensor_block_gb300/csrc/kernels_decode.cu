@@ -688,6 +688,28 @@ cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner
     return cudaSuccess;
 }
 
+// 3-D bf16 tensor [d2][d1][d0] (d0 contiguous), boxes box0 x box1 x 1; not cached.
+cudaError_t tensor_map_3d(const void* base, long d0, long d1, long d2, int box0, int box1, int swizzle128,
+                          CUtensorMap* out) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&encode),
+                                                         12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || !encode) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    }
+    cuuint64_t gdim[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+    cuuint64_t gstride[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)d0 * d1 * 2};
+    cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, 1u};
+    cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap* out, int box_rows = 32) {
     return tensor_map_2d(W, K, rows, kBoxK, box_rows, 0, out);
 }

@@ -31,12 +31,13 @@ constexpr int kTcSmem = 1024 + kTcStages * kTcStageBytes;
 
 struct TcGemmArgs {
     CUtensorMap ta;       // A [M, K], boxes 64 x 128, 128-byte swizzle
-    CUtensorMap tb;       // B [N, K], boxes 64 x 256, 128-byte swizzle
+    CUtensorMap tb;       // B [N, K] boxes 64 x 256, or (B_KN) B [K, N] boxes 64 x 64; 128-byte swizzle
     float* C;             // [M, N]
     int M, N, K;
     int* status;
 };
 
+template <bool B_KN>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_plain_kernel(const __grid_constant__ TcGemmArgs g) {
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -74,7 +75,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_plain_kernel(const __gr
                 mbar_arrive_expect_tx(&full[s], kTcStageBytes);
                 unsigned char* st = stages + s * kTcStageBytes;
                 tma_load_2d_keep(st, &g.ta, kb * kTcBK, m0, &full[s]);
-                tma_load_2d_keep(st + kTcABytes, &g.tb, kb * kTcBK, n0, &full[s]);
+                if (B_KN) {
+                    // four [64 K x 64 N] boxes: the tile's N range in 64-element atoms
+#pragma unroll
+                    for (int nb = 0; nb < kTcBN / 64; ++nb)
+                        tma_load_2d_keep(st + kTcABytes + nb * 8192, &g.tb, n0 + nb * 64, kb * kTcBK, &full[s]);
+                } else {
+                    tma_load_2d_keep(st + kTcABytes, &g.tb, kb * kTcBK, n0, &full[s]);
+                }
             }
             // no copy may still be landing when the CTA exits
             volatile int no_abort = 0;
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_plain_kernel(const __gr
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kTcBM, kTcBN);
+            const uint32_t idesc = B_KN ? idesc_bf16_bmn(kTcBM, kTcBN) : idesc_bf16(kTcBM, kTcBN);
             bool ok = !*abort_flag;
             for (int kb = 0; kb < nk && ok; ++kb) {
                 const int s = kb % kTcStages;
@@ -94,9 +102,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_plain_kernel(const __gr
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(stages + s * kTcStageBytes), b0 = a0 + kTcABytes;
 #pragma unroll
-                for (int k = 0; k < kTcBK / 16; ++k)
-                    tc_mma(tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
-                           (kb | k) != 0);
+                for (int k = 0; k < kTcBK / 16; ++k) {
+                    // MN-major B: 16 K rows of 128 bytes per step; 64-element N atoms 8 KB apart
+                    const uint64_t bd = B_KN ? smem_desc_mn_sw128(b0 + k * 2048, 8192, 1024) : smem_desc_sw128(b0 + k * 32);
+                    tc_mma(tmem, smem_desc_sw128(a0 + k * 32), bd, idesc, (kb | k) != 0);
+                }
                 tc_commit(smem_u32(&empty[s]));
             }
             tc_commit(smem_u32(accum));       // fires when every issued MMA has completed
@@ -133,25 +143,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_plain_kernel(const __gr
 }
 
 cudaError_t launch_tc_gemm_plain(const void* A, const void* B, float* C, int M, int N, int K, int* status,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, bool b_kn) {
     TcGemmArgs g;
     memset(&g, 0, sizeof g);
     cudaError_t e = tensor_map_2d(A, K, M, kTcBK, kTcBM, 1, &g.ta);
-    if (e == cudaSuccess) e = tensor_map_2d(B, K, N, kTcBK, kTcBN, 1, &g.tb);
+    if (e == cudaSuccess) e = b_kn ? tensor_map_2d(B, N, K, 64, kTcBK, 1, &g.tb) : tensor_map_2d(B, K, N, kTcBK, kTcBN, 1, &g.tb);
     if (e != cudaSuccess) return e;
     g.C = C;
     g.M = M;
     g.N = N;
     g.K = K;
     g.status = status;
-    static bool set = false;
-    if (!set) {
-        e = cudaFuncSetAttribute(tc_gemm_plain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    static bool set[2] = {false, false};
+    if (!set[b_kn]) {
+        e = cudaFuncSetAttribute(b_kn ? tc_gemm_plain_kernel<true> : tc_gemm_plain_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         if (e != cudaSuccess) return e;
-        set = true;
+        set[b_kn] = true;
     }
     dim3 grid(M / kTcBM, N / kTcBN);
-    tc_gemm_plain_kernel<<<grid, kTcThreads, kTcSmem, s>>>(g);
+    if (b_kn) tc_gemm_plain_kernel<true><<<grid, kTcThreads, kTcSmem, s>>>(g);
+    else tc_gemm_plain_kernel<false><<<grid, kTcThreads, kTcSmem, s>>>(g);
     return cudaGetLastError();
 }
 
@@ -637,62 +649,78 @@ __global__ void rope_table_kernel(float2* tab, int max_pos, int half, int d, flo
 }
 
 // ---------------------------------------------------------------------------
-// causal prefill attention (FlashAttention-2 style on mma.sync): one CTA per
-// 64 queries of one head of one sequence of one shard; K/V tiles of 64 keys in
-// padded shared memory (conflict-free ldmatrix), online softmax in registers.
+// causal prefill attention on the fifth-generation tensor cores: one CTA per
+// 128 queries of one head of one sequence of one shard.
+//   warp 0    TMA: the Q tile once, then K and V blocks of 128 keys into a
+//             2-stage ring (128-byte swizzle, through a [group][key][d]
+//             tensor map: a block starting before key 0 reads zeros);
+//   warp 1    tensor memory (512 columns) and the MMA thread: S_j = Q K_j^T
+//             into one of two S buffers, then O_j = P_j V_j into one of two O
+//             buffers, V being the MN-major operand ([keys][d], d contiguous);
+//   warps 2-5 one query row per thread: S from tensor memory (twice: row max,
+//             then exp2 and sum), P_j as bf16 into one of two swizzled shared
+//             buffers, and O accumulated in registers with the online
+//             rescaling o = o * alpha_j + O_j, one block behind the MMA.
+// Keys of a block that are not the block's own (the last block is loaded
+// shifted to end at the last needed key, so every row it reads is a written
+// key or zero fill), or lie after the query, get probability 0.
 // ---------------------------------------------------------------------------
 
-struct FlashArgs {
-    const bf16* q;                        // [N][T][hq_s * D]
-    const void* kcache[TP_MAX_SHARDS];    // [Bmax][hkv_s][max_kv][D]
-    const void* vcache[TP_MAX_SHARDS];
+constexpr int kFtQ = 128, kFtK = 128, kFtStages = 2, kFtThreads = 192;
+
+template <int D>
+struct FtShape {
+    static constexpr int NKB = D / 64;
+    static constexpr int QB = kFtQ * D * 2;
+    static constexpr int KB = kFtK * D * 2;
+    static constexpr int STAGE = 2 * KB;                 // K then V
+    static constexpr int PB = kFtQ * kFtK * 2;           // one P buffer: 2 x [128 rows x 64 keys]
+    static constexpr int SMEM = 1024 + QB + kFtStages * STAGE + 2 * PB;
+};
+
+struct FtArgs {
+    CUtensorMap tq;                       // q [N*T, hq_s*D], boxes 64 x 128
+    CUtensorMap tk[TP_MAX_SHARDS];        // caches [Bmax*Hkv'][max_kv][D], boxes 64 x 128 x 1
+    CUtensorMap tv[TP_MAX_SHARDS];
     bf16* out;                            // [N][T][hq_s * D]
     const int* pos;
     int N, B, S, T, hq_s, hkv_s, max_kv;
-    float scale;
+    float scale_log2;                     // log2(e) / sqrt(D)
     int* status;
 };
 
-constexpr int kFaQ = 64, kFaK = 64;
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
 
 template <int D>
-struct FaShape {
-    static constexpr int kPitch = D + 8;                                  // bf16 per shared row
-    static constexpr int kTile = kFaK * kPitch;                           // one K or V tile
-    static constexpr int kSmem = (kFaQ * kPitch + 4 * kTile) * 2;         // Q + 2 x (K, V)
-};
+__global__ void __launch_bounds__(kFtThreads, 1) attn_tc_prefill_kernel(const __grid_constant__ FtArgs f) {
+    using Sh = FtShape<D>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;          // [2]
+    uint64_t* kv_empty = bars + 3;         // [2]
+    uint64_t* s_full = bars + 5;           // [2]
+    uint64_t* s_empty = bars + 7;          // [2]
+    uint64_t* p_full = bars + 9;           // [2]
+    uint64_t* p_empty = bars + 11;         // [2]
+    uint64_t* o_full = bars + 13;          // [2]
+    uint64_t* o_empty = bars + 15;         // [2]
+    uint64_t* done = bars + 17;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    unsigned char* sq = smem + 1024;
+    unsigned char* skv = sq + Sh::QB;
+    unsigned char* sp = skv + kFtStages * Sh::STAGE;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-    const int n = pred ? 16 : 0;                   // 0: fill 16 zero bytes, read nothing
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
-}
-
-// Each of the 4 warps owns 16 query rows; lane (g = lane/4, tq = lane%4)
-// holds rows g and g+8 of the score and output fragments.
-template <int D>
-__global__ void __launch_bounds__(128) flash_prefill_kernel(const FlashArgs f) {
-    using Sh = FaShape<D>;
-    constexpr int P = Sh::kPitch, KS = D / 16, NO = D / 8;
-    extern __shared__ __align__(16) unsigned char fa_smem[];
-    bf16* sq = reinterpret_cast<bf16*>(fa_smem);
-    bf16* sk = sq + kFaQ * P;                      // [2][kFaK * P]
-    bf16* sv = sk + 2 * Sh::kTile;                 // [2][kFaK * P]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, tq = lane & 3;
-    const int nqb = (f.S + kFaQ - 1) / kFaQ;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // heaviest query blocks first (causal work grows with the block index)
+    const int nqb = (f.S + kFtQ - 1) / kFtQ;
     int idx = blockIdx.x;
     const int qb = nqb - 1 - idx % nqb;
     idx /= nqb;
@@ -702,145 +730,204 @@ __global__ void __launch_bounds__(128) flash_prefill_kernel(const FlashArgs f) {
     const int r = idx / f.B;
     const int G = f.hq_s / f.hkv_s, kvh = h / G;
     const int p0 = f.pos[b];
-    const int rows = min(kFaQ, f.S - qb * kFaQ);         // valid queries in this block
-    const int q_first = p0 + qb * kFaQ;                   // position of the block's first query
-    const int nkeys = max(0, min(q_first + rows, f.max_kv));   // keys 0 .. last query position
-    const int ntiles = (nkeys + kFaK - 1) / kFaK;
-    const int t0 = b * f.S + qb * kFaQ;                   // token row of the block's first query
-    const size_t qstride = (size_t)f.hq_s * D;
-    const bf16* qsrc = f.q + ((size_t)r * f.T + t0) * qstride + h * D;
-    const bf16* kbase = reinterpret_cast<const bf16*>(f.kcache[r]) + ((size_t)b * f.hkv_s + kvh) * f.max_kv * D;
-    const bf16* vbase = reinterpret_cast<const bf16*>(f.vcache[r]) + ((size_t)b * f.hkv_s + kvh) * f.max_kv * D;
+    const int rows = min(kFtQ, f.S - qb * kFtQ);
+    const int q_first = p0 + qb * kFtQ;
+    const int nkeys = max(0, min(q_first + rows, f.max_kv));
+    const int nblk = (nkeys + kFtK - 1) / kFtK;
+    const int t0 = b * f.S + qb * kFtQ;
+    const int grp = b * f.hkv_s + kvh;
 
-    for (int i = tid; i < kFaQ * D / 8; i += 128) {
-        const int row = i / (D / 8), c = i - row * (D / 8);
-        const bool in = row < rows;
-        cp_async16(smem_u32(sq + row * P + c * 8), qsrc + (size_t)(in ? row : 0) * qstride + c * 8, in);
-    }
-    auto load_kv = [&](int kt, int buf) {
-        for (int i = tid; i < kFaK * D / 8; i += 128) {
-            const int row = i / (D / 8), c = i - row * (D / 8);
-            const int key = kt * kFaK + row;
-            const bool in = key < nkeys;
-            const size_t off = (size_t)(in ? key : 0) * D + c * 8;
-            cp_async16(smem_u32(sk + buf * Sh::kTile + row * P + c * 8), kbase + off, in);
-            cp_async16(smem_u32(sv + buf * Sh::kTile + row * P + c * 8), vbase + off, in);
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 4);
         }
-    };
-    if (ntiles > 0) load_kv(0, 0);
-    cp_async_commit();
+        mbar_init(done, 1);
+        *abort_flag = (smem_u32(sq) & 1023u) ? 1 : 0;
+        if (*abort_flag) set_status(f.status, TP_ERR_ALIGN);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    float o[NO][4];
+    if (warp == 0) {
+        if (lane == 0 && !*abort_flag) {
+            mbar_arrive_expect_tx(q_full, Sh::QB);
 #pragma unroll
-    for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    uint32_t qa[KS][4];
-    const int mi = lane >> 3, rr = lane & 7;
-    const int qpos0 = q_first + 16 * warp + g, qpos1 = qpos0 + 8;
-
-    for (int kt = 0; kt < ntiles; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < ntiles) load_kv(kt + 1, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const bf16* kt_s = sk + buf * Sh::kTile;
-        const bf16* vt_s = sv + buf * Sh::kTile;
-        if (kt == 0) {
+            for (int kb = 0; kb < Sh::NKB; ++kb)
+                tma_load_2d_keep(sq + kb * (kFtQ * 128), &f.tq, h * D + kb * 64, r * f.T + t0, q_full);
+            int j = 0;
+            for (; j < nblk; ++j) {
+                const int s = j % kFtStages;
+                if (!mbar_wait(&kv_empty[s], ((j / kFtStages) & 1) ^ 1, abort_flag, f.status)) break;
+                mbar_arrive_expect_tx(&kv_full[s], Sh::STAGE);
+                const int key0 = min(j * kFtK, nkeys - kFtK);   // may be negative: zero fill
+                unsigned char* st = skv + s * Sh::STAGE;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-                ldsm4(smem_u32(sq + (16 * warp + (mi & 1) * 8 + rr) * P + ks * 16 + (mi >> 1) * 8), qa[ks][0],
-                      qa[ks][1], qa[ks][2], qa[ks][3]);
-        }
-        float s[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-        for (int np = 0; np < 4; ++np)
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t b0, b1, b2, b3;
-                ldsm4(smem_u32(kt_s + (16 * np + (mi >> 1) * 8 + rr) * P + ks * 16 + (mi & 1) * 8), b0, b1, b2, b3);
-                mma_bf16_16816(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                mma_bf16_16816(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+                for (int kb = 0; kb < Sh::NKB; ++kb) {
+                    tma_load_3d(st + kb * (kFtK * 128), &f.tk[r], kb * 64, key0, grp, &kv_full[s]);
+                    tma_load_3d(st + Sh::KB + kb * (kFtK * 128), &f.tv[r], kb * 64, key0, grp, &kv_full[s]);
+                }
             }
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int key = kt * kFaK + 8 * n + 2 * tq;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float v0 = s[n][e] * f.scale, v1 = s[n][2 + e] * f.scale;
-                if (key + e > qpos0 || key + e >= nkeys) v0 = -INFINITY;
-                if (key + e > qpos1 || key + e >= nkeys) v1 = -INFINITY;
-                s[n][e] = v0;
-                s[n][2 + e] = v1;
-                mx0 = fmaxf(mx0, v0);
-                mx1 = fmaxf(mx1, v1);
-            }
+            volatile int no_abort = 0;
+            mbar_wait(q_full, 0, &no_abort, nullptr);
+            for (int k = j > kFtStages ? j - kFtStages : 0; k < j; ++k)
+                mbar_wait(&kv_full[k % kFtStages], (k / kFtStages) & 1, &no_abort, nullptr);
         }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = (mn0 == -INFINITY) ? 1.f : expf(m0 - mn0);
-        const float al1 = (mn1 == -INFINITY) ? 1.f : expf(m1 - mn1);
-        float ps0 = 0.f, ps1 = 0.f;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(kFtQ, kFtK);
+            const uint32_t id_o = idesc_bf16_bmn(kFtQ, D);
+            bool ok = !*abort_flag && mbar_wait(q_full, 0, abort_flag, f.status);
+            for (int j = 0; j <= nblk && ok; ++j) {
+                if (j < nblk) {                            // S_j = Q K_j^T
+                    const int s = j % kFtStages, bb = j & 1;
+                    if (!mbar_wait(&kv_full[s], (j / kFtStages) & 1, abort_flag, f.status)) break;
+                    if (!mbar_wait(&s_empty[bb], ((j >> 1) & 1) ^ 1, abort_flag, f.status)) break;
+                    tc_fence_after();
+                    const uint32_t qa = smem_u32(sq), ka = smem_u32(skv + s * Sh::STAGE);
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+                    for (int kb = 0; kb < Sh::NKB; ++kb)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float e0 = (s[n][e] == -INFINITY) ? 0.f : expf(s[n][e] - mn0);
-                const float e1 = (s[n][2 + e] == -INFINITY) ? 0.f : expf(s[n][2 + e] - mn1);
-                s[n][e] = e0;
-                s[n][2 + e] = e1;
-                ps0 += e0;
-                ps1 += e1;
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma(tmem + kFtK * bb, smem_desc_sw128(qa + kb * (kFtQ * 128) + k * 32),
+                                   smem_desc_sw128(ka + kb * (kFtK * 128) + k * 32), id_s, (kb | k) != 0);
+                    tc_commit(smem_u32(&s_full[bb]));
+                }
+                if (j >= 1) {                              // O_{j-1} = P_{j-1} V_{j-1}
+                    const int jj = j - 1, s = jj % kFtStages, bb = jj & 1;
+                    if (!mbar_wait(&p_full[bb], (jj >> 1) & 1, abort_flag, f.status)) break;
+                    if (!mbar_wait(&o_empty[bb], ((jj >> 1) & 1) ^ 1, abort_flag, f.status)) break;
+                    tc_fence_after();
+                    const uint32_t pa = smem_u32(sp + bb * Sh::PB), va = smem_u32(skv + s * Sh::STAGE + Sh::KB);
+#pragma unroll
+                    for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma(tmem + 2 * kFtK + D * bb, smem_desc_sw128(pa + kb2 * (kFtQ * 128) + k * 32),
+                                   smem_desc_mn_sw128(va + (kb2 * 64 + k * 16) * 128, kFtK * 128, 1024), id_o,
+                                   (kb2 | k) != 0);
+                    tc_commit(smem_u32(&o_full[bb]));
+                    tc_commit(smem_u32(&p_empty[bb]));
+                    tc_commit(smem_u32(&kv_empty[s]));
+                }
             }
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int n = 0; n < NO; ++n) {
-            o[n][0] *= al0;
-            o[n][1] *= al0;
-            o[n][2] *= al1;
-            o[n][3] *= al1;
+            tc_commit(smem_u32(done));
         }
+    } else {
+        // softmax: warps 2..5 -> tensor-memory lane quarters 2,3,0,1
+        const int qd = warp & 3;
+        const int m = 32 * qd + lane;                       // query row of the tile
+        const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
+        const int q_pos = q_first + m;
+        float o[D];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {          // 16 keys per step
-            const uint32_t a0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-            const uint32_t a1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-            const uint32_t a2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-            const uint32_t a3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+        for (int d = 0; d < D; ++d) o[d] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
+        bool ok = true;
+        // o = o * alpha + O_jj (block jj's product, from tensor memory)
+        auto accumulate = [&](int jj, float alpha) {
+            const int bb = jj & 1;
+            ok = ok && mbar_wait(&o_full[bb], (jj >> 1) & 1, abort_flag, f.status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
 #pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-                uint32_t b0, b1, b2, b3;
-                ldsm4t(smem_u32(vt_s + (16 * kk + (mi & 1) * 8 + rr) * P + 16 * np + (mi >> 1) * 8), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + 2 * kFtK + D * bb + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[32 * c + i] = fmaf(o[32 * c + i], alpha, __uint_as_float(v[i]));
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[bb]);
+        };
+        for (int j = 0; j < nblk; ++j) {
+            const int bb = j & 1;
+            ok = ok && mbar_wait(&s_full[bb], (j >> 1) & 1, abort_flag, f.status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            const int key0 = min(j * kFtK, nkeys - kFtK);
+            const int lo = j * kFtK, hi = min(lo + kFtK, nkeys);
+            const int kmax = min(hi - 1, q_pos);           // last key this row sees in the block
+            // pass 1: row maximum over the visible keys (log2 domain)
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kFtK * bb + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int key = key0 + 32 * c + i;
+                    if (key >= lo && key <= kmax) mx = fmaxf(mx, __uint_as_float(v[i]) * f.scale_log2);
+                }
+            }
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            // pass 2: probabilities into the P buffer (128-byte swizzled K-major rows)
+            ok = ok && mbar_wait(&p_empty[bb], ((j >> 1) & 1) ^ 1, abort_flag, f.status);
+            ok = __all_sync(0xffffffffu, ok);
+            unsigned char* prow = sp + bb * Sh::PB + m * 128;
+            float sum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kFtK * bb + 32 * c, v);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int key = key0 + 32 * c + i;
+                    const float e0 = (key >= lo && key <= kmax) ? exp2f(__uint_as_float(v[i]) * f.scale_log2 - m_new) : 0.f;
+                    const float e1 =
+                        (key + 1 >= lo && key + 1 <= kmax) ? exp2f(__uint_as_float(v[i + 1]) * f.scale_log2 - m_new) : 0.f;
+                    sum += e0 + e1;
+                    pk[i / 2] = pack_bf16x2(e0, e1);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = (c & 1) * 4 + q;       // 16-byte chunk within the 64-key half
+                    *reinterpret_cast<uint4*>(prow + (c >> 1) * (kFtQ * 128) + ((chunk ^ (m & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P is read by the tensor cores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s_empty[bb]);
+                mbar_arrive(&p_full[bb]);
+            }
+            l_run = l_run * alpha + sum;
+            m_run = m_new;
+            if (j >= 1) accumulate(j - 1, alpha_prev);
+            alpha_prev = alpha;
         }
-        __syncthreads();                           // this buffer is refilled two tiles later
+        if (nblk >= 1) accumulate(nblk - 1, alpha_prev);
+        // the output row
+        if (ok && m < rows) {
+            const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+            bf16* dst = f.out + ((size_t)r * f.T + t0 + m) * f.hq_s * D + h * D;
+#pragma unroll
+            for (int d = 0; d < D; d += 8)
+                *reinterpret_cast<uint4*>(dst + d) =
+                    make_uint4(pack_bf16x2(o[d] * inv, o[d + 1] * inv), pack_bf16x2(o[d + 2] * inv, o[d + 3] * inv),
+                               pack_bf16x2(o[d + 4] * inv, o[d + 5] * inv), pack_bf16x2(o[d + 6] * inv, o[d + 7] * inv));
+        }
     }
-    cp_async_wait<0>();
-    const float inv0 = l0 > 0.f ? 1.0f / l0 : 0.f, inv1 = l1 > 0.f ? 1.0f / l1 : 0.f;
-    const int row0 = 16 * warp + g, row1 = row0 + 8;
-    bf16* dst0 = f.out + ((size_t)r * f.T + t0 + row0) * qstride + h * D;
-    bf16* dst1 = f.out + ((size_t)r * f.T + t0 + row1) * qstride + h * D;
-#pragma unroll
-    for (int n = 0; n < NO; ++n) {
-        if (row0 < rows)
-            *reinterpret_cast<uint32_t*>(dst0 + 8 * n + 2 * tq) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
-        if (row1 < rows)
-            *reinterpret_cast<uint32_t*>(dst1 + 8 * n + 2 * tq) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
-    }
+    tc_teardown(done, 0, tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -941,13 +1028,18 @@ cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s) {
-    FlashArgs f;
+    const long grid = (long)p.N * p.B * p.hq_s * ((p.S + kFtQ - 1) / kFtQ);
+    if (grid == 0) return cudaSuccess;
+    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+    FtArgs f;
     memset(&f, 0, sizeof f);
-    f.q = static_cast<const bf16*>(p.q);
-    for (int r = 0; r < p.N; ++r) {
-        f.kcache[r] = p.kcache[r];
-        f.vcache[r] = p.vcache[r];
+    cudaError_t e = tensor_map_2d(p.q, (long)p.hq_s * p.d, (long)p.N * p.T, 64, kFtQ, 1, &f.tq);
+    const long groups = (long)p.max_batch * p.hkv_s;
+    for (int r = 0; r < p.N && e == cudaSuccess; ++r) {
+        e = tensor_map_3d(p.kcache[r], p.d, p.max_kv, groups, 64, kFtK, 1, &f.tk[r]);
+        if (e == cudaSuccess) e = tensor_map_3d(p.vcache[r], p.d, p.max_kv, groups, 64, kFtK, 1, &f.tv[r]);
     }
+    if (e != cudaSuccess) return e;
     f.out = static_cast<bf16*>(p.out);
     f.pos = p.pos;
     f.N = p.N;
@@ -957,23 +1049,20 @@ cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s) {
     f.hq_s = p.hq_s;
     f.hkv_s = p.hkv_s;
     f.max_kv = p.max_kv;
-    f.scale = p.scale;
+    f.scale_log2 = p.scale * 1.4426950408889634f;
     f.status = p.status;
-    const long grid = (long)p.N * p.B * p.hq_s * ((p.S + kFaQ - 1) / kFaQ);
-    if (grid == 0) return cudaSuccess;
-    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     static bool set[2] = {false, false};
     const int which = p.d == 128 ? 1 : 0;
-    const void* fn = which ? reinterpret_cast<const void*>(flash_prefill_kernel<128>)
-                           : reinterpret_cast<const void*>(flash_prefill_kernel<64>);
-    const int smem = which ? FaShape<128>::kSmem : FaShape<64>::kSmem;
+    const void* fn = which ? reinterpret_cast<const void*>(attn_tc_prefill_kernel<128>)
+                           : reinterpret_cast<const void*>(attn_tc_prefill_kernel<64>);
+    const int smem = which ? FtShape<128>::SMEM : FtShape<64>::SMEM;
     if (!set[which]) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         set[which] = true;
     }
     void* args[] = {&f};
-    cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(128), args, smem, s);
+    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kFtThreads), args, smem, s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -35,6 +35,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory descriptor of an MN-major bf16 operand tile stored with the
+// 128-byte swizzle: each 128-byte row holds 64 consecutive M (or N) elements of
+// one K index, 8 K indices form a 1024-byte atom. `lbo` = bytes between atoms
+// along M/N (the next 64 elements), `sbo` = bytes between atoms along K (the
+// next 8 K indices).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4)                     // D: f32
@@ -43,6 +58,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
            | ((uint32_t)(N >> 3) << 17)  // N / 8
            | ((uint32_t)(M >> 4) << 24); // M / 16
 }
+
+// As idesc_bf16 with B MN-major (B given as [K][N], N contiguous).
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) { return idesc_bf16(M, N) | (1u << 16); }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

@@ -980,6 +980,7 @@ static tp_status forward_prefill(tp_plan_t P, const tp_shard_set* w, const tp_kv
     f.hq_s = (int)I.hq_shard;
     f.hkv_s = (int)I.hkv_shard;
     f.max_kv = (int)d.max_kv;
+    f.max_batch = (int)d.max_batch;
     f.d = hd;
     f.scale = (float)(1.0 / std::sqrt((double)hd));
     f.status = status;
@@ -1096,6 +1097,21 @@ extern "C" tp_status tp_gemm_bf16(const void* A, const void* B, float* C, int64_
     if (st) return st;
     cudaError_t e = launch_tc_gemm_plain(A, B, C, (int)M, (int)N, (int)K, device_status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tp_gemm_bf16: launch");
+    return ok();
+}
+
+extern "C" tp_status tp_gemm_bf16_kn(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                                     int32_t* device_status, void* stream) {
+    if (!A || !B || !C) return fail(TP_ERR_NULL, "tp_gemm_bf16_kn: NULL operand");
+    if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 256 || K % 64 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return fail(TP_ERR_SHAPE, "tp_gemm_bf16_kn: need M %% 128 == 0, N %% 256 == 0, K %% 64 == 0 (got %lld, %lld, %lld)",
+                    (long long)M, (long long)N, (long long)K);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return fail(TP_ERR_ALIGN, "tp_gemm_bf16_kn: pointers must be 16-byte aligned");
+    tp_status st = check_device();
+    if (st) return st;
+    cudaError_t e = launch_tc_gemm_plain(A, B, C, (int)M, (int)N, (int)K, device_status, static_cast<cudaStream_t>(stream),
+                                         true);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_gemm_bf16_kn: launch");
     return ok();
 }
 

@@ -150,11 +150,13 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
 // 2-D bf16 tensor map [rows, inner] with boxes box_inner x box_rows (cached).
 cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner, int box_rows, int swizzle128,
                           CUtensorMap* out);
+cudaError_t tensor_map_3d(const void* base, long d0, long d1, long d2, int box0, int box1, int swizzle128,
+                          CUtensorMap* out);
 
 // tcgen05 GEMM, C[M, N] (fp32) = A[M, K] * B[N, K]^T (bf16, K-major),
 // M % 128 == 0, N % 256 == 0, K % 64 == 0.
 cudaError_t launch_tc_gemm_plain(const void* A, const void* B, float* C, int M, int N, int K, int* status,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool b_kn = false);
 
 // Prefill (tcgen05) projections and attention.
 struct PrefillColParams {
@@ -187,6 +189,7 @@ struct FlashParams {
     void* out;
     const int* pos;
     int N, B, S, T, hq_s, hkv_s, max_kv, d;   // d: head_dim, 64 or 128
+    int max_batch;                        // cache extent: groups = max_batch * hkv_s
     float scale;
     int* status;
 };
