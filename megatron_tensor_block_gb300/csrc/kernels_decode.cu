@@ -576,6 +576,9 @@ constexpr int kAtKeys = 64;                   // keys per stage
 constexpr int kAtRing = 5;
 constexpr int kAtMaxStage = 4 * kAtKeys * 72 * 2;   // K and V, two column halves each (head_dim 128)
 constexpr int kAtSlot = 1024;                 // floats per merge slot (G * head_dim <= 1024)
+constexpr int kQStage = 3584;                 // bf16 elements of q staged for the attention phase (7 KB)
+constexpr int kQSegs = 7;                     // segments whose q is staged
+constexpr int kSegTab = 8;                    // attention segments per CTA listed ahead of the phase
 
 template <int D>
 struct AtShape {
@@ -958,10 +961,13 @@ struct SkPend {
 };
 
 // Issues every pending activation box, waiting for the barriers in order.
-__device__ __forceinline__ bool sk_flush(SkPend& pd, const StepArgs& A, unsigned char* ring, uint64_t* full,
-                                         unsigned long long gen0, volatile int* abort, int* status) {
+// Returns the last barrier waited for (0 if none was pending).
+__device__ __forceinline__ unsigned sk_flush(SkPend& pd, const StepArgs& A, unsigned char* ring, uint64_t* full,
+                                             unsigned long long gen0, volatile int* abort, int* status) {
     bool ok = true;
+    unsigned last = 0;
     for (int i = 0; i < pd.n; ++i) {
+        last = pd.need[i];
         if (ok) ok = sk_wait_gen(A.bar, gen0, pd.need[i], abort, status);
         // the activations were written by other CTAs' ordinary stores
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -970,59 +976,121 @@ __device__ __forceinline__ bool sk_flush(SkPend& pd, const StepArgs& A, unsigned
                          &full[pd.slot[i]]);
     }
     pd.n = 0;
-    return ok;
+    return last;
 }
 
-// Before the producer reuses the slot of stage `it` (last held by stage
-// it - kSkRing): if that stage is still pending, its consumers cannot release
-// the slot until its activation box is issued.
-__device__ __forceinline__ void sk_before_reuse(SkPend& pd, uint32_t it, const StepArgs& A, unsigned char* ring,
-                                                uint64_t* full, unsigned long long gen0, volatile int* abort,
-                                                int* status) {
-    if (pd.n > 0 && pd.stage[0] + kSkRing <= it) sk_flush(pd, A, ring, full, gen0, abort, status);
+// Stage range [f0, f1) of this CTA in a projection phase; S stages per segment.
+__device__ __forceinline__ void sk_gemv_range(const GemvParams& p, int epi, int& f0, int& f1, int& S) {
+    S = (p.K + kBoxK - 1) / kBoxK;
+    const int W = sk_nseg(p, epi) * S;
+    const int R = sk_phase_share(p, epi, S);
+    f0 = min((int)blockIdx.x * R, W);
+    f1 = min(f0 + R, W);
+}
+
+// Positions and the attention key space, read by the producer thread once the
+// dependency on the preceding launch is resolved.
+struct SkKeys {
+    KeySpace ks;
+    int posv[kTMax];
+    int k0, k1;            // this CTA's attention keys
+    bool ready;
+};
+
+__device__ __forceinline__ void sk_keys_ready(SkKeys& K, const StepArgs& A) {
+    if (K.ready) return;
+    pdl_wait();                                         // cache rows and positions of the preceding step
+    for (int b = 0; b < kTMax; ++b) K.posv[b] = b < A.a.B ? A.a.pos[b] : 0;
+    K.ks = sk_keyspace(A.a, K.posv);
+    const int R = sk_share(K.ks.total, step_min_keys(A.a.max_kv));
+    K.k0 = min((int)blockIdx.x * R, K.ks.total);
+    K.k1 = min(K.k0 + R, K.ks.total);
+    K.ready = true;
+}
+
+// One attention segment: the CTA's keys of one group, walked from the end of
+// the CTA's range backwards (the block holding a new position comes last).
+struct SkSeg {
+    int k, len, row0, r, j_new;     // j_new: first block offset holding the new position
+};
+
+__device__ __forceinline__ SkSeg sk_attn_segment(const SkKeys& K, const AttnDecodeParams& p, int ke) {
+    int gi, b, off, gstart;
+    sk_locate(K.ks, p, ke - 1, gi, b, off, gstart);
+    SkSeg g;
+    g.k = max(K.k0, gstart);
+    sk_locate(K.ks, p, g.k, gi, b, off, gstart);
+    g.len = ke - g.k;
+    const int kh = gi % p.hkv_s;
+    g.r = gi / (p.hkv_s * p.B);
+    g.row0 = (b * p.hkv_s + kh) * p.max_kv + off;
+    g.j_new = K.posv[b] - off - kAtKeys + 1;
+    return g;
 }
 
 // Producer of one projection phase: weight boxes at once, the activation box
-// once barrier `need` has passed.
+// once barrier `need` has passed. The per-stage path is kept short (one
+// thread issues every copy of the CTA): segment geometry is computed once per
+// segment, the ring slot and parity advance incrementally.
 __device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, const StepArgs& A, unsigned char* ring,
                                                 uint64_t* full, uint64_t* empty, uint32_t& it, SkPend& pd,
                                                 unsigned long long gen0, volatile int* abort, uint64_t pol) {
     const GemvParams& p = A.g[wi];
-    const int S = (p.K + kBoxK - 1) / kBoxK;
-    const int W = sk_nseg(p, epi) * S;
-    const int R = sk_phase_share(p, epi, S);
-    const int f0 = min((int)blockIdx.x * R, W), f1 = min(f0 + R, W);
+    int f0, f1, S;
+    sk_gemv_range(p, epi, f0, f1, S);
+    if (f0 >= f1) return true;
     // the barrier is polled once per phase (an acquire load is an L2 round trip
     // the producer would otherwise pay per stage); once pending boxes have been
     // flushed, the barrier is known to have passed
-    bool passed = f0 < f1 && sk_passed(A.bar, gen0, need);
-    if (passed) asm volatile("fence.proxy.async.global;" ::: "memory");   // activations written by ordinary stores
-    for (int f = f0; f < f1; ++f, ++it) {
-        const int seg = f / S, st = f - seg * S;
+    bool passed = sk_passed(A.bar, gen0, need);
+    if (passed) {
+        // every earlier barrier has passed too: issue what is still pending
+        sk_flush(pd, A, ring, full, gen0, abort, p.status);
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // activations written by ordinary stores
+    }
+    // first stage that reuses the slot of the oldest pending stage
+    uint32_t flush_at = pd.n > 0 ? pd.stage[0] + kSkRing : 0xffffffffu;
+    uint32_t sl = it % kSkRing, par = ((it / kSkRing) & 1) ^ 1;
+    const CUtensorMap* xm = &A.xm[wi];
+    int seg = f0 / S, st = f0 - seg * S;
+    for (int f = f0; f < f1; ++seg, st = 0) {
         int r, tb;
         sk_segment(p, epi, seg, r, tb);
+        const CUtensorMap* wmap = &A.wm[wi][r];
         const int rowa = tile_row(epi, tb, 0, p.head_dim, p.ffn_s);
         const int rowb = tile_row(epi, tb, 32, p.head_dim, p.ffn_s);
-        const int sl = it % kSkRing;
-        if (pd.n > 0 && pd.stage[0] + kSkRing <= it) {
-            sk_flush(pd, A, ring, full, gen0, abort, p.status);
-            passed = true;
-        }
-        if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
-        mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
-        unsigned char* dst = ring + sl * kSkStage;
-        tma_load_2d(dst, &A.wm[wi][r], st * kBoxK, rowa, &full[sl], pol);
-        tma_load_2d(dst + kBoxBytes, &A.wm[wi][r], st * kBoxK, rowb, &full[sl], pol);
-        if (pd.n == 0 && passed) {
-            tma_load_2d_keep(dst + 2 * kBoxBytes, &A.xm[wi], st * kBoxK, r * kTMax, &full[sl]);
-        } else {
-            pd.stage[pd.n] = it;
-            pd.slot[pd.n] = sl;
-            pd.x[pd.n] = st * kBoxK;
-            pd.y[pd.n] = r * kTMax;
-            pd.map[pd.n] = wi;
-            pd.need[pd.n] = need;
-            ++pd.n;
+        const int y = r * kTMax;
+        const int n = min(S - st, f1 - f);
+        f += n;
+        for (int x = st * kBoxK, xe = (st + n) * kBoxK; x < xe; x += kBoxK, ++it) {
+            if (it >= flush_at) {
+                // the flushed boxes may all belong to an earlier phase
+                passed = sk_flush(pd, A, ring, full, gen0, abort, p.status) >= need ||
+                         sk_passed(A.bar, gen0, need);
+                if (passed) asm volatile("fence.proxy.async.global;" ::: "memory");
+                flush_at = 0xffffffffu;
+            }
+            if (!mbar_wait(&empty[sl], par, abort, p.status)) return false;
+            mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
+            unsigned char* dst = ring + sl * kSkStage;
+            tma_load_2d(dst, wmap, x, rowa, &full[sl], pol);
+            tma_load_2d(dst + kBoxBytes, wmap, x, rowb, &full[sl], pol);
+            if (passed) {
+                tma_load_2d_keep(dst + 2 * kBoxBytes, xm, x, y, &full[sl]);
+            } else {
+                if (pd.n == 0) flush_at = it + kSkRing;
+                pd.stage[pd.n] = it;
+                pd.slot[pd.n] = sl;
+                pd.x[pd.n] = x;
+                pd.y[pd.n] = y;
+                pd.map[pd.n] = wi;
+                pd.need[pd.n] = need;
+                ++pd.n;
+            }
+            if (++sl == kSkRing) {
+                sl = 0;
+                par ^= 1;
+            }
         }
     }
     return true;
@@ -1030,47 +1098,47 @@ __device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, 
 
 template <int D>
 __device__ __forceinline__ bool sk_produce_attn(unsigned need, const StepArgs& A, unsigned char* ring, uint64_t* full,
-                                                uint64_t* empty, uint32_t& it, SkPend& pd, unsigned long long gen0,
-                                                volatile int* abort, uint64_t pol, const int* posv) {
+                                                uint64_t* empty, uint32_t& it, SkPend& pd, SkKeys& keys,
+                                                unsigned long long gen0, volatile int* abort, uint64_t pol) {
     using S = AtShape<D>;
     const AttnDecodeParams& p = A.a;
-    pdl_wait();                                         // cache rows and positions of the preceding step
-    const KeySpace ks = sk_keyspace(p, posv);
-    const int R = sk_share(ks.total, step_min_keys(p.max_kv));
-    const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
+    sk_keys_ready(keys, A);
     bool passed = false;
+    uint32_t flush_at = pd.n > 0 ? pd.stage[0] + kSkRing : 0xffffffffu;
+    uint32_t sl = it % kSkRing, par = ((it / kSkRing) & 1) ^ 1;
     // segments in reverse order: a block holding a new position (a group's last
     // keys) comes last in the CTA's range, so everything before it can stream
     // while the QKV phase is still running
-    for (int ke = k1; ke > k0;) {
-        int gi, b, off, gstart;
-        sk_locate(ks, p, ke - 1, gi, b, off, gstart);
-        const int k = max(k0, gstart);
-        sk_locate(ks, p, k, gi, b, off, gstart);
-        const int seg_len = ke - k;
-        const int kh = gi % p.hkv_s, r = gi / (p.hkv_s * p.B);
-        const int row0 = (b * p.hkv_s + kh) * p.max_kv + off;
-        const int pos = posv[b];
-        for (int j = 0; j < seg_len; j += kAtKeys, ++it) {
-            // the block holding the new position is written by the QKV phase
-            if (!passed && off + j + kAtKeys > pos) {
+    for (int ke = keys.k1; ke > keys.k0;) {
+        const SkSeg g = sk_attn_segment(keys, p, ke);
+        const CUtensorMap* tk = &A.tk[g.r];
+        const CUtensorMap* tv = &A.tv[g.r];
+        for (int j = 0; j < g.len; j += kAtKeys, ++it) {
+            if (!passed && j >= g.j_new) {              // written by the QKV phase
                 sk_flush(pd, A, ring, full, gen0, abort, p.status);
+                flush_at = 0xffffffffu;
                 sk_wait_gen(A.bar, gen0, need, abort, p.status);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 passed = true;
             }
-            const int sl = it % kSkRing;
-            sk_before_reuse(pd, it, A, ring, full, gen0, abort, p.status);
-            if (!mbar_wait(&empty[sl], ((it / kSkRing) & 1) ^ 1, abort, p.status)) return false;
+            if (it >= flush_at) {
+                sk_flush(pd, A, ring, full, gen0, abort, p.status);
+                flush_at = 0xffffffffu;
+            }
+            if (!mbar_wait(&empty[sl], par, abort, p.status)) return false;
             mbar_arrive_expect_tx(&full[sl], (uint32_t)S::STAGE);
             unsigned char* st = ring + sl * kSkStage;
 #pragma unroll
             for (int h = 0; h < S::NB; ++h) {
-                tma_load_2d(st + h * S::BOX, &A.tk[r], h * 64, row0 + j, &full[sl], pol);
-                tma_load_2d(st + (S::NB + h) * S::BOX, &A.tv[r], h * 64, row0 + j, &full[sl], pol);
+                tma_load_2d(st + h * S::BOX, tk, h * 64, g.row0 + j, &full[sl], pol);
+                tma_load_2d(st + (S::NB + h) * S::BOX, tv, h * 64, g.row0 + j, &full[sl], pol);
+            }
+            if (++sl == kSkRing) {
+                sl = 0;
+                par ^= 1;
             }
         }
-        ke = k;
+        ke = g.k;
     }
     return true;
 }
@@ -1222,6 +1290,67 @@ __device__ __forceinline__ void sk_col_finish(const GemvParams& p, int seg, int 
     consumer_sync(kConsumers);
 }
 
+// Output rows of a row-parallel tile, per thread: row j of tile tb, tokens
+// 2*tp and 2*tp + 1. y = residual + sum; the next norm's operands
+// bf16(y * gamma_r) for every shard, and per-8-row sums of squares.
+__device__ __forceinline__ void sk_row_out(const GemvParams& p, int tb, float2 total, float2 res, const float* g2) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j8 = lane >> 2, tp = lane & 3;
+    const int row = tb * kTileRows + warp * 8 + j8;
+    float sq[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int t = 2 * tp + e;
+        float yv = 0.f;
+        if (t < p.T) {
+            const size_t o = (size_t)t * p.rows + row;
+            yv = (e ? res.y : res.x) + (e ? total.y : total.x);
+            p.y[o] = yv;
+            if (p.norm_out) {
+                bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
+                for (int r2 = 0; r2 < p.n_shards; ++r2)
+                    nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * g2[r2]);
+            }
+        }
+        sq[e] = yv * yv;
+    }
+    if (p.norm_out) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
+            sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
+        }
+        if (j8 == 0) {
+            const size_t item = (size_t)tb * 8 + warp;
+            p.ss_tiles_out[item * kTMax + 2 * tp] = sq[0];
+            p.ss_tiles_out[item * kTMax + 2 * tp + 1] = sq[1];
+        }
+    }
+}
+
+// The inputs of a tile's output rows that do not depend on the phase (the
+// residual and the next norm's gamma), copied asynchronously into this
+// thread's slots of `slot` ([2 + TP_MAX_SHARDS] floats per thread) when the
+// tile starts, so its epilogue does not wait on a round trip to L2.
+constexpr int kRowSlot = 2 + TP_MAX_SHARDS;
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void sk_row_prefetch(const GemvParams& p, int tb, float* slot) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j8 = lane >> 2, tp = lane & 3;
+    const int row = tb * kTileRows + warp * 8 + j8;
+    float* my = slot + threadIdx.x * kRowSlot;
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+        if (2 * tp + e < p.T) cp_async4(my + e, p.resid + (size_t)(2 * tp + e) * p.rows + row);
+    if (p.norm_out)
+        for (int r2 = 0; r2 < p.n_shards; ++r2) cp_async4(my + 2 + r2, p.gamma2[r2] + row);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 // Consumers: row-parallel output tile tb -- pieces (CTA order) within each
 // rank, then ranks in order, then the residual; with norm_out also the next
 // norm's operands and per-(8-row slice, token) sums of squares. One 8-row
@@ -1236,6 +1365,14 @@ __device__ __forceinline__ void sk_row_finish(const GemvParams& p, int tb, int S
         return reinterpret_cast<const float2*>(p.part + ((size_t)(tb * p.n_shards + r) * nsplit + c) * kPartStride +
                                                j * kTMax + 2 * tp);
     };
+    // the residual and gamma are read with the pieces: one round trip
+    const int row = tb * kTileRows + j;
+    float2 res = make_float2(0.f, 0.f);
+    if (2 * tp < p.T) res.x = __ldcg(p.resid + (size_t)(2 * tp) * p.rows + row);
+    if (2 * tp + 1 < p.T) res.y = __ldcg(p.resid + (size_t)(2 * tp + 1) * p.rows + row);
+    float g2[TP_MAX_SHARDS];
+#pragma unroll
+    for (int r2 = 0; r2 < TP_MAX_SHARDS; ++r2) g2[r2] = p.norm_out && r2 < p.n_shards ? p.gamma2[r2][row] : 0.f;
     int cnt_r[TP_MAX_SHARDS];
     float2 v[TP_MAX_SHARDS][kPer];
 #pragma unroll
@@ -1265,75 +1402,20 @@ __device__ __forceinline__ void sk_row_finish(const GemvParams& p, int tb, int S
             total = r == 0 ? pr : make_float2(total.x + pr.x, total.y + pr.y);
         }
     }
-    const int row = tb * kTileRows + j;
-    float sq[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int t = 2 * tp + e;
-        float yv = 0.f;
-        if (t < p.T) {
-            const size_t o = (size_t)t * p.rows + row;
-            yv = p.resid[o] + (e ? total.y : total.x);
-            p.y[o] = yv;
-            if (p.norm_out) {
-                bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
-                for (int r2 = 0; r2 < p.n_shards; ++r2)
-                    nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
-            }
-        }
-        sq[e] = yv * yv;
-    }
-    if (p.norm_out) {
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
-            sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
-        }
-        if (j8 == 0) {
-            const size_t item = (size_t)tb * 8 + warp;
-            p.ss_tiles_out[item * kTMax + 2 * tp] = sq[0];
-            p.ss_tiles_out[item * kTMax + 2 * tp + 1] = sq[1];
-        }
-    }
+    sk_row_out(p, tb, total, res, g2);
 }
 
 // Consumers: output tile tb of a row-parallel phase whose rank-ordered sum
-// over the shards is in `acc` ([64][8]): residual, next norm operands, sums of
-// squares (layout as in sk_row_finish).
-__device__ __forceinline__ void sk_row_epilogue(const GemvParams& p, int tb, const float* acc) {
+// over the shards is in `acc` ([64][8]); the tile's inputs were prefetched
+// into `slot` by sk_row_prefetch.
+__device__ __forceinline__ void sk_row_epilogue(const GemvParams& p, int tb, const float* acc, const float* slot) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j8 = lane >> 2, tp = lane & 3;
-    const int j = warp * 8 + j8;
-    const int row = tb * kTileRows + j;
-    float sq[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int t = 2 * tp + e;
-        float yv = 0.f;
-        if (t < p.T) {
-            const size_t o = (size_t)t * p.rows + row;
-            yv = p.resid[o] + acc[j * kTMax + t];
-            p.y[o] = yv;
-            if (p.norm_out) {
-                bf16* nout = reinterpret_cast<bf16*>(p.norm_out);
-                for (int r2 = 0; r2 < p.n_shards; ++r2)
-                    nout[((size_t)r2 * kTMax + t) * p.rows + row] = __float2bfloat16_rn(yv * p.gamma2[r2][row]);
-            }
-        }
-        sq[e] = yv * yv;
-    }
-    if (p.norm_out) {
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], off);
-            sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], off);
-        }
-        if (j8 == 0) {
-            const size_t item = (size_t)tb * 8 + warp;
-            p.ss_tiles_out[item * kTMax + 2 * tp] = sq[0];
-            p.ss_tiles_out[item * kTMax + 2 * tp + 1] = sq[1];
-        }
-    }
+    const int j = warp * 8 + (lane >> 2), tp = lane & 3;
+    asm volatile("cp.async.wait_all;" ::: "memory");    // this thread's own copies
+    const float* my = slot + threadIdx.x * kRowSlot;
+    const float2 res = make_float2(my[0], my[1]);
+    const float2 total = make_float2(acc[j * kTMax + 2 * tp], acc[j * kTMax + 2 * tp + 1]);
+    sk_row_out(p, tb, total, res, my + 2);
 }
 
 // Consumers: KV group gi -- the pieces' (max, sum, unnormalised output)
@@ -1390,7 +1472,8 @@ __device__ __forceinline__ void sk_attn_finish(const AttnDecodeParams& p, int gi
 template <int EPI>
 __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned char* ring, uint64_t* full,
                                         uint64_t* empty, volatile int* abort, uint32_t& it, float* tile, float* acc,
-                                        float* ss, int* s_pos, float* s_bias, SkQueue* qu, uint32_t& jn) {
+                                        float* ss, int* s_pos, float* s_bias, float* slot, SkQueue* qu,
+                                        uint32_t& jn) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = (p.K + kBoxK - 1) / kBoxK;
     const int W = sk_nseg(p, EPI) * S;
@@ -1414,6 +1497,7 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
         const int st1 = min(S, st0 + (f1 - f));       // this CTA's stages of the segment: [st0, st1)
         int r, tb;
         sk_segment(p, EPI, seg, r, tb);
+        if (EPI == EPI_ROWPAR && p.whole_tiles && r == 0) sk_row_prefetch(p, tb, slot);
         float bias_v = 0.f;
         if (EPI == EPI_QKV_ROPE && tid < kTileRows && p.bias[r])
             bias_v = p.bias[r][tile_row(EPI_QKV_ROPE, tb, tid, p.head_dim, 0)];
@@ -1488,7 +1572,7 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
                 acc[i] = r == 0 ? tile[i] : acc[i] + tile[i];   // ((p0 + p1) + p2) + ...
             consumer_sync(kConsumers);
             if (r == p.n_shards - 1) {
-                sk_row_epilogue(p, tb, acc);
+                sk_row_epilogue(p, tb, acc, slot);
                 consumer_sync(kConsumers);
             }
             continue;
@@ -1519,6 +1603,43 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
     }
 }
 
+// The CTA's attention segments, listed once at the start of the step (they
+// depend only on the positions) so the attention phase starts without walking
+// the key space. More than kSegTab segments: the phase walks it instead.
+struct SkSegInfo {
+    int gi, b, kh, r, gstart, len, n, qoff;
+};
+
+template <int D>
+__device__ __forceinline__ void sk_seg_table(const AttnDecodeParams& p, SkSegInfo* tab, int* s_nseg) {
+    pdl_wait();                                         // positions of the preceding step
+    int posv[kTMax];
+    for (int b = 0; b < kTMax; ++b) posv[b] = b < p.B ? p.pos[b] : 0;
+    const KeySpace ks = sk_keyspace(p, posv);
+    const int G = p.hq_s / p.hkv_s;
+    const int R = sk_share(ks.total, step_min_keys(p.max_kv));
+    const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
+    int n = 0;
+    for (int ke = k1; ke > k0 && n <= kSegTab; ++n) {
+        int gi, b, off, gstart;
+        sk_locate(ks, p, ke - 1, gi, b, off, gstart);
+        const int k = max(k0, gstart);
+        if (n < kSegTab) {
+            SkSegInfo& e = tab[n];
+            e.gi = gi;
+            e.b = b;
+            e.kh = gi % p.hkv_s;
+            e.r = gi / (p.hkv_s * p.B);
+            e.gstart = gstart;
+            e.len = ks.len[b];
+            e.n = ke - k;
+            e.qoff = ((e.r * kTMax + b) * p.hq_s + e.kh * G) * D;
+        }
+        ke = k;
+    }
+    *s_nseg = n;                                        // kSegTab + 1: too many to list
+}
+
 // Attention phase on the consumer side: this CTA's key range, one group
 // segment at a time (every warp waits for and releases every stage; the
 // 64-key blocks of a segment alternate between warps 0-3 and 4-7). A segment
@@ -1528,7 +1649,9 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
 template <int D>
 __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char* ring, uint64_t* full,
                                         uint64_t* empty, volatile int* abort, uint32_t& it, float* red,
-                                        float* s_ml2, float* s_cmb, const int* s_pos, SkQueue* qu, uint32_t& jn) {
+                                        float* s_ml2, float* s_cmb, const int* s_pos, bf16* qs,
+                                        const SkSegInfo* tab, const int* s_nseg, uint64_t* tab_ready,
+                                        SkQueue* qu, uint32_t& jn) {
     using S = AtShape<D>;
     constexpr int KS = D / 16;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1542,24 +1665,70 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
     const KeySpace ks = sk_keyspace(p, s_pos);
     const int R = sk_share(ks.total, step_min_keys(p.max_kv));
     const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
+    // q of the CTA's first segments, scaled and rounded to bf16 once and staged
+    // in shared memory: one round trip of loads for all of them instead of one
+    // per segment (q was written by other CTAs in the QKV phase)
+    mbar_wait(tab_ready, 0, abort, p.status);
+    const int nseg = *s_nseg;
+    const bool listed = nseg <= kSegTab;
+    const int qper = G * D;
+    const int nq = listed ? min(min(nseg, kQSegs), kQStage / qper) : 0;
+    {
+        constexpr int kPer = kQStage / kConsumers;
+        const int n = nq * qper;
+        float v[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int idx = tid + i * kConsumers;
+            if (idx < n) {
+                const int sg = idx / qper;
+                v[i] = __ldcg(p.q + tab[sg].qoff + (idx - sg * qper));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int idx = tid + i * kConsumers;
+            if (idx < n) qs[idx] = __float2bfloat16_rn(v[i] * p.scale);
+        }
+    }
+    consumer_sync(kConsumers);
     int ui = 0;
     for (int ke = k1; ke > k0; ++ui) {                  // segments in reverse order (as the producer)
-        int gi, b, off, gstart;
-        sk_locate(ks, p, ke - 1, gi, b, off, gstart);
-        const int k = max(k0, gstart);
-        const int len = ks.len[b];
-        const int n = ke - k;                           // keys of this segment
-        ke = k;
-        const int kh = gi % p.hkv_s, r = gi / (p.hkv_s * p.B);
+        int gi, b, gstart, len, n, kh, r;
+        if (listed) {
+            const SkSegInfo& e = tab[ui];
+            gi = e.gi;
+            b = e.b;
+            gstart = e.gstart;
+            len = e.len;
+            n = e.n;                                    // keys of this segment
+            kh = e.kh;
+            r = e.r;
+        } else {
+            int off;
+            sk_locate(ks, p, ke - 1, gi, b, off, gstart);
+            len = ks.len[b];
+            n = ke - max(k0, gstart);
+            kh = gi % p.hkv_s;
+            r = gi / (p.hkv_s * p.B);
+        }
+        ke -= n;
         const int nblk = (n + kAtKeys - 1) / kAtKeys;
         uint32_t qb[KS][2];
-        {
+        if (ui < nq) {
+            const bf16* qp = qs + ui * qper + (g < G ? g : 0) * D;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                qb[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * t) : 0u;
+                qb[kk][1] = g < G ? *reinterpret_cast<const uint32_t*>(qp + 16 * kk + 8 + 2 * t) : 0u;
+            }
+        } else {
             const float* qp = p.q + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 if (g < G) {
-                    const float2 a = *reinterpret_cast<const float2*>(qp + 16 * kk + 2 * t);
-                    const float2 c2 = *reinterpret_cast<const float2*>(qp + 16 * kk + 8 + 2 * t);
+                    const float2 a = __ldcg(reinterpret_cast<const float2*>(qp + 16 * kk + 2 * t));
+                    const float2 c2 = __ldcg(reinterpret_cast<const float2*>(qp + 16 * kk + 8 + 2 * t));
                     qb[kk][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
                     qb[kk][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
                 } else {
@@ -1706,11 +1875,12 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
 constexpr int kStepThreads = kStreamThreads + 32;       // + the finisher warp
 
 size_t decode_step_smem() {
-    // ring | red [8][kAtSlot] | s_ml [2][8][8][2] | tile [64][8] | ss, pos, bias | s_cmb | ftile [64][8] | queue
+    // ring | red [8][kAtSlot] | s_ml [2][8][8][2] | tile [64][8] | ss, pos, bias | s_cmb | ftile [64][8] |
+    // queue | table-ready barrier | segment table [kSegTab] | segment count (8 bytes) | staged q [kQStage] bf16
     return 1024 + (size_t)kSkRing * kSkStage +
            (size_t)(8 * kAtSlot + 2 * 8 * kMaxGroup * 2 + kTileRows * kTMax + kTMax + kTMax + 96 + 2 * kMaxGroup +
                     kTileRows * kTMax) * 4 +
-           sizeof(SkQueue);
+           sizeof(SkQueue) + 8 + kSegTab * sizeof(SkSegInfo) + 8 + (size_t)kQStage * 2;
 }
 
 // The finisher warp: the jobs of the consumers, in order. Piece jobs are
@@ -1800,6 +1970,10 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     float* s_cmb = s_bias + 96;
     float* ftile = s_cmb + 2 * kMaxGroup;
     SkQueue* qu = reinterpret_cast<SkQueue*>(ftile + kTileRows * kTMax);
+    uint64_t* tab_ready = reinterpret_cast<uint64_t*>(qu + 1);
+    SkSegInfo* seg_tab = reinterpret_cast<SkSegInfo*>(tab_ready + 1);
+    int* s_nseg = reinterpret_cast<int*>(seg_tab + kSegTab);
+    bf16* qs = reinterpret_cast<bf16*>(s_nseg + 2);
     int* status = A.a.status;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1813,6 +1987,7 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
             mbar_init(&qu->empty[i], 1);
         }
         mbar_init(&qu->drained, 1);
+        mbar_init(tab_ready, 1);
         qu->n_fin = 0;
         *abort_flag = (smem_u32(ring) & 127u) ? 1 : 0;
         if (*abort_flag) set_status(status, TP_ERR_ALIGN);
@@ -1834,13 +2009,12 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
             uint32_t it = 0;
             SkPend pd;
             pd.n = 0;
+            SkKeys keys;
+            keys.ready = false;
             // weights do not depend on the preceding step: QKV streams at once; the
             // activation boxes wait for barrier 1, which follows the consumers' wait
             bool ok = sk_produce_gemv(EPI_QKV_ROPE, 0, 1, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
-            pdl_wait();
-            int posv[kTMax];
-            for (int b = 0; b < kTMax; ++b) posv[b] = b < A.a.B ? A.a.pos[b] : 0;
-            if (ok) ok = sk_produce_attn<D>(2, A, ring, full, empty, it, pd, gen0, abort_flag, pol, posv);
+            if (ok) ok = sk_produce_attn<D>(2, A, ring, full, empty, it, pd, keys, gen0, abort_flag, pol);
             if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 1, 3, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
             if (ok) ok = sk_produce_gemv(EPI_SWIGLU, 2, 4, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
             if (ok) ok = sk_produce_gemv(EPI_ROWPAR, 3, 5, A, ring, full, empty, it, pd, gen0, abort_flag, pol);
@@ -1853,6 +2027,11 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
         return;
     }
     if (warp == kConsumers / 32 + 1) {                 // ---- finisher
+        if (lane == 0) {
+            sk_seg_table<D>(A.a, seg_tab, s_nseg);
+            mbar_arrive(tab_ready);
+        }
+        __syncwarp();
         sk_finisher(A, qu, abort_flag);
         return;
     }
@@ -1865,16 +2044,17 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     uint32_t it = 0, jn = 0;
     sk_norm(A.np);
     sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
     sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
-    sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qu, jn);
+    sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qs, seg_tab, s_nseg, tab_ready, qu,
+               jn);
     sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
     sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
     sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
     pdl_trigger();                                      // the next launch may start streaming its weights
-    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, qu, jn);
+    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
     sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
 }
 
