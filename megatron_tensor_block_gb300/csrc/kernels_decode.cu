@@ -717,6 +717,39 @@ static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap
     return tensor_map_2d(W, K, rows, kBoxK, box_rows, 0, out);
 }
 
+// Stage boxes of the one-launch decode step: a [rows][K] bf16 matrix viewed as
+// [rows][K / 64][64] so one box ({64, 4, box_rows}: box_rows rows x 256
+// columns) lands 128-byte swizzled in shared memory. K % 64 == 0.
+static cudaError_t step_stage_map(const void* W, int K, int rows, int box_rows, CUtensorMap* out) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    struct Entry { const void* w; int K, rows, br; CUtensorMap tm; };
+    static std::vector<Entry> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+        if (e.w == W && e.K == K && e.rows == rows && e.br == box_rows) {
+            *out = e.tm;
+            return cudaSuccess;
+        }
+    if (K % 64) return cudaErrorInvalidValue;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&encode),
+                                                         12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || !encode) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    }
+    cuuint64_t gdim[3] = {64u, (cuuint64_t)(K / 64), (cuuint64_t)rows};
+    cuuint64_t gstride[2] = {128u, (cuuint64_t)K * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)(kBoxK / 64), (cuuint32_t)box_rows};
+    cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    cache.push_back({W, K, rows, box_rows, *out});
+    return cudaSuccess;
+}
+
 // fp32 projections (bf16 decode runs as one launch: launch_decode_step)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s) {
     if (dtype != TP_F32) return cudaErrorInvalidValue;
@@ -972,7 +1005,7 @@ __device__ __forceinline__ unsigned sk_flush(SkPend& pd, const StepArgs& A, unsi
         // the activations were written by other CTAs' ordinary stores
         asm volatile("fence.proxy.async.global;" ::: "memory");
         // issued even after a failed wait: the stage's byte count must complete
-        tma_load_2d_keep(ring + pd.slot[i] * kSkStage + 2 * kBoxBytes, &A.xm[pd.map[i]], pd.x[i], pd.y[i],
+        tma_load_3d_keep(ring + pd.slot[i] * kSkStage + 2 * kBoxBytes, &A.xm[pd.map[i]], 0, pd.x[i] >> 6, pd.y[i],
                          &full[pd.slot[i]]);
     }
     pd.n = 0;
@@ -1073,10 +1106,10 @@ __device__ __forceinline__ bool sk_produce_gemv(int epi, int wi, unsigned need, 
             if (!mbar_wait(&empty[sl], par, abort, p.status)) return false;
             mbar_arrive_expect_tx(&full[sl], 2u * kBoxBytes + kXBoxBytes);
             unsigned char* dst = ring + sl * kSkStage;
-            tma_load_2d(dst, wmap, x, rowa, &full[sl], pol);
-            tma_load_2d(dst + kBoxBytes, wmap, x, rowb, &full[sl], pol);
+            tma_load_3d_hint(dst, wmap, 0, x >> 6, rowa, &full[sl], pol);
+            tma_load_3d_hint(dst + kBoxBytes, wmap, 0, x >> 6, rowb, &full[sl], pol);
             if (passed) {
-                tma_load_2d_keep(dst + 2 * kBoxBytes, xm, x, y, &full[sl]);
+                tma_load_3d_keep(dst + 2 * kBoxBytes, xm, 0, x >> 6, y, &full[sl]);
             } else {
                 if (pd.n == 0) flush_at = it + kSkRing;
                 pd.stage[pd.n] = it;
@@ -1511,10 +1544,14 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             mbar_wait(&full[sl], (it / kSkRing) & 1, abort, p.status);
             __syncwarp();
             const int steps_here = min(kBoxK / kKStep, (p.K - st * kBoxK) / kKStep);
+            // Boxes are 128-byte swizzled: 16-byte unit u of the 128-byte row
+            // (row, chunk c) sits at unit u ^ ((4 * row + c) & 7). A lane reads
+            // unit 4h + tq of chunk `step` in rows of its own parity (g & 1), so
+            // the eight rows a quarter warp touches fall on distinct banks.
             const unsigned char* stage = ring + sl * kSkStage;
-            const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
+            const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2);
             const unsigned char* wB = wA + 8 * (kBoxK * 2);
-            const unsigned char* px = stage + 2 * kBoxBytes + g * (kBoxK * 2) + tq * 16;
+            const unsigned char* px = stage + 2 * kBoxBytes + g * (kBoxK * 2);
             uint4 fa[2][2], fb[2][2], fx[2][2];
 #pragma unroll
             for (int s2 = 0; s2 < 2; ++s2)
@@ -1522,9 +1559,10 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
                 for (int h = 0; h < 2; ++h) {
                     const int step = wk + 2 * s2;
                     if (step < steps_here) {
-                        fa[s2][h] = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
-                        fb[s2][h] = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
-                        fx[s2][h] = *reinterpret_cast<const uint4*>(px + step * 128 + h * 64);
+                        const int off = step * 128 + ((h ^ (g & 1)) << 6) + ((tq ^ step) << 4);
+                        fa[s2][h] = *reinterpret_cast<const uint4*>(wA + off);
+                        fb[s2][h] = *reinterpret_cast<const uint4*>(wB + off);
+                        fx[s2][h] = *reinterpret_cast<const uint4*>(px + off);
                     }
                 }
             __syncwarp();
@@ -1989,7 +2027,7 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
         mbar_init(&qu->drained, 1);
         mbar_init(tab_ready, 1);
         qu->n_fin = 0;
-        *abort_flag = (smem_u32(ring) & 127u) ? 1 : 0;
+        *abort_flag = (smem_u32(ring) & 1023u) ? 1 : 0;       // 128-byte-swizzled boxes need 1024-byte alignment
         if (*abort_flag) set_status(status, TP_ERR_ALIGN);
         // read before this CTA arrives anywhere: fewer than gridDim.x arrivals of
         // this step can precede it
@@ -2082,10 +2120,10 @@ cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
         const GemvParams& p = P.g[i];
         A.g[i] = p;
         for (int r = 0; r < p.n_shards; ++r) {
-            cudaError_t e = weight_tensor_map(p.W[r], p.K, p.rows, &A.wm[i][r]);
+            cudaError_t e = step_stage_map(p.W[r], p.K, p.rows, 32, &A.wm[i][r]);
             if (e != cudaSuccess) return e;
         }
-        cudaError_t e = weight_tensor_map(p.xact, p.K, p.n_shards * kTMax, &A.xm[i], kTMax);
+        cudaError_t e = step_stage_map(p.xact, p.K, p.n_shards * kTMax, kTMax, &A.xm[i]);
         if (e != cudaSuccess) return e;
     }
     A.a = P.a;
