@@ -576,6 +576,7 @@ constexpr int kAtKeys = 64;                   // keys per stage
 constexpr int kAtRing = 5;
 constexpr int kAtMaxStage = 4 * kAtKeys * 72 * 2;   // K and V, two column halves each (head_dim 128)
 constexpr int kAtSlot = 1024;                 // floats per merge slot (G * head_dim <= 1024)
+static_assert(32 * kTMax <= kConsumers, "one QKV epilogue output per consumer thread");
 constexpr int kQStage = 3584;                 // bf16 elements of q staged for the attention phase (7 KB)
 constexpr int kQSegs = 7;                     // segments whose q is staged
 constexpr int kSegTab = 8;                    // attention segments per CTA listed ahead of the phase
@@ -971,7 +972,8 @@ struct SkQueue {
 
 // Consumer thread 0 only: the stores the job covers were made before a
 // consumer_sync; the mbarrier arrival orders them before the finisher's wait.
-__device__ __forceinline__ void sk_post(SkQueue* qu, uint32_t& jn, int type, int pi, int idx, unsigned expected,
+// Every consumer thread counts the posts (jn stays uniform across them).
+__device__ __forceinline__ void sk_post(SkQueue* qu, uint32_t jn, int type, int pi, int idx, unsigned expected,
                                         volatile int* abort, int* status) {
     const int sl = jn % kJobs;
     mbar_wait(&qu->empty[sl], ((jn / kJobs) & 1) ^ 1, abort, status);
@@ -980,7 +982,6 @@ __device__ __forceinline__ void sk_post(SkQueue* qu, uint32_t& jn, int type, int
     qu->job[sl].idx = idx;
     qu->job[sl].expected = expected;
     mbar_arrive(&qu->full[sl]);
-    ++jn;
 }
 
 // ---- producer helpers -------------------------------------------------------
@@ -1210,6 +1211,64 @@ __device__ __forceinline__ void sk_norm(const NormPrepParams& p) {
     }
 }
 
+// QKV output i of tile tb (token i / 32, tile rows i % 32 and i % 32 + 32,
+// a rotary pair): the factors that do not depend on the projection -- the
+// token's 1/rms, the biases and the rotation -- and their application.
+struct QkvPrep {
+    float rinv, ba, bb, cs, sn;
+};
+
+__device__ __forceinline__ QkvPrep sk_qkv_prep(const GemvParams& p, int r, int tb, int i, const float* ss,
+                                               const int* s_pos, const float* s_bias) {
+    const int d = p.head_dim, half = d >> 1;
+    const int t = i >> 5, j = i & 31;
+    QkvPrep q;
+    q.rinv = 1.0f / sqrtf(ss[t] * (1.0f / (float)p.K) + p.eps);
+    const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
+    const int head = rowA / d, ii = rowA - head * d;
+    q.ba = q.bb = 0.f;
+    if (s_bias) {
+        q.ba = s_bias[j];
+        q.bb = s_bias[j + 32];
+    } else if (p.bias[r]) {
+        q.ba = p.bias[r][rowA];
+        q.bb = p.bias[r][rowA + half];
+    }
+    q.cs = 1.f;
+    q.sn = 0.f;
+    if (head < p.hq_s + p.hkv_s)                        // q and k rotate, v does not
+        sincosf((float)s_pos[t] * exp2f(-(2.0f * ii / d) * (float)p.log2_theta), &q.sn, &q.cs);
+    return q;
+}
+
+__device__ __forceinline__ void sk_qkv_apply(const GemvParams& p, int r, int tb, int i, const float* tile,
+                                             const int* s_pos, const QkvPrep& q) {
+    const int d = p.head_dim, half = d >> 1;
+    const int t = i >> 5, j = i & 31;
+    const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
+    const int head = rowA / d, ii = rowA - head * d;
+    const float va = tile[j * kTMax + t] * q.rinv + q.ba;
+    const float vb = tile[(j + 32) * kTMax + t] * q.rinv + q.bb;
+    const float ra = va * q.cs - vb * q.sn, rb = va * q.sn + vb * q.cs;
+    if (head < p.hq_s) {
+        float* qo = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
+        qo[0] = ra;
+        qo[half] = rb;
+    } else {
+        const bool is_k = head < p.hq_s + p.hkv_s;
+        const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
+        const int pos = s_pos[t];
+        if (pos < 0 || pos >= p.max_kv) {
+            set_status(p.status, TP_ERR_CAPACITY);
+            return;
+        }
+        bf16* cache = reinterpret_cast<bf16*>(is_k ? p.kcache[r] : p.vcache[r]);
+        bf16* dst = cache + (((size_t)t * p.hkv_s + kvh) * p.max_kv + pos) * d + ii;
+        dst[0] = __float2bfloat16_rn(ra);
+        dst[half] = __float2bfloat16_rn(rb);
+    }
+}
+
 // Epilogue of a column-parallel tile whose full sum is in `tile` ([64][8]).
 // Threads tid0, tid0 + nthr, ... of the caller share the outputs. The bias of
 // the tile's rows comes from s_bias (shared) or, when null, from global memory.
@@ -1229,48 +1288,8 @@ __device__ __forceinline__ void sk_col_epilogue(const GemvParams& p, int r, int 
             out[((size_t)r * kTMax + t) * p.ffn_s + tb * 32 + j] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
         }
     } else {
-        const int d = p.head_dim, half = d >> 1;
-        const float inv_k = 1.0f / (float)p.K;
-        for (int i = tid; i < 32 * T; i += nthr) {
-            const int t = i >> 5, j = i & 31;
-            const float rinv = 1.0f / sqrtf(ss[t] * inv_k + p.eps);
-            const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
-            const int head = rowA / d, ii = rowA - head * d;
-            float ba = 0.f, bb = 0.f;
-            if (s_bias) {
-                ba = s_bias[j];
-                bb = s_bias[j + 32];
-            } else if (p.bias[r]) {
-                ba = p.bias[r][rowA];
-                bb = p.bias[r][rowA + half];
-            }
-            float va = tile[j * kTMax + t] * rinv + ba;
-            float vb = tile[(j + 32) * kTMax + t] * rinv + bb;
-            const int pos = s_pos[t];
-            if (head < p.hq_s + p.hkv_s) {
-                float cs, sn;
-                sincosf((float)pos * exp2f(-(2.0f * ii / d) * (float)p.log2_theta), &sn, &cs);
-                const float ra = va * cs - vb * sn, rb = va * sn + vb * cs;
-                va = ra;
-                vb = rb;
-            }
-            if (head < p.hq_s) {
-                float* q = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
-                q[0] = va;
-                q[half] = vb;
-            } else {
-                const bool is_k = head < p.hq_s + p.hkv_s;
-                const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
-                if (pos < 0 || pos >= p.max_kv) {
-                    set_status(p.status, TP_ERR_CAPACITY);
-                    continue;
-                }
-                bf16* cache = reinterpret_cast<bf16*>(is_k ? p.kcache[r] : p.vcache[r]);
-                bf16* dst = cache + (((size_t)t * p.hkv_s + kvh) * p.max_kv + pos) * d + ii;
-                dst[0] = __float2bfloat16_rn(va);
-                dst[half] = __float2bfloat16_rn(vb);
-            }
-        }
+        for (int i = tid; i < 32 * T; i += nthr)
+            sk_qkv_apply(p, r, tb, i, tile, s_pos, sk_qkv_prep(p, r, tb, i, ss, s_pos, s_bias));
     }
 }
 
@@ -1531,9 +1550,19 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
         int r, tb;
         sk_segment(p, EPI, seg, r, tb);
         if (EPI == EPI_ROWPAR && p.whole_tiles && r == 0) sk_row_prefetch(p, tb, slot);
-        float bias_v = 0.f;
-        if (EPI == EPI_QKV_ROPE && tid < kTileRows && p.bias[r])
-            bias_v = p.bias[r][tile_row(EPI_QKV_ROPE, tb, tid, p.head_dim, 0)];
+        int first, last;
+        sk_owners(seg, S, R, first, last);
+        if (EPI == EPI_QKV_ROPE && first == last && tid < 32 * p.T) {
+            // this CTA runs the tile's epilogue: its projection-independent
+            // factors are computed while the weights stream (thread-private slots)
+            const QkvPrep q = sk_qkv_prep(p, r, tb, tid, ss, s_pos, nullptr);
+            float* my = slot + tid * 8;
+            my[0] = q.rinv;
+            my[1] = q.ba;
+            my[2] = q.bb;
+            my[3] = q.cs;
+            my[4] = q.sn;
+        }
         // four independent accumulators (per 64-element step half and 16-byte
         // half) so the tensor-core ops of a stage do not form one dependent chain
         float ca[4][4];
@@ -1593,7 +1622,6 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             tile[i1] = c[2];
             tile[i1 + 1] = c[3];
         }
-        if (EPI == EPI_QKV_ROPE && tid < kTileRows) s_bias[tid] = bias_v;
         consumer_sync(kConsumers);
         if (wk == 1) {
             tile[i0] += c[0];
@@ -1602,8 +1630,6 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             tile[i1 + 1] += c[3];
         }
         consumer_sync(kConsumers);
-        int first, last;
-        sk_owners(seg, S, R, first, last);
         const int nsplit = p.shape.chunks;
         if (EPI == EPI_ROWPAR && p.whole_tiles) {       // this CTA holds every shard of output tile tb
             for (int i = tid; i < kTileRows * kTMax; i += kConsumers)
@@ -1616,7 +1642,14 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             continue;
         }
         if (EPI != EPI_ROWPAR && first == last) {      // the whole tile was this CTA's
-            sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, s_bias);
+            if (EPI == EPI_QKV_ROPE) {
+                if (tid < 32 * p.T) {
+                    const float* my = slot + tid * 8;
+                    sk_qkv_apply(p, r, tb, tid, tile, s_pos, QkvPrep{my[0], my[1], my[2], my[3], my[4]});
+                }
+            } else {
+                sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, s_bias);
+            }
             consumer_sync(kConsumers);
             continue;
         }
@@ -1638,6 +1671,7 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
                 sk_post(qu, jn, JOB_COL, pi, seg, (unsigned)(last - first + 1), abort, p.status);
             }
         }
+        ++jn;
     }
 }
 
@@ -1907,6 +1941,7 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
         }
         consumer_sync(kConsumers);                      // the piece is stored; the slots may be reused
         if (tid == 0) sk_post(qu, jn, JOB_ATTN, 0, gi, (unsigned)(last - first + 1), abort, p.status);
+        ++jn;
     }
 }
 
@@ -1951,20 +1986,30 @@ __device__ __forceinline__ void sk_finisher(const StepArgs& A, SkQueue* qu, vola
 
 // Consumers at the end of phase k (k = 1..kSkBarriers; k = kSkBarriers + 1 is
 // the last phase, which has no barrier): hand the phase end to the finisher,
-// run the finishes this CTA owes, then arrive at grid barrier k and wait.
+// run the finishes this CTA owes, then arrive at grid barrier k and wait. A
+// phase in which this CTA posted no piece job owes no finish: it skips the
+// hand-over (except the last, whose end job lets the finisher exit). `jn_mark`
+// is the post count at the previous phase end, `nd` the hand-overs so far.
 template <int D>
 __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long long base, unsigned k,
-                                             volatile int* abort, SkQueue* qu, uint32_t& jn, float* tile,
-                                             const float* ss, const int* s_pos, float* red, float* s_inv,
-                                             unsigned long long* st) {
+                                             volatile int* abort, SkQueue* qu, uint32_t& jn, uint32_t& jn_mark,
+                                             uint32_t& nd, float* tile, const float* ss, const int* s_pos,
+                                             float* red, float* s_inv, unsigned long long* st) {
     int* status = A.a.status;
+    const bool hand_over = jn != jn_mark || k > kSkBarriers;
     consumer_sync(kConsumers);
     if (threadIdx.x == 0) {
         if (st) st[2 * k - 1] = global_ns();
-        sk_post(qu, jn, k > kSkBarriers ? JOB_END : JOB_PHASE, 0, (int)k, 0u, abort, status);
+        if (hand_over) sk_post(qu, jn, k > kSkBarriers ? JOB_END : JOB_PHASE, 0, (int)k, 0u, abort, status);
     }
-    mbar_wait(&qu->drained, (k - 1) & 1, abort, status);
-    const int nf = *reinterpret_cast<volatile int*>(&qu->n_fin);
+    int nf = 0;
+    if (hand_over) {
+        ++jn;
+        mbar_wait(&qu->drained, nd & 1, abort, status);
+        ++nd;
+        nf = *reinterpret_cast<volatile int*>(&qu->n_fin);
+    }
+    jn_mark = jn;
     for (int f = 0; f < nf; ++f) {
         const SkJob j = qu->fin[f];
         if (j.type == JOB_COL) {
@@ -1980,7 +2025,7 @@ __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long lo
     }
     consumer_sync(kConsumers);
     if (threadIdx.x == 0) {
-        qu->n_fin = 0;
+        if (nf) qu->n_fin = 0;
         if (st) st[2 * k] = global_ns();
         if (k <= kSkBarriers) {
             asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(A.bar) : "memory");
@@ -2079,21 +2124,21 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     pdl_wait();                                         // x, positions and caches of the preceding step
     if (tid < kTMax) s_pos[tid] = tid < A.a.B ? A.a.pos[tid] : 0;
     consumer_sync(kConsumers);
-    uint32_t it = 0, jn = 0;
+    uint32_t it = 0, jn = 0, jn_mark = 0, nd = 0;
     sk_norm(A.np);
-    sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qs, seg_tab, s_nseg, tab_ready, qu,
                jn);
-    sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     pdl_trigger();                                      // the next launch may start streaming its weights
     sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
 }
 
 cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
