@@ -793,9 +793,10 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_
 // stages of the projections, or keys of the attention -- is laid out in one
 // flattened order and split evenly into one contiguous range per CTA, so
 // every SM streams the same number of bytes. A 64-row tile (or KV group)
-// whose range straddles two CTAs gets one fp32 partial per CTA; the CTA that
-// finishes last (a per-tile arrival counter) sums them in CTA order and runs
-// the epilogue, so results are deterministic and no extra phase is needed.
+// whose range straddles two CTAs gets one fp32 partial per CTA; one CTA --
+// the last to arrive for a tile (a per-tile arrival counter), the one holding
+// a KV group's last keys -- combines them in CTA order and runs the epilogue,
+// so results are deterministic and no extra phase is needed.
 // The producer thread streams the data of later phases that does not depend
 // on earlier ones -- every weight box, and every K/V block except the one
 // holding the new position -- through the same 5-stage ring while the
@@ -823,6 +824,12 @@ struct StepArgs {
     unsigned long long* bar;                // grid-barrier arrival counter (only grows)
     unsigned long long* stamps;             // optional [grid][kStepStamps]: start, barrier arrivals, end (ns)
 };
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
@@ -946,16 +953,17 @@ __device__ __forceinline__ void sk_locate(const KeySpace& ks, const AttnDecodePa
 
 // ---- finisher warp ----------------------------------------------------------------
 //
-// The consumer warps never wait for another CTA. When a piece of a tile (or
-// KV group) that other CTAs share is stored, or a phase is done, consumer
-// thread 0 posts a job to a small shared-memory queue and the consumers go
-// on streaming. A tenth warp takes the jobs in order: it publishes the
-// CTA's stores, counts the arrival for the tile, and if this CTA arrived last
-// it sums the pieces in CTA order and runs the epilogue; a phase-end job is
-// the CTA's arrival at the grid barrier, after every earlier job is done.
+// When a piece of a projection tile that other CTAs share is stored, or a
+// phase is done, consumer thread 0 posts a job to a small shared-memory queue
+// and the consumers go on streaming. A tenth warp takes the jobs in order: it
+// publishes the CTA's stores, counts the arrival for the tile, and if this
+// CTA arrived last the consumers sum the pieces in CTA order and run the
+// epilogue at the phase end. A KV group split over CTAs is finished instead
+// by the CTA holding its last keys (it streams them last): the others
+// release-increment the group's counter after storing their pieces.
 
 constexpr int kJobs = 8;
-enum SkJobType : int { JOB_COL = 0, JOB_ROW = 1, JOB_ATTN = 2, JOB_PHASE = 3, JOB_END = 4 };
+enum SkJobType : int { JOB_COL = 0, JOB_ROW = 1, JOB_PHASE = 3, JOB_END = 4 };
 struct SkJob {
     int type, pi, idx;
     unsigned expected;
@@ -1470,55 +1478,6 @@ __device__ __forceinline__ void sk_row_epilogue(const GemvParams& p, int tb, con
     sk_row_out(p, tb, total, res, my + 2);
 }
 
-// Consumers: KV group gi -- the pieces' (max, sum, unnormalised output)
-// combined with log-sum-exp weights in CTA order. `wgt` holds [pieces][8]
-// weights, `lsum` the same for the sums, `s_inv` 8 reciprocals.
-template <int D>
-__device__ __forceinline__ void sk_attn_finish(const AttnDecodeParams& p, int gi, int nc, float* wgt, float* lsum,
-                                               float* s_inv) {
-    const int tid = threadIdx.x;
-    const int G = p.hq_s / p.hkv_s, pstride = G * (D + 2);
-    const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
-    for (int i = tid; i < nc * G; i += kConsumers) {
-        const int cc = i / G, q = i - cc * G;
-        wgt[cc * kMaxGroup + q] = __ldcg(base + (size_t)cc * pstride + G * D + q);
-        lsum[cc * kMaxGroup + q] = __ldcg(base + (size_t)cc * pstride + G * D + G + q);
-    }
-    consumer_sync(kConsumers);
-    if (tid < G) {
-        float M = -INFINITY;
-        for (int cc = 0; cc < nc; ++cc)
-            if (lsum[cc * kMaxGroup + tid] > 0.f) M = fmaxf(M, wgt[cc * kMaxGroup + tid]);
-        float den = 0.f;
-        for (int cc = 0; cc < nc; ++cc) {
-            const float l = lsum[cc * kMaxGroup + tid];
-            const float w = l > 0.f ? expf(wgt[cc * kMaxGroup + tid] - M) : 0.f;
-            wgt[cc * kMaxGroup + tid] = w;
-            den = fmaf(l, w, den);
-        }
-        s_inv[tid] = den > 0.f ? 1.0f / den : 0.f;
-    }
-    consumer_sync(kConsumers);
-    const int kh = gi % p.hkv_s, rb = gi / p.hkv_s, b = rb % p.B, r = rb / p.B;
-    bf16* out = reinterpret_cast<bf16*>(p.out) + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)kh * G * D;
-    constexpr int kMaxSplit = 8;
-    for (int i = tid; i < G * D; i += kConsumers) {
-        const int gq = i / D;
-        float v[kMaxSplit];
-#pragma unroll
-        for (int cc = 0; cc < kMaxSplit; ++cc)
-            if (cc < nc) v[cc] = __ldcg(base + (size_t)cc * pstride + i);
-        float num = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < kMaxSplit; ++cc)
-            if (cc < nc) num = fmaf(v[cc], wgt[cc * kMaxGroup + gq], num);
-        for (int cc = kMaxSplit; cc < nc; ++cc)
-            num = fmaf(__ldcg(base + (size_t)cc * pstride + i), wgt[cc * kMaxGroup + gq], num);
-        out[i] = __float2bfloat16_rn(num * s_inv[gq]);
-    }
-    consumer_sync(kConsumers);
-}
-
 // One projection phase on the consumer side: this CTA's stage range, one
 // segment (tile of one shard) at a time.
 template <int EPI>
@@ -1928,20 +1887,91 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
             }
             continue;                                   // slots are rewritten after the next segment's first barrier
         }
-        float* mine = p.part + ((size_t)gi * p.n_chunks + ((int)blockIdx.x - first)) * pstride;
-        for (int i = tid; i < G * D; i += kConsumers) {
-            float acc = red[i];
+        const int nc = last - first + 1;
+        if ((int)blockIdx.x != last) {                  // a piece of a group the CTA holding its last keys finishes
+            float* mine = p.part + ((size_t)gi * p.n_chunks + ((int)blockIdx.x - first)) * pstride;
+            for (int i = tid; i < G * D; i += kConsumers) {
+                float acc = red[i];
 #pragma unroll
-            for (int w = 1; w < 8; ++w) acc += red[w * kAtSlot + i];
-            mine[i] = acc;
+                for (int w = 1; w < 8; ++w) acc += red[w * kAtSlot + i];
+                mine[i] = acc;
+            }
+            if (tid < G) {
+                mine[G * D + tid] = s_cmb[tid];
+                mine[G * D + G + tid] = s_cmb[kMaxGroup + tid];
+            }
+            consumer_sync(kConsumers);                  // the piece is stored; the slots may be reused
+            if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.cnt + gi) : "memory");
+            continue;
         }
-        if (tid < G) {
-            mine[G * D + tid] = s_cmb[tid];
-            mine[G * D + G + tid] = s_cmb[kMaxGroup + tid];
+        // This CTA holds the group's last keys (its block with the new position
+        // is streamed last, so it is normally the last to finish): wait for the
+        // other nc - 1 pieces, then combine them with its own, still in shared
+        // memory, in CTA order -- max, weights exp(m_c - M), sum of l_c w_c,
+        // sum of O_c w_c -- and store the normalised output.
+        if (tid == 0) {
+            const unsigned want = (unsigned)(nc - 1);
+            if (ld_acquire_u32(p.cnt + gi) != want) {
+                const uint64_t t0 = global_ns();
+                while (ld_acquire_u32(p.cnt + gi) != want) {
+                    if (*abort) break;
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        *abort = 1;
+                        set_status(p.status, TP_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            p.cnt[gi] = 0u;                             // counters are zero at every launch
         }
-        consumer_sync(kConsumers);                      // the piece is stored; the slots may be reused
-        if (tid == 0) sk_post(qu, jn, JOB_ATTN, 0, gi, (unsigned)(last - first + 1), abort, p.status);
-        ++jn;
+        consumer_sync(kConsumers);
+        const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
+        constexpr int kMaxSplit = 8;                    // pieces loaded in one batch (more: one at a time)
+        for (int i = tid; i < G * D; i += kConsumers) {
+            const int gq = i / D;
+            float pm[kMaxSplit], pl[kMaxSplit], pv[kMaxSplit];
+#pragma unroll
+            for (int cc = 0; cc < kMaxSplit; ++cc) {
+                if (cc < nc - 1) {
+                    const float* pc = base + (size_t)cc * pstride;
+                    pm[cc] = __ldcg(pc + G * D + gq);
+                    pl[cc] = __ldcg(pc + G * D + G + gq);
+                    pv[cc] = __ldcg(pc + i);
+                }
+            }
+            float own = red[i];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) own += red[w * kAtSlot + i];
+            const float mo = s_cmb[gq], lo = s_cmb[kMaxGroup + gq];
+            float M = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < kMaxSplit; ++cc)
+                if (cc < nc - 1 && pl[cc] > 0.f) M = fmaxf(M, pm[cc]);
+            for (int cc = kMaxSplit; cc < nc - 1; ++cc)
+                if (__ldcg(base + (size_t)cc * pstride + G * D + G + gq) > 0.f)
+                    M = fmaxf(M, __ldcg(base + (size_t)cc * pstride + G * D + gq));
+            if (lo > 0.f) M = fmaxf(M, mo);
+            float den = 0.f, num = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kMaxSplit; ++cc) {
+                if (cc < nc - 1) {
+                    const float w = pl[cc] > 0.f ? expf(pm[cc] - M) : 0.f;
+                    den = fmaf(pl[cc], w, den);
+                    num = fmaf(pv[cc], w, num);
+                }
+            }
+            for (int cc = kMaxSplit; cc < nc - 1; ++cc) {
+                const float* pc = base + (size_t)cc * pstride;
+                const float l = __ldcg(pc + G * D + G + gq);
+                const float w = l > 0.f ? expf(__ldcg(pc + G * D + gq) - M) : 0.f;
+                den = fmaf(l, w, den);
+                num = fmaf(__ldcg(pc + i), w, num);
+            }
+            const float wo = lo > 0.f ? expf(mo - M) : 0.f;
+            den = fmaf(lo, wo, den);
+            num = fmaf(own, wo, num);
+            out[i] = __float2bfloat16_rn(num * (den > 0.f ? 1.0f / den : 0.f));
+        }
     }
 }
 
@@ -1969,8 +1999,8 @@ __device__ __forceinline__ void sk_finisher(const StepArgs& A, SkQueue* qu, vola
         __syncwarp();
         if (!__all_sync(0xffffffffu, ok)) return;       // the consumers stopped posting (error already set)
         const SkJob j = qu->job[sl];
-        if (j.type == JOB_COL || j.type == JOB_ROW || j.type == JOB_ATTN) {
-            unsigned* cnt = j.type == JOB_ATTN ? A.a.cnt : A.g[j.pi].cnt;
+        if (j.type == JOB_COL || j.type == JOB_ROW) {
+            unsigned* cnt = A.g[j.pi].cnt;
             if (fin_arrive(cnt + j.idx, j.expected) && lane == 0) {
                 if (qu->n_fin < kMaxFin) qu->fin[qu->n_fin++] = j;
                 else set_status(status, TP_ERR_UNSUPPORTED);
@@ -2019,8 +2049,6 @@ __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long lo
             const GemvParams& p = A.g[j.pi];
             const int S = (p.K + kBoxK - 1) / kBoxK;
             sk_row_finish(p, j.idx, S, sk_phase_share(p, EPI_ROWPAR, S));
-        } else {
-            sk_attn_finish<D>(A.a, j.idx, (int)j.expected, red, red + 32 * kMaxGroup, s_inv);
         }
     }
     consumer_sync(kConsumers);
