@@ -963,7 +963,7 @@ __device__ __forceinline__ void sk_locate(const KeySpace& ks, const AttnDecodePa
 // release-increment the group's counter after storing their pieces.
 
 constexpr int kJobs = 8;
-enum SkJobType : int { JOB_COL = 0, JOB_ROW = 1, JOB_PHASE = 3, JOB_END = 4 };
+enum SkJobType : int { JOB_COL = 0, JOB_ROW = 1, JOB_GRP = 2, JOB_PHASE = 3, JOB_END = 4 };
 struct SkJob {
     int type, pi, idx;
     unsigned expected;
@@ -1484,7 +1484,7 @@ template <int EPI>
 __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned char* ring, uint64_t* full,
                                         uint64_t* empty, volatile int* abort, uint32_t& it, float* tile, float* acc,
                                         float* ss, int* s_pos, float* s_bias, float* slot, SkQueue* qu,
-                                        uint32_t& jn) {
+                                        uint32_t& jn, uint32_t& jf) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = (p.K + kBoxK - 1) / kBoxK;
     const int W = sk_nseg(p, EPI) * S;
@@ -1631,6 +1631,7 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             }
         }
         ++jn;
+        ++jf;
     }
 }
 
@@ -1863,16 +1864,26 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
                 dst[q1 * D + 16 * dt + g + 8] = o[dt][3] * c1;
             }
         }
-        if (tid < G) {                                  // this segment's (max, sum) per query
-            float M = -INFINITY;
-            for (int w = 0; w < 8; ++w) M = fmaxf(M, s_ml[(w * kMaxGroup + tid) * 2]);
-            float L = 0.f;
-            for (int w = 0; w < 8; ++w) {
-                const float mw = s_ml[(w * kMaxGroup + tid) * 2];
-                if (mw != -INFINITY) L += s_ml[(w * kMaxGroup + tid) * 2 + 1] * expf(mw - M);
+        if (warp == 0) {                                // this segment's (max, sum) per query: lane 4w + t
+            const int w = lane >> 2;                    // holds warp w's share of queries 2t, 2t + 1
+            const float mw0 = s_ml[(w * kMaxGroup + q0) * 2], mw1 = s_ml[(w * kMaxGroup + q1) * 2];
+            float L0 = mw0 == -INFINITY ? 0.f : s_ml[(w * kMaxGroup + q0) * 2 + 1] * expf(mw0 - M0);
+            float L1 = mw1 == -INFINITY ? 0.f : s_ml[(w * kMaxGroup + q1) * 2 + 1] * expf(mw1 - M1);
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                L0 += __shfl_xor_sync(0xffffffffu, L0, sh);
+                L1 += __shfl_xor_sync(0xffffffffu, L1, sh);
             }
-            s_cmb[tid] = M;
-            s_cmb[kMaxGroup + tid] = L;
+            if (lane < 4) {
+                if (q0 < G) {
+                    s_cmb[q0] = M0;
+                    s_cmb[kMaxGroup + q0] = L0;
+                }
+                if (q1 < G) {
+                    s_cmb[q1] = M1;
+                    s_cmb[kMaxGroup + q1] = L1;
+                }
+            }
         }
         consumer_sync(kConsumers);
         const int first = gstart / R, last = (gstart + len - 1) / R;
@@ -1901,7 +1912,9 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
                 mine[G * D + G + tid] = s_cmb[kMaxGroup + tid];
             }
             consumer_sync(kConsumers);                  // the piece is stored; the slots may be reused
-            if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.cnt + gi) : "memory");
+            // the finisher warp publishes the piece (its release would hold up this thread)
+            if (tid == 0) sk_post(qu, jn, JOB_GRP, 0, gi, 0u, abort, p.status);
+            ++jn;
             continue;
         }
         // This CTA holds the group's last keys (its block with the new position
@@ -1999,7 +2012,9 @@ __device__ __forceinline__ void sk_finisher(const StepArgs& A, SkQueue* qu, vola
         __syncwarp();
         if (!__all_sync(0xffffffffu, ok)) return;       // the consumers stopped posting (error already set)
         const SkJob j = qu->job[sl];
-        if (j.type == JOB_COL || j.type == JOB_ROW) {
+        if (j.type == JOB_GRP) {                        // an attention piece stored: count it for the group
+            if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(A.a.cnt + j.idx) : "memory");
+        } else if (j.type == JOB_COL || j.type == JOB_ROW) {
             unsigned* cnt = A.g[j.pi].cnt;
             if (fin_arrive(cnt + j.idx, j.expected) && lane == 0) {
                 if (qu->n_fin < kMaxFin) qu->fin[qu->n_fin++] = j;
@@ -2018,15 +2033,16 @@ __device__ __forceinline__ void sk_finisher(const StepArgs& A, SkQueue* qu, vola
 // the last phase, which has no barrier): hand the phase end to the finisher,
 // run the finishes this CTA owes, then arrive at grid barrier k and wait. A
 // phase in which this CTA posted no piece job owes no finish: it skips the
-// hand-over (except the last, whose end job lets the finisher exit). `jn_mark`
-// is the post count at the previous phase end, `nd` the hand-overs so far.
+// hand-over (except the last, whose end job lets the finisher exit). `jf`
+// counts the posts that can make this CTA owe a finish, `jf_mark` its value at
+// the previous phase end, `nd` the hand-overs so far.
 template <int D>
 __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long long base, unsigned k,
-                                             volatile int* abort, SkQueue* qu, uint32_t& jn, uint32_t& jn_mark,
+                                             volatile int* abort, SkQueue* qu, uint32_t& jn, uint32_t jf, uint32_t& jf_mark,
                                              uint32_t& nd, float* tile, const float* ss, const int* s_pos,
                                              float* red, float* s_inv, unsigned long long* st) {
     int* status = A.a.status;
-    const bool hand_over = jn != jn_mark || k > kSkBarriers;
+    const bool hand_over = jf != jf_mark || k > kSkBarriers;
     consumer_sync(kConsumers);
     if (threadIdx.x == 0) {
         if (st) st[2 * k - 1] = global_ns();
@@ -2039,7 +2055,7 @@ __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long lo
         ++nd;
         nf = *reinterpret_cast<volatile int*>(&qu->n_fin);
     }
-    jn_mark = jn;
+    jf_mark = jf;
     for (int f = 0; f < nf; ++f) {
         const SkJob j = qu->fin[f];
         if (j.type == JOB_COL) {
@@ -2152,21 +2168,21 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     pdl_wait();                                         // x, positions and caches of the preceding step
     if (tid < kTMax) s_pos[tid] = tid < A.a.B ? A.a.pos[tid] : 0;
     consumer_sync(kConsumers);
-    uint32_t it = 0, jn = 0, jn_mark = 0, nd = 0;
+    uint32_t it = 0, jn = 0, jf = 0, jf_mark = 0, nd = 0;
     sk_norm(A.np);
-    sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qs, seg_tab, s_nseg, tab_ready, qu,
                jn);
-    sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     pdl_trigger();                                      // the next launch may start streaming its weights
-    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn);
-    sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, jn_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
 }
 
 cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
