@@ -1836,6 +1836,28 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
 
         // ---- merge the eight warps: common max per query, every warp's rescaled
         // output into its slot, then all threads sum the slots in warp order
+        const int first = gstart / R, last = (gstart + len - 1) / R;
+        const int nc = last - first + 1;
+        // A KV group split over CTAs is combined by the CTA holding its last keys
+        // (its block with the new position streams last, so it normally finishes
+        // last): it waits for the other nc - 1 pieces here, and their loads go out
+        // during the merge below.
+        const bool owner = nc > 1 && (int)blockIdx.x == last;
+        if (owner && tid == 0) {
+            const unsigned want = (unsigned)(nc - 1);
+            if (ld_acquire_u32(p.cnt + gi) != want) {
+                const uint64_t t0 = global_ns();
+                while (ld_acquire_u32(p.cnt + gi) != want) {
+                    if (*abort) break;
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        *abort = 1;
+                        set_status(p.status, TP_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            p.cnt[gi] = 0u;                             // counters are zero at every launch
+        }
         float* s_ml = s_ml2 + (ui & 1) * (8 * kMaxGroup * 2);   // double-buffered across segments
         if (g == 0) {
             s_ml[(warp * kMaxGroup + q0) * 2] = m0;
@@ -1843,7 +1865,25 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
             s_ml[(warp * kMaxGroup + q1) * 2] = m1;
             s_ml[(warp * kMaxGroup + q1) * 2 + 1] = l1;
         }
-        consumer_sync(kConsumers);
+        consumer_sync(kConsumers);                      // also orders the pieces' loads after the wait
+        const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
+        constexpr int kEarly = 2;                       // pieces loaded before the merge's second half
+        const bool early = owner && G * D <= 2 * kConsumers;
+        float em[kEarly][2], el[kEarly][2], evv[kEarly][2];
+        if (early) {
+#pragma unroll
+            for (int cc = 0; cc < kEarly; ++cc)
+#pragma unroll
+                for (int o = 0; o < 2; ++o) {
+                    const int i = tid + o * kConsumers;
+                    if (cc < nc - 1 && i < G * D) {
+                        const float* pc = base + (size_t)cc * pstride;
+                        em[cc][o] = __ldcg(pc + G * D + i / D);
+                        el[cc][o] = __ldcg(pc + G * D + G + i / D);
+                        evv[cc][o] = __ldcg(pc + i);
+                    }
+                }
+        }
         float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
@@ -1886,9 +1926,8 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
             }
         }
         consumer_sync(kConsumers);
-        const int first = gstart / R, last = (gstart + len - 1) / R;
         bf16* out = reinterpret_cast<bf16*>(p.out) + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)kh * G * D;
-        if (first == last) {                            // the whole group: normalise and store
+        if (nc == 1) {                                  // the whole group: normalise and store
             for (int i = tid; i < G * D; i += kConsumers) {
                 float acc = red[i];
 #pragma unroll
@@ -1898,8 +1937,7 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
             }
             continue;                                   // slots are rewritten after the next segment's first barrier
         }
-        const int nc = last - first + 1;
-        if ((int)blockIdx.x != last) {                  // a piece of a group the CTA holding its last keys finishes
+        if (!owner) {                                   // a piece of a group another CTA finishes
             float* mine = p.part + ((size_t)gi * p.n_chunks + ((int)blockIdx.x - first)) * pstride;
             for (int i = tid; i < G * D; i += kConsumers) {
                 float acc = red[i];
@@ -1917,39 +1955,26 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
             ++jn;
             continue;
         }
-        // This CTA holds the group's last keys (its block with the new position
-        // is streamed last, so it is normally the last to finish): wait for the
-        // other nc - 1 pieces, then combine them with its own, still in shared
-        // memory, in CTA order -- max, weights exp(m_c - M), sum of l_c w_c,
-        // sum of O_c w_c -- and store the normalised output.
-        if (tid == 0) {
-            const unsigned want = (unsigned)(nc - 1);
-            if (ld_acquire_u32(p.cnt + gi) != want) {
-                const uint64_t t0 = global_ns();
-                while (ld_acquire_u32(p.cnt + gi) != want) {
-                    if (*abort) break;
-                    if (global_ns() - t0 > kWaitLimitNs) {
-                        *abort = 1;
-                        set_status(p.status, TP_ERR_TIMEOUT);
-                        break;
-                    }
-                }
-            }
-            p.cnt[gi] = 0u;                             // counters are zero at every launch
-        }
-        consumer_sync(kConsumers);
-        const float* base = p.part + (size_t)gi * p.n_chunks * pstride;
+        // owner: the pieces in CTA order -- max, weights exp(m_c - M), sum of
+        // l_c w_c, sum of O_c w_c -- with its own piece (in shared memory) last
         constexpr int kMaxSplit = 8;                    // pieces loaded in one batch (more: one at a time)
-        for (int i = tid; i < G * D; i += kConsumers) {
+        int o_idx = 0;
+        for (int i = tid; i < G * D; i += kConsumers, ++o_idx) {
             const int gq = i / D;
             float pm[kMaxSplit], pl[kMaxSplit], pv[kMaxSplit];
 #pragma unroll
             for (int cc = 0; cc < kMaxSplit; ++cc) {
                 if (cc < nc - 1) {
-                    const float* pc = base + (size_t)cc * pstride;
-                    pm[cc] = __ldcg(pc + G * D + gq);
-                    pl[cc] = __ldcg(pc + G * D + G + gq);
-                    pv[cc] = __ldcg(pc + i);
+                    if (early && cc < kEarly) {
+                        pm[cc] = o_idx ? em[cc][1] : em[cc][0];
+                        pl[cc] = o_idx ? el[cc][1] : el[cc][0];
+                        pv[cc] = o_idx ? evv[cc][1] : evv[cc][0];
+                    } else {
+                        const float* pc = base + (size_t)cc * pstride;
+                        pm[cc] = __ldcg(pc + G * D + gq);
+                        pl[cc] = __ldcg(pc + G * D + G + gq);
+                        pv[cc] = __ldcg(pc + i);
+                    }
                 }
             }
             float own = red[i];
