@@ -648,35 +648,7 @@ __global__ void rope_table_kernel(float2* tab, int max_pos, int half, int d, flo
     tab[i] = make_float2(cs, sn);
 }
 
-// ---------------------------------------------------------------------------
-// causal prefill attention on the fifth-generation tensor cores: one CTA per
-// 128 queries of one head of one sequence of one shard.
-//   warp 0    TMA: the Q tile once, then K and V blocks of 128 keys into a
-//             2-stage ring (128-byte swizzle, through a [group][key][d]
-//             tensor map: a block starting before key 0 reads zeros);
-//   warp 1    tensor memory (512 columns) and the MMA thread: S_j = Q K_j^T
-//             into one of two S buffers, then O_j = P_j V_j into one of two O
-//             buffers, V being the MN-major operand ([keys][d], d contiguous);
-//   warps 2-5 one query row per thread: S from tensor memory (twice: row max,
-//             then exp2 and sum), P_j as bf16 into one of two swizzled shared
-//             buffers, and O accumulated in registers with the online
-//             rescaling o = o * alpha_j + O_j, one block behind the MMA.
-// Keys of a block that are not the block's own (the last block is loaded
-// shifted to end at the last needed key, so every row it reads is a written
-// key or zero fill), or lie after the query, get probability 0.
-// ---------------------------------------------------------------------------
-
-constexpr int kFtQ = 128, kFtK = 128, kFtStages = 2, kFtThreads = 192;
-
-template <int D>
-struct FtShape {
-    static constexpr int NKB = D / 64;
-    static constexpr int QB = kFtQ * D * 2;
-    static constexpr int KB = kFtK * D * 2;
-    static constexpr int STAGE = 2 * KB;                 // K then V
-    static constexpr int PB = kFtQ * kFtK * 2;           // one P buffer: 2 x [128 rows x 64 keys]
-    static constexpr int SMEM = 1024 + QB + kFtStages * STAGE + 2 * PB;
-};
+constexpr int kFtQ = 128, kFtK = 128;          // queries per tile, keys per block
 
 struct FtArgs {
     CUtensorMap tq;                       // q [N*T, hq_s*D], boxes 64 x 128
@@ -697,38 +669,83 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, in
         : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// causal prefill attention, two query heads per CTA: the CTA takes one
+// 128-query tile for a pair of query heads that share a KV head, so both
+// tiles need the same keys. K/V stream once for the pair and the two tiles
+// take turns on the tensor cores while the other tile's softmax runs.
+//   warp 0    TMA: both Q tiles once, then K and V blocks of 128 keys into a
+//             2-stage ring (128-byte swizzle, [group][key][d] tensor map: a
+//             block starting before key 0 reads zeros);
+//   warp 1    tensor memory (512 columns: S_0, S_1, O_0, O_1) and the MMA
+//             thread: S_t = Q_t K_j^T, then O_t += P_t V_j with P_t read from
+//             tensor memory (written over S_t as bf16) and V the MN-major
+//             operand; S_t of the next block is issued right after O_t's
+//             product, so one tile's MMAs run under the other's softmax;
+//   warps 2-5 and 6-9: the softmax of tile 0 and 1, one query row per thread:
+//             S from tensor memory in one load, masked row max, P =
+//             exp2(S * scale - m) written back as bf16, running sum. The
+//             running max used for P moves only when a row's max grows by
+//             more than 8 (a factor 256, safe in bf16 and fp32); O is then
+//             rescaled in tensor memory. The commit that signals S_t of
+//             block j follows O_t of block j - 1, so O is complete whenever
+//             S is ready.
+// Keys of a block that are not the block's own (the last block is loaded
+// shifted to end at the last needed key) or lie after the query get
+// probability 0. The result is O / l per row.
+// ---------------------------------------------------------------------------
+
+constexpr int kFaThreads = 320;
+constexpr float kFaRescale = 8.0f;             // log2 of the growth that triggers a rescale
+constexpr int kFaKSt = 3, kFaVSt = 2;          // K and V rings: a K slot frees once S is computed
+
 template <int D>
-__global__ void __launch_bounds__(kFtThreads, 1) attn_tc_prefill_kernel(const __grid_constant__ FtArgs f) {
-    using Sh = FtShape<D>;
+struct FaShape {
+    static constexpr int NKB = D / 64;
+    static constexpr int QB = kFtQ * D * 2;             // one Q tile
+    static constexpr int KB = kFtK * D * 2;             // one K (or V) block
+    static constexpr int SMEM = 1024 + 2 * QB + (kFaKSt + kFaVSt) * KB;
+};
+
+// A shared-memory descriptor advanced by `bytes` (start address in 16-byte
+// units in the low bits; no carry for addresses below 256 KB).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+template <int D>
+__global__ void __launch_bounds__(kFaThreads, 1) attn_fa_prefill_kernel(const __grid_constant__ FtArgs f) {
+    using Sh = FaShape<D>;
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;          // [2]
-    uint64_t* kv_empty = bars + 3;         // [2]
-    uint64_t* s_full = bars + 5;           // [2]
-    uint64_t* s_empty = bars + 7;          // [2]
-    uint64_t* p_full = bars + 9;           // [2]
-    uint64_t* p_empty = bars + 11;         // [2]
-    uint64_t* o_full = bars + 13;          // [2]
-    uint64_t* o_empty = bars + 15;         // [2]
-    uint64_t* done = bars + 17;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+    uint64_t* k_full = bars + 1;           // [kFaKSt]
+    uint64_t* k_empty = k_full + kFaKSt;   // [kFaKSt]
+    uint64_t* v_full = k_empty + kFaKSt;   // [kFaVSt]
+    uint64_t* v_empty = v_full + kFaVSt;   // [kFaVSt]
+    uint64_t* s_full = v_empty + kFaVSt;   // [2] per tile
+    uint64_t* p_full = s_full + 2;         // [2] per tile
+    uint64_t* o_full = p_full + 2;         // [2] per tile: the last block's product
+    uint64_t* done = o_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     unsigned char* sq = smem + 1024;
-    unsigned char* skv = sq + Sh::QB;
-    unsigned char* sp = skv + kFtStages * Sh::STAGE;
+    unsigned char* sk = sq + 2 * Sh::QB;
+    unsigned char* sv = sk + kFaKSt * Sh::KB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // heaviest query blocks first (causal work grows with the block index)
+    const int G = f.hq_s / f.hkv_s, HP = (G + 1) / 2;
     const int nqb = (f.S + kFtQ - 1) / kFtQ;
     int idx = blockIdx.x;
     const int qb = nqb - 1 - idx % nqb;
     idx /= nqb;
-    const int h = idx % f.hq_s;
-    idx /= f.hq_s;
+    const int hp = idx % HP;
+    idx /= HP;
+    const int kvh = idx % f.hkv_s;
+    idx /= f.hkv_s;
     const int b = idx % f.B;
     const int r = idx / f.B;
-    const int G = f.hq_s / f.hkv_s, kvh = h / G;
+    const int h0 = kvh * G + 2 * hp;
+    const int ntile = (2 * hp + 1 < G) ? 2 : 1;
     const int p0 = f.pos[b];
     const int rows = min(kFtQ, f.S - qb * kFtQ);
     const int q_first = p0 + qb * kFtQ;
@@ -739,15 +756,18 @@ __global__ void __launch_bounds__(kFtThreads, 1) attn_tc_prefill_kernel(const __
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        for (int i = 0; i < kFaKSt; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < kFaVSt; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
             mbar_init(&p_full[i], 4);
-            mbar_init(&p_empty[i], 1);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_empty[i], 4);
         }
         mbar_init(done, 1);
         *abort_flag = (smem_u32(sq) & 1023u) ? 1 : 0;
@@ -762,169 +782,195 @@ __global__ void __launch_bounds__(kFtThreads, 1) attn_tc_prefill_kernel(const __
 
     if (warp == 0) {
         if (lane == 0 && !*abort_flag) {
-            mbar_arrive_expect_tx(q_full, Sh::QB);
+            mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * Sh::QB));
+            for (int t = 0; t < ntile; ++t)
 #pragma unroll
-            for (int kb = 0; kb < Sh::NKB; ++kb)
-                tma_load_2d_keep(sq + kb * (kFtQ * 128), &f.tq, h * D + kb * 64, r * f.T + t0, q_full);
-            int j = 0;
-            for (; j < nblk; ++j) {
-                const int s = j % kFtStages;
-                if (!mbar_wait(&kv_empty[s], ((j / kFtStages) & 1) ^ 1, abort_flag, f.status)) break;
-                mbar_arrive_expect_tx(&kv_full[s], Sh::STAGE);
+                for (int kb = 0; kb < Sh::NKB; ++kb)
+                    tma_load_2d_keep(sq + t * Sh::QB + kb * (kFtQ * 128), &f.tq, (h0 + t) * D + kb * 64, r * f.T + t0,
+                                     q_full);
+            // K runs ahead of V: block j's K is needed one product earlier than its V
+            int jk = 0, jv = 0;
+            bool ok = true;
+            while (ok && (jk < nblk || jv < nblk)) {
+                const bool do_k = jk < nblk && (jv >= nblk || jk <= jv + kFaKSt - 1);
+                const int j = do_k ? jk : jv;
                 const int key0 = min(j * kFtK, nkeys - kFtK);   // may be negative: zero fill
-                unsigned char* st = skv + s * Sh::STAGE;
+                if (do_k) {
+                    const int s = j % kFaKSt;
+                    if (!(ok = mbar_wait(&k_empty[s], ((j / kFaKSt) & 1) ^ 1, abort_flag, f.status))) break;
+                    mbar_arrive_expect_tx(&k_full[s], Sh::KB);
 #pragma unroll
-                for (int kb = 0; kb < Sh::NKB; ++kb) {
-                    tma_load_3d(st + kb * (kFtK * 128), &f.tk[r], kb * 64, key0, grp, &kv_full[s]);
-                    tma_load_3d(st + Sh::KB + kb * (kFtK * 128), &f.tv[r], kb * 64, key0, grp, &kv_full[s]);
+                    for (int kb = 0; kb < Sh::NKB; ++kb)
+                        tma_load_3d(sk + s * Sh::KB + kb * (kFtK * 128), &f.tk[r], kb * 64, key0, grp, &k_full[s]);
+                    ++jk;
+                } else {
+                    const int s = j % kFaVSt;
+                    if (!(ok = mbar_wait(&v_empty[s], ((j / kFaVSt) & 1) ^ 1, abort_flag, f.status))) break;
+                    mbar_arrive_expect_tx(&v_full[s], Sh::KB);
+#pragma unroll
+                    for (int kb = 0; kb < Sh::NKB; ++kb)
+                        tma_load_3d(sv + s * Sh::KB + kb * (kFtK * 128), &f.tv[r], kb * 64, key0, grp, &v_full[s]);
+                    ++jv;
                 }
             }
             volatile int no_abort = 0;
             mbar_wait(q_full, 0, &no_abort, nullptr);
-            for (int k = j > kFtStages ? j - kFtStages : 0; k < j; ++k)
-                mbar_wait(&kv_full[k % kFtStages], (k / kFtStages) & 1, &no_abort, nullptr);
+            for (int k = jk > kFaKSt ? jk - kFaKSt : 0; k < jk; ++k)
+                mbar_wait(&k_full[k % kFaKSt], (k / kFaKSt) & 1, &no_abort, nullptr);
+            for (int k = jv > kFaVSt ? jv - kFaVSt : 0; k < jv; ++k)
+                mbar_wait(&v_full[k % kFaVSt], (k / kFaVSt) & 1, &no_abort, nullptr);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(kFtQ, kFtK);
             const uint32_t id_o = idesc_bf16_bmn(kFtQ, D);
+            const uint64_t dq0 = smem_desc_sw128(smem_u32(sq)), dk0 = smem_desc_sw128(smem_u32(sk));
+            const uint64_t dv0 = smem_desc_mn_sw128(smem_u32(sv), kFtK * 128, 1024);
+            auto issue_s = [&](int t, int j) {          // S_t = Q_t K_j^T
+                const uint64_t dq = desc_add(dq0, t * Sh::QB), dk = desc_add(dk0, (j % kFaKSt) * Sh::KB);
+#pragma unroll
+                for (int kb = 0; kb < Sh::NKB; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        tc_mma(tmem + kFtK * t, desc_add(dq, kb * (kFtQ * 128) + k * 32),
+                               desc_add(dk, kb * (kFtK * 128) + k * 32), id_s, (kb | k) != 0);
+                tc_commit(smem_u32(&s_full[t]));
+            };
+            auto wait_k = [&](int j) {
+                const bool w = mbar_wait(&k_full[j % kFaKSt], (j / kFaKSt) & 1, abort_flag, f.status);
+                tc_fence_after();
+                return w;
+            };
             bool ok = !*abort_flag && mbar_wait(q_full, 0, abort_flag, f.status);
-            for (int j = 0; j <= nblk && ok; ++j) {
-                if (j < nblk) {                            // S_j = Q K_j^T
-                    const int s = j % kFtStages, bb = j & 1;
-                    if (!mbar_wait(&kv_full[s], (j / kFtStages) & 1, abort_flag, f.status)) break;
-                    if (!mbar_wait(&s_empty[bb], ((j >> 1) & 1) ^ 1, abort_flag, f.status)) break;
+            if (ok && nblk > 0 && (ok = wait_k(0))) {
+                for (int t = 0; t < ntile; ++t) issue_s(t, 0);
+                tc_commit(smem_u32(&k_empty[0]));
+            }
+            for (int j = 0; j < nblk && ok; ++j) {
+                const uint64_t dv = desc_add(dv0, (j % kFaVSt) * Sh::KB);
+                if (!(ok = mbar_wait(&v_full[j % kFaVSt], (j / kFaVSt) & 1, abort_flag, f.status))) break;
+                for (int t = 0; t < ntile && ok; ++t) {
+                    // O_t += P_t V_j, P_t in the first 64 columns of S_t
+                    if (!(ok = mbar_wait(&p_full[t], j & 1, abort_flag, f.status))) break;
                     tc_fence_after();
-                    const uint32_t qa = smem_u32(sq), ka = smem_u32(skv + s * Sh::STAGE);
 #pragma unroll
-                    for (int kb = 0; kb < Sh::NKB; ++kb)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma(tmem + kFtK * bb, smem_desc_sw128(qa + kb * (kFtQ * 128) + k * 32),
-                                   smem_desc_sw128(ka + kb * (kFtK * 128) + k * 32), id_s, (kb | k) != 0);
-                    tc_commit(smem_u32(&s_full[bb]));
+                    for (int kk = 0; kk < kFtK / 16; ++kk)
+                        tc_mma_ts(tmem + 2 * kFtK + D * t, tmem + kFtK * t + 8 * kk, desc_add(dv, kk * 16 * 128),
+                                  id_o, (j | kk) != 0);
+                    if (j + 1 == nblk) tc_commit(smem_u32(&o_full[t]));
+                    if (j + 1 < nblk) {                     // S_t of the next block, after O_t in issue order
+                        if (t == 0 && !(ok = wait_k(j + 1))) break;
+                        issue_s(t, j + 1);
+                    }
                 }
-                if (j >= 1) {                              // O_{j-1} = P_{j-1} V_{j-1}
-                    const int jj = j - 1, s = jj % kFtStages, bb = jj & 1;
-                    if (!mbar_wait(&p_full[bb], (jj >> 1) & 1, abort_flag, f.status)) break;
-                    if (!mbar_wait(&o_empty[bb], ((jj >> 1) & 1) ^ 1, abort_flag, f.status)) break;
-                    tc_fence_after();
-                    const uint32_t pa = smem_u32(sp + bb * Sh::PB), va = smem_u32(skv + s * Sh::STAGE + Sh::KB);
-#pragma unroll
-                    for (int kb2 = 0; kb2 < 2; ++kb2)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma(tmem + 2 * kFtK + D * bb, smem_desc_sw128(pa + kb2 * (kFtQ * 128) + k * 32),
-                                   smem_desc_mn_sw128(va + (kb2 * 64 + k * 16) * 128, kFtK * 128, 1024), id_o,
-                                   (kb2 | k) != 0);
-                    tc_commit(smem_u32(&o_full[bb]));
-                    tc_commit(smem_u32(&p_empty[bb]));
-                    tc_commit(smem_u32(&kv_empty[s]));
-                }
+                if (j + 1 < nblk) tc_commit(smem_u32(&k_empty[(j + 1) % kFaKSt]));
+                tc_commit(smem_u32(&v_empty[j % kFaVSt]));   // every MMA reading V_j has been issued
             }
             tc_commit(smem_u32(done));
         }
     } else {
-        // softmax: warps 2..5 -> tensor-memory lane quarters 2,3,0,1
-        const int qd = warp & 3;
+        const int t = (warp - 2) >> 2;                      // tile
+        const int qd = warp & 3;                            // tensor-memory lane quarter
         const int m = 32 * qd + lane;                       // query row of the tile
         const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
+        const uint32_t s_col = tmem + lane_off + kFtK * t, o_col = tmem + lane_off + 2 * kFtK + D * t;
         const int q_pos = q_first + m;
-        float o[D];
-#pragma unroll
-        for (int d = 0; d < D; ++d) o[d] = 0.f;
-        float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;
-        bool ok = true;
-        // o = o * alpha + O_jj (block jj's product, from tensor memory)
-        auto accumulate = [&](int jj, float alpha) {
-            const int bb = jj & 1;
-            ok = ok && mbar_wait(&o_full[bb], (jj >> 1) & 1, abort_flag, f.status);
+        const int warp_first = q_first + 32 * qd;           // the warp's smallest query position
+        float m_use = -INFINITY, l_run = 0.f;
+        bool ok = t < ntile;
+        for (int j = 0; j < nblk && ok; ++j) {
+            ok = mbar_wait(&s_full[t], j & 1, abort_flag, f.status);
             ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
             tc_fence_after();
+            uint32_t v[4][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + 2 * kFtK + D * bb + 32 * c, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[32 * c + i] = fmaf(o[32 * c + i], alpha, __uint_as_float(v[i]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_empty[bb]);
-        };
-        for (int j = 0; j < nblk; ++j) {
-            const int bb = j & 1;
-            ok = ok && mbar_wait(&s_full[bb], (j >> 1) & 1, abort_flag, f.status);
-            ok = __all_sync(0xffffffffu, ok);
-            tc_fence_after();
+            for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32 * c, v[c]);
+            tmem_wait_ld();
             const int key0 = min(j * kFtK, nkeys - kFtK);
             const int lo = j * kFtK, hi = min(lo + kFtK, nkeys);
-            const int kmax = min(hi - 1, q_pos);           // last key this row sees in the block
-            // pass 1: row maximum over the visible keys (log2 domain)
+            // a block whose keys all precede every row of the warp needs no mask
+            const bool whole = key0 == lo && hi == lo + kFtK && lo + kFtK - 1 <= warp_first;
+            const int kmax = min(hi - 1, q_pos);
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kFtK * bb + 32 * c, v);
-                tmem_wait_ld();
+            if (whole) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int key = key0 + 32 * c + i;
-                    if (key >= lo && key <= kmax) mx = fmaxf(mx, __uint_as_float(v[i]) * f.scale_log2);
-                }
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[c][i]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int key = key0 + 32 * c + i;
+                        if (key >= lo && key <= kmax) mx = fmaxf(mx, __uint_as_float(v[c][i]));
+                    }
             }
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-            // pass 2: probabilities into the P buffer (128-byte swizzled K-major rows)
-            ok = ok && mbar_wait(&p_empty[bb], ((j >> 1) & 1) ^ 1, abort_flag, f.status);
-            ok = __all_sync(0xffffffffu, ok);
-            unsigned char* prow = sp + bb * Sh::PB + m * 128;
+            const float m_blk = mx == -INFINITY ? -INFINITY : mx * f.scale_log2;
+            // the max used for P moves only on a large growth (or the first keys)
+            const bool grow = m_blk > m_use + kFaRescale;
+            const float alpha = grow ? ex2_approx(m_use - m_blk) : 1.f;   // 0 when m_use is -inf
+            if (grow) m_use = m_blk;
             float sum = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kFtK * bb + 32 * c, v);
-                tmem_wait_ld();
-                uint32_t pk[16];
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const int key = key0 + 32 * c + i;
-                    const float e0 = (key >= lo && key <= kmax) ? exp2f(__uint_as_float(v[i]) * f.scale_log2 - m_new) : 0.f;
-                    const float e1 =
-                        (key + 1 >= lo && key + 1 <= kmax) ? exp2f(__uint_as_float(v[i + 1]) * f.scale_log2 - m_new) : 0.f;
+                    const bool v0 = whole || (key >= lo && key <= kmax);
+                    const bool v1 = whole || (key + 1 >= lo && key + 1 <= kmax);
+                    const float e0 = v0 ? ex2_approx(fmaf(__uint_as_float(v[c][i]), f.scale_log2, -m_use)) : 0.f;
+                    const float e1 = v1 ? ex2_approx(fmaf(__uint_as_float(v[c][i + 1]), f.scale_log2, -m_use)) : 0.f;
                     sum += e0 + e1;
-                    pk[i / 2] = pack_bf16x2(e0, e1);
+                    pk[c >> 1][(c & 1) * 16 + i / 2] = pack_bf16x2(e0, e1);
                 }
+            l_run = l_run * alpha + sum;
+            tmem_st32(s_col, pk[0]);
+            tmem_st32(s_col + 32, pk[1]);
+            // O holds blocks 0 .. j-1 (complete: their products precede S of this
+            // block in the MMA order); rescale it where this row's max moved
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_col + 32 * c, o);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = (c & 1) * 4 + q;       // 16-byte chunk within the 64-key half
-                    *reinterpret_cast<uint4*>(prow + (c >> 1) * (kFtQ * 128) + ((chunk ^ (m & 7)) << 4)) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(o_col + 32 * c, o);
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P is read by the tensor cores
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&s_empty[bb]);
-                mbar_arrive(&p_full[bb]);
-            }
-            l_run = l_run * alpha + sum;
-            m_run = m_new;
-            if (j >= 1) accumulate(j - 1, alpha_prev);
-            alpha_prev = alpha;
+            if (lane == 0) mbar_arrive(&p_full[t]);
         }
-        if (nblk >= 1) accumulate(nblk - 1, alpha_prev);
-        // the output row
-        if (ok && m < rows) {
+        // the output row: O / l
+        if (ok && nblk > 0) {
+            ok = mbar_wait(&o_full[t], 0, abort_flag, f.status);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok && t < ntile) {
+            tc_fence_after();
             const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-            bf16* dst = f.out + ((size_t)r * f.T + t0 + m) * f.hq_s * D + h * D;
+            bf16* dst = f.out + ((size_t)r * f.T + t0 + m) * f.hq_s * D + (h0 + t) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(o_col + 32 * c, o);
+                tmem_wait_ld();
+                if (m < rows) {
 #pragma unroll
-            for (int d = 0; d < D; d += 8)
-                *reinterpret_cast<uint4*>(dst + d) =
-                    make_uint4(pack_bf16x2(o[d] * inv, o[d + 1] * inv), pack_bf16x2(o[d + 2] * inv, o[d + 3] * inv),
-                               pack_bf16x2(o[d + 4] * inv, o[d + 5] * inv), pack_bf16x2(o[d + 6] * inv, o[d + 7] * inv));
+                    for (int i = 0; i < 32; i += 8)
+                        *reinterpret_cast<uint4*>(dst + 32 * c + i) = make_uint4(
+                            pack_bf16x2(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv));
+                }
+            }
         }
     }
     tc_teardown(done, 0, tmem, 512);
@@ -1028,7 +1074,8 @@ cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s) {
-    const long grid = (long)p.N * p.B * p.hq_s * ((p.S + kFtQ - 1) / kFtQ);
+    const int G = p.hq_s / p.hkv_s;
+    const long grid = (long)p.N * p.B * p.hkv_s * ((G + 1) / 2) * ((p.S + kFtQ - 1) / kFtQ);
     if (grid == 0) return cudaSuccess;
     if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     FtArgs f;
@@ -1053,16 +1100,16 @@ cudaError_t launch_flash_prefill(const FlashParams& p, cudaStream_t s) {
     f.status = p.status;
     static bool set[2] = {false, false};
     const int which = p.d == 128 ? 1 : 0;
-    const void* fn = which ? reinterpret_cast<const void*>(attn_tc_prefill_kernel<128>)
-                           : reinterpret_cast<const void*>(attn_tc_prefill_kernel<64>);
-    const int smem = which ? FtShape<128>::SMEM : FtShape<64>::SMEM;
+    const void* fn = which ? reinterpret_cast<const void*>(attn_fa_prefill_kernel<128>)
+                           : reinterpret_cast<const void*>(attn_fa_prefill_kernel<64>);
+    const int smem = which ? FaShape<128>::SMEM : FaShape<64>::SMEM;
     if (!set[which]) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         set[which] = true;
     }
     void* args[] = {&f};
-    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kFtThreads), args, smem, s);
+    e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(kFaThreads), args, smem, s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
