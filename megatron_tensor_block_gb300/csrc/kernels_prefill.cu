@@ -892,40 +892,50 @@ __global__ void __launch_bounds__(kFaThreads, 1) attn_fa_prefill_kernel(const __
             // a block whose keys all precede every row of the warp needs no mask
             const bool whole = key0 == lo && hi == lo + kFtK && lo + kFtK - 1 <= warp_first;
             const int kmax = min(hi - 1, q_pos);
-            float mx = -INFINITY;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // independent chains
             if (whole) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[c][i]));
+                    for (int i = 0; i < 32; ++i) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(v[c][i]));
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int key = key0 + 32 * c + i;
-                        if (key >= lo && key <= kmax) mx = fmaxf(mx, __uint_as_float(v[c][i]));
+                        if (key >= lo && key <= kmax) mq[i & 3] = fmaxf(mq[i & 3], __uint_as_float(v[c][i]));
                     }
             }
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             const float m_blk = mx == -INFINITY ? -INFINITY : mx * f.scale_log2;
             // the max used for P moves only on a large growth (or the first keys)
             const bool grow = m_blk > m_use + kFaRescale;
             const float alpha = grow ? ex2_approx(m_use - m_blk) : 1.f;   // 0 when m_use is -inf
             if (grow) m_use = m_blk;
-            float sum = 0.f;
+            // P = 2^(S * scale - m) in independent passes (arguments, exponentials,
+            // sums, packing) so the exponentials of a row overlap; a masked key's
+            // argument is -inf, whose exponential is 0
+            float* e = reinterpret_cast<float*>(&v[0][0]);
+            if (whole) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) e[i] = fmaf(e[i], f.scale_log2, -m_use);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    const int key = key0 + i;
+                    e[i] = (key >= lo && key <= kmax) ? fmaf(e[i], f.scale_log2, -m_use) : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 128; ++i) e[i] = ex2_approx(e[i]);
+            float sq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 128; ++i) sq[i & 7] += e[i];
+            const float sum = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
             uint32_t pk[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int key = key0 + 32 * c + i;
-                    const bool v0 = whole || (key >= lo && key <= kmax);
-                    const bool v1 = whole || (key + 1 >= lo && key + 1 <= kmax);
-                    const float e0 = v0 ? ex2_approx(fmaf(__uint_as_float(v[c][i]), f.scale_log2, -m_use)) : 0.f;
-                    const float e1 = v1 ? ex2_approx(fmaf(__uint_as_float(v[c][i + 1]), f.scale_log2, -m_use)) : 0.f;
-                    sum += e0 + e1;
-                    pk[c >> 1][(c & 1) * 16 + i / 2] = pack_bf16x2(e0, e1);
-                }
+            for (int i = 0; i < 64; ++i) pk[i >> 5][i & 31] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
             l_run = l_run * alpha + sum;
             tmem_st32(s_col, pk[0]);
             tmem_st32(s_col + 32, pk[1]);
