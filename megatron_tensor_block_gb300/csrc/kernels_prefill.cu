@@ -821,7 +821,8 @@ __global__ void __launch_bounds__(kFaThreads, 1) attn_fa_prefill_kernel(const __
                 mbar_wait(&v_full[k % kFaVSt], (k / kFaVSt) & 1, &no_abort, nullptr);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        // the whole warp runs the loop (warp-uniform operands); one elected lane issues
+        {
             const uint32_t id_s = idesc_bf16(kFtQ, kFtK);
             const uint32_t id_o = idesc_bf16_bmn(kFtQ, D);
             const uint64_t dq0 = smem_desc_sw128(smem_u32(sq)), dk0 = smem_desc_sw128(smem_u32(sk));
@@ -832,41 +833,45 @@ __global__ void __launch_bounds__(kFaThreads, 1) attn_fa_prefill_kernel(const __
                 for (int kb = 0; kb < Sh::NKB; ++kb)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        tc_mma(tmem + kFtK * t, desc_add(dq, kb * (kFtQ * 128) + k * 32),
+                        tc_mma_w(tmem + kFtK * t, desc_add(dq, kb * (kFtQ * 128) + k * 32),
                                desc_add(dk, kb * (kFtK * 128) + k * 32), id_s, (kb | k) != 0);
-                tc_commit(smem_u32(&s_full[t]));
+                tc_commit_w(smem_u32(&s_full[t]));
+            };
+            // every lane waits; the outcome is made warp-uniform so the lanes stay together
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, f.status));
             };
             auto wait_k = [&](int j) {
-                const bool w = mbar_wait(&k_full[j % kFaKSt], (j / kFaKSt) & 1, abort_flag, f.status);
+                const bool w = wait_all(&k_full[j % kFaKSt], (j / kFaKSt) & 1);
                 tc_fence_after();
                 return w;
             };
-            bool ok = !*abort_flag && mbar_wait(q_full, 0, abort_flag, f.status);
+            bool ok = __all_sync(0xffffffffu, !*abort_flag) && wait_all(q_full, 0);
             if (ok && nblk > 0 && (ok = wait_k(0))) {
                 for (int t = 0; t < ntile; ++t) issue_s(t, 0);
-                tc_commit(smem_u32(&k_empty[0]));
+                tc_commit_w(smem_u32(&k_empty[0]));
             }
             for (int j = 0; j < nblk && ok; ++j) {
                 const uint64_t dv = desc_add(dv0, (j % kFaVSt) * Sh::KB);
-                if (!(ok = mbar_wait(&v_full[j % kFaVSt], (j / kFaVSt) & 1, abort_flag, f.status))) break;
+                if (!(ok = wait_all(&v_full[j % kFaVSt], (j / kFaVSt) & 1))) break;
                 for (int t = 0; t < ntile && ok; ++t) {
                     // O_t += P_t V_j, P_t in the first 64 columns of S_t
-                    if (!(ok = mbar_wait(&p_full[t], j & 1, abort_flag, f.status))) break;
+                    if (!(ok = wait_all(&p_full[t], j & 1))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kFtK / 16; ++kk)
-                        tc_mma_ts(tmem + 2 * kFtK + D * t, tmem + kFtK * t + 8 * kk, desc_add(dv, kk * 16 * 128),
+                        tc_mma_ts_w(tmem + 2 * kFtK + D * t, tmem + kFtK * t + 8 * kk, desc_add(dv, kk * 16 * 128),
                                   id_o, (j | kk) != 0);
-                    if (j + 1 == nblk) tc_commit(smem_u32(&o_full[t]));
+                    if (j + 1 == nblk) tc_commit_w(smem_u32(&o_full[t]));
                     if (j + 1 < nblk) {                     // S_t of the next block, after O_t in issue order
                         if (t == 0 && !(ok = wait_k(j + 1))) break;
                         issue_s(t, j + 1);
                     }
                 }
-                if (j + 1 < nblk) tc_commit(smem_u32(&k_empty[(j + 1) % kFaKSt]));
-                tc_commit(smem_u32(&v_empty[j % kFaVSt]));   // every MMA reading V_j has been issued
+                if (j + 1 < nblk) tc_commit_w(smem_u32(&k_empty[(j + 1) % kFaKSt]));
+                tc_commit_w(smem_u32(&v_empty[j % kFaVSt]));   // every MMA reading V_j has been issued
             }
-            tc_commit(smem_u32(done));
+            tc_commit_w(smem_u32(done));
         }
     } else {
         const int t = (warp - 2) >> 2;                      // tile
