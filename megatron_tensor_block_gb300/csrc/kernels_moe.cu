@@ -26,6 +26,8 @@ constexpr int kMoeGroups = kMoeTokPass / 8;
 constexpr int kMoeXBytes = kMoeGroups * kBoxK * 8 * 2; // 4 activation boxes of 8 rows x 256
 constexpr int kMoeStageBytes = 2 * kBoxBytes + kMoeXBytes;
 constexpr int kMoeStages = 3;
+constexpr int kMoeTG = 4;                // down projection with one stage per tile: tiles per unit
+constexpr int kMoeTS = kMoeTokPass + 1;  // tile row stride in shared memory (column reads free of bank conflicts)
 constexpr int kMaxExperts = 256;         // router
 constexpr int kMaxBucketExperts = 64;    // bucketing (per-warp count table)
 
@@ -185,18 +187,20 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
 
 // ---------------------------------------------------------------- grouped streaming GEMM
 //
-// Unit = (shard r, expert e, 64-row tile). Gate/up: rows are 32 gate + the
-// matching 32 up rows of the expert's shard slice, K = H. Down: 64 rows of H,
-// K = Fs. The expert's slots are processed in passes of 32 (four 8-column MMA
-// groups); each stage carries the weight boxes and up to four activation boxes.
+// Unit = (shard r, expert e, group of tiles of 64 rows). Gate/up: rows are 32
+// gate + the matching 32 up rows of the expert's shard slice, K = H, one tile
+// per unit. Down: 64 rows of H, K = Fs; when Fs fits one stage, a unit takes
+// kMoeTG tiles of the same expert, whose activation boxes arrive with the first
+// stage only and stay in registers for the rest. The expert's slots are
+// processed in passes of 32 (four 8-column MMA groups).
 
 __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeArgs A) {
     const MoeParams& p = A.p;
     extern __shared__ __align__(1024) unsigned char smem[];
     const Ring R = ring_setup(smem, kMoeStages);
     unsigned char* ring = smem + kCtrlBytes;
-    float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [64][32]
-    int* s_off = reinterpret_cast<int*>(tile + kTileRows * kMoeTokPass);          // [E+1]
+    float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [64][kMoeTS]
+    int* s_off = reinterpret_cast<int*>(tile + kTileRows * kMoeTS);               // [E+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool down = A.down != 0;
@@ -204,7 +208,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     const int tiles = down ? p.H / kTileRows : (2 * p.Fs) / kTileRows;
     const int K = down ? p.Fs : p.H;
     const int spu = (K + kBoxK - 1) / kBoxK;
-    const int U = p.N * p.E * tiles;
+    const int TG = (down && spu == 1) ? kMoeTG : 1;     // tiles per unit sharing the activation boxes
+    const int ngrp = (tiles + TG - 1) / TG;
+    const int U = p.N * p.E * ngrp;
 
     if (warp == kConsumers / 32) {                     // ---- producer
         if (lane == 0) {
@@ -217,31 +223,36 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                 set_status(p.status, TP_ERR_ALIGN);
             }
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const int tb = u % tiles, e = (u / tiles) % p.E, r = u / (tiles * p.E);
+                const int tg = u % ngrp, e = (u / ngrp) % p.E, r = u / (ngrp * p.E);
+                const int ntg = min(TG, tiles - tg * TG);
                 const int off = p.offsets[e], cnt = p.offsets[e + 1] - off;
-                int rowa, rowb;
-                if (down) {
-                    rowa = e * p.H + tb * kTileRows;
-                    rowb = rowa + 32;
-                } else {
-                    rowa = e * 2 * p.Fs + tb * 32;
-                    rowb = rowa + p.Fs;
-                }
                 for (int ps = 0; ps < cnt && ok; ps += kMoeTokPass) {
                     const int ng = min(kMoeGroups, (cnt - ps + 7) / 8);
-                    for (int st = 0; st < spu; ++st, ++it) {
-                        const int sl = it % kMoeStages;
-                        if (!mbar_wait(&R.empty[sl], ((it / kMoeStages) & 1) ^ 1, R.abort, p.status)) {
-                            ok = false;
-                            break;
+                    for (int i = 0; i < ntg && ok; ++i) {
+                        const int tb = tg * TG + i;
+                        int rowa, rowb;
+                        if (down) {
+                            rowa = e * p.H + tb * kTileRows;
+                            rowb = rowa + 32;
+                        } else {
+                            rowa = e * 2 * p.Fs + tb * 32;
+                            rowb = rowa + p.Fs;
                         }
-                        mbar_arrive_expect_tx(&R.full[sl], 2u * kBoxBytes + (uint32_t)ng * kBoxK * 8 * 2);
-                        unsigned char* dst = ring + sl * kMoeStageBytes;
-                        tma_load_2d(dst, &A.tw[r], st * kBoxK, rowa, &R.full[sl], pol);
-                        tma_load_2d(dst + kBoxBytes, &A.tw[r], st * kBoxK, rowb, &R.full[sl], pol);
-                        for (int g = 0; g < ng; ++g)
-                            tma_load_2d_keep(dst + 2 * kBoxBytes + g * kBoxK * 8 * 2, &A.tx[r], st * kBoxK,
-                                             off + ps + 8 * g, &R.full[sl]);
+                        const int nx = (TG == 1 || i == 0) ? ng : 0;    // activation boxes of this stage
+                        for (int st = 0; st < spu; ++st, ++it) {
+                            const int sl = it % kMoeStages;
+                            if (!mbar_wait(&R.empty[sl], ((it / kMoeStages) & 1) ^ 1, R.abort, p.status)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&R.full[sl], 2u * kBoxBytes + (uint32_t)nx * kBoxK * 8 * 2);
+                            unsigned char* dst = ring + sl * kMoeStageBytes;
+                            tma_load_2d(dst, &A.tw[r], st * kBoxK, rowa, &R.full[sl], pol);
+                            tma_load_2d(dst + kBoxBytes, &A.tw[r], st * kBoxK, rowb, &R.full[sl], pol);
+                            for (int g = 0; g < nx; ++g)
+                                tma_load_2d_keep(dst + 2 * kBoxBytes + g * kBoxK * 8 * 2, &A.tx[r], st * kBoxK,
+                                                 off + ps + 8 * g, &R.full[sl]);
+                        }
                     }
                 }
             }
@@ -260,91 +271,106 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     const int box = wm >> 1, brow = 16 * (wm & 1) + g;
     uint32_t it = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int tb = u % tiles, e = (u / tiles) % p.E, r = u / (tiles * p.E);
+        const int tg = u % ngrp, e = (u / ngrp) % p.E, r = u / (ngrp * p.E);
+        const int ntg = min(TG, tiles - tg * TG);
         const int off = s_off[e], cnt = s_off[e + 1] - off;
         for (int ps = 0; ps < cnt; ps += kMoeTokPass) {
             const int ng = min(kMoeGroups, (cnt - ps + 7) / 8);
-            float c[kMoeGroups][4];
+            uint4 xr[2][2][kMoeGroups];                 // activation fragments (kept across a unit's tiles)
+            for (int i = 0; i < ntg; ++i) {
+                const int tb = tg * TG + i;
+                float c[kMoeGroups][4];
 #pragma unroll
-            for (int q = 0; q < kMoeGroups; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
-            for (int st = 0; st < spu; ++st, ++it) {
-                const int sl = it % kMoeStages;
-                mbar_wait(&R.full[sl], (it / kMoeStages) & 1, R.abort, p.status);
-                __syncwarp();
-                const int steps_here = min(kBoxK / kKStep, (K - st * kBoxK) / kKStep);
-                const unsigned char* stage = ring + sl * kMoeStageBytes;
-                const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
-                const unsigned char* wB = wA + 8 * (kBoxK * 2);
+                for (int q = 0; q < kMoeGroups; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
+                for (int st = 0; st < spu; ++st, ++it) {
+                    const int sl = it % kMoeStages;
+                    mbar_wait(&R.full[sl], (it / kMoeStages) & 1, R.abort, p.status);
+                    __syncwarp();
+                    const int steps_here = min(kBoxK / kKStep, (K - st * kBoxK) / kKStep);
+                    const unsigned char* stage = ring + sl * kMoeStageBytes;
+                    const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
+                    const unsigned char* wB = wA + 8 * (kBoxK * 2);
+                    if (TG == 1 || i == 0) {
 #pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                    const int step = wk + 2 * s2;
-                    if (step < steps_here) {
+                        for (int s2 = 0; s2 < 2; ++s2)
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
-                            const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
+                            for (int h = 0; h < 2; ++h)
 #pragma unroll
-                            for (int q = 0; q < kMoeGroups; ++q) {
-                                if (q < ng) {
-                                    const uint4 xv = *reinterpret_cast<const uint4*>(
-                                        stage + 2 * kBoxBytes + q * kBoxK * 16 + g * (kBoxK * 2) + tq * 16 +
-                                        step * 128 + h * 64);
-                                    mma_bf16_16816(c[q], a.x, b.x, a.y, b.y, xv.x, xv.y);
-                                    mma_bf16_16816(c[q], a.z, b.z, a.w, b.w, xv.z, xv.w);
+                                for (int q = 0; q < kMoeGroups; ++q)
+                                    if (wk + 2 * s2 < steps_here && q < ng)
+                                        xr[s2][h][q] = *reinterpret_cast<const uint4*>(
+                                            stage + 2 * kBoxBytes + q * kBoxK * 16 + g * (kBoxK * 2) + tq * 16 +
+                                            (wk + 2 * s2) * 128 + h * 64);
+                    }
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const int step = wk + 2 * s2;
+                        if (step < steps_here) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
+                                const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
+#pragma unroll
+                                for (int q = 0; q < kMoeGroups; ++q) {
+                                    if (q < ng) {
+                                        const uint4 xv = xr[s2][h][q];
+                                        mma_bf16_16816(c[q], a.x, b.x, a.y, b.y, xv.x, xv.y);
+                                        mma_bf16_16816(c[q], a.z, b.z, a.w, b.w, xv.z, xv.w);
+                                    }
                                 }
                             }
                         }
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&R.empty[sl]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&R.empty[sl]);
-            }
-            // tile[row][slot] = half 0 + half 1
+                // tile[row][slot] = half 0 + half 1
 #pragma unroll
-            for (int q = 0; q < kMoeGroups; ++q) {
-                const int c0 = 8 * q + 2 * tq;
-                const int i0 = (16 * wm + g) * kMoeTokPass + c0, i1 = (16 * wm + g + 8) * kMoeTokPass + c0;
-                if (wk == 0) {
-                    tile[i0] = c[q][0];
-                    tile[i0 + 1] = c[q][1];
-                    tile[i1] = c[q][2];
-                    tile[i1 + 1] = c[q][3];
+                for (int q = 0; q < kMoeGroups; ++q) {
+                    const int c0 = 8 * q + 2 * tq;
+                    const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+                    if (wk == 0) {
+                        tile[i0] = c[q][0];
+                        tile[i0 + 1] = c[q][1];
+                        tile[i1] = c[q][2];
+                        tile[i1 + 1] = c[q][3];
+                    }
                 }
-            }
-            consumer_sync(kConsumers);
+                consumer_sync(kConsumers);
 #pragma unroll
-            for (int q = 0; q < kMoeGroups; ++q) {
-                const int c0 = 8 * q + 2 * tq;
-                const int i0 = (16 * wm + g) * kMoeTokPass + c0, i1 = (16 * wm + g + 8) * kMoeTokPass + c0;
-                if (wk == 1) {
-                    tile[i0] += c[q][0];
-                    tile[i0 + 1] += c[q][1];
-                    tile[i1] += c[q][2];
-                    tile[i1 + 1] += c[q][3];
+                for (int q = 0; q < kMoeGroups; ++q) {
+                    const int c0 = 8 * q + 2 * tq;
+                    const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+                    if (wk == 1) {
+                        tile[i0] += c[q][0];
+                        tile[i0 + 1] += c[q][1];
+                        tile[i1] += c[q][2];
+                        tile[i1 + 1] += c[q][3];
+                    }
                 }
+                consumer_sync(kConsumers);
+                const int nt = min(kMoeTokPass, cnt - ps);
+                if (down) {
+                    // expert output rows for this pass's slots (64 consecutive floats per slot)
+                    for (int i2 = tid; i2 < kTileRows * nt; i2 += kConsumers) {
+                        const int q = i2 / kTileRows, j = i2 - q * kTileRows;
+                        const int slot = off + ps + q;
+                        p.o[((size_t)r * nslot + slot) * p.H + tb * kTileRows + j] = tile[j * kMoeTS + q];
+                    }
+                } else {
+                    bf16* act = reinterpret_cast<bf16*>(p.act);
+                    for (int i2 = tid; i2 < 32 * nt; i2 += kConsumers) {   // 32 consecutive outputs per slot
+                        const int q = i2 >> 5, j = i2 & 31;
+                        const int slot = off + ps + q;
+                        const float rv = p.rinv[slot];
+                        const float gt = tile[j * kMoeTS + q] * rv;
+                        const float up = tile[(j + 32) * kMoeTS + q] * rv;
+                        act[((size_t)r * nslot + slot) * p.Fs + tb * 32 + j] =
+                            __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                    }
+                }
+                consumer_sync(kConsumers);
             }
-            consumer_sync(kConsumers);
-            const int nt = min(kMoeTokPass, cnt - ps);
-            if (down) {
-                // expert output rows for this pass's slots
-                for (int i = tid; i < kTileRows * nt; i += kConsumers) {
-                    const int j = i / nt, q = i - j * nt;
-                    const int slot = off + ps + q;
-                    p.o[((size_t)r * nslot + slot) * p.H + tb * kTileRows + j] = tile[j * kMoeTokPass + q];
-                }
-            } else {
-                bf16* act = reinterpret_cast<bf16*>(p.act);
-                for (int i = tid; i < 32 * nt; i += kConsumers) {
-                    const int j = i / nt, q = i - j * nt;
-                    const int slot = off + ps + q;
-                    const float rv = p.rinv[slot];
-                    const float gt = tile[j * kMoeTokPass + q] * rv;
-                    const float up = tile[(j + 32) * kMoeTokPass + q] * rv;
-                    act[((size_t)r * nslot + slot) * p.Fs + tb * 32 + j] =
-                        __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
-                }
-            }
-            consumer_sync(kConsumers);
         }
     }
 }
@@ -380,7 +406,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
 // ---------------------------------------------------------------- launch sequence
 
 static size_t moe_gemm_smem(int E) {
-    return kCtrlBytes + (size_t)kMoeStages * kMoeStageBytes + (size_t)kTileRows * kMoeTokPass * 4 +
+    return kCtrlBytes + (size_t)kMoeStages * kMoeStageBytes + (size_t)kTileRows * kMoeTS * 4 +
            (size_t)(E + 1) * 4 + 16;
 }
 
@@ -428,7 +454,8 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
             if (e != cudaSuccess) return e;
         }
         const int tiles = down ? p.H / kTileRows : 2 * p.Fs / kTileRows;
-        const int U = p.N * p.E * tiles;
+        const int TG = (down && (p.Fs + kBoxK - 1) / kBoxK == 1) ? kMoeTG : 1;
+        const int U = p.N * p.E * ((tiles + TG - 1) / TG);
         void* args[] = {&A};
         e = launch_pdl(reinterpret_cast<const void*>(moe_gemm_kernel), args, U < kSMs ? U : kSMs, smem, s,
                        kStreamThreads);
