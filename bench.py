@@ -40,7 +40,7 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
-FWD_PER_GRAPH = 8                  # forwards captured per CUDA graph in the timed region
+FWD_PER_GRAPH = 32                 # forwards captured per CUDA graph in the timed region
 
 METRIC = "TP-block decode tokens/s + HBM GB/s (% of ~8 TB/s peak) on 1 GB300"
 METRICS = {
