@@ -718,10 +718,11 @@ static cudaError_t weight_tensor_map(const void* W, int K, int rows, CUtensorMap
     return tensor_map_2d(W, K, rows, kBoxK, box_rows, 0, out);
 }
 
-// Stage boxes of the one-launch decode step: a [rows][K] bf16 matrix viewed as
-// [rows][K / 64][64] so one box ({64, 4, box_rows}: box_rows rows x 256
-// columns) lands 128-byte swizzled in shared memory. K % 64 == 0.
-static cudaError_t step_stage_map(const void* W, int K, int rows, int box_rows, CUtensorMap* out) {
+// Stage boxes of the streaming GEMVs (decode step, MoE experts): a [rows][K]
+// bf16 matrix viewed as [rows][K / 64][64] so one box ({64, 4, box_rows}:
+// box_rows rows x 256 columns) lands 128-byte swizzled in shared memory.
+// K % 64 == 0.
+cudaError_t step_stage_map(const void* W, int K, int rows, int box_rows, CUtensorMap* out) {
     static std::mutex mu;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     struct Entry { const void* w; int K, rows, br; CUtensorMap tm; };

@@ -32,8 +32,8 @@ constexpr int kMaxExperts = 256;         // router
 constexpr int kMaxBucketExperts = 64;    // bucketing (per-warp count table)
 
 struct MoeArgs {
-    CUtensorMap tw[TP_MAX_SHARDS];   // weights of the launch (egu or ed), boxes 256 x 32
-    CUtensorMap tx[TP_MAX_SHARDS];   // activations in slot order (xs or act), boxes 256 x 8
+    CUtensorMap tw[TP_MAX_SHARDS];   // weights of the launch (egu or ed), 128-byte-swizzled boxes of 32 rows x 256
+    CUtensorMap tx[TP_MAX_SHARDS];   // activations in slot order (xs or act), swizzled boxes of 8 rows x 256
     MoeParams p;
     int down;                        // 0: gate/up, 1: down
 };
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     const MoeParams& p = A.p;
     extern __shared__ __align__(1024) unsigned char smem[];
     const Ring R = ring_setup(smem, kMoeStages);
-    unsigned char* ring = smem + kCtrlBytes;
+    unsigned char* ring = smem + 1024;                  // swizzled boxes need 1024-byte alignment
     float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [64][kMoeTS]
     int* s_off = reinterpret_cast<int*>(tile + kTileRows * kMoeTS);               // [E+1]
 
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
             pdl_wait();                                // routing and activations come from earlier kernels
             const uint64_t pol = l2_evict_first_policy();
             uint32_t it = 0;
-            bool ok = (smem_u32(ring) & 127u) == 0;
+            bool ok = (smem_u32(ring) & 1023u) == 0;
             if (!ok) {
                 *R.abort = 1;
                 set_status(p.status, TP_ERR_ALIGN);
@@ -247,11 +247,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                             }
                             mbar_arrive_expect_tx(&R.full[sl], 2u * kBoxBytes + (uint32_t)nx * kBoxK * 8 * 2);
                             unsigned char* dst = ring + sl * kMoeStageBytes;
-                            tma_load_2d(dst, &A.tw[r], st * kBoxK, rowa, &R.full[sl], pol);
-                            tma_load_2d(dst + kBoxBytes, &A.tw[r], st * kBoxK, rowb, &R.full[sl], pol);
+                            tma_load_3d_hint(dst, &A.tw[r], 0, st * (kBoxK / 64), rowa, &R.full[sl], pol);
+                            tma_load_3d_hint(dst + kBoxBytes, &A.tw[r], 0, st * (kBoxK / 64), rowb, &R.full[sl], pol);
                             for (int g = 0; g < nx; ++g)
-                                tma_load_2d_keep(dst + 2 * kBoxBytes + g * kBoxK * 8 * 2, &A.tx[r], st * kBoxK,
-                                                 off + ps + 8 * g, &R.full[sl]);
+                                tma_load_3d_keep(dst + 2 * kBoxBytes + g * kBoxK * 8 * 2, &A.tx[r], 0,
+                                                 st * (kBoxK / 64), off + ps + 8 * g, &R.full[sl]);
                         }
                     }
                 }
@@ -287,8 +287,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                     mbar_wait(&R.full[sl], (it / kMoeStages) & 1, R.abort, p.status);
                     __syncwarp();
                     const int steps_here = min(kBoxK / kKStep, (K - st * kBoxK) / kKStep);
+                    // 128-byte-swizzled boxes: 16-byte unit u of the 128-byte row (row, chunk c)
+                    // sits at unit u ^ ((4 * row + c) & 7); every row a lane reads has parity g & 1
                     const unsigned char* stage = ring + sl * kMoeStageBytes;
-                    const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2) + tq * 16;
+                    const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2);
                     const unsigned char* wB = wA + 8 * (kBoxK * 2);
                     if (TG == 1 || i == 0) {
 #pragma unroll
@@ -297,10 +299,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                             for (int h = 0; h < 2; ++h)
 #pragma unroll
                                 for (int q = 0; q < kMoeGroups; ++q)
-                                    if (wk + 2 * s2 < steps_here && q < ng)
+                                    if (wk + 2 * s2 < steps_here && q < ng) {
+                                        const int step = wk + 2 * s2;
                                         xr[s2][h][q] = *reinterpret_cast<const uint4*>(
-                                            stage + 2 * kBoxBytes + q * kBoxK * 16 + g * (kBoxK * 2) + tq * 16 +
-                                            (wk + 2 * s2) * 128 + h * 64);
+                                            stage + 2 * kBoxBytes + q * kBoxK * 16 + g * (kBoxK * 2) + step * 128 +
+                                            ((h ^ (g & 1)) << 6) + ((tq ^ step) << 4));
+                                    }
                     }
 #pragma unroll
                     for (int s2 = 0; s2 < 2; ++s2) {
@@ -308,8 +312,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                         if (step < steps_here) {
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
-                                const uint4 a = *reinterpret_cast<const uint4*>(wA + step * 128 + h * 64);
-                                const uint4 b = *reinterpret_cast<const uint4*>(wB + step * 128 + h * 64);
+                                const int off_w = step * 128 + ((h ^ (g & 1)) << 6) + ((tq ^ step) << 4);
+                                const uint4 a = *reinterpret_cast<const uint4*>(wA + off_w);
+                                const uint4 b = *reinterpret_cast<const uint4*>(wB + off_w);
 #pragma unroll
                                 for (int q = 0; q < kMoeGroups; ++q) {
                                     if (q < ng) {
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
 // ---------------------------------------------------------------- launch sequence
 
 static size_t moe_gemm_smem(int E) {
-    return kCtrlBytes + (size_t)kMoeStages * kMoeStageBytes + (size_t)kTileRows * kMoeTS * 4 +
+    return 1024 + (size_t)kMoeStages * kMoeStageBytes + (size_t)kTileRows * kMoeTS * 4 +
            (size_t)(E + 1) * 4 + 16;
 }
 
@@ -441,15 +446,15 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         A.down = down;
         for (int r = 0; r < p.N; ++r) {
             if (down) {
-                e = tensor_map_2d(p.ed[r], p.Fs, (long)p.E * p.H, kBoxK, 32, 0, &A.tw[r]);
+                e = step_stage_map(p.ed[r], p.Fs, p.E * p.H, 32, &A.tw[r]);
                 if (e == cudaSuccess)
-                    e = tensor_map_2d(static_cast<const bf16*>(p.act) + (size_t)r * nslot * p.Fs, p.Fs, nslot, kBoxK, 8,
-                                      0, &A.tx[r]);
+                    e = step_stage_map(static_cast<const bf16*>(p.act) + (size_t)r * nslot * p.Fs, p.Fs, (int)nslot, 8,
+                                       &A.tx[r]);
             } else {
-                e = tensor_map_2d(p.egu[r], p.H, (long)p.E * 2 * p.Fs, kBoxK, 32, 0, &A.tw[r]);
+                e = step_stage_map(p.egu[r], p.H, p.E * 2 * p.Fs, 32, &A.tw[r]);
                 if (e == cudaSuccess)
-                    e = tensor_map_2d(static_cast<const bf16*>(p.xs) + (size_t)r * nslot * p.H, p.H, nslot, kBoxK, 8, 0,
-                                      &A.tx[r]);
+                    e = step_stage_map(static_cast<const bf16*>(p.xs) + (size_t)r * nslot * p.H, p.H, (int)nslot, 8,
+                                       &A.tx[r]);
             }
             if (e != cudaSuccess) return e;
         }

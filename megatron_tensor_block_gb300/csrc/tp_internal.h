@@ -152,6 +152,9 @@ cudaError_t tensor_map_2d(const void* base, long inner, long rows, int box_inner
                           CUtensorMap* out);
 cudaError_t tensor_map_3d(const void* base, long d0, long d1, long d2, int box0, int box1, int swizzle128,
                           CUtensorMap* out);
+// Streaming-GEMV stage boxes: [rows][K] bf16 as [rows][K/64][64], boxes of
+// box_rows rows x 256 columns, 128-byte swizzled (cached). K % 64 == 0.
+cudaError_t step_stage_map(const void* W, int K, int rows, int box_rows, CUtensorMap* out);
 
 // tcgen05 GEMM, C[M, N] (fp32) = A[M, K] * B[N, K]^T (bf16, K-major),
 // M % 128 == 0, N % 256 == 0, K % 64 == 0.
