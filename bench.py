@@ -357,9 +357,9 @@ def run_ours(args, world, rank, local):
     kind = WORKLOAD_KIND[w.name]
     stages = STAGES[kind]
     inputs = synth.make_inputs(w, with_head=False)
-    # replicated norm gammas: one tensor shared by the shards (prefill forms
-    # one normalised copy; decode reads it per shard either way)
-    model = Model(inputs, share_norm=(kind == "prefill"))
+    # replicated norm gammas: one tensor shared by the shards (prefill and MoE
+    # form one normalised copy; decode reads it per shard either way)
+    model = Model(inputs, share_norm=(kind in ("prefill", "moe")))
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 

@@ -40,12 +40,8 @@ struct MoeArgs {
 
 // ---------------------------------------------------------------- route
 
-__global__ void __launch_bounds__(256) moe_route_kernel(const MoeParams p) {
-    pdl_trigger();
-    pdl_wait();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= p.T) return;
+// One token per warp: the chosen experts and their renormalised weights.
+__device__ __forceinline__ void moe_route_token(const MoeParams& p, int t, int lane) {
     const float* lg = p.logits + (size_t)t * p.E;
     constexpr int kPer = kMaxExperts / 32;
     float v[kPer];
@@ -93,6 +89,13 @@ __global__ void __launch_bounds__(256) moe_route_kernel(const MoeParams p) {
             p.wts[t * p.top_k + j] = expf(sl[j] - sl[0]) / den;
         }
     }
+}
+
+__global__ void __launch_bounds__(256) moe_route_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t < p.T) moe_route_token(p, t, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------- bucket (one CTA, 1024 threads)
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
         a = fmaf(v.y, v.y, a);
         a = fmaf(v.z, v.z, a);
         a = fmaf(v.w, v.w, a);
-        for (int r = 0; r < p.N; ++r) {
+        for (int r = 0; r < p.xs_copies; ++r) {
             const float4 g = *reinterpret_cast<const float4*>(p.gamma[r] + k);
             uint2 pk;
             pk.x = pack_bf16x2(v.x * g.x, v.y * g.y);
@@ -426,6 +429,11 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         if (i < n_marks && marks[i]) cudaEventRecord(marks[i], s);
     };
     mark(0);
+    // one normalised copy of the slots' activations when every shard shares the gamma
+    q.xs_copies = p.N;
+    bool same = true;
+    for (int r = 1; r < p.N; ++r) same = same && p.gamma[r] == p.gamma[0];
+    if (same) q.xs_copies = 1;
     cudaError_t e = launch_small(reinterpret_cast<const void*>(moe_route_kernel), &q, (p.T + 7) / 8, 256, s);
     if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_bucket_kernel), &q, 1, 1024, s);
     if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_prep_kernel), &q, p.T * p.top_k, 256, s);
@@ -442,7 +450,7 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
     for (int down = 0; down < 2; ++down) {
         MoeArgs A;
         memset(&A, 0, sizeof A);
-        A.p = p;
+        A.p = q;
         A.down = down;
         for (int r = 0; r < p.N; ++r) {
             if (down) {
@@ -453,8 +461,8 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
             } else {
                 e = step_stage_map(p.egu[r], p.H, p.E * 2 * p.Fs, 32, &A.tw[r]);
                 if (e == cudaSuccess)
-                    e = step_stage_map(static_cast<const bf16*>(p.xs) + (size_t)r * nslot * p.H, p.H, (int)nslot, 8,
-                                       &A.tx[r]);
+                    e = step_stage_map(static_cast<const bf16*>(p.xs) + (size_t)(q.xs_copies > 1 ? r : 0) * nslot * p.H,
+                                       p.H, (int)nslot, 8, &A.tx[r]);
             }
             if (e != cudaSuccess) return e;
         }

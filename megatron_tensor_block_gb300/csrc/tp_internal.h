@@ -137,7 +137,8 @@ struct MoeParams {
     int* perm;                             // [T*k] slot -> flat choice index t*k + j
     int* slot_of;                          // [T*k] flat choice index -> slot
     float* rinv;                           // [T*k] 1/rms of each slot's token
-    void* xs;                              // [N][T*k][H] bf16: x_t * gamma_r in slot order
+    void* xs;                              // [xs_copies][T*k][H] bf16: x_t * gamma_r in slot order
+    int xs_copies;                         // 1 when every shard points at the same gamma, else N
     void* act;                             // [N][T*k][Fs] bf16: SwiGLU outputs per slot
     float* o;                              // [N][T*k][H] expert outputs per slot
     float* y;                              // [T][H]

@@ -71,3 +71,19 @@ def test_moe_is_deterministic(gpu_lib):
     b = m.forward().clone()
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("case", ["moe_expert_slice_tp4", "moe_small_tp2_skewed_ragged"])
+def test_moe_shared_gamma_gives_identical_bytes(gpu_lib, case):
+    # Every shard pointing at one gamma tensor: one normalised copy of the
+    # slots' activations serves all shards; same values, so the same bytes.
+    import torch
+    from megatron_tensor_block_gb300.runtime import Model
+    inputs = CASES[case]()
+    m1 = Model(inputs)
+    y1 = m1.forward().clone()
+    m2 = Model(inputs, share_norm=True)
+    y2 = m2.forward().clone()
+    torch.cuda.synchronize()
+    assert m1.ws.status() == 0 and m2.ws.status() == 0
+    assert torch.equal(y1, y2)
