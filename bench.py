@@ -64,7 +64,8 @@ STEP_INTERVALS = [f"{ph}{part}" for ph in STEP_PHASES for part in ("", "/finish"
 # the committed ncu summary of each dominant kernel and the source it was taken on
 PROFILE = {"decode": ("decode_step_llama3_8b_decode.md", "kernels_decode.cu"),
            "prefill": ("tc_gateup_llama3_8b_prefill.md", "kernels_prefill.cu"),
-           "moe": ("moe_gemm_expert_slice.md", "kernels_moe.cu")}
+           "moe": ("moe_gemm_expert_slice.md", "kernels_moe.cu"),
+           "stack": ("chain_qwen25_05b_decode.md", "kernels_chain.cu")}
 LAUNCHES_PER_LAYER = {"decode": 1, "prefill": 8, "moe": 6}
 L2_BYTES = 129e6
 
@@ -360,6 +361,9 @@ def run_ours(args, world, rank, local):
     # replicated norm gammas: one tensor shared by the shards (prefill and MoE
     # form one normalised copy; decode reads it per shard either way)
     model = Model(inputs, share_norm=(kind in ("prefill", "moe")))
+    # several decode layers: all of them in one launch per token
+    stacked = kind == "decode" and w.dtype == "bf16" and w.n_layers > 1 and args.stack
+    fwd = model.forward_stack if stacked else model.forward
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -370,16 +374,16 @@ def run_ours(args, world, rank, local):
     # one-forward graph covers a remainder.
     with torch.cuda.stream(stream):
         for _ in range(3):
-            model.forward(stream=stream)
+            fwd(stream=stream)
     stream.synchronize()
     per = max(1, min(FWD_PER_GRAPH, args.steps))
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for _ in range(per):
-            model.forward(stream=stream)
+            fwd(stream=stream)
     graph1 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph1, stream=stream):
-        model.forward(stream=stream)
+        fwd(stream=stream)
     for _ in range(max(args.warmup, 3)):
         graph.replay()
         graph1.replay()
@@ -410,9 +414,9 @@ def run_ours(args, world, rank, local):
     value = tokens_step * args.steps * world / (t_ms / 1e3)
 
     # ---- per-kernel durations: events around each launch, on the launching stream
-    step_kernel = kind == "decode" and w.dtype == "bf16"     # the whole step is one persistent launch
+    step_kernel = kind == "decode" and w.dtype == "bf16" and not stacked   # one persistent launch per layer
     n_prof = max(1, min(args.steps, 2000 if kind != "prefill" else 200))
-    n_ev = 2 if step_kernel else len(stages) + 1
+    n_ev = 2 if (step_kernel or stacked) else len(stages) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_prof)]
     for row in evs:          # torch creates events lazily: record once so the raw handles exist
         for e in row:
@@ -421,6 +425,11 @@ def run_ours(args, world, rank, local):
     phases = []
     with torch.cuda.stream(stream):
         for i in range(n_prof):
+            if stacked:
+                evs[i][0].record(stream)
+                fwd(stream=stream)
+                evs[i][1].record(stream)
+                continue
             tb.tp_profile_stages(model.plan, evs[i])
             model.forward(stream=stream)
             if step_kernel and i % 10 == 0:
@@ -428,7 +437,10 @@ def run_ours(args, world, rank, local):
         tb.tp_profile_stages(model.plan, None)
     torch.cuda.synchronize()
     stage_ms = {}
-    if step_kernel:
+    if stacked:
+        kernel_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(n_prof))
+        stage_ms["all_layers"] = kernel_ms
+    elif step_kernel:
         stages = STEP_INTERVALS
         for j, name in enumerate(stages):
             stage_ms[name] = statistics.mean(ph[0][j] for ph in phases) / 1e3
@@ -442,7 +454,20 @@ def run_ours(args, world, rank, local):
     dom = DOMINANT[kind]
     dom_ms = stage_ms.get(dom)
     extra = {}
-    if step_kernel:
+    if stacked:
+        # back-to-back launches of the one multi-layer kernel: its average
+        # launch duration in the timed region is the step time
+        sb = step_bytes(w)
+        achieved = sb / (ms_step / 1e3) / 1e9
+        peak = pk["hbm"]
+        roof = {"bound": "hbm", "kernel": f"chain_kernel (all {w.n_layers} layers in one persistent launch)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": pk["kind"] + " copy bandwidth", "algorithmic_bytes": sb, "launch_us": ms_step * 1e3,
+                "launch_us_isolated": kernel_ms * 1e3, "traffic": kernel_traffic("stack")}
+        extra["hbm"] = {"step_bytes": sb, "step_gbs": achieved, "frac_of_peak": achieved / peak,
+                        "frac_of_8000": achieved / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
+        l2_note = f"inputs larger than L2 ({sb / 1e6:.1f} MB read per step vs 129 MB L2)"
+    elif step_kernel:
         # the timed region is back-to-back launches of this one kernel (one per
         # layer): its average launch duration there is the step time per layer
         sb = step_bytes(w) // max(w.n_layers, 1)            # one launch = one layer
@@ -513,7 +538,7 @@ def run_ours(args, world, rank, local):
         model.x.copy_(x_host, non_blocking=True)
         for dev, host in extra_in:
             dev.copy_(host, non_blocking=True)
-        model.forward(stream=stream)
+        fwd(stream=stream)
         y_host.copy_(model.y, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -549,8 +574,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * 4 + sum(h.numel() * h.element_size() for _, h in extra_in),
                 "d2h_bytes_per_step": y_host.numel() * 4, "steps": e2e_steps,
-                "path": "tp_block_forward via the ctypes binding"},
-        "gpu_launches": (LAUNCHES_PER_LAYER[kind] if w.dtype == "bf16" else 5) * max(w.n_layers, 1) * args.steps,
+                "path": ("tp_stack_decode" if stacked else "tp_block_forward") + " via the ctypes binding"},
+        "gpu_launches": args.steps if stacked else
+        (LAUNCHES_PER_LAYER[kind] if w.dtype == "bf16" else 5) * max(w.n_layers, 1) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -567,6 +593,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_KIND))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack", action="store_true",
+                    help="multi-layer decode: one launch per token for all layers (tp_stack_decode) instead of one "
+                         "per layer (tp_block_forward)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -315,6 +315,61 @@ tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set* w, const 
                                    const float* x, float* y, const int32_t* pos, int32_t B,
                                    void* stream);
 
+/* ------------------------------------------- several decode blocks, one launch */
+
+typedef struct tp_stack_s* tp_stack_t;
+
+/* Prepares DECODE over a stack of n_layers blocks of one plan, layer l with
+ * its own shard tensors w[l] and KV caches kv[l] (HOST arrays of n_layers
+ * entries of caller-owned device pointers, as for tp_block_forward). Layer
+ * l's output is layer l+1's input: the decoder of [MG] How tensor
+ * parallelism works, steps 1-3, repeated per layer, with the pages' fused
+ * per-rank block graphs ([MG] CUDA graphs; [RT] Design) taken to one launch
+ * for all layers. The handle owns a small device buffer (TMA descriptors of
+ * every weight and cache, item tables); it reads the pointers, not the
+ * data, so weights and caches may change between calls but must not move.
+ * Requires a bf16 plan with head_dim 64 or 128, at most 8 query heads per KV
+ * head and max_batch <= 8. Allocates (cudaMalloc) and synchronises once.
+ * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no attention block, n_layers
+ * outside 1..255), TP_ERR_UNSUPPORTED (dtype, shape limits above), TP_ERR_ALIGN,
+ * TP_ERR_CUDA. */
+tp_status tp_stack_create(tp_plan_t plan, int32_t n_layers, const tp_shard_set* w,
+                          const tp_kv_set* kv, tp_stack_t* out);
+
+/* Frees a stack handle and its device buffer. NULL is accepted. */
+void tp_stack_destroy(tp_stack_t stack);
+
+/* CTAs of one tp_stack_decode launch (one per SM, at most 160); 0 for NULL. */
+int32_t tp_stack_ctas(tp_stack_t stack);
+
+/* Measurement hook: while set, every tp_stack_decode launch writes
+ * %globaltimer nanoseconds into `stamps` (DEVICE uint64, rows x n_layers x
+ * 5 x 2, caller-owned and zeroed by the caller): for CTA c, layer l and
+ * phase p (0 QKV, 1 attention, 2 o_proj, 3 gate/up, 4 down) the time the
+ * phase's inputs had arrived and the time its last output was stored.
+ * Phases in which a CTA has no work keep their entries. rows >= the
+ * stack's CTA count; NULL clears the hook.
+ * Errors: TP_ERR_NULL (stack), TP_ERR_SHAPE (rows too small). */
+tp_status tp_stack_set_stamps(tp_stack_t stack, uint64_t* stamps, int32_t rows);
+
+/* One decode token per sequence through every layer of the stack: the same
+ * values as n_layers calls of tp_block_forward (DECODE, T_per_seq = 1)
+ * chained through the layers, up to float32 summation order and the bf16
+ * rounding of the projection operands; K/V rows of every layer appended at
+ * pos[b]. x and y are float32 [B, H] (16-byte aligned, y != x); pos is DEVICE
+ * int32 [B], the same for every layer. `workspace` is a tp_workspace_init'ed
+ * workspace of at least the plan's workspace_bytes (its own region of it:
+ * the call may share a workspace with the other modes, but calls on one
+ * workspace must not overlap on the GPU). One kernel launch, no allocation:
+ * the call may be captured in a CUDA graph. A device-side wait that gives up
+ * (1 s) records TP_ERR_TIMEOUT in the status word; a position outside
+ * 0..max_kv-1 records TP_ERR_CAPACITY and is not written.
+ * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG, TP_ERR_SHAPE (B outside
+ * 1..min(max_batch, 8)), TP_ERR_CAPACITY (workspace too small), TP_ERR_ALIGN,
+ * TP_ERR_CUDA. */
+tp_status tp_stack_decode(tp_stack_t stack, const float* x, float* y, const int32_t* pos, int32_t B,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Standalone rank-order reduction ([RT] Collective backend abstraction,
  * copy-and-reduce; [MG] Local TP: the add after the copies):
  *   out[m, :] = residual[m, :] + (((p_0 + p_1) + p_2) + ... + p_{tp-1})[m, :] + bias

@@ -103,6 +103,11 @@ def load(path: str | None = None) -> C.CDLL:
                                    I32, VP, VP, C.c_size_t, VP]),
         "tp_block_forward_noalloc": (I32, [P, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), VP, VP, VP, I32,
                                            VP]),
+        "tp_stack_create": (I32, [P, I32, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), C.POINTER(P)]),
+        "tp_stack_destroy": (None, [P]),
+        "tp_stack_ctas": (I32, [P]),
+        "tp_stack_set_stamps": (I32, [P, VP, I32]),
+        "tp_stack_decode": (I32, [P, VP, VP, VP, I32, VP, C.c_size_t, VP]),
         "tp_reduce_partials": (I32, [P, VP, VP, VP, VP, I64, VP]),
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
         "tp_gemm_bf16": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
@@ -233,6 +238,46 @@ def tp_block_forward_noalloc(plan: Plan, shards: dict, kv: tuple, x, y, pos, B: 
     kvs = _kv_set(*kv)
     _check(load().tp_block_forward_noalloc(plan.handle, C.byref(_shard_set(shards)), C.byref(kvs), _ptr(x),
                                            _ptr(y), _ptr(pos), B, _stream(stream)))
+
+
+class Stack:
+    """Owns a ``tp_stack_t`` (several decode blocks in one launch); keeps the
+    plan alive and is destroyed with the object."""
+
+    def __init__(self, handle: int, plan: Plan):
+        self.handle = handle
+        self.plan = plan
+
+    def __del__(self):
+        if self.handle and _lib is not None:
+            _lib.tp_stack_destroy(self.handle)
+            self.handle = None
+
+
+def tp_stack_create(plan: Plan, layers: list, kvs: list) -> Stack:
+    """``layers``: per layer a shard dict (as for tp_block_forward);
+    ``kvs``: per layer a (k list, v list) pair."""
+    n = len(layers)
+    sets = (tp_shard_set * n)(*[_shard_set(d) for d in layers])
+    kvset = (tp_kv_set * n)(*[_kv_set(*kv) for kv in kvs])
+    h = C.c_void_p()
+    _check(load().tp_stack_create(plan.handle, n, sets, kvset, C.byref(h)))
+    return Stack(h.value, plan)
+
+
+def tp_stack_ctas(stack: Stack) -> int:
+    return int(load().tp_stack_ctas(stack.handle))
+
+
+def tp_stack_set_stamps(stack: Stack, stamps, rows: int) -> None:
+    """Measurement hook (``stamps``: zeroed device uint64 tensor of
+    rows x layers x 5 x 2, or None to clear)."""
+    _check(load().tp_stack_set_stamps(stack.handle, _ptr(stamps), rows))
+
+
+def tp_stack_decode(stack: Stack, x, y, pos, B: int, workspace, nbytes: int, stream=None) -> None:
+    _check(load().tp_stack_decode(stack.handle, _ptr(x), _ptr(y), _ptr(pos), B, _ptr(workspace), nbytes,
+                                  _stream(stream)))
 
 
 def tp_reduce_partials(plan: Plan, partials, residual, bias, out, M: int, stream=None) -> None:

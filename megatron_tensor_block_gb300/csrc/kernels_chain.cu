@@ -1,0 +1,1141 @@
+// Several decode blocks in one persistent launch, latency first.
+//
+// The computation of every layer is the decode block of "Tensor Parallelism
+// in llama.cpp" (How tensor parallelism works, steps 1-3): column-parallel
+// QKV with RoPE and a per-shard KV append, grouped-query attention over the
+// shard's own heads, the row-parallel o_proj whose shard partials are summed
+// in rank order before the residual, then the same for SwiGLU gate/up and
+// down_proj. Layer l's output is layer l+1's input.
+//
+// GB300 design: one CTA per SM; a producer warp streams each CTA's weight and
+// KV tiles for all layers through a ring of 16 KB slots (TMA, 128-byte
+// swizzled 3-D boxes), so weights are in shared memory before the activation
+// they multiply exists. Activations move between phases as 8-byte pairs
+// (float value, 32-bit epoch) written with one store: a consumer polls the
+// data itself, which replaces "store, fence, arrive, poll a counter, load"
+// by one round trip to L2 per phase. Every CTA that needs a whole vector
+// (the RMSNorm statistics, the split-KV combine) computes it itself from the
+// pairs instead of waiting for another CTA to do it.
+//
+// Phases of a layer and the CTA items of each (8 output rows per item; the
+// host balances the bytes of all items over the CTAs):
+//   QKV  rows 8i..8i+7 of shard r's [q_r; k_r; v_r] (+ bias)     -> fq
+//   ATT  keys of one (shard, sequence, KV head) group, one 16 KB tile of K
+//        and of V; RoPE of q and of the new key, online softmax  -> fp
+//   O    output rows 8i.., every shard (rank order) + residual   -> fh
+//   GU   SwiGLU rows 8i.. of shard r                              -> fa
+//   D    output rows 8i.., every shard (rank order) + residual   -> fx / y
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "stream.cuh"
+#include "tp_internal.h"
+
+namespace tpk {
+
+namespace {
+
+constexpr int kCW = 8;            // consumer warps
+constexpr int kCT = kCW * 32;     // consumer threads
+enum { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3 };   // projection phases (item tables)
+
+// ---- (value, epoch) pairs -------------------------------------------------------
+//
+// A pair is one naturally aligned 8-byte word, written and read as a unit, so a
+// reader that sees the epoch it expects sees the value written with it.
+
+__device__ __forceinline__ unsigned long long ll_pack(float v, unsigned ep) {
+    return ((unsigned long long)ep << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ void ll_st(unsigned long long* p, float v, unsigned ep) {
+    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, ep)) : "memory");
+}
+__device__ __forceinline__ void ll_ld2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ bool ll_ok(unsigned long long v, unsigned ep) { return (unsigned)(v >> 32) == ep; }
+__device__ __forceinline__ float ll_val(unsigned long long v) { return __uint_as_float((unsigned)v); }
+
+// Bounded polling: gives up after kWaitLimitNs, or at once when this CTA or
+// any other has given up (the CTA-local flag, then the workspace flag).
+struct Poll {
+    uint64_t t0 = 0;
+    int rounds = 0;
+};
+__device__ __forceinline__ bool poll_more(Poll& pl, const ChainArgs& A, volatile int* abort) {
+    if (*abort) return false;
+    if (pl.rounds++ == 0) pl.t0 = global_ns();
+    if ((pl.rounds & 15) == 0) {
+        if (*reinterpret_cast<volatile int*>(A.gabort)) {
+            *abort = 1;
+            return false;
+        }
+        if (global_ns() - pl.t0 > kWaitLimitNs) {
+            *abort = 1;
+            *reinterpret_cast<volatile int*>(A.gabort) = 1;
+            set_status(A.status, TP_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+
+
+// Barrier of the consumer warps that also ORs a flag over them, so that every
+// consumer takes the same branch after it.
+__device__ __forceinline__ bool csync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(kCT)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
+
+
+// ---- ring -------------------------------------------------------------------------
+
+struct CRing {
+    uint64_t* full;
+    uint64_t* empty;
+    unsigned char* base;   // slot 0, 1024-byte aligned
+    int ns;
+    volatile int* abort;
+};
+
+__device__ __forceinline__ unsigned char* ring_wait(const CRing& R, uint32_t k, int* status) {
+    mbar_wait(&R.full[k % R.ns], (k / R.ns) & 1, R.abort, status);
+    return R.base + (size_t)(k % R.ns) * kChainSlot;
+}
+// Every consumer warp releases every load it waited for.
+__device__ __forceinline__ void ring_release(const CRing& R, uint32_t k) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[k % R.ns]);
+}
+
+// ---- polling ----------------------------------------------------------------------
+//
+// A wait on pairs keeps every load of a round in flight: NB double pairs
+// (16 bytes: two pairs) per thread in registers, at double-pair offsets
+// off[u] from base (off < 0: none), the missing ones reloaded each round
+// until every pair carries epoch ep.
+constexpr int kPoll = 16;
+template <int NB>
+__device__ __forceinline__ bool ll_wait2(const unsigned long long* base, const int (&off)[NB],
+                                         unsigned long long (&v)[NB][2], unsigned ep, const ChainArgs& A,
+                                         volatile int* abort) {
+    unsigned need = 0;
+#pragma unroll
+    for (int u = 0; u < NB; ++u)
+        if (off[u] >= 0) {
+            ll_ld2(base + 2 * (size_t)off[u], v[u][0], v[u][1]);
+            need |= 1u << u;
+        }
+    Poll pl;
+    while (true) {
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            if ((need >> u & 1) && ll_ok(v[u][0], ep) && ll_ok(v[u][1], ep)) need &= ~(1u << u);
+        if (!need) return true;
+        if (!poll_more(pl, A, abort)) return false;
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            if (need >> u & 1) ll_ld2(base + 2 * (size_t)off[u], v[u][0], v[u][1]);
+    }
+}
+
+// Polls the double pairs of an index space 0..n-1 (thread: tid, tid + kCT,
+// ...; kPoll per round trip): src(i) is the double-pair offset from the
+// workspace region base, put(i, a, b) consumes the two values.
+template <class Src, class Put>
+__device__ __forceinline__ bool poll_space(const ChainArgs& A, int n, unsigned ep, volatile int* abort, Src src,
+                                           Put put) {
+    bool ok = true;
+#pragma unroll 1
+    for (int i0 = threadIdx.x; i0 < n; i0 += kPoll * kCT) {
+        int off[kPoll];
+        unsigned long long v[kPoll][2];
+#pragma unroll
+        for (int u = 0; u < kPoll; ++u) {
+            const int i = i0 + u * kCT;
+            off[u] = i < n ? src(i) : -1;
+        }
+        ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, abort) && ok;
+#pragma unroll
+        for (int u = 0; u < kPoll; ++u)
+            if (off[u] >= 0) put(i0 + u * kCT, ll_val(v[u][0]), ll_val(v[u][1]));
+    }
+    return ok;
+}
+
+// double-pair offset of a pair buffer element from the region base
+__device__ __forceinline__ int dp_off(const ChainArgs& A, const unsigned long long* p) {
+    return (int)((p - A.cbase) >> 1);
+}
+
+// ---- projection micro-kernel --------------------------------------------------------
+//
+// A load holds 8 weight rows as [row][kc chunks][64] bf16 (128-byte lines,
+// 16-byte unit u of line L stored at u ^ (L & 7)). With at most 8 tokens a
+// row's dot products are CUDA-core work (the MMA shapes would be at least half
+// empty): warp w takes row w of the box, each lane 16-byte units of it; a
+// warp's lanes read 512 contiguous bytes of weights and of the operand row.
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float s) {
+    s = fmaf(bf_lo(w.x), bf_lo(x.x), s);
+    s = fmaf(bf_hi(w.x), bf_hi(x.x), s);
+    s = fmaf(bf_lo(w.y), bf_lo(x.y), s);
+    s = fmaf(bf_hi(w.y), bf_hi(x.y), s);
+    s = fmaf(bf_lo(w.z), bf_lo(x.z), s);
+    s = fmaf(bf_hi(w.z), bf_hi(x.z), s);
+    s = fmaf(bf_lo(w.w), bf_lo(x.w), s);
+    s = fmaf(bf_hi(w.w), bf_hi(x.w), s);
+    return s;
+}
+// this lane's part of row `warp` of the box at w times one operand row
+__device__ __forceinline__ float row_dot(const unsigned char* w, int kc, int nvalid, const bf16* xrow) {
+    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float s = 0.f;
+#pragma unroll 2
+    for (int u = lane; u < 8 * nvalid; u += 32) {
+        const int ch = u >> 3, u8 = u & 7, line = row * kc + ch;
+        const uint4 wv = *reinterpret_cast<const uint4*>(w + line * 128 + ((u8 ^ (line & 7)) << 4));
+        const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 64 * ch + 8 * u8);
+        s = dot8(wv, xv, s);
+    }
+    return s;
+}
+
+// ---- shared memory ---------------------------------------------------------------------
+
+struct ChainSmem {
+    int ctrl, misc, xin, xa, gam, att, stage, qs, res, ring, total;
+};
+constexpr int kMiscBytes = 4096;
+constexpr int kPsBytes = kCW * 16 * 8 * 4;      // attention probabilities [128 keys][8 heads]
+constexpr int kStageFloats = 11 * 128;      // q (G <= 8 heads), new k, new v of one group, rotation
+__host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
+__host__ __device__ inline ChainSmem chain_layout(int MB, int H, int xs, int d, int ns) {
+    ChainSmem L;
+    int o = 0;
+    L.ctrl = o;  o += 256;                                   // full[12], empty[12], abort
+    L.misc = o;  o += kMiscBytes;
+    L.xin = o;   o = al16(o + MB * H * 4);
+    L.xa = o;    o = al16(o + MB * xs * 2);
+    L.gam = o;   o = al16(o + 2 * H * 4);                     // up to two gammas of a phase (float32)
+    L.att = o;   o += kCW * 8 * d * 4;                       // per-warp attention outputs [warp][head][d]
+    L.stage = o; o += kStageFloats * 4;
+    L.qs = o;    o = al16(o + kPsBytes + 2 * d * 2);           // probabilities [key][8 heads], new k, v (bf16)
+    L.res = o;   o = al16(o + kChainMaxItems * MB * 8 * 4);
+    o = (o + 1023) & ~1023;
+    L.ring = o;  o += ns * kChainSlot;
+    L.total = o + 1024;                                      // slack to align the base to 1024 bytes
+    return L;
+}
+// misc area (int offsets): item counts [4], items [4][kChainMaxItems], positions,
+// 1/rms per token, per-warp attention (max, sum) for 16 head rows
+constexpr int kMiCnt = 0, kMiItems = 4, kMiPos = kMiItems + 4 * kChainMaxItems, kMiRinv = kMiPos + 8,
+              kMiNch = kMiRinv + 8, kMiMl = kMiNch + 8;
+static_assert((kMiMl + kCW * 16 * 2) * 4 <= 2048, "misc area below the layer records");
+
+// ---- attention items ---------------------------------------------------------------------
+//
+// Items are (shard r, sequence b < T, KV head kh, key chunk c) in that order.
+// Sequence b holds len_b = min(pos_b + 1, max_kv) keys, split into chunks of
+// cs_b keys (a multiple of 16, at most ck, about even).
+
+__device__ __forceinline__ void att_split(int len, int ck, int& nch, int& cs) {
+    if (len <= 0) {
+        nch = 0;
+        cs = ck;
+        return;
+    }
+    const int n0 = (len + ck - 1) / ck;
+    cs = (((len + n0 - 1) / n0) + 15) & ~15;
+    if (cs > ck) cs = ck;
+    nch = (len + cs - 1) / cs;
+}
+__device__ __forceinline__ int att_len(const ChainArgs& A, int pos) { return min(max(pos + 1, 0), A.max_kv); }
+
+struct AttItem {
+    int r, b, kh, c, k0, nk, len;
+};
+__device__ __forceinline__ int att_count(const ChainArgs& A, const int* pos) {
+    int per_r = 0;
+    #pragma unroll 1
+    for (int b = 0; b < A.T; ++b) {
+        int nch, cs;
+        att_split(att_len(A, pos[b]), A.ck, nch, cs);
+        per_r += nch * A.hkv_s;
+    }
+    return per_r * A.N;
+}
+__device__ __forceinline__ AttItem att_item(const ChainArgs& A, const int* pos, int i) {
+    int per_r = 0;
+    #pragma unroll 1
+    for (int b = 0; b < A.T; ++b) {
+        int nch, cs;
+        att_split(att_len(A, pos[b]), A.ck, nch, cs);
+        per_r += nch * A.hkv_s;
+    }
+    AttItem it;
+    it.r = i / per_r;
+    int rem = i - it.r * per_r;
+    #pragma unroll 1
+    for (int b = 0; b < A.T; ++b) {
+        const int len = att_len(A, pos[b]);
+        int nch, cs;
+        att_split(len, A.ck, nch, cs);
+        if (rem < nch * A.hkv_s) {
+            it.b = b;
+            it.kh = rem / nch;
+            it.c = rem - it.kh * nch;
+            it.k0 = it.c * cs;
+            it.nk = min(cs, len - it.k0);
+            it.len = len;
+            return it;
+        }
+        rem -= nch * A.hkv_s;
+    }
+    it.b = it.kh = it.c = it.k0 = it.nk = it.len = 0;   // not reached for i < att_count
+    return it;
+}
+
+// ---- producer --------------------------------------------------------------------------
+//
+// One thread issues every copy of the CTA, in the order the consumers use
+// them: per layer the QKV items, the attention tiles, the o_proj items, the
+// gate/up items, the down items. Weight copies start before the preceding
+// kernel has finished (they do not depend on it); KV tiles after it.
+// Copy k of the CTA into its ring slot once the slot is free: one box, or
+// two boxes half a slot apart (tm2). False if the wait gave up.
+__device__ __forceinline__ bool prod_put(const CRing& R, uint32_t k, const CUtensorMap* tm, int y, int z, uint32_t bytes,
+                                      const CUtensorMap* tm2, int z2, uint64_t pol, int* status) {
+    const int s = (int)(k % (uint32_t)R.ns);
+    if (k >= (uint32_t)R.ns && !mbar_wait(&R.empty[s], (k / R.ns - 1) & 1, R.abort, status)) return false;
+    unsigned char* dst = R.base + (size_t)s * kChainSlot;
+    mbar_arrive_expect_tx(&R.full[s], bytes);
+    tma_load_3d_hint(dst, tm, 0, y, z, &R.full[s], pol);
+    if (tm2) tma_load_3d_hint(dst + kChainSlot / 2, tm2, 0, y, z2, &R.full[s], pol);
+    return true;
+}
+
+__device__ __forceinline__ void chain_producer(const ChainArgs& A, const CRing& R, const int* misc) {
+    const uint64_t pol = l2_evict_first_policy();
+    const int* cnt = misc + kMiCnt;
+    const int* items = misc + kMiItems;
+    uint32_t k = 0;
+    bool ok = true;
+    auto put = [&](const CUtensorMap* tm, int y, int z, uint32_t bytes, const CUtensorMap* tm2, int z2) {
+        ok = prod_put(R, k, tm, y, z, bytes, tm2, z2, pol, A.status);
+        k += ok ? 1u : 0u;
+    };
+    int pos[kTMax];
+    bool have_pos = false;
+    const int N = A.N;
+    #pragma unroll 1
+    for (int l = 0; l < A.L && ok; ++l) {
+        const CUtensorMap* M = A.maps + (size_t)l * kChainMaps * N;   // [kind][shard]
+        const int rbq = A.qkv_rows / 8;
+        #pragma unroll 1
+        for (int n = 0; n < cnt[PH_QKV] && ok; ++n) {
+            const int it = items[PH_QKV * kChainMaxItems + n], r = it / rbq, i = it - r * rbq;
+            #pragma unroll 1
+            for (int j = 0; j < A.nl[0] && ok; ++j) put(M + 0 * N + r, j * A.kc[0], 8 * i, 1024u * A.kc[0], nullptr, 0);
+        }
+        if (!have_pos) {
+            pdl_wait();                                   // KV caches and positions of the preceding kernel
+            #pragma unroll 1
+            for (int b = 0; b < kTMax; ++b) pos[b] = b < A.T ? A.pos[b] : 0;
+            have_pos = true;
+        }
+        const int na = att_count(A, pos);
+        #pragma unroll 1
+        for (int i = A.att_rank[blockIdx.x]; i < na && ok; i += A.grid) {
+            const AttItem a = att_item(A, pos, i);
+            const int row = (a.b * A.hkv_s + a.kh) * A.max_kv + a.k0;
+            const uint32_t bytes = (uint32_t)A.ck * A.d * 2;
+            put(M + 4 * N + a.r, 0, row, bytes, nullptr, 0);
+            if (ok) put(M + 5 * N + a.r, 0, row, bytes, nullptr, 0);
+        }
+        #pragma unroll 1
+        for (int n = 0; n < cnt[PH_O] && ok; ++n) {
+            const int i = items[PH_O * kChainMaxItems + n];
+            #pragma unroll 1
+            for (int r = 0; r < N && ok; ++r)
+                #pragma unroll 1
+                for (int j = 0; j < A.nl[1] && ok; ++j) put(M + 1 * N + r, j * A.kc[1], 8 * i, 1024u * A.kc[1], nullptr, 0);
+        }
+        const int rbg = A.F_s / 8;
+        #pragma unroll 1
+        for (int n = 0; n < cnt[PH_GU] && ok; ++n) {
+            const int it = items[PH_GU * kChainMaxItems + n], r = it / rbg, i = it - r * rbg;
+            #pragma unroll 1
+            for (int j = 0; j < A.nl[2] && ok; ++j)
+                put(M + 2 * N + r, j * A.kc[2], 8 * i, 2048u * A.kc[2], M + 2 * N + r, A.F_s + 8 * i);
+        }
+        #pragma unroll 1
+        for (int n = 0; n < cnt[PH_D] && ok; ++n) {
+            const int i = items[PH_D * kChainMaxItems + n];
+            #pragma unroll 1
+            for (int r = 0; r < N && ok; ++r)
+                #pragma unroll 1
+                for (int j = 0; j < A.nl[3] && ok; ++j) put(M + 3 * N + r, j * A.kc[3], 8 * i, 1024u * A.kc[3], nullptr, 0);
+        }
+    }
+    // every copy issued has landed before this thread leaves (if the consumers
+    // gave up, some were never waited for); bounded, independent of the abort flag
+    volatile int no_abort = 0;
+    const uint32_t first = k > (uint32_t)R.ns ? k - R.ns : 0u;
+    #pragma unroll 1
+    for (uint32_t q = first; q < k; ++q) mbar_wait(&R.full[q % R.ns], (q / R.ns) & 1, &no_abort, nullptr);
+}
+
+// ---- consumers ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+constexpr int kLayOff = 2048;   // byte offset of the two ChainLayer copies in the misc area
+
+// Per-CTA consumer state. Shared-memory regions are addressed from one base
+// and the launch's offsets (kernel parameters), so no pointer stays live in a
+// register across phases.
+struct Ctx {
+    unsigned char* sm;
+    int o_misc, o_xin, o_xa, o_gam, o_att, o_stage, o_qs, o_res, o_ring, ns, d;
+    uint32_t k = 0;          // ring loads consumed
+    int lb = 0;              // this layer's pointer record (0 or 1)
+    __device__ __forceinline__ void init(unsigned char* base, const ChainArgs& A) {
+        sm = base;
+        o_misc = A.sm_misc;
+        o_xin = A.sm_xin;
+        o_xa = A.sm_xa;
+        o_gam = A.sm_gam;
+        o_att = A.sm_att;
+        o_stage = A.sm_stage;
+        o_qs = A.sm_qs;
+        o_res = A.sm_res;
+        o_ring = A.sm_ring;
+        ns = A.n_slots;
+        d = A.d;
+    }
+    __device__ __forceinline__ int* misc() const { return reinterpret_cast<int*>(sm + o_misc); }
+    __device__ __forceinline__ float* xin() const { return reinterpret_cast<float*>(sm + o_xin); }
+    __device__ __forceinline__ bf16* xa() const { return reinterpret_cast<bf16*>(sm + o_xa); }
+    __device__ __forceinline__ float* gam() const { return reinterpret_cast<float*>(sm + o_gam); }
+    __device__ __forceinline__ float* att() const { return reinterpret_cast<float*>(sm + o_att); }
+    __device__ __forceinline__ float* stage() const { return reinterpret_cast<float*>(sm + o_stage); }
+    __device__ __forceinline__ float* ps() const { return reinterpret_cast<float*>(sm + o_qs); }
+    __device__ __forceinline__ bf16* knew() const { return reinterpret_cast<bf16*>(sm + o_qs + kPsBytes); }
+    __device__ __forceinline__ bf16* vnew() const { return knew() + d; }
+    __device__ __forceinline__ float* res() const { return reinterpret_cast<float*>(sm + o_res); }
+    __device__ __forceinline__ const ChainLayer* lay() const {
+        return reinterpret_cast<const ChainLayer*>(sm + o_misc + kLayOff) + lb;
+    }
+    __device__ __forceinline__ CRing ring() const {
+        CRing R;
+        R.full = reinterpret_cast<uint64_t*>(sm);
+        R.empty = R.full + kChainMaxSlots;
+        R.abort = reinterpret_cast<volatile int*>(R.empty + kChainMaxSlots);
+        R.base = sm + o_ring;
+        R.ns = ns;
+        return R;
+    }
+    __device__ __forceinline__ volatile int* abort() const {
+        return reinterpret_cast<volatile int*>(reinterpret_cast<uint64_t*>(sm) + 2 * kChainMaxSlots);
+    }
+};
+
+// Measurement hook: %globaltimer when a phase's inputs have arrived (w = 0)
+// and when its last output is stored (w = 1).
+__device__ __forceinline__ void stamp(const ChainArgs& A, int l, int ph, int w) {
+    if (A.stamps && threadIdx.x == 0) A.stamps[(((size_t)blockIdx.x * A.L + l) * 5 + ph) * 2 + w] = global_ns();
+}
+
+// The gammas of a phase's items (sorted by shard): the first, and the first
+// different one if the operand buffer has room for a second copy.
+struct Gammas {
+    const float* g0;
+    const float* g1;
+};
+__device__ __forceinline__ Gammas pick_gammas(const ChainArgs& A, const float* const* g, const int* items, int cnt,
+                                              int per_shard) {
+    Gammas r{g[items[0] / per_shard], nullptr};
+    if (2 * A.H + 8 > A.xa_stride) return r;
+    #pragma unroll 1
+    for (int n = 1; n < cnt; ++n) {
+        const float* x = g[items[n] / per_shard];
+        if (x != r.g0) {
+            r.g1 = x;
+            break;
+        }
+    }
+    return r;
+}
+// Copies the gammas into shared memory (asynchronously: call before a poll).
+__device__ __forceinline__ void gammas_fetch(Ctx& C, const ChainArgs& A, const Gammas& gs) {
+    #pragma unroll 1
+    for (int i = threadIdx.x; i < A.H / 4; i += kCT) {
+        cp_async16(C.gam() + 4 * i, gs.g0 + 4 * i);
+        if (gs.g1) cp_async16(C.gam() + A.H + 4 * i, gs.g1 + 4 * i);
+    }
+    cp_commit();
+}
+
+// The layer's input vector (T x H) into xin: from the pairs (src) or plain
+// (layer 0), then 1/rms per token and the bf16 operand copies x * gamma
+// (gammas staged by gammas_fetch; copy 1 at columns H..2H-1).
+__device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsigned long long* src, const float* plain, unsigned ep,
+                         bool two) {
+    const int T = A.T, H = A.H, n2 = T * H / 2;
+    float* xin = C.xin();
+    bool ok = true;
+    if (plain) {
+        #pragma unroll 1
+        for (int i = threadIdx.x; i < n2; i += kCT)
+            *reinterpret_cast<float2*>(xin + 2 * i) = *reinterpret_cast<const float2*>(plain + 2 * (size_t)i);
+    } else {
+        ok = poll_space(A, n2, ep, C.abort(), [&](int i) { return dp_off(A, src) + i; },
+                        [&](int i, float a, float b) { *reinterpret_cast<float2*>(xin + 2 * i) = make_float2(a, b); });
+    }
+    cp_wait();
+    if (csync_or(!ok)) return false;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    #pragma unroll 1
+    for (int t = warp; t < T; t += kCW) {
+        float a = 0.f;
+        #pragma unroll 1
+        for (int kk = lane; kk < H; kk += 32) a = fmaf(xin[t * H + kk], xin[t * H + kk], a);
+        a = warp_sum(a);
+        if (lane == 0) reinterpret_cast<float*>(C.misc())[kMiRinv + t] = 1.0f / sqrtf(a * (1.0f / (float)H) + A.eps);
+    }
+    const float* gm = C.gam();
+    #pragma unroll 1
+    for (int c = 0; c < (two ? 2 : 1); ++c)
+        #pragma unroll 1
+        for (int i = threadIdx.x; i < n2; i += kCT) {
+            const int e = 2 * i, t = e / H, kk = e - t * H;
+            *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + c * H + kk) =
+                pack_bf16x2(xin[e] * gm[c * H + kk], xin[e + 1] * gm[c * H + kk + 1]);
+        }
+    csync();
+    return true;
+}
+
+// xa (copy 0) = bf16(xin * gamma) for a further shard's gamma (read from global).
+__device__ __forceinline__ void build_xa(Ctx& C, const ChainArgs& A, const float* gamma) {
+    const int T = A.T, H = A.H;
+    csync();                                            // every warp is done with the previous operand
+    #pragma unroll 1
+    for (int i = threadIdx.x; i < T * H / 2; i += kCT) {
+        const int e = 2 * i, t = e / H, kk = e - t * H;
+        const float2 g = __ldg(reinterpret_cast<const float2*>(gamma + kk));
+        *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + kk) =
+            pack_bf16x2(C.xin()[e] * g.x, C.xin()[e + 1] * g.y);
+    }
+    csync();
+}
+
+// Row `warp` of an item whose nl loads are the next ring slots (NBOX boxes
+// per slot, half a slot apart), against every token's operand row from
+// column kbase: lane t (< T) accumulates token t's total into mine[b].
+template <int NBOX>
+__device__ __forceinline__ void item_rows(Ctx& C, const ChainArgs& A, int nl, int kc, int nch, int kbase,
+                                          float (&mine)[NBOX]) {
+    const int lane = threadIdx.x & 31;
+    #pragma unroll 1
+    for (int j = 0; j < nl; ++j) {
+        const unsigned char* w = ring_wait(C.ring(), C.k, A.status);
+        const int nv = min(kc, nch - j * kc);
+        #pragma unroll 1
+        for (int t = 0; t < A.T; ++t) {
+            const bf16* xr = C.xa() + (size_t)t * A.xa_stride + kbase + j * kc * 64;
+#pragma unroll
+            for (int b = 0; b < NBOX; ++b) {
+                const float sv = warp_sum(row_dot(w + b * (kChainSlot / 2), kc, nv, xr));
+                if (lane == t) mine[b] += sv;
+            }
+        }
+        ring_release(C.ring(), C.k);
+        ++C.k;
+    }
+}
+
+// The gamma copy holding shard r's operand (rebuilding copy 0 for a third distinct gamma).
+__device__ __forceinline__ int operand_col(Ctx& C, const ChainArgs& A, const Gammas& gs, const float*& have0,
+                                           const float* g) {
+    if (g == have0) return 0;
+    if (g == gs.g1) return A.H;
+    have0 = g;
+    build_xa(C, A, g);
+    return 0;
+}
+
+__device__ __forceinline__ bool phase_qkv(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
+    const int cnt = C.misc()[kMiCnt + PH_QKV];
+    if (csync_or(*C.abort())) return false;
+    if (!cnt) return true;
+    const int* items = C.misc() + kMiItems + PH_QKV * kChainMaxItems;
+    const int rbq = A.qkv_rows / 8, tid = threadIdx.x, MB = A.max_batch;
+    const ChainLayer& Ly = *C.lay();
+    // biases and gammas into shared memory while the input is polled
+    float* sbias = C.res();
+    #pragma unroll 1
+    for (int e = tid; e < 8 * cnt; e += kCT) {
+        const int it = items[e >> 3], r = it / rbq, i = it - r * rbq;
+        if (Ly.bqkv[r]) cp_async4(sbias + e, Ly.bqkv[r] + 8 * i + (e & 7));
+        else sbias[e] = 0.f;
+    }
+    const Gammas gs = pick_gammas(A, Ly.g_attn, items, cnt, rbq);
+    gammas_fetch(C, A, gs);
+    if (!load_vec(C, A, l == 0 ? nullptr : A.fx, l == 0 ? A.x : nullptr, ep, gs.g1 != nullptr)) return false;
+    stamp(A, l, 0, 0);
+    const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
+    const float* have0 = gs.g0;
+    const int warp = tid >> 5, lane = tid & 31;
+    #pragma unroll 1
+    for (int n = 0; n < cnt; ++n) {
+        const int it = items[n], r = it / rbq, i = it - r * rbq;
+        const int kb = operand_col(C, A, gs, have0, Ly.g_attn[r]);
+        float mine[1] = {0.f};
+        item_rows<1>(C, A, A.nl[0], A.kc[0], A.H / 64, kb, mine);
+        if (lane < A.T)
+            ll_st(A.fq + (size_t)(r * MB + lane) * A.qkv_rows + 8 * i + warp, mine[0] * rinv[lane] + sbias[8 * n + warp],
+                  ep);
+    }
+    stamp(A, l, 0, 1);
+    return true;
+}
+
+// Attention items of this CTA: RoPE of q and of the new key (rotate-half
+// pairs (e, e + d/2) at angle pos * theta^(-2e/d)), the new K/V row written
+// into the shared-memory tiles and into the shard's cache; then per warp its
+// keys: scores q K^T (scaled, log2 units), online softmax, O = P V; the warps'
+// (max, sum, O) merged into the chunk's partial.
+__device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int* pos = C.misc() + kMiPos;
+    const int G = A.G, d = A.d, half = d >> 1, MB = A.max_batch, DC = d >> 6;
+    const int na = att_count(A, pos);
+    const ChainLayer& Ly = *C.lay();
+    float* ml = reinterpret_cast<float*>(C.misc()) + kMiMl;
+    float* st = C.stage();
+    #pragma unroll 1
+    for (int i = A.att_rank[blockIdx.x]; i < na; i += A.grid) {
+        if (csync_or(*C.abort())) return false;
+        const AttItem a = att_item(A, pos, i);
+        const int pb = pos[a.b];
+        const bool has_new = pb >= 0 && pb < A.max_kv && pb >= a.k0 && pb < a.k0 + a.nk;
+        // the rotation of this position (table row) while q, k, v are polled
+        float* rot = st + (G + 2) * d;                       // [d/2] (cos, sin)
+        if (pb >= 0 && pb < A.max_kv)
+            #pragma unroll 1
+            for (int e = tid; e < half / 2; e += kCT) cp_async16(rot + 4 * e, A.rope + ((size_t)pb * half + 2 * e));
+        cp_commit();
+        // raw q (G heads), k and v of the group, as written by the QKV phase
+        const unsigned long long* row = A.fq + (size_t)(a.r * MB + a.b) * A.qkv_rows;
+        const bool ok = poll_space(A, (G + 2) * half, ep, C.abort(),
+            [&](int p) {
+                const int e2 = 2 * p, hr = e2 / d, e = e2 - hr * d;
+                const int src = hr < G ? (a.kh * G + hr) * d + e
+                                       : (hr == G ? (A.hq_s + a.kh) * d + e : (A.hq_s + A.hkv_s + a.kh) * d + e);
+                return dp_off(A, row + src);
+            },
+            [&](int p, float x0, float x1) { *reinterpret_cast<float2*>(st + 2 * p) = make_float2(x0, x1); });
+        cp_wait();
+        if (csync_or(!ok)) return false;
+        if (i == A.att_rank[blockIdx.x]) stamp(A, l, 1, 0);
+        const bool inrange = pb >= 0 && pb < A.max_kv;
+        #pragma unroll 1
+        for (int p = tid; p < (G + 1) * half; p += kCT) {
+            const int hr = p / half, e = p - hr * half;
+            const float x0 = st[hr * d + e], x1 = st[hr * d + e + half];
+            const float cs = inrange ? rot[2 * e] : 1.f, sn = inrange ? rot[2 * e + 1] : 0.f;
+            const float r0 = x0 * cs - x1 * sn, r1 = x0 * sn + x1 * cs;
+            if (hr < G) {                                // q: rotated and scaled, in place
+                st[hr * d + e] = r0 * A.qscale;
+                st[hr * d + e + half] = r1 * A.qscale;
+            } else {
+                C.knew()[e] = __float2bfloat16_rn(r0);
+                C.knew()[e + half] = __float2bfloat16_rn(r1);
+            }
+        }
+        #pragma unroll 1
+        for (int e = tid; e < d; e += kCT) C.vnew()[e] = __float2bfloat16_rn(st[(G + 1) * d + e]);
+        csync();
+        const uint32_t k0 = C.k;
+        C.k += 2;
+        unsigned char* Kt = ring_wait(C.ring(), k0, A.status);
+        unsigned char* Vt = ring_wait(C.ring(), k0 + 1, A.status);
+        if (has_new) {
+            const int kr = pb - a.k0;
+            #pragma unroll 1
+            for (int e2 = tid; e2 < half; e2 += kCT) {     // bf16 pairs of the new row
+                const int e = 2 * e2, line = kr * DC + (e >> 6);
+                const int byte = line * 128 + ((((e & 63) >> 3) ^ (line & 7)) << 4) + (e & 7) * 2;
+                const uint32_t kv = *reinterpret_cast<const uint32_t*>(C.knew() + e);
+                const uint32_t vv = *reinterpret_cast<const uint32_t*>(C.vnew() + e);
+                *reinterpret_cast<uint32_t*>(Kt + byte) = kv;
+                *reinterpret_cast<uint32_t*>(Vt + byte) = vv;
+                const size_t crow = ((size_t)(a.b * A.hkv_s + a.kh) * A.max_kv + pb) * d + e;
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<bf16*>(Ly.kc[a.r]) + crow) = kv;
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<bf16*>(Ly.vc[a.r]) + crow) = vv;
+            }
+            // generic-proxy writes into a slot the next copy (async proxy) will overwrite
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        csync();
+        // scores: tpk threads per key, 32 dimensions each (K row converted once)
+        const int tpk = kCT / A.ck, kpw = 32 / tpk;
+        const int nw = min(kCW, (a.nk + kpw - 1) / kpw);   // warps holding keys
+        float* ps = C.ps();                                  // [key][8 heads]
+        if (warp < nw) {
+            const int key = tid / tpk, part = tid % tpk, e0 = 32 * part;
+            float kf[32];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + 8 * u, line = key * DC + (e >> 6);
+                const uint4 kv = *reinterpret_cast<const uint4*>(Kt + line * 128 + ((((e & 63) >> 3) ^ (line & 7)) << 4));
+                kf[8 * u + 0] = bf_lo(kv.x);
+                kf[8 * u + 1] = bf_hi(kv.x);
+                kf[8 * u + 2] = bf_lo(kv.y);
+                kf[8 * u + 3] = bf_hi(kv.y);
+                kf[8 * u + 4] = bf_lo(kv.z);
+                kf[8 * u + 5] = bf_hi(kv.z);
+                kf[8 * u + 6] = bf_lo(kv.w);
+                kf[8 * u + 7] = bf_hi(kv.w);
+            }
+            #pragma unroll 1
+            for (int h = 0; h < G; ++h) {
+                const float* q = st + h * d + e0;
+                float sc = 0.f;
+#pragma unroll
+                for (int z = 0; z < 32; z += 4) {
+                    const float4 qv = *reinterpret_cast<const float4*>(q + z);
+                    sc = fmaf(qv.x, kf[z], sc);
+                    sc = fmaf(qv.y, kf[z + 1], sc);
+                    sc = fmaf(qv.z, kf[z + 2], sc);
+                    sc = fmaf(qv.w, kf[z + 3], sc);
+                }
+                #pragma unroll 1
+                for (int o = 1; o < tpk; o <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+                if (part == 0) ps[key * 8 + h] = sc;
+            }
+            __syncwarp();
+            // online softmax over the warp's keys, per head
+            const int kbeg = warp * kpw, kend = min(kbeg + kpw, a.nk);
+            #pragma unroll 1
+            for (int h = 0; h < G; ++h) {
+                const bool v = lane < kend - kbeg;
+                const float sv = v ? ps[(kbeg + lane) * 8 + h] : -INFINITY;
+                const float m = warp_max(sv);
+                const float pv = v ? ex2_approx(sv - m) : 0.f;
+                const float lsum = warp_sum(pv);
+                if (v) ps[(kbeg + lane) * 8 + h] = pv;
+                if (lane == 0) {
+                    ml[(warp * 16 + h) * 2] = m;
+                    ml[(warp * 16 + h) * 2 + 1] = lsum;
+                }
+            }
+            __syncwarp();
+            // O_w = P V: lane takes d / 32 dimensions
+            const int dpl = d >> 5, ev = lane * dpl;
+            #pragma unroll 1
+            for (int h = 0; h < G; ++h) {
+                float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+                #pragma unroll 1
+                for (int kk = kbeg; kk < kend; ++kk) {
+                    const int line = kk * DC + (ev >> 6);
+                    const unsigned char* vp = Vt + line * 128 + ((((ev & 63) >> 3) ^ (line & 7)) << 4) + (ev & 7) * 2;
+                    const float pr = ps[kk * 8 + h];
+                    const uint32_t v0 = *reinterpret_cast<const uint32_t*>(vp);
+                    o0 = fmaf(pr, bf_lo(v0), o0);
+                    o1 = fmaf(pr, bf_hi(v0), o1);
+                    if (dpl == 4) {
+                        const uint32_t v1 = *reinterpret_cast<const uint32_t*>(vp + 4);
+                        o2 = fmaf(pr, bf_lo(v1), o2);
+                        o3 = fmaf(pr, bf_hi(v1), o3);
+                    }
+                }
+                float* dst = C.att() + (warp * G + h) * d + ev;
+                if (dpl == 4) *reinterpret_cast<float4*>(dst) = make_float4(o0, o1, o2, o3);
+                else *reinterpret_cast<float2*>(dst) = make_float2(o0, o1);
+            }
+        }
+        ring_release(C.ring(), k0);
+        ring_release(C.ring(), k0 + 1);
+        csync();
+        // merge the warps (fixed order) into the chunk partial: O (unnormalised), then (max, sum) per head
+        const int gi = (a.r * MB + a.b) * A.hkv_s + a.kh;
+        unsigned long long* part = A.fp + ((size_t)gi * A.maxch + a.c) * G * (d + 2);
+        #pragma unroll 1
+        for (int idx = tid; idx < G * d; idx += kCT) {
+            const int j = idx / d, e = idx - j * d;
+            float M = -INFINITY;
+            #pragma unroll 1
+            for (int w = 0; w < nw; ++w) M = fmaxf(M, ml[(w * 16 + j) * 2]);
+            float num = 0.f, den = 0.f;
+            #pragma unroll 1
+            for (int w = 0; w < nw; ++w) {
+                const float f = ex2_approx(ml[(w * 16 + j) * 2] - M);
+                num = fmaf(f, C.att()[(w * G + j) * d + e], num);
+                den = fmaf(f, ml[(w * 16 + j) * 2 + 1], den);
+            }
+            ll_st(part + j * d + e, num, ep);
+            if (e == 0) {
+                ll_st(part + G * d + 2 * j, M, ep);
+                ll_st(part + G * d + 2 * j + 1, den, ep);
+            }
+        }
+        stamp(A, l, 1, 1);
+    }
+    return true;
+}
+
+// o_proj: every CTA with o_proj items combines the split-KV partials of all
+// groups itself (chunks in order: running max, rescaled sums), then each item
+// sums its shards' partial outputs in rank order and adds the residual.
+__device__ __forceinline__ bool phase_o(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
+    const int cnt = C.misc()[kMiCnt + PH_O];
+    if (csync_or(*C.abort())) return false;
+    if (!cnt) return true;
+    const int* items = C.misc() + kMiItems + PH_O * kChainMaxItems;
+    const int tid = threadIdx.x, T = A.T, MB = A.max_batch, G = A.G, d = A.d, hk = A.hkv_s;
+    const int* nch_t = C.misc() + kMiNch;
+    const int nq = A.N * T * hk * G * (d / 4), nres = cnt * T * 4;
+    float* res = C.res();
+    auto res_at = [&](int p, int& t) {                  // residual double pair p: (item, token, column pair)
+        const int it = p / (T * 4), rem = p - it * T * 4;
+        t = rem >> 2;
+        return t * A.H + 8 * items[it] + 2 * (rem & 3);
+    };
+    if (l == 0)                                         // the layer's input is the caller's x
+        #pragma unroll 1
+        for (int p = tid; p < nres; p += kCT) {
+            int t;
+            const int e = res_at(p, t);
+            *reinterpret_cast<float2*>(res + (p / (T * 4) * MB + t) * 8 + 2 * (p & 3)) =
+                *reinterpret_cast<const float2*>(A.x + e);
+        }
+    bool ok = true;
+    const int passes = (max(nq, nres) + kCT - 1) / kCT;
+    #pragma unroll 1
+    for (int pass = 0; pass < passes; ++pass) {
+        const int q = tid + pass * kCT;
+        int r = 0, t = 0, kh = 0, j = 0, e4 = 0, n = 0;
+        if (q < nq) {
+            e4 = q % (d / 4);
+            const int rest = q / (d / 4);
+            j = rest % G;
+            const int rest2 = rest / G;
+            kh = rest2 % hk;
+            const int rt = rest2 / hk;
+            t = rt % T;
+            r = rt / T;
+            n = nch_t[t];
+        }
+        const int gi = (r * MB + t) * hk + kh;
+        const bool rs = pass == 0 && l > 0 && tid < nres;
+        float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
+        int c0 = 0;
+        do {
+            int off[kPoll];
+            unsigned long long v[kPoll][2];
+#pragma unroll
+            for (int u = 0; u < kPoll; ++u) off[u] = -1;
+            const int nb = min(5, n - c0);                 // 3 double pairs per chunk
+#pragma unroll
+            for (int c = 0; c < 5; ++c)
+                if (c < nb) {
+                    const int base = dp_off(A, A.fp + ((size_t)gi * A.maxch + c0 + c) * G * (d + 2));
+                    off[3 * c] = base + (j * d + 4 * e4) / 2;
+                    off[3 * c + 1] = off[3 * c] + 1;
+                    off[3 * c + 2] = base + (G * d + 2 * j) / 2;
+                }
+            int rt = 0;
+            if (rs && c0 == 0) off[kPoll - 1] = dp_off(A, A.fx) + res_at(tid, rt) / 2;
+            ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
+#pragma unroll
+            for (int c = 0; c < 5; ++c)
+                if (c < nb) {
+                    const float mc = ll_val(v[3 * c + 2][0]), Mn = fmaxf(M, mc);
+                    const float fa = ex2_approx(M - Mn), fb = ex2_approx(mc - Mn);
+                    den = fmaf(den, fa, ll_val(v[3 * c + 2][1]) * fb);
+                    num0 = fmaf(num0, fa, ll_val(v[3 * c][0]) * fb);
+                    num1 = fmaf(num1, fa, ll_val(v[3 * c][1]) * fb);
+                    num2 = fmaf(num2, fa, ll_val(v[3 * c + 1][0]) * fb);
+                    num3 = fmaf(num3, fa, ll_val(v[3 * c + 1][1]) * fb);
+                    M = Mn;
+                }
+            if (rs && c0 == 0)
+                *reinterpret_cast<float2*>(res + (tid / (T * 4) * MB + rt) * 8 + 2 * (tid & 3)) =
+                    make_float2(ll_val(v[kPoll - 1][0]), ll_val(v[kPoll - 1][1]));
+            c0 += max(nb, 0);
+        } while (c0 < n && ok);
+        if (q < nq) {
+            const float inv = den > 0.f ? 1.0f / den : 0.f;
+            bf16* dst = C.xa() + (size_t)t * A.xa_stride + r * A.hq_s * d + (kh * G + j) * d + 4 * e4;
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(num0 * inv, num1 * inv);
+            *reinterpret_cast<uint32_t*>(dst + 2) = pack_bf16x2(num2 * inv, num3 * inv);
+        }
+    }
+    if (csync_or(!ok)) return false;
+    stamp(A, l, 2, 0);
+    const int Ko = A.hq_s * d, warp = tid >> 5, lane = tid & 31;
+    #pragma unroll 1
+    for (int n = 0; n < cnt; ++n) {
+        const int i = items[n];
+        float tot = 0.f;
+        #pragma unroll 1
+        for (int r = 0; r < A.N; ++r) {
+            float mine[1] = {0.f};
+            item_rows<1>(C, A, A.nl[1], A.kc[1], Ko / 64, r * Ko, mine);
+            tot = r == 0 ? mine[0] : tot + mine[0];      // ((p0 + p1) + p2) + ...
+        }
+        if (lane < T) ll_st(A.fh + (size_t)lane * A.H + 8 * i + warp, tot + res[(n * MB + lane) * 8 + warp], ep);
+    }
+    stamp(A, l, 2, 1);
+    return true;
+}
+
+// gate/up: RMSNorm statistics of the residual stream, then per item the gate
+// and up rows (two boxes per load), SwiGLU.
+__device__ __forceinline__ bool phase_gu(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
+    const int cnt = C.misc()[kMiCnt + PH_GU];
+    if (csync_or(*C.abort())) return false;
+    if (!cnt) return true;
+    const int* items = C.misc() + kMiItems + PH_GU * kChainMaxItems;
+    const int tid = threadIdx.x, MB = A.max_batch, rbg = A.F_s / 8, warp = tid >> 5, lane = tid & 31;
+    const ChainLayer& Ly = *C.lay();
+    const Gammas gs = pick_gammas(A, Ly.g_ffn, items, cnt, rbg);
+    gammas_fetch(C, A, gs);
+    if (!load_vec(C, A, A.fh, nullptr, ep, gs.g1 != nullptr)) return false;
+    stamp(A, l, 3, 0);
+    const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
+    const float* have0 = gs.g0;
+    #pragma unroll 1
+    for (int n = 0; n < cnt; ++n) {
+        const int it = items[n], r = it / rbg, i = it - r * rbg;
+        const int kb = operand_col(C, A, gs, have0, Ly.g_ffn[r]);
+        float mine[2] = {0.f, 0.f};                         // gate, up
+        item_rows<2>(C, A, A.nl[2], A.kc[2], A.H / 64, kb, mine);
+        if (lane < A.T) {
+            const float gt = mine[0] * rinv[lane], up = mine[1] * rinv[lane];
+            ll_st(A.fa + (size_t)(r * MB + lane) * A.F_s + 8 * i + warp, gt / (1.0f + expf(-gt)) * up, ep);
+        }
+    }
+    stamp(A, l, 3, 1);
+    return true;
+}
+
+// down: the SwiGLU outputs of every shard as the operand, then per item the
+// rank-ordered sum over shards plus the residual: the layer's output.
+__device__ __forceinline__ bool phase_d(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
+    const int cnt = C.misc()[kMiCnt + PH_D];
+    if (csync_or(*C.abort())) return false;
+    if (!cnt) return true;
+    const int* items = C.misc() + kMiItems + PH_D * kChainMaxItems;
+    const int tid = threadIdx.x, T = A.T, MB = A.max_batch, F = A.F_s, warp = tid >> 5, lane = tid & 31;
+    const int n_act = A.N * T * F / 2, nres = cnt * T * 4;
+    float* res = C.res();
+    // the operand (every shard's SwiGLU outputs) and this CTA's residual rows, polled together
+    const bool ok = poll_space(A, n_act + nres, ep, C.abort(),
+        [&](int i) {
+            if (i < n_act) {
+                const int e = 2 * i, rt = e / F, t = rt % T, r = rt / T;
+                return dp_off(A, A.fa + (size_t)(r * MB + t) * F + (e - rt * F));
+            }
+            const int p = i - n_act, it = p / (T * 4), rem = p - it * T * 4;
+            return dp_off(A, A.fh + (size_t)(rem >> 2) * A.H + 8 * items[it] + 2 * (rem & 3));
+        },
+        [&](int i, float x0, float x1) {
+            if (i < n_act) {
+                const int e = 2 * i, rt = e / F, t = rt % T, r = rt / T;
+                *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + r * F + (e - rt * F)) =
+                    pack_bf16x2(x0, x1);
+            } else {
+                const int p = i - n_act, it = p / (T * 4), rem = p - it * T * 4;
+                *reinterpret_cast<float2*>(res + (it * MB + (rem >> 2)) * 8 + 2 * (rem & 3)) = make_float2(x0, x1);
+            }
+        });
+    if (csync_or(!ok)) return false;
+    stamp(A, l, 4, 0);
+    const bool last = l == A.L - 1;
+    #pragma unroll 1
+    for (int n = 0; n < cnt; ++n) {
+        const int i = items[n];
+        float tot = 0.f;
+        #pragma unroll 1
+        for (int r = 0; r < A.N; ++r) {
+            float mine[1] = {0.f};
+            item_rows<1>(C, A, A.nl[3], A.kc[3], F / 64, r * F, mine);
+            tot = r == 0 ? mine[0] : tot + mine[0];
+        }
+        if (lane < T) {
+            const float v = tot + res[(n * MB + lane) * 8 + warp];
+            if (last) A.y[(size_t)lane * A.H + 8 * i + warp] = v;
+            else ll_st(A.fx + (size_t)lane * A.H + 8 * i + warp, v, ep + 1);
+        }
+    }
+    stamp(A, l, 4, 1);
+    return true;
+}
+
+__global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainArgs A) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    Ctx C;
+    C.init(sm, A);
+    const CRing R = C.ring();
+    ChainLayer* lay = reinterpret_cast<ChainLayer*>(sm + A.sm_misc + kLayOff);
+    if (tid == 0) {
+        for (int s = 0; s < A.n_slots; ++s) {
+            mbar_init(&R.full[s], 1);
+            mbar_init(&R.empty[s], kCW);
+        }
+        *R.abort = 0;
+        fence_mbar_init();
+    }
+    // this CTA's items of the projection phases (static tables)
+    int* misc = C.misc();
+    for (int p = 0; p < 4; ++p) {
+        const int* st = A.tab + A.tab_off[p];
+        const int a = st[blockIdx.x], n = st[blockIdx.x + 1] - a;
+        if (tid == 0) misc[kMiCnt + p] = n;
+        for (int i = tid; i < n; i += blockDim.x) misc[kMiItems + p * kChainMaxItems + i] = st[A.grid + 1 + a + i];
+    }
+    // layer 0's pointers
+    for (int i = tid; i < (int)(sizeof(ChainLayer) / 8); i += blockDim.x)
+        reinterpret_cast<unsigned long long*>(&lay[0])[i] = reinterpret_cast<const unsigned long long*>(A.layers)[i];
+    __syncthreads();
+    pdl_trigger();
+    if (warp == kCW) {
+        if ((tid & 31) == 0) chain_producer(A, R, misc);
+        return;
+    }
+    pdl_wait();   // inputs, positions, caches and the launch counter of the preceding kernel
+    const unsigned gen = *reinterpret_cast<volatile unsigned*>(A.gen);
+    if (tid < kTMax) {
+        const int p = tid < A.T ? A.pos[tid] : 0;
+        misc[kMiPos + tid] = p;
+        if (tid < A.T && (p < 0 || p >= A.max_kv)) set_status(A.status, TP_ERR_CAPACITY);
+        int nch = 0, cs;
+        if (tid < A.T) att_split(att_len(A, p), A.ck, nch, cs);
+        misc[kMiNch + tid] = nch;
+    }
+    constexpr int kLayChunks = (int)(sizeof(ChainLayer) / 16);
+    static_assert(sizeof(ChainLayer) % 16 == 0, "layer record copied in 16-byte pieces");
+    for (int l = 0; l < A.L; ++l) {
+        if (l > 0) asm volatile("cp.async.wait_all;" ::: "memory");
+        csync();
+        C.lb = l & 1;
+        if (l + 1 < A.L && tid < kLayChunks) {
+            cp_async16(reinterpret_cast<unsigned char*>(&lay[(l + 1) & 1]) + 16 * tid,
+                       reinterpret_cast<const unsigned char*>(A.layers + l + 1) + 16 * tid);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        const unsigned ep = gen * 256u + (unsigned)l + 1u;
+        if (!phase_qkv(C, A, l, ep) || !phase_att(C, A, l, ep) || !phase_o(C, A, l, ep) ||
+            !phase_gu(C, A, l, ep) || !phase_d(C, A, l, ep))
+            break;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    csync();
+    if (tid == 0) {
+        // the last CTA to finish advances the launch counter (epochs of the next launch)
+        __threadfence();
+        const unsigned old = atomicAdd(A.done, 1u);
+        if (old == (unsigned)A.grid - 1u) {
+            *reinterpret_cast<volatile unsigned*>(A.done) = 0u;
+            __threadfence();
+            atomicAdd(A.gen, 1u);
+        }
+    }
+}
+
+}  // namespace
+
+size_t chain_smem(ChainArgs& a) {
+    const ChainSmem L = chain_layout(a.max_batch, a.H, a.xa_stride, a.d, a.n_slots);
+    a.sm_misc = L.misc;
+    a.sm_xin = L.xin;
+    a.sm_xa = L.xa;
+    a.sm_gam = L.gam;
+    a.sm_att = L.att;
+    a.sm_stage = L.stage;
+    a.sm_qs = L.qs;
+    a.sm_res = L.res;
+    a.sm_ring = L.ring;
+    return (size_t)L.total;
+}
+
+cudaError_t chain_map(const void* W, long K, long rows, int kc, int box_rows, CUtensorMap* out) {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (K % 64 || kc < 1 || kc > 256 || box_rows < 1 || box_rows > 256) return cudaErrorInvalidValue;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&encode),
+                                                         12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || !encode) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    }
+    cuuint64_t gdim[3] = {64u, (cuuint64_t)(K / 64), (cuuint64_t)rows};
+    cuuint64_t gstride[2] = {128u, (cuuint64_t)K * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)kc, (cuuint32_t)box_rows};
+    cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_chain(const ChainArgs& a, size_t smem, cudaStream_t s) {
+    static size_t configured = 0;
+    if (smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(chain_kernel),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(kChainThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    // One CTA per SM, every SM taken: once the preceding kernel's CTAs have
+    // left, the whole grid is resident, which the consumers' polls rely on
+    // (bounded: a grid that could not become resident ends with
+    // TP_ERR_TIMEOUT). Programmatic serialization lets the weight copies start
+    // on SMs the preceding kernel has already left.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ChainArgs A = a;
+    void* args[] = {&A};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(chain_kernel), args);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace tpk

@@ -70,6 +70,11 @@ struct tp_plan_s {
     size_t off_p_xn = 0, off_p_q = 0, off_p_ao = 0, off_p_h = 0, off_p_act = 0, off_p_rope = 0, ws_prefill_end = 0;
     size_t ws_bytes = 0;
     size_t ws_decode_end = 0;           // end of the decode buffers (control words included)
+    // multi-layer decode (tp_stack_decode): control words, then its own pair buffers
+    // at the end of the workspace (no other mode writes them, so no stale epoch matches)
+    size_t off_c_ctrl = 0, off_c_x = 0, off_c_q = 0, off_c_p = 0, off_c_h = 0, off_c_a = 0,
+           off_c_begin = 0, off_c_end = 0;
+    int c_ck = 0, c_maxch = 0;
     // measurement hook (tp_profile_stages)
     cudaEvent_t stage_ev[16] = {};
     int n_stage_ev = 0;
@@ -244,6 +249,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_cnt_gu = take(sizeof(unsigned) * P->g_gu.groups);
         P->off_cnt_down = take(sizeof(unsigned) * P->g_down.groups);
         P->off_step_bar = take(sizeof(unsigned long long));
+        P->off_c_ctrl = take(4 * sizeof(unsigned));   // launch counter, CTAs finished, abort flag
     }
     P->ctrl_bytes = off;
     if (dense) {
@@ -310,6 +316,21 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
     }
     P->ws_bytes = std::max(P->ws_decode_end, std::max(P->ws_moe_end, P->ws_prefill_end));
     if (P->ws_bytes < P->ctrl_bytes) P->ws_bytes = P->ctrl_bytes;
+    if (dense && d->dtype == TP_BF16 && (d->head_dim == 64 || d->head_dim == 128)) {
+        off = P->ws_bytes;
+        const int64_t MB = d->max_batch, hd = d->head_dim, G = d->n_heads / d->n_kv_heads;
+        P->c_ck = (int)(8192 / hd);                              // keys per 16 KB tile of K
+        P->c_maxch = (int)((d->max_kv + P->c_ck - 1) / P->c_ck);
+        const int64_t groups = N * MB * I.hkv_shard;
+        P->off_c_begin = off;
+        P->off_c_x = take((size_t)MB * H * 8);
+        P->off_c_q = take((size_t)N * MB * I.qkv_rows * 8);
+        P->off_c_p = take((size_t)groups * P->c_maxch * G * (hd + 2) * 8);
+        P->off_c_h = take((size_t)MB * H * 8);
+        P->off_c_a = take((size_t)N * MB * I.ffn_shard * 8);
+        P->off_c_end = off;
+        P->ws_bytes = off;
+    }
     I.workspace_bytes = (int64_t)P->ws_bytes;
     *out = P;
     return ok();
@@ -583,6 +604,10 @@ extern "C" tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t b
     if (st) return st;
     TP_CUDA(cudaMemsetAsync(workspace, 0, plan->ctrl_bytes, static_cast<cudaStream_t>(stream)),
             "tp_workspace_init: memset");
+    if (plan->off_c_end > plan->off_c_begin)   // pair buffers: epoch 0 is never current
+        TP_CUDA(cudaMemsetAsync(static_cast<char*>(workspace) + plan->off_c_begin, 0,
+                                plan->off_c_end - plan->off_c_begin, static_cast<cudaStream_t>(stream)),
+                "tp_workspace_init: memset");
     return ok();
 }
 
@@ -1239,4 +1264,250 @@ extern "C" tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set
     // the array keeps the previous call's contents: counters and status start at zero
     TP_CUDA(cudaMemsetAsync(scratch, 0, plan->ctrl_bytes, s), "tp_block_forward_noalloc: clearing counters");
     return forward_decode(plan, w, kv, x, y, pos, B, static_cast<char*>(scratch), s);
+}
+
+// ---------------------------------------------------------------- several decode blocks in one launch
+
+struct tp_stack_s {
+    tp_plan_t plan = nullptr;
+    int L = 0;
+    void* dev = nullptr;         // tensor maps, layer records, item tables (device memory)
+    tpk::ChainArgs a{};          // per-call fields filled by tp_stack_decode
+    size_t smem = 0;
+};
+
+namespace {
+
+// Chunks of 64 columns per box (odd, at most kmax) and loads per item for a
+// reduction of nch chunks.
+void chain_split(int nch, int kmax, int& kc, int& nl) {
+    const int n = (nch + kmax - 1) / kmax;
+    kc = (nch + n - 1) / n;
+    if (!(kc & 1)) ++kc;
+    nl = (nch + kc - 1) / kc;
+}
+
+}  // namespace
+
+extern "C" tp_status tp_stack_create(tp_plan_t plan, int32_t n_layers, const tp_shard_set* w, const tp_kv_set* kv,
+                                     tp_stack_t* out) {
+    using namespace tpk;
+    if (!plan || !w || !kv || !out) return fail(TP_ERR_NULL, "tp_stack_create: NULL argument");
+    *out = nullptr;
+    const tp_model_desc& d = plan->d;
+    const tp_plan_info& I = plan->info;
+    if (!plan->dense) return fail(TP_ERR_INVALID_ARG, "tp_stack_create: the plan has no attention block");
+    if (d.dtype != TP_BF16) return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: bf16 plans only");
+    if (plan->off_c_end <= plan->off_c_begin || plan->c_ck <= 0)
+        return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: head_dim must be 64 or 128");
+    if (n_layers < 1 || n_layers > 255) return fail(TP_ERR_INVALID_ARG, "tp_stack_create: n_layers %d outside 1..255", n_layers);
+    const int N = plan->N, H = (int)d.hidden, hd = (int)d.head_dim, G = (int)(d.n_heads / d.n_kv_heads);
+    const int MB = (int)d.max_batch, hq_s = (int)I.hq_shard, hkv_s = (int)I.hkv_shard, F_s = (int)I.ffn_shard;
+    const int qkv_rows = (int)I.qkv_rows;
+    if (G > 8) return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: at most 8 query heads per KV head (got %d)", G);
+    if (MB > kTMax) return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: max_batch above %d", kTMax);
+    const long groups = (long)N * MB * hkv_s;
+    for (int l = 0; l < n_layers; ++l)
+        for (int r = 0; r < N; ++r) {
+            const tp_shard_set& s = w[l];
+            if (!s.wqkv[r] || !s.wo[r] || !s.wgu[r] || !s.wd[r] || !s.gamma_attn[r] || !s.gamma_ffn[r] ||
+                !kv[l].k[r] || !kv[l].v[r])
+                return fail(TP_ERR_NULL, "tp_stack_create: layer %d shard %d pointer is NULL", l, r);
+            if (d.has_qkv_bias && !s.bqkv[r]) return fail(TP_ERR_NULL, "tp_stack_create: layer %d shard %d bias is NULL", l, r);
+            const void* al[] = {s.wqkv[r], s.wo[r], s.wgu[r], s.wd[r], s.gamma_attn[r], s.gamma_ffn[r], kv[l].k[r],
+                                kv[l].v[r]};
+            for (const void* p : al)
+                if (!aligned16(p)) return fail(TP_ERR_ALIGN, "tp_stack_create: layer %d shard %d pointer not 16-byte aligned", l, r);
+        }
+    tp_status st = check_device();
+    if (st) return st;
+    int dev = 0, sms = 0, smem_max = 0;
+    TP_CUDA(cudaGetDevice(&dev), "tp_stack_create: cudaGetDevice");
+    TP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "tp_stack_create: SM count");
+    TP_CUDA(cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "tp_stack_create: smem");
+    const int grid = std::min(sms, kChainMaxCtas);
+
+    ChainArgs A{};
+    A.H = H;
+    A.N = N;
+    A.hq_s = hq_s;
+    A.hkv_s = hkv_s;
+    A.d = hd;
+    A.G = G;
+    A.qkv_rows = qkv_rows;
+    A.F_s = F_s;
+    A.max_batch = MB;
+    A.max_kv = (int)d.max_kv;
+    A.L = n_layers;
+    A.grid = grid;
+    A.ck = plan->c_ck;
+    A.maxch = plan->c_maxch;
+    A.eps = (float)d.eps;
+    A.log2_theta = (float)std::log2(d.rope_theta);
+    A.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
+    chain_split(H / 64, 15, A.kc[0], A.nl[0]);
+    chain_split(hq_s * hd / 64, 15, A.kc[1], A.nl[1]);
+    chain_split(H / 64, 7, A.kc[2], A.nl[2]);
+    chain_split(F_s / 64, 15, A.kc[3], A.nl[3]);
+    A.xa_stride = std::max(H, std::max(N * hq_s * hd, N * F_s)) + 8;
+    size_t smem = 0;
+    for (A.n_slots = kChainMaxSlots; A.n_slots >= 4; --A.n_slots) {
+        smem = chain_smem(A);
+        if (smem <= (size_t)smem_max) break;
+    }
+    if (A.n_slots < 4)
+        return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: operands of this shape leave no room for the weight ring");
+
+    // ---- items of the projection phases, bytes balanced over the CTAs (largest first)
+    struct Item { long bytes; int phase, id; };
+    std::vector<Item> items;
+    const int nph[4] = {N * qkv_rows / 8, H / 8, N * F_s / 8, H / 8};
+    const long bph[4] = {16L * H, 16L * N * hq_s * hd, 32L * H, 16L * N * F_s};
+    // o_proj and down items: one residual double pair per consumer thread (items x tokens x 4 <= 256)
+    const int cap[4] = {kChainMaxItems, std::min(kChainMaxItems, 64 / MB), kChainMaxItems,
+                        std::min(kChainMaxItems, 64 / MB)};
+    for (int p = 0; p < 4; ++p) {
+        if (nph[p] > (long)grid * cap[p])
+            return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: %d items of phase %d exceed %d CTAs x %d", nph[p], p, grid,
+                        cap[p]);
+        for (int i = 0; i < nph[p]; ++i) items.push_back({bph[p], p, i});
+    }
+    std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) { return x.bytes > y.bytes; });
+    std::vector<long> load(grid, 0);
+    std::vector<std::vector<int>> own(4 * (size_t)grid);
+    for (const Item& it : items) {
+        int best = -1;
+        for (int c = 0; c < grid; ++c)
+            if ((int)own[(size_t)it.phase * grid + c].size() < cap[it.phase] && (best < 0 || load[c] < load[best]))
+                best = c;
+        own[(size_t)it.phase * grid + best].push_back(it.id);
+        load[best] += it.bytes;
+    }
+    for (auto& v : own) std::sort(v.begin(), v.end());   // shard-major: one normalised operand per shard run
+    std::vector<int> tab;
+    for (int p = 0; p < 4; ++p) {
+        A.tab_off[p] = (int)tab.size();
+        int acc = 0;
+        for (int c = 0; c < grid; ++c) {
+            tab.push_back(acc);
+            acc += (int)own[(size_t)p * grid + c].size();
+        }
+        tab.push_back(acc);
+        for (int c = 0; c < grid; ++c)
+            for (int id : own[(size_t)p * grid + c]) tab.push_back(id);
+    }
+    // attention items go round robin over the CTAs, least loaded first
+    std::vector<int> order(grid);
+    for (int c = 0; c < grid; ++c) order[c] = c;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return load[x] < load[y]; });
+    std::vector<int> rank(grid);
+    for (int i = 0; i < grid; ++i) rank[order[i]] = i;
+
+    // ---- device buffer: maps [L][6][N], layer records [L], tables, ranks
+    const size_t n_maps = (size_t)n_layers * kChainMaps * N;
+    const size_t off_lay = n_maps * sizeof(CUtensorMap);
+    const size_t off_tab = off_lay + (size_t)n_layers * sizeof(ChainLayer);
+    const size_t off_rank = off_tab + tab.size() * sizeof(int);
+    const size_t off_rope = (off_rank + (size_t)grid * sizeof(int) + 15) & ~(size_t)15;
+    const size_t bytes = off_rope + (size_t)d.max_kv * (hd / 2) * 2 * sizeof(float);
+    std::vector<unsigned char> host(bytes, 0);
+    CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(host.data());
+    ChainLayer* lays = reinterpret_cast<ChainLayer*>(host.data() + off_lay);
+    const long kv_rows = (long)MB * hkv_s * d.max_kv;
+    for (int l = 0; l < n_layers; ++l) {
+        for (int r = 0; r < N; ++r) {
+            CUtensorMap* m = maps + (size_t)l * kChainMaps * N;
+            cudaError_t e = chain_map(w[l].wqkv[r], H, qkv_rows, A.kc[0], 8, &m[0 * N + r]);
+            if (e == cudaSuccess) e = chain_map(w[l].wo[r], (long)hq_s * hd, H, A.kc[1], 8, &m[1 * N + r]);
+            if (e == cudaSuccess) e = chain_map(w[l].wgu[r], H, 2L * F_s, A.kc[2], 8, &m[2 * N + r]);
+            if (e == cudaSuccess) e = chain_map(w[l].wd[r], F_s, H, A.kc[3], 8, &m[3 * N + r]);
+            if (e == cudaSuccess) e = chain_map(kv[l].k[r], hd, kv_rows, hd / 64, A.ck, &m[4 * N + r]);
+            if (e == cudaSuccess) e = chain_map(kv[l].v[r], hd, kv_rows, hd / 64, A.ck, &m[5 * N + r]);
+            if (e != cudaSuccess) return cuda_fail(e, "tp_stack_create: tensor map");
+            lays[l].bqkv[r] = d.has_qkv_bias ? w[l].bqkv[r] : nullptr;
+            lays[l].g_attn[r] = w[l].gamma_attn[r];
+            lays[l].g_ffn[r] = w[l].gamma_ffn[r];
+            lays[l].kc[r] = kv[l].k[r];
+            lays[l].vc[r] = kv[l].v[r];
+        }
+    }
+    memcpy(host.data() + off_tab, tab.data(), tab.size() * sizeof(int));
+    memcpy(host.data() + off_rank, rank.data(), (size_t)grid * sizeof(int));
+    // rotary table: angle pos * theta^(-2e/d) for pair e, in double, rounded once
+    float* rope = reinterpret_cast<float*>(host.data() + off_rope);
+    for (long p = 0; p < d.max_kv; ++p)
+        for (int e = 0; e < hd / 2; ++e) {
+            const double ang = (double)p * std::pow(d.rope_theta, -2.0 * e / hd);
+            rope[(p * (hd / 2) + e) * 2] = (float)std::cos(ang);
+            rope[(p * (hd / 2) + e) * 2 + 1] = (float)std::sin(ang);
+        }
+    tp_stack_s* S = new (std::nothrow) tp_stack_s();
+    if (!S) return fail(TP_ERR_INVALID_ARG, "tp_stack_create: out of host memory");
+    cudaError_t e = cudaMalloc(&S->dev, bytes);
+    if (e == cudaSuccess) e = cudaMemcpy(S->dev, host.data(), bytes, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        if (S->dev) cudaFree(S->dev);
+        delete S;
+        return cuda_fail(e, "tp_stack_create: device tables");
+    }
+    unsigned char* db = static_cast<unsigned char*>(S->dev);
+    A.maps = reinterpret_cast<const CUtensorMap*>(db);
+    A.layers = reinterpret_cast<const ChainLayer*>(db + off_lay);
+    A.tab = reinterpret_cast<const int*>(db + off_tab);
+    A.att_rank = reinterpret_cast<const int*>(db + off_rank);
+    A.rope = reinterpret_cast<const float2*>(db + off_rope);
+    S->plan = plan;
+    S->L = n_layers;
+    S->a = A;
+    S->smem = smem;
+    *out = S;
+    return ok();
+}
+
+extern "C" tp_status tp_stack_set_stamps(tp_stack_t stack, uint64_t* stamps, int32_t rows) {
+    if (!stack) return fail(TP_ERR_NULL, "tp_stack_set_stamps: NULL stack");
+    if (stamps && rows < stack->a.grid)
+        return fail(TP_ERR_SHAPE, "tp_stack_set_stamps: %d rows < %d CTAs", rows, stack->a.grid);
+    stack->a.stamps = reinterpret_cast<unsigned long long*>(stamps);
+    return ok();
+}
+
+extern "C" int32_t tp_stack_ctas(tp_stack_t stack) { return stack ? stack->a.grid : 0; }
+
+extern "C" void tp_stack_destroy(tp_stack_t stack) {
+    if (!stack) return;
+    if (stack->dev) cudaFree(stack->dev);
+    delete stack;
+}
+
+extern "C" tp_status tp_stack_decode(tp_stack_t stack, const float* x, float* y, const int32_t* pos, int32_t B,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (!stack || !x || !y || !pos || !workspace) return fail(TP_ERR_NULL, "tp_stack_decode: NULL argument");
+    tp_plan_t P = stack->plan;
+    if (x == y) return fail(TP_ERR_INVALID_ARG, "tp_stack_decode: y must not alias x");
+    if (B < 1 || B > P->d.max_batch || B > tpk::kTMax)
+        return fail(TP_ERR_SHAPE, "tp_stack_decode: B=%d outside 1..min(max_batch, %d)", B, tpk::kTMax);
+    if (workspace_bytes < P->ws_bytes)
+        return fail(TP_ERR_CAPACITY, "tp_stack_decode: workspace %zu bytes < required %zu", workspace_bytes, P->ws_bytes);
+    if (!aligned16(workspace) || !aligned16(x) || !aligned16(y))
+        return fail(TP_ERR_ALIGN, "tp_stack_decode: x, y and workspace must be 16-byte aligned");
+    char* ws = static_cast<char*>(workspace);
+    tpk::ChainArgs A = stack->a;
+    A.T = B;
+    A.x = x;
+    A.y = y;
+    A.pos = pos;
+    A.cbase = reinterpret_cast<const unsigned long long*>(ws + P->off_c_begin);
+    A.fx = reinterpret_cast<unsigned long long*>(ws + P->off_c_x);
+    A.fq = reinterpret_cast<unsigned long long*>(ws + P->off_c_q);
+    A.fp = reinterpret_cast<unsigned long long*>(ws + P->off_c_p);
+    A.fh = reinterpret_cast<unsigned long long*>(ws + P->off_c_h);
+    A.fa = reinterpret_cast<unsigned long long*>(ws + P->off_c_a);
+    unsigned* cw = reinterpret_cast<unsigned*>(ws + P->off_c_ctrl);
+    A.gen = cw;
+    A.done = cw + 1;
+    A.gabort = reinterpret_cast<int*>(cw + 2);
+    A.status = reinterpret_cast<int*>(ws + P->off_status);
+    TP_CUDA(tpk::launch_chain(A, stack->smem, static_cast<cudaStream_t>(stream)), "tp_stack_decode: launch");
+    return ok();
 }

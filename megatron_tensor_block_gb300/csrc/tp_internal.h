@@ -227,6 +227,63 @@ inline int step_min_keys(int max_kv) {
 }
 constexpr int kStepStamps = 13;          // per CTA: start, then per phase: streaming done, arrival (or end)
 
+// Several decode blocks in one persistent launch: every CTA streams its own
+// weight and KV tiles for all layers through a ring of 16 KB slots, and the
+// activations between phases travel as (value, epoch) pairs so a consumer
+// polls the data itself instead of a grid barrier.
+constexpr int kChainThreads = 288;       // eight consumer warps + one producer warp
+constexpr int kChainSlot = 16384;        // bytes per ring slot
+constexpr int kChainMaxSlots = 12;
+constexpr int kChainMaxItems = 40;       // items of one projection phase per CTA
+constexpr int kChainMaxCtas = 160;
+constexpr int kChainMaps = 6;            // per layer and shard: wqkv, wo, wgu, wd, K cache, V cache
+struct ChainLayer {
+    const float* bqkv[TP_MAX_SHARDS];    // QKV bias or null
+    const float* g_attn[TP_MAX_SHARDS];
+    const float* g_ffn[TP_MAX_SHARDS];
+    void* kc[TP_MAX_SHARDS];             // [max_batch][hkv_s][max_kv][d] bf16
+    void* vc[TP_MAX_SHARDS];
+};
+struct ChainArgs {
+    int H, N, hq_s, hkv_s, d, G, qkv_rows, F_s, T, max_batch, max_kv, L, grid;
+    int ck;                              // keys per attention tile (16 KB of K)
+    int n_slots;
+    int kc[4];                           // chunks of 64 columns per box: qkv, o, gate/up (each half), down
+    int nl[4];                           // loads per 8-row item and shard: qkv, o, gate/up, down
+    float eps, log2_theta, qscale;       // qscale = log2(e) / sqrt(d)
+    const CUtensorMap* maps;             // [L][kChainMaps][N], 64-byte aligned, device memory
+    const ChainLayer* layers;            // [L], device memory
+    const int* tab;                      // per projection phase p: starts [grid + 1] at tab_off[p], items after
+    int tab_off[4];
+    const int* att_rank;                 // [grid]: the CTA's place in the attention round robin
+    const float* x;                      // [T][H] input of layer 0
+    float* y;                            // [T][H] output of the last layer
+    const int* pos;                      // [T]
+    const float2* rope;                  // [max_kv][d/2]: (cos, sin) of pos * theta^(-2e/d)
+    const unsigned long long* cbase;     // start of the pair buffers (polling offsets are relative to it)
+    unsigned long long* fx;              // [max_batch][H] layer inputs (layers 1..)
+    unsigned long long* fq;              // [N][max_batch][qkv_rows] projections before rotation
+    unsigned long long* fp;              // [N * max_batch * hkv_s][maxch][G (d + 2)] attention partials:
+                                         // output [G][d] (unnormalised), then (max, sum) per head
+    unsigned long long* fh;              // [max_batch][H] residual stream after attention
+    unsigned long long* fa;              // [N][max_batch][F_s] SwiGLU outputs
+    int maxch;
+    unsigned* gen;                       // launch counter (epochs) and CTAs finished
+    unsigned* done;
+    int* gabort;
+    int* status;
+    unsigned long long* stamps;          // optional [grid][L][5 phases][inputs arrived, outputs stored] (ns)
+    int xa_stride;                       // bf16 elements per token row of the operand buffer
+    int sm_misc, sm_xin, sm_xa, sm_gam, sm_att, sm_stage, sm_qs, sm_res, sm_ring;   // shared-memory offsets
+};
+// Fills the shared-memory offsets of `a` (max_batch, H, xa_stride, d, n_slots
+// set) and returns the dynamic shared-memory bytes of a launch.
+size_t chain_smem(ChainArgs& a);
+cudaError_t launch_chain(const ChainArgs& a, size_t smem, cudaStream_t s);
+// 3-D bf16 map over a [rows][K] matrix viewed as [rows][K/64][64], boxes of
+// {64, kc, box_rows}, 128-byte swizzled, written to `out` (any memory).
+cudaError_t chain_map(const void* W, long K, long rows, int kc, int box_rows, CUtensorMap* out);
+
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)

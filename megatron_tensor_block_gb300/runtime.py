@@ -155,6 +155,20 @@ class Model:
     def mode(self) -> int:
         return {"decode": B.TP_MODE_DECODE, "prefill": B.TP_MODE_PREFILL, "moe_ffn": B.TP_MODE_MOE_FFN}[self.w.mode]
 
+    def stack(self):
+        """The decode layers as one ``tp_stack_t`` (created on first use)."""
+        if getattr(self, "_stack", None) is None:
+            self._stack = B.tp_stack_create(self.plan, [L.shards for L in self.layers],
+                                            [(c.k, c.v) for c in self.caches])
+        return self._stack
+
+    def forward_stack(self, x=None, y=None, stream=None):
+        """Decode through every layer in one launch (``tp_stack_decode``)."""
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        B.tp_stack_decode(self.stack(), x, y, self.pos, self.w.batch, self.ws.buf, self.ws.nbytes, stream)
+        return y
+
     def forward(self, x=None, y=None, stream=None):
         """Runs every layer; returns the output tensor."""
         x = self.x if x is None else x
