@@ -129,7 +129,7 @@ __device__ __forceinline__ void ring_release(const CRing& R, uint32_t k) {
 // (16 bytes: two pairs) per thread in registers, at double-pair offsets
 // off[u] from base (off < 0: none), the missing ones reloaded each round
 // until every pair carries epoch ep.
-constexpr int kPoll = 16;
+constexpr int kPoll = 8;
 template <int NB>
 __device__ __forceinline__ bool ll_wait2(const unsigned long long* base, const int (&off)[NB],
                                          unsigned long long (&v)[NB][2], unsigned ep, const ChainArgs& A,
@@ -207,7 +207,7 @@ __device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float s) {
 __device__ __forceinline__ float row_dot(const unsigned char* w, int kc, int nvalid, const bf16* xrow) {
     const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float s = 0.f;
-#pragma unroll 2
+#pragma unroll 4
     for (int u = lane; u < 8 * nvalid; u += 32) {
         const int ch = u >> 3, u8 = u & 7, line = row * kc + ch;
         const uint4 wv = *reinterpret_cast<const uint4*>(w + line * 128 + ((u8 ^ (line & 7)) << 4));
@@ -217,13 +217,34 @@ __device__ __forceinline__ float row_dot(const unsigned char* w, int kc, int nva
     return s;
 }
 
+// the same for two boxes half a slot apart (gate and up rows), sharing the operand loads
+__device__ __forceinline__ void row_dot2(const unsigned char* w, int kc, int nvalid, const bf16* xrow, float& s0,
+                                         float& s1) {
+    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll 4
+    for (int u = lane; u < 8 * nvalid; u += 32) {
+        const int ch = u >> 3, u8 = u & 7, line = row * kc + ch;
+        const int off = line * 128 + ((u8 ^ (line & 7)) << 4);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 64 * ch + 8 * u8);
+        s0 = dot8(*reinterpret_cast<const uint4*>(w + off), xv, s0);
+        s1 = dot8(*reinterpret_cast<const uint4*>(w + kChainSlot / 2 + off), xv, s1);
+    }
+}
+
+__device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
 // ---- shared memory ---------------------------------------------------------------------
 
 struct ChainSmem {
     int ctrl, misc, xin, xa, gam, att, stage, qs, res, ring, total;
 };
 constexpr int kMiscBytes = 4096;
-constexpr int kPsBytes = kCW * 16 * 8 * 4;      // attention probabilities [128 keys][8 heads]
+constexpr int kPsBytes = 16 * (128 + 8) * 2;    // attention query tile [16 rows][d + 8] bf16
 constexpr int kStageFloats = 11 * 128;      // q (G <= 8 heads), new k, new v of one group, rotation
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
 __host__ __device__ inline ChainSmem chain_layout(int MB, int H, int xs, int d, int ns) {
@@ -443,7 +464,7 @@ struct Ctx {
     __device__ __forceinline__ float* gam() const { return reinterpret_cast<float*>(sm + o_gam); }
     __device__ __forceinline__ float* att() const { return reinterpret_cast<float*>(sm + o_att); }
     __device__ __forceinline__ float* stage() const { return reinterpret_cast<float*>(sm + o_stage); }
-    __device__ __forceinline__ float* ps() const { return reinterpret_cast<float*>(sm + o_qs); }
+    __device__ __forceinline__ bf16* qs() const { return reinterpret_cast<bf16*>(sm + o_qs); }
     __device__ __forceinline__ bf16* knew() const { return reinterpret_cast<bf16*>(sm + o_qs + kPsBytes); }
     __device__ __forceinline__ bf16* vnew() const { return knew() + d; }
     __device__ __forceinline__ float* res() const { return reinterpret_cast<float*>(sm + o_res); }
@@ -518,24 +539,33 @@ __device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsig
     }
     cp_wait();
     if (csync_or(!ok)) return false;
+    // operand copies and per-token sums of squares with every thread; the
+    // warps' partial sums meet in shared memory
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* gm = C.gam();
+    float* part = C.att();                                // [token][warp] partial sums
     #pragma unroll 1
-    for (int t = warp; t < T; t += kCW) {
+    for (int t = 0; t < T; ++t) {
+        float sq = 0.f;
+        #pragma unroll 1
+        for (int k2 = threadIdx.x; k2 < H / 2; k2 += kCT) {
+            const int kk = 2 * k2;
+            const float2 xv = *reinterpret_cast<const float2*>(xin + t * H + kk);
+            sq = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, sq));
+            bf16* xr = C.xa() + (size_t)t * A.xa_stride + kk;
+            *reinterpret_cast<uint32_t*>(xr) = pack_bf16x2(xv.x * gm[kk], xv.y * gm[kk + 1]);
+            if (two) *reinterpret_cast<uint32_t*>(xr + H) = pack_bf16x2(xv.x * gm[H + kk], xv.y * gm[H + kk + 1]);
+        }
+        sq = warp_sum(sq);
+        if (lane == 0) part[t * kCW + warp] = sq;
+    }
+    csync();
+    if (threadIdx.x < T) {
         float a = 0.f;
         #pragma unroll 1
-        for (int kk = lane; kk < H; kk += 32) a = fmaf(xin[t * H + kk], xin[t * H + kk], a);
-        a = warp_sum(a);
-        if (lane == 0) reinterpret_cast<float*>(C.misc())[kMiRinv + t] = 1.0f / sqrtf(a * (1.0f / (float)H) + A.eps);
+        for (int w = 0; w < kCW; ++w) a += part[threadIdx.x * kCW + w];
+        reinterpret_cast<float*>(C.misc())[kMiRinv + threadIdx.x] = 1.0f / sqrtf(a * (1.0f / (float)H) + A.eps);
     }
-    const float* gm = C.gam();
-    #pragma unroll 1
-    for (int c = 0; c < (two ? 2 : 1); ++c)
-        #pragma unroll 1
-        for (int i = threadIdx.x; i < n2; i += kCT) {
-            const int e = 2 * i, t = e / H, kk = e - t * H;
-            *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + c * H + kk) =
-                pack_bf16x2(xin[e] * gm[c * H + kk], xin[e + 1] * gm[c * H + kk + 1]);
-        }
     csync();
     return true;
 }
@@ -568,11 +598,23 @@ __device__ __forceinline__ void item_rows(Ctx& C, const ChainArgs& A, int nl, in
         #pragma unroll 1
         for (int t = 0; t < A.T; ++t) {
             const bf16* xr = C.xa() + (size_t)t * A.xa_stride + kbase + j * kc * 64;
+            if (NBOX == 1) {
+                const float sv = warp_sum(row_dot(w, kc, nv, xr));
+                if (lane == t) mine[0] += sv;
+            } else {
+                float s0 = 0.f, s1 = 0.f;
+                row_dot2(w, kc, nv, xr, s0, s1);
 #pragma unroll
-            for (int b = 0; b < NBOX; ++b) {
-                const float sv = warp_sum(row_dot(w + b * (kChainSlot / 2), kc, nv, xr));
-                if (lane == t) mine[b] += sv;
+                for (int o = 16; o > 0; o >>= 1) {          // the two sums side by side
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                }
+                if (lane == t) {
+                    mine[0] += s0;
+                    mine[NBOX - 1] += s1;
+                }
             }
+
         }
         ring_release(C.ring(), C.k);
         ++C.k;
@@ -670,9 +712,9 @@ __device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, uns
             const float x0 = st[hr * d + e], x1 = st[hr * d + e + half];
             const float cs = inrange ? rot[2 * e] : 1.f, sn = inrange ? rot[2 * e + 1] : 0.f;
             const float r0 = x0 * cs - x1 * sn, r1 = x0 * sn + x1 * cs;
-            if (hr < G) {                                // q: rotated and scaled, in place
-                st[hr * d + e] = r0 * A.qscale;
-                st[hr * d + e + half] = r1 * A.qscale;
+            if (hr < G) {                                // q: rotated and scaled, bf16 tile rows 0..G-1
+                C.qs()[hr * (d + 8) + e] = __float2bfloat16_rn(r0 * A.qscale);
+                C.qs()[hr * (d + 8) + e + half] = __float2bfloat16_rn(r1 * A.qscale);
             } else {
                 C.knew()[e] = __float2bfloat16_rn(r0);
                 C.knew()[e + half] = __float2bfloat16_rn(r1);
@@ -703,81 +745,58 @@ __device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, uns
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         csync();
-        // scores: tpk threads per key, 32 dimensions each (K row converted once)
-        const int tpk = kCT / A.ck, kpw = 32 / tpk;
-        const int nw = min(kCW, (a.nk + kpw - 1) / kpw);   // warps holding keys
-        float* ps = C.ps();                                  // [key][8 heads]
+        // tensor cores: warp w takes keys 16w..16w+15 of the tile. S = q K^T
+        // (q rows = heads, 16 with zero rows >= G), masked online softmax per
+        // head row, O = P V with V read transposed by ldmatrix.
+        const int nw = min(A.ck / 16, (a.nk + 15) / 16);   // warps holding keys
         if (warp < nw) {
-            const int key = tid / tpk, part = tid % tpk, e0 = 32 * part;
-            float kf[32];
+            const int g = lane >> 2, t = lane & 3, qst = d + 8;
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+            const bf16* qr = C.qs() + g * qst + 2 * t;
+            #pragma unroll 1
+            for (int kk = 0; kk < d / 16; ++kk) {
+                const uint32_t a0 = lds32(qr + 16 * kk), a2 = lds32(qr + 16 * kk + 8);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = e0 + 8 * u, line = key * DC + (e >> 6);
-                const uint4 kv = *reinterpret_cast<const uint4*>(Kt + line * 128 + ((((e & 63) >> 3) ^ (line & 7)) << 4));
-                kf[8 * u + 0] = bf_lo(kv.x);
-                kf[8 * u + 1] = bf_hi(kv.x);
-                kf[8 * u + 2] = bf_lo(kv.y);
-                kf[8 * u + 3] = bf_hi(kv.y);
-                kf[8 * u + 4] = bf_lo(kv.z);
-                kf[8 * u + 5] = bf_hi(kv.z);
-                kf[8 * u + 6] = bf_lo(kv.w);
-                kf[8 * u + 7] = bf_hi(kv.w);
-            }
-            #pragma unroll 1
-            for (int h = 0; h < G; ++h) {
-                const float* q = st + h * d + e0;
-                float sc = 0.f;
-#pragma unroll
-                for (int z = 0; z < 32; z += 4) {
-                    const float4 qv = *reinterpret_cast<const float4*>(q + z);
-                    sc = fmaf(qv.x, kf[z], sc);
-                    sc = fmaf(qv.y, kf[z + 1], sc);
-                    sc = fmaf(qv.z, kf[z + 2], sc);
-                    sc = fmaf(qv.w, kf[z + 3], sc);
-                }
-                #pragma unroll 1
-                for (int o = 1; o < tpk; o <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
-                if (part == 0) ps[key * 8 + h] = sc;
-            }
-            __syncwarp();
-            // online softmax over the warp's keys, per head
-            const int kbeg = warp * kpw, kend = min(kbeg + kpw, a.nk);
-            #pragma unroll 1
-            for (int h = 0; h < G; ++h) {
-                const bool v = lane < kend - kbeg;
-                const float sv = v ? ps[(kbeg + lane) * 8 + h] : -INFINITY;
-                const float m = warp_max(sv);
-                const float pv = v ? ex2_approx(sv - m) : 0.f;
-                const float lsum = warp_sum(pv);
-                if (v) ps[(kbeg + lane) * 8 + h] = pv;
-                if (lane == 0) {
-                    ml[(warp * 16 + h) * 2] = m;
-                    ml[(warp * 16 + h) * 2 + 1] = lsum;
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int key = 16 * warp + 8 * nt + g, line = key * DC + (kk >> 2);
+                    const unsigned char* ln = Kt + line * 128 + 4 * t;
+                    const uint32_t b0 = lds32(ln + (((2 * (kk & 3)) ^ (line & 7)) << 4));
+                    const uint32_t b1 = lds32(ln + (((2 * (kk & 3) + 1) ^ (line & 7)) << 4));
+                    mma_bf16_16816(nt ? s1 : s0, a0, 0u, a2, 0u, b0, b1);
                 }
             }
-            __syncwarp();
-            // O_w = P V: lane takes d / 32 dimensions
-            const int dpl = d >> 5, ev = lane * dpl;
+            const int kb = 16 * warp + 2 * t;
+            const bool v00 = kb < a.nk, v01 = kb + 1 < a.nk, v10 = kb + 8 < a.nk, v11 = kb + 9 < a.nk;
+            float mx = fmaxf(fmaxf(v00 ? s0[0] : -INFINITY, v01 ? s0[1] : -INFINITY),
+                             fmaxf(v10 ? s1[0] : -INFINITY, v11 ? s1[1] : -INFINITY));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float p00 = v00 ? ex2_approx(s0[0] - mx) : 0.f, p01 = v01 ? ex2_approx(s0[1] - mx) : 0.f;
+            const float p10 = v10 ? ex2_approx(s1[0] - mx) : 0.f, p11 = v11 ? ex2_approx(s1[1] - mx) : 0.f;
+            float lsum = (p00 + p01) + (p10 + p11);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+            const uint32_t pa0 = pack_bf16x2(p00, p01), pa2 = pack_bf16x2(p10, p11);
+            const uint32_t vbase = smem_u32(Vt);
+            const int mi = lane >> 3, rr = lane & 7;
+            const int vkey = 16 * warp + (mi & 1) * 8 + rr;
             #pragma unroll 1
-            for (int h = 0; h < G; ++h) {
-                float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-                #pragma unroll 1
-                for (int kk = kbeg; kk < kend; ++kk) {
-                    const int line = kk * DC + (ev >> 6);
-                    const unsigned char* vp = Vt + line * 128 + ((((ev & 63) >> 3) ^ (line & 7)) << 4) + (ev & 7) * 2;
-                    const float pr = ps[kk * 8 + h];
-                    const uint32_t v0 = *reinterpret_cast<const uint32_t*>(vp);
-                    o0 = fmaf(pr, bf_lo(v0), o0);
-                    o1 = fmaf(pr, bf_hi(v0), o1);
-                    if (dpl == 4) {
-                        const uint32_t v1 = *reinterpret_cast<const uint32_t*>(vp + 4);
-                        o2 = fmaf(pr, bf_lo(v1), o2);
-                        o3 = fmaf(pr, bf_hi(v1), o3);
-                    }
+            for (int jj = 0; jj < d / 16; ++jj) {
+                const int e0 = 16 * jj + (mi >> 1) * 8, line = vkey * DC + (e0 >> 6);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vbase + line * 128 + ((((e0 & 63) >> 3) ^ (line & 7)) << 4), b0, b1, b2, b3);
+                float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16_16816(o0, pa0, 0u, pa2, 0u, b0, b1);
+                mma_bf16_16816(o1, pa0, 0u, pa2, 0u, b2, b3);
+                if (g < G) {
+                    float* dst = C.att() + (warp * G + g) * d + 16 * jj + 2 * t;
+                    *reinterpret_cast<float2*>(dst) = make_float2(o0[0], o0[1]);
+                    *reinterpret_cast<float2*>(dst + 8) = make_float2(o1[0], o1[1]);
                 }
-                float* dst = C.att() + (warp * G + h) * d + ev;
-                if (dpl == 4) *reinterpret_cast<float4*>(dst) = make_float4(o0, o1, o2, o3);
-                else *reinterpret_cast<float2*>(dst) = make_float2(o0, o1);
+            }
+            if (g < G && t == 0) {
+                ml[(warp * 16 + g) * 2] = mx;
+                ml[(warp * 16 + g) * 2 + 1] = lsum;
             }
         }
         ring_release(C.ring(), k0);
@@ -861,9 +880,9 @@ __device__ __forceinline__ bool phase_o(Ctx& C, const ChainArgs& A, int l, unsig
             unsigned long long v[kPoll][2];
 #pragma unroll
             for (int u = 0; u < kPoll; ++u) off[u] = -1;
-            const int nb = min(5, n - c0);                 // 3 double pairs per chunk
+            const int nb = min(2, n - c0);                 // 3 double pairs per chunk
 #pragma unroll
-            for (int c = 0; c < 5; ++c)
+            for (int c = 0; c < 2; ++c)
                 if (c < nb) {
                     const int base = dp_off(A, A.fp + ((size_t)gi * A.maxch + c0 + c) * G * (d + 2));
                     off[3 * c] = base + (j * d + 4 * e4) / 2;
@@ -874,7 +893,7 @@ __device__ __forceinline__ bool phase_o(Ctx& C, const ChainArgs& A, int l, unsig
             if (rs && c0 == 0) off[kPoll - 1] = dp_off(A, A.fx) + res_at(tid, rt) / 2;
             ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
 #pragma unroll
-            for (int c = 0; c < 5; ++c)
+            for (int c = 0; c < 2; ++c)
                 if (c < nb) {
                     const float mc = ll_val(v[3 * c + 2][0]), Mn = fmaxf(M, mc);
                     const float fa = ex2_approx(M - Mn), fb = ex2_approx(mc - Mn);
@@ -1023,6 +1042,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         if (tid == 0) misc[kMiCnt + p] = n;
         for (int i = tid; i < n; i += blockDim.x) misc[kMiItems + p * kChainMaxItems + i] = st[A.grid + 1 + a + i];
     }
+    // query rows >= G of the attention tile stay zero
+    for (int i = tid; i < kPsBytes / 2; i += blockDim.x) C.qs()[i] = __float2bfloat16_rn(0.f);
     // layer 0's pointers
     for (int i = tid; i < (int)(sizeof(ChainLayer) / 8); i += blockDim.x)
         reinterpret_cast<unsigned long long*>(&lay[0])[i] = reinterpret_cast<const unsigned long long*>(A.layers)[i];

@@ -1358,30 +1358,30 @@ extern "C" tp_status tp_stack_create(tp_plan_t plan, int32_t n_layers, const tp_
     if (A.n_slots < 4)
         return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: operands of this shape leave no room for the weight ring");
 
-    // ---- items of the projection phases, bytes balanced over the CTAs (largest first)
-    struct Item { long bytes; int phase, id; };
-    std::vector<Item> items;
+    // ---- items of the projection phases: each phase dealt round robin over
+    // the CTAs (a phase lasts as long as its busiest CTA), starting each phase
+    // after the CTAs the previous phases loaded most, so the bytes spread too
     const int nph[4] = {N * qkv_rows / 8, H / 8, N * F_s / 8, H / 8};
     const long bph[4] = {16L * H, 16L * N * hq_s * hd, 32L * H, 16L * N * F_s};
     // o_proj and down items: one residual double pair per consumer thread (items x tokens x 4 <= 256)
     const int cap[4] = {kChainMaxItems, std::min(kChainMaxItems, 64 / MB), kChainMaxItems,
                         std::min(kChainMaxItems, 64 / MB)};
-    for (int p = 0; p < 4; ++p) {
+    std::vector<long> load(grid, 0);
+    std::vector<std::vector<int>> own(4 * (size_t)grid);
+    const int order_ph[4] = {3, 2, 0, 1};                   // down, gate/up, qkv, o_proj
+    for (int k = 0; k < 4; ++k) {
+        const int p = order_ph[k];
         if (nph[p] > (long)grid * cap[p])
             return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: %d items of phase %d exceed %d CTAs x %d", nph[p], p, grid,
                         cap[p]);
-        for (int i = 0; i < nph[p]; ++i) items.push_back({bph[p], p, i});
-    }
-    std::stable_sort(items.begin(), items.end(), [](const Item& x, const Item& y) { return x.bytes > y.bytes; });
-    std::vector<long> load(grid, 0);
-    std::vector<std::vector<int>> own(4 * (size_t)grid);
-    for (const Item& it : items) {
-        int best = -1;
-        for (int c = 0; c < grid; ++c)
-            if ((int)own[(size_t)it.phase * grid + c].size() < cap[it.phase] && (best < 0 || load[c] < load[best]))
-                best = c;
-        own[(size_t)it.phase * grid + best].push_back(it.id);
-        load[best] += it.bytes;
+        std::vector<int> by_load(grid);
+        for (int c = 0; c < grid; ++c) by_load[c] = c;
+        std::stable_sort(by_load.begin(), by_load.end(), [&](int x, int y) { return load[x] < load[y]; });
+        for (int i = 0; i < nph[p]; ++i) {
+            const int c = by_load[i % grid];
+            own[(size_t)p * grid + c].push_back(i);
+            load[c] += bph[p];
+        }
     }
     for (auto& v : own) std::sort(v.begin(), v.end());   // shard-major: one normalised operand per shard run
     std::vector<int> tab;
