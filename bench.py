@@ -362,7 +362,7 @@ def run_ours(args, world, rank, local):
     # form one normalised copy; decode reads it per shard either way)
     model = Model(inputs, share_norm=(kind in ("prefill", "moe")))
     # several decode layers: all of them in one launch per token
-    stacked = kind == "decode" and w.dtype == "bf16" and w.n_layers > 1 and args.stack
+    stacked = kind == "decode" and w.dtype == "bf16" and w.n_layers > 1 and not args.per_layer
     fwd = model.forward_stack if stacked else model.forward
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -593,9 +593,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_KIND))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--stack", action="store_true",
-                    help="multi-layer decode: one launch per token for all layers (tp_stack_decode) instead of one "
-                         "per layer (tp_block_forward)")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="multi-layer decode: one launch per layer (tp_block_forward) instead of one launch per "
+                         "token for all layers (tp_stack_decode)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -45,17 +45,18 @@ enum { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3 };   // projection phases (item
 
 // ---- (value, epoch) pairs -------------------------------------------------------
 //
-// A pair is one naturally aligned 8-byte word, written and read as a unit, so a
-// reader that sees the epoch it expects sees the value written with it.
+// A pair is one naturally aligned 8-byte word, written and read as a unit
+// (relaxed, GPU scope: the exchange never leaves the device), so a reader that
+// sees the epoch it expects sees the value written with it.
 
 __device__ __forceinline__ unsigned long long ll_pack(float v, unsigned ep) {
     return ((unsigned long long)ep << 32) | __float_as_uint(v);
 }
 __device__ __forceinline__ void ll_st(unsigned long long* p, float v, unsigned ep) {
-    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, ep)) : "memory");
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, ep)) : "memory");
 }
 __device__ __forceinline__ void ll_ld2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
-    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 __device__ __forceinline__ bool ll_ok(unsigned long long v, unsigned ep) { return (unsigned)(v >> 32) == ep; }
 __device__ __forceinline__ float ll_val(unsigned long long v) { return __uint_as_float((unsigned)v); }
