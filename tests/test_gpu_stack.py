@@ -30,6 +30,9 @@ CASES = {
     # tp 1: the unsharded block, 2 layers, keys exactly one tile (128)
     "qwen_shape_tp1": synth.scaled(QWEN, hidden=256, n_heads=4, n_kv_heads=1, ffn=512, tp=1, batch=2,
                                    kv_len=127, n_layers=2, seed=24, org_vocab=0),
+    # tp 8, one KV head and two query heads per shard, head_dim 128, a full batch of 8, 129 keys in chunks of 48, 48, 33
+    "llama_shape_tp8_b8": synth.scaled(LLAMA, hidden=1024, n_heads=16, n_kv_heads=8, ffn=2048, tp=8, batch=8,
+                                       kv_len=128, n_layers=1, seed=25),
 }
 
 
@@ -130,3 +133,28 @@ def test_stack_position_past_capacity_is_reported(gpu_lib):
     assert m.ws.status() == tb.binding.TP_ERR_CAPACITY
     for c, kb in zip(m.caches, k_before):
         assert torch.equal(kb, c.k[0])
+
+
+def test_stack_shares_a_workspace_with_per_layer_launches(gpu_lib):
+    import torch
+    inputs = synth.make_inputs(CASES["qwen_shape_3_layers_kv300"])
+    m = _model(inputs)
+    a = m.forward_stack().clone()
+    b = m.forward().clone()                  # the other mode writes the shared data region
+    c = m.forward_stack().clone()
+    torch.cuda.synchronize()
+    assert m.ws.status() == 0
+    assert torch.equal(a, c)
+    assert O.relerr(a.double().cpu().numpy(), b.double().cpu().numpy()) <= TOL
+
+
+def test_stack_many_launches_keep_their_epochs(gpu_lib):
+    import torch
+    inputs = synth.make_inputs(CASES["qwen_shape_tp1"])
+    m = _model(inputs)
+    ref = m.forward_stack().clone()
+    for _ in range(300):                     # the launch counter advances once per launch
+        m.forward_stack()
+    torch.cuda.synchronize()
+    assert m.ws.status() == 0
+    assert torch.equal(m.y, ref)
