@@ -415,6 +415,24 @@ def block_rows_tpN(shards, x, k_caches, v_caches, pos, S, cfg, N, rows):
 # ---------------------------------------------------------------------------
 
 
+def lm_head_logits(h: np.ndarray, gamma: np.ndarray, W: np.ndarray, eps: float) -> np.ndarray:
+    """Logits of the final hidden state over the unpadded head ``W``
+    ``[org_vocab, H]``: ``RMSNorm(h) @ W.T``. The norm is replicated ("Multi-GPU
+    & Multi-Node", How tensor parallelism works); the head is the gathered
+    vocab-parallel parameter (the gather-on-read PR, Change)."""
+    return rmsnorm(h, gamma, eps) @ W.T
+
+
+def lm_head_logits_tpN(h: np.ndarray, gamma: np.ndarray, head_shards: list, org_vocab: int,
+                       eps: float) -> np.ndarray:
+    """Vocab-parallel logits: shard r computes the logits of its rows of the
+    padded head (column-parallel over the vocabulary), the shards' logits are
+    concatenated in rank order and the padding columns (rows >= org_vocab of
+    the head) are dropped, as the vocab-parallel gather drops its rows."""
+    n = rmsnorm(h, gamma, eps)
+    return np.concatenate([n @ Wr.T for Wr in head_shards], axis=1)[:, :org_vocab]
+
+
 def router_topk(logits: np.ndarray, k: int):
     """Softmax over all experts, the k largest probabilities (ties to the
     lower expert id), renormalised to sum to one. Returns ``ids [T, k]``

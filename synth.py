@@ -155,7 +155,8 @@ def make_inputs(w: Workload, with_head: bool = True) -> dict:
     (per layer, ``[batch, kv_heads, kv_len, head_dim]`` in the storage type:
     keys are taken as already rotated), ``pos`` (``int32 [batch]``, the first
     new position of each sequence), and where present ``lm_head``
-    (``[org_vocab, hidden]``) or the MoE tensors.
+    (``[org_vocab, hidden]``) with the final norm's ``gamma_final``, or the
+    MoE tensors.
     """
     d = _Draw(w.seed)
     out = {"workload": w}
@@ -180,6 +181,7 @@ def make_inputs(w: Workload, with_head: bool = True) -> dict:
     out["pos"] = np.full((w.batch,), w.kv_len, dtype=np.int32)
     if with_head and w.org_vocab:
         out["lm_head"] = d.stored((w.org_vocab, w.hidden), w.dtype, 0.02)
+        out["gamma_final"] = d.normal((w.hidden,), 0.02, 1.0)     # the final norm before the head
     return out
 
 

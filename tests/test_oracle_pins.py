@@ -508,3 +508,56 @@ def test_moe_matches_dense_per_token_loop():
             a = F.silu(torch.from_numpy(eg[e] @ n[t])).numpy() * (eu[e] @ n[t])
             acc += p[t, e] / p[t, top].sum() * (ed[e] @ a)
         assert np.allclose(y[t], x[t] + acc, rtol=1e-13, atol=1e-13)
+
+
+# ---- lens / logits over the vocab-parallel head ---------------------------------
+
+
+def test_lm_head_identity_head_gives_the_closed_form_norm():
+    # head rows = unit vectors, h = a constant c, gamma = 1: every logit is
+    # RMSNorm(c) = sign(c) / sqrt(1 + eps / c^2), whatever the row
+    H, V, eps = 64, 40, 1e-6
+    W = np.eye(H)[:V]
+    for c in (-2.5, 0.75, 3.0):
+        h = np.full((2, H), c)
+        logits = O.lm_head_logits(h, np.ones(H), W, eps)
+        assert logits.shape == (2, V)
+        assert np.allclose(logits, math.copysign(1.0, c) / math.sqrt(1.0 + eps / (c * c)), rtol=1e-15)
+
+
+def test_lm_head_identity_head_picks_normalised_columns():
+    # with unit-vector rows, logit i is column i of RMSNorm(h) (the head's
+    # orientation: logits = n @ W.T, not W @ n)
+    H, V, eps = 32, 20, 1e-6
+    h = rng(71).standard_normal((3, H))
+    g = rng(72).uniform(0.5, 1.5, H)
+    perm = rng(73).permutation(H)[:V]
+    W = np.eye(H)[perm]
+    n = h / np.sqrt((h * h).mean(-1, keepdims=True) + eps) * g
+    assert np.allclose(O.lm_head_logits(h, g, W, eps), n[:, perm], rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_lm_head_vocab_parallel_equals_unsharded_and_drops_padding(N):
+    H, V, eps = 64, 1000, 1e-5           # 1000 rows: padded to a multiple of 64 N, padding on the last shard
+    h = rng(81).standard_normal((2, H))
+    g = rng(82).uniform(0.5, 1.5, H)
+    W = rng(83).standard_normal((V, H)) * 0.02
+    shards = O.shard_vocab(W, N)          # padding rows are NaN: any leak shows up
+    assert sum(s.shape[0] for s in shards) == O.vocab_padded(V, N)
+    tpN = O.lm_head_logits_tpN(h, g, shards, V, eps)
+    assert tpN.shape == (2, V) and np.isfinite(tpN).all()
+    ref = O.lm_head_logits(h, g, W, eps)
+    assert np.allclose(tpN, ref, rtol=1e-12, atol=1e-14)
+    # the last real row lives on the last shard (the cross-shard index of the gather)
+    last = O.rmsnorm(h, g, eps) @ W[V - 1]
+    assert np.allclose(tpN[:, V - 1], last, rtol=1e-12)
+
+
+def test_lm_head_matches_torch():
+    H, V, eps = 96, 300, 1e-6
+    h = rng(91).standard_normal((4, H))
+    g = rng(92).uniform(0.5, 1.5, H)
+    W = rng(93).standard_normal((V, H))
+    t = F.linear(F.rms_norm(torch.from_numpy(h), (H,), torch.from_numpy(g), eps), torch.from_numpy(W)).numpy()
+    assert np.allclose(O.lm_head_logits(h, g, W, eps), t, rtol=1e-12, atol=1e-12)
