@@ -370,6 +370,27 @@ tp_status tp_stack_set_stamps(tp_stack_t stack, uint64_t* stamps, int32_t rows);
 tp_status tp_stack_decode(tp_stack_t stack, const float* x, float* y, const int32_t* pos, int32_t B,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Logits of the final hidden state over the vocab-parallel head ([GA] Change:
+ * the head split by vocabulary rows, padded to a multiple of 64*tp with the
+ * padding at the tail of the last shard, padding dropped on gather; [MG] How
+ * tensor parallelism works: the norm before it replicated):
+ *   logits[t][v] = RMSNorm(x[t]) . W[v],   v < org_vocab,
+ * with RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gamma and W the shards
+ * stacked in rank order. Each shard's rows give its column-parallel logits;
+ * writing only v < org_vocab is the gather (padding never reaches `logits`).
+ * head_shards: HOST array of tp device pointers, each [vocab_rows_shard, H]
+ * bf16 (as tp_shard_param with TP_PARAM_VOCAB_PARALLEL writes them). gamma
+ * float32 [H], x float32 [T, H], logits float32 [T, org_vocab], all device,
+ * 16-byte aligned. The norm's operand x * gamma is rounded to bf16 for the
+ * products, which accumulate in float32. `device_status` (nullable, device
+ * int32) receives TP_ERR_TIMEOUT if a bounded wait gives up. One launch.
+ * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no head in the plan),
+ * TP_ERR_UNSUPPORTED (not bf16), TP_ERR_SHAPE (T outside 1..8), TP_ERR_ALIGN,
+ * TP_ERR_CUDA. */
+tp_status tp_lm_head_forward(tp_plan_t plan, const void* const* head_shards, const float* gamma,
+                             const float* x, int32_t T, float* logits, int32_t* device_status,
+                             void* stream);
+
 /* Standalone rank-order reduction ([RT] Collective backend abstraction,
  * copy-and-reduce; [MG] Local TP: the add after the copies):
  *   out[m, :] = residual[m, :] + (((p_0 + p_1) + p_2) + ... + p_{tp-1})[m, :] + bias

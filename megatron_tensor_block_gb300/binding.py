@@ -108,6 +108,7 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_stack_ctas": (I32, [P]),
         "tp_stack_set_stamps": (I32, [P, VP, I32]),
         "tp_stack_decode": (I32, [P, VP, VP, VP, I32, VP, C.c_size_t, VP]),
+        "tp_lm_head_forward": (I32, [P, C.POINTER(VP), VP, VP, I32, VP, VP, VP]),
         "tp_reduce_partials": (I32, [P, VP, VP, VP, VP, I64, VP]),
         "tp_get_device_status": (I32, [VP, C.POINTER(I32), VP]),
         "tp_gemm_bf16": (I32, [VP, VP, VP, I64, I64, I64, VP, VP]),
@@ -278,6 +279,14 @@ def tp_stack_set_stamps(stack: Stack, stamps, rows: int) -> None:
 def tp_stack_decode(stack: Stack, x, y, pos, B: int, workspace, nbytes: int, stream=None) -> None:
     _check(load().tp_stack_decode(stack.handle, _ptr(x), _ptr(y), _ptr(pos), B, _ptr(workspace), nbytes,
                                   _stream(stream)))
+
+
+def tp_lm_head_forward(plan: Plan, head_shards: list, gamma, x, T: int, logits, device_status=None,
+                       stream=None) -> None:
+    """Logits of the final hidden state over the vocab-parallel head."""
+    arr = (C.c_void_p * len(head_shards))(*[_ptr(t) for t in head_shards])
+    _check(load().tp_lm_head_forward(plan.handle, arr, _ptr(gamma), _ptr(x), T, _ptr(logits),
+                                     _ptr(device_status), _stream(stream)))
 
 
 def tp_reduce_partials(plan: Plan, partials, residual, bias, out, M: int, stream=None) -> None:

@@ -21,7 +21,7 @@ LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libtpblock.so")
 
 SOURCES = ["tp_api.cu", "kernels_decode.cu", "kernels_copy.cu", "kernels_moe.cu", "kernels_prefill.cu",
-           "kernels_chain.cu"]
+           "kernels_chain.cu", "kernels_head.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "-I", INCLUDE, "-I", CSRC]

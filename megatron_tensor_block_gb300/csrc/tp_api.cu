@@ -1511,3 +1511,49 @@ extern "C" tp_status tp_stack_decode(tp_stack_t stack, const float* x, float* y,
     TP_CUDA(tpk::launch_chain(A, stack->smem, static_cast<cudaStream_t>(stream)), "tp_stack_decode: launch");
     return ok();
 }
+
+// ---------------------------------------------------------------- logits over the vocab-parallel head
+
+extern "C" tp_status tp_lm_head_forward(tp_plan_t plan, const void* const* head_shards, const float* gamma,
+                                        const float* x, int32_t T, float* logits, int32_t* device_status,
+                                        void* stream) {
+    if (!plan || !head_shards || !gamma || !x || !logits) return fail(TP_ERR_NULL, "tp_lm_head_forward: NULL argument");
+    const tp_model_desc& d = plan->d;
+    const tp_plan_info& I = plan->info;
+    if (d.org_vocab <= 0) return fail(TP_ERR_INVALID_ARG, "tp_lm_head_forward: the plan has no head (org_vocab 0)");
+    if (d.dtype != TP_BF16) return fail(TP_ERR_UNSUPPORTED, "tp_lm_head_forward: bf16 heads only");
+    if (T < 1 || T > tpk::kTMax) return fail(TP_ERR_SHAPE, "tp_lm_head_forward: T=%d outside 1..%d", T, tpk::kTMax);
+    const int N = plan->N;
+    for (int r = 0; r < N; ++r) {
+        if (!head_shards[r]) return fail(TP_ERR_NULL, "tp_lm_head_forward: shard %d is NULL", r);
+        if (!aligned16(head_shards[r])) return fail(TP_ERR_ALIGN, "tp_lm_head_forward: shard %d not 16-byte aligned", r);
+    }
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(logits))
+        return fail(TP_ERR_ALIGN, "tp_lm_head_forward: x, gamma and logits must be 16-byte aligned");
+    tp_status st = check_device();
+    if (st) return st;
+    int dev = 0, sms = 0, smem_max = 0;
+    TP_CUDA(cudaGetDevice(&dev), "tp_lm_head_forward: cudaGetDevice");
+    TP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "tp_lm_head_forward: SM count");
+    TP_CUDA(cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "tp_lm_head_forward: smem");
+    tpk::HeadArgs A{};
+    for (int r = 0; r < N; ++r) A.W[r] = head_shards[r];
+    A.N = N;
+    A.rows_s = (int)I.vocab_rows_shard;
+    A.org_vocab = (int)d.org_vocab;
+    A.H = (int)d.hidden;
+    A.T = T;
+    A.grid = sms;
+    A.x = x;
+    A.gamma = gamma;
+    A.eps = (float)d.eps;
+    A.logits = logits;
+    A.status = reinterpret_cast<int*>(device_status);
+    const size_t smem = tpk::head_smem(A, smem_max);
+    if (A.ns < 2) return fail(TP_ERR_UNSUPPORTED, "tp_lm_head_forward: hidden size too large for the stage ring");
+    const long total = (long)N * A.rows_s;
+    long rpc = (total + A.grid - 1) / A.grid;
+    A.rpc = (rpc + A.rs - 1) / A.rs * A.rs;
+    TP_CUDA(tpk::launch_lm_head(A, smem, static_cast<cudaStream_t>(stream)), "tp_lm_head_forward: launch");
+    return ok();
+}

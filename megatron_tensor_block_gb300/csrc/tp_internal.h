@@ -284,6 +284,25 @@ cudaError_t launch_chain(const ChainArgs& a, size_t smem, cudaStream_t s);
 // {64, kc, box_rows}, 128-byte swizzled, written to `out` (any memory).
 cudaError_t chain_map(const void* W, long K, long rows, int kc, int box_rows, CUtensorMap* out);
 
+// Logits of the final hidden state over the vocab-parallel head (bf16 rows of
+// every shard stacked in rank order; rows >= org_vocab are padding, not written).
+constexpr int kHeadThreads = 288;        // eight consumer warps + a copy-issuing warp
+constexpr int kHeadMaxStages = 16;
+struct HeadArgs {
+    const void* W[TP_MAX_SHARDS];        // [rows_s][H] bf16 per shard
+    int N, rows_s, org_vocab, H, T, grid;
+    long rpc;                            // rows per CTA (a multiple of rs)
+    int rs, ns, ring_off;                // rows per stage, stages, ring offset in shared memory
+    const float* x;                      // [T][H]
+    const float* gamma;                  // [H]
+    float eps;
+    float* logits;                       // [T][org_vocab]
+    int* status;                         // nullable
+};
+// Picks the stage geometry of `a` (H set) for smem_max bytes; returns the launch's shared-memory bytes.
+size_t head_smem(HeadArgs& a, int smem_max);
+cudaError_t launch_lm_head(const HeadArgs& a, size_t smem, cudaStream_t s);
+
 // launchers (return the launch's cudaError_t)
 cudaError_t launch_gemv(const GemvParams& p, int epi, int dtype, cudaStream_t s);
 void set_pdl(bool on);   // programmatic dependent launch between the kernels of a call (default on)
