@@ -288,6 +288,40 @@ class OracleLeg:
         return 1
 
 
+def lens_timing(w, stream, peak: float, n: int = 50) -> dict:
+    """Logits of the final hidden state over the vocab-parallel head (the
+    lens), timed alone on a head of the workload's shape: one launch reads
+    the whole head (larger than L2, so no flush between launches)."""
+    import torch
+    import megatron_tensor_block_gb300 as tb
+    from megatron_tensor_block_gb300.runtime import desc_of, to_device
+    hi = synth.make_inputs(synth.scaled(w, n_layers=1))
+    plan = tb.tp_plan(desc_of(w), w.tp)
+    info = tb.tp_plan_get_info(plan)
+    V, H = hi["lm_head"].shape
+    full = to_device(hi["lm_head"])
+    shards = [torch.empty(info["vocab_rows_shard"], H, dtype=full.dtype, device="cuda") for _ in range(w.tp)]
+    tb.tp_shard_param(plan, tb.TP_PARAM_VOCAB_PARALLEL, full, V, H, tb.TP_BF16, shards)
+    del full
+    x = to_device(hi["x"])
+    g = to_device(hi["gamma_final"].astype(np.float32))
+    out = torch.empty(w.tokens * V, dtype=torch.float32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            tb.tp_lm_head_forward(plan, shards, g, x, w.tokens, out, None, stream)
+        e0.record(stream)
+        for _ in range(n):
+            tb.tp_lm_head_forward(plan, shards, g, x, w.tokens, out, None, stream)
+        e1.record(stream)
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    nbytes = info["vocab_rows_shard"] * w.tp * H * 2
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"kernel": "lm_head_kernel (tp_lm_head_forward)", "us": us, "algorithmic_bytes": nbytes, "gbs": gbs,
+            "frac_of_peak": gbs / peak, "launches": n}
+
+
 def cpu_baseline(inputs, budget_s: float = 20.0) -> dict:
     leg = OracleLeg(inputs)
     leg.step()                                           # warm
@@ -523,6 +557,9 @@ def run_ours(args, world, rank, local):
         extra["hbm"] = {"step_bytes": step_bytes(w), "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak,
                         "frac_of_8000": step_gbs / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
         l2_note = f"inputs larger than L2 ({step_bytes(w) / 1e6:.1f} MB read per step vs 129 MB L2)"
+
+    if kind == "decode" and w.dtype == "bf16" and w.org_vocab:
+        extra["lens"] = lens_timing(w, stream, pk["hbm"])   # reported beside the block, not in its time
 
     # ---- end to end through the public API: pinned host inputs -> device, forward, y -> pinned host
     x_host = torch.from_numpy(np.ascontiguousarray(inputs["x"])).pin_memory()

@@ -1551,6 +1551,7 @@ extern "C" tp_status tp_lm_head_forward(tp_plan_t plan, const void* const* head_
     A.status = reinterpret_cast<int*>(device_status);
     const size_t smem = tpk::head_smem(A, smem_max);
     if (A.ns < 2) return fail(TP_ERR_UNSUPPORTED, "tp_lm_head_forward: hidden size too large for the stage ring");
+    A.grid = sms * A.cps;
     const long total = (long)N * A.rows_s;
     long rpc = (total + A.grid - 1) / A.grid;
     A.rpc = (rpc + A.rs - 1) / A.rs * A.rs;

@@ -292,7 +292,7 @@ struct HeadArgs {
     const void* W[TP_MAX_SHARDS];        // [rows_s][H] bf16 per shard
     int N, rows_s, org_vocab, H, T, grid;
     long rpc;                            // rows per CTA (a multiple of rs)
-    int rs, ns, ring_off;                // rows per stage, stages, ring offset in shared memory
+    int rs, ns, ring_off, cps;           // rows per stage, stages, ring offset in shared memory, CTAs per SM
     const float* x;                      // [T][H]
     const float* gamma;                  // [H]
     float eps;
