@@ -122,3 +122,13 @@ def test_decode_position_past_capacity_is_reported(gpu_lib):
     torch.cuda.synchronize()
     assert m.ws.status() == tb.binding.TP_ERR_CAPACITY
     assert torch.equal(k_before, m.caches[0].k[0])
+
+
+def test_decode_ragged_positions_match_oracle(gpu_lib):
+    # every sequence at its own position: ragged KV lengths (300, 0 and 151 cached keys before the step)
+    w = CASES["llama_shape_small_tp4_b3"]
+    inputs = synth.make_inputs(w)
+    inputs["pos"] = np.array([300, 0, 151], dtype=np.int32)
+    m, y = _run(gpu_lib, inputs)
+    ref, _ = R.dense_tpN(inputs, m.max_kv)
+    assert O.relerr(y, ref) <= TOL[w.dtype]

@@ -158,3 +158,26 @@ def test_stack_many_launches_keep_their_epochs(gpu_lib):
     torch.cuda.synchronize()
     assert m.ws.status() == 0
     assert torch.equal(m.y, ref)
+
+
+RAGGED = {
+    # per-sequence positions (ragged KV lengths), each attending over its own keys 0..pos[b]
+    "llama_shape_tp4_b3_2_layers": [200, 5, 130],
+    "llama_shape_tp8_b8": [128, 0, 64, 127, 1, 99, 3, 50],
+}
+
+
+@pytest.mark.parametrize("case", list(RAGGED))
+def test_stack_ragged_positions_match_oracle(gpu_lib, case):
+    w = CASES[case]
+    inputs = synth.make_inputs(w)
+    inputs["pos"] = np.array(RAGGED[case], dtype=np.int32)
+    m = _model(inputs)
+    y = _run_stack(m)
+    ref, caches = R.dense_tpN(inputs, m.max_kv)
+    assert O.relerr(y, ref) <= TOL
+    k, _ = m.caches[0].full()
+    pos = inputs["pos"]
+    kk = np.stack([k[b, :, pos[b]].double().cpu().numpy() for b in range(len(pos))])
+    rk = np.stack([caches[0][0][b, :, pos[b]] for b in range(len(pos))])
+    assert O.relerr(kk, rk) <= TOL
