@@ -894,7 +894,8 @@ __device__ __forceinline__ int sk_nseg(const GemvParams& p, int epi) {
 // epilogue, which costs more than the imbalance). A row-parallel phase either
 // gives each CTA whole output tiles -- every shard's piece, reduced in rank
 // order inside the CTA (whole_tiles) -- or is split evenly, its pieces then
-// reduced by the CTA that finishes last.
+// reduced by the CTA holding the tile's last stage, which polls them as
+// (value, epoch) pairs (without a pair buffer: by the CTA that arrives last).
 __device__ __forceinline__ int sk_phase_share(const GemvParams& p, int epi, int S) {
     const int nseg = sk_nseg(p, epi);
     if (epi != EPI_ROWPAR) return S * ((nseg + (int)gridDim.x - 1) / (int)gridDim.x);
@@ -1466,6 +1467,113 @@ __device__ __forceinline__ void sk_row_finish(const GemvParams& p, int tb, int S
     sk_row_out(p, tb, total, res, g2);
 }
 
+// (value, epoch) pairs: a 64-bit word per value, the epoch of the launch
+// that wrote it in the high half. A single-copy-atomic 64-bit access needs no
+// fence or counter: a reader that sees the current epoch sees the value.
+__device__ __forceinline__ unsigned long long sk_pack(float v, unsigned ep) {
+    return ((unsigned long long)ep << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ void sk_pair_store2(unsigned long long* p, float a, float b, unsigned ep) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(sk_pack(a, ep)), "l"(sk_pack(b, ep))
+                 : "memory");
+}
+__device__ __forceinline__ void sk_pair_load2(const unsigned long long* p, unsigned long long& a,
+                                              unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// Consumers: row-parallel output tile tb split over CTAs, combined by the CTA
+// holding its last stage. Every thread polls its (row, token pair) of every
+// piece at once until all carry this launch's epoch (bounded), then sums
+// the pieces in CTA order within each rank, the ranks in order, and adds the
+// residual -- the order of the counted finish, without its fence, counter
+// and second round trip.
+__device__ __forceinline__ void sk_row_combine(const GemvParams& p, int tb, int S, int R, unsigned ep,
+                                               volatile int* abort) {
+    constexpr int kPer = 2;                            // pieces per shard polled from registers
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j8 = lane >> 2, tp = lane & 3;
+    const int j = warp * 8 + j8;
+    const int nsplit = p.shape.chunks;
+    auto piece = [&](int r, int c) {
+        return p.pairs + ((size_t)(tb * p.n_shards + r) * nsplit + c) * (kTileRows * kTMax) + j * kTMax + 2 * tp;
+    };
+    const int row = tb * kTileRows + j;
+    float2 res = make_float2(0.f, 0.f);
+    if (2 * tp < p.T) res.x = __ldcg(p.resid + (size_t)(2 * tp) * p.rows + row);
+    if (2 * tp + 1 < p.T) res.y = __ldcg(p.resid + (size_t)(2 * tp + 1) * p.rows + row);
+    float g2[TP_MAX_SHARDS];
+#pragma unroll
+    for (int r2 = 0; r2 < TP_MAX_SHARDS; ++r2) g2[r2] = p.norm_out && r2 < p.n_shards ? p.gamma2[r2][row] : 0.f;
+    int cnt_r[TP_MAX_SHARDS];
+    unsigned long long va[TP_MAX_SHARDS][kPer], vb[TP_MAX_SHARDS][kPer];
+#pragma unroll
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        cnt_r[r] = 0;
+        if (r < p.n_shards) {
+            int first, last;
+            sk_owners(tb * p.n_shards + r, S, R, first, last);
+            cnt_r[r] = last - first + 1;
+        }
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) va[r][c] = vb[r][c] = 0ull;
+    }
+    auto cur = [&](unsigned long long a, unsigned long long b) {
+        return (unsigned)(a >> 32) == ep && (unsigned)(b >> 32) == ep;
+    };
+    uint64_t t0 = 0;
+    for (int round = 0;; ++round) {
+#pragma unroll
+        for (int r = 0; r < TP_MAX_SHARDS; ++r)
+#pragma unroll
+            for (int c = 0; c < kPer; ++c)
+                if (c < cnt_r[r] && !cur(va[r][c], vb[r][c])) sk_pair_load2(piece(r, c), va[r][c], vb[r][c]);
+        bool all = true;
+#pragma unroll
+        for (int r = 0; r < TP_MAX_SHARDS; ++r)
+#pragma unroll
+            for (int c = 0; c < kPer; ++c)
+                if (c < cnt_r[r]) all = all && cur(va[r][c], vb[r][c]);
+        if (all) break;
+        if (round == 0) t0 = global_ns();
+        if (*abort) break;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            set_status(p.status, TP_ERR_TIMEOUT);
+            break;
+        }
+    }
+    float2 total = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < TP_MAX_SHARDS; ++r) {
+        if (r < p.n_shards) {
+            float2 pr = make_float2(__uint_as_float((unsigned)va[r][0]), __uint_as_float((unsigned)vb[r][0]));
+#pragma unroll
+            for (int c = 1; c < kPer; ++c)
+                if (c < cnt_r[r])
+                    pr = make_float2(pr.x + __uint_as_float((unsigned)va[r][c]),
+                                     pr.y + __uint_as_float((unsigned)vb[r][c]));
+            for (int c = kPer; c < cnt_r[r]; ++c) {        // more pieces than registers: one at a time
+                unsigned long long a = 0ull, b = 0ull;
+                const uint64_t t1 = global_ns();
+                while (true) {
+                    sk_pair_load2(piece(r, c), a, b);
+                    if (cur(a, b) || *abort) break;
+                    if (global_ns() - t1 > kWaitLimitNs) {
+                        *abort = 1;
+                        set_status(p.status, TP_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+                pr = make_float2(pr.x + __uint_as_float((unsigned)a), pr.y + __uint_as_float((unsigned)b));
+            }
+            total = r == 0 ? pr : make_float2(total.x + pr.x, total.y + pr.y);
+        }
+    }
+    __syncwarp();
+    sk_row_out(p, tb, total, res, g2);
+}
+
 // Consumers: output tile tb of a row-parallel phase whose rank-ordered sum
 // over the shards is in `acc` ([64][8]); the tile's inputs were prefetched
 // into `slot` by sk_row_prefetch.
@@ -1485,7 +1593,7 @@ template <int EPI>
 __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned char* ring, uint64_t* full,
                                         uint64_t* empty, volatile int* abort, uint32_t& it, float* tile, float* acc,
                                         float* ss, int* s_pos, float* s_bias, float* slot, SkQueue* qu,
-                                        uint32_t& jn, uint32_t& jf) {
+                                        uint32_t& jn, uint32_t& jf, unsigned ep) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = (p.K + kBoxK - 1) / kBoxK;
     const int W = sk_nseg(p, EPI) * S;
@@ -1613,6 +1721,12 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             consumer_sync(kConsumers);
             continue;
         }
+        if (EPI == EPI_ROWPAR && p.pairs) {              // the piece as (value, epoch) pairs, polled by the combiner
+            unsigned long long* pm = p.pairs + ((size_t)seg * nsplit + ((int)blockIdx.x - first)) * (kTileRows * kTMax);
+            for (int i = tid * 2; i < kTileRows * kTMax; i += kConsumers * 2) sk_pair_store2(pm + i, tile[i], tile[i + 1], ep);
+            consumer_sync(kConsumers);                  // `tile` may be reused
+            continue;
+        }
         float* mine = p.part + ((size_t)seg * nsplit + ((int)blockIdx.x - first)) * kPartStride;
         for (int i = tid * 4; i < kTileRows * kTMax; i += kConsumers * 4)
             *reinterpret_cast<float4*>(mine + i) = *reinterpret_cast<const float4*>(tile + i);
@@ -1633,6 +1747,14 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
         }
         ++jn;
         ++jf;
+    }
+    if (EPI == EPI_ROWPAR && p.pairs) {
+        // output tiles whose last stage is this CTA's: it combines their pieces
+        const int per_tile = p.n_shards * S;
+        for (int tb = (f0 + 1 + per_tile - 1) / per_tile - 1; (tb + 1) * per_tile <= f1; ++tb) {
+            if (tb < 0) continue;
+            sk_row_combine(p, tb, S, R, ep, abort);
+        }
     }
 }
 
@@ -2153,6 +2275,8 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     }
     __syncthreads();
     const unsigned long long gen0 = *s_gen0;
+    // this launch's epoch: the barrier counter grows by kSkBarriers * gridDim.x a launch (never 0)
+    const unsigned ep = (unsigned)(gen0 / ((unsigned long long)kSkBarriers * gridDim.x)) + 1u;
     unsigned long long* st =
         A.stamps && blockIdx.x < kMaxStepCtas ? A.stamps + (size_t)blockIdx.x * kStepStamps : nullptr;
 
@@ -2197,17 +2321,17 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     uint32_t it = 0, jn = 0, jf = 0, jf_mark = 0, nd = 0;
     sk_norm(A.np);
     sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf, ep);
     sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qs, seg_tab, s_nseg, tab_ready, qu,
                jn);
     sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf, ep);
     sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
-    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_gemv<EPI_SWIGLU>(A.g[2], 2, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf, ep);
     sk_phase_end<D>(A, gen0, 5, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     pdl_trigger();                                      // the next launch may start streaming its weights
-    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf);
+    sk_gemv<EPI_ROWPAR>(A.g[3], 3, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf, ep);
     sk_phase_end<D>(A, gen0, kSkBarriers + 1, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
 }
 

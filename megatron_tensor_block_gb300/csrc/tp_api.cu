@@ -72,6 +72,7 @@ struct tp_plan_s {
     size_t ws_decode_end = 0;           // end of the decode buffers (control words included)
     // multi-layer decode (tp_stack_decode): control words, then its own pair buffers
     // at the end of the workspace (no other mode writes them, so no stale epoch matches)
+    size_t off_step_pairs = 0;
     size_t off_c_ctrl = 0, off_c_x = 0, off_c_q = 0, off_c_p = 0, off_c_h = 0, off_c_a = 0,
            off_c_begin = 0, off_c_end = 0;
     int c_ck = 0, c_maxch = 0;
@@ -323,6 +324,8 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->c_maxch = (int)((d->max_kv + P->c_ck - 1) / P->c_ck);
         const int64_t groups = N * MB * I.hkv_shard;
         P->off_c_begin = off;
+        // split row-parallel tiles of the one-launch step: (value, epoch) pieces of the down phase
+        P->off_step_pairs = take((size_t)P->g_down.groups * N * P->step_split[3] * kTileRows * kTMax * 8);
         P->off_c_x = take((size_t)MB * H * 8);
         P->off_c_q = take((size_t)N * MB * I.qkv_rows * 8);
         P->off_c_p = take((size_t)groups * P->c_maxch * G * (hd + 2) * 8);
@@ -706,6 +709,7 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     dn.y = y;
     for (int r = 0; r < N; ++r) dn.W[r] = w->wd[r];
     dn.xact = ws + P->off_act;
+    dn.pairs = P->off_step_pairs ? reinterpret_cast<unsigned long long*>(ws + P->off_step_pairs) : nullptr;
 
     st.bar = reinterpret_cast<unsigned long long*>(ws + P->off_step_bar);
     st.stamps = P->n_stage_ev > 0 ? reinterpret_cast<unsigned long long*>(ws + P->off_stamps) : nullptr;

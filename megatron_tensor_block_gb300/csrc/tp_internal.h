@@ -82,6 +82,9 @@ struct GemvParams {
     float* ss_tiles_out;               // o_proj: [H / 8][kTMax] per-8-row sums of squares
     const float* gamma2[TP_MAX_SHARDS];
     int whole_tiles;                   // one-launch step, row-parallel: each CTA takes every shard of its output tiles
+    // one-launch step, row-parallel tiles split over CTAs: pieces as (value, epoch)
+    // pairs [segments][chunks][kTileRows * kTMax], polled by the tile's combiner; or NULL
+    unsigned long long* pairs;
 };
 
 // RMSNorm operand preparation: xg[r][t][k] = bf16(x[t][k] * gamma_r[k]),
