@@ -110,6 +110,21 @@ def test_decode_is_deterministic(gpu_lib):
     assert torch.equal(y1, y2)
 
 
+def test_decode_many_launches_keep_their_epochs(gpu_lib):
+    # split down tiles are combined from (value, epoch) pieces: every launch
+    # has its own epoch, so a piece left by an earlier launch never counts
+    import torch
+    from megatron_tensor_block_gb300.runtime import Model
+    inputs = synth.make_inputs(CASES["llama_shape_small_tp4_b3"])
+    m = Model(inputs)
+    ref = m.forward().clone()
+    for _ in range(200):
+        m.forward()
+    torch.cuda.synchronize()
+    assert m.ws.status() == 0
+    assert torch.equal(m.y, ref)
+
+
 def test_decode_position_past_capacity_is_reported(gpu_lib):
     import torch
     import megatron_tensor_block_gb300 as tb
