@@ -870,6 +870,34 @@ __device__ __forceinline__ int sk_share(int W, int min_r) {
     return r > min_r ? r : min_r;
 }
 
+// Attention keys of the one-launch step: CTAs 0..na-1 (those holding a QKV
+// tile) take ra keys each, the others -- idle during the QKV phase, when they
+// prefetch their keys into L2 -- take rb = ra * kIdleKeyNum / kIdleKeyDen
+// (rounded up). ra is at least min_r, so a
+// KV group of max_kv keys spans at most ceil(max_kv / min_r) + 1 CTAs.
+constexpr int kIdleKeyNum = 4, kIdleKeyDen = 3;     // an idle CTA's key share relative to a busy one's (measured best)
+struct KeySplit {
+    int ra, rb, na;
+};
+__device__ __forceinline__ KeySplit sk_key_split(int total, int min_r, int busy) {
+    KeySplit s;
+    s.na = busy > 0 && busy < (int)gridDim.x ? busy : (int)gridDim.x;
+    const long long units = (long long)s.na * kIdleKeyDen + (long long)((int)gridDim.x - s.na) * kIdleKeyNum;
+    s.ra = max((int)(((long long)total * kIdleKeyDen + units - 1) / units), min_r);
+    s.rb = s.na < (int)gridDim.x ? (s.ra * kIdleKeyNum + kIdleKeyDen - 1) / kIdleKeyDen : s.ra;
+    return s;
+}
+// First key of CTA c (c = gridDim.x gives the end), clipped to the key space.
+__device__ __forceinline__ int sk_key_start(const KeySplit& s, int c, int total) {
+    const long long k = c <= s.na ? (long long)c * s.ra : (long long)s.na * s.ra + (long long)(c - s.na) * s.rb;
+    return (int)min(k, (long long)total);
+}
+// CTA holding key k (k inside the key space).
+__device__ __forceinline__ int sk_key_cta(const KeySplit& s, int k) {
+    const long long ka = (long long)s.na * s.ra;
+    return k < ka ? k / s.ra : s.na + (int)((k - ka) / s.rb);
+}
+
 // Projection tiles ("segments"): column-parallel -- one 64-row tile of one
 // shard per group (decode_unit with one unit per group); row-parallel -- the
 // shards of 64-row output tile tb are segments tb*N .. tb*N + N-1. Each has
@@ -1046,9 +1074,9 @@ __device__ __forceinline__ void sk_keys_ready(SkKeys& K, const StepArgs& A) {
     pdl_wait();                                         // cache rows and positions of the preceding step
     for (int b = 0; b < kTMax; ++b) K.posv[b] = b < A.a.B ? A.a.pos[b] : 0;
     K.ks = sk_keyspace(A.a, K.posv);
-    const int R = sk_share(K.ks.total, step_min_keys(A.a.max_kv));
-    K.k0 = min((int)blockIdx.x * R, K.ks.total);
-    K.k1 = min(K.k0 + R, K.ks.total);
+    const KeySplit sp = sk_key_split(K.ks.total, step_min_keys(A.a.max_kv), A.a.key_busy);
+    K.k0 = sk_key_start(sp, (int)blockIdx.x, K.ks.total);
+    K.k1 = sk_key_start(sp, (int)blockIdx.x + 1, K.ks.total);
     K.ready = true;
 }
 
@@ -1147,6 +1175,23 @@ __device__ __forceinline__ bool sk_produce_attn(unsigned need, const StepArgs& A
     using S = AtShape<D>;
     const AttnDecodeParams& p = A.a;
     sk_keys_ready(keys, A);
+    if ((int)blockIdx.x >= p.key_busy && p.key_busy < (int)gridDim.x) {
+        // no QKV tile here: pull this CTA's K and V rows into L2 while the
+        // other CTAs run the QKV phase (its share of keys is the larger one)
+        for (int ke = keys.k1; ke > keys.k0;) {
+            const SkSeg g = sk_attn_segment(keys, p, ke);
+            const size_t rb = (size_t)D * sizeof(bf16);
+            const char* kb = static_cast<const char*>(p.kcache[g.r]) + (size_t)g.row0 * rb;
+            const char* vb = static_cast<const char*>(p.vcache[g.r]) + (size_t)g.row0 * rb;
+            const size_t n = (size_t)g.len * rb;
+            for (size_t o = 0; o < n; o += 32768) {
+                const uint32_t sz = (uint32_t)min((size_t)32768, n - o);
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(kb + o), "r"(sz) : "memory");
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vb + o), "r"(sz) : "memory");
+            }
+            ke = g.k;
+        }
+    }
     bool passed = false;
     uint32_t flush_at = pd.n > 0 ? pd.stage[0] + kSkRing : 0xffffffffu;
     uint32_t sl = it % kSkRing, par = ((it / kSkRing) & 1) ^ 1;
@@ -1772,8 +1817,8 @@ __device__ __forceinline__ void sk_seg_table(const AttnDecodeParams& p, SkSegInf
     for (int b = 0; b < kTMax; ++b) posv[b] = b < p.B ? p.pos[b] : 0;
     const KeySpace ks = sk_keyspace(p, posv);
     const int G = p.hq_s / p.hkv_s;
-    const int R = sk_share(ks.total, step_min_keys(p.max_kv));
-    const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
+    const KeySplit sp = sk_key_split(ks.total, step_min_keys(p.max_kv), p.key_busy);
+    const int k0 = sk_key_start(sp, (int)blockIdx.x, ks.total), k1 = sk_key_start(sp, (int)blockIdx.x + 1, ks.total);
     int n = 0;
     for (int ke = k1; ke > k0 && n <= kSegTab; ++n) {
         int gi, b, off, gstart;
@@ -1818,8 +1863,8 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
     const int q0 = 2 * t, q1 = 2 * t + 1;
     const int pstride = G * (D + 2);
     const KeySpace ks = sk_keyspace(p, s_pos);
-    const int R = sk_share(ks.total, step_min_keys(p.max_kv));
-    const int k0 = min((int)blockIdx.x * R, ks.total), k1 = min(k0 + R, ks.total);
+    const KeySplit sp = sk_key_split(ks.total, step_min_keys(p.max_kv), p.key_busy);
+    const int k0 = sk_key_start(sp, (int)blockIdx.x, ks.total), k1 = sk_key_start(sp, (int)blockIdx.x + 1, ks.total);
     // q of the CTA's first segments, scaled and rounded to bf16 once and staged
     // in shared memory: one round trip of loads for all of them instead of one
     // per segment (q was written by other CTAs in the QKV phase)
@@ -1959,7 +2004,7 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
 
         // ---- merge the eight warps: common max per query, every warp's rescaled
         // output into its slot, then all threads sum the slots in warp order
-        const int first = gstart / R, last = (gstart + len - 1) / R;
+        const int first = sk_key_cta(sp, gstart), last = sk_key_cta(sp, gstart + len - 1);
         const int nc = last - first + 1;
         // A KV group split over CTAs is combined by the CTA holding its last keys
         // (its block with the new position streams last, so it normally finishes
@@ -2366,6 +2411,12 @@ cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     A.a = P.a;
+    {
+        // CTAs holding a QKV tile: whole tiles, ceil(tiles / grid) per CTA
+        const int tiles = P.g[0].shape.groups, g = grid_sz[which];
+        const int per = (tiles + g - 1) / g;
+        A.a.key_busy = (tiles + per - 1) / per;
+    }
     A.np = P.np;
     const long rows = (long)P.a.max_batch * P.a.hkv_s * P.a.max_kv;
     for (int r = 0; r < P.a.N; ++r) {

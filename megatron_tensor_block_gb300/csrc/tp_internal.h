@@ -109,6 +109,8 @@ struct AttnDecodeParams {
     void* out;                         // [N][kTMax][Hq' d] storage type
     int* status;
     unsigned part_units;               // capacity of `part` in chunk partials
+    int key_busy;                      // one-launch step: CTAs 0..key_busy-1 hold a QKV tile (the rest take a
+                                       // larger attention key share, prefetched into L2 during QKV)
 };
 
 struct CopyDesc {
