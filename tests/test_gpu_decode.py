@@ -32,6 +32,10 @@ CASES = {
     # tp=1 degenerates to the unsharded block
     "llama_shape_tp1": synth.scaled(LLAMA, hidden=512, n_heads=8, n_kv_heads=2, ffn=1024, tp=1,
                                     batch=2, kv_len=40, seed=14),
+    # 160 QKV tiles, more than there are SMs: two per CTA on the first 80, so the key split gives the
+    # other CTAs the larger share; 8 query heads per KV head, 2 sequences, ragged last key block
+    "qkv_tiles_exceed_sms_tp4": synth.scaled(LLAMA, hidden=1024, n_heads=64, n_kv_heads=8, ffn=1024, tp=4,
+                                             batch=2, kv_len=100, seed=15),
 }
 
 
