@@ -409,9 +409,7 @@ def block_rows_tpN(shards, x, k_caches, v_caches, pos, S, cfg, N, rows):
 
 
 # ---------------------------------------------------------------------------
-# MoE feed-forward block with expert slicing ("Multi-GPU & Multi-Node",
-# Supported architectures: each shard holds 1/tp of every expert, the router
-# is replicated)
+# logits over the vocab-parallel head
 # ---------------------------------------------------------------------------
 
 
@@ -431,6 +429,13 @@ def lm_head_logits_tpN(h: np.ndarray, gamma: np.ndarray, head_shards: list, org_
     the head) are dropped, as the vocab-parallel gather drops its rows."""
     n = rmsnorm(h, gamma, eps)
     return np.concatenate([n @ Wr.T for Wr in head_shards], axis=1)[:, :org_vocab]
+
+
+# ---------------------------------------------------------------------------
+# MoE feed-forward block ("Multi-GPU & Multi-Node", Supported architectures:
+# the router is replicated; experts are either sliced -- each shard holds 1/tp
+# of every expert -- or placed whole, 1/tp of the experts per shard)
+# ---------------------------------------------------------------------------
 
 
 def router_topk(logits: np.ndarray, k: int):
@@ -509,6 +514,53 @@ def moe_ffn_tpN(shards, gammas, x, logits, eps, k, N):
             acc = acc + w[:, j:j + 1] * c
         partials.append(acc)
     return x + reduce_rank_order(partials)
+
+
+def shard_experts_ep(e_gate, e_up, e_down, N):
+    """Expert parallelism: shard r holds the whole experts
+    ``[r*E/N, (r+1)*E/N)``, fused as ``egu_r [E/N, 2Fe, H]`` (gate rows then up
+    rows) and ``ed_r [E/N, H, Fe]``; ``first`` is its first expert id. E must
+    divide by N (the pages' divisibility rule, Requirements & constraints)."""
+    E = e_gate.shape[0]
+    if E % N:
+        raise ValueError(f"{E} experts do not divide over {N} shards")
+    per = E // N
+    out = []
+    for r in range(N):
+        sl = slice(r * per, (r + 1) * per)
+        out.append({"egu": np.concatenate([e_gate[sl], e_up[sl]], axis=1), "ed": e_down[sl].copy(),
+                    "first": r * per})
+    return out
+
+
+def moe_ffn_ep_partials(shards, gammas, x, logits, eps, k):
+    """Per-shard partials of the expert-parallel MoE FFN: shard r sums, over the
+    choices j in order, ``w_tj * SwiGLU_e(RMSNorm_r(x)_t)`` for the chosen
+    experts e it holds; a choice held elsewhere adds nothing on shard r."""
+    ids, w = router_topk(logits, k)
+    partials = []
+    for r, sh in enumerate(shards):
+        egu, ed, e0 = sh["egu"], sh["ed"], sh["first"]
+        per, Fe = egu.shape[0], ed.shape[2]
+        n = rmsnorm(x, gammas[r], eps)
+        acc = np.zeros_like(x)
+        for j in range(k):
+            c = np.zeros_like(x)
+            for e in np.unique(ids[:, j]):
+                if not e0 <= e < e0 + per:
+                    continue
+                t = np.nonzero(ids[:, j] == e)[0]
+                gu = n[t] @ egu[e - e0].T
+                c[t] = (silu(gu[:, :Fe]) * gu[:, Fe:]) @ ed[e - e0].T
+            acc = acc + w[:, j:j + 1] * c
+        partials.append(acc)
+    return partials
+
+
+def moe_ffn_ep_tpN(shards, gammas, x, logits, eps, k):
+    """Expert-parallel MoE FFN: the shards' partials reduced in rank order and
+    added to ``x`` -- the same reduce point as expert slicing."""
+    return x + reduce_rank_order(moe_ffn_ep_partials(shards, gammas, x, logits, eps, k))
 
 
 # ---------------------------------------------------------------------------

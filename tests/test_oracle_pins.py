@@ -510,6 +510,56 @@ def test_moe_matches_dense_per_token_loop():
         assert np.allclose(y[t], x[t] + acc, rtol=1e-13, atol=1e-13)
 
 
+# ---- MoE with expert parallelism (whole experts per shard) ------------------------
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 6])
+def test_moe_ep_equals_tp1(N):
+    # whole experts placed on shards, partials reduced in rank order: the
+    # unsharded MoE block up to rounding
+    x, g, eg, eu, ed, logits = _moe_inputs(130 + N)
+    ref = O.moe_ffn_tp1(x, g, eg, eu, ed, logits, 1e-5, 4)
+    got = O.moe_ffn_ep_tpN(O.shard_experts_ep(eg, eu, ed, N), [g] * N, x, logits, 1e-5, 4)
+    assert O.relerr(got, ref) < 1e-13
+
+
+def test_moe_ep_equals_expert_slicing():
+    x, g, eg, eu, ed, logits = _moe_inputs(140)
+    ep = O.moe_ffn_ep_tpN(O.shard_experts_ep(eg, eu, ed, 2), [g] * 2, x, logits, 1e-5, 3)
+    sl = O.moe_ffn_tpN(O.shard_experts(eg, eu, ed, 2), [g] * 2, x, logits, 1e-5, 3, 2)
+    assert O.relerr(ep, sl) < 1e-13
+
+
+def test_moe_ep_partials_stay_on_the_owner():
+    # every token picks experts 0 and 1, both on shard 0 of 3: the other
+    # shards add exactly nothing, and shard 0's partial is the whole MoE term
+    x, g, eg, eu, ed, logits = _moe_inputs(141)
+    logits[:, :2] += 40.0
+    parts = O.moe_ffn_ep_partials(O.shard_experts_ep(eg, eu, ed, 3), [g] * 3, x, logits, 1e-5, 2)
+    assert not parts[1].any() and not parts[2].any()
+    ref = O.moe_ffn_tp1(x, g, eg, eu, ed, logits, 1e-5, 2) - x
+    assert O.relerr(parts[0], ref) < 1e-13
+    # and a choice of shard 2's expert lands on shard 2 only
+    logits[0, 5] += 200.0
+    parts = O.moe_ffn_ep_partials(O.shard_experts_ep(eg, eu, ed, 3), [g] * 3, x, logits, 1e-5, 2)
+    assert not parts[1].any() and parts[2][0].any() and not parts[2][1:].any()
+
+
+def test_moe_ep_shards_regroup_to_the_experts():
+    _, _, eg, eu, ed, _ = _moe_inputs(142)
+    sh = O.shard_experts_ep(eg, eu, ed, 3)
+    assert [s["first"] for s in sh] == [0, 2, 4]
+    egu = np.concatenate([s["egu"] for s in sh])
+    assert np.array_equal(egu[:, :8], eg) and np.array_equal(egu[:, 8:], eu)
+    assert np.array_equal(np.concatenate([s["ed"] for s in sh]), ed)
+
+
+def test_moe_ep_rejects_indivisible_expert_count():
+    _, _, eg, eu, ed, _ = _moe_inputs(143)
+    with pytest.raises(ValueError):
+        O.shard_experts_ep(eg, eu, ed, 4)
+
+
 # ---- lens / logits over the vocab-parallel head ---------------------------------
 
 
