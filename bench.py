@@ -47,10 +47,11 @@ METRICS = {
     "decode": METRIC,
     "prefill": "TP-block prefill tokens/s + bf16 tensor TFLOP/s (% of dense peak) on 1 GB300",
     "moe": "MoE expert-sliced FFN tokens/s + HBM GB/s on 1 GB300",
+    "moe_ep": "MoE expert-parallel FFN tokens/s + HBM GB/s on 1 GB300",
 }
 DEFAULT_WORKLOAD = "llama3_8b_decode_tp4"
 WORKLOAD_KIND = {"llama3_8b_decode_tp4": "decode", "qwen25_05b_decode_tp2": "decode",
-                 "llama3_8b_prefill_tp8": "prefill", "moe_expert_slice_tp4": "moe"}
+                 "llama3_8b_prefill_tp8": "prefill", "moe_expert_slice_tp4": "moe", "moe_expert_parallel_tp4": "moe"}
 STAGES = {
     "decode": ["qkv_rope", "attention", "o_proj_reduce", "gate_up_swiglu", "down_reduce"],
     "prefill": ["qkv_rope", "attention", "o_proj_reduce", "gate_up_swiglu", "down_reduce"],
@@ -236,7 +237,8 @@ class OracleLeg:
         self.i = 0
         if self.kind == "moe":
             eg, eu, ed = (O.to_f64(inputs[k]) for k in ("e_gate", "e_up", "e_down"))
-            self.shards = O.shard_experts(eg, eu, ed, w.tp)
+            self.ep = bool(w.expert_parallel)
+            self.shards = (O.shard_experts_ep if self.ep else O.shard_experts)(eg, eu, ed, w.tp)
             self.gammas = [O.to_f64(inputs["gamma_ffn"])] * w.tp
             self.x = np.asarray(inputs["x"], dtype=np.float64)
             self.chunk = 16
@@ -256,7 +258,7 @@ class OracleLeg:
     def describe(self) -> str:
         if self.kind == "moe":
             return (f"{self.chunk}-token slices of the {self.w.tokens} routed tokens through the float64 numpy "
-                    f"oracle's expert-sliced MoE block (tp={self.w.tp})")
+                    f"oracle's {'expert-parallel' if self.ep else 'expert-sliced'} MoE block (tp={self.w.tp})")
         if self.kind == "prefill":
             return (f"the first {self.chunk} prompt tokens (positions 0..{self.chunk - 1}) of one sequence through "
                     f"the float64 numpy oracle's sharded block (tp={self.w.tp}), repeated; the full workload is "
@@ -270,8 +272,12 @@ class OracleLeg:
             t0 = (self.i * self.chunk) % w.tokens
             self.i += 1
             sl = slice(t0, t0 + self.chunk)
-            O.moe_ffn_tpN(self.shards, self.gammas, self.x[sl], self.inputs["router_logits"][sl], w.eps, w.top_k,
-                          w.tp)
+            if self.ep:
+                O.moe_ffn_ep_tpN(self.shards, self.gammas, self.x[sl], self.inputs["router_logits"][sl], w.eps,
+                                 w.top_k)
+            else:
+                O.moe_ffn_tpN(self.shards, self.gammas, self.x[sl], self.inputs["router_logits"][sl], w.eps,
+                              w.top_k, w.tp)
             return self.chunk
         if self.kind == "prefill":
             x = self.x[:self.chunk]
@@ -368,7 +374,7 @@ def run_reference(args, world, rank):
     value = tok / el
     cores = int(os.environ["OMP_NUM_THREADS"])
     sample = (f"each step is {leg.describe()}; {n} of {args.steps} requested steps fit the {budget:.0f} s bound")
-    line = {"impl": "reference", "metric": METRICS[kind], "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": METRICS["moe_ep" if getattr(w, "expert_parallel", 0) else kind], "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": n, "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(n, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w),
@@ -629,7 +635,7 @@ def run_ours(args, world, rank, local):
                    "launch": f"CUDA graph of {per} forwards (programmatic dependent launch between them), "
                              f"replayed; a one-forward graph for a remainder"})
     line = {
-        "metric": METRICS[kind], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRICS["moe_ep" if getattr(w, "expert_parallel", 0) else kind], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config,

@@ -99,6 +99,10 @@ typedef struct tp_model_desc {
     int64_t max_batch;     /* sequences per call */
     int64_t max_tokens;    /* B * T_per_seq per call */
     int64_t max_kv;        /* KV cache capacity (positions) per sequence */
+    int32_t expert_parallel; /* MoE sharding: 0 expert slicing (every shard holds 1/tp of every expert's
+                              * FFN width), 1 expert parallelism (shard r holds the whole experts
+                              * [r*E/tp, (r+1)*E/tp); E must divide by tp) */
+    int32_t reserved0;       /* must be 0 */
 } tp_model_desc;
 
 typedef struct tp_plan_s* tp_plan_t;
@@ -110,7 +114,7 @@ typedef struct tp_plan_info {
     int64_t hq_shard;            /* Hq' = Hq/tp */
     int64_t hkv_shard;           /* Hkv' */
     int64_t ffn_shard;           /* F' */
-    int64_t expert_ffn_shard;    /* Fe' */
+    int64_t expert_ffn_shard;    /* Fe' (Fe/tp when sliced, Fe with expert parallelism) */
     int64_t qkv_rows;            /* (Hq' + 2 Hkv') d */
     int64_t vocab_padded;        /* org_vocab rounded up to a multiple of 64*tp */
     int64_t vocab_rows_shard;    /* vocab_padded / tp */
@@ -125,6 +129,7 @@ typedef struct tp_plan_info {
      * after a MOE_FFN call): chosen expert ids int32 [T*top_k], bucket starts
      * int32 [E+1], slot -> choice index int32 [T*top_k]. -1 without experts. */
     int64_t moe_ids_offset, moe_bucket_offset, moe_perm_offset;
+    int64_t experts_shard;       /* experts held per shard: E sliced, E/tp with expert parallelism */
 } tp_plan_info;
 
 /* Full (unsharded) block weights, caller-owned device memory. */

@@ -43,7 +43,7 @@ class tp_model_desc(C.Structure):
                 ("top_k", C.c_int64), ("expert_ffn", C.c_int64), ("org_vocab", C.c_int64),
                 ("eps", C.c_double), ("rope_theta", C.c_double), ("dtype", C.c_int32),
                 ("has_qkv_bias", C.c_int32), ("max_batch", C.c_int64), ("max_tokens", C.c_int64),
-                ("max_kv", C.c_int64)]
+                ("max_kv", C.c_int64), ("expert_parallel", C.c_int32), ("reserved0", C.c_int32)]
 
 
 class tp_plan_info(C.Structure):
@@ -53,7 +53,7 @@ class tp_plan_info(C.Structure):
             "vocab_rows_shard", "wqkv_bytes", "bqkv_bytes", "wo_bytes", "wgu_bytes", "wd_bytes",
             "gamma_bytes", "egu_bytes", "ed_bytes", "kv_cache_bytes", "lm_head_bytes", "workspace_bytes",
             "weight_bytes_shard", "weight_bytes_total", "moe_ids_offset", "moe_bucket_offset",
-            "moe_perm_offset")]
+            "moe_perm_offset", "experts_shard")]
 
 
 class tp_block_weights(C.Structure):

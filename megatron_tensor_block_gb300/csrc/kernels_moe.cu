@@ -1,16 +1,18 @@
-// Expert-sliced MoE feed-forward block ("Multi-GPU & Multi-Node", Supported
-// architectures: each shard holds 1/tp of every expert's weights and the
-// router is replicated, so the load stays balanced whichever experts a token
-// picks). Decode-sized token counts, bf16 weights, fp32 accumulation.
+// MoE feed-forward block ("Multi-GPU & Multi-Node", Supported architectures:
+// the router is replicated; each shard holds 1/tp of every expert's weights --
+// expert slicing, balanced whichever experts a token picks -- or, with expert
+// parallelism, 1/tp of the experts whole). Decode-sized token counts, bf16
+// weights, fp32 accumulation.
 //
 //   route   : softmax top-k per token (chosen by logit, ties to the lower id),
 //             weights renormalised over the chosen experts
 //   bucket  : stable counting sort of the (token, choice) slots by expert
 //   prep    : x_t * gamma_r (bf16) for every slot and shard, 1/rms per slot
-//   gate/up : per shard and expert, streaming grouped GEMM over the expert's
-//             slots, SwiGLU epilogue
-//   down    : per shard and expert, streaming grouped GEMM -> slot outputs
-//   combine : y_t = x_t + sum_r ( sum_j w_tj * o[r][slot(t, j)] ), j then r
+//   gate/up : per shard and expert it holds, streaming grouped GEMM over the
+//             expert's slots, SwiGLU epilogue
+//   down    : per shard and expert it holds, streaming grouped GEMM -> slot outputs
+//   combine : y_t = x_t + sum_r ( sum_j w_tj * o[r][slot(t, j)] ), j then r; with
+//             expert parallelism shard r's sum keeps the choices of its experts
 #include <cuda.h>
 
 #include <cstring>
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     const int spu = (K + kBoxK - 1) / kBoxK;
     const int TG = (down && spu == 1) ? kMoeTG : 1;     // tiles per unit sharing the activation boxes
     const int ngrp = (tiles + TG - 1) / TG;
-    const int U = p.N * p.E * ngrp;
+    const int U = p.N * p.El * ngrp;                   // units: (shard, expert it holds, tile group)
 
     if (warp == kConsumers / 32) {                     // ---- producer
         if (lane == 0) {
@@ -226,7 +228,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                 set_status(p.status, TP_ERR_ALIGN);
             }
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const int tg = u % ngrp, e = (u / ngrp) % p.E, r = u / (ngrp * p.E);
+                const int tg = u % ngrp, le = (u / ngrp) % p.El, r = u / (ngrp * p.El);
+                const int e = p.ep ? r * p.El + le : le;     // global expert id (slot buckets)
                 const int ntg = min(TG, tiles - tg * TG);
                 const int off = p.offsets[e], cnt = p.offsets[e + 1] - off;
                 for (int ps = 0; ps < cnt && ok; ps += kMoeTokPass) {
@@ -235,10 +238,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                         const int tb = tg * TG + i;
                         int rowa, rowb;
                         if (down) {
-                            rowa = e * p.H + tb * kTileRows;
+                            rowa = le * p.H + tb * kTileRows;
                             rowb = rowa + 32;
                         } else {
-                            rowa = e * 2 * p.Fs + tb * 32;
+                            rowa = le * 2 * p.Fs + tb * 32;
                             rowb = rowa + p.Fs;
                         }
                         const int nx = (TG == 1 || i == 0) ? ng : 0;    // activation boxes of this stage
@@ -274,7 +277,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     const int box = wm >> 1, brow = 16 * (wm & 1) + g;
     uint32_t it = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int tg = u % ngrp, e = (u / ngrp) % p.E, r = u / (ngrp * p.E);
+        const int tg = u % ngrp, le = (u / ngrp) % p.El, r = u / (ngrp * p.El);
+        const int e = p.ep ? r * p.El + le : le;
         const int ntg = min(TG, tiles - tg * TG);
         const int off = s_off[e], cnt = s_off[e + 1] - off;
         for (int ps = 0; ps < cnt; ps += kMoeTokPass) {
@@ -395,6 +399,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < p.top_k; ++j) {
                 const int f = t * p.top_k + j;
+                if (p.ep && p.ids[f] / p.El != r) continue;   // that expert lives on another shard
                 const float w = p.wts[f];
                 const float4 v = *reinterpret_cast<const float4*>(p.o + ((size_t)r * nslot + p.slot_of[f]) * p.H + h);
                 acc.x = fmaf(w, v.x, acc.x);
@@ -454,12 +459,12 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         A.down = down;
         for (int r = 0; r < p.N; ++r) {
             if (down) {
-                e = step_stage_map(p.ed[r], p.Fs, p.E * p.H, 32, &A.tw[r]);
+                e = step_stage_map(p.ed[r], p.Fs, p.El * p.H, 32, &A.tw[r]);
                 if (e == cudaSuccess)
                     e = step_stage_map(static_cast<const bf16*>(p.act) + (size_t)r * nslot * p.Fs, p.Fs, (int)nslot, 8,
                                        &A.tx[r]);
             } else {
-                e = step_stage_map(p.egu[r], p.H, p.E * 2 * p.Fs, 32, &A.tw[r]);
+                e = step_stage_map(p.egu[r], p.H, p.El * 2 * p.Fs, 32, &A.tw[r]);
                 if (e == cudaSuccess)
                     e = step_stage_map(static_cast<const bf16*>(p.xs) + (size_t)(q.xs_copies > 1 ? r : 0) * nslot * p.H,
                                        p.H, (int)nslot, 8, &A.tx[r]);
@@ -468,7 +473,7 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         }
         const int tiles = down ? p.H / kTileRows : 2 * p.Fs / kTileRows;
         const int TG = (down && (p.Fs + kBoxK - 1) / kBoxK == 1) ? kMoeTG : 1;
-        const int U = p.N * p.E * ((tiles + TG - 1) / TG);
+        const int U = p.N * p.El * ((tiles + TG - 1) / TG);
         void* args[] = {&A};
         e = launch_pdl(reinterpret_cast<const void*>(moe_gemm_kernel), args, U < kSMs ? U : kSMs, smem, s,
                        kStreamThreads);

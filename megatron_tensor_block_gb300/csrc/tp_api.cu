@@ -169,10 +169,17 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         if (d->ffn % tp)
             return fail(TP_ERR_INDIVISIBLE, "tp_plan: ffn=%lld not divisible by tp=%d", (long long)d->ffn, tp);
     }
+    if (d->reserved0 != 0) return fail(TP_ERR_INVALID_ARG, "tp_plan: reserved0 must be 0");
+    if (!moe && d->expert_parallel) return fail(TP_ERR_INVALID_ARG, "tp_plan: expert_parallel without experts");
     if (moe) {
         if (d->top_k < 1 || d->top_k > d->n_experts || d->expert_ffn <= 0)
             return fail(TP_ERR_INVALID_ARG, "tp_plan: need 1 <= top_k <= n_experts and expert_ffn > 0");
-        if (d->expert_ffn % tp)
+        if (d->expert_parallel != 0 && d->expert_parallel != 1)
+            return fail(TP_ERR_INVALID_ARG, "tp_plan: expert_parallel must be 0 or 1");
+        if (d->expert_parallel && d->n_experts % tp)
+            return fail(TP_ERR_INDIVISIBLE, "tp_plan: n_experts=%lld not divisible by tp=%d (expert parallelism)",
+                        (long long)d->n_experts, tp);
+        if (!d->expert_parallel && d->expert_ffn % tp)
             return fail(TP_ERR_INDIVISIBLE, "tp_plan: expert_ffn=%lld not divisible by tp=%d", (long long)d->expert_ffn, tp);
     }
     // ranges the kernels handle
@@ -184,8 +191,8 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         if (d->n_heads / d->n_kv_heads > 8)
             return fail(TP_ERR_UNSUPPORTED, "tp_plan: more than 8 query heads per KV head");
     }
-    if (moe && (d->expert_ffn / tp) % 64)
-        return fail(TP_ERR_UNSUPPORTED, "tp_plan: expert_ffn/tp must be a multiple of 64");
+    if (moe && (d->expert_ffn / (d->expert_parallel ? 1 : tp)) % 64)
+        return fail(TP_ERR_UNSUPPORTED, "tp_plan: the expert FFN width per shard must be a multiple of 64");
     if (moe && (d->n_experts > 64 || d->top_k > 8))
         return fail(TP_ERR_UNSUPPORTED, "tp_plan: MoE supports up to 64 experts and top_k <= 8");
 
@@ -214,9 +221,10 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
     }
     I.gamma_bytes = H * 4;
     if (moe) {
-        I.expert_ffn_shard = d->expert_ffn / N;
-        I.egu_bytes = d->n_experts * 2 * I.expert_ffn_shard * H * esz;
-        I.ed_bytes = d->n_experts * H * I.expert_ffn_shard * esz;
+        I.expert_ffn_shard = d->expert_parallel ? d->expert_ffn : d->expert_ffn / N;
+        I.experts_shard = d->expert_parallel ? d->n_experts / N : d->n_experts;
+        I.egu_bytes = I.experts_shard * 2 * I.expert_ffn_shard * H * esz;
+        I.ed_bytes = I.experts_shard * H * I.expert_ffn_shard * esz;
     }
     if (d->org_vocab > 0) {
         const int64_t m = 64 * N;
@@ -452,7 +460,15 @@ extern "C" tp_status tp_shard_weights(tp_plan_t plan, const tp_block_weights* fu
         if (!full->e_gate || !full->e_up || !full->e_down)
             return fail(TP_ERR_NULL, "tp_shard_weights: expert weight pointer is NULL");
         const int64_t E = d.n_experts, Fe = d.expert_ffn, Fs = I.expert_ffn_shard, row = H * es;
-        for (int r = 0; r < N; ++r) {
+        for (int r = 0; r < N && d.expert_parallel; ++r) {
+            if (!out->egu[r] || !out->ed[r]) return fail(TP_ERR_NULL, "tp_shard_weights: shard %d expert buffer is NULL", r);
+            // whole experts [r*E/N, (r+1)*E/N): gate rows then up rows of each -> [E/N][2Fe][H], down -> [E/N][H][Fe]
+            const int64_t per = I.experts_shard, e0 = r * per;
+            B.add(cptr(full->e_gate, e0 * Fe * row), mptr(out->egu[r], 0), per, Fe * row, Fe * row, 2 * Fe * row);
+            B.add(cptr(full->e_up, e0 * Fe * row), mptr(out->egu[r], Fe * row), per, Fe * row, Fe * row, 2 * Fe * row);
+            B.add(cptr(full->e_down, e0 * H * Fe * es), out->ed[r], per * H, Fe * es, Fe * es, Fe * es);
+        }
+        for (int r = 0; r < N && !d.expert_parallel; ++r) {
             if (!out->egu[r] || !out->ed[r]) return fail(TP_ERR_NULL, "tp_shard_weights: shard %d expert buffer is NULL", r);
             // every expert: gate rows and up rows [r*Fe', (r+1)*Fe') -> [E][2Fe'][H]
             B.add(cptr(full->e_gate, r * Fs * row), mptr(out->egu[r], 0), E, Fs * row, Fe * row, 2 * Fs * row);
@@ -899,6 +915,8 @@ static tp_status forward_moe(tp_plan_t P, const tp_shard_set* w, const float* x,
     m.E = (int)d.n_experts;
     m.top_k = (int)d.top_k;
     m.Fs = (int)P->info.expert_ffn_shard;
+    m.El = (int)P->info.experts_shard;
+    m.ep = d.expert_parallel;
     m.eps = (float)d.eps;
     m.x = x;
     m.logits = logits;

@@ -130,12 +130,14 @@ struct CopyBatch {
 // Expert-sliced MoE feed-forward block (bf16), slots = (token, choice) pairs.
 struct MoeParams {
     int N, T, H, E, top_k, Fs;             // Fs: expert FFN width per shard
+    int El, ep;                            // experts per shard (E, or E/N with expert parallelism); ep: 1 when
+                                           // shard r holds the whole experts [r*El, (r+1)*El)
     float eps;
     const float* x;                        // [T][H]
     const float* logits;                   // [T][E]
     const float* gamma[TP_MAX_SHARDS];     // [H] per shard
-    const void* egu[TP_MAX_SHARDS];        // [E][2Fs][H]: gate rows then up rows per expert
-    const void* ed[TP_MAX_SHARDS];         // [E][H][Fs]
+    const void* egu[TP_MAX_SHARDS];        // [El][2Fs][H]: gate rows then up rows per expert
+    const void* ed[TP_MAX_SHARDS];         // [El][H][Fs]
     int* ids;                              // [T*k] chosen experts, descending logit
     float* wts;                            // [T*k] renormalised routing weights
     int* offsets;                          // [E+1] bucket starts (slot order)

@@ -28,7 +28,8 @@ def desc_of(w, max_kv: int | None = None, max_batch: int | None = None, max_toke
                 n_experts=w.n_experts, top_k=w.top_k, expert_ffn=w.expert_ffn, org_vocab=w.org_vocab,
                 eps=w.eps, rope_theta=w.rope_theta, dtype=B.TP_BF16 if w.dtype == "bf16" else B.TP_F32,
                 has_qkv_bias=int(w.qkv_bias), max_batch=max_batch or w.batch,
-                max_tokens=max_tokens or w.tokens, max_kv=max_kv or max(w.max_kv, 1))
+                max_tokens=max_tokens or w.tokens, max_kv=max_kv or max(w.max_kv, 1),
+                expert_parallel=int(getattr(w, "expert_parallel", 0)))
 
 
 class Workspace:

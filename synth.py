@@ -50,6 +50,7 @@ class Workload:
     n_experts: int = 0
     top_k: int = 0
     expert_ffn: int = 0
+    expert_parallel: int = 0  # MoE sharding: 0 expert slicing, 1 whole experts per shard
     mode: str = "decode"      # decode | prefill | moe_ffn
 
     @property
@@ -90,6 +91,12 @@ WORKLOADS = {
         head_dim=0, ffn=0, eps=1e-5, rope_theta=0.0, dtype=BF16, tp=4,
         batch=256, tokens_per_seq=1, kv_len=0, seed=4, n_experts=64, top_k=4,
         expert_ffn=1024, mode="moe_ffn"),
+    # The same MoE block with expert parallelism: 16 whole experts per shard.
+    "moe_expert_parallel_tp4": Workload(
+        name="moe_expert_parallel_tp4", hidden=2048, n_heads=0, n_kv_heads=0,
+        head_dim=0, ffn=0, eps=1e-5, rope_theta=0.0, dtype=BF16, tp=4,
+        batch=256, tokens_per_seq=1, kv_len=0, seed=4, n_experts=64, top_k=4,
+        expert_ffn=1024, expert_parallel=1, mode="moe_ffn"),
 }
 
 

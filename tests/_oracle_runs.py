@@ -46,6 +46,9 @@ def moe_tpN(inputs: dict):
     N = w.tp
     eg, eu, ed = (O.to_f64(inputs[k]) for k in ("e_gate", "e_up", "e_down"))
     g = O.to_f64(inputs["gamma_ffn"])
+    x = np.asarray(inputs["x"], dtype=np.float64)
+    if getattr(w, "expert_parallel", 0):                 # whole experts per shard
+        return O.moe_ffn_ep_tpN(O.shard_experts_ep(eg, eu, ed, N), [g] * N, x, inputs["router_logits"], w.eps,
+                                w.top_k)
     shards = O.shard_experts(eg, eu, ed, N)
-    return O.moe_ffn_tpN(shards, [g] * N, np.asarray(inputs["x"], dtype=np.float64),
-                         inputs["router_logits"], w.eps, w.top_k, N)
+    return O.moe_ffn_tpN(shards, [g] * N, x, inputs["router_logits"], w.eps, w.top_k, N)

@@ -101,7 +101,24 @@ def test_plan_rejects_invalid_inputs_with_clear_errors():
     m = desc_of(synth.WORKLOADS["moe_expert_slice_tp4"])
     assert _status(dict(m, top_k=65), 4) == B.TP_ERR_INVALID_ARG
     assert _status(dict(m, expert_ffn=1022), 4) == B.TP_ERR_INDIVISIBLE
+    # expert parallelism: whole experts per shard, so the expert count must divide
+    assert _status(dict(m, expert_parallel=1, n_experts=62), 4) == B.TP_ERR_INDIVISIBLE
+    assert _status(dict(m, expert_parallel=2), 4) == B.TP_ERR_INVALID_ARG
+    assert _status(dict(d, expert_parallel=1), 2) == B.TP_ERR_INVALID_ARG      # no experts
+    assert _status(dict(m, reserved0=1), 4) == B.TP_ERR_INVALID_ARG
     assert _status(d, 2) == 0 and tb.tp_last_error() == ""
+
+
+def test_expert_parallel_plan_holds_whole_experts():
+    # the same bytes per shard as expert slicing: E/N whole experts instead of
+    # 1/N of every expert
+    m = desc_of(synth.WORKLOADS["moe_expert_slice_tp4"])
+    sl = tb.tp_plan_get_info(tb.tp_plan(m, 4))
+    ep = tb.tp_plan_get_info(tb.tp_plan(dict(m, expert_parallel=1), 4))
+    assert (sl["experts_shard"], sl["expert_ffn_shard"]) == (64, 256)
+    assert (ep["experts_shard"], ep["expert_ffn_shard"]) == (16, 1024)
+    assert ep["egu_bytes"] == sl["egu_bytes"] == 16 * 2 * 1024 * 2048 * 2
+    assert ep["ed_bytes"] == sl["ed_bytes"]
 
 
 def test_describe_reports_one_nth_of_the_weights():

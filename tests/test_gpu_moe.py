@@ -1,4 +1,5 @@
-"""Expert-sliced MoE feed-forward block: the CUDA path against the oracle.
+"""MoE feed-forward block, expert slicing and expert parallelism (whole
+experts per shard): the CUDA path against the oracle.
 
 Routing and bucketing are integer results and must match bit for bit (the
 top-k choice is made on the given float32 logits on both sides); the block
@@ -32,6 +33,16 @@ CASES = {
         synth.scaled(MOE, hidden=512, n_experts=16, top_k=2, expert_ffn=512, tp=2, batch=90, seed=41), 5),
     "moe_small_tp1_top1": lambda: synth.make_inputs(
         synth.scaled(MOE, hidden=256, n_experts=8, top_k=1, expert_ffn=256, tp=1, batch=9, seed=42)),
+    # expert parallelism: the full-size shape with 16 whole experts per shard
+    "moe_ep_tp4": lambda: synth.make_inputs(synth.scaled(MOE, expert_parallel=1, seed=43)),
+    # expert parallelism with most tokens on expert 3 (shard 0) and the last expert never chosen
+    "moe_ep_small_tp2_skewed_ragged": lambda: _skewed(
+        synth.scaled(MOE, hidden=512, n_experts=16, top_k=2, expert_ffn=512, tp=2, batch=90, seed=44,
+                     expert_parallel=1), 6),
+    # expert parallelism over 8 shards, 2 experts each
+    "moe_ep_tp8": lambda: synth.make_inputs(
+        synth.scaled(MOE, hidden=512, n_experts=16, top_k=4, expert_ffn=256, tp=8, batch=33, seed=45,
+                     expert_parallel=1)),
 }
 
 
