@@ -15,8 +15,9 @@
  *        org_vocab_size, fused rows grouped by rank, gathered tensor is a
  *        copy).
  *  [MG]  "Multi-GPU & Multi-Node": How tensor parallelism works (steps 1-3,
- *        replicated norms), Supported architectures (expert slicing with a
- *        replicated router), Requirements & constraints (divisibility).
+ *        replicated norms), Supported architectures (expert slicing, or
+ *        expert parallelism, with a replicated router), Requirements &
+ *        constraints (divisibility).
  *
  * Conventions for every call:
  *  - All tensor arguments are plain pointers to DEVICE memory on the current
@@ -65,7 +66,7 @@ typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
 typedef enum tp_mode {
     TP_MODE_DECODE = 0,   /* one new token per sequence at pos[b] */
     TP_MODE_PREFILL = 1,  /* T_per_seq new tokens per sequence at pos[b].. (causal) */
-    TP_MODE_MOE_FFN = 2   /* feed-forward half only, expert-sliced MoE */
+    TP_MODE_MOE_FFN = 2   /* feed-forward half only, MoE (sliced or expert-parallel, per the plan) */
 } tp_mode;
 
 /* Kinds of sharded parameter ([GA] Change): which dim is split and how the
@@ -160,8 +161,10 @@ typedef struct tp_shard_set {
     void* wd[TP_MAX_SHARDS];          /* [H, F']: columns r*F'.. of down_proj */
     float* gamma_attn[TP_MAX_SHARDS]; /* [H] replicated copy */
     float* gamma_ffn[TP_MAX_SHARDS];  /* [H] replicated copy */
-    void* egu[TP_MAX_SHARDS];         /* [E, 2Fe', H]: per expert gate_r then up_r rows */
-    void* ed[TP_MAX_SHARDS];          /* [E, H, Fe']: per expert columns r*Fe'.. of down */
+    void* egu[TP_MAX_SHARDS];         /* [E, 2Fe', H]: per expert gate_r then up_r rows; expert
+                                       * parallel: [E/tp, 2Fe, H], experts r*E/tp.. whole */
+    void* ed[TP_MAX_SHARDS];          /* [E, H, Fe']: per expert columns r*Fe'.. of down; expert
+                                       * parallel: [E/tp, H, Fe] */
 } tp_shard_set;
 
 /* Per-shard KV caches: shard r owns KV heads [r Hkv', (r+1) Hkv').
@@ -202,7 +205,8 @@ tp_status tp_plan_describe(tp_plan_t plan, char* buf, size_t n);
 /* Builds every shard's tensors from the full block weights ([MG] How tensor
  * parallelism works: QKV and gate/up split their output dim, o_proj and
  * down_proj their input dim; norms replicated; [MG] Supported architectures:
- * each shard holds 1/tp of every expert). Bit-exact copies, asynchronous on
+ * each shard holds 1/tp of every expert, or with expert_parallel the whole
+ * experts r*E/tp .. (r+1)*E/tp - 1). Bit-exact copies, asynchronous on
  * `stream`. Pointers in `full` that the block does not use may be NULL.
  * Errors: TP_ERR_NULL, TP_ERR_ALIGN (matrix pointers must be 16-byte
  * aligned), TP_ERR_UNSUPPORTED, TP_ERR_CUDA. */
@@ -262,6 +266,8 @@ tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t bytes, void*
  *   MOE_FFN: y = x + sum_r sum_j w_tj SwiGLU_{e_tj, r}(RMSNorm(x)_t), with
  *     softmax top-k routing of `router_logits` ([T, E] float32), ties to the
  *     lower expert id, weights renormalised; j-order then rank-order sums.
+ *     With expert_parallel, SwiGLU_{e, r} is the whole expert e on the shard
+ *     holding it and 0 on the others.
  * x and y are float32 [B*T_per_seq, H], rows sequence-major, y != x. pos is
  * DEVICE int32 [B]. `workspace` holds `workspace_bytes` >= the plan's
  * workspace_bytes and was set up by tp_workspace_init. Results are
