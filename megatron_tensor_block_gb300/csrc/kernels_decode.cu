@@ -792,12 +792,15 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, int dtype, cudaStream_
 // separated by five grid barriers (a monotonic arrival counter in the
 // workspace; every wait bounded). Each phase's work -- 256-element reduction
 // stages of the projections, or keys of the attention -- is laid out in one
-// flattened order and split evenly into one contiguous range per CTA, so
-// every SM streams the same number of bytes. A 64-row tile (or KV group)
-// whose range straddles two CTAs gets one fp32 partial per CTA; one CTA --
-// the last to arrive for a tile (a per-tile arrival counter), the one holding
-// a KV group's last keys -- combines them in CTA order and runs the epilogue,
-// so results are deterministic and no extra phase is needed.
+// flattened order and split into one contiguous range per CTA: whole tiles
+// for the column-parallel phases and o_proj, an even split of the down
+// stages, and for attention two key shares -- CTAs without a QKV tile take
+// the larger one and prefetch it into L2 while QKV runs. A 64-row tile (or
+// KV group) whose range straddles two CTAs gets one fp32 partial per CTA; one
+// CTA combines them in CTA order and runs the epilogue: for down tiles the
+// one holding the tile's last stage, polling (value, epoch) pieces; for a
+// KV group the one holding its last keys, after a per-group counter. Results
+// are deterministic and no extra phase is needed.
 // The producer thread streams the data of later phases that does not depend
 // on earlier ones -- every weight box, and every K/V block except the one
 // holding the new position -- through the same 5-stage ring while the
