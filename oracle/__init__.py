@@ -25,8 +25,9 @@ Sources, cited by page title and section:
   tp=1 tensor, fused weights equal as a row multiset, lm_head row vocab-5).
 * "Multi-GPU & Multi-Node" (the TensorSharp docs): section How tensor
   parallelism works (steps 1-3 and the replicated norms paragraph), section
-  Supported architectures (expert slicing with a replicated router) and
-  section Requirements & constraints (divisibility).
+  Supported architectures (expert slicing, and expert parallelism with whole
+  experts per rank, both with a replicated router) and section Requirements &
+  constraints (divisibility).
 
 The per-op formulas (RMSNorm, rotate-half RoPE, GQA head grouping, SwiGLU) are
 not written out on the pages; the workload descriptions name them and the
