@@ -74,10 +74,11 @@ def test_moe_block_matches_oracle(gpu_lib, case):
     assert err <= 2e-2, err
 
 
-def test_moe_is_deterministic(gpu_lib):
+@pytest.mark.parametrize("case", ["moe_small_tp2_skewed_ragged", "moe_ep_small_tp2_skewed_ragged"])
+def test_moe_is_deterministic(gpu_lib, case):
     import torch
     from megatron_tensor_block_gb300.runtime import Model
-    m = Model(CASES["moe_small_tp2_skewed_ragged"]())
+    m = Model(CASES[case]())
     a = m.forward().clone()
     b = m.forward().clone()
     torch.cuda.synchronize()
