@@ -131,6 +131,9 @@ typedef struct tp_plan_info {
      * int32 [E+1], slot -> choice index int32 [T*top_k]. -1 without experts. */
     int64_t moe_ids_offset, moe_bucket_offset, moe_perm_offset;
     int64_t experts_shard;       /* experts held per shard: E sliced, E/tp with expert parallelism */
+    int64_t noalloc_scratch_bytes; /* bytes of the static array a DECODE call of
+                                  * tp_block_forward_noalloc uses (0 without an
+                                  * attention block); must be <= TP_NOALLOC_SCRATCH_BYTES */
 } tp_plan_info;
 
 /* Full (unsharded) block weights, caller-owned device memory. */
@@ -296,7 +299,7 @@ tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_se
 #define TP_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
 
 /* DECODE forward (same computation, kernels and results as tp_block_forward
- * with TP_MODE_DECODE, T_per_seq = 1) for callers that must not allocate
+ * with TP_MODE_DECODE, T_per_seq = 1) for callers that cannot allocate
  * device memory: code that runs while a CUDA graph is being captured, where
  * an allocation is not allowed; plug-ins inside a host program that owns all
  * device memory through its own pool; and latency-bound loops that cannot
@@ -311,20 +314,35 @@ tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, const tp_kv_se
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture. Later calls only enqueue work.
  *  - Every call on a device shares the one array, which keeps the last call's
- *    contents; each call clears the counters and status word it needs on
- *    `stream` before its kernels run. Calls whose work overlaps on the GPU
- *    (other streams, other host threads) race on the array and give wrong
- *    results: issue them on one stream, or serialise them.
- *  - Plans whose decode scratch exceeds TP_NOALLOC_SCRATCH_BYTES are rejected
- *    with TP_ERR_CAPACITY before any GPU work (the Llama-3-8B-shaped block at
- *    tp 4, batch 8, KV 2049 needs about 10 MB). Positions past max_kv are
- *    skipped as in tp_block_forward, but the status word is not readable here.
+ *    contents. Each call first clears, on `stream`, the control words
+ *    (counters, status word, grid-barrier counter) and the buffer of
+ *    cross-SM pieces, so nothing an earlier call left is taken as this
+ *    call's. Calls whose work overlaps on the GPU (other streams, other host
+ *    threads) race on the array and give wrong results: issue them on one
+ *    stream, or serialise them.
+ *  - The array must hold the plan's whole decode footprint,
+ *    tp_plan_info.noalloc_scratch_bytes: control words, decode buffers and
+ *    the piece buffer (the Llama-3-8B-shaped block at tp 4, batch 8,
+ *    max_kv 2049 needs about 11 MB). Larger plans are rejected with
+ *    TP_ERR_CAPACITY before any GPU work. The footprint does not depend on
+ *    max_tokens (prefill and MoE buffers are not used here).
+ *  - Positions past max_kv are skipped as in tp_block_forward and recorded
+ *    as TP_ERR_CAPACITY in the array's status word; a bounded device wait
+ *    that gives up records TP_ERR_TIMEOUT there. tp_noalloc_status reads it.
  * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no attention block, y == x),
  * TP_ERR_SHAPE (B outside 1..min(max_batch, 8)), TP_ERR_CAPACITY,
  * TP_ERR_ALIGN, TP_ERR_UNSUPPORTED, TP_ERR_CUDA. */
 tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set* w, const tp_kv_set* kv,
                                    const float* x, float* y, const int32_t* pos, int32_t B,
                                    void* stream);
+
+/* Reads the status word of the current device's static array (TP_OK, or the
+ * first device-detected error of the latest tp_block_forward_noalloc call
+ * on this device, which cleared it) into *out (host). Synchronises `stream`;
+ * pass the stream of that call. Like the entry point, the first call on a
+ * device looks up the array's address. No counterpart on the pages.
+ * Errors: TP_ERR_NULL, TP_ERR_UNSUPPORTED, TP_ERR_CUDA. */
+tp_status tp_noalloc_status(int32_t* out, void* stream);
 
 /* ------------------------------------------- several decode blocks, one launch */
 

@@ -14,6 +14,7 @@ import os
 from . import build as _build
 
 TP_MAX_SHARDS = 8
+TP_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 TP_OK = 0
 TP_ERR_INVALID_ARG = -1
@@ -53,7 +54,7 @@ class tp_plan_info(C.Structure):
             "vocab_rows_shard", "wqkv_bytes", "bqkv_bytes", "wo_bytes", "wgu_bytes", "wd_bytes",
             "gamma_bytes", "egu_bytes", "ed_bytes", "kv_cache_bytes", "lm_head_bytes", "workspace_bytes",
             "weight_bytes_shard", "weight_bytes_total", "moe_ids_offset", "moe_bucket_offset",
-            "moe_perm_offset", "experts_shard")]
+            "moe_perm_offset", "experts_shard", "noalloc_scratch_bytes")]
 
 
 class tp_block_weights(C.Structure):
@@ -103,6 +104,7 @@ def load(path: str | None = None) -> C.CDLL:
                                    I32, VP, VP, C.c_size_t, VP]),
         "tp_block_forward_noalloc": (I32, [P, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), VP, VP, VP, I32,
                                            VP]),
+        "tp_noalloc_status": (I32, [C.POINTER(I32), VP]),
         "tp_stack_create": (I32, [P, I32, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), C.POINTER(P)]),
         "tp_stack_destroy": (None, [P]),
         "tp_stack_ctas": (I32, [P]),
@@ -239,6 +241,14 @@ def tp_block_forward_noalloc(plan: Plan, shards: dict, kv: tuple, x, y, pos, B: 
     kvs = _kv_set(*kv)
     _check(load().tp_block_forward_noalloc(plan.handle, C.byref(_shard_set(shards)), C.byref(kvs), _ptr(x),
                                            _ptr(y), _ptr(pos), B, _stream(stream)))
+
+
+def tp_noalloc_status(stream=None) -> int:
+    """Status word of the static scratch array on the current device (the
+    latest ``tp_block_forward_noalloc`` call's device-detected error, or 0)."""
+    v = C.c_int32()
+    _check(load().tp_noalloc_status(C.byref(v), _stream(stream)))
+    return v.value
 
 
 class Stack:

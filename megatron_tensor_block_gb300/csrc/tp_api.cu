@@ -73,6 +73,9 @@ struct tp_plan_s {
     // multi-layer decode (tp_stack_decode): control words, then its own pair buffers
     // at the end of the workspace (no other mode writes them, so no stale epoch matches)
     size_t off_step_pairs = 0;
+    // tp_block_forward_noalloc: the decode buffers, then the down pieces' pair
+    // buffer right after them (the workspace path keeps it at off_step_pairs)
+    size_t na_pairs_off = 0, na_pairs_bytes = 0, na_end = 0;
     size_t off_c_ctrl = 0, off_c_x = 0, off_c_q = 0, off_c_p = 0, off_c_h = 0, off_c_a = 0,
            off_c_begin = 0, off_c_end = 0;
     int c_ck = 0, c_maxch = 0;
@@ -238,7 +241,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
     // ---- workspace layout: control words first, then the data buffers
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
-    P->off_status = take(sizeof(int));
+    P->off_status = take(sizeof(int));   // offset 0 in every layout (tp_noalloc_status relies on it)
     if (dense) {
         const int hd = (int)d->head_dim;
         P->g_qkv = make_shape((int)(N * I.qkv_rows / kTileRows), 1, (int)H, P->esz);
@@ -333,7 +336,8 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         const int64_t groups = N * MB * I.hkv_shard;
         P->off_c_begin = off;
         // split row-parallel tiles of the one-launch step: (value, epoch) pieces of the down phase
-        P->off_step_pairs = take((size_t)P->g_down.groups * N * P->step_split[3] * kTileRows * kTMax * 8);
+        P->na_pairs_bytes = (size_t)P->g_down.groups * N * P->step_split[3] * kTileRows * kTMax * 8;
+        P->off_step_pairs = take(P->na_pairs_bytes);
         P->off_c_x = take((size_t)MB * H * 8);
         P->off_c_q = take((size_t)N * MB * I.qkv_rows * 8);
         P->off_c_p = take((size_t)groups * P->c_maxch * G * (hd + 2) * 8);
@@ -343,6 +347,15 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->ws_bytes = off;
     }
     I.workspace_bytes = (int64_t)P->ws_bytes;
+    if (dense) {
+        // every byte a decode step writes: control words, decode buffers, pair buffer
+        P->na_end = P->ws_decode_end;
+        if (P->off_step_pairs) {
+            P->na_pairs_off = align256(P->ws_decode_end);
+            P->na_end = align256(P->na_pairs_off + P->na_pairs_bytes);
+        }
+        I.noalloc_scratch_bytes = (int64_t)P->na_end;
+    }
     *out = P;
     return ok();
 }
@@ -633,8 +646,8 @@ extern "C" tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t b
 // bf16 decode: every stage in one persistent launch (the launch sequence of
 // the separate fp32 kernels below, as phases of one kernel).
 static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_kv_set* kv, const float* x, float* y,
-                                  const int32_t* pos, int B, char* ws, cudaStream_t s, const GemvParams& q,
-                                  const NormPrepParams& np) {
+                                  const int32_t* pos, int B, char* ws, size_t pairs_off, cudaStream_t s,
+                                  const GemvParams& q, const NormPrepParams& np) {
     const tp_model_desc& d = P->d;
     const tp_plan_info& I = P->info;
     const int N = P->N, T = B, hd = (int)d.head_dim;
@@ -725,7 +738,7 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     dn.y = y;
     for (int r = 0; r < N; ++r) dn.W[r] = w->wd[r];
     dn.xact = ws + P->off_act;
-    dn.pairs = P->off_step_pairs ? reinterpret_cast<unsigned long long*>(ws + P->off_step_pairs) : nullptr;
+    dn.pairs = pairs_off ? reinterpret_cast<unsigned long long*>(ws + pairs_off) : nullptr;
 
     st.bar = reinterpret_cast<unsigned long long*>(ws + P->off_step_bar);
     st.stamps = P->n_stage_ev > 0 ? reinterpret_cast<unsigned long long*>(ws + P->off_stamps) : nullptr;
@@ -739,8 +752,10 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     return ok();
 }
 
+// `pairs_off`: byte offset of the down pieces' (value, epoch) buffer in `ws`
+// (0: none, the counted finish instead).
 static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_set* kv, const float* x,
-                                float* y, const int32_t* pos, int B, char* ws, cudaStream_t s) {
+                                float* y, const int32_t* pos, int B, char* ws, size_t pairs_off, cudaStream_t s) {
     const tp_model_desc& d = P->d;
     const tp_plan_info& I = P->info;
     const int N = P->N, T = B;
@@ -801,7 +816,7 @@ static tp_status forward_decode(tp_plan_t P, const tp_shard_set* w, const tp_kv_
         q.xact = ws + P->off_xg;
         q.ss_tiles = np.ss;
         q.n_ss_tiles = (int)((d.hidden + 255) / 256);
-        return decode_step_bf16(P, w, kv, x, y, pos, B, ws, s, q, np);
+        return decode_step_bf16(P, w, kv, x, y, pos, B, ws, pairs_off, s, q, np);
     }
     // fp32: one launch per stage
     stage_mark(P, 0, s);
@@ -1098,7 +1113,7 @@ extern "C" tp_status tp_block_forward(tp_plan_t plan, const tp_shard_set* w, con
         if (!kv || !pos) return fail(TP_ERR_NULL, "tp_block_forward: DECODE needs kv and pos");
         if (T_per_seq != 1) return fail(TP_ERR_SHAPE, "tp_block_forward: DECODE takes T_per_seq == 1");
         if (B > kTMax) return fail(TP_ERR_SHAPE, "tp_block_forward: DECODE handles at most %d sequences", kTMax);
-        return forward_decode(plan, w, kv, x, y, pos, B, ws, s);
+        return forward_decode(plan, w, kv, x, y, pos, B, ws, plan->off_step_pairs, s);
     }
     if (mode == TP_MODE_MOE_FFN) {
         if (!plan->moe) return fail(TP_ERR_INVALID_ARG, "tp_block_forward: MOE_FFN needs a plan with experts");
@@ -1271,11 +1286,13 @@ extern "C" tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set
     if (x == y) return fail(TP_ERR_INVALID_ARG, "tp_block_forward_noalloc: y must not alias x");
     if (B < 1 || B > plan->d.max_batch || B > kTMax)
         return fail(TP_ERR_SHAPE, "tp_block_forward_noalloc: B=%d outside 1..min(max_batch, %d)", B, kTMax);
-    if (plan->ws_decode_end > (size_t)TP_NOALLOC_SCRATCH_BYTES)
+    // na_end covers every byte the decode step touches: control words, the
+    // decode buffers and the down pieces' pair buffer placed right after them
+    if (plan->na_end > (size_t)TP_NOALLOC_SCRATCH_BYTES)
         return fail(TP_ERR_CAPACITY,
                     "tp_block_forward_noalloc: this plan's decode needs %zu bytes of scratch; the static array "
                     "holds %lld (use tp_block_forward with a caller workspace)",
-                    plan->ws_decode_end, (long long)TP_NOALLOC_SCRATCH_BYTES);
+                    plan->na_end, (long long)TP_NOALLOC_SCRATCH_BYTES);
     if (!aligned16(x) || !aligned16(y)) return fail(TP_ERR_ALIGN, "tp_block_forward_noalloc: x and y must be 16-byte aligned");
     tp_status st = check_device();
     if (st) return st;
@@ -1283,9 +1300,30 @@ extern "C" tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set
     st = noalloc_scratch(&scratch);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: counters and status start at zero
-    TP_CUDA(cudaMemsetAsync(scratch, 0, plan->ctrl_bytes, s), "tp_block_forward_noalloc: clearing counters");
-    return forward_decode(plan, w, kv, x, y, pos, B, static_cast<char*>(scratch), s);
+    char* base = static_cast<char*>(scratch);
+    // The array keeps whatever the previous call (of any plan) left. Counters,
+    // status word and grid-barrier counter start at zero, so this launch's
+    // epoch is 1; the pair buffer starts at zero too, so no piece of an
+    // earlier call (also epoch 1) can pass for one of this call's.
+    TP_CUDA(cudaMemsetAsync(base, 0, plan->ctrl_bytes, s), "tp_block_forward_noalloc: clearing counters");
+    if (plan->na_pairs_off)
+        TP_CUDA(cudaMemsetAsync(base + plan->na_pairs_off, 0, plan->na_pairs_bytes, s),
+                "tp_block_forward_noalloc: clearing the pair buffer");
+    return forward_decode(plan, w, kv, x, y, pos, B, base, plan->na_pairs_off, s);
+}
+
+extern "C" tp_status tp_noalloc_status(int32_t* out, void* stream) {
+    if (!out) return fail(TP_ERR_NULL, "tp_noalloc_status: NULL argument");
+    tp_status st = check_device();
+    if (st) return st;
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the status word is the first word of every plan's layout
+    TP_CUDA(cudaMemcpyAsync(out, scratch, sizeof(int32_t), cudaMemcpyDeviceToHost, s), "tp_noalloc_status: copy");
+    TP_CUDA(cudaStreamSynchronize(s), "tp_noalloc_status: sync");
+    return ok();
 }
 
 // ---------------------------------------------------------------- several decode blocks in one launch

@@ -164,3 +164,30 @@ def test_argument_errors_precede_any_launch():
         tb.tp_block_forward(plan, {}, None, 4096, 8192, 0, 2, 1, B.TP_MODE_DECODE, None, 16384,
                             info["workspace_bytes"], stream=0)
     assert e.value.status == B.TP_ERR_SHAPE          # B above max_batch
+
+
+def test_noalloc_footprint_covers_the_piece_buffer_and_ignores_max_tokens():
+    # the no-alloc decode uses control words, decode buffers and the down
+    # pieces' pair buffer; prefill/MoE buffers (sized by max_tokens) are not
+    # part of it
+    w = synth.WORKLOADS["llama3_8b_decode_tp4"]
+    small = tb.tp_plan_get_info(tb.tp_plan(desc_of(w), 4))
+    big = tb.tp_plan_get_info(tb.tp_plan(desc_of(w, max_tokens=8192), 4))
+    assert small["noalloc_scratch_bytes"] == big["noalloc_scratch_bytes"]
+    assert 0 < small["noalloc_scratch_bytes"] <= B.TP_NOALLOC_SCRATCH_BYTES
+    assert big["workspace_bytes"] > B.TP_NOALLOC_SCRATCH_BYTES     # the whole workspace would not fit
+    # down pieces: 64 output tiles x 4 shards x 2 slots x 64 rows x 8 tokens x 8 bytes = 1 MiB
+    assert small["noalloc_scratch_bytes"] >= 64 * 4 * 2 * 64 * 8 * 8
+    moe = tb.tp_plan_get_info(tb.tp_plan(desc_of(synth.WORKLOADS["moe_expert_slice_tp4"]), 4))
+    assert moe["noalloc_scratch_bytes"] == 0
+
+
+def test_noalloc_rejects_an_oversized_plan_before_any_launch():
+    w = synth.WORKLOADS["llama3_8b_decode_tp4"]
+    plan = tb.tp_plan(desc_of(w, max_kv=200000), 4)
+    assert tb.tp_plan_get_info(plan)["noalloc_scratch_bytes"] > B.TP_NOALLOC_SCRATCH_BYTES
+    # the pointers are never dereferenced: the capacity check comes first
+    with pytest.raises(tb.TpError) as e:
+        tb.tp_block_forward_noalloc(plan, {}, ([0] * 4, [0] * 4), 4096, 8192, 16384, w.batch, stream=0)
+    assert e.value.status == B.TP_ERR_CAPACITY
+    assert "static array" in str(e.value)
