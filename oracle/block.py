@@ -574,3 +574,15 @@ def relerr(gpu: np.ndarray, ref: np.ndarray) -> float:
     ref = np.asarray(ref, dtype=np.float64)
     den = np.max(np.abs(ref))
     return float(np.max(np.abs(gpu - ref)) / (den if den > 0 else 1.0))
+
+
+def relerr_elementwise(gpu: np.ndarray, ref: np.ndarray, floor: float = 1e-6) -> float:
+    """``max_i |gpu_i - ref_i| / max(|ref_i|, floor * max|ref|)``: the
+    element-wise relative error, a diagnostic reported beside the normwise
+    figure (a small localised error can hide under the normwise one; the
+    floor keeps entries near zero from dominating)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    top = np.max(np.abs(ref)) if ref.size else 0.0
+    den = np.maximum(np.abs(ref), floor * (top if top > 0 else 1.0))
+    return float(np.max(np.abs(gpu - ref) / den)) if ref.size else 0.0

@@ -611,3 +611,22 @@ def test_lm_head_matches_torch():
     W = rng(93).standard_normal((V, H))
     t = F.linear(F.rms_norm(torch.from_numpy(h), (H,), torch.from_numpy(g), eps), torch.from_numpy(W)).numpy()
     assert np.allclose(O.lm_head_logits(h, g, W, eps), t, rtol=1e-12, atol=1e-12)
+
+
+def test_elementwise_error_sees_what_the_normwise_error_hides():
+    # the survey's o16 diagnostic: per-entry error relative to the entry, with
+    # a floor of 1e-6 of the largest magnitude for entries near zero
+    ref = np.array([1000.0, 1.0])
+    gpu = np.array([1000.0, 1.5])
+    assert O.relerr(gpu, ref) == pytest.approx(0.5 / 1000.0)
+    assert O.relerr_elementwise(gpu, ref) == pytest.approx(0.5)
+    # an exact zero in ref is measured against the floor, not divided by zero
+    assert O.relerr_elementwise(np.array([1.0, 1e-7]), np.array([1.0, 0.0])) == pytest.approx(0.1)
+    # sign errors count in full; equal arrays give 0
+    assert O.relerr_elementwise(np.array([-2.0, 4.0]), np.array([2.0, 4.0])) == pytest.approx(2.0)
+    assert O.relerr_elementwise(ref, ref) == 0.0
+    # never below the normwise figure
+    rng = np.random.default_rng(0)
+    a = rng.standard_normal(1000)
+    b = a + 1e-3 * rng.standard_normal(1000)
+    assert O.relerr_elementwise(b, a) >= O.relerr(b, a)
