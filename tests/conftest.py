@@ -21,3 +21,18 @@ def gpu_lib():
     import megatron_tensor_block_gb300 as tb
     tb.load()
     return tb
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Normwise and element-wise relative errors of every parity comparison
+    made through ``tests/_parity.py`` in this session."""
+    try:
+        from tests import _parity
+    except ImportError:
+        return
+    if not _parity.RECORDS:
+        return
+    tr = terminalreporter
+    tr.section("parity: normwise | element-wise relative error")
+    for test, what, n, e in _parity.RECORDS:
+        tr.write_line(f"{n:9.2e} | {e:9.2e}  {test}{' ' + what if what else ''}")

@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tests import _parity as P
 import synth
 from tests import _oracle_runs as R
 
@@ -63,14 +64,14 @@ def test_decode_block_matches_oracle(gpu_lib, case):
     inputs = synth.make_inputs(w)
     m, y = _run(gpu_lib, inputs)
     ref, caches = R.dense_tpN(inputs, m.max_kv)
-    err = O.relerr(y, ref)
+    err = P.err(y, ref)
     assert err <= TOL[w.dtype], err
     # the new K (rotated) and V rows written to each shard's cache
     kk, vv = _cache_at_new_positions(m, 0, inputs)
     pos = inputs["pos"]
     rk = np.stack([caches[0][0][b, :, pos[b]] for b in range(len(pos))])
     rv = np.stack([caches[0][1][b, :, pos[b]] for b in range(len(pos))])
-    assert O.relerr(kk, rk) <= TOL[w.dtype] and O.relerr(vv, rv) <= TOL[w.dtype]
+    assert P.err(kk, rk) <= TOL[w.dtype] and P.err(vv, rv) <= TOL[w.dtype]
     # and nothing else in the caches moved
     k, v = m.caches[0].full()
     old = R.full_cache(inputs["k_cache"][0], m.max_kv)
@@ -84,14 +85,14 @@ def test_decode_tpN_equals_unsharded_block(gpu_lib):
     w = CASES["llama_shape_small_tp4_b3"]
     inputs = synth.make_inputs(w)
     m, y = _run(gpu_lib, inputs)
-    assert O.relerr(y, R.dense_tp1(inputs, m.max_kv)) <= TOL[w.dtype]
+    assert P.err(y, R.dense_tp1(inputs, m.max_kv)) <= TOL[w.dtype]
 
 
 def test_decode_llama3_8b_full_size(gpu_lib):
     inputs = synth.make_inputs(LLAMA)
     m, y = _run(gpu_lib, inputs)
     ref, _ = R.dense_tpN(inputs, m.max_kv)
-    err = O.relerr(y, ref)
+    err = P.err(y, ref)
     assert err <= TOL["bf16"], err
 
 
@@ -99,7 +100,7 @@ def test_decode_qwen25_24_layers_full_size(gpu_lib):
     inputs = synth.make_inputs(QWEN, with_head=False)
     m, y = _run(gpu_lib, inputs)
     ref, _ = R.dense_tpN(inputs, m.max_kv)
-    err = O.relerr(y, ref)
+    err = P.err(y, ref)
     assert err <= TOL["bf16"], err
 
 
@@ -150,4 +151,4 @@ def test_decode_ragged_positions_match_oracle(gpu_lib):
     inputs["pos"] = np.array([300, 0, 151], dtype=np.int32)
     m, y = _run(gpu_lib, inputs)
     ref, _ = R.dense_tpN(inputs, m.max_kv)
-    assert O.relerr(y, ref) <= TOL[w.dtype]
+    assert P.err(y, ref) <= TOL[w.dtype]

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tests import _parity as P
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -69,10 +70,10 @@ def test_lm_head_matches_oracle(gpu_lib, case):
     h = np.asarray(inputs["x"], dtype=np.float64)
     g = np.asarray(inputs["gamma_final"], dtype=np.float64)
     ref = O.lm_head_logits(h, g, O.to_f64(inputs["lm_head"]), w.eps)
-    err = O.relerr(got, ref)
+    err = P.err(got, ref)
     assert err <= TOL, err
     # the last real row sits on the last shard: the cross-shard index of the gather
-    assert O.relerr(got[:, V - 1:], ref[:, V - 1:]) <= TOL
+    assert P.err(got[:, V - 1:], ref[:, V - 1:]) <= TOL
 
 
 def test_lm_head_is_deterministic(gpu_lib):

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tests import _parity as P
 import synth
 from tests import _oracle_runs as R
 
@@ -70,7 +71,7 @@ def test_moe_block_matches_oracle(gpu_lib, case):
     assert np.array_equal(_ws_int(m, m.info["moe_perm_offset"], n), perm)
     # block output
     ref = R.moe_tpN(inputs)
-    err = O.relerr(y.double().cpu().numpy(), ref)
+    err = P.err(y.double().cpu().numpy(), ref)
     assert err <= 2e-2, err
 
 

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tests import _parity as P
 import synth
 from tests import _oracle_runs as R
 
@@ -53,15 +54,15 @@ def test_prefill_block_matches_oracle(gpu_lib, case):
     inputs = synth.make_inputs(w, with_head=False)
     m, y = _run(inputs)
     ref, caches = R.dense_tpN(inputs, m.max_kv)
-    err = O.relerr(y, ref)
+    err = P.err(y, ref)
     assert err <= TOL, err
     # every cache row the block wrote (rotated K, V), and nothing else moved
     k, v = (t.double().cpu().numpy() for t in m.caches[0].full())
     S, pos = w.tokens_per_seq, inputs["pos"]
     for b in range(w.batch):
         new = slice(int(pos[b]), int(pos[b]) + S)
-        assert O.relerr(k[b, :, new], caches[0][0][b, :, new]) <= TOL
-        assert O.relerr(v[b, :, new], caches[0][1][b, :, new]) <= TOL
+        assert P.err(k[b, :, new], caches[0][0][b, :, new]) <= TOL
+        assert P.err(v[b, :, new], caches[0][1][b, :, new]) <= TOL
     old_k = R.full_cache(inputs["k_cache"][0], m.max_kv)
     for b in range(w.batch):
         k[b, :, int(pos[b]):int(pos[b]) + S] = old_k[b, :, int(pos[b]):int(pos[b]) + S]
@@ -132,6 +133,6 @@ def test_full_llama3_8b_prefill_tp8_sampled_rows(gpu_lib):
     vs = O.shard_kv_cache(R.full_cache(inputs["v_cache"][0], m.max_kv), w.tp)
     ref, order = O.block_rows_tpN(shards, np.asarray(inputs["x"], dtype=np.float64), ks, vs, inputs["pos"], S, w,
                                   w.tp, rows)
-    err = O.relerr(y[order], ref)
+    err = P.err(y[order], ref)
     assert err <= TOL, err
     assert np.isfinite(y).all()

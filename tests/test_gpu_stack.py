@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tests import _parity as P
 import synth
 from tests import _oracle_runs as R
 
@@ -56,7 +57,7 @@ def test_stack_matches_oracle(gpu_lib, case):
     m = _model(inputs)
     y = _run_stack(m)
     ref, caches = R.dense_tpN(inputs, m.max_kv)
-    err = O.relerr(y, ref)
+    err = P.err(y, ref)
     assert err <= TOL, err
     pos = inputs["pos"]
     for layer in range(w.n_layers):
@@ -65,7 +66,7 @@ def test_stack_matches_oracle(gpu_lib, case):
         vv = np.stack([v[b, :, pos[b]].double().cpu().numpy() for b in range(len(pos))])
         rk = np.stack([caches[layer][0][b, :, pos[b]] for b in range(len(pos))])
         rv = np.stack([caches[layer][1][b, :, pos[b]] for b in range(len(pos))])
-        assert O.relerr(kk, rk) <= TOL and O.relerr(vv, rv) <= TOL, layer
+        assert P.err(kk, rk) <= TOL and P.err(vv, rv) <= TOL, layer
         # nothing else in the cache moved
         old = R.full_cache(inputs["k_cache"][layer], m.max_kv)
         kn = k.double().cpu().numpy()
@@ -79,7 +80,7 @@ def test_stack_qwen25_24_layers_full_size(gpu_lib):
     m = _model(inputs)
     y = _run_stack(m)
     ref, _ = R.dense_tpN(inputs, m.max_kv)
-    err = O.relerr(y, ref)
+    err = P.err(y, ref)
     assert err <= TOL, err
 
 
@@ -91,7 +92,7 @@ def test_stack_agrees_with_per_layer_launches(gpu_lib):
     y_layers = m.forward().clone()
     torch.cuda.synchronize()
     a, b = y_stack.double().cpu().numpy(), y_layers.double().cpu().numpy()
-    assert O.relerr(a, b) <= TOL
+    assert P.err(a, b) <= TOL
 
 
 def test_stack_is_deterministic_across_launches(gpu_lib):
@@ -145,7 +146,7 @@ def test_stack_shares_a_workspace_with_per_layer_launches(gpu_lib):
     torch.cuda.synchronize()
     assert m.ws.status() == 0
     assert torch.equal(a, c)
-    assert O.relerr(a.double().cpu().numpy(), b.double().cpu().numpy()) <= TOL
+    assert P.err(a.double().cpu().numpy(), b.double().cpu().numpy()) <= TOL
 
 
 def test_stack_many_launches_keep_their_epochs(gpu_lib):
@@ -175,9 +176,9 @@ def test_stack_ragged_positions_match_oracle(gpu_lib, case):
     m = _model(inputs)
     y = _run_stack(m)
     ref, caches = R.dense_tpN(inputs, m.max_kv)
-    assert O.relerr(y, ref) <= TOL
+    assert P.err(y, ref) <= TOL
     k, _ = m.caches[0].full()
     pos = inputs["pos"]
     kk = np.stack([k[b, :, pos[b]].double().cpu().numpy() for b in range(len(pos))])
     rk = np.stack([caches[0][0][b, :, pos[b]] for b in range(len(pos))])
-    assert O.relerr(kk, rk) <= TOL
+    assert P.err(kk, rk) <= TOL

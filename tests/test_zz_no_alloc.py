@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from tests import _parity as P
 import synth
 from tests import _oracle_runs as R
 
@@ -69,7 +70,7 @@ def test_noalloc_decode_two_calls_on_different_inputs(gpu_lib, name):
         ref, _ = R.dense_tpN(inputs, m.max_kv)
         got = y.double().cpu().numpy()
         assert np.isfinite(got).all()
-        err = O.relerr(got, ref)
+        err = P.err(got, ref)
         assert err <= TOL[w.dtype], f"call {i}: relative error {err}"
 
 
