@@ -249,6 +249,22 @@ tp_status tp_gather_param(tp_plan_t plan, int32_t k, const void* const* shards,
                           int64_t rows_per_shard, int64_t cols_per_shard,
                           int32_t dtype, void* out, void* stream);
 
+/* Places a full KV cache into the per-shard caches ([MG] How tensor
+ * parallelism works, step 2: each shard attends over its own heads' cache;
+ * shard r owns KV heads [r Hkv', (r+1) Hkv'), contiguous groups, so every
+ * query head's KV head sits on the same shard):
+ *   kv->k[r][b][h][p][:] = k_full[b][r Hkv' + h][p][:]   for p < L,
+ * and the same for V. k_full and v_full are DEVICE [B][Hkv][L][d] in the
+ * plan dtype (keys already rotated); the shard caches are the
+ * [max_batch][Hkv'][max_kv][d] buffers of tp_kv_set. Positions >= L and
+ * sequences >= B of the shard caches are left as they are. Bit-exact copies,
+ * asynchronous on `stream`; the full cache is only read.
+ * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (no attention block), TP_ERR_SHAPE
+ * (B outside 1..max_batch), TP_ERR_CAPACITY (L outside 0..max_kv),
+ * TP_ERR_UNSUPPORTED, TP_ERR_CUDA. */
+tp_status tp_shard_kv(tp_plan_t plan, const void* k_full, const void* v_full, int64_t B, int64_t L,
+                      const tp_kv_set* kv, void* stream);
+
 /* ------------------------------------------------------------- forward */
 
 /* Zeroes the control words (completion counters, status) at the start of a
@@ -449,7 +465,9 @@ tp_status tp_gemm_bf16_kn(const void* A, const void* B, float* C, int64_t M, int
                           int32_t* device_status, void* stream);
 
 /* Reads the workspace status word (TP_OK or the first device-detected error
- * since tp_workspace_init) into *out (host). Synchronises `stream`. */
+ * since tp_workspace_init) into *out (host). Synchronises `stream`. After
+ * TP_ERR_TIMEOUT the workspace's counters may be left mid-way: call
+ * tp_workspace_init on it before the next forward. */
 tp_status tp_get_device_status(void* workspace, int32_t* out, void* stream);
 
 /* Measurement hook: while set, tp_block_forward records events[i]
@@ -485,6 +503,19 @@ tp_status tp_profile_phases(tp_plan_t plan, double* out_us, double* median_us, i
  * launch order) x 13 values (start; then per phase: streaming done, barrier
  * arrival or end), %globaltimer nanoseconds, copied to `out` (host). */
 tp_status tp_profile_phase_stamps(tp_plan_t plan, uint64_t* out, int32_t rows, void* stream);
+
+/* Test hook for the bounded-wait path ([RT] Acceptance criteria: no silent
+ * wrong results). While on (1), every bf16 DECODE launch of this plan waits
+ * at each of its grid barriers for one arrival more than its CTAs make, as
+ * if one CTA had been lost: the first barrier's wait gives up after the 1 s
+ * limit, the launch records TP_ERR_TIMEOUT in the workspace status word, and
+ * every CTA leaves through its abort path (all waits are bounded, so the
+ * launch ends within a few seconds). The output and the KV rows at pos are
+ * then undefined; call tp_workspace_init on the workspace before its next
+ * forward. Off (0) by default; nothing in the library turns it on. No
+ * counterpart on the pages.
+ * Errors: TP_ERR_NULL, TP_ERR_INVALID_ARG (on not 0 or 1). */
+tp_status tp_debug_withhold_arrival(tp_plan_t plan, int32_t on);
 
 /* ----------------------------------------------------------------- misc */
 

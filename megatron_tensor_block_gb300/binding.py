@@ -99,6 +99,7 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_shard_weights": (I32, [P, C.POINTER(tp_block_weights), C.POINTER(tp_shard_set), VP]),
         "tp_shard_param": (I32, [P, I32, VP, I64, I64, I32, C.POINTER(I64), I32, C.POINTER(VP), VP]),
         "tp_gather_param": (I32, [P, I32, C.POINTER(VP), I64, I64, I32, VP, VP]),
+        "tp_shard_kv": (I32, [P, VP, VP, I64, I64, C.POINTER(tp_kv_set), VP]),
         "tp_workspace_init": (I32, [P, VP, C.c_size_t, VP]),
         "tp_block_forward": (I32, [P, C.POINTER(tp_shard_set), C.POINTER(tp_kv_set), VP, VP, VP, I32, I32,
                                    I32, VP, VP, C.c_size_t, VP]),
@@ -118,6 +119,7 @@ def load(path: str | None = None) -> C.CDLL:
         "tp_profile_stages": (I32, [P, C.POINTER(VP), I32]),
         "tp_profile_phases": (I32, [P, C.POINTER(C.c_double), C.POINTER(C.c_double), I32, VP]),
         "tp_profile_phase_stamps": (I32, [P, C.POINTER(C.c_uint64), I32, VP]),
+        "tp_debug_withhold_arrival": (I32, [P, I32]),
         "tp_last_error": (C.c_char_p, []),
         "tp_version": (I32, []),
     }
@@ -222,6 +224,12 @@ def tp_gather_param(plan: Plan, kind: int, shards: list, rows_per_shard: int, co
                                   _ptr(out), _stream(stream)))
 
 
+def tp_shard_kv(plan: Plan, k_full, v_full, B: int, L: int, kv: tuple, stream=None) -> None:
+    """Copies full ``[B, Hkv, L, d]`` caches into the shards' caches ``kv = (k_list, v_list)``."""
+    kvs = _kv_set(*kv)
+    _check(load().tp_shard_kv(plan.handle, _ptr(k_full), _ptr(v_full), B, L, C.byref(kvs), _stream(stream)))
+
+
 def tp_workspace_init(plan: Plan, workspace, nbytes: int, stream=None) -> None:
     _check(load().tp_workspace_init(plan.handle, _ptr(workspace), nbytes, _stream(stream)))
 
@@ -312,6 +320,12 @@ def tp_gemm_bf16(A, B, C, M: int, N: int, K: int, device_status=None, stream=Non
 def tp_gemm_bf16_kn(A, B, C, M: int, N: int, K: int, device_status=None, stream=None) -> None:
     """C[M, N] = A[M, K] @ B[K, N] on the tensor cores (B N-contiguous)."""
     _check(load().tp_gemm_bf16_kn(_ptr(A), _ptr(B), _ptr(C), M, N, K, _ptr(device_status), _stream(stream)))
+
+
+def tp_debug_withhold_arrival(plan: Plan, on: bool) -> None:
+    """Test hook: the plan's decode launches wait for one grid-barrier
+    arrival too many, so their bounded waits run out (TP_ERR_TIMEOUT)."""
+    _check(load().tp_debug_withhold_arrival(plan.handle, 1 if on else 0))
 
 
 def tp_get_device_status(workspace, stream=None) -> int:

@@ -83,6 +83,7 @@ struct tp_plan_s {
     cudaEvent_t stage_ev[16] = {};
     int n_stage_ev = 0;
     char* last_stamps_ws = nullptr;     // workspace of the last profiled decode step
+    unsigned dbg_bar_extra = 0;         // test hook (tp_debug_withhold_arrival): 0 in every product path
 };
 
 static void stage_mark(tp_plan_t P, int i, cudaStream_t s) {
@@ -625,6 +626,38 @@ extern "C" tp_status tp_gather_param(tp_plan_t plan, int32_t k, const void* cons
     return ok();
 }
 
+extern "C" tp_status tp_shard_kv(tp_plan_t plan, const void* k_full, const void* v_full, int64_t B, int64_t L,
+                                 const tp_kv_set* kv, void* stream) {
+    if (!plan || !k_full || !v_full || !kv) return fail(TP_ERR_NULL, "tp_shard_kv: NULL argument");
+    if (!plan->dense) return fail(TP_ERR_INVALID_ARG, "tp_shard_kv: the plan has no attention block");
+    const tp_model_desc& d = plan->d;
+    if (B < 1 || B > d.max_batch)
+        return fail(TP_ERR_SHAPE, "tp_shard_kv: B=%lld outside 1..max_batch (%lld)", (long long)B,
+                    (long long)d.max_batch);
+    if (L < 0 || L > d.max_kv)
+        return fail(TP_ERR_CAPACITY, "tp_shard_kv: L=%lld outside 0..max_kv (%lld)", (long long)L, (long long)d.max_kv);
+    const int N = plan->N;
+    for (int r = 0; r < N; ++r)
+        if (!kv->k[r] || !kv->v[r]) return fail(TP_ERR_NULL, "tp_shard_kv: shard %d cache pointer is NULL", r);
+    tp_status st = check_device();
+    if (st) return st;
+    if (L == 0) return ok();
+    const int64_t Hs = plan->info.hkv_shard, Hkv = d.n_kv_heads, hd = d.head_dim;
+    const int64_t es = (int64_t)plan->esz, run = L * hd * es;   // one head's first L positions
+    Batcher Bt(static_cast<cudaStream_t>(stream));
+    for (int r = 0; r < N; ++r)
+        for (int64_t b = 0; b < B; ++b) {
+            // heads r*Hs .. r*Hs+Hs-1 of sequence b: contiguous in the full cache,
+            // one max_kv-long row each in the shard's cache
+            const int64_t src = ((b * Hkv) + r * Hs) * run, dst = b * Hs * d.max_kv * hd * es;
+            Bt.add(cptr(k_full, src), mptr(kv->k[r], dst), Hs, run, run, d.max_kv * hd * es);
+            Bt.add(cptr(v_full, src), mptr(kv->v[r], dst), Hs, run, run, d.max_kv * hd * es);
+        }
+    Bt.flush();
+    if (Bt.err != cudaSuccess) return cuda_fail(Bt.err, "tp_shard_kv: copy launch");
+    return ok();
+}
+
 // ---------------------------------------------------------------- forward
 
 extern "C" tp_status tp_workspace_init(tp_plan_t plan, void* workspace, size_t bytes, void* stream) {
@@ -741,6 +774,7 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     dn.pairs = pairs_off ? reinterpret_cast<unsigned long long*>(ws + pairs_off) : nullptr;
 
     st.bar = reinterpret_cast<unsigned long long*>(ws + P->off_step_bar);
+    st.bar_extra = P->dbg_bar_extra;
     st.stamps = P->n_stage_ev > 0 ? reinterpret_cast<unsigned long long*>(ws + P->off_stamps) : nullptr;
     P->last_stamps_ws = st.stamps ? ws : nullptr;
     // with per-step events recorded around the launch, launch without programmatic overlap
@@ -1238,6 +1272,13 @@ extern "C" tp_status tp_profile_phase_stamps(tp_plan_t plan, uint64_t* out, int3
     TP_CUDA(cudaMemcpyAsync(out, plan->last_stamps_ws + plan->off_stamps, (size_t)rows * kStepStamps * 8,
                             cudaMemcpyDeviceToHost, s), "tp_profile_phase_stamps: copy");
     TP_CUDA(cudaStreamSynchronize(s), "tp_profile_phase_stamps: sync");
+    return ok();
+}
+
+extern "C" tp_status tp_debug_withhold_arrival(tp_plan_t plan, int32_t on) {
+    if (!plan) return fail(TP_ERR_NULL, "tp_debug_withhold_arrival: NULL plan");
+    if (on != 0 && on != 1) return fail(TP_ERR_INVALID_ARG, "tp_debug_withhold_arrival: on must be 0 or 1");
+    plan->dbg_bar_extra = (unsigned)on;
     return ok();
 }
 

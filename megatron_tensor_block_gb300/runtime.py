@@ -89,10 +89,10 @@ class ShardedLayer:
 
 class KVCache:
     """Per-shard caches ``[max_batch][Hkv'][max_kv][d]`` filled from the full
-    cache ``[B][Hkv][L][d]`` (the harness's input placement)."""
+    cache ``[B][Hkv][L][d]`` by ``tp_shard_kv`` (contiguous KV-head groups)."""
 
     def __init__(self, w, k_full: np.ndarray | None, v_full: np.ndarray | None, max_kv: int, max_batch: int,
-                 device="cuda"):
+                 device="cuda", plan: B.Plan | None = None):
         torch = _torch()
         N = w.tp
         dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -100,11 +100,10 @@ class KVCache:
         self.k = [torch.zeros(max_batch, Hs, max_kv, w.head_dim, dtype=dt, device=device) for _ in range(N)]
         self.v = [torch.zeros(max_batch, Hs, max_kv, w.head_dim, dtype=dt, device=device) for _ in range(N)]
         if k_full is not None and k_full.shape[2] > 0:
+            if plan is None:
+                raise ValueError("KVCache: filling the shards from a full cache needs the plan")
             kf, vf = to_device(k_full, device), to_device(v_full, device)
-            L, Bn = kf.shape[2], kf.shape[0]
-            for r in range(N):
-                self.k[r][:Bn, :, :L] = kf[:, r * Hs:(r + 1) * Hs]
-                self.v[r][:Bn, :, :L] = vf[:, r * Hs:(r + 1) * Hs]
+            B.tp_shard_kv(plan, kf, vf, kf.shape[0], kf.shape[2], (self.k, self.v))
 
     def full(self):
         """Concatenation of the shards' caches over the KV-head dim."""
@@ -138,7 +137,7 @@ class Model:
             for i, L in enumerate(inputs["layers"]):
                 self.layers.append(ShardedLayer(self.plan, self.info, w, L, device))
                 self.caches.append(KVCache(w, inputs["k_cache"][i], inputs["v_cache"][i], self.max_kv,
-                                           self.max_batch, device))
+                                           self.max_batch, device, plan=self.plan))
             self.pos = torch.from_numpy(inputs["pos"]).to(device)
         if share_norm:
             for l in self.layers:

@@ -191,3 +191,31 @@ def test_noalloc_rejects_an_oversized_plan_before_any_launch():
         tb.tp_block_forward_noalloc(plan, {}, ([0] * 4, [0] * 4), 4096, 8192, 16384, w.batch, stream=0)
     assert e.value.status == B.TP_ERR_CAPACITY
     assert "static array" in str(e.value)
+
+
+def test_kv_placement_argument_errors_precede_any_launch():
+    w = synth.WORKLOADS["llama3_8b_decode_tp4"]
+    plan = tb.tp_plan(desc_of(w), 4)
+    kv = ([4096] * 4, [8192] * 4)
+    with pytest.raises(tb.TpError) as e:
+        tb.tp_shard_kv(plan, 4096, 8192, 9, 10, kv, stream=0)
+    assert e.value.status == B.TP_ERR_SHAPE                  # B above max_batch
+    with pytest.raises(tb.TpError) as e:
+        tb.tp_shard_kv(plan, 4096, 8192, 8, w.max_kv + 1, kv, stream=0)
+    assert e.value.status == B.TP_ERR_CAPACITY               # L above max_kv
+    with pytest.raises(tb.TpError) as e:
+        tb.tp_shard_kv(plan, 4096, 8192, 8, 10, ([4096] * 3 + [0], [8192] * 4), stream=0)
+    assert e.value.status == B.TP_ERR_NULL
+    moe = tb.tp_plan(desc_of(synth.WORKLOADS["moe_expert_slice_tp4"]), 4)
+    with pytest.raises(tb.TpError) as e:
+        tb.tp_shard_kv(moe, 4096, 8192, 8, 10, kv, stream=0)
+    assert e.value.status == B.TP_ERR_INVALID_ARG
+
+
+def test_withhold_hook_is_off_by_default_and_validates():
+    w = synth.WORKLOADS["llama3_8b_decode_tp4"]
+    plan = tb.tp_plan(desc_of(w), 4)
+    tb.tp_debug_withhold_arrival(plan, True)
+    tb.tp_debug_withhold_arrival(plan, False)
+    assert tb.load().tp_debug_withhold_arrival(plan.handle, 2) == B.TP_ERR_INVALID_ARG
+    assert tb.load().tp_debug_withhold_arrival(None, 1) == B.TP_ERR_NULL

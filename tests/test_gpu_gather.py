@@ -160,3 +160,41 @@ def test_reduce_partials_rank_order(gpu_lib):
     p = np.random.Generator(np.random.PCG64(3)).standard_normal((N, M, H)).astype(np.float32)
     tb.tp_reduce_partials(plan, torch.from_numpy(p).cuda(), None, None, out, M)
     assert O.relerr(out.cpu().numpy(), O.reduce_rank_order([p[r].astype(np.float64) for r in range(N)])) < 1e-6
+
+
+@pytest.mark.parametrize("case", [
+    dict(N=4, heads=(32, 8), d=128, B=8, L=2048, max_kv=2049, max_batch=8, dtype="bf16"),   # Llama-3-8B shape
+    dict(N=2, heads=(14, 2), d=64, B=1, L=512, max_kv=513, max_batch=1, dtype="bf16"),      # Qwen shape
+    dict(N=8, heads=(16, 8), d=64, B=3, L=37, max_kv=64, max_batch=5, dtype="f32"),         # ragged, partial batch
+    dict(N=1, heads=(8, 2), d=128, B=2, L=1, max_kv=3, max_batch=2, dtype="f32"),
+])
+def test_kv_cache_placement_matches_the_oracle(gpu_lib, case):
+    # each shard's cache holds its contiguous group of KV heads ("Multi-GPU &
+    # Multi-Node", How tensor parallelism works, step 2), bit for bit; the
+    # positions past L and the sequences past B stay as they were
+    import torch
+    import megatron_tensor_block_gb300 as tb
+    from megatron_tensor_block_gb300.runtime import desc_of, to_device
+    N, (Hq, Hkv), d = case["N"], case["heads"], case["d"]
+    w = synth.scaled(synth.WORKLOADS["llama3_8b_decode_tp4"], hidden=512, n_heads=Hq, n_kv_heads=Hkv, head_dim=d,
+                     ffn=512 * N, tp=N, batch=case["max_batch"], kv_len=case["max_kv"] - 1, dtype=case["dtype"])
+    plan = tb.tp_plan(desc_of(w, max_kv=case["max_kv"], max_batch=case["max_batch"]), N)
+    rng = np.random.Generator(np.random.PCG64(77 + N))
+    B, L = case["B"], case["L"]
+    full = [rng.standard_normal((B, Hkv, L, d)).astype(np.float32) for _ in range(2)]
+    if case["dtype"] == "bf16":
+        full = [synth.round_to_bf16_bits(a) for a in full]
+    dt = torch.bfloat16 if case["dtype"] == "bf16" else torch.float32
+    shape = (case["max_batch"], Hkv // N, case["max_kv"], d)
+    k = [torch.full(shape, 7.0, dtype=dt, device="cuda") for _ in range(N)]
+    v = [torch.full(shape, -3.0, dtype=dt, device="cuda") for _ in range(N)]
+    kf, vf = (to_device(a) for a in full)
+    tb.tp_shard_kv(plan, kf, vf, B, L, (k, v))
+    torch.cuda.synchronize()
+    for src, dst, sentinel in ((full[0], k, 7.0), (full[1], v, -3.0)):
+        ref = O.shard_kv_cache(src, N)
+        for r in range(N):
+            got = _np(dst[r])
+            assert np.array_equal(got[:B, :, :L], ref[r]), f"shard {r}"
+            rest = dst[r].float().cpu().numpy()
+            assert (rest[:, :, L:] == sentinel).all() and (rest[B:] == sentinel).all()
