@@ -827,6 +827,7 @@ struct StepArgs {
     NormPrepParams np;
     unsigned long long* bar;                // grid-barrier arrival counter (only grows)
     unsigned long long* stamps;             // optional [grid][kStepStamps]: start, barrier arrivals, end (ns)
+    unsigned bar_extra;                     // test hook: extra arrivals every grid barrier waits for (0)
 };
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
@@ -2318,7 +2319,10 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
         // this step can precede it
         const unsigned long long per_step = (unsigned long long)kSkBarriers * gridDim.x;
         const unsigned long long c = ld_acquire_u64(A.bar);
-        *s_gen0 = c - c % per_step;
+        // bar_extra (a test hook, 0 otherwise) raises every barrier's target
+        // above what the grid's arrivals reach, so the waits run out; the
+        // arrivals themselves, and so the next launch's base, are unchanged
+        *s_gen0 = c - c % per_step + A.bar_extra;
         fence_mbar_init();
     }
     __syncthreads();
@@ -2430,6 +2434,7 @@ cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
     }
     A.bar = P.bar;
     A.stamps = P.stamps;
+    A.bar_extra = P.bar_extra;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_sz[which]);
     cfg.blockDim = dim3(kStepThreads);

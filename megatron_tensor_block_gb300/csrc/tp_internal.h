@@ -219,6 +219,7 @@ struct DecodeStepParams {
     NormPrepParams np;
     unsigned long long* bar;              // grid-barrier arrival counter in the workspace (zero-initialised)
     unsigned long long* stamps;           // optional per-CTA phase end times
+    unsigned bar_extra;                   // test hook: arrivals every grid barrier waits for beyond the grid (0)
 };
 cudaError_t launch_decode_step(const DecodeStepParams& p, cudaStream_t s);
 constexpr int kMaxStepCtas = 256;        // stamp rows reserved in the workspace
