@@ -134,6 +134,18 @@ def peaks():
     return {"hbm": 6800.0, "tensor_burst": 1900.0, "tensor_sustained": 1700.0, "kind": "fallback"}
 
 
+def traffic_fields(kind: str) -> dict:
+    """`traffic` (DRAM bytes per launch of the dominant kernel) and where it
+    comes from: the committed ncu summary of that kernel, used only if it was
+    taken on the current kernel source; null otherwise."""
+    name, src_name = PROFILE[kind]
+    v = kernel_traffic(kind)
+    src = (f"profiles/{name}: dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture, taken on the "
+           f"current {src_name}" if v is not None else
+           f"none: no ncu capture of the current {src_name} (profiles/{name} predates it)")
+    return {"traffic": v, "traffic_source": src}
+
+
 def kernel_traffic(kind: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -328,7 +340,27 @@ def lens_timing(w, stream, peak: float, n: int = 50) -> dict:
             "frac_of_peak": gbs / peak, "launches": n}
 
 
-def cpu_baseline(inputs, budget_s: float = 20.0) -> dict:
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu on Arm hosts, /proc/cpuinfo elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_rate(inputs, budget_s: float) -> dict:
+    """Tokens per second of the oracle leg over about `budget_s` seconds."""
     leg = OracleLeg(inputs)
     leg.step()                                           # warm
     n, tok, t0 = 0, 0, time.perf_counter()
@@ -338,8 +370,55 @@ def cpu_baseline(inputs, budget_s: float = 20.0) -> dict:
         el = time.perf_counter() - t0
         if el >= budget_s or n >= 4096:
             break
-    return {"value": tok / el, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
-            "sample": f"{n} x " + leg.describe() + "; weights pre-sharded to float64 outside the timing"}
+    out = {"value": tok / el, "unit": "tokens/s", "steps": n, "seconds": el,
+           "sample": f"{n} x " + leg.describe() + "; weights pre-sharded to float64 outside the timing"}
+    if leg.kind == "prefill":
+        out["extrapolation"] = prefill_extrapolation(leg, el / n)
+    return out
+
+
+def prefill_extrapolation(leg, s_per_sample: float) -> dict:
+    """The whole prefill step's oracle time, extrapolated from the sample by
+    FLOPs: the sample is `chunk` prompt tokens at positions 0..chunk-1 of one
+    sequence, so its linear FLOPs scale with tokens and its attention FLOPs
+    with the visible keys."""
+    w = leg.w
+    full = sum(prefill_flops(w).values())
+    sample = sum(prefill_flops(synth.scaled(w, batch=1, tokens_per_seq=leg.chunk, kv_len=0)).values())
+    return {"method": "sample seconds x (full-step FLOPs / sample FLOPs)", "sample_flops": sample,
+            "full_step_flops": full, "full_step_s": s_per_sample * full / sample,
+            "tokens_per_s": w.tokens / (s_per_sample * full / sample)}
+
+
+def cpu_baseline(inputs, budget_s: float = 15.0) -> dict:
+    """The oracle as it stands, on the host: all cores in this process (the
+    reported value), then one thread in a child process (BLAS threads are
+    fixed when numpy loads)."""
+    w = inputs["workload"]
+    allc = oracle_rate(inputs, budget_s)
+    out = {"value": allc["value"], "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+           "kind": "oracle", "cpu_model": cpu_model(), "sample": allc["sample"]}
+    if "extrapolation" in allc:
+        out["extrapolation"] = allc["extrapolation"]
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-leg", "--workload", w.name,
+                            "--cpu-budget", str(budget_s / 2)], env=env, capture_output=True, text=True,
+                           timeout=300)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        out["single_thread"] = {"value": one["value"], "unit": "tokens/s", "cores": 1, "sample": one["sample"]}
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError, KeyError) as e:
+        out["single_thread"] = {"value": None, "error": f"{type(e).__name__}: {e}"[:200]}
+    return out
+
+
+def run_cpu_leg(args):
+    """Child process of cpu_baseline: the oracle leg with this process's
+    thread settings, as one JSON line."""
+    w = synth.WORKLOADS[args.workload]
+    r = oracle_rate(synth.make_inputs(w, with_head=False), args.cpu_budget)
+    r["threads"] = int(os.environ.get("OMP_NUM_THREADS", "0"))
+    print(json.dumps(r), flush=True)
 
 
 def config_of(w) -> dict:
@@ -374,11 +453,15 @@ def run_reference(args, world, rank):
     value = tok / el
     cores = int(os.environ["OMP_NUM_THREADS"])
     sample = (f"each step is {leg.describe()}; {n} of {args.steps} requested steps fit the {budget:.0f} s bound")
+    cpu = {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+           "sample": sample}
+    if leg.kind == "prefill":
+        cpu["extrapolation"] = prefill_extrapolation(leg, el / max(n, 1))
     line = {"impl": "reference", "metric": METRICS["moe_ep" if getattr(w, "expert_parallel", 0) else kind], "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": n, "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / max(n, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -386,6 +469,122 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+
+
+def graph_timing(fwd, stream, steps: int, warmup: int, local: int, world: int):
+    """Device-resident timing of `steps` forwards: forwards are captured
+    FWD_PER_GRAPH to a CUDA graph, so consecutive launches overlap through
+    programmatic dependent launch as they would inside a model's graph (a
+    dependency between two graph launches is a full serialisation); a
+    one-forward graph covers a remainder. Returns the slowest rank's
+    milliseconds, the forwards per graph and the clock record of the timed
+    region (barrier and device synchronisation on both sides)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fwd(stream=stream)
+    stream.synchronize()
+    per = max(1, min(FWD_PER_GRAPH, steps))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(per):
+            fwd(stream=stream)
+    graph1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph1, stream=stream):
+        fwd(stream=stream)
+    for _ in range(max(warmup, 3)):
+        graph.replay()
+        graph1.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps // per):
+            graph.replay()
+        for _ in range(steps % per):
+            graph1.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    return max_over_ranks(ev0.elapsed_time(ev1), world), per, clk
+
+
+# workloads measured beside the headline in the default run, with the number
+# of forwards that fill about a second of device time
+SIDE_WORKLOADS = {"llama3_8b_prefill_tp8": 2.7, "moe_expert_slice_tp4": 0.2, "moe_expert_parallel_tp4": 0.18}
+
+
+def side_measure(name: str, args, local: int) -> dict:
+    """Device-resident measurement of another workload, reported as a key of
+    the headline line: the same graph timing as the headline over about a
+    second of forwards (so the clock record has samples under load), then
+    events around each stage of 200 more forwards, and the roofline of the
+    dominant stage."""
+    import torch
+    import megatron_tensor_block_gb300 as tb
+    from megatron_tensor_block_gb300.runtime import Model
+    w = synth.WORKLOADS[name]
+    kind = WORKLOAD_KIND[name]
+    inputs = synth.make_inputs(w, with_head=False)
+    model = Model(inputs, share_norm=True)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    steps = max(args.steps, int(1000.0 / SIDE_WORKLOADS[name]))
+    t_ms, per, clk = graph_timing(model.forward, stream, steps, args.warmup, local, 1)
+    assert model.ws.status() == 0, f"{name}: device status after the timed region"
+    ms_step = t_ms / steps
+    stages = STAGES[kind]
+    n_prof = 200
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(n_prof)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            tb.tp_profile_stages(model.plan, evs[i])
+            model.forward(stream=stream)
+        tb.tp_profile_stages(model.plan, None)
+    torch.cuda.synchronize()
+    stage_ms = {st: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_prof))
+                for j, st in enumerate(stages)}
+    pk = peaks()
+    dom = DOMINANT[kind]
+    out = {"workload": name, "config": config_of(w), "steps": steps, "ms_per_step": ms_step,
+           "tokens_per_s": w.tokens * steps / (t_ms / 1e3), "stages_us": {k: 1e3 * v for k, v in stage_ms.items()},
+           "launch": f"CUDA graph of {per} forwards, replayed; stage times from 200 forwards with events "
+                     f"between the stages (programmatic overlap off)", "clocks": clk}
+    if kind == "prefill":
+        fl = prefill_flops(w)
+        step_tf = sum(fl.values()) / (ms_step / 1e3) / 1e12
+        dom_tf = fl[dom] / (stage_ms[dom] / 1e3) / 1e12
+        out.update(step_flops=sum(fl.values()), step_tflops=step_tf,
+                   frac_of_burst=step_tf / pk["tensor_burst"], frac_of_sustained=step_tf / pk["tensor_sustained"],
+                   frac_of_nominal_2250=step_tf / 2250.0,
+                   roofline={"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": pk["tensor_sustained"],
+                             "unit": "TFLOP/s", "frac": dom_tf / pk["tensor_sustained"],
+                             "peak_kind": pk["kind"] + " bf16 dense, sustained", "algorithmic_flops": fl[dom]},
+                   stage_tflops={k: fl[k] / (stage_ms[k] / 1e3) / 1e12 for k in stages})
+    else:
+        mb = moe_bytes(inputs)
+        sb = mb["expert_gate_up"] + mb["expert_down"]
+        gbs = sb / (ms_step / 1e3) / 1e9
+        dom_gbs = mb[dom] / (stage_ms[dom] / 1e3) / 1e9
+        out.update(step_bytes=sb, step_gbs=gbs, frac_of_peak=gbs / pk["hbm"], experts_hit=mb["experts_hit"],
+                   roofline={"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                             "frac": dom_gbs / pk["hbm"], "peak_kind": pk["kind"] + " copy bandwidth",
+                             "algorithmic_bytes": mb[dom]})
+    del model
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, world, rank, local):
@@ -407,48 +606,8 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    # ---- device-resident timing: one step = one forward. Forwards are captured
-    # FWD_PER_GRAPH to a CUDA graph, so consecutive launches overlap through
-    # programmatic dependent launch as they would inside a model's graph (a
-    # dependency between two graph launches is a full serialisation); a
-    # one-forward graph covers a remainder.
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            fwd(stream=stream)
-    stream.synchronize()
-    per = max(1, min(FWD_PER_GRAPH, args.steps))
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for _ in range(per):
-            fwd(stream=stream)
-    graph1 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph1, stream=stream):
-        fwd(stream=stream)
-    for _ in range(max(args.warmup, 3)):
-        graph.replay()
-        graph1.replay()
-    torch.cuda.synchronize()
-    assert model.ws.status() == 0, "device status after warm-up"
-
-    clocks = Clocks(local)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps // per):
-            graph.replay()
-        for _ in range(args.steps % per):
-            graph1.replay()
-        ev1.record(stream)
-    ev1.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    t_ms = ev0.elapsed_time(ev1)
-    t_ms = max_over_ranks(t_ms, world)
+    t_ms, per, clk = graph_timing(fwd, stream, args.steps, args.warmup, local, world)
+    assert model.ws.status() == 0, "device status after the timed region"
     ms_step = t_ms / args.steps
     tokens_step = w.tokens
     value = tokens_step * args.steps * world / (t_ms / 1e3)
@@ -503,7 +662,7 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "hbm", "kernel": f"chain_kernel (all {w.n_layers} layers in one persistent launch)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": pk["kind"] + " copy bandwidth", "algorithmic_bytes": sb, "launch_us": ms_step * 1e3,
-                "launch_us_isolated": kernel_ms * 1e3, "traffic": kernel_traffic("stack")}
+                "launch_us_isolated": kernel_ms * 1e3, **traffic_fields("stack")}
         extra["hbm"] = {"step_bytes": sb, "step_gbs": achieved, "frac_of_peak": achieved / peak,
                         "frac_of_8000": achieved / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
         l2_note = f"inputs larger than L2 ({sb / 1e6:.1f} MB read per step vs 129 MB L2)"
@@ -517,7 +676,7 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "hbm", "kernel": "decode_step_kernel (one persistent launch per layer)", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": pk["kind"] + " copy bandwidth",
                 "algorithmic_bytes": sb, "launch_us": launch_ms * 1e3,
-                "launch_us_isolated": kernel_ms * 1e3, "traffic": kernel_traffic(kind)}
+                "launch_us_isolated": kernel_ms * 1e3, **traffic_fields(kind)}
         if w.n_layers > 1:
             roof["note"] = "phase times of the last layer of each profiled step"
         step_gbs = step_bytes(w) / (ms_step / 1e3) / 1e9
@@ -531,7 +690,7 @@ def run_ours(args, world, rank, local):
         peak = pk["tensor_sustained"]
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_kind": pk["kind"] + " bf16 dense, sustained (kernel timed inside "
-                "a long loop of steps)", "algorithmic_flops": fl[dom], "traffic": kernel_traffic(kind)}
+                "a long loop of steps)", "algorithmic_flops": fl[dom], **traffic_fields(kind)}
         step_tf = sum(fl.values()) / (ms_step / 1e3) / 1e12
         extra["tensor"] = {"step_flops": sum(fl.values()), "step_tflops": step_tf, "frac_of_peak": step_tf / peak,
                            "peak_tflops": peak, "stage_tflops": {k: fl[k] / (stage_ms[k] / 1e3) / 1e12
@@ -544,7 +703,7 @@ def run_ours(args, world, rank, local):
         peak = pk["hbm"]
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": pk["kind"], "algorithmic_bytes": mb[dom],
-                "traffic": kernel_traffic(kind)}
+                **traffic_fields(kind)}
         sb = mb["expert_gate_up"] + mb["expert_down"]
         step_gbs = sb / (ms_step / 1e3) / 1e9
         extra["hbm"] = {"step_bytes": sb, "step_gbs": step_gbs, "frac_of_peak": step_gbs / peak, "peak_gbs": peak,
@@ -556,7 +715,7 @@ def run_ours(args, world, rank, local):
         peak = pk["hbm"]
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": pk["kind"], "algorithmic_bytes": sb[dom],
-                "traffic": kernel_traffic(kind)}
+                **traffic_fields(kind)}
         if w.n_layers > 1:
             roof["note"] = "stage times of the last layer of each step"
         step_gbs = step_bytes(w) / (ms_step / 1e3) / 1e9
@@ -651,6 +810,11 @@ def run_ours(args, world, rank, local):
         (LAUNCHES_PER_LAYER[kind] if w.dtype == "bf16" else 5) * max(w.n_layers, 1) * args.steps,
         "clocks": clk,
     }
+    if world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_side:
+        # the other measured configurations, device-timed, beside the headline
+        for name in SIDE_WORKLOADS:
+            line[WORKLOAD_KIND[name] if not synth.WORKLOADS[name].expert_parallel else "moe_ep"] = \
+                side_measure(name, args, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inputs)
     if rank == 0:
@@ -665,10 +829,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_KIND))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="default workload only: skip the prefill and MoE measurements reported beside it")
+    ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help=argparse.SUPPRESS)
     ap.add_argument("--per-layer", action="store_true",
                     help="multi-layer decode: one launch per layer (tp_block_forward) instead of one launch per "
                          "token for all layers (tp_stack_decode)")
     args = ap.parse_args()
+    if args.cpu_leg:
+        run_cpu_leg(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
