@@ -723,6 +723,11 @@ def run_ours(args, world, rank, local):
                         "frac_of_8000": step_gbs / 8000.0, "peak_gbs": peak, "peak_kind": pk["kind"]}
         l2_note = f"inputs larger than L2 ({step_bytes(w) / 1e6:.1f} MB read per step vs 129 MB L2)"
 
+    if roof.get("traffic") and roof.get("launch_us"):
+        # the DRAM rate implied by the captured traffic (steady state: L2 may still hold part of the previous
+        # step's reads, so this can sit below the algorithmic rate)
+        roof["traffic_gbs"] = roof["traffic"] / (roof["launch_us"] * 1e-6) / 1e9
+        roof["traffic_frac"] = roof["traffic_gbs"] / roof["peak"]
     if kind == "decode" and w.dtype == "bf16" and w.org_vocab:
         extra["lens"] = lens_timing(w, stream, pk["hbm"])   # reported beside the block, not in its time
 
