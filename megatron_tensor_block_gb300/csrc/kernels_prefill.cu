@@ -471,6 +471,18 @@ struct TcRowArgs {
     int* status;
 };
 
+// Tile order of the row-parallel projections (o_proj, down_proj): output-
+// column tiles vary fastest, so the CTAs resident at one time cover a few
+// token tiles across every output column. A wave then reads each of its token
+// tiles' activations (every shard's) once, and the weights, read again by
+// every wave, are loaded evict-last while the activations stream evict-first.
+// (Token tiles fastest re-read every shard's activations once per wave: 2.07
+// against 1.33 GB of DRAM reads per down_proj launch.)
+__device__ __forceinline__ void row_tile(const TcRowArgs& g, int tile, int& m0, int& n0) {
+    m0 = (tile / g.n_nt) * kTcBM;
+    n0 = (tile % g.n_nt) * kRowBN;
+}
+
 __global__ void __launch_bounds__(kRowThreads, 1) tc_row_kernel(const __grid_constant__ TcRowArgs g) {
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full, *empty, *extra;
@@ -491,8 +503,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) tc_row_kernel(const __grid_con
         if (lane == 0 && !*abort_flag) {
             uint32_t it = 0;
             bool ok = true;
+            const uint64_t pol_a = l2_evict_first_policy(), pol_b = l2_evict_last_policy();
             for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % g.n_mt) * kTcBM, n0 = (tile / g.n_mt) * kRowBN;
+                int m0, n0;
+                row_tile(g, tile, m0, n0);
                 for (int r = 0; r < g.N && ok; ++r)
                     for (int kb = 0; kb < nk; ++kb, ++it) {
                         const int s = it % kRowStages;
@@ -502,8 +516,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) tc_row_kernel(const __grid_con
                         }
                         mbar_arrive_expect_tx(&full[s], kRowStageBytes);
                         unsigned char* st = stages + s * kRowStageBytes;
-                        tma_load_2d_keep(st, &g.ta, kb * kTcBK, r * g.T + m0, &full[s]);
-                        tma_load_2d_keep(st + kTcABytes, &g.tb[r], kb * kTcBK, n0, &full[s]);
+                        tma_load_2d(st, &g.ta, kb * kTcBK, r * g.T + m0, &full[s], pol_a);
+                        tma_load_2d(st + kTcABytes, &g.tb[r], kb * kTcBK, n0, &full[s], pol_b);
                     }
             }
             volatile int no_abort = 0;
@@ -549,7 +563,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) tc_row_kernel(const __grid_con
         uint32_t pi = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const int m0 = (tile % g.n_mt) * kTcBM, n0 = (tile / g.n_mt) * kRowBN;
+            int m0, n0;
+            row_tile(g, tile, m0, n0);
             float sum[128];
             for (int r = 0; r < g.N; ++r, ++pi) {
                 const int buf = pi & 1;
