@@ -826,6 +826,12 @@ struct StepArgs {
     AttnDecodeParams a;                     // n_chunks = partial slots per KV group
     NormPrepParams np;
     unsigned long long* bar;                // grid-barrier arrival counter (only grows)
+    // Arrivals after the QKV phase, one per CTA and launch (only grows). The
+    // consumers do not wait at barrier 2 (the attention phase polls q's
+    // epochs), so a CTA may reach barrier 3 before another reaches barrier 2,
+    // and the shared counter can pass barrier 2's target early; the key block
+    // holding a new position waits on this count instead.
+    unsigned long long* kv_ready;
     unsigned long long* stamps;             // optional [grid][kStepStamps]: start, barrier arrivals, end (ns)
     unsigned bar_extra;                     // test hook: extra arrivals every grid barrier waits for (0)
 };
@@ -856,6 +862,25 @@ __device__ __forceinline__ bool sk_wait_gen(const unsigned long long* bar, unsig
     const uint64_t t0 = global_ns();
     while (true) {
         if (sk_passed(bar, base, k)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            set_status(status, TP_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Every CTA of this launch has counted its QKV phase done: kv_ready reaches
+// (launch index + 1) * grid (+ the test hook's extra, like every barrier).
+__device__ __forceinline__ bool sk_wait_kv(const StepArgs& A, unsigned long long gen0, volatile int* abort,
+                                           int* status) {
+    const unsigned long long per_step = (unsigned long long)kSkBarriers * gridDim.x;
+    const unsigned long long want = (gen0 / per_step + 1ull) * gridDim.x + gen0 % per_step;
+    if (ld_acquire_u64(A.kv_ready) >= want) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (ld_acquire_u64(A.kv_ready) >= want) return true;
         if (*abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
@@ -1210,7 +1235,7 @@ __device__ __forceinline__ bool sk_produce_attn(unsigned need, const StepArgs& A
             if (!passed && j >= g.j_new) {              // written by the QKV phase
                 sk_flush(pd, A, ring, full, gen0, abort, p.status);
                 flush_at = 0xffffffffu;
-                sk_wait_gen(A.bar, gen0, need, abort, p.status);
+                sk_wait_kv(A, gen0, abort, p.status);
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 passed = true;
             }
@@ -1273,6 +1298,39 @@ __device__ __forceinline__ void sk_norm(const NormPrepParams& p) {
 // QKV output i of tile tb (token i / 32, tile rows i % 32 and i % 32 + 32,
 // a rotary pair): the factors that do not depend on the projection -- the
 // token's 1/rms, the biases and the rotation -- and their application.
+// A (value, epoch) pair is one aligned 64-bit store: a reader that sees the
+// epoch sees the value written with it.
+__device__ __forceinline__ void sk_pair_st(unsigned long long* p, float v, unsigned ep) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p),
+                 "l"(((unsigned long long)ep << 32) | __float_as_uint(v))
+                 : "memory");
+}
+
+__device__ __forceinline__ unsigned long long sk_pair_ld(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Two consecutive pairs (16-byte aligned), polled until both carry epoch ep
+// (bounded: gives up after kWaitLimitNs or when the CTA has given up).
+__device__ __forceinline__ float2 sk_pair_wait2(const unsigned long long* p, unsigned ep, volatile int* abort,
+                                                int* status) {
+    unsigned long long a, b;
+    uint64_t t0 = 0;
+    while (true) {
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+        if (((unsigned)(a >> 32) == ep && (unsigned)(b >> 32) == ep) || *abort) break;
+        if (!t0) t0 = global_ns();
+        else if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            set_status(status, TP_ERR_TIMEOUT);
+            break;
+        }
+    }
+    return make_float2(__uint_as_float((unsigned)a), __uint_as_float((unsigned)b));
+}
+
 struct QkvPrep {
     float rinv, ba, bb, cs, sn;
 };
@@ -1301,7 +1359,7 @@ __device__ __forceinline__ QkvPrep sk_qkv_prep(const GemvParams& p, int r, int t
 }
 
 __device__ __forceinline__ void sk_qkv_apply(const GemvParams& p, int r, int tb, int i, const float* tile,
-                                             const int* s_pos, const QkvPrep& q) {
+                                             const int* s_pos, const QkvPrep& q, unsigned ep) {
     const int d = p.head_dim, half = d >> 1;
     const int t = i >> 5, j = i & 31;
     const int rowA = tile_row(EPI_QKV_ROPE, tb, j, d, 0);
@@ -1310,9 +1368,13 @@ __device__ __forceinline__ void sk_qkv_apply(const GemvParams& p, int r, int tb,
     const float vb = tile[(j + 32) * kTMax + t] * q.rinv + q.bb;
     const float ra = va * q.cs - vb * q.sn, rb = va * q.sn + vb * q.cs;
     if (head < p.hq_s) {
-        float* qo = p.q_out + ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
-        qo[0] = ra;
-        qo[half] = rb;
+        const size_t o = ((size_t)r * kTMax + t) * p.hq_s * d + head * d + ii;
+        p.q_out[o] = ra;
+        p.q_out[o + half] = rb;
+        if (p.q_pairs) {                                // read by the attention phase without a grid barrier
+            sk_pair_st(p.q_pairs + o, ra, ep);
+            sk_pair_st(p.q_pairs + o + half, rb, ep);
+        }
     } else {
         const bool is_k = head < p.hq_s + p.hkv_s;
         const int kvh = is_k ? head - p.hq_s : head - p.hq_s - p.hkv_s;
@@ -1333,7 +1395,7 @@ __device__ __forceinline__ void sk_qkv_apply(const GemvParams& p, int r, int tb,
 // the tile's rows comes from s_bias (shared) or, when null, from global memory.
 template <int EPI>
 __device__ __forceinline__ void sk_col_epilogue(const GemvParams& p, int r, int tb, const float* tile, const float* ss,
-                                                const int* s_pos, const float* s_bias, int tid0 = -1,
+                                                const int* s_pos, const float* s_bias, unsigned ep, int tid0 = -1,
                                                 int nthr = kConsumers) {
     const int tid = tid0 < 0 ? (int)threadIdx.x : tid0, T = p.T;
     if (EPI == EPI_SWIGLU) {
@@ -1348,7 +1410,7 @@ __device__ __forceinline__ void sk_col_epilogue(const GemvParams& p, int r, int 
         }
     } else {
         for (int i = tid; i < 32 * T; i += nthr)
-            sk_qkv_apply(p, r, tb, i, tile, s_pos, sk_qkv_prep(p, r, tb, i, ss, s_pos, s_bias));
+            sk_qkv_apply(p, r, tb, i, tile, s_pos, sk_qkv_prep(p, r, tb, i, ss, s_pos, s_bias), ep);
     }
 }
 
@@ -1375,7 +1437,7 @@ __device__ __forceinline__ bool fin_arrive(unsigned* cnt, unsigned expected) {
 // `tile`, then the epilogue (the tile's bias read from global memory).
 template <int EPI>
 __device__ __forceinline__ void sk_col_finish(const GemvParams& p, int seg, int np, float* tile, const float* ss,
-                                              const int* s_pos) {
+                                              const int* s_pos, unsigned ep) {
     const int tid = threadIdx.x;
     constexpr int kMaxSplit = 8;
     const int nsplit = p.shape.chunks;
@@ -1397,7 +1459,7 @@ __device__ __forceinline__ void sk_col_finish(const GemvParams& p, int seg, int 
     consumer_sync(kConsumers);
     int r, tb;
     sk_segment(p, EPI, seg, r, tb);
-    sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, nullptr);
+    sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, nullptr, ep);
     consumer_sync(kConsumers);
 }
 
@@ -1762,10 +1824,10 @@ __device__ __forceinline__ void sk_gemv(const GemvParams& p, int pi, unsigned ch
             if (EPI == EPI_QKV_ROPE) {
                 if (tid < 32 * p.T) {
                     const float* my = slot + tid * 8;
-                    sk_qkv_apply(p, r, tb, tid, tile, s_pos, QkvPrep{my[0], my[1], my[2], my[3], my[4]});
+                    sk_qkv_apply(p, r, tb, tid, tile, s_pos, QkvPrep{my[0], my[1], my[2], my[3], my[4]}, ep);
                 }
             } else {
-                sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, s_bias);
+                sk_col_epilogue<EPI>(p, r, tb, tile, ss, s_pos, s_bias, ep);
             }
             consumer_sync(kConsumers);
             continue;
@@ -1855,7 +1917,7 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
                                         uint64_t* empty, volatile int* abort, uint32_t& it, float* red,
                                         float* s_ml2, float* s_cmb, const int* s_pos, bf16* qs,
                                         const SkSegInfo* tab, const int* s_nseg, uint64_t* tab_ready,
-                                        SkQueue* qu, uint32_t& jn) {
+                                        SkQueue* qu, uint32_t& jn, unsigned ep) {
     using S = AtShape<D>;
     constexpr int KS = D / 16;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1879,14 +1941,51 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
     const int nq = listed ? min(min(nseg, kQSegs), kQStage / qper) : 0;
     {
         constexpr int kPer = kQStage / kConsumers;
+        static_assert(kPer <= 32, "one bit per staged value");
         const int n = nq * qper;
         float v[kPer];
+        if (p.q_pairs) {
+            // poll the (value, epoch) pairs: every load of a round in flight, the
+            // missing ones reloaded until each carries this launch's epoch
+            unsigned long long u[kPer];
+            unsigned need = 0;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int idx = tid + i * kConsumers;
-            if (idx < n) {
-                const int sg = idx / qper;
-                v[i] = __ldcg(p.q + tab[sg].qoff + (idx - sg * qper));
+            for (int i = 0; i < kPer; ++i) {
+                const int idx = tid + i * kConsumers;
+                if (idx < n) {
+                    const int sg = idx / qper;
+                    u[i] = sk_pair_ld(p.q_pairs + tab[sg].qoff + (idx - sg * qper));
+                    if ((unsigned)(u[i] >> 32) != ep) need |= 1u << i;
+                }
+            }
+            uint64_t t0 = 0;
+            while (need) {
+                if (*abort) break;
+                if (!t0) t0 = global_ns();
+                else if (global_ns() - t0 > kWaitLimitNs) {
+                    *abort = 1;
+                    set_status(p.status, TP_ERR_TIMEOUT);
+                    break;
+                }
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    if (need & (1u << i)) {
+                        const int idx = tid + i * kConsumers, sg = idx / qper;
+                        u[i] = sk_pair_ld(p.q_pairs + tab[sg].qoff + (idx - sg * qper));
+                        if ((unsigned)(u[i] >> 32) == ep) need &= ~(1u << i);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) v[i] = __uint_as_float((unsigned)u[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int idx = tid + i * kConsumers;
+                if (idx < n) {
+                    const int sg = idx / qper;
+                    v[i] = __ldcg(p.q + tab[sg].qoff + (idx - sg * qper));
+                }
             }
         }
 #pragma unroll
@@ -1927,12 +2026,16 @@ __device__ __forceinline__ void sk_attn(const AttnDecodeParams& p, unsigned char
                 qb[kk][1] = g < G ? *reinterpret_cast<const uint32_t*>(qp + 16 * kk + 8 + 2 * t) : 0u;
             }
         } else {
-            const float* qp = p.q + ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
+            const size_t qo = ((size_t)r * kTMax + b) * p.hq_s * D + (size_t)(kh * G + (g < G ? g : 0)) * D;
+            const float* qp = p.q + qo;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 if (g < G) {
-                    const float2 a = __ldcg(reinterpret_cast<const float2*>(qp + 16 * kk + 2 * t));
-                    const float2 c2 = __ldcg(reinterpret_cast<const float2*>(qp + 16 * kk + 8 + 2 * t));
+                    const float2 a = p.q_pairs ? sk_pair_wait2(p.q_pairs + qo + 16 * kk + 2 * t, ep, abort, p.status)
+                                               : __ldcg(reinterpret_cast<const float2*>(qp + 16 * kk + 2 * t));
+                    const float2 c2 = p.q_pairs
+                                          ? sk_pair_wait2(p.q_pairs + qo + 16 * kk + 8 + 2 * t, ep, abort, p.status)
+                                          : __ldcg(reinterpret_cast<const float2*>(qp + 16 * kk + 8 + 2 * t));
                     qb[kk][0] = pack_bf16x2(a.x * p.scale, a.y * p.scale);
                     qb[kk][1] = pack_bf16x2(c2.x * p.scale, c2.y * p.scale);
                 } else {
@@ -2237,7 +2340,7 @@ template <int D>
 __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long long base, unsigned k,
                                              volatile int* abort, SkQueue* qu, uint32_t& jn, uint32_t jf, uint32_t& jf_mark,
                                              uint32_t& nd, float* tile, const float* ss, const int* s_pos,
-                                             float* red, float* s_inv, unsigned long long* st) {
+                                             float* red, float* s_inv, unsigned long long* st, bool wait = true) {
     int* status = A.a.status;
     const bool hand_over = jf != jf_mark || k > kSkBarriers;
     consumer_sync(kConsumers);
@@ -2256,8 +2359,9 @@ __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long lo
     for (int f = 0; f < nf; ++f) {
         const SkJob j = qu->fin[f];
         if (j.type == JOB_COL) {
-            if (j.pi == 0) sk_col_finish<EPI_QKV_ROPE>(A.g[0], j.idx, (int)j.expected, tile, ss, s_pos);
-            else sk_col_finish<EPI_SWIGLU>(A.g[2], j.idx, (int)j.expected, tile, ss, s_pos);
+            const unsigned ep = (unsigned)(base / ((unsigned long long)kSkBarriers * gridDim.x)) + 1u;
+            if (j.pi == 0) sk_col_finish<EPI_QKV_ROPE>(A.g[0], j.idx, (int)j.expected, tile, ss, s_pos, ep);
+            else sk_col_finish<EPI_SWIGLU>(A.g[2], j.idx, (int)j.expected, tile, ss, s_pos, ep);
         } else if (j.type == JOB_ROW) {
             const GemvParams& p = A.g[j.pi];
             const int S = (p.K + kBoxK - 1) / kBoxK;
@@ -2269,9 +2373,12 @@ __device__ __forceinline__ void sk_phase_end(const StepArgs& A, unsigned long lo
         if (nf) qu->n_fin = 0;
         if (st) st[2 * k] = global_ns();
         if (k <= kSkBarriers) {
+            if (k == 2) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(A.kv_ready) : "memory");
             asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(A.bar) : "memory");
-            sk_wait_gen(A.bar, base, k, abort, status);
-            __threadfence();
+            if (wait) {                                 // (else the next phase polls its inputs' epochs)
+                sk_wait_gen(A.bar, base, k, abort, status);
+                __threadfence();
+            }
         }
     }
     consumer_sync(kConsumers);
@@ -2374,9 +2481,12 @@ __global__ void __maxnreg__(168) decode_step_kernel(const __grid_constant__ Step
     sk_norm(A.np);
     sk_phase_end<D>(A, gen0, 1, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_gemv<EPI_QKV_ROPE>(A.g[0], 0, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf, ep);
-    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
+    // with q published as (value, epoch) pairs the consumers only arrive at barrier 2 (the producer still
+    // waits for it before loading the key block holding a new position)
+    sk_phase_end<D>(A, gen0, 2, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st,
+                    A.a.q_pairs == nullptr);
     sk_attn<D>(A.a, ring, full, empty, abort_flag, it, red, s_ml, s_cmb, s_pos, qs, seg_tab, s_nseg, tab_ready, qu,
-               jn);
+               jn, ep);
     sk_phase_end<D>(A, gen0, 3, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
     sk_gemv<EPI_ROWPAR>(A.g[1], 1, ring, full, empty, abort_flag, it, tile, ftile, ss, s_pos, s_bias, red, qu, jn, jf, ep);
     sk_phase_end<D>(A, gen0, 4, abort_flag, qu, jn, jf, jf_mark, nd, tile, ss, s_pos, red, s_cmb, st);
@@ -2433,6 +2543,7 @@ cudaError_t launch_decode_step(const DecodeStepParams& P, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     A.bar = P.bar;
+    A.kv_ready = P.kv_ready;
     A.stamps = P.stamps;
     A.bar_extra = P.bar_extra;
     cudaLaunchConfig_t cfg = {};

@@ -58,7 +58,7 @@ struct tp_plan_s {
     size_t off_step_part = 0;           // their partials (one region, reused phase after phase)
     // workspace layout (byte offsets)
     size_t off_status = 0, off_cnt_qkv = 0, off_cnt_attn = 0, off_cnt_o = 0, off_cnt_gu = 0,
-           off_cnt_down = 0, off_step_bar = 0, ctrl_bytes = 0;
+           off_cnt_down = 0, off_step_bar = 0, off_kv_ready = 0, ctrl_bytes = 0;
     size_t off_stamps = 0;              // per-CTA phase end times of the decode step (profiling)
     size_t off_q = 0, off_attn_part = 0, off_attn_out = 0, off_h = 0, off_act = 0;
     size_t off_part_qkv = 0, off_part_o = 0, off_part_gu = 0, off_part_down = 0;
@@ -76,6 +76,8 @@ struct tp_plan_s {
     // tp_block_forward_noalloc: the decode buffers, then the down pieces' pair
     // buffer right after them (the workspace path keeps it at off_step_pairs)
     size_t na_pairs_off = 0, na_pairs_bytes = 0, na_end = 0;
+    // q of the one-launch step as (value, epoch) pairs, right after the down pieces (both layouts)
+    size_t off_q_pairs = 0, q_pairs_bytes = 0;
     size_t off_c_ctrl = 0, off_c_x = 0, off_c_q = 0, off_c_p = 0, off_c_h = 0, off_c_a = 0,
            off_c_begin = 0, off_c_end = 0;
     int c_ck = 0, c_maxch = 0;
@@ -262,6 +264,7 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         P->off_cnt_gu = take(sizeof(unsigned) * P->g_gu.groups);
         P->off_cnt_down = take(sizeof(unsigned) * P->g_down.groups);
         P->off_step_bar = take(sizeof(unsigned long long));
+        P->off_kv_ready = take(sizeof(unsigned long long));   // QKV epilogues done (one arrival per CTA and launch)
         P->off_c_ctrl = take(4 * sizeof(unsigned));   // launch counter, CTAs finished, abort flag
     }
     P->ctrl_bytes = off;
@@ -339,6 +342,8 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         // split row-parallel tiles of the one-launch step: (value, epoch) pieces of the down phase
         P->na_pairs_bytes = (size_t)P->g_down.groups * N * P->step_split[3] * kTileRows * kTMax * 8;
         P->off_step_pairs = take(P->na_pairs_bytes);
+        P->q_pairs_bytes = (size_t)kTMax * d->n_heads * hd * 8;
+        P->off_q_pairs = take(P->q_pairs_bytes);
         P->off_c_x = take((size_t)MB * H * 8);
         P->off_c_q = take((size_t)N * MB * I.qkv_rows * 8);
         P->off_c_p = take((size_t)groups * P->c_maxch * G * (hd + 2) * 8);
@@ -352,8 +357,9 @@ extern "C" tp_status tp_plan(const tp_model_desc* d, int32_t tp, tp_plan_t* out)
         // every byte a decode step writes: control words, decode buffers, pair buffer
         P->na_end = P->ws_decode_end;
         if (P->off_step_pairs) {
+            // the same two pair buffers, contiguous, after the decode buffers
             P->na_pairs_off = align256(P->ws_decode_end);
-            P->na_end = align256(P->na_pairs_off + P->na_pairs_bytes);
+            P->na_end = align256(P->na_pairs_off + (P->off_q_pairs - P->off_step_pairs) + P->q_pairs_bytes);
         }
         I.noalloc_scratch_bytes = (int64_t)P->na_end;
     }
@@ -772,8 +778,14 @@ static tp_status decode_step_bf16(tp_plan_t P, const tp_shard_set* w, const tp_k
     for (int r = 0; r < N; ++r) dn.W[r] = w->wd[r];
     dn.xact = ws + P->off_act;
     dn.pairs = pairs_off ? reinterpret_cast<unsigned long long*>(ws + pairs_off) : nullptr;
+    // q pairs sit at the same distance after the down pieces in the workspace and no-alloc layouts
+    unsigned long long* qp =
+        pairs_off ? reinterpret_cast<unsigned long long*>(ws + pairs_off + (P->off_q_pairs - P->off_step_pairs)) : nullptr;
+    st.g[0].q_pairs = qp;
+    st.a.q_pairs = qp;
 
     st.bar = reinterpret_cast<unsigned long long*>(ws + P->off_step_bar);
+    st.kv_ready = reinterpret_cast<unsigned long long*>(ws + P->off_kv_ready);
     st.bar_extra = P->dbg_bar_extra;
     st.stamps = P->n_stage_ev > 0 ? reinterpret_cast<unsigned long long*>(ws + P->off_stamps) : nullptr;
     P->last_stamps_ws = st.stamps ? ws : nullptr;
@@ -1348,8 +1360,8 @@ extern "C" tp_status tp_block_forward_noalloc(tp_plan_t plan, const tp_shard_set
     // earlier call (also epoch 1) can pass for one of this call's.
     TP_CUDA(cudaMemsetAsync(base, 0, plan->ctrl_bytes, s), "tp_block_forward_noalloc: clearing counters");
     if (plan->na_pairs_off)
-        TP_CUDA(cudaMemsetAsync(base + plan->na_pairs_off, 0, plan->na_pairs_bytes, s),
-                "tp_block_forward_noalloc: clearing the pair buffer");
+        TP_CUDA(cudaMemsetAsync(base + plan->na_pairs_off, 0, plan->na_end - plan->na_pairs_off, s),
+                "tp_block_forward_noalloc: clearing the pair buffers");
     return forward_decode(plan, w, kv, x, y, pos, B, base, plan->na_pairs_off, s);
 }
 

@@ -85,6 +85,9 @@ struct GemvParams {
     // one-launch step, row-parallel tiles split over CTAs: pieces as (value, epoch)
     // pairs [segments][chunks][kTileRows * kTMax], polled by the tile's combiner; or NULL
     unsigned long long* pairs;
+    // one-launch step, QKV: the rotated queries also as (value, epoch) pairs [N][kTMax][Hq' d],
+    // polled by the attention phase instead of a grid barrier; or NULL
+    unsigned long long* q_pairs;
 };
 
 // RMSNorm operand preparation: xg[r][t][k] = bf16(x[t][k] * gamma_r[k]),
@@ -111,6 +114,7 @@ struct AttnDecodeParams {
     unsigned part_units;               // capacity of `part` in chunk partials
     int key_busy;                      // one-launch step: CTAs 0..key_busy-1 hold a QKV tile (the rest take a
                                        // larger attention key share, prefetched into L2 during QKV)
+    const unsigned long long* q_pairs; // one-launch step: q as (value, epoch) pairs [N][kTMax][Hq' d]
 };
 
 struct CopyDesc {
@@ -218,6 +222,7 @@ struct DecodeStepParams {
     AttnDecodeParams a;
     NormPrepParams np;
     unsigned long long* bar;              // grid-barrier arrival counter in the workspace (zero-initialised)
+    unsigned long long* kv_ready;         // arrivals after the QKV phase (new K/V rows written), zero-initialised
     unsigned long long* stamps;           // optional per-CTA phase end times
     unsigned bar_extra;                   // test hook: arrivals every grid barrier waits for beyond the grid (0)
 };
