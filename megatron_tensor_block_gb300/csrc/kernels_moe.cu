@@ -27,7 +27,7 @@ constexpr int kMoeTokPass = 32;                        // slots per pass of a un
 constexpr int kMoeGroups = kMoeTokPass / 8;
 constexpr int kMoeXBytes = kMoeGroups * kBoxK * 8 * 2; // 4 activation boxes of 8 rows x 256
 constexpr int kMoeStageBytes = 2 * kBoxBytes + kMoeXBytes;
-constexpr int kMoeStages = 3;
+constexpr int kMoeStages = 4;
 constexpr int kMoeTG = 4;                // down projection with one stage per tile: tiles per unit
 constexpr int kMoeTS = kMoeTokPass + 1;  // tile row stride in shared memory (column reads free of bank conflicts)
 constexpr int kMaxExperts = 256;         // router
@@ -199,16 +199,19 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
 // stage only and stay in registers for the rest. The expert's slots are
 // processed in passes of 32 (four 8-column MMA groups).
 
+// DOWN: the expert down projection (else gate/up + SwiGLU), one instantiation
+// each so that neither epilogue shapes the other's code.
+template <bool DOWN>
 __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeArgs A) {
     const MoeParams& p = A.p;
     extern __shared__ __align__(1024) unsigned char smem[];
     const Ring R = ring_setup(smem, kMoeStages);
     unsigned char* ring = smem + 1024;                  // swizzled boxes need 1024-byte alignment
-    float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [64][kMoeTS]
-    int* s_off = reinterpret_cast<int*>(tile + kTileRows * kMoeTS);               // [E+1]
+    float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [2][64][kMoeTS]
+    int* s_off = reinterpret_cast<int*>(tile + 2 * kTileRows * kMoeTS);           // [E+1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool down = A.down != 0;
+    constexpr bool down = DOWN;
     const int nslot = p.T * p.top_k;
     const int tiles = down ? p.H / kTileRows : (2 * p.Fs) / kTileRows;
     const int K = down ? p.Fs : p.H;
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     const int wm = warp & 3, wk = warp >> 2;
     const int g = lane >> 2, tq = lane & 3;
     const int box = wm >> 1, brow = 16 * (wm & 1) + g;
-    uint32_t it = 0;
+    uint32_t it = 0, ntile = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
         const int tg = u % ngrp, le = (u / ngrp) % p.El, r = u / (ngrp * p.El);
         const int e = p.ep ? r * p.El + le : le;
@@ -336,52 +339,83 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&R.empty[sl]);
                 }
-                // tile[row][slot] = half 0 + half 1
-#pragma unroll
-                for (int q = 0; q < kMoeGroups; ++q) {
-                    const int c0 = 8 * q + 2 * tq;
-                    const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
-                    if (wk == 0) {
-                        tile[i0] = c[q][0];
-                        tile[i0 + 1] = c[q][1];
-                        tile[i1] = c[q][2];
-                        tile[i1 + 1] = c[q][3];
-                    }
-                }
-                consumer_sync(kConsumers);
-#pragma unroll
-                for (int q = 0; q < kMoeGroups; ++q) {
-                    const int c0 = 8 * q + 2 * tq;
-                    const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+                if constexpr (DOWN) {
+                    // the second K half parks its sums in one of two tile buffers; after one barrier the
+                    // first half adds them (half 0 + half 1) and stores the expert's output rows from
+                    // registers: lanes g = 0..7 write 8 consecutive rows of one slot. The next tile
+                    // writes the other buffer, so no barrier is needed after the reads.
+                    float* tb2 = tile + (ntile & 1) * (kTileRows * kMoeTS);
+                    ++ntile;
                     if (wk == 1) {
-                        tile[i0] += c[q][0];
-                        tile[i0 + 1] += c[q][1];
-                        tile[i1] += c[q][2];
-                        tile[i1 + 1] += c[q][3];
+#pragma unroll
+                        for (int q = 0; q < kMoeGroups; ++q) {
+                            const int c0 = 8 * q + 2 * tq;
+                            const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+                            tb2[i0] = c[q][0];
+                            tb2[i0 + 1] = c[q][1];
+                            tb2[i1] = c[q][2];
+                            tb2[i1 + 1] = c[q][3];
+                        }
                     }
-                }
-                consumer_sync(kConsumers);
-                const int nt = min(kMoeTokPass, cnt - ps);
-                if (down) {
-                    // expert output rows for this pass's slots (64 consecutive floats per slot)
-                    for (int i2 = tid; i2 < kTileRows * nt; i2 += kConsumers) {
-                        const int q = i2 / kTileRows, j = i2 - q * kTileRows;
-                        const int slot = off + ps + q;
-                        p.o[((size_t)r * nslot + slot) * p.H + tb * kTileRows + j] = tile[j * kMoeTS + q];
+                    consumer_sync(kConsumers);
+                    if (wk == 0) {
+                        const int nt = min(kMoeTokPass, cnt - ps);
+                        const int row0 = tb * kTileRows + 16 * wm + g;
+#pragma unroll
+                        for (int q = 0; q < kMoeGroups; ++q) {
+                            const int c0 = 8 * q + 2 * tq;
+                            const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                if (c0 + e2 < nt) {
+                                    float* o = p.o + ((size_t)r * nslot + off + ps + c0 + e2) * p.H + row0;
+                                    o[0] = c[q][e2] + tb2[i0 + e2];
+                                    o[8] = c[q][2 + e2] + tb2[i1 + e2];
+                                }
+                            }
+                        }
                     }
                 } else {
-                    bf16* act = reinterpret_cast<bf16*>(p.act);
-                    for (int i2 = tid; i2 < 32 * nt; i2 += kConsumers) {   // 32 consecutive outputs per slot
-                        const int q = i2 >> 5, j = i2 & 31;
-                        const int slot = off + ps + q;
-                        const float rv = p.rinv[slot];
-                        const float gt = tile[j * kMoeTS + q] * rv;
-                        const float up = tile[(j + 32) * kMoeTS + q] * rv;
-                        act[((size_t)r * nslot + slot) * p.Fs + tb * 32 + j] =
-                            __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                    // gate/up: tile[row][slot] = half 0 + half 1
+#pragma unroll
+                    for (int q = 0; q < kMoeGroups; ++q) {
+                        const int c0 = 8 * q + 2 * tq;
+                        const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+                        if (wk == 0) {
+                            tile[i0] = c[q][0];
+                            tile[i0 + 1] = c[q][1];
+                            tile[i1] = c[q][2];
+                            tile[i1 + 1] = c[q][3];
+                        }
                     }
+                    consumer_sync(kConsumers);
+#pragma unroll
+                    for (int q = 0; q < kMoeGroups; ++q) {
+                        const int c0 = 8 * q + 2 * tq;
+                        const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
+                        if (wk == 1) {
+                            tile[i0] += c[q][0];
+                            tile[i0 + 1] += c[q][1];
+                            tile[i1] += c[q][2];
+                            tile[i1 + 1] += c[q][3];
+                        }
+                    }
+                    consumer_sync(kConsumers);
+                    {
+                        const int nt = min(kMoeTokPass, cnt - ps);
+                        bf16* act = reinterpret_cast<bf16*>(p.act);
+                        for (int i2 = tid; i2 < 32 * nt; i2 += kConsumers) {   // 32 consecutive outputs per slot
+                            const int q = i2 >> 5, j = i2 & 31;
+                            const int slot = off + ps + q;
+                            const float rv = p.rinv[slot];
+                            const float gt = tile[j * kMoeTS + q] * rv;
+                            const float up = tile[(j + 32) * kMoeTS + q] * rv;
+                            act[((size_t)r * nslot + slot) * p.Fs + tb * 32 + j] =
+                                __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
+                        }
+                    }
+                    consumer_sync(kConsumers);
                 }
-                consumer_sync(kConsumers);
             }
         }
     }
@@ -419,7 +453,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
 // ---------------------------------------------------------------- launch sequence
 
 static size_t moe_gemm_smem(int E) {
-    return 1024 + (size_t)kMoeStages * kMoeStageBytes + (size_t)kTileRows * kMoeTS * 4 +
+    return 1024 + (size_t)kMoeStages * kMoeStageBytes + (size_t)2 * kTileRows * kMoeTS * 4 +
            (size_t)(E + 1) * 4 + 16;
 }
 
@@ -447,7 +481,9 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
     const size_t smem = moe_gemm_smem(p.E);
     static int set_bytes = -1;
     if ((int)smem > set_bytes) {
-        e = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(moe_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         set_bytes = (int)smem;
     }
@@ -475,8 +511,9 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         const int TG = (down && (p.Fs + kBoxK - 1) / kBoxK == 1) ? kMoeTG : 1;
         const int U = p.N * p.El * ((tiles + TG - 1) / TG);
         void* args[] = {&A};
-        e = launch_pdl(reinterpret_cast<const void*>(moe_gemm_kernel), args, U < kSMs ? U : kSMs, smem, s,
-                       kStreamThreads);
+        const void* fn = down ? reinterpret_cast<const void*>(moe_gemm_kernel<true>)
+                              : reinterpret_cast<const void*>(moe_gemm_kernel<false>);
+        e = launch_pdl(fn, args, U < kSMs ? U : kSMs, smem, s, kStreamThreads);
         if (e != cudaSuccess) return e;
         mark(2 + down);
     }
