@@ -10,7 +10,10 @@
 // GB300 design: one CTA per SM; a producer warp streams each CTA's weight and
 // KV tiles for all layers through a ring of 16 KB slots (TMA, 128-byte
 // swizzled 3-D boxes), so weights are in shared memory before the activation
-// they multiply exists. Activations move between phases as 8-byte pairs
+// they multiply exists. The consumer warps take a projection phase's slots as
+// independent tasks (a slot, or a K part of one when the CTA has fewer than
+// eight), each warp multiplying all rows of its slot with one operand load per
+// 16-byte unit; the tasks' partial sums meet in shared memory in a fixed order. Activations move between phases as 8-byte pairs
 // (float value, 32-bit epoch) written with one store: a consumer polls the
 // data itself, which replaces "store, fence, arrive, poll a counter, load"
 // by one round trip to L2 per phase. Every CTA that needs a whole vector
@@ -41,6 +44,7 @@ namespace {
 
 constexpr int kCW = 8;            // consumer warps
 constexpr int kCT = kCW * 32;     // consumer threads
+constexpr int kProducerRegs = 40, kConsumerRegs = 232;   // registers per thread after the split
 enum { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_D = 3 };   // projection phases (item tables)
 
 // ---- (value, epoch) pairs -------------------------------------------------------
@@ -187,49 +191,48 @@ __device__ __forceinline__ int dp_off(const ChainArgs& A, const unsigned long lo
 // ---- projection micro-kernel --------------------------------------------------------
 //
 // A load holds 8 weight rows as [row][kc chunks][64] bf16 (128-byte lines,
-// 16-byte unit u of line L stored at u ^ (L & 7)). With at most 8 tokens a
-// row's dot products are CUDA-core work (the MMA shapes would be at least half
-// empty): warp w takes row w of the box, each lane 16-byte units of it; a
-// warp's lanes read 512 contiguous bytes of weights and of the operand row.
+// 16-byte unit u of line L stored at u ^ (L & 7)); gate/up loads hold two
+// such boxes half a slot apart. With at most 8 tokens a row's dot products are
+// CUDA-core work (the MMA shapes would be at least half empty). A task is one
+// warp's share of a load: all its rows over a range of 16-byte K units, lane l
+// taking units l, l + 32, ...: the operand unit is loaded once and multiplied
+// into every row, fp32 sums per lane, then one transposing butterfly.
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float s) {
-    s = fmaf(bf_lo(w.x), bf_lo(x.x), s);
-    s = fmaf(bf_hi(w.x), bf_hi(x.x), s);
-    s = fmaf(bf_lo(w.y), bf_lo(x.y), s);
-    s = fmaf(bf_hi(w.y), bf_hi(x.y), s);
-    s = fmaf(bf_lo(w.z), bf_lo(x.z), s);
-    s = fmaf(bf_hi(w.z), bf_hi(x.z), s);
-    s = fmaf(bf_lo(w.w), bf_lo(x.w), s);
-    s = fmaf(bf_hi(w.w), bf_hi(x.w), s);
-    return s;
-}
-// this lane's part of row `warp` of the box at w times one operand row
-__device__ __forceinline__ float row_dot(const unsigned char* w, int kc, int nvalid, const bf16* xrow) {
-    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float s = 0.f;
-#pragma unroll 4
-    for (int u = lane; u < 8 * nvalid; u += 32) {
-        const int ch = u >> 3, u8 = u & 7, line = row * kc + ch;
-        const uint4 wv = *reinterpret_cast<const uint4*>(w + line * 128 + ((u8 ^ (line & 7)) << 4));
-        const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 64 * ch + 8 * u8);
-        s = dot8(wv, xv, s);
-    }
+__device__ __forceinline__ float dot8f(const uint4 w, const float (&x)[8], float s) {
+    s = fmaf(bf_lo(w.x), x[0], s);
+    s = fmaf(bf_hi(w.x), x[1], s);
+    s = fmaf(bf_lo(w.y), x[2], s);
+    s = fmaf(bf_hi(w.y), x[3], s);
+    s = fmaf(bf_lo(w.z), x[4], s);
+    s = fmaf(bf_hi(w.z), x[5], s);
+    s = fmaf(bf_lo(w.w), x[6], s);
+    s = fmaf(bf_hi(w.w), x[7], s);
     return s;
 }
 
-// the same for two boxes half a slot apart (gate and up rows), sharing the operand loads
-__device__ __forceinline__ void row_dot2(const unsigned char* w, int kc, int nvalid, const bf16* xrow, float& s0,
-                                         float& s1) {
-    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll 4
-    for (int u = lane; u < 8 * nvalid; u += 32) {
-        const int ch = u >> 3, u8 = u & 7, line = row * kc + ch;
-        const int off = line * 128 + ((u8 ^ (line & 7)) << 4);
-        const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 64 * ch + 8 * u8);
-        s0 = dot8(*reinterpret_cast<const uint4*>(w + off), xv, s0);
-        s1 = dot8(*reinterpret_cast<const uint4*>(w + kChainSlot / 2 + off), xv, s1);
+// Sums each of the NR values over the warp's 32 lanes. Round by round every
+// lane gives away half of its values and keeps the other half (lanes with the
+// round's offset bit set keep the upper half), so NR sums cost NR - 1 + (5 -
+// log2 NR) shuffles; lane l returns the total of value l >> (5 - log2 NR).
+template <int NR>
+__device__ __forceinline__ float lane_reduce(float (&a)[NR]) {
+    const int lane = threadIdx.x & 31;
+    int o = 16;
+#pragma unroll
+    for (int n = NR; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? a[i] : a[i + n / 2];
+            const float keep = up ? a[i + n / 2] : a[i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
     }
+    float v = a[0];
+#pragma unroll
+    for (; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
 }
 
 __device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
@@ -242,24 +245,27 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 // ---- shared memory ---------------------------------------------------------------------
 
 struct ChainSmem {
-    int ctrl, misc, xin, xa, gam, att, stage, qs, res, ring, total;
+    int ctrl, misc, xin, xa, gam, att, stage, qs, res, part, carry, ring, total;
 };
 constexpr int kMiscBytes = 4096;
 constexpr int kPsBytes = 16 * (128 + 8) * 2;    // attention query tile [16 rows][d + 8] bf16
 constexpr int kStageFloats = 11 * 128;      // q (G <= 8 heads), new k, new v of one group, rotation
 __host__ __device__ inline int al16(int x) { return (x + 15) & ~15; }
-__host__ __device__ inline ChainSmem chain_layout(int MB, int H, int xs, int d, int ns) {
+constexpr int kPartFloats = kTMax * 16;    // one task's partial sums: [token][up to 16 rows]
+__host__ __device__ inline ChainSmem chain_layout(int N, int MB, int H, int xs, int d, int ns) {
     ChainSmem L;
     int o = 0;
     L.ctrl = o;  o += 256;                                   // full[12], empty[12], abort
     L.misc = o;  o += kMiscBytes;
     L.xin = o;   o = al16(o + MB * H * 4);
     L.xa = o;    o = al16(o + MB * xs * 2);
-    L.gam = o;   o = al16(o + 2 * H * 4);                     // up to two gammas of a phase (float32)
+    L.gam = o;   o = al16(o + N * H * 4);                     // the shards' gammas of a phase (float32)
     L.att = o;   o += kCW * 8 * d * 4;                       // per-warp attention outputs [warp][head][d]
     L.stage = o; o += kStageFloats * 4;
     L.qs = o;    o = al16(o + kPsBytes + 2 * d * 2);           // probabilities [key][8 heads], new k, v (bf16)
     L.res = o;   o = al16(o + kChainMaxItems * MB * 8 * 4);
+    L.part = o;  o += kCW * kPartFloats * 4;                  // the partial sums of a wave of tasks
+    L.carry = o; o += 2 * kTMax * 8 * 2 * 4;                  // an item's fold state across waves (two copies)
     o = (o + 1023) & ~1023;
     L.ring = o;  o += ns * kChainSlot;
     L.total = o + 1024;                                      // slack to align the base to 1024 bytes
@@ -442,7 +448,7 @@ constexpr int kLayOff = 2048;   // byte offset of the two ChainLayer copies in t
 // register across phases.
 struct Ctx {
     unsigned char* sm;
-    int o_misc, o_xin, o_xa, o_gam, o_att, o_stage, o_qs, o_res, o_ring, ns, d;
+    int o_misc, o_xin, o_xa, o_gam, o_att, o_stage, o_qs, o_res, o_part, o_carry, o_ring, ns, d;
     uint32_t k = 0;          // ring loads consumed
     int lb = 0;              // this layer's pointer record (0 or 1)
     __device__ __forceinline__ void init(unsigned char* base, const ChainArgs& A) {
@@ -455,6 +461,8 @@ struct Ctx {
         o_stage = A.sm_stage;
         o_qs = A.sm_qs;
         o_res = A.sm_res;
+        o_part = A.sm_part;
+        o_carry = A.sm_carry;
         o_ring = A.sm_ring;
         ns = A.n_slots;
         d = A.d;
@@ -469,6 +477,8 @@ struct Ctx {
     __device__ __forceinline__ bf16* knew() const { return reinterpret_cast<bf16*>(sm + o_qs + kPsBytes); }
     __device__ __forceinline__ bf16* vnew() const { return knew() + d; }
     __device__ __forceinline__ float* res() const { return reinterpret_cast<float*>(sm + o_res); }
+    __device__ __forceinline__ float* part() const { return reinterpret_cast<float*>(sm + o_part); }
+    __device__ __forceinline__ float* carry() const { return reinterpret_cast<float*>(sm + o_carry); }
     __device__ __forceinline__ const ChainLayer* lay() const {
         return reinterpret_cast<const ChainLayer*>(sm + o_misc + kLayOff) + lb;
     }
@@ -492,41 +502,22 @@ __device__ __forceinline__ void stamp(const ChainArgs& A, int l, int ph, int w) 
     if (A.stamps && threadIdx.x == 0) A.stamps[(((size_t)blockIdx.x * A.L + l) * 5 + ph) * 2 + w] = global_ns();
 }
 
-// The gammas of a phase's items (sorted by shard): the first, and the first
-// different one if the operand buffer has room for a second copy.
-struct Gammas {
-    const float* g0;
-    const float* g1;
-};
-__device__ __forceinline__ Gammas pick_gammas(const ChainArgs& A, const float* const* g, const int* items, int cnt,
-                                              int per_shard) {
-    Gammas r{g[items[0] / per_shard], nullptr};
-    if (2 * A.H + 8 > A.xa_stride) return r;
+// Copies every shard's gamma into shared memory, [N][H] (asynchronously:
+// call before a poll).
+__device__ __forceinline__ void gammas_fetch(Ctx& C, const ChainArgs& A, const float* const* g) {
+    const int H4 = A.H / 4;
     #pragma unroll 1
-    for (int n = 1; n < cnt; ++n) {
-        const float* x = g[items[n] / per_shard];
-        if (x != r.g0) {
-            r.g1 = x;
-            break;
-        }
-    }
-    return r;
-}
-// Copies the gammas into shared memory (asynchronously: call before a poll).
-__device__ __forceinline__ void gammas_fetch(Ctx& C, const ChainArgs& A, const Gammas& gs) {
-    #pragma unroll 1
-    for (int i = threadIdx.x; i < A.H / 4; i += kCT) {
-        cp_async16(C.gam() + 4 * i, gs.g0 + 4 * i);
-        if (gs.g1) cp_async16(C.gam() + A.H + 4 * i, gs.g1 + 4 * i);
+    for (int i = threadIdx.x; i < A.N * H4; i += kCT) {
+        const int r = i / H4, e = i - r * H4;
+        cp_async16(C.gam() + r * A.H + 4 * e, g[r] + 4 * e);
     }
     cp_commit();
 }
 
 // The layer's input vector (T x H) into xin: from the pairs (src) or plain
-// (layer 0), then 1/rms per token and the bf16 operand copies x * gamma
-// (gammas staged by gammas_fetch; copy 1 at columns H..2H-1).
-__device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsigned long long* src, const float* plain, unsigned ep,
-                         bool two) {
+// (layer 0), then 1/rms per token.
+__device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsigned long long* src, const float* plain,
+                                         unsigned ep) {
     const int T = A.T, H = A.H, n2 = T * H / 2;
     float* xin = C.xin();
     bool ok = true;
@@ -540,22 +531,16 @@ __device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsig
     }
     cp_wait();
     if (csync_or(!ok)) return false;
-    // operand copies and per-token sums of squares with every thread; the
-    // warps' partial sums meet in shared memory
+    // per-token sums of squares with every thread; the warps' partial sums meet in shared memory
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float* gm = C.gam();
     float* part = C.att();                                // [token][warp] partial sums
     #pragma unroll 1
     for (int t = 0; t < T; ++t) {
         float sq = 0.f;
         #pragma unroll 1
         for (int k2 = threadIdx.x; k2 < H / 2; k2 += kCT) {
-            const int kk = 2 * k2;
-            const float2 xv = *reinterpret_cast<const float2*>(xin + t * H + kk);
+            const float2 xv = *reinterpret_cast<const float2*>(xin + t * H + 2 * k2);
             sq = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, sq));
-            bf16* xr = C.xa() + (size_t)t * A.xa_stride + kk;
-            *reinterpret_cast<uint32_t*>(xr) = pack_bf16x2(xv.x * gm[kk], xv.y * gm[kk + 1]);
-            if (two) *reinterpret_cast<uint32_t*>(xr + H) = pack_bf16x2(xv.x * gm[H + kk], xv.y * gm[H + kk + 1]);
         }
         sq = warp_sum(sq);
         if (lane == 0) part[t * kCW + warp] = sq;
@@ -571,65 +556,163 @@ __device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsig
     return true;
 }
 
-// xa (copy 0) = bf16(xin * gamma) for a further shard's gamma (read from global).
-__device__ __forceinline__ void build_xa(Ctx& C, const ChainArgs& A, const float* gamma) {
-    const int T = A.T, H = A.H;
-    csync();                                            // every warp is done with the previous operand
-    #pragma unroll 1
-    for (int i = threadIdx.x; i < T * H / 2; i += kCT) {
-        const int e = 2 * i, t = e / H, kk = e - t * H;
-        const float2 g = __ldg(reinterpret_cast<const float2*>(gamma + kk));
-        *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + kk) =
-            pack_bf16x2(C.xin()[e] * g.x, C.xin()[e + 1] * g.y);
-    }
-    csync();
+// ---- projection tasks -----------------------------------------------------------------
+//
+// A phase of a CTA holds cnt items of sl ring loads each (load js of an item:
+// shard js / nl, K range js % nl), consumed in the producer's order. Load j is
+// split into f K parts (f: the largest power of two with cnt * sl * f <= kCW,
+// at least 1), so that a CTA with few loads still keeps every warp busy. Task
+// q = j * f + part; tasks go to the warps in waves of kCW (task q to warp
+// q % kCW). Each task writes its rows' per-token partial sums to part[warp];
+// after a wave every (item, token, row) folds its tasks' partials in task
+// order: per shard the K parts and loads in order, the shards' sums in rank
+// order ((p0 + p1) + p2) + ... An item that continues into the next wave
+// leaves its state in carry.
+
+struct Phase {
+    int cnt, sl, nl, nsh, f, ntask;
+};
+__device__ __forceinline__ Phase make_phase(int cnt, int nsh, int nl) {
+    Phase P;
+    P.cnt = cnt;
+    P.nsh = nsh;
+    P.nl = nl;
+    P.sl = nsh * nl;
+    P.f = 1;
+    while (cnt * P.sl * P.f * 2 <= kCW) P.f *= 2;
+    P.ntask = cnt * P.sl * P.f;
+    return P;
 }
 
-// Row `warp` of an item whose nl loads are the next ring slots (NBOX boxes
-// per slot, half a slot apart), against every token's operand row from
-// column kbase: lane t (< T) accumulates token t's total into mine[b].
-template <int NBOX>
-__device__ __forceinline__ void item_rows(Ctx& C, const ChainArgs& A, int nl, int kc, int nch, int kbase,
-                                          float (&mine)[NBOX]) {
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t cnt) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(cnt) : "memory");
+}
+
+// The task of this warp: K part kp of f of ring load k (kc chunks per row, nv
+// of them valid), NBOX boxes of 8 rows. xl(t, ch, u8, xf) gives token t's
+// operand unit u8 of chunk ch of the load as 8 floats. Releases the load's
+// share of the slot when done.
+template <int NBOX, class XL>
+__device__ __forceinline__ void run_task(Ctx& C, const ChainArgs& A, uint32_t k, int kc, int nv, int kp, int f, XL xl) {
+    constexpr int NR = 8 * NBOX, SH = NBOX == 1 ? 2 : 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const CRing R = C.ring();
+    const unsigned char* w = ring_wait(R, k, A.status);
+    const int U = nv * 8, u0 = kp * U / f, u1 = (kp + 1) * U / f;
+    float* part = C.part() + warp * kPartFloats;
     #pragma unroll 1
-    for (int j = 0; j < nl; ++j) {
-        const unsigned char* w = ring_wait(C.ring(), C.k, A.status);
-        const int nv = min(kc, nch - j * kc);
-        #pragma unroll 1
-        for (int t = 0; t < A.T; ++t) {
-            const bf16* xr = C.xa() + (size_t)t * A.xa_stride + kbase + j * kc * 64;
-            if (NBOX == 1) {
-                const float sv = warp_sum(row_dot(w, kc, nv, xr));
-                if (lane == t) mine[0] += sv;
-            } else {
-                float s0 = 0.f, s1 = 0.f;
-                row_dot2(w, kc, nv, xr, s0, s1);
+    for (int t = 0; t < A.T; ++t) {
+        float acc[NR];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {          // the two sums side by side
-                    s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-                    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-                }
-                if (lane == t) {
-                    mine[0] += s0;
-                    mine[NBOX - 1] += s1;
+        for (int i = 0; i < NR; ++i) acc[i] = 0.f;
+        #pragma unroll 1
+        for (int u = u0 + lane; u < u1; u += 32) {
+            const int ch = u >> 3, u8 = u & 7;
+            float xf[8];
+            xl(t, ch, u8, xf);
+#pragma unroll
+            for (int row = 0; row < 8; ++row) {
+                const int line = row * kc + ch;
+                const int off = (line << 7) + ((u8 ^ (line & 7)) << 4);
+#pragma unroll
+                for (int b = 0; b < NBOX; ++b)
+                    acc[8 * b + row] =
+                        dot8f(*reinterpret_cast<const uint4*>(w + b * (kChainSlot / 2) + off), xf, acc[8 * b + row]);
+            }
+        }
+        const float v = lane_reduce<NR>(acc);
+        if ((lane & ((1 << SH) - 1)) == 0) part[t * 16 + (lane >> SH)] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cnt(&R.empty[k % R.ns], (uint32_t)(kCW / f));
+}
+
+// Runs the phase's tasks. xl(n, r, jj, t, ch, u8, xf): the operand unit of item
+// n, shard r, load jj. epi(n, t, row, v0, v1): the item's totals for (token,
+// row) -- v0 the row's sum (gate with two boxes), v1 the up row's.
+template <int NBOX, class XL, class EPI>
+__device__ __forceinline__ void run_phase(Ctx& C, const ChainArgs& A, const Phase& P, int kc, int nch, XL xl, EPI epi) {
+    const int tid = threadIdx.x, warp = tid >> 5, T = A.T;
+    const int per = P.sl * P.f;                         // tasks per item
+    int wave = 0;
+    #pragma unroll 1
+    for (int w0 = 0; w0 < P.ntask; w0 += kCW, ++wave) {
+        const int q = w0 + warp;
+        if (q < P.ntask) {
+            const int j = q / P.f, kp = q - j * P.f;
+            const int n = j / P.sl, js = j - n * P.sl, r = js / P.nl, jj = js - r * P.nl;
+            const int nv = min(kc, nch - jj * kc);
+            run_task<NBOX>(C, A, C.k + (uint32_t)j, kc, nv, kp, P.f,
+                           [&](int t, int ch, int u8, float (&xf)[8]) { xl(n, r, jj, t, ch, u8, xf); });
+        }
+        csync();
+        const int qe = min(w0 + kCW, P.ntask);
+        const int n0 = w0 / per, n1 = (qe - 1) / per;
+        const float* cin = C.carry() + ((wave - 1) & 1) * (kTMax * 16);
+        float* cout = C.carry() + (wave & 1) * (kTMax * 16);
+        #pragma unroll 1
+        for (int idx = tid; idx < (n1 - n0 + 1) * T * 8; idx += kCT) {
+            const int nn = idx / (T * 8), rem = idx - nn * (T * 8), t = rem >> 3, row = rem & 7;
+            const int n = n0 + nn, qa = max(n * per, w0), qb = min((n + 1) * per, qe);
+            float c0 = 0.f, c1 = 0.f;                   // shard sum (gate), and total so far (up)
+            if (qa > n * per) {
+                c0 = cin[(t * 8 + row) * 2];
+                c1 = cin[(t * 8 + row) * 2 + 1];
+            }
+            #pragma unroll 1
+            for (int qq = qa; qq < qb; ++qq) {
+                const float* pp = C.part() + (qq - w0) * kPartFloats + t * 16;
+                const int i = qq - n * per;
+                if (NBOX == 2) {
+                    c0 = i == 0 ? pp[row] : c0 + pp[row];
+                    c1 = i == 0 ? pp[8 + row] : c1 + pp[8 + row];
+                } else if (i == 0) {
+                    c0 = pp[row];
+                } else if (i % (P.nl * P.f) == 0) {     // first part of shard i / (nl f): fold the last one
+                    c1 = i == P.nl * P.f ? c0 : c1 + c0;
+                    c0 = pp[row];
+                } else {
+                    c0 += pp[row];
                 }
             }
-
+            if (qb == (n + 1) * per) {
+                if (NBOX == 2) epi(n, t, row, c0, c1);
+                else epi(n, t, row, P.nsh > 1 ? c1 + c0 : c0, 0.f);
+            } else {
+                cout[(t * 8 + row) * 2] = c0;
+                cout[(t * 8 + row) * 2 + 1] = c1;
+            }
         }
-        ring_release(C.ring(), C.k);
-        ++C.k;
+        if (w0 + kCW < P.ntask) csync();                // the next wave overwrites the partials
     }
+    C.k += (uint32_t)(P.ntask / P.f);
 }
 
-// The gamma copy holding shard r's operand (rebuilding copy 0 for a third distinct gamma).
-__device__ __forceinline__ int operand_col(Ctx& C, const ChainArgs& A, const Gammas& gs, const float*& have0,
-                                           const float* g) {
-    if (g == have0) return 0;
-    if (g == gs.g1) return A.H;
-    have0 = g;
-    build_xa(C, A, g);
-    return 0;
+// x * gamma_r of token t for the 16-byte unit at column k (8 floats)
+__device__ __forceinline__ void xg_unit(const Ctx& C, const ChainArgs& A, int r, int t, int k, float (&xf)[8]) {
+    const float4* x = reinterpret_cast<const float4*>(C.xin() + t * A.H + k);
+    const float4* g = reinterpret_cast<const float4*>(C.gam() + r * A.H + k);
+    const float4 x0 = x[0], x1 = x[1], g0 = g[0], g1 = g[1];
+    xf[0] = x0.x * g0.x;
+    xf[1] = x0.y * g0.y;
+    xf[2] = x0.z * g0.z;
+    xf[3] = x0.w * g0.w;
+    xf[4] = x1.x * g1.x;
+    xf[5] = x1.y * g1.y;
+    xf[6] = x1.z * g1.z;
+    xf[7] = x1.w * g1.w;
+}
+// bf16 operand row unit at element e of xa's token row t (8 floats)
+__device__ __forceinline__ void xa_unit(const Ctx& C, const ChainArgs& A, int t, int e, float (&xf)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(C.xa() + (size_t)t * A.xa_stride + e);
+    xf[0] = bf_lo(v.x);
+    xf[1] = bf_hi(v.x);
+    xf[2] = bf_lo(v.y);
+    xf[3] = bf_hi(v.y);
+    xf[4] = bf_lo(v.z);
+    xf[5] = bf_hi(v.z);
+    xf[6] = bf_lo(v.w);
+    xf[7] = bf_hi(v.w);
 }
 
 __device__ __forceinline__ bool phase_qkv(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
@@ -647,23 +730,19 @@ __device__ __forceinline__ bool phase_qkv(Ctx& C, const ChainArgs& A, int l, uns
         if (Ly.bqkv[r]) cp_async4(sbias + e, Ly.bqkv[r] + 8 * i + (e & 7));
         else sbias[e] = 0.f;
     }
-    const Gammas gs = pick_gammas(A, Ly.g_attn, items, cnt, rbq);
-    gammas_fetch(C, A, gs);
-    if (!load_vec(C, A, l == 0 ? nullptr : A.fx, l == 0 ? A.x : nullptr, ep, gs.g1 != nullptr)) return false;
+    gammas_fetch(C, A, Ly.g_attn);
+    if (!load_vec(C, A, l == 0 ? nullptr : A.fx, l == 0 ? A.x : nullptr, ep)) return false;
     stamp(A, l, 0, 0);
     const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
-    const float* have0 = gs.g0;
-    const int warp = tid >> 5, lane = tid & 31;
-    #pragma unroll 1
-    for (int n = 0; n < cnt; ++n) {
-        const int it = items[n], r = it / rbq, i = it - r * rbq;
-        const int kb = operand_col(C, A, gs, have0, Ly.g_attn[r]);
-        float mine[1] = {0.f};
-        item_rows<1>(C, A, A.nl[0], A.kc[0], A.H / 64, kb, mine);
-        if (lane < A.T)
-            ll_st(A.fq + (size_t)(r * MB + lane) * A.qkv_rows + 8 * i + warp, mine[0] * rinv[lane] + sbias[8 * n + warp],
-                  ep);
-    }
+    const int kc = A.kc[0];
+    run_phase<1>(C, A, make_phase(cnt, 1, A.nl[0]), kc, A.H / 64,
+        [&](int n, int, int jj, int t, int ch, int u8, float (&xf)[8]) {
+            xg_unit(C, A, items[n] / rbq, t, (jj * kc + ch) * 64 + 8 * u8, xf);
+        },
+        [&](int n, int t, int row, float v, float) {
+            const int it = items[n], r = it / rbq, i = it - r * rbq;
+            ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row, v * rinv[t] + sbias[8 * n + row], ep);
+        });
     stamp(A, l, 0, 1);
     return true;
 }
@@ -919,19 +998,14 @@ __device__ __forceinline__ bool phase_o(Ctx& C, const ChainArgs& A, int l, unsig
     }
     if (csync_or(!ok)) return false;
     stamp(A, l, 2, 0);
-    const int Ko = A.hq_s * d, warp = tid >> 5, lane = tid & 31;
-    #pragma unroll 1
-    for (int n = 0; n < cnt; ++n) {
-        const int i = items[n];
-        float tot = 0.f;
-        #pragma unroll 1
-        for (int r = 0; r < A.N; ++r) {
-            float mine[1] = {0.f};
-            item_rows<1>(C, A, A.nl[1], A.kc[1], Ko / 64, r * Ko, mine);
-            tot = r == 0 ? mine[0] : tot + mine[0];      // ((p0 + p1) + p2) + ...
-        }
-        if (lane < T) ll_st(A.fh + (size_t)lane * A.H + 8 * i + warp, tot + res[(n * MB + lane) * 8 + warp], ep);
-    }
+    const int Ko = A.hq_s * d, kc = A.kc[1];
+    run_phase<1>(C, A, make_phase(cnt, A.N, A.nl[1]), kc, Ko / 64,
+        [&](int, int r, int jj, int t, int ch, int u8, float (&xf)[8]) {
+            xa_unit(C, A, t, r * Ko + (jj * kc + ch) * 64 + 8 * u8, xf);
+        },
+        [&](int n, int t, int row, float v, float) {
+            ll_st(A.fh + (size_t)t * A.H + 8 * items[n] + row, v + res[(n * MB + t) * 8 + row], ep);
+        });
     stamp(A, l, 2, 1);
     return true;
 }
@@ -943,25 +1017,22 @@ __device__ __forceinline__ bool phase_gu(Ctx& C, const ChainArgs& A, int l, unsi
     if (csync_or(*C.abort())) return false;
     if (!cnt) return true;
     const int* items = C.misc() + kMiItems + PH_GU * kChainMaxItems;
-    const int tid = threadIdx.x, MB = A.max_batch, rbg = A.F_s / 8, warp = tid >> 5, lane = tid & 31;
+    const int MB = A.max_batch, rbg = A.F_s / 8;
     const ChainLayer& Ly = *C.lay();
-    const Gammas gs = pick_gammas(A, Ly.g_ffn, items, cnt, rbg);
-    gammas_fetch(C, A, gs);
-    if (!load_vec(C, A, A.fh, nullptr, ep, gs.g1 != nullptr)) return false;
+    gammas_fetch(C, A, Ly.g_ffn);
+    if (!load_vec(C, A, A.fh, nullptr, ep)) return false;
     stamp(A, l, 3, 0);
     const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
-    const float* have0 = gs.g0;
-    #pragma unroll 1
-    for (int n = 0; n < cnt; ++n) {
-        const int it = items[n], r = it / rbg, i = it - r * rbg;
-        const int kb = operand_col(C, A, gs, have0, Ly.g_ffn[r]);
-        float mine[2] = {0.f, 0.f};                         // gate, up
-        item_rows<2>(C, A, A.nl[2], A.kc[2], A.H / 64, kb, mine);
-        if (lane < A.T) {
-            const float gt = mine[0] * rinv[lane], up = mine[1] * rinv[lane];
-            ll_st(A.fa + (size_t)(r * MB + lane) * A.F_s + 8 * i + warp, gt / (1.0f + expf(-gt)) * up, ep);
-        }
-    }
+    const int kc = A.kc[2];
+    run_phase<2>(C, A, make_phase(cnt, 1, A.nl[2]), kc, A.H / 64,
+        [&](int n, int, int jj, int t, int ch, int u8, float (&xf)[8]) {
+            xg_unit(C, A, items[n] / rbg, t, (jj * kc + ch) * 64 + 8 * u8, xf);
+        },
+        [&](int n, int t, int row, float g, float u) {
+            const int it = items[n], r = it / rbg, i = it - r * rbg;
+            const float gt = g * rinv[t], up = u * rinv[t];
+            ll_st(A.fa + (size_t)(r * MB + t) * A.F_s + 8 * i + row, gt / (1.0f + expf(-gt)) * up, ep);
+        });
     stamp(A, l, 3, 1);
     return true;
 }
@@ -973,7 +1044,7 @@ __device__ __forceinline__ bool phase_d(Ctx& C, const ChainArgs& A, int l, unsig
     if (csync_or(*C.abort())) return false;
     if (!cnt) return true;
     const int* items = C.misc() + kMiItems + PH_D * kChainMaxItems;
-    const int tid = threadIdx.x, T = A.T, MB = A.max_batch, F = A.F_s, warp = tid >> 5, lane = tid & 31;
+    const int T = A.T, MB = A.max_batch, F = A.F_s;
     const int n_act = A.N * T * F / 2, nres = cnt * T * 4;
     float* res = C.res();
     // the operand (every shard's SwiGLU outputs) and this CTA's residual rows, polled together
@@ -999,22 +1070,16 @@ __device__ __forceinline__ bool phase_d(Ctx& C, const ChainArgs& A, int l, unsig
     if (csync_or(!ok)) return false;
     stamp(A, l, 4, 0);
     const bool last = l == A.L - 1;
-    #pragma unroll 1
-    for (int n = 0; n < cnt; ++n) {
-        const int i = items[n];
-        float tot = 0.f;
-        #pragma unroll 1
-        for (int r = 0; r < A.N; ++r) {
-            float mine[1] = {0.f};
-            item_rows<1>(C, A, A.nl[3], A.kc[3], F / 64, r * F, mine);
-            tot = r == 0 ? mine[0] : tot + mine[0];
-        }
-        if (lane < T) {
-            const float v = tot + res[(n * MB + lane) * 8 + warp];
-            if (last) A.y[(size_t)lane * A.H + 8 * i + warp] = v;
-            else ll_st(A.fx + (size_t)lane * A.H + 8 * i + warp, v, ep + 1);
-        }
-    }
+    const int kc = A.kc[3];
+    run_phase<1>(C, A, make_phase(cnt, A.N, A.nl[3]), kc, F / 64,
+        [&](int, int r, int jj, int t, int ch, int u8, float (&xf)[8]) {
+            xa_unit(C, A, t, r * F + (jj * kc + ch) * 64 + 8 * u8, xf);
+        },
+        [&](int n, int t, int row, float tot, float) {
+            const float v = tot + res[(n * MB + t) * 8 + row];
+            if (last) A.y[(size_t)t * A.H + 8 * items[n] + row] = v;
+            else ll_st(A.fx + (size_t)t * A.H + 8 * items[n] + row, v, ep + 1);
+        });
     stamp(A, l, 4, 1);
     return true;
 }
@@ -1050,10 +1115,17 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         reinterpret_cast<unsigned long long*>(&lay[0])[i] = reinterpret_cast<const unsigned long long*>(A.layers)[i];
     __syncthreads();
     pdl_trigger();
-    if (warp == kCW) {
-        if ((tid & 31) == 0) chain_producer(A, R, misc);
+    // Register split: the launch gives each of the 384 threads 168 registers
+    // (64512). The third warpgroup (the copy-issuing warp and three idle
+    // warps) keeps 40 each (5120), which leaves the consumers 232 each
+    // (59392): 5120 + 59392 = 64512, so the increase is always satisfiable
+    // (the launcher checks the launch's register count).
+    if (warp >= kCW) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs) : "memory");
+        if (warp == kCW && (tid & 31) == 0) chain_producer(A, R, misc);
         return;
     }
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs) : "memory");
     pdl_wait();   // inputs, positions, caches and the launch counter of the preceding kernel
     const unsigned gen = *reinterpret_cast<volatile unsigned*>(A.gen);
     if (tid < kTMax) {
@@ -1097,7 +1169,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
 }  // namespace
 
 size_t chain_smem(ChainArgs& a) {
-    const ChainSmem L = chain_layout(a.max_batch, a.H, a.xa_stride, a.d, a.n_slots);
+    const ChainSmem L = chain_layout(a.N, a.max_batch, a.H, a.xa_stride, a.d, a.n_slots);
     a.sm_misc = L.misc;
     a.sm_xin = L.xin;
     a.sm_xa = L.xa;
@@ -1106,6 +1178,8 @@ size_t chain_smem(ChainArgs& a) {
     a.sm_stage = L.stage;
     a.sm_qs = L.qs;
     a.sm_res = L.res;
+    a.sm_part = L.part;
+    a.sm_carry = L.carry;
     a.sm_ring = L.ring;
     return (size_t)L.total;
 }
@@ -1131,8 +1205,20 @@ cudaError_t chain_map(const void* W, long K, long rows, int kc, int box_rows, CU
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+static_assert(kChainThreads == 3 * 128, "two consumer warpgroups and the producer's warpgroup");
+
 cudaError_t launch_chain(const ChainArgs& a, size_t smem, cudaStream_t s) {
     static size_t configured = 0;
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(chain_kernel));
+        if (e != cudaSuccess) return e;
+        launch_regs = fa.numRegs;
+    }
+    // the consumers' register increase waits for registers the launch holds:
+    // refuse a build whose launch holds fewer than the split hands out
+    if (kChainThreads * launch_regs < 128 * kProducerRegs + 256 * kConsumerRegs) return cudaErrorInvalidConfiguration;
     if (smem > configured) {
         cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(chain_kernel),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -421,33 +421,74 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __gri
     }
 }
 
-// ---------------------------------------------------------------- combine (one CTA per token)
+// ---------------------------------------------------------------- combine
+//
+// y_t = x_t + sum over shards r (rank order) of sum over the token's choices j
+// (descending logit) of w_tj * o[r][slot(t, j)]. One CTA per (token, 512-column
+// block), one float4 column group per thread. The token's slots and weights
+// are staged in shared memory once; the (r, j) terms are walked in that order
+// in batches of 16 whose loads are all issued before any is summed, so a
+// thread waits about one memory round trip per batch.
+constexpr int kCombineCols = 512, kCombineBatch = 16;
 
-__global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
+__global__ void __launch_bounds__(kCombineCols / 4) moe_combine_kernel(const MoeParams p) {
+    __shared__ int s_slot[8];
+    __shared__ int s_owner[8];
+    __shared__ float s_w[8];
     pdl_trigger();
     pdl_wait();
-    const int t = blockIdx.x, nslot = p.T * p.top_k;
-    for (int h = threadIdx.x * 4; h < p.H; h += 1024) {
-        float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = 0; r < p.N; ++r) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < p.top_k; ++j) {
-                const int f = t * p.top_k + j;
-                if (p.ep && p.ids[f] / p.El != r) continue;   // that expert lives on another shard
-                const float w = p.wts[f];
-                const float4 v = *reinterpret_cast<const float4*>(p.o + ((size_t)r * nslot + p.slot_of[f]) * p.H + h);
-                acc.x = fmaf(w, v.x, acc.x);
-                acc.y = fmaf(w, v.y, acc.y);
-                acc.z = fmaf(w, v.z, acc.z);
-                acc.w = fmaf(w, v.w, acc.w);
-            }
-            if (r == 0) total = acc;
-            else { total.x += acc.x; total.y += acc.y; total.z += acc.z; total.w += acc.w; }
-        }
-        const float4 xv = *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + h);
-        *reinterpret_cast<float4*>(p.y + (size_t)t * p.H + h) =
-            make_float4(xv.x + total.x, xv.y + total.y, xv.z + total.z, xv.w + total.w);
+    const int nhb = (p.H + kCombineCols - 1) / kCombineCols;
+    const int t = blockIdx.x / nhb, h = (blockIdx.x - t * nhb) * kCombineCols + threadIdx.x * 4;
+    const int nslot = p.T * p.top_k, K = p.top_k, nterm = p.N * K;
+    if (threadIdx.x < K) {
+        const int f = t * K + threadIdx.x;
+        s_slot[threadIdx.x] = p.slot_of[f];
+        s_w[threadIdx.x] = p.wts[f];
+        s_owner[threadIdx.x] = p.ep ? p.ids[f] / p.El : -1;   // -1: every shard holds a slice
     }
+    __syncthreads();
+    if (h >= p.H) return;
+    const float* o = p.o + h;
+    float4 total = make_float4(0.f, 0.f, 0.f, 0.f), acc = total;
+    int r0 = 0, j0 = 0;                                 // the batch's first term
+    #pragma unroll 1
+    for (int b0 = 0; b0 < nterm; b0 += kCombineBatch) {
+        float4 v[kCombineBatch];
+        int r = r0, j = j0;
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) {
+            if (b0 + u < nterm && (s_owner[j] < 0 || s_owner[j] == r))
+                v[u] = *reinterpret_cast<const float4*>(o + ((size_t)r * nslot + s_slot[j]) * p.H);
+            if (++j == K) { j = 0; ++r; }
+        }
+        r = r0;
+        j = j0;
+#pragma unroll
+        for (int u = 0; u < kCombineBatch; ++u) {
+            if (b0 + u < nterm) {
+                if (j == 0 && r > 0) {                  // shard r-1 done: ((p0 + p1) + p2) + ...
+                    if (r == 1) total = acc;
+                    else { total.x += acc.x; total.y += acc.y; total.z += acc.z; total.w += acc.w; }
+                    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (s_owner[j] < 0 || s_owner[j] == r) {
+                    const float w = s_w[j];
+                    acc.x = fmaf(w, v[u].x, acc.x);
+                    acc.y = fmaf(w, v[u].y, acc.y);
+                    acc.z = fmaf(w, v[u].z, acc.z);
+                    acc.w = fmaf(w, v[u].w, acc.w);
+                }
+            }
+            if (++j == K) { j = 0; ++r; }
+        }
+        r0 = r;
+        j0 = j;
+    }
+    if (p.N == 1) total = acc;
+    else { total.x += acc.x; total.y += acc.y; total.z += acc.z; total.w += acc.w; }
+    const float4 xv = *reinterpret_cast<const float4*>(p.x + (size_t)t * p.H + h);
+    *reinterpret_cast<float4*>(p.y + (size_t)t * p.H + h) =
+        make_float4(xv.x + total.x, xv.y + total.y, xv.z + total.z, xv.w + total.w);
 }
 
 // ---------------------------------------------------------------- launch sequence
@@ -517,7 +558,8 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         if (e != cudaSuccess) return e;
         mark(2 + down);
     }
-    e = launch_small(reinterpret_cast<const void*>(moe_combine_kernel), &q, p.T, 256, s);
+    e = launch_small(reinterpret_cast<const void*>(moe_combine_kernel), &q,
+                     p.T * ((p.H + kCombineCols - 1) / kCombineCols), kCombineCols / 4, s);
     mark(4);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -244,7 +244,7 @@ constexpr int kStepStamps = 13;          // per CTA: start, then per phase: stre
 // weight and KV tiles for all layers through a ring of 16 KB slots, and the
 // activations between phases travel as (value, epoch) pairs so a consumer
 // polls the data itself instead of a grid barrier.
-constexpr int kChainThreads = 288;       // eight consumer warps + one producer warp
+constexpr int kChainThreads = 384;       // eight consumer warps, then a warpgroup holding the producer warp
 constexpr int kChainSlot = 16384;        // bytes per ring slot
 constexpr int kChainMaxSlots = 12;
 constexpr int kChainMaxItems = 40;       // items of one projection phase per CTA
@@ -287,10 +287,11 @@ struct ChainArgs {
     int* status;
     unsigned long long* stamps;          // optional [grid][L][5 phases][inputs arrived, outputs stored] (ns)
     int xa_stride;                       // bf16 elements per token row of the operand buffer
-    int sm_misc, sm_xin, sm_xa, sm_gam, sm_att, sm_stage, sm_qs, sm_res, sm_ring;   // shared-memory offsets
+    int sm_misc, sm_xin, sm_xa, sm_gam, sm_att, sm_stage, sm_qs, sm_res, sm_part, sm_carry,
+        sm_ring;                         // shared-memory offsets
 };
-// Fills the shared-memory offsets of `a` (max_batch, H, xa_stride, d, n_slots
-// set) and returns the dynamic shared-memory bytes of a launch.
+// Fills the shared-memory offsets of `a` (N, max_batch, H, xa_stride, d,
+// n_slots set) and returns the dynamic shared-memory bytes of a launch.
 size_t chain_smem(ChainArgs& a);
 cudaError_t launch_chain(const ChainArgs& a, size_t smem, cudaStream_t s);
 // 3-D bf16 map over a [rows][K] matrix viewed as [rows][K/64][64], boxes of
