@@ -215,8 +215,9 @@ __device__ __forceinline__ float dot8f(const uint4 w, const float (&x)[8], float
 // lane gives away half of its values and keeps the other half (lanes with the
 // round's offset bit set keep the upper half), so NR sums cost NR - 1 + (5 -
 // log2 NR) shuffles; lane l returns the total of value l >> (5 - log2 NR).
-template <int NR>
-__device__ __forceinline__ float lane_reduce(float (&a)[NR]) {
+template <int NR, int SZ>
+__device__ __forceinline__ float lane_reduce(float (&a)[SZ]) {
+    static_assert(NR <= SZ, "values to reduce");
     const int lane = threadIdx.x & 31;
     int o = 16;
 #pragma unroll
@@ -345,7 +346,9 @@ __device__ __forceinline__ AttItem att_item(const ChainArgs& A, const int* pos, 
 // One thread issues every copy of the CTA, in the order the consumers use
 // them: per layer the QKV items, the attention tiles, the o_proj items, the
 // gate/up items, the down items. Weight copies start before the preceding
-// kernel has finished (they do not depend on it); KV tiles after it.
+// kernel has finished (they do not depend on it); KV tiles after it. One loop
+// serves every projection step (the geometry is chosen at run time), so the
+// issuing code is small.
 // Copy k of the CTA into its ring slot once the slot is free: one box, or
 // two boxes half a slot apart (tm2). False if the wait gave up.
 __device__ __forceinline__ bool prod_put(const CRing& R, uint32_t k, const CUtensorMap* tm, int y, int z, uint32_t bytes,
@@ -359,67 +362,64 @@ __device__ __forceinline__ bool prod_put(const CRing& R, uint32_t k, const CUten
     return true;
 }
 
+// the projection phase of step s of a layer (steps: QKV, attention, o_proj, gate/up, down)
+__device__ __forceinline__ int step_phase(int s) { return s == 0 ? PH_QKV : s == 2 ? PH_O : s == 3 ? PH_GU : PH_D; }
+
 __device__ __forceinline__ void chain_producer(const ChainArgs& A, const CRing& R, const int* misc) {
     const uint64_t pol = l2_evict_first_policy();
     const int* cnt = misc + kMiCnt;
     const int* items = misc + kMiItems;
     uint32_t k = 0;
     bool ok = true;
-    auto put = [&](const CUtensorMap* tm, int y, int z, uint32_t bytes, const CUtensorMap* tm2, int z2) {
-        ok = prod_put(R, k, tm, y, z, bytes, tm2, z2, pol, A.status);
-        k += ok ? 1u : 0u;
-    };
     int pos[kTMax];
     bool have_pos = false;
     const int N = A.N;
     #pragma unroll 1
     for (int l = 0; l < A.L && ok; ++l) {
         const CUtensorMap* M = A.maps + (size_t)l * kChainMaps * N;   // [kind][shard]
-        const int rbq = A.qkv_rows / 8;
         #pragma unroll 1
-        for (int n = 0; n < cnt[PH_QKV] && ok; ++n) {
-            const int it = items[PH_QKV * kChainMaxItems + n], r = it / rbq, i = it - r * rbq;
-            #pragma unroll 1
-            for (int j = 0; j < A.nl[0] && ok; ++j) put(M + 0 * N + r, j * A.kc[0], 8 * i, 1024u * A.kc[0], nullptr, 0);
-        }
-        if (!have_pos) {
-            pdl_wait();                                   // KV caches and positions of the preceding kernel
-            #pragma unroll 1
-            for (int b = 0; b < kTMax; ++b) pos[b] = b < A.T ? A.pos[b] : 0;
-            have_pos = true;
-        }
-        const int na = att_count(A, pos);
-        #pragma unroll 1
-        for (int i = A.att_rank[blockIdx.x]; i < na && ok; i += A.grid) {
-            const AttItem a = att_item(A, pos, i);
-            const int row = (a.b * A.hkv_s + a.kh) * A.max_kv + a.k0;
-            const uint32_t bytes = (uint32_t)A.ck * A.d * 2;
-            put(M + 4 * N + a.r, 0, row, bytes, nullptr, 0);
-            if (ok) put(M + 5 * N + a.r, 0, row, bytes, nullptr, 0);
-        }
-        #pragma unroll 1
-        for (int n = 0; n < cnt[PH_O] && ok; ++n) {
-            const int i = items[PH_O * kChainMaxItems + n];
-            #pragma unroll 1
-            for (int r = 0; r < N && ok; ++r)
+        for (int s = 0; s < 5 && ok; ++s) {
+            if (s == 1) {
+                if (!have_pos) {
+                    pdl_wait();                                   // KV caches and positions of the preceding kernel
+                    #pragma unroll 1
+                    for (int b = 0; b < kTMax; ++b) pos[b] = b < A.T ? A.pos[b] : 0;
+                    have_pos = true;
+                }
+                const int na = att_count(A, pos);
+                const uint32_t bytes = (uint32_t)A.ck * A.d * 2;
                 #pragma unroll 1
-                for (int j = 0; j < A.nl[1] && ok; ++j) put(M + 1 * N + r, j * A.kc[1], 8 * i, 1024u * A.kc[1], nullptr, 0);
-        }
-        const int rbg = A.F_s / 8;
-        #pragma unroll 1
-        for (int n = 0; n < cnt[PH_GU] && ok; ++n) {
-            const int it = items[PH_GU * kChainMaxItems + n], r = it / rbg, i = it - r * rbg;
+                for (int i = A.att_rank[blockIdx.x]; i < na && ok; i += A.grid) {
+                    const AttItem a = att_item(A, pos, i);
+                    const int row = (a.b * A.hkv_s + a.kh) * A.max_kv + a.k0;
+                    #pragma unroll 1
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        ok = prod_put(R, k, M + (4 + kv) * N + a.r, 0, row, bytes, nullptr, 0, pol, A.status);
+                        k += ok ? 1u : 0u;
+                    }
+                }
+                continue;
+            }
+            const int ph = step_phase(s);
+            const bool col = ph == PH_QKV || ph == PH_GU;          // items of one shard; else every shard's rows
+            const int per_r = ph == PH_QKV ? A.qkv_rows / 8 : A.F_s / 8;
+            const int nsh = col ? 1 : N, nl = A.nl[ph], kc = A.kc[ph];
+            const uint32_t bytes = (ph == PH_GU ? 2048u : 1024u) * kc;
             #pragma unroll 1
-            for (int j = 0; j < A.nl[2] && ok; ++j)
-                put(M + 2 * N + r, j * A.kc[2], 8 * i, 2048u * A.kc[2], M + 2 * N + r, A.F_s + 8 * i);
-        }
-        #pragma unroll 1
-        for (int n = 0; n < cnt[PH_D] && ok; ++n) {
-            const int i = items[PH_D * kChainMaxItems + n];
-            #pragma unroll 1
-            for (int r = 0; r < N && ok; ++r)
+            for (int n = 0; n < cnt[ph] && ok; ++n) {
+                const int it = items[ph * kChainMaxItems + n];
+                const int r0 = col ? it / per_r : 0, i = col ? it - r0 * per_r : it;
                 #pragma unroll 1
-                for (int j = 0; j < A.nl[3] && ok; ++j) put(M + 3 * N + r, j * A.kc[3], 8 * i, 1024u * A.kc[3], nullptr, 0);
+                for (int r = r0; r < r0 + nsh && ok; ++r) {
+                    const CUtensorMap* tm = M + ph * N + r;
+                    #pragma unroll 1
+                    for (int j = 0; j < nl && ok; ++j) {
+                        ok = prod_put(R, k, tm, j * kc, 8 * i, bytes, ph == PH_GU ? tm : nullptr, A.F_s + 8 * i, pol,
+                                      A.status);
+                        k += ok ? 1u : 0u;
+                    }
+                }
+            }
         }
     }
     // every copy issued has landed before this thread leaves (if the consumers
@@ -514,25 +514,10 @@ __device__ __forceinline__ void gammas_fetch(Ctx& C, const ChainArgs& A, const f
     cp_commit();
 }
 
-// The layer's input vector (T x H) into xin: from the pairs (src) or plain
-// (layer 0), then 1/rms per token.
-__device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsigned long long* src, const float* plain,
-                                         unsigned ep) {
-    const int T = A.T, H = A.H, n2 = T * H / 2;
-    float* xin = C.xin();
-    bool ok = true;
-    if (plain) {
-        #pragma unroll 1
-        for (int i = threadIdx.x; i < n2; i += kCT)
-            *reinterpret_cast<float2*>(xin + 2 * i) = *reinterpret_cast<const float2*>(plain + 2 * (size_t)i);
-    } else {
-        ok = poll_space(A, n2, ep, C.abort(), [&](int i) { return dp_off(A, src) + i; },
-                        [&](int i, float a, float b) { *reinterpret_cast<float2*>(xin + 2 * i) = make_float2(a, b); });
-    }
-    cp_wait();
-    if (csync_or(!ok)) return false;
-    // per-token sums of squares with every thread; the warps' partial sums meet in shared memory
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// 1/rms of every token of xin (T x H, float32) into the misc area.
+__device__ __forceinline__ void rms_stats(Ctx& C, const ChainArgs& A) {
+    const int T = A.T, H = A.H, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* xin = C.xin();
     float* part = C.att();                                // [token][warp] partial sums
     #pragma unroll 1
     for (int t = 0; t < T; ++t) {
@@ -553,21 +538,79 @@ __device__ __forceinline__ bool load_vec(Ctx& C, const ChainArgs& A, const unsig
         reinterpret_cast<float*>(C.misc())[kMiRinv + threadIdx.x] = 1.0f / sqrtf(a * (1.0f / (float)H) + A.eps);
     }
     csync();
-    return true;
 }
 
-// ---- projection tasks -----------------------------------------------------------------
+// The o_proj operand: every CTA with o_proj items combines the split-KV
+// partials of all groups itself (chunks in order: running max, rescaled
+// sums) into xa, [token][shard r's heads] bf16.
+__device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned ep) {
+    const int tid = threadIdx.x, T = A.T, MB = A.max_batch, G = A.G, d = A.d, hk = A.hkv_s;
+    const int* nch_t = C.misc() + kMiNch;
+    const int nq = A.N * T * hk * G * (d / 4);
+    bool ok = true;
+    #pragma unroll 1
+    for (int q = tid; q < nq; q += kCT) {
+        const int e4 = q % (d / 4), rest = q / (d / 4), j = rest % G, rest2 = rest / G, kh = rest2 % hk;
+        const int rt = rest2 / hk, t = rt % T, r = rt / T, n = nch_t[t];
+        const int gi = (r * MB + t) * hk + kh;
+        float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
+        int c0 = 0;
+        do {
+            int off[kPoll];
+            unsigned long long v[kPoll][2];
+#pragma unroll
+            for (int u = 0; u < kPoll; ++u) off[u] = -1;
+            const int nb = min(2, n - c0);                 // 3 double pairs per chunk
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                if (c < nb) {
+                    const int base = dp_off(A, A.fp + ((size_t)gi * A.maxch + c0 + c) * G * (d + 2));
+                    off[3 * c] = base + (j * d + 4 * e4) / 2;
+                    off[3 * c + 1] = off[3 * c] + 1;
+                    off[3 * c + 2] = base + (G * d + 2 * j) / 2;
+                }
+            ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                if (c < nb) {
+                    const float mc = ll_val(v[3 * c + 2][0]), Mn = fmaxf(M, mc);
+                    const float fa = ex2_approx(M - Mn), fb = ex2_approx(mc - Mn);
+                    den = fmaf(den, fa, ll_val(v[3 * c + 2][1]) * fb);
+                    num0 = fmaf(num0, fa, ll_val(v[3 * c][0]) * fb);
+                    num1 = fmaf(num1, fa, ll_val(v[3 * c][1]) * fb);
+                    num2 = fmaf(num2, fa, ll_val(v[3 * c + 1][0]) * fb);
+                    num3 = fmaf(num3, fa, ll_val(v[3 * c + 1][1]) * fb);
+                    M = Mn;
+                }
+            c0 += max(nb, 0);
+        } while (c0 < n && ok);
+        const float inv = den > 0.f ? 1.0f / den : 0.f;
+        bf16* dst = C.xa() + (size_t)t * A.xa_stride + r * A.hq_s * d + (kh * G + j) * d + 4 * e4;
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(num0 * inv, num1 * inv);
+        *reinterpret_cast<uint32_t*>(dst + 2) = pack_bf16x2(num2 * inv, num3 * inv);
+    }
+    return ok;
+}
+
+// ---- projection steps -------------------------------------------------------------------
 //
-// A phase of a CTA holds cnt items of sl ring loads each (load js of an item:
+// A step of a CTA holds cnt items of sl ring loads each (load js of an item:
 // shard js / nl, K range js % nl), consumed in the producer's order. Load j is
 // split into f K parts (f: the largest power of two with cnt * sl * f <= kCW,
 // at least 1), so that a CTA with few loads still keeps every warp busy. Task
 // q = j * f + part; tasks go to the warps in waves of kCW (task q to warp
-// q % kCW). Each task writes its rows' per-token partial sums to part[warp];
-// after a wave every (item, token, row) folds its tasks' partials in task
-// order: per shard the K parts and loads in order, the shards' sums in rank
-// order ((p0 + p1) + p2) + ... An item that continues into the next wave
-// leaves its state in carry.
+// q % kCW). A task is one warp's share of a load: all its rows (8, or 16 for
+// gate/up) over a range of 16-byte K units, lane l taking units l, l + 32,
+// ...: the operand unit is loaded once and multiplied into every row, fp32
+// sums per lane, then one transposing butterfly; the per-token partial sums
+// go to part[warp]. After a wave every (item, token, row) folds its tasks'
+// partials in task order: per shard the K parts and loads in order, the
+// shards' sums in rank order ((p0 + p1) + p2) + ... An item that continues
+// into the next wave leaves its state in carry.
+//
+// One copy of this code serves all four projection steps of every layer (the
+// operand, geometry and epilogue are chosen at run time), so that the code a
+// layer runs stays small.
 
 struct Phase {
     int cnt, sl, nl, nsh, f, ntask;
@@ -588,64 +631,141 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t cnt) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(cnt) : "memory");
 }
 
-// The task of this warp: K part kp of f of ring load k (kc chunks per row, nv
-// of them valid), NBOX boxes of 8 rows. xl(t, ch, u8, xf) gives token t's
-// operand unit u8 of chunk ch of the load as 8 floats. Releases the load's
-// share of the slot when done.
-template <int NBOX, class XL>
-__device__ __forceinline__ void run_task(Ctx& C, const ChainArgs& A, uint32_t k, int kc, int nv, int kp, int f, XL xl) {
-    constexpr int NR = 8 * NBOX, SH = NBOX == 1 ? 2 : 1;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const CRing R = C.ring();
-    const unsigned char* w = ring_wait(R, k, A.status);
-    const int U = nv * 8, u0 = kp * U / f, u1 = (kp + 1) * U / f;
-    float* part = C.part() + warp * kPartFloats;
-    #pragma unroll 1
-    for (int t = 0; t < A.T; ++t) {
-        float acc[NR];
-#pragma unroll
-        for (int i = 0; i < NR; ++i) acc[i] = 0.f;
+// The step's input vector: the layer input x (step QKV) or the residual
+// stream after attention (gate/up) into xin as float32, or every shard's
+// SwiGLU outputs (down) into xa as bf16; then, for QKV and gate/up, 1/rms
+// per token. Every CTA loads x and h, items or not: they are the residuals
+// of the o_proj and down epilogues.
+__device__ __forceinline__ bool step_input(Ctx& C, const ChainArgs& A, int l, int ph, unsigned ep) {
+    const int T = A.T, H = A.H;
+    bool ok = true;
+    if (ph == PH_QKV && l == 0) {
         #pragma unroll 1
-        for (int u = u0 + lane; u < u1; u += 32) {
-            const int ch = u >> 3, u8 = u & 7;
-            float xf[8];
-            xl(t, ch, u8, xf);
-#pragma unroll
-            for (int row = 0; row < 8; ++row) {
-                const int line = row * kc + ch;
-                const int off = (line << 7) + ((u8 ^ (line & 7)) << 4);
-#pragma unroll
-                for (int b = 0; b < NBOX; ++b)
-                    acc[8 * b + row] =
-                        dot8f(*reinterpret_cast<const uint4*>(w + b * (kChainSlot / 2) + off), xf, acc[8 * b + row]);
-            }
-        }
-        const float v = lane_reduce<NR>(acc);
-        if ((lane & ((1 << SH) - 1)) == 0) part[t * 16 + (lane >> SH)] = v;
+        for (int i = threadIdx.x; i < T * H / 2; i += kCT)
+            *reinterpret_cast<float2*>(C.xin() + 2 * i) = *reinterpret_cast<const float2*>(A.x + 2 * (size_t)i);
+    } else {
+        const bool down = ph == PH_D;
+        const unsigned long long* src = ph == PH_QKV ? A.fx : down ? A.fa : A.fh;
+        const int cols = (down ? A.N * A.F_s : H) / 2;     // double pairs per token
+        ok = poll_space(A, T * cols, ep, C.abort(), [&](int i) { return dp_off(A, src) + i; },
+            [&](int i, float a, float b) {
+                if (down) {
+                    const int t = i / cols, c = i - t * cols;
+                    *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + 2 * c) = pack_bf16x2(a, b);
+                } else {
+                    *reinterpret_cast<float2*>(C.xin() + 2 * i) = make_float2(a, b);
+                }
+            });
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cnt(&R.empty[k % R.ns], (uint32_t)(kCW / f));
+    cp_wait();
+    if (csync_or(!ok)) return false;
+    if (ph != PH_D) rms_stats(C, A);
+    return true;
 }
 
-// Runs the phase's tasks. xl(n, r, jj, t, ch, u8, xf): the operand unit of item
-// n, shard r, load jj. epi(n, t, row, v0, v1): the item's totals for (token,
-// row) -- v0 the row's sum (gate with two boxes), v1 the up row's.
-template <int NBOX, class XL, class EPI>
-__device__ __forceinline__ void run_phase(Ctx& C, const ChainArgs& A, const Phase& P, int kc, int nch, XL xl, EPI epi) {
-    const int tid = threadIdx.x, warp = tid >> 5, T = A.T;
-    const int per = P.sl * P.f;                         // tasks per item
+__device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, unsigned ep, int ph) {
+    const int cnt = C.misc()[kMiCnt + ph];
+    if (csync_or(*C.abort())) return false;
+    const int* items = C.misc() + kMiItems + ph * kChainMaxItems;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, T = A.T, MB = A.max_batch, H = A.H, N = A.N;
+    const ChainLayer& Ly = *C.lay();
+    const bool norm = ph == PH_QKV || ph == PH_GU;     // RMSNorm input: operand x * gamma_r, items of one shard
+    const int per_r = ph == PH_QKV ? A.qkv_rows / 8 : A.F_s / 8;
+    const int sidx = ph == PH_QKV ? 0 : ph == PH_O ? 2 : ph == PH_GU ? 3 : 4;   // step (stamps)
+    if ((ph == PH_O || ph == PH_D) && !cnt) return true;
+    if (ph == PH_QKV) {                                  // biases into shared memory while the input is polled
+        float* sbias = C.res();
+        #pragma unroll 1
+        for (int e = tid; e < 8 * cnt; e += kCT) {
+            const int it = items[e >> 3], r = it / per_r, i = it - r * per_r;
+            if (Ly.bqkv[r]) cp_async4(sbias + e, Ly.bqkv[r] + 8 * i + (e & 7));
+            else sbias[e] = 0.f;
+        }
+    }
+    if (norm) gammas_fetch(C, A, ph == PH_QKV ? Ly.g_attn : Ly.g_ffn);
+    if (ph == PH_O) {
+        const bool ok = combine_att(C, A, ep);
+        if (csync_or(!ok)) return false;
+    } else if (!step_input(C, A, l, ph, ep)) {
+        return false;
+    }
+    stamp(A, l, sidx, 0);
+    if (!cnt) return true;
+
+    const int nsh = norm ? 1 : N, nl = A.nl[ph], kc = A.kc[ph];
+    const int Ks = ph == PH_O ? A.hq_s * A.d : ph == PH_D ? A.F_s : H;   // operand columns per shard
+    const int nch = Ks / 64, nbox = ph == PH_GU ? 2 : 1;
+    const Phase P = make_phase(cnt, nsh, nl);
+    const int per = P.sl * P.f;                          // tasks per item
+    const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
+    const CRing R = C.ring();
     int wave = 0;
     #pragma unroll 1
     for (int w0 = 0; w0 < P.ntask; w0 += kCW, ++wave) {
         const int q = w0 + warp;
         if (q < P.ntask) {
             const int j = q / P.f, kp = q - j * P.f;
-            const int n = j / P.sl, js = j - n * P.sl, r = js / P.nl, jj = js - r * P.nl;
-            const int nv = min(kc, nch - jj * kc);
-            run_task<NBOX>(C, A, C.k + (uint32_t)j, kc, nv, kp, P.f,
-                           [&](int t, int ch, int u8, float (&xf)[8]) { xl(n, r, jj, t, ch, u8, xf); });
+            const int n = j / P.sl, js = j - n * P.sl, r = js / nl, jj = js - r * nl;
+            const int nv = min(kc, nch - jj * kc), U = nv * 8, u0 = kp * U / P.f, u1 = (kp + 1) * U / P.f;
+            const uint32_t k = C.k + (uint32_t)j;
+            const unsigned char* w = ring_wait(R, k, A.status);
+            const int kb = jj * kc * 64;                 // the load's first operand column
+            const float* gam = C.gam() + (items[n] / per_r) * H + kb;
+            const bf16* xa0 = C.xa() + r * Ks + kb;
+            float* part = C.part() + warp * kPartFloats;
+            #pragma unroll 1
+            for (int t = 0; t < T; ++t) {
+                float acc[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                #pragma unroll 1
+                for (int u = u0 + lane; u < u1; u += 32) {
+                    const int ch = u >> 3, u8 = u & 7, e = 64 * ch + 8 * u8;
+                    float xf[8];
+                    if (norm) {
+                        const float4* xp = reinterpret_cast<const float4*>(C.xin() + t * H + kb + e);
+                        const float4* gp = reinterpret_cast<const float4*>(gam + e);
+                        const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
+                        xf[0] = x0.x * g0.x;
+                        xf[1] = x0.y * g0.y;
+                        xf[2] = x0.z * g0.z;
+                        xf[3] = x0.w * g0.w;
+                        xf[4] = x1.x * g1.x;
+                        xf[5] = x1.y * g1.y;
+                        xf[6] = x1.z * g1.z;
+                        xf[7] = x1.w * g1.w;
+                    } else {
+                        const uint4 v = *reinterpret_cast<const uint4*>(xa0 + (size_t)t * A.xa_stride + e);
+                        xf[0] = bf_lo(v.x);
+                        xf[1] = bf_hi(v.x);
+                        xf[2] = bf_lo(v.y);
+                        xf[3] = bf_hi(v.y);
+                        xf[4] = bf_lo(v.z);
+                        xf[5] = bf_hi(v.z);
+                        xf[6] = bf_lo(v.w);
+                        xf[7] = bf_hi(v.w);
+                    }
+#pragma unroll
+                    for (int row = 0; row < 8; ++row) {
+                        const int line = row * kc + ch;
+                        const unsigned char* wl = w + (line << 7) + ((u8 ^ (line & 7)) << 4);
+                        acc[row] = dot8f(*reinterpret_cast<const uint4*>(wl), xf, acc[row]);
+                        if (nbox == 2) acc[8 + row] = dot8f(*reinterpret_cast<const uint4*>(wl + kChainSlot / 2), xf, acc[8 + row]);
+                    }
+                }
+                if (nbox == 2) {
+                    const float v = lane_reduce<16>(acc);
+                    if (!(lane & 1)) part[t * 16 + (lane >> 1)] = v;
+                } else {
+                    const float v = lane_reduce<8>(acc);
+                    if (!(lane & 3)) part[t * 16 + (lane >> 2)] = v;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cnt(&R.empty[k % R.ns], (uint32_t)(kCW / P.f));
         }
         csync();
+        // fold the wave's partials; items that end in this wave run the epilogue
         const int qe = min(w0 + kCW, P.ntask);
         const int n0 = w0 / per, n1 = (qe - 1) / per;
         const float* cin = C.carry() + ((wave - 1) & 1) * (kTMax * 16);
@@ -663,87 +783,46 @@ __device__ __forceinline__ void run_phase(Ctx& C, const ChainArgs& A, const Phas
             for (int qq = qa; qq < qb; ++qq) {
                 const float* pp = C.part() + (qq - w0) * kPartFloats + t * 16;
                 const int i = qq - n * per;
-                if (NBOX == 2) {
+                if (nbox == 2) {
                     c0 = i == 0 ? pp[row] : c0 + pp[row];
                     c1 = i == 0 ? pp[8 + row] : c1 + pp[8 + row];
                 } else if (i == 0) {
                     c0 = pp[row];
-                } else if (i % (P.nl * P.f) == 0) {     // first part of shard i / (nl f): fold the last one
-                    c1 = i == P.nl * P.f ? c0 : c1 + c0;
+                } else if (i % (nl * P.f) == 0) {       // first part of shard i / (nl f): fold the last one
+                    c1 = i == nl * P.f ? c0 : c1 + c0;
                     c0 = pp[row];
                 } else {
                     c0 += pp[row];
                 }
             }
-            if (qb == (n + 1) * per) {
-                if (NBOX == 2) epi(n, t, row, c0, c1);
-                else epi(n, t, row, P.nsh > 1 ? c1 + c0 : c0, 0.f);
-            } else {
+            if (qb < (n + 1) * per) {
                 cout[(t * 8 + row) * 2] = c0;
                 cout[(t * 8 + row) * 2 + 1] = c1;
+                continue;
+            }
+            // epilogue of item n, token t, row
+            const int it = items[n];
+            if (norm) {
+                const int r = it / per_r, i = it - r * per_r;
+                if (ph == PH_QKV) {
+                    ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row,
+                          c0 * rinv[t] + C.res()[8 * n + row], ep);
+                } else {
+                    const float gt = c0 * rinv[t], up = c1 * rinv[t];
+                    ll_st(A.fa + (size_t)(t * N + r) * A.F_s + 8 * i + row, gt / (1.0f + expf(-gt)) * up, ep);
+                }
+            } else {
+                const int e = t * H + 8 * it + row;
+                const float v = (nsh > 1 ? c1 + c0 : c0) + C.xin()[e];   // + the residual
+                if (ph == PH_O) ll_st(A.fh + e, v, ep);
+                else if (l == A.L - 1) A.y[e] = v;
+                else ll_st(A.fx + e, v, ep + 1);
             }
         }
         if (w0 + kCW < P.ntask) csync();                // the next wave overwrites the partials
     }
     C.k += (uint32_t)(P.ntask / P.f);
-}
-
-// x * gamma_r of token t for the 16-byte unit at column k (8 floats)
-__device__ __forceinline__ void xg_unit(const Ctx& C, const ChainArgs& A, int r, int t, int k, float (&xf)[8]) {
-    const float4* x = reinterpret_cast<const float4*>(C.xin() + t * A.H + k);
-    const float4* g = reinterpret_cast<const float4*>(C.gam() + r * A.H + k);
-    const float4 x0 = x[0], x1 = x[1], g0 = g[0], g1 = g[1];
-    xf[0] = x0.x * g0.x;
-    xf[1] = x0.y * g0.y;
-    xf[2] = x0.z * g0.z;
-    xf[3] = x0.w * g0.w;
-    xf[4] = x1.x * g1.x;
-    xf[5] = x1.y * g1.y;
-    xf[6] = x1.z * g1.z;
-    xf[7] = x1.w * g1.w;
-}
-// bf16 operand row unit at element e of xa's token row t (8 floats)
-__device__ __forceinline__ void xa_unit(const Ctx& C, const ChainArgs& A, int t, int e, float (&xf)[8]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(C.xa() + (size_t)t * A.xa_stride + e);
-    xf[0] = bf_lo(v.x);
-    xf[1] = bf_hi(v.x);
-    xf[2] = bf_lo(v.y);
-    xf[3] = bf_hi(v.y);
-    xf[4] = bf_lo(v.z);
-    xf[5] = bf_hi(v.z);
-    xf[6] = bf_lo(v.w);
-    xf[7] = bf_hi(v.w);
-}
-
-__device__ __forceinline__ bool phase_qkv(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
-    const int cnt = C.misc()[kMiCnt + PH_QKV];
-    if (csync_or(*C.abort())) return false;
-    if (!cnt) return true;
-    const int* items = C.misc() + kMiItems + PH_QKV * kChainMaxItems;
-    const int rbq = A.qkv_rows / 8, tid = threadIdx.x, MB = A.max_batch;
-    const ChainLayer& Ly = *C.lay();
-    // biases and gammas into shared memory while the input is polled
-    float* sbias = C.res();
-    #pragma unroll 1
-    for (int e = tid; e < 8 * cnt; e += kCT) {
-        const int it = items[e >> 3], r = it / rbq, i = it - r * rbq;
-        if (Ly.bqkv[r]) cp_async4(sbias + e, Ly.bqkv[r] + 8 * i + (e & 7));
-        else sbias[e] = 0.f;
-    }
-    gammas_fetch(C, A, Ly.g_attn);
-    if (!load_vec(C, A, l == 0 ? nullptr : A.fx, l == 0 ? A.x : nullptr, ep)) return false;
-    stamp(A, l, 0, 0);
-    const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
-    const int kc = A.kc[0];
-    run_phase<1>(C, A, make_phase(cnt, 1, A.nl[0]), kc, A.H / 64,
-        [&](int n, int, int jj, int t, int ch, int u8, float (&xf)[8]) {
-            xg_unit(C, A, items[n] / rbq, t, (jj * kc + ch) * 64 + 8 * u8, xf);
-        },
-        [&](int n, int t, int row, float v, float) {
-            const int it = items[n], r = it / rbq, i = it - r * rbq;
-            ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row, v * rinv[t] + sbias[8 * n + row], ep);
-        });
-    stamp(A, l, 0, 1);
+    stamp(A, l, sidx, 1);
     return true;
 }
 
@@ -909,181 +988,6 @@ __device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, uns
     return true;
 }
 
-// o_proj: every CTA with o_proj items combines the split-KV partials of all
-// groups itself (chunks in order: running max, rescaled sums), then each item
-// sums its shards' partial outputs in rank order and adds the residual.
-__device__ __forceinline__ bool phase_o(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
-    const int cnt = C.misc()[kMiCnt + PH_O];
-    if (csync_or(*C.abort())) return false;
-    if (!cnt) return true;
-    const int* items = C.misc() + kMiItems + PH_O * kChainMaxItems;
-    const int tid = threadIdx.x, T = A.T, MB = A.max_batch, G = A.G, d = A.d, hk = A.hkv_s;
-    const int* nch_t = C.misc() + kMiNch;
-    const int nq = A.N * T * hk * G * (d / 4), nres = cnt * T * 4;
-    float* res = C.res();
-    auto res_at = [&](int p, int& t) {                  // residual double pair p: (item, token, column pair)
-        const int it = p / (T * 4), rem = p - it * T * 4;
-        t = rem >> 2;
-        return t * A.H + 8 * items[it] + 2 * (rem & 3);
-    };
-    if (l == 0)                                         // the layer's input is the caller's x
-        #pragma unroll 1
-        for (int p = tid; p < nres; p += kCT) {
-            int t;
-            const int e = res_at(p, t);
-            *reinterpret_cast<float2*>(res + (p / (T * 4) * MB + t) * 8 + 2 * (p & 3)) =
-                *reinterpret_cast<const float2*>(A.x + e);
-        }
-    bool ok = true;
-    const int passes = (max(nq, nres) + kCT - 1) / kCT;
-    #pragma unroll 1
-    for (int pass = 0; pass < passes; ++pass) {
-        const int q = tid + pass * kCT;
-        int r = 0, t = 0, kh = 0, j = 0, e4 = 0, n = 0;
-        if (q < nq) {
-            e4 = q % (d / 4);
-            const int rest = q / (d / 4);
-            j = rest % G;
-            const int rest2 = rest / G;
-            kh = rest2 % hk;
-            const int rt = rest2 / hk;
-            t = rt % T;
-            r = rt / T;
-            n = nch_t[t];
-        }
-        const int gi = (r * MB + t) * hk + kh;
-        const bool rs = pass == 0 && l > 0 && tid < nres;
-        float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
-        int c0 = 0;
-        do {
-            int off[kPoll];
-            unsigned long long v[kPoll][2];
-#pragma unroll
-            for (int u = 0; u < kPoll; ++u) off[u] = -1;
-            const int nb = min(2, n - c0);                 // 3 double pairs per chunk
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-                if (c < nb) {
-                    const int base = dp_off(A, A.fp + ((size_t)gi * A.maxch + c0 + c) * G * (d + 2));
-                    off[3 * c] = base + (j * d + 4 * e4) / 2;
-                    off[3 * c + 1] = off[3 * c] + 1;
-                    off[3 * c + 2] = base + (G * d + 2 * j) / 2;
-                }
-            int rt = 0;
-            if (rs && c0 == 0) off[kPoll - 1] = dp_off(A, A.fx) + res_at(tid, rt) / 2;
-            ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-                if (c < nb) {
-                    const float mc = ll_val(v[3 * c + 2][0]), Mn = fmaxf(M, mc);
-                    const float fa = ex2_approx(M - Mn), fb = ex2_approx(mc - Mn);
-                    den = fmaf(den, fa, ll_val(v[3 * c + 2][1]) * fb);
-                    num0 = fmaf(num0, fa, ll_val(v[3 * c][0]) * fb);
-                    num1 = fmaf(num1, fa, ll_val(v[3 * c][1]) * fb);
-                    num2 = fmaf(num2, fa, ll_val(v[3 * c + 1][0]) * fb);
-                    num3 = fmaf(num3, fa, ll_val(v[3 * c + 1][1]) * fb);
-                    M = Mn;
-                }
-            if (rs && c0 == 0)
-                *reinterpret_cast<float2*>(res + (tid / (T * 4) * MB + rt) * 8 + 2 * (tid & 3)) =
-                    make_float2(ll_val(v[kPoll - 1][0]), ll_val(v[kPoll - 1][1]));
-            c0 += max(nb, 0);
-        } while (c0 < n && ok);
-        if (q < nq) {
-            const float inv = den > 0.f ? 1.0f / den : 0.f;
-            bf16* dst = C.xa() + (size_t)t * A.xa_stride + r * A.hq_s * d + (kh * G + j) * d + 4 * e4;
-            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(num0 * inv, num1 * inv);
-            *reinterpret_cast<uint32_t*>(dst + 2) = pack_bf16x2(num2 * inv, num3 * inv);
-        }
-    }
-    if (csync_or(!ok)) return false;
-    stamp(A, l, 2, 0);
-    const int Ko = A.hq_s * d, kc = A.kc[1];
-    run_phase<1>(C, A, make_phase(cnt, A.N, A.nl[1]), kc, Ko / 64,
-        [&](int, int r, int jj, int t, int ch, int u8, float (&xf)[8]) {
-            xa_unit(C, A, t, r * Ko + (jj * kc + ch) * 64 + 8 * u8, xf);
-        },
-        [&](int n, int t, int row, float v, float) {
-            ll_st(A.fh + (size_t)t * A.H + 8 * items[n] + row, v + res[(n * MB + t) * 8 + row], ep);
-        });
-    stamp(A, l, 2, 1);
-    return true;
-}
-
-// gate/up: RMSNorm statistics of the residual stream, then per item the gate
-// and up rows (two boxes per load), SwiGLU.
-__device__ __forceinline__ bool phase_gu(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
-    const int cnt = C.misc()[kMiCnt + PH_GU];
-    if (csync_or(*C.abort())) return false;
-    if (!cnt) return true;
-    const int* items = C.misc() + kMiItems + PH_GU * kChainMaxItems;
-    const int MB = A.max_batch, rbg = A.F_s / 8;
-    const ChainLayer& Ly = *C.lay();
-    gammas_fetch(C, A, Ly.g_ffn);
-    if (!load_vec(C, A, A.fh, nullptr, ep)) return false;
-    stamp(A, l, 3, 0);
-    const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
-    const int kc = A.kc[2];
-    run_phase<2>(C, A, make_phase(cnt, 1, A.nl[2]), kc, A.H / 64,
-        [&](int n, int, int jj, int t, int ch, int u8, float (&xf)[8]) {
-            xg_unit(C, A, items[n] / rbg, t, (jj * kc + ch) * 64 + 8 * u8, xf);
-        },
-        [&](int n, int t, int row, float g, float u) {
-            const int it = items[n], r = it / rbg, i = it - r * rbg;
-            const float gt = g * rinv[t], up = u * rinv[t];
-            ll_st(A.fa + (size_t)(r * MB + t) * A.F_s + 8 * i + row, gt / (1.0f + expf(-gt)) * up, ep);
-        });
-    stamp(A, l, 3, 1);
-    return true;
-}
-
-// down: the SwiGLU outputs of every shard as the operand, then per item the
-// rank-ordered sum over shards plus the residual: the layer's output.
-__device__ __forceinline__ bool phase_d(Ctx& C, const ChainArgs& A, int l, unsigned ep) {
-    const int cnt = C.misc()[kMiCnt + PH_D];
-    if (csync_or(*C.abort())) return false;
-    if (!cnt) return true;
-    const int* items = C.misc() + kMiItems + PH_D * kChainMaxItems;
-    const int T = A.T, MB = A.max_batch, F = A.F_s;
-    const int n_act = A.N * T * F / 2, nres = cnt * T * 4;
-    float* res = C.res();
-    // the operand (every shard's SwiGLU outputs) and this CTA's residual rows, polled together
-    const bool ok = poll_space(A, n_act + nres, ep, C.abort(),
-        [&](int i) {
-            if (i < n_act) {
-                const int e = 2 * i, rt = e / F, t = rt % T, r = rt / T;
-                return dp_off(A, A.fa + (size_t)(r * MB + t) * F + (e - rt * F));
-            }
-            const int p = i - n_act, it = p / (T * 4), rem = p - it * T * 4;
-            return dp_off(A, A.fh + (size_t)(rem >> 2) * A.H + 8 * items[it] + 2 * (rem & 3));
-        },
-        [&](int i, float x0, float x1) {
-            if (i < n_act) {
-                const int e = 2 * i, rt = e / F, t = rt % T, r = rt / T;
-                *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + r * F + (e - rt * F)) =
-                    pack_bf16x2(x0, x1);
-            } else {
-                const int p = i - n_act, it = p / (T * 4), rem = p - it * T * 4;
-                *reinterpret_cast<float2*>(res + (it * MB + (rem >> 2)) * 8 + 2 * (rem & 3)) = make_float2(x0, x1);
-            }
-        });
-    if (csync_or(!ok)) return false;
-    stamp(A, l, 4, 0);
-    const bool last = l == A.L - 1;
-    const int kc = A.kc[3];
-    run_phase<1>(C, A, make_phase(cnt, A.N, A.nl[3]), kc, F / 64,
-        [&](int, int r, int jj, int t, int ch, int u8, float (&xf)[8]) {
-            xa_unit(C, A, t, r * F + (jj * kc + ch) * 64 + 8 * u8, xf);
-        },
-        [&](int n, int t, int row, float tot, float) {
-            const float v = tot + res[(n * MB + t) * 8 + row];
-            if (last) A.y[(size_t)t * A.H + 8 * items[n] + row] = v;
-            else ll_st(A.fx + (size_t)t * A.H + 8 * items[n] + row, v, ep + 1);
-        });
-    stamp(A, l, 4, 1);
-    return true;
-}
-
 __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainArgs A) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1148,9 +1052,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
         const unsigned ep = gen * 256u + (unsigned)l + 1u;
-        if (!phase_qkv(C, A, l, ep) || !phase_att(C, A, l, ep) || !phase_o(C, A, l, ep) ||
-            !phase_gu(C, A, l, ep) || !phase_d(C, A, l, ep))
-            break;
+        bool ok = true;
+        #pragma unroll 1
+        for (int st = 0; st < 5 && ok; ++st) ok = st == 1 ? phase_att(C, A, l, ep) : proj_step(C, A, l, ep, step_phase(st));
+        if (!ok) break;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     csync();
