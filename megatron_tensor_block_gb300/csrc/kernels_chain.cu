@@ -118,8 +118,21 @@ struct CRing {
     volatile int* abort;
 };
 
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// (a copy that has landed is taken without the blocking wait)
 __device__ __forceinline__ unsigned char* ring_wait(const CRing& R, uint32_t k, int* status) {
-    mbar_wait(&R.full[k % R.ns], (k / R.ns) & 1, R.abort, status);
+    const uint32_t par = (k / R.ns) & 1;
+    if (!mbar_test(&R.full[k % R.ns], par)) mbar_wait(&R.full[k % R.ns], par, R.abort, status);
     return R.base + (size_t)(k % R.ns) * kChainSlot;
 }
 // Every consumer warp releases every load it waited for.
@@ -402,13 +415,12 @@ __device__ __forceinline__ void chain_producer(const ChainArgs& A, const CRing& 
             }
             const int ph = step_phase(s);
             const bool col = ph == PH_QKV || ph == PH_GU;          // items of one shard; else every shard's rows
-            const int per_r = ph == PH_QKV ? A.qkv_rows / 8 : A.F_s / 8;
             const int nsh = col ? 1 : N, nl = A.nl[ph], kc = A.kc[ph];
             const uint32_t bytes = (ph == PH_GU ? 2048u : 1024u) * kc;
             #pragma unroll 1
             for (int n = 0; n < cnt[ph] && ok; ++n) {
                 const int it = items[ph * kChainMaxItems + n];
-                const int r0 = col ? it / per_r : 0, i = col ? it - r0 * per_r : it;
+                const int r0 = col ? it >> 16 : 0, i = col ? it & 0xffff : it;
                 #pragma unroll 1
                 for (int r = r0; r < r0 + nsh && ok; ++r) {
                     const CUtensorMap* tm = M + ph * N + r;
@@ -532,9 +544,10 @@ __device__ __forceinline__ void rms_stats(Ctx& C, const ChainArgs& A) {
     }
     csync();
     if (threadIdx.x < T) {
+        const float* pt = part + threadIdx.x * kCW;
         float a = 0.f;
-        #pragma unroll 1
-        for (int w = 0; w < kCW; ++w) a += part[threadIdx.x * kCW + w];
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) a += pt[w];
         reinterpret_cast<float*>(C.misc())[kMiRinv + threadIdx.x] = 1.0f / sqrtf(a * (1.0f / (float)H) + A.eps);
     }
     csync();
@@ -612,8 +625,14 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
 // operand, geometry and epilogue are chosen at run time), so that the code a
 // layer runs stays small.
 
+// floor(a / b) for 0 <= a < 2^16 and 1 <= b <= 64, with rb = 1 / b rounded
+// to float: (a + 1/2) / b lies at least 1/(2b) from an integer, and the
+// float product errs by at most a 2^-7 of that, so truncation is exact.
+__device__ __forceinline__ int qdiv(int a, float rb) { return (int)(((float)a + 0.5f) * rb); }
+
 struct Phase {
-    int cnt, sl, nl, nsh, f, ntask;
+    int cnt, sl, nl, nsh, f, lf, ntask;
+    float rsl, rnl, rsb;    // 1 / sl, 1 / nl, 1 / (nl f)
 };
 __device__ __forceinline__ Phase make_phase(int cnt, int nsh, int nl) {
     Phase P;
@@ -622,8 +641,15 @@ __device__ __forceinline__ Phase make_phase(int cnt, int nsh, int nl) {
     P.nl = nl;
     P.sl = nsh * nl;
     P.f = 1;
-    while (cnt * P.sl * P.f * 2 <= kCW) P.f *= 2;
+    P.lf = 0;
+    while (cnt * P.sl * P.f * 2 <= kCW) {
+        P.f *= 2;
+        ++P.lf;
+    }
     P.ntask = cnt * P.sl * P.f;
+    P.rsl = 1.0f / (float)P.sl;
+    P.rnl = 1.0f / (float)nl;
+    P.rsb = 1.0f / (float)(nl * P.f);
     return P;
 }
 
@@ -670,14 +696,13 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, T = A.T, MB = A.max_batch, H = A.H, N = A.N;
     const ChainLayer& Ly = *C.lay();
     const bool norm = ph == PH_QKV || ph == PH_GU;     // RMSNorm input: operand x * gamma_r, items of one shard
-    const int per_r = ph == PH_QKV ? A.qkv_rows / 8 : A.F_s / 8;
     const int sidx = ph == PH_QKV ? 0 : ph == PH_O ? 2 : ph == PH_GU ? 3 : 4;   // step (stamps)
     if ((ph == PH_O || ph == PH_D) && !cnt) return true;
     if (ph == PH_QKV) {                                  // biases into shared memory while the input is polled
         float* sbias = C.res();
         #pragma unroll 1
         for (int e = tid; e < 8 * cnt; e += kCT) {
-            const int it = items[e >> 3], r = it / per_r, i = it - r * per_r;
+            const int it = items[e >> 3], r = it >> 16, i = it & 0xffff;
             if (Ly.bqkv[r]) cp_async4(sbias + e, Ly.bqkv[r] + 8 * i + (e & 7));
             else sbias[e] = 0.f;
         }
@@ -704,13 +729,13 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
     for (int w0 = 0; w0 < P.ntask; w0 += kCW, ++wave) {
         const int q = w0 + warp;
         if (q < P.ntask) {
-            const int j = q / P.f, kp = q - j * P.f;
-            const int n = j / P.sl, js = j - n * P.sl, r = js / nl, jj = js - r * nl;
-            const int nv = min(kc, nch - jj * kc), U = nv * 8, u0 = kp * U / P.f, u1 = (kp + 1) * U / P.f;
+            const int j = q >> P.lf, kp = q - (j << P.lf);
+            const int n = qdiv(j, P.rsl), js = j - n * P.sl, r = qdiv(js, P.rnl), jj = js - r * nl;
+            const int nv = min(kc, nch - jj * kc), U = nv * 8, u0 = (kp * U) >> P.lf, u1 = ((kp + 1) * U) >> P.lf;
             const uint32_t k = C.k + (uint32_t)j;
             const unsigned char* w = ring_wait(R, k, A.status);
             const int kb = jj * kc * 64;                 // the load's first operand column
-            const float* gam = C.gam() + (items[n] / per_r) * H + kb;
+            const float* gam = C.gam() + (items[n] >> 16) * H + kb;
             const bf16* xa0 = C.xa() + r * Ks + kb;
             float* part = C.part() + warp * kPartFloats;
             #pragma unroll 1
@@ -774,26 +799,30 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
         for (int idx = tid; idx < (n1 - n0 + 1) * T * 8; idx += kCT) {
             const int nn = idx / (T * 8), rem = idx - nn * (T * 8), t = rem >> 3, row = rem & 7;
             const int n = n0 + nn, qa = max(n * per, w0), qb = min((n + 1) * per, qe);
-            float c0 = 0.f, c1 = 0.f;                   // shard sum (gate), and total so far (up)
+            // c0: the current shard's sum (gate rows for gate/up), c1: the total of the
+            // shards before it (up rows for gate/up); selects, not branches
+            float c0 = 0.f, c1 = 0.f;
             if (qa > n * per) {
                 c0 = cin[(t * 8 + row) * 2];
                 c1 = cin[(t * 8 + row) * 2 + 1];
             }
-            #pragma unroll 1
-            for (int qq = qa; qq < qb; ++qq) {
-                const float* pp = C.part() + (qq - w0) * kPartFloats + t * 16;
-                const int i = qq - n * per;
+            const float* pp = C.part() + (qa - w0) * kPartFloats + t * 16 + row;
+            const int sb = nl * P.f;                     // tasks per shard
+            int i = qa - n * per, sh = qdiv(i, P.rsb), k = i - sh * sb;
+            #pragma unroll 4
+            for (int qq = qa; qq < qb; ++qq, pp += kPartFloats) {
+                const float v0 = pp[0], v1 = nbox == 2 ? pp[8] : 0.f;
+                const bool start = k == 0;
                 if (nbox == 2) {
-                    c0 = i == 0 ? pp[row] : c0 + pp[row];
-                    c1 = i == 0 ? pp[8 + row] : c1 + pp[8 + row];
-                } else if (i == 0) {
-                    c0 = pp[row];
-                } else if (i % (nl * P.f) == 0) {       // first part of shard i / (nl f): fold the last one
-                    c1 = i == nl * P.f ? c0 : c1 + c0;
-                    c0 = pp[row];
+                    c0 = start ? v0 : c0 + v0;
+                    c1 = start ? v1 : c1 + v1;
                 } else {
-                    c0 += pp[row];
+                    c1 = start && sh > 0 ? (sh == 1 ? c0 : c1 + c0) : c1;   // fold the finished shard, rank order
+                    c0 = start ? v0 : c0 + v0;
                 }
+                const bool wrap = ++k == sb;
+                k = wrap ? 0 : k;
+                sh += wrap ? 1 : 0;
             }
             if (qb < (n + 1) * per) {
                 cout[(t * 8 + row) * 2] = c0;
@@ -803,7 +832,7 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
             // epilogue of item n, token t, row
             const int it = items[n];
             if (norm) {
-                const int r = it / per_r, i = it - r * per_r;
+                const int r = it >> 16, i = it & 0xffff;
                 if (ph == PH_QKV) {
                     ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row,
                           c0 * rinv[t] + C.res()[8 * n + row], ep);
@@ -1010,7 +1039,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         const int* st = A.tab + A.tab_off[p];
         const int a = st[blockIdx.x], n = st[blockIdx.x + 1] - a;
         if (tid == 0) misc[kMiCnt + p] = n;
-        for (int i = tid; i < n; i += blockDim.x) misc[kMiItems + p * kChainMaxItems + i] = st[A.grid + 1 + a + i];
+        // QKV and gate/up items as (shard << 16) | row block
+        const int per_r = p == PH_QKV ? A.qkv_rows / 8 : p == PH_GU ? A.F_s / 8 : 0;
+        for (int i = tid; i < n; i += blockDim.x) {
+            const int v = st[A.grid + 1 + a + i];
+            misc[kMiItems + p * kChainMaxItems + i] = per_r ? (v / per_r) << 16 | (v % per_r) : v;
+        }
     }
     // query rows >= G of the attention tile stay zero
     for (int i = tid; i < kPsBytes / 2; i += blockDim.x) C.qs()[i] = __float2bfloat16_rn(0.f);
