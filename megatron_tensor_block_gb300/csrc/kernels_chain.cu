@@ -148,6 +148,7 @@ __device__ __forceinline__ void ring_release(const CRing& R, uint32_t k) {
 // off[u] from base (off < 0: none), the missing ones reloaded each round
 // until every pair carries epoch ep.
 constexpr int kPoll = 8;
+constexpr int kPollWide = 16;      // the split-KV combine (one round trip for up to five chunks)
 template <int NB>
 __device__ __forceinline__ bool ll_wait2(const unsigned long long* base, const int (&off)[NB],
                                          unsigned long long (&v)[NB][2], unsigned ep, const ChainArgs& A,
@@ -173,24 +174,24 @@ __device__ __forceinline__ bool ll_wait2(const unsigned long long* base, const i
 }
 
 // Polls the double pairs of an index space 0..n-1 (thread: tid, tid + kCT,
-// ...; kPoll per round trip): src(i) is the double-pair offset from the
+// ...; NB per round trip): src(i) is the double-pair offset from the
 // workspace region base, put(i, a, b) consumes the two values.
-template <class Src, class Put>
+template <int NB = kPoll, class Src, class Put>
 __device__ __forceinline__ bool poll_space(const ChainArgs& A, int n, unsigned ep, volatile int* abort, Src src,
                                            Put put) {
     bool ok = true;
 #pragma unroll 1
-    for (int i0 = threadIdx.x; i0 < n; i0 += kPoll * kCT) {
-        int off[kPoll];
-        unsigned long long v[kPoll][2];
+    for (int i0 = threadIdx.x; i0 < n; i0 += NB * kCT) {
+        int off[NB];
+        unsigned long long v[NB][2];
 #pragma unroll
-        for (int u = 0; u < kPoll; ++u) {
+        for (int u = 0; u < NB; ++u) {
             const int i = i0 + u * kCT;
             off[u] = i < n ? src(i) : -1;
         }
-        ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, abort) && ok;
+        ok = ll_wait2<NB>(A.cbase, off, v, ep, A, abort) && ok;
 #pragma unroll
-        for (int u = 0; u < kPoll; ++u)
+        for (int u = 0; u < NB; ++u)
             if (off[u] >= 0) put(i0 + u * kCT, ll_val(v[u][0]), ll_val(v[u][1]));
     }
     return ok;
@@ -568,23 +569,24 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
         const int gi = (r * MB + t) * hk + kh;
         float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
         int c0 = 0;
+        constexpr int kCh = kPollWide / 3;             // chunks per round trip (3 double pairs each)
         do {
-            int off[kPoll];
-            unsigned long long v[kPoll][2];
+            int off[kPollWide];
+            unsigned long long v[kPollWide][2];
 #pragma unroll
-            for (int u = 0; u < kPoll; ++u) off[u] = -1;
-            const int nb = min(2, n - c0);                 // 3 double pairs per chunk
+            for (int u = 0; u < kPollWide; ++u) off[u] = -1;
+            const int nb = min(kCh, n - c0);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < kCh; ++c)
                 if (c < nb) {
                     const int base = dp_off(A, A.fp + ((size_t)gi * A.maxch + c0 + c) * G * (d + 2));
                     off[3 * c] = base + (j * d + 4 * e4) / 2;
                     off[3 * c + 1] = off[3 * c] + 1;
                     off[3 * c + 2] = base + (G * d + 2 * j) / 2;
                 }
-            ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
+            ok = ll_wait2<kPollWide>(A.cbase, off, v, ep, A, C.abort()) && ok;
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < kCh; ++c)
                 if (c < nb) {
                     const float mc = ll_val(v[3 * c + 2][0]), Mn = fmaxf(M, mc);
                     const float fa = ex2_approx(M - Mn), fb = ex2_approx(mc - Mn);
@@ -675,12 +677,8 @@ __device__ __forceinline__ bool step_input(Ctx& C, const ChainArgs& A, int l, in
         const int cols = (down ? A.N * A.F_s : H) / 2;     // double pairs per token
         ok = poll_space(A, T * cols, ep, C.abort(), [&](int i) { return dp_off(A, src) + i; },
             [&](int i, float a, float b) {
-                if (down) {
-                    const int t = i / cols, c = i - t * cols;
-                    *reinterpret_cast<uint32_t*>(C.xa() + (size_t)t * A.xa_stride + 2 * c) = pack_bf16x2(a, b);
-                } else {
-                    *reinterpret_cast<float2*>(C.xin() + 2 * i) = make_float2(a, b);
-                }
+                if (down) *reinterpret_cast<uint32_t*>(C.xa() + 2 * i) = pack_bf16x2(a, b);   // [token][N F_s]
+                else *reinterpret_cast<float2*>(C.xin() + 2 * i) = make_float2(a, b);
             });
     }
     cp_wait();
@@ -737,12 +735,16 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
             const int kb = jj * kc * 64;                 // the load's first operand column
             const float* gam = C.gam() + (items[n] >> 16) * H + kb;
             const bf16* xa0 = C.xa() + r * Ks + kb;
+            const int xs = ph == PH_D ? N * A.F_s : A.xa_stride;   // the down operand's tokens are unpadded
             float* part = C.part() + warp * kPartFloats;
+            // (token, box) pairs: gate/up loads hold a gate box and an up box, each of 8 rows
             #pragma unroll 1
-            for (int t = 0; t < T; ++t) {
-                float acc[16];
+            for (int tb = 0; tb < T * nbox; ++tb) {
+                const int t = tb >> (nbox - 1), b = tb & (nbox - 1);
+                const unsigned char* wb = w + b * (kChainSlot / 2);
+                float acc[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
                 #pragma unroll 1
                 for (int u = u0 + lane; u < u1; u += 32) {
                     const int ch = u >> 3, u8 = u & 7, e = 64 * ch + 8 * u8;
@@ -760,7 +762,7 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
                         xf[6] = x1.z * g1.z;
                         xf[7] = x1.w * g1.w;
                     } else {
-                        const uint4 v = *reinterpret_cast<const uint4*>(xa0 + (size_t)t * A.xa_stride + e);
+                        const uint4 v = *reinterpret_cast<const uint4*>(xa0 + (size_t)t * xs + e);
                         xf[0] = bf_lo(v.x);
                         xf[1] = bf_hi(v.x);
                         xf[2] = bf_lo(v.y);
@@ -773,18 +775,12 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
 #pragma unroll
                     for (int row = 0; row < 8; ++row) {
                         const int line = row * kc + ch;
-                        const unsigned char* wl = w + (line << 7) + ((u8 ^ (line & 7)) << 4);
+                        const unsigned char* wl = wb + (line << 7) + ((u8 ^ (line & 7)) << 4);
                         acc[row] = dot8f(*reinterpret_cast<const uint4*>(wl), xf, acc[row]);
-                        if (nbox == 2) acc[8 + row] = dot8f(*reinterpret_cast<const uint4*>(wl + kChainSlot / 2), xf, acc[8 + row]);
                     }
                 }
-                if (nbox == 2) {
-                    const float v = lane_reduce<16>(acc);
-                    if (!(lane & 1)) part[t * 16 + (lane >> 1)] = v;
-                } else {
-                    const float v = lane_reduce<8>(acc);
-                    if (!(lane & 3)) part[t * 16 + (lane >> 2)] = v;
-                }
+                const float v = lane_reduce<8>(acc);
+                if (!(lane & 3)) part[t * 16 + 8 * b + (lane >> 2)] = v;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_cnt(&R.empty[k % R.ns], (uint32_t)(kCW / P.f));
@@ -882,13 +878,11 @@ __device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, uns
         cp_commit();
         // raw q (G heads), k and v of the group, as written by the QKV phase
         const unsigned long long* row = A.fq + (size_t)(a.r * MB + a.b) * A.qkv_rows;
+        // three runs of double pairs: q of the group's G heads, then k, then v
+        const int dpq = dp_off(A, row + a.kh * G * d), dpk = dp_off(A, row + (A.hq_s + a.kh) * d),
+                  dpv = dp_off(A, row + (A.hq_s + A.hkv_s + a.kh) * d), nq2 = G * half, nk2 = nq2 + half;
         const bool ok = poll_space(A, (G + 2) * half, ep, C.abort(),
-            [&](int p) {
-                const int e2 = 2 * p, hr = e2 / d, e = e2 - hr * d;
-                const int src = hr < G ? (a.kh * G + hr) * d + e
-                                       : (hr == G ? (A.hq_s + a.kh) * d + e : (A.hq_s + A.hkv_s + a.kh) * d + e);
-                return dp_off(A, row + src);
-            },
+            [&](int p) { return p < nq2 ? dpq + p : p < nk2 ? dpk + (p - nq2) : dpv + (p - nk2); },
             [&](int p, float x0, float x1) { *reinterpret_cast<float2*>(st + 2 * p) = make_float2(x0, x1); });
         cp_wait();
         if (csync_or(!ok)) return false;
