@@ -59,6 +59,11 @@ __device__ __forceinline__ unsigned long long ll_pack(float v, unsigned ep) {
 __device__ __forceinline__ void ll_st(unsigned long long* p, float v, unsigned ep) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(ll_pack(v, ep)) : "memory");
 }
+// two adjacent pairs with one 16-byte store (16-byte aligned; each pair stays one unit)
+__device__ __forceinline__ void ll_st2(unsigned long long* p, float v0, float v1, unsigned ep) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(ll_pack(v0, ep)), "l"(ll_pack(v1, ep))
+                 : "memory");
+}
 __device__ __forceinline__ void ll_ld2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
     asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
@@ -984,27 +989,39 @@ __device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, uns
         ring_release(C.ring(), k0);
         ring_release(C.ring(), k0 + 1);
         csync();
-        // merge the warps (fixed order) into the chunk partial: O (unnormalised), then (max, sum) per head
+        // merge the warps (fixed order) into the chunk partial: O (unnormalised), then (max, sum) per head.
+        // First each head's chunk maximum and the warps' factors relative to it, then O two columns a thread.
         const int gi = (a.r * MB + a.b) * A.hkv_s + a.kh;
         unsigned long long* part = A.fp + ((size_t)gi * A.maxch + a.c) * G * (d + 2);
-        #pragma unroll 1
-        for (int idx = tid; idx < G * d; idx += kCT) {
-            const int j = idx / d, e = idx - j * d;
+        float* fw = st;                                  // [warp][8 heads] (the staged q, k, v are consumed)
+        if (tid < G) {
             float M = -INFINITY;
             #pragma unroll 1
-            for (int w = 0; w < nw; ++w) M = fmaxf(M, ml[(w * 16 + j) * 2]);
-            float num = 0.f, den = 0.f;
+            for (int w = 0; w < nw; ++w) M = fmaxf(M, ml[(w * 16 + tid) * 2]);
+            float den = 0.f;
             #pragma unroll 1
             for (int w = 0; w < nw; ++w) {
-                const float f = ex2_approx(ml[(w * 16 + j) * 2] - M);
-                num = fmaf(f, C.att()[(w * G + j) * d + e], num);
-                den = fmaf(f, ml[(w * 16 + j) * 2 + 1], den);
+                const float f = ex2_approx(ml[(w * 16 + tid) * 2] - M);
+                fw[w * 8 + tid] = f;
+                den = fmaf(f, ml[(w * 16 + tid) * 2 + 1], den);
             }
-            ll_st(part + j * d + e, num, ep);
-            if (e == 0) {
-                ll_st(part + G * d + 2 * j, M, ep);
-                ll_st(part + G * d + 2 * j + 1, den, ep);
+            ll_st(part + G * d + 2 * tid, M, ep);
+            ll_st(part + G * d + 2 * tid + 1, den, ep);
+        }
+        csync();
+        const int lh = d == 128 ? 6 : 5;                 // log2(d / 2)
+        #pragma unroll 1
+        for (int idx = tid; idx < G * d / 2; idx += kCT) {
+            const int j = idx >> lh, e = 2 * (idx - (j << lh));
+            float n0 = 0.f, n1 = 0.f;
+            #pragma unroll 1
+            for (int w = 0; w < nw; ++w) {
+                const float f = fw[w * 8 + j];
+                const float2 o = *reinterpret_cast<const float2*>(C.att() + (w * G + j) * d + e);
+                n0 = fmaf(f, o.x, n0);
+                n1 = fmaf(f, o.y, n1);
             }
+            ll_st2(part + j * d + e, n0, n1, ep);
         }
         stamp(A, l, 1, 1);
     }
