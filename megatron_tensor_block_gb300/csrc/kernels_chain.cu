@@ -723,10 +723,105 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
     const int nsh = norm ? 1 : N, nl = A.nl[ph], kc = A.kc[ph];
     const int Ks = ph == PH_O ? A.hq_s * A.d : ph == PH_D ? A.F_s : H;   // operand columns per shard
     const int nch = Ks / 64, nbox = ph == PH_GU ? 2 : 1;
-    const Phase P = make_phase(cnt, nsh, nl);
-    const int per = P.sl * P.f;                          // tasks per item
     const float* rinv = reinterpret_cast<const float*>(C.misc()) + kMiRinv;
     const CRing R = C.ring();
+    const int xs = ph == PH_D ? N * A.F_s : A.xa_stride;   // the down operand's tokens are unpadded
+    // the output of item n, token t, row: v0 the row's total (the gate row's for gate/up), v1 the up row's
+    auto epilogue = [&](int n, int t, int row, float v0, float v1) {
+        const int it = items[n];
+        if (norm) {
+            const int r = it >> 16, i = it & 0xffff;
+            if (ph == PH_QKV) {
+                ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row, v0 * rinv[t] + C.res()[8 * n + row], ep);
+            } else {
+                const float gt = v0 * rinv[t], up = v1 * rinv[t];
+                ll_st(A.fa + (size_t)(t * N + r) * A.F_s + 8 * i + row, gt / (1.0f + expf(-gt)) * up, ep);
+            }
+        } else {
+            const int e = t * H + 8 * it + row;
+            const float v = v0 + C.xin()[e];             // + the residual
+            if (ph == PH_O) ll_st(A.fh + e, v, ep);
+            else if (l == A.L - 1) A.y[e] = v;
+            else ll_st(A.fx + e, v, ep + 1);
+        }
+    };
+    if (nbox == 1 && cnt * nsh * nl <= 2) {
+        // One box per load and at most two loads (QKV, o_proj here): warp w computes row w of every
+        // item over all its loads, in order (per shard the loads in K order, the shards' sums in rank order); each
+        // load is used for every token, then released; lane t ends with token t's output.
+        const int sl = nsh * nl;
+        #pragma unroll 1
+        for (int n = 0; n < cnt; ++n) {
+            const float* gam = C.gam() + (items[n] >> 16) * H;
+            float tot = 0.f;
+            #pragma unroll 1
+            for (int r = 0; r < nsh; ++r) {
+                float acc[kTMax];
+#pragma unroll
+                for (int t = 0; t < kTMax; ++t) acc[t] = 0.f;
+                #pragma unroll 1
+                for (int jj = 0; jj < nl; ++jj) {
+                    const uint32_t k = C.k + (uint32_t)(n * sl + r * nl + jj);
+                    const unsigned char* w = ring_wait(R, k, A.status);
+                    const int nv = min(kc, nch - jj * kc), kb = jj * kc * 64;
+                    #pragma unroll 1
+                    for (int u = lane; u < nv * 8; u += 32) {
+                        const int ch = u >> 3, u8 = u & 7, e = kb + 64 * ch + 8 * u8, line = warp * kc + ch;
+                        const uint4 wv = *reinterpret_cast<const uint4*>(w + (line << 7) + ((u8 ^ (line & 7)) << 4));
+                        const float wf[8] = {bf_lo(wv.x), bf_hi(wv.x), bf_lo(wv.y), bf_hi(wv.y),
+                                             bf_lo(wv.z), bf_hi(wv.z), bf_lo(wv.w), bf_hi(wv.w)};
+#pragma unroll
+                        for (int t = 0; t < kTMax; ++t) {
+                            if (t >= T) break;
+                            float xf[8];
+                            if (norm) {
+                                const float4* xp = reinterpret_cast<const float4*>(C.xin() + t * H + e);
+                                const float4* gp = reinterpret_cast<const float4*>(gam + e);
+                                const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
+                                xf[0] = x0.x * g0.x;
+                                xf[1] = x0.y * g0.y;
+                                xf[2] = x0.z * g0.z;
+                                xf[3] = x0.w * g0.w;
+                                xf[4] = x1.x * g1.x;
+                                xf[5] = x1.y * g1.y;
+                                xf[6] = x1.z * g1.z;
+                                xf[7] = x1.w * g1.w;
+                            } else {
+                                const uint4 v = *reinterpret_cast<const uint4*>(C.xa() + (size_t)t * xs + r * Ks + e);
+                                xf[0] = bf_lo(v.x);
+                                xf[1] = bf_hi(v.x);
+                                xf[2] = bf_lo(v.y);
+                                xf[3] = bf_hi(v.y);
+                                xf[4] = bf_lo(v.z);
+                                xf[5] = bf_hi(v.z);
+                                xf[6] = bf_lo(v.w);
+                                xf[7] = bf_hi(v.w);
+                            }
+                            float a = acc[t];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) a = fmaf(wf[i], xf[i], a);
+                            acc[t] = a;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&R.empty[k % R.ns]);
+                }
+#pragma unroll
+                for (int t = 0; t < kTMax; ++t) {
+                    if (t >= T) break;
+                    const float ps = warp_sum(acc[t]);
+                    if (lane == t) tot = r == 0 ? ps : tot + ps;
+                }
+            }
+            if (lane < T) epilogue(n, lane, warp, tot, 0.f);
+        }
+        C.k += (uint32_t)(cnt * sl);
+        stamp(A, l, sidx, 1);
+        return true;
+    }
+    // Tasks over the loads (gate/up, and steps with more loads): partial sums folded in shared memory.
+    const Phase P = make_phase(cnt, nsh, nl);
+    const int per = P.sl * P.f;                          // tasks per item
     int wave = 0;
     #pragma unroll 1
     for (int w0 = 0; w0 < P.ntask; w0 += kCW, ++wave) {
@@ -740,7 +835,6 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
             const int kb = jj * kc * 64;                 // the load's first operand column
             const float* gam = C.gam() + (items[n] >> 16) * H + kb;
             const bf16* xa0 = C.xa() + r * Ks + kb;
-            const int xs = ph == PH_D ? N * A.F_s : A.xa_stride;   // the down operand's tokens are unpadded
             float* part = C.part() + warp * kPartFloats;
             // (token, box) pairs: gate/up loads hold a gate box and an up box, each of 8 rows
             #pragma unroll 1
@@ -830,24 +924,7 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
                 cout[(t * 8 + row) * 2 + 1] = c1;
                 continue;
             }
-            // epilogue of item n, token t, row
-            const int it = items[n];
-            if (norm) {
-                const int r = it >> 16, i = it & 0xffff;
-                if (ph == PH_QKV) {
-                    ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row,
-                          c0 * rinv[t] + C.res()[8 * n + row], ep);
-                } else {
-                    const float gt = c0 * rinv[t], up = c1 * rinv[t];
-                    ll_st(A.fa + (size_t)(t * N + r) * A.F_s + 8 * i + row, gt / (1.0f + expf(-gt)) * up, ep);
-                }
-            } else {
-                const int e = t * H + 8 * it + row;
-                const float v = (nsh > 1 ? c1 + c0 : c0) + C.xin()[e];   // + the residual
-                if (ph == PH_O) ll_st(A.fh + e, v, ep);
-                else if (l == A.L - 1) A.y[e] = v;
-                else ll_st(A.fx + e, v, ep + 1);
-            }
+            epilogue(n, t, row, nsh > 1 ? c1 + c0 : c0, c1);
         }
         if (w0 + kCW < P.ntask) csync();                // the next wave overwrites the partials
     }
