@@ -533,28 +533,31 @@ __device__ __forceinline__ void gammas_fetch(Ctx& C, const ChainArgs& A, const f
 }
 
 // 1/rms of every token of xin (T x H, float32) into the misc area.
-__device__ __forceinline__ void rms_stats(Ctx& C, const ChainArgs& A) {
+// (with a single token the warps' partial sums were stored while the vector was polled: have_part)
+__device__ __forceinline__ void rms_stats(Ctx& C, const ChainArgs& A, bool have_part) {
     const int T = A.T, H = A.H, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* xin = C.xin();
     float* part = C.att();                                // [token][warp] partial sums
-    #pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-        float sq = 0.f;
+    if (!have_part) {
         #pragma unroll 1
-        for (int k2 = threadIdx.x; k2 < H / 2; k2 += kCT) {
-            const float2 xv = *reinterpret_cast<const float2*>(xin + t * H + 2 * k2);
-            sq = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, sq));
+        for (int t = 0; t < T; ++t) {
+            float sq = 0.f;
+            #pragma unroll 1
+            for (int k2 = threadIdx.x; k2 < H / 2; k2 += kCT) {
+                const float2 xv = *reinterpret_cast<const float2*>(xin + t * H + 2 * k2);
+                sq = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, sq));
+            }
+            sq = warp_sum(sq);
+            if (lane == 0) part[t * kCW + warp] = sq;
         }
-        sq = warp_sum(sq);
-        if (lane == 0) part[t * kCW + warp] = sq;
+        csync();
     }
-    csync();
     if (threadIdx.x < T) {
         const float* pt = part + threadIdx.x * kCW;
         float a = 0.f;
 #pragma unroll
         for (int w = 0; w < kCW; ++w) a += pt[w];
-        reinterpret_cast<float*>(C.misc())[kMiRinv + threadIdx.x] = 1.0f / sqrtf(a * (1.0f / (float)H) + A.eps);
+        reinterpret_cast<float*>(C.misc())[kMiRinv + threadIdx.x] = rsqrtf(a * (1.0f / (float)H) + A.eps);
     }
     csync();
 }
@@ -672,23 +675,36 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t cnt) {
 __device__ __forceinline__ bool step_input(Ctx& C, const ChainArgs& A, int l, int ph, unsigned ep) {
     const int T = A.T, H = A.H;
     bool ok = true;
+    float sq = 0.f;                                      // this thread's sum of squares (one token)
     if (ph == PH_QKV && l == 0) {
         #pragma unroll 1
-        for (int i = threadIdx.x; i < T * H / 2; i += kCT)
-            *reinterpret_cast<float2*>(C.xin() + 2 * i) = *reinterpret_cast<const float2*>(A.x + 2 * (size_t)i);
+        for (int i = threadIdx.x; i < T * H / 2; i += kCT) {
+            const float2 v = *reinterpret_cast<const float2*>(A.x + 2 * (size_t)i);
+            *reinterpret_cast<float2*>(C.xin() + 2 * i) = v;
+            sq = fmaf(v.x, v.x, fmaf(v.y, v.y, sq));
+        }
     } else {
         const bool down = ph == PH_D;
         const unsigned long long* src = ph == PH_QKV ? A.fx : down ? A.fa : A.fh;
         const int cols = (down ? A.N * A.F_s : H) / 2;     // double pairs per token
         ok = poll_space(A, T * cols, ep, C.abort(), [&](int i) { return dp_off(A, src) + i; },
             [&](int i, float a, float b) {
-                if (down) *reinterpret_cast<uint32_t*>(C.xa() + 2 * i) = pack_bf16x2(a, b);   // [token][N F_s]
-                else *reinterpret_cast<float2*>(C.xin() + 2 * i) = make_float2(a, b);
+                if (down) {
+                    *reinterpret_cast<uint32_t*>(C.xa() + 2 * i) = pack_bf16x2(a, b);   // [token][N F_s]
+                } else {
+                    *reinterpret_cast<float2*>(C.xin() + 2 * i) = make_float2(a, b);
+                    sq = fmaf(a, a, fmaf(b, b, sq));
+                }
             });
     }
     cp_wait();
+    const bool one = T == 1 && ph != PH_D;
+    if (one) {
+        sq = warp_sum(sq);
+        if ((threadIdx.x & 31) == 0) C.att()[threadIdx.x >> 5] = sq;
+    }
     if (csync_or(!ok)) return false;
-    if (ph != PH_D) rms_stats(C, A);
+    if (ph != PH_D) rms_stats(C, A, one);
     return true;
 }
 
