@@ -12,6 +12,8 @@
 // Every wait is bounded; tensor memory is freed on every path.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include <cstring>
 
 #include "common.cuh"
@@ -230,6 +232,7 @@ struct TcColArgs {
     int T, K, S;                          // tokens, reduction length, tokens per sequence
     int a_row_stride;                     // first A row of shard r = r * a_row_stride (0: shared copy)
     int n_mt, n_nt, N;                    // tiles: token tiles, column tiles per shard, shards
+    int gm;                               // token tiles per group (tile order, below)
     int hq_s, hkv_s, d, max_kv, ffn_s;
     const float* bias[TP_MAX_SHARDS];
     const int* pos;                       // [B] first new position of each sequence
@@ -241,11 +244,17 @@ struct TcColArgs {
     int* status;
 };
 
-// tile -> (token tile, column tile, shard); token tiles vary fastest so that
-// the CTAs resident at one time share the weight tiles they stream
+// tile -> (token tile, column tile, shard). The token tiles are taken in
+// groups of gm whose activations fit in L2 with room to spare; within a group
+// token tiles vary fastest, so that the CTAs resident at one time share the
+// weight tiles they stream, and the group's activations stay in L2 while every
+// column tile of every shard passes over them. The weights are read once per
+// group, the activations about once.
 __device__ __forceinline__ void col_tile(const TcColArgs& g, int tile, int& mt, int& nt, int& r) {
-    mt = tile % g.n_mt;
-    const int rest = tile / g.n_mt;
+    const int per_g = g.gm * g.n_nt * g.N, grp = tile / per_g, local = tile - grp * per_g;
+    const int m0 = grp * g.gm, gm = min(g.gm, g.n_mt - m0);
+    mt = m0 + local % gm;
+    const int rest = local / gm;
     nt = rest % g.n_nt;
     r = rest / g.n_nt;
 }
@@ -466,21 +475,26 @@ struct TcRowArgs {
     CUtensorMap tb[TP_MAX_SHARDS];        // shard weights [H, Kr], boxes 64 x 256
     int T, Kr, N, H;
     int n_mt, n_nt;
+    int gn;                               // output-column tiles per group (tile order, below)
     const float* resid;                   // [T][H]
     float* out;                           // [T][H]
     int* status;
 };
 
-// Tile order of the row-parallel projections (o_proj, down_proj): output-
-// column tiles vary fastest, so the CTAs resident at one time cover a few
-// token tiles across every output column. A wave then reads each of its token
-// tiles' activations (every shard's) once, and the weights, read again by
-// every wave, are loaded evict-last while the activations stream evict-first.
-// (Token tiles fastest re-read every shard's activations once per wave: 2.07
-// against 1.33 GB of DRAM reads per down_proj launch.)
+// Tile order of the row-parallel projections (o_proj, down_proj): the output-
+// column tiles are taken in groups of gn whose weights (every shard's) fit in
+// L2 with room to spare. Within a group output-column tiles vary fastest, so
+// the CTAs resident at one time cover a few token tiles across the group's
+// columns: a wave reads each of its token tiles' activations (every shard's)
+// once, and the group's weights, read by every wave, are loaded evict-last
+// while the activations stream evict-first. The activations are read once per
+// group. (Token tiles fastest re-read every shard's activations once per wave:
+// 2.07 GB of DRAM reads per down_proj launch; one group of all columns, 1.39 GB.)
 __device__ __forceinline__ void row_tile(const TcRowArgs& g, int tile, int& m0, int& n0) {
-    m0 = (tile / g.n_nt) * kTcBM;
-    n0 = (tile % g.n_nt) * kRowBN;
+    const int per_g = g.gn * g.n_mt, grp = tile / per_g, local = tile - grp * per_g;
+    const int c0 = grp * g.gn, gn = min(g.gn, g.n_nt - c0);
+    m0 = (local / gn) * kTcBM;
+    n0 = (c0 + local % gn) * kRowBN;
 }
 
 __global__ void __launch_bounds__(kRowThreads, 1) tc_row_kernel(const __grid_constant__ TcRowArgs g) {
@@ -1066,6 +1080,9 @@ cudaError_t launch_tc_col(int mode, const PrefillColParams& p, cudaStream_t s) {
     g.n_mt = (p.T + kTcBM - 1) / kTcBM;
     g.n_nt = mode == TC_QKV ? (p.rows + kTcBN - 1) / kTcBN : (p.ffn_s + 127) / 128;
     g.N = p.N;
+    // token tiles per group: about 32 MB of activations (a quarter of L2) per group, every copy counted
+    const long tile_bytes = (long)kTcBM * p.K * 2 * copies;
+    g.gm = (int)std::max(1L, std::min((long)g.n_mt, (32L << 20) / tile_bytes));
     const long tiles = (long)g.n_mt * g.n_nt * g.N;
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
     const int grid = tiles < kSMs ? (int)tiles : kSMs;
@@ -1096,6 +1113,9 @@ cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s) {
     }
     g.n_mt = (p.T + kTcBM - 1) / kTcBM;
     g.n_nt = (p.H + kRowBN - 1) / kRowBN;
+    // output-column tiles per group: about 64 MB of weights (half of L2) per group
+    const long col_bytes = (long)kRowBN * p.Kr * p.N * 2;
+    g.gn = (int)std::max(1L, std::min((long)g.n_nt, (64L << 20) / col_bytes));
     const long tiles = (long)g.n_mt * g.n_nt;
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
     const int grid = tiles < kSMs ? (int)tiles : kSMs;
