@@ -465,6 +465,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_col_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 
 constexpr int kRowBN = 256;
+// L2 budgets of the tile orders (MB): a token-tile group's activations in the
+// column-parallel kernels, an output-column group's weights in the row-parallel ones
+#ifndef TP_COL_GROUP_MB
+#define TP_COL_GROUP_MB 32
+#endif
+#ifndef TP_ROW_GROUP_MB
+#define TP_ROW_GROUP_MB 64
+#endif
+constexpr int kColGroupMB = TP_COL_GROUP_MB, kRowGroupMB = TP_ROW_GROUP_MB;
 constexpr int kRowStages = 4;
 constexpr int kRowStageBytes = kTcABytes + kRowBN * kTcBK * 2;   // 48 KB
 constexpr int kRowSmem = 1024 + kRowStages * kRowStageBytes;
@@ -1080,9 +1089,9 @@ cudaError_t launch_tc_col(int mode, const PrefillColParams& p, cudaStream_t s) {
     g.n_mt = (p.T + kTcBM - 1) / kTcBM;
     g.n_nt = mode == TC_QKV ? (p.rows + kTcBN - 1) / kTcBN : (p.ffn_s + 127) / 128;
     g.N = p.N;
-    // token tiles per group: about 32 MB of activations (a quarter of L2) per group, every copy counted
+    // token tiles per group: about kColGroupMB of activations per group, every copy counted
     const long tile_bytes = (long)kTcBM * p.K * 2 * copies;
-    g.gm = (int)std::max(1L, std::min((long)g.n_mt, (32L << 20) / tile_bytes));
+    g.gm = (int)std::max(1L, std::min((long)g.n_mt, ((long)kColGroupMB << 20) / tile_bytes));
     const long tiles = (long)g.n_mt * g.n_nt * g.N;
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
     const int grid = tiles < kSMs ? (int)tiles : kSMs;
@@ -1113,9 +1122,9 @@ cudaError_t launch_tc_row(const PrefillRowParams& p, cudaStream_t s) {
     }
     g.n_mt = (p.T + kTcBM - 1) / kTcBM;
     g.n_nt = (p.H + kRowBN - 1) / kRowBN;
-    // output-column tiles per group: about 64 MB of weights (half of L2) per group
+    // output-column tiles per group: about kRowGroupMB of weights per group
     const long col_bytes = (long)kRowBN * p.Kr * p.N * 2;
-    g.gn = (int)std::max(1L, std::min((long)g.n_nt, (64L << 20) / col_bytes));
+    g.gn = (int)std::max(1L, std::min((long)g.n_nt, ((long)kRowGroupMB << 20) / col_bytes));
     const long tiles = (long)g.n_mt * g.n_nt;
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
     const int grid = tiles < kSMs ? (int)tiles : kSMs;
