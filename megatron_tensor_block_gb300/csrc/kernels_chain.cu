@@ -852,14 +852,12 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
             const float* gam = C.gam() + (items[n] >> 16) * H + kb;
             const bf16* xa0 = C.xa() + r * Ks + kb;
             float* part = C.part() + warp * kPartFloats;
-            // (token, box) pairs: gate/up loads hold a gate box and an up box, each of 8 rows
+            // a gate/up load holds a gate box and an up box of 8 rows each, both multiplied per operand unit
             #pragma unroll 1
-            for (int tb = 0; tb < T * nbox; ++tb) {
-                const int t = tb >> (nbox - 1), b = tb & (nbox - 1);
-                const unsigned char* wb = w + b * (kChainSlot / 2);
-                float acc[8];
+            for (int t = 0; t < T; ++t) {
+                float acc[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+                for (int i = 0; i < 16; ++i) acc[i] = 0.f;
                 #pragma unroll 1
                 for (int u = u0 + lane; u < u1; u += 32) {
                     const int ch = u >> 3, u8 = u & 7, e = 64 * ch + 8 * u8;
@@ -890,12 +888,18 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
 #pragma unroll
                     for (int row = 0; row < 8; ++row) {
                         const int line = row * kc + ch;
-                        const unsigned char* wl = wb + (line << 7) + ((u8 ^ (line & 7)) << 4);
+                        const unsigned char* wl = w + (line << 7) + ((u8 ^ (line & 7)) << 4);
                         acc[row] = dot8f(*reinterpret_cast<const uint4*>(wl), xf, acc[row]);
+                        if (nbox == 2) acc[8 + row] = dot8f(*reinterpret_cast<const uint4*>(wl + kChainSlot / 2), xf, acc[8 + row]);
                     }
                 }
-                const float v = lane_reduce<8>(acc);
-                if (!(lane & 3)) part[t * 16 + 8 * b + (lane >> 2)] = v;
+                if (nbox == 2) {
+                    const float v = lane_reduce<16>(acc);
+                    if (!(lane & 1)) part[t * 16 + (lane >> 1)] = v;
+                } else {
+                    const float v = lane_reduce<8>(acc);
+                    if (!(lane & 3)) part[t * 16 + (lane >> 2)] = v;
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_cnt(&R.empty[k % R.ns], (uint32_t)(kCW / P.f));
