@@ -761,10 +761,10 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
             else ll_st(A.fx + e, v, ep + 1);
         }
     };
-    if (nbox == 1 && cnt * nsh * nl <= 2) {
-        // One box per load and at most two loads (QKV, o_proj here): warp w computes row w of every
-        // item over all its loads, in order (per shard the loads in K order, the shards' sums in rank order); each
-        // load is used for every token, then released; lane t ends with token t's output.
+    if (nbox == 1 && T == 1 && cnt * nsh * nl <= 2) {
+        // One token, one box per load and at most two loads (QKV, o_proj here): warp w computes
+        // row w of every item over all its loads, in order (per shard the loads in K order, the
+        // shards' sums in rank order), then releases them; lane 0 writes the output.
         const int sl = nsh * nl;
         #pragma unroll 1
         for (int n = 0; n < cnt; ++n) {
@@ -772,9 +772,7 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
             float tot = 0.f;
             #pragma unroll 1
             for (int r = 0; r < nsh; ++r) {
-                float acc[kTMax];
-#pragma unroll
-                for (int t = 0; t < kTMax; ++t) acc[t] = 0.f;
+                float acc = 0.f;
                 #pragma unroll 1
                 for (int jj = 0; jj < nl; ++jj) {
                     const uint32_t k = C.k + (uint32_t)(n * sl + r * nl + jj);
@@ -783,53 +781,39 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
                     #pragma unroll 1
                     for (int u = lane; u < nv * 8; u += 32) {
                         const int ch = u >> 3, u8 = u & 7, e = kb + 64 * ch + 8 * u8, line = warp * kc + ch;
-                        const uint4 wv = *reinterpret_cast<const uint4*>(w + (line << 7) + ((u8 ^ (line & 7)) << 4));
-                        const float wf[8] = {bf_lo(wv.x), bf_hi(wv.x), bf_lo(wv.y), bf_hi(wv.y),
-                                             bf_lo(wv.z), bf_hi(wv.z), bf_lo(wv.w), bf_hi(wv.w)};
-#pragma unroll
-                        for (int t = 0; t < kTMax; ++t) {
-                            if (t >= T) break;
-                            float xf[8];
-                            if (norm) {
-                                const float4* xp = reinterpret_cast<const float4*>(C.xin() + t * H + e);
-                                const float4* gp = reinterpret_cast<const float4*>(gam + e);
-                                const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
-                                xf[0] = x0.x * g0.x;
-                                xf[1] = x0.y * g0.y;
-                                xf[2] = x0.z * g0.z;
-                                xf[3] = x0.w * g0.w;
-                                xf[4] = x1.x * g1.x;
-                                xf[5] = x1.y * g1.y;
-                                xf[6] = x1.z * g1.z;
-                                xf[7] = x1.w * g1.w;
-                            } else {
-                                const uint4 v = *reinterpret_cast<const uint4*>(C.xa() + (size_t)t * xs + r * Ks + e);
-                                xf[0] = bf_lo(v.x);
-                                xf[1] = bf_hi(v.x);
-                                xf[2] = bf_lo(v.y);
-                                xf[3] = bf_hi(v.y);
-                                xf[4] = bf_lo(v.z);
-                                xf[5] = bf_hi(v.z);
-                                xf[6] = bf_lo(v.w);
-                                xf[7] = bf_hi(v.w);
-                            }
-                            float a = acc[t];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) a = fmaf(wf[i], xf[i], a);
-                            acc[t] = a;
+                        float xf[8];
+                        if (norm) {
+                            const float4* xp = reinterpret_cast<const float4*>(C.xin() + e);
+                            const float4* gp = reinterpret_cast<const float4*>(gam + e);
+                            const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
+                            xf[0] = x0.x * g0.x;
+                            xf[1] = x0.y * g0.y;
+                            xf[2] = x0.z * g0.z;
+                            xf[3] = x0.w * g0.w;
+                            xf[4] = x1.x * g1.x;
+                            xf[5] = x1.y * g1.y;
+                            xf[6] = x1.z * g1.z;
+                            xf[7] = x1.w * g1.w;
+                        } else {
+                            const uint4 v = *reinterpret_cast<const uint4*>(C.xa() + r * Ks + e);
+                            xf[0] = bf_lo(v.x);
+                            xf[1] = bf_hi(v.x);
+                            xf[2] = bf_lo(v.y);
+                            xf[3] = bf_hi(v.y);
+                            xf[4] = bf_lo(v.z);
+                            xf[5] = bf_hi(v.z);
+                            xf[6] = bf_lo(v.w);
+                            xf[7] = bf_hi(v.w);
                         }
+                        acc = dot8f(*reinterpret_cast<const uint4*>(w + (line << 7) + ((u8 ^ (line & 7)) << 4)), xf, acc);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&R.empty[k % R.ns]);
                 }
-#pragma unroll
-                for (int t = 0; t < kTMax; ++t) {
-                    if (t >= T) break;
-                    const float ps = warp_sum(acc[t]);
-                    if (lane == t) tot = r == 0 ? ps : tot + ps;
-                }
+                const float ps = warp_sum(acc);
+                tot = r == 0 ? ps : tot + ps;
             }
-            if (lane < T) epilogue(n, lane, warp, tot, 0.f);
+            if (lane == 0) epilogue(n, 0, warp, tot, 0.f);
         }
         C.k += (uint32_t)(cnt * sl);
         stamp(A, l, sidx, 1);
