@@ -153,7 +153,6 @@ __device__ __forceinline__ void ring_release(const CRing& R, uint32_t k) {
 // off[u] from base (off < 0: none), the missing ones reloaded each round
 // until every pair carries epoch ep.
 constexpr int kPoll = 8;
-constexpr int kPollWide = 16;      // the split-KV combine (one round trip for up to five chunks)
 template <int NB>
 __device__ __forceinline__ bool ll_wait2(const unsigned long long* base, const int (&off)[NB],
                                          unsigned long long (&v)[NB][2], unsigned ep, const ChainArgs& A,
@@ -577,12 +576,13 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
         const int gi = (r * MB + t) * hk + kh;
         float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
         int c0 = 0;
-        constexpr int kCh = kPollWide / 3;             // chunks per round trip (3 double pairs each)
+        constexpr int kCh = kPoll / 3;                 // chunks per round trip (3 double pairs each; a wider
+                                                       // poll made the launch slower through its code size)
         do {
-            int off[kPollWide];
-            unsigned long long v[kPollWide][2];
+            int off[kPoll];
+            unsigned long long v[kPoll][2];
 #pragma unroll
-            for (int u = 0; u < kPollWide; ++u) off[u] = -1;
+            for (int u = 0; u < kPoll; ++u) off[u] = -1;
             const int nb = min(kCh, n - c0);
 #pragma unroll
             for (int c = 0; c < kCh; ++c)
@@ -592,7 +592,7 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
                     off[3 * c + 1] = off[3 * c] + 1;
                     off[3 * c + 2] = base + (G * d + 2 * j) / 2;
                 }
-            ok = ll_wait2<kPollWide>(A.cbase, off, v, ep, A, C.abort()) && ok;
+            ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
 #pragma unroll
             for (int c = 0; c < kCh; ++c)
                 if (c < nb) {
