@@ -576,13 +576,13 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
         const int gi = (r * MB + t) * hk + kh;
         float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
         int c0 = 0;
-        constexpr int kCh = kPoll / 3;                 // chunks per round trip (3 double pairs each; a wider
+        constexpr int kCh = 3;                         // chunks per round trip (3 double pairs each; a wider
                                                        // poll made the launch slower through its code size)
         do {
-            int off[kPoll];
-            unsigned long long v[kPoll][2];
+            int off[3 * kCh];
+            unsigned long long v[3 * kCh][2];
 #pragma unroll
-            for (int u = 0; u < kPoll; ++u) off[u] = -1;
+            for (int u = 0; u < 3 * kCh; ++u) off[u] = -1;
             const int nb = min(kCh, n - c0);
 #pragma unroll
             for (int c = 0; c < kCh; ++c)
@@ -592,7 +592,7 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
                     off[3 * c + 1] = off[3 * c] + 1;
                     off[3 * c + 2] = base + (G * d + 2 * j) / 2;
                 }
-            ok = ll_wait2<kPoll>(A.cbase, off, v, ep, A, C.abort()) && ok;
+            ok = ll_wait2<3 * kCh>(A.cbase, off, v, ep, A, C.abort()) && ok;
 #pragma unroll
             for (int c = 0; c < kCh; ++c)
                 if (c < nb) {
