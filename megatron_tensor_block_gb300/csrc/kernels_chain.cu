@@ -686,11 +686,11 @@ __device__ __forceinline__ bool step_input(Ctx& C, const ChainArgs& A, int l, in
     } else {
         const bool down = ph == PH_D;
         const unsigned long long* src = ph == PH_QKV ? A.fx : down ? A.fa : A.fh;
-        const int cols = (down ? A.N * A.F_s : H) / 2;     // double pairs per token
+        const int cols = down ? A.N * A.F_s / 4 : H / 2;    // double pairs per token (down: 4 bf16 values each)
         ok = poll_space(A, T * cols, ep, C.abort(), [&](int i) { return dp_off(A, src) + i; },
             [&](int i, float a, float b) {
-                if (down) {
-                    *reinterpret_cast<uint32_t*>(C.xa() + 2 * i) = pack_bf16x2(a, b);   // [token][N F_s]
+                if (down) {                              // [token][N F_s] bf16, four values a double pair
+                    *reinterpret_cast<uint2*>(C.xa() + 4 * i) = make_uint2(__float_as_uint(a), __float_as_uint(b));
                 } else {
                     *reinterpret_cast<float2*>(C.xin() + 2 * i) = make_float2(a, b);
                     sq = fmaf(a, a, fmaf(b, b, sq));
@@ -751,7 +751,14 @@ __device__ __forceinline__ bool proj_step(Ctx& C, const ChainArgs& A, int l, uns
                 ll_st(A.fq + (size_t)(r * MB + t) * A.qkv_rows + 8 * i + row, v0 * rinv[t] + C.res()[8 * n + row], ep);
             } else {
                 const float gt = v0 * rinv[t], up = v1 * rinv[t];
-                ll_st(A.fa + (size_t)(t * N + r) * A.F_s + 8 * i + row, gt / (1.0f + expf(-gt)) * up, ep);
+                // rows 2j and 2j + 1 as one pair of bf16 values (the down operand is bf16 anyway): the row
+                // pair sits in adjacent lanes of the fold, and the even one stores both
+                const float v = gt / (1.0f + expf(-gt)) * up, nv = __shfl_down_sync(__activemask(), v, 1);
+                if (!(row & 1)) {
+                    const unsigned long long pv = ((unsigned long long)ep << 32) | pack_bf16x2(v, nv);
+                    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(A.fa + ((size_t)(t * N + r) * A.F_s + 8 * i + row) / 2),
+                                 "l"(pv) : "memory");
+                }
             }
         } else {
             const int e = t * H + 8 * it + row;

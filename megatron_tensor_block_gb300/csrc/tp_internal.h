@@ -279,7 +279,7 @@ struct ChainArgs {
     unsigned long long* fp;              // [N * max_batch * hkv_s][maxch][G (d + 2)] attention partials:
                                          // output [G][d] (unnormalised), then (max, sum) per head
     unsigned long long* fh;              // [max_batch][H] residual stream after attention
-    unsigned long long* fa;              // [max_batch][N][F_s] SwiGLU outputs
+    unsigned long long* fa;              // [max_batch][N][F_s / 2] SwiGLU outputs, two bf16 values a pair
     int maxch;
     unsigned* gen;                       // launch counter (epochs) and CTAs finished
     unsigned* done;
