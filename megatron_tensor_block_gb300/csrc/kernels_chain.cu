@@ -576,33 +576,33 @@ __device__ __forceinline__ bool combine_att(Ctx& C, const ChainArgs& A, unsigned
         const int gi = (r * MB + t) * hk + kh;
         float M = -INFINITY, den = 0.f, num0 = 0.f, num1 = 0.f, num2 = 0.f, num3 = 0.f;
         int c0 = 0;
-        constexpr int kCh = 3;                         // chunks per round trip (3 double pairs each; a wider
-                                                       // poll made the launch slower through its code size)
+        // per chunk two double pairs: O's four values as bf16, then (max, sum)
+        constexpr int kCh = 5;                         // chunks per round trip
         do {
-            int off[3 * kCh];
-            unsigned long long v[3 * kCh][2];
+            int off[2 * kCh];
+            unsigned long long v[2 * kCh][2];
 #pragma unroll
-            for (int u = 0; u < 3 * kCh; ++u) off[u] = -1;
+            for (int u = 0; u < 2 * kCh; ++u) off[u] = -1;
             const int nb = min(kCh, n - c0);
 #pragma unroll
             for (int c = 0; c < kCh; ++c)
                 if (c < nb) {
                     const int base = dp_off(A, A.fp + ((size_t)gi * A.maxch + c0 + c) * G * (d + 2));
-                    off[3 * c] = base + (j * d + 4 * e4) / 2;
-                    off[3 * c + 1] = off[3 * c] + 1;
-                    off[3 * c + 2] = base + (G * d + 2 * j) / 2;
+                    off[2 * c] = base + (j * d + 4 * e4) / 4;
+                    off[2 * c + 1] = base + (G * d / 2 + 2 * j) / 2;
                 }
-            ok = ll_wait2<3 * kCh>(A.cbase, off, v, ep, A, C.abort()) && ok;
+            ok = ll_wait2<2 * kCh>(A.cbase, off, v, ep, A, C.abort()) && ok;
 #pragma unroll
             for (int c = 0; c < kCh; ++c)
                 if (c < nb) {
-                    const float mc = ll_val(v[3 * c + 2][0]), Mn = fmaxf(M, mc);
+                    const float mc = ll_val(v[2 * c + 1][0]), Mn = fmaxf(M, mc);
                     const float fa = ex2_approx(M - Mn), fb = ex2_approx(mc - Mn);
-                    den = fmaf(den, fa, ll_val(v[3 * c + 2][1]) * fb);
-                    num0 = fmaf(num0, fa, ll_val(v[3 * c][0]) * fb);
-                    num1 = fmaf(num1, fa, ll_val(v[3 * c][1]) * fb);
-                    num2 = fmaf(num2, fa, ll_val(v[3 * c + 1][0]) * fb);
-                    num3 = fmaf(num3, fa, ll_val(v[3 * c + 1][1]) * fb);
+                    const uint32_t o01 = (uint32_t)v[2 * c][0], o23 = (uint32_t)v[2 * c][1];
+                    den = fmaf(den, fa, ll_val(v[2 * c + 1][1]) * fb);
+                    num0 = fmaf(num0, fa, bf_lo(o01) * fb);
+                    num1 = fmaf(num1, fa, bf_hi(o01) * fb);
+                    num2 = fmaf(num2, fa, bf_lo(o23) * fb);
+                    num3 = fmaf(num3, fa, bf_hi(o23) * fb);
                     M = Mn;
                 }
             c0 += max(nb, 0);
@@ -1093,23 +1093,29 @@ __device__ __forceinline__ bool phase_att(Ctx& C, const ChainArgs& A, int l, uns
                 fw[w * 8 + tid] = f;
                 den = fmaf(f, ml[(w * 16 + tid) * 2 + 1], den);
             }
-            ll_st(part + G * d + 2 * tid, M, ep);
-            ll_st(part + G * d + 2 * tid + 1, den, ep);
+            ll_st(part + G * d / 2 + 2 * tid, M, ep);
+            ll_st(part + G * d / 2 + 2 * tid + 1, den, ep);
         }
         csync();
-        const int lh = d == 128 ? 6 : 5;                 // log2(d / 2)
+        // O as bf16 (it feeds the bf16 o_proj operand): four values a thread, two to a pair
+        const int lq = d == 128 ? 5 : 4;                 // log2(d / 4)
         #pragma unroll 1
-        for (int idx = tid; idx < G * d / 2; idx += kCT) {
-            const int j = idx >> lh, e = 2 * (idx - (j << lh));
-            float n0 = 0.f, n1 = 0.f;
+        for (int idx = tid; idx < G * d / 4; idx += kCT) {
+            const int j = idx >> lq, e = 4 * (idx - (j << lq));
+            float4 nsum = make_float4(0.f, 0.f, 0.f, 0.f);
             #pragma unroll 1
             for (int w = 0; w < nw; ++w) {
                 const float f = fw[w * 8 + j];
-                const float2 o = *reinterpret_cast<const float2*>(C.att() + (w * G + j) * d + e);
-                n0 = fmaf(f, o.x, n0);
-                n1 = fmaf(f, o.y, n1);
+                const float4 o = *reinterpret_cast<const float4*>(C.att() + (w * G + j) * d + e);
+                nsum.x = fmaf(f, o.x, nsum.x);
+                nsum.y = fmaf(f, o.y, nsum.y);
+                nsum.z = fmaf(f, o.z, nsum.z);
+                nsum.w = fmaf(f, o.w, nsum.w);
             }
-            ll_st2(part + j * d + e, n0, n1, ep);
+            const unsigned long long p0 = ((unsigned long long)ep << 32) | pack_bf16x2(nsum.x, nsum.y);
+            const unsigned long long p1 = ((unsigned long long)ep << 32) | pack_bf16x2(nsum.z, nsum.w);
+            asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(part + (j * d + e) / 2), "l"(p0), "l"(p1)
+                         : "memory");
         }
         stamp(A, l, 1, 1);
     }

@@ -277,7 +277,8 @@ struct ChainArgs {
     unsigned long long* fx;              // [max_batch][H] layer inputs (layers 1..)
     unsigned long long* fq;              // [N][max_batch][qkv_rows] projections before rotation
     unsigned long long* fp;              // [N * max_batch * hkv_s][maxch][G (d + 2)] attention partials:
-                                         // output [G][d] (unnormalised), then (max, sum) per head
+                                         // output [G][d / 2] (unnormalised, two bf16 values a pair), then
+                                         // (max, sum) per head
     unsigned long long* fh;              // [max_batch][H] residual stream after attention
     unsigned long long* fa;              // [max_batch][N][F_s / 2] SwiGLU outputs, two bf16 values a pair
     int maxch;
