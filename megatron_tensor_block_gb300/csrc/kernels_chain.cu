@@ -10,15 +10,23 @@
 // GB300 design: one CTA per SM; a producer warp streams each CTA's weight and
 // KV tiles for all layers through a ring of 16 KB slots (TMA, 128-byte
 // swizzled 3-D boxes), so weights are in shared memory before the activation
-// they multiply exists. The consumer warps take a projection phase's slots as
-// independent tasks (a slot, or a K part of one when the CTA has fewer than
-// eight), each warp multiplying all rows of its slot with one operand load per
-// 16-byte unit; the tasks' partial sums meet in shared memory in a fixed order. Activations move between phases as 8-byte pairs
-// (float value, 32-bit epoch) written with one store: a consumer polls the
+// they multiply exists. A step with one or two loads per CTA (QKV, o_proj) is
+// computed a row per warp; a step with more (gate/up, down) splits its loads
+// into tasks, one load (or a K part of one) per warp, each warp multiplying
+// all rows of its load with one operand load per 16-byte unit, and the tasks'
+// partial sums meet in shared memory in a fixed order. One copy of the code
+// serves all four projection steps, since the launch's speed follows the
+// size of the code each layer runs.
+//
+// Activations move between steps as 8-byte pairs (a value, or two bf16
+// values, and a 32-bit epoch) written with one store: a consumer polls the
 // data itself, which replaces "store, fence, arrive, poll a counter, load"
-// by one round trip to L2 per phase. Every CTA that needs a whole vector
-// (the RMSNorm statistics, the split-KV combine) computes it itself from the
-// pairs instead of waiting for another CTA to do it.
+// by one round trip to L2 per step. The residual stream and q, k, v cross as
+// fp32; the SwiGLU outputs and the attention chunk outputs, which feed bf16
+// operands, cross as bf16 pairs, so that every step's input fits one round
+// trip. Every CTA that needs a whole vector (the RMSNorm statistics, the
+// split-KV combine) computes it itself from the pairs instead of waiting for
+// another CTA to do it.
 //
 // Phases of a layer and the CTA items of each (8 output rows per item; the
 // host balances the bytes of all items over the CTAs):
