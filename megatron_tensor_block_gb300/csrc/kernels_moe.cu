@@ -7,7 +7,7 @@
 //   route   : softmax top-k per token (chosen by logit, ties to the lower id),
 //             weights renormalised over the chosen experts
 //   bucket  : stable counting sort of the (token, choice) slots by expert
-//   prep    : x_t * gamma_r (bf16) for every slot and shard, 1/rms per slot
+//   prep    : per token, x_t * gamma_r (bf16) into each of its slots' rows, 1/rms per slot
 //   gate/up : per shard and expert it holds, streaming grouped GEMM over the
 //             expert's slots, SwiGLU epilogue
 //   down    : per shard and expert it holds, streaming grouped GEMM -> slot outputs
@@ -161,8 +161,11 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
     pdl_trigger();
     pdl_wait();
     __shared__ float wsum[8];
-    const int s = blockIdx.x, tid = threadIdx.x;
-    const int t = p.perm[s] / p.top_k;
+    __shared__ int s_slot[8];
+    const int t = blockIdx.x, tid = threadIdx.x, K = p.top_k, nslot = p.T * K;
+    if (tid < K) s_slot[tid] = p.slot_of[t * K + tid];
+    __syncthreads();
+    // one CTA per token: its sum of squares once, x * gamma_r written to each of its slots' rows
     const float* x = p.x + (size_t)t * p.H;
     float a = 0.f;
     for (int k = tid * 4; k < p.H; k += 1024) {
@@ -176,17 +179,19 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
             uint2 pk;
             pk.x = pack_bf16x2(v.x * g.x, v.y * g.y);
             pk.y = pack_bf16x2(v.z * g.z, v.w * g.w);
-            const size_t row = (size_t)r * p.T * p.top_k + s;
-            *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xs) + row * p.H + k) = pk;
+            for (int j = 0; j < K; ++j) {
+                const size_t row = (size_t)r * nslot + s_slot[j];
+                *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(p.xs) + row * p.H + k) = pk;
+            }
         }
     }
     a = warp_sum(a);
     if ((tid & 31) == 0) wsum[tid >> 5] = a;
     __syncthreads();
-    if (tid == 0) {
+    if (tid < K) {
         float ss = 0.f;
         for (int w = 0; w < 8; ++w) ss += wsum[w];
-        p.rinv[s] = 1.0f / sqrtf(ss / (float)p.H + p.eps);
+        p.rinv[s_slot[tid]] = 1.0f / sqrtf(ss / (float)p.H + p.eps);
     }
 }
 
@@ -516,7 +521,7 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
     if (same) q.xs_copies = 1;
     cudaError_t e = launch_small(reinterpret_cast<const void*>(moe_route_kernel), &q, (p.T + 7) / 8, 256, s);
     if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_bucket_kernel), &q, 1, 1024, s);
-    if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_prep_kernel), &q, p.T * p.top_k, 256, s);
+    if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_prep_kernel), &q, p.T, 256, s);
     if (e != cudaSuccess) return e;
     mark(1);
     const size_t smem = moe_gemm_smem(p.E);
