@@ -1462,9 +1462,11 @@ extern "C" tp_status tp_stack_create(tp_plan_t plan, int32_t n_layers, const tp_
     chain_split(hq_s * hd / 64, 15, A.kc[1], A.nl[1]);
     chain_split(H / 64, 7, A.kc[2], A.nl[2]);
     chain_split(F_s / 64, 15, A.kc[3], A.nl[3]);
-    for (int k = 0; k < 4; ++k)   // loads per item stay small (the kernel's item decoding assumes at most 64)
-        if ((k == 1 || k == 3 ? N : 1) * A.nl[k] > 64)
-            return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: %d loads per item of phase %d exceed 64", N * A.nl[k], k);
+    for (int k = 0; k < 4; ++k) {   // loads per item stay small (the kernel's item decoding assumes at most 64)
+        const int loads = (k == 1 || k == 3 ? N : 1) * A.nl[k];
+        if (loads > 64)
+            return fail(TP_ERR_UNSUPPORTED, "tp_stack_create: %d loads per item of phase %d exceed 64", loads, k);
+    }
     A.xa_stride = std::max(N * hq_s * hd, N * F_s) + 8;   // bf16 operands of o_proj and down
     size_t smem = 0;
     for (A.n_slots = kChainMaxSlots; A.n_slots >= 4; --A.n_slots) {
