@@ -8,9 +8,9 @@
 //             weights renormalised over the chosen experts
 //   bucket  : stable counting sort of the (token, choice) slots by expert
 //   prep    : per token, x_t * gamma_r (bf16) into each of its slots' rows, 1/rms per slot
-//   gate/up : per shard and expert it holds, streaming grouped GEMM over the
-//             expert's slots, SwiGLU epilogue
-//   down    : per shard and expert it holds, streaming grouped GEMM -> slot outputs
+//   gate/up : per shard and expert it holds, grouped GEMM on the tensor cores
+//             (tcgen05) over the expert's slots, SwiGLU epilogue
+//   down    : per shard and expert it holds, the same grouped GEMM -> slot outputs
 //   combine : y_t = x_t + sum_r ( sum_j w_tj * o[r][slot(t, j)] ), j then r; with
 //             expert parallelism shard r's sum keeps the choices of its experts
 #include <cuda.h>
@@ -19,23 +19,28 @@
 
 #include "common.cuh"
 #include "stream.cuh"
+#include "tcgen05.cuh"
 #include "tp_internal.h"
 
 namespace tpk {
 
-constexpr int kMoeTokPass = 32;                        // slots per pass of a unit (4 MMA column groups)
-constexpr int kMoeGroups = kMoeTokPass / 8;
-constexpr int kMoeXBytes = kMoeGroups * kBoxK * 8 * 2; // 4 activation boxes of 8 rows x 256
-constexpr int kMoeStageBytes = 2 * kBoxBytes + kMoeXBytes;
-constexpr int kMoeStages = 4;
-constexpr int kMoeTG = 4;                // down projection with one stage per tile: tiles per unit
-constexpr int kMoeTS = kMoeTokPass + 1;  // tile row stride in shared memory (column reads free of bank conflicts)
+// Expert GEMMs (tcgen05): weight tiles of 128 rows are the MMA's A operand,
+// a pass of at most kMtN of the expert's slots its N dimension.
+constexpr int kMtN = 32;                          // slots per pass (MMA N: 16 or 32)
+constexpr int kMtKB = 2;                          // K-blocks of 64 elements per stage
+constexpr int kMtA = 128 * 64 * 2;                // one K-block of a weight tile: 16 KB
+constexpr int kMtB = kMtN * 64 * 2;               // one K-block of a pass's slots: 4 KB
+constexpr int kMtStage = kMtKB * (kMtA + kMtB);   // 40 KB
+constexpr int kMtStages = 4;
+constexpr int kMtThreads = 192;                   // copy warp, MMA warp, four read-back warps
+constexpr int kMtCols = 2 * kMtN;                 // tensor-memory columns: two accumulator buffers
 constexpr int kMaxExperts = 256;         // router
 constexpr int kMaxBucketExperts = 64;    // bucketing (per-warp count table)
 
 struct MoeArgs {
-    CUtensorMap tw[TP_MAX_SHARDS];   // weights of the launch (egu or ed), 128-byte-swizzled boxes of 32 rows x 256
-    CUtensorMap tx[TP_MAX_SHARDS];   // activations in slot order (xs or act), swizzled boxes of 8 rows x 256
+    CUtensorMap tw[TP_MAX_SHARDS];   // weights of the launch (egu or ed), 128-byte-swizzled boxes 64 x 16 (gate/up)
+                                     // or 64 x 128 (down)
+    CUtensorMap tx[TP_MAX_SHARDS];   // activations in slot order (xs or act), 128-byte-swizzled boxes 64 x 8
     MoeParams p;
     int down;                        // 0: gate/up, 1: down
 };
@@ -195,234 +200,221 @@ __global__ void __launch_bounds__(256) moe_prep_kernel(const MoeParams p) {
     }
 }
 
-// ---------------------------------------------------------------- grouped streaming GEMM
+// ---------------------------------------------------------------- expert GEMMs
 //
-// Unit = (shard r, expert e, group of tiles of 64 rows). Gate/up: rows are 32
-// gate + the matching 32 up rows of the expert's shard slice, K = H, one tile
-// per unit. Down: 64 rows of H, K = Fs; when Fs fits one stage, a unit takes
-// kMoeTG tiles of the same expert, whose activation boxes arrive with the first
-// stage only and stay in registers for the rest. The expert's slots are
-// processed in passes of 32 (four 8-column MMA groups).
+// Unit = (shard r, expert it holds, tile of 128 weight rows). Down: 128 rows of
+// the expert's [H][Fs] slice, K = Fs. Gate/up: 64 gate rows and the matching 64
+// up rows, K = H, interleaved in 16-row groups (gate rows 16q.., then up rows
+// 16q..), so that tensor-memory lane quarter q holds 16 gate rows in lanes 0-15
+// and their up rows in lanes 16-31 and SwiGLU pairs them with one shuffle.
+//
+// The weight tile is the A operand of tcgen05.mma (M = 128, one row per
+// tensor-memory lane); the expert's slots, in passes of at most kMtN, are the
+// B operand (N = the pass rounded up to 16). The slots arrive in boxes of 8
+// rows; B rows past the pass's last box hold whatever the stage held before,
+// and the accumulator columns they produce are dropped (a column of the
+// product depends on its own B row only). fp32 accumulators live in tensor memory, in two
+// buffers, so that one unit's read-back overlaps the next unit's MMAs.
+//   warp 0, one thread: TMA copies, two K-blocks of 64 per stage, a ring of
+//           four stages (weights evict-first: read once)
+//   warp 1, one thread: the MMAs of a stage, then a commit that frees it
+//   warps 2-5: read lane quarter (warp % 4) of the accumulator back; down
+//           stores each slot's 128 outputs (fp32 partial of shard r), gate/up
+//           applies 1/rms and SwiGLU and stores the bf16 activations
+// Every wait is bounded; a CTA that gives up sets the status, lets its copies
+// land, waits for its MMAs and frees its tensor memory before it exits.
+
+struct MoeUnit {
+    int r, le, tb, off, cnt;
+};
+__device__ __forceinline__ MoeUnit moe_unit(const MoeParams& p, const int* s_off, int tiles, int u) {
+    MoeUnit m;
+    m.tb = u % tiles;
+    m.le = (u / tiles) % p.El;
+    m.r = u / (tiles * p.El);
+    const int e = p.ep ? m.r * p.El + m.le : m.le;   // global expert id (slot buckets)
+    m.off = s_off[e];
+    m.cnt = s_off[e + 1] - m.off;
+    return m;
+}
 
 // DOWN: the expert down projection (else gate/up + SwiGLU), one instantiation
 // each so that neither epilogue shapes the other's code.
 template <bool DOWN>
-__global__ void __launch_bounds__(kStreamThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeArgs A) {
+__global__ void __launch_bounds__(kMtThreads, 1) moe_gemm_kernel(const __grid_constant__ MoeArgs A) {
     const MoeParams& p = A.p;
     extern __shared__ __align__(1024) unsigned char smem[];
-    const Ring R = ring_setup(smem, kMoeStages);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kMtStages;
+    uint64_t* acc_full = empty + kMtStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* done = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     unsigned char* ring = smem + 1024;                  // swizzled boxes need 1024-byte alignment
-    float* tile = reinterpret_cast<float*>(ring + kMoeStages * kMoeStageBytes);   // [2][64][kMoeTS]
-    int* s_off = reinterpret_cast<int*>(tile + 2 * kTileRows * kMoeTS);           // [E+1]
-
+    int* s_off = reinterpret_cast<int*>(ring + kMtStages * kMtStage);   // [E+1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr bool down = DOWN;
-    const int nslot = p.T * p.top_k;
-    const int tiles = down ? p.H / kTileRows : (2 * p.Fs) / kTileRows;
-    const int K = down ? p.Fs : p.H;
-    const int spu = (K + kBoxK - 1) / kBoxK;
-    const int TG = (down && spu == 1) ? kMoeTG : 1;     // tiles per unit sharing the activation boxes
-    const int ngrp = (tiles + TG - 1) / TG;
-    const int U = p.N * p.El * ngrp;                   // units: (shard, expert it holds, tile group)
 
-    if (warp == kConsumers / 32) {                     // ---- producer
+    if (tid == 0) {
+        for (int i = 0; i < kMtStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);                // one arrival per read-back warp
+        }
+        mbar_init(done, 1);
+        *abort_flag = (smem_u32(ring) & 1023u) ? 1 : 0;
+        if (*abort_flag) set_status(p.status, TP_ERR_ALIGN);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kMtCols);
+    pdl_wait();                                         // routing, slot rows and activations of earlier kernels
+    for (int i = tid; i <= p.E; i += kMtThreads) s_off[i] = p.offsets[i];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int nslot = p.T * p.top_k;
+    const int K = DOWN ? p.Fs : p.H;
+    const int tiles = DOWN ? p.H / 128 : p.Fs / 64;
+    const int nst = K / (64 * kMtKB);                   // stages per pass
+    const int U = p.N * p.El * tiles;
+
+    if (warp == 0) {
         if (lane == 0) {
-            pdl_wait();                                // routing and activations come from earlier kernels
             const uint64_t pol = l2_evict_first_policy();
             uint32_t it = 0;
-            bool ok = (smem_u32(ring) & 1023u) == 0;
-            if (!ok) {
-                *R.abort = 1;
-                set_status(p.status, TP_ERR_ALIGN);
-            }
+            bool ok = !*abort_flag;
             for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-                const int tg = u % ngrp, le = (u / ngrp) % p.El, r = u / (ngrp * p.El);
-                const int e = p.ep ? r * p.El + le : le;     // global expert id (slot buckets)
-                const int ntg = min(TG, tiles - tg * TG);
-                const int off = p.offsets[e], cnt = p.offsets[e + 1] - off;
-                for (int ps = 0; ps < cnt && ok; ps += kMoeTokPass) {
-                    const int ng = min(kMoeGroups, (cnt - ps + 7) / 8);
-                    for (int i = 0; i < ntg && ok; ++i) {
-                        const int tb = tg * TG + i;
-                        int rowa, rowb;
-                        if (down) {
-                            rowa = le * p.H + tb * kTileRows;
-                            rowb = rowa + 32;
-                        } else {
-                            rowa = le * 2 * p.Fs + tb * 32;
-                            rowb = rowa + p.Fs;
+                const MoeUnit m = moe_unit(p, s_off, tiles, u);
+                const int row0 = DOWN ? m.le * p.H + m.tb * 128 : m.le * 2 * p.Fs + m.tb * 64;
+                for (int ps = 0; ps < m.cnt && ok; ps += kMtN) {
+                    const int nb = (min(kMtN, m.cnt - ps) + 7) / 8;     // 8-slot boxes of the pass
+                    for (int st = 0; st < nst; ++st, ++it) {
+                        const int s = it % kMtStages;
+                        if (!mbar_wait(&empty[s], ((it / kMtStages) & 1) ^ 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
                         }
-                        const int nx = (TG == 1 || i == 0) ? ng : 0;    // activation boxes of this stage
-                        for (int st = 0; st < spu; ++st, ++it) {
-                            const int sl = it % kMoeStages;
-                            if (!mbar_wait(&R.empty[sl], ((it / kMoeStages) & 1) ^ 1, R.abort, p.status)) {
-                                ok = false;
-                                break;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(kMtKB * (kMtA + nb * 1024)));
+                        unsigned char* sa = ring + s * kMtStage;
+                        unsigned char* sb = sa + kMtKB * kMtA;
+                        for (int kb = 0; kb < kMtKB; ++kb) {
+                            const int x = (st * kMtKB + kb) * 64;
+                            if (DOWN) {
+                                tma_load_2d(sa + kb * kMtA, &A.tw[m.r], x, row0, &full[s], pol);
+                            } else {
+                                // 16-row groups: gate rows 16q.., then up rows 16q.. (2 KB each)
+                                for (int q = 0; q < 4; ++q) {
+                                    tma_load_2d(sa + kb * kMtA + q * 4096, &A.tw[m.r], x, row0 + 16 * q, &full[s], pol);
+                                    tma_load_2d(sa + kb * kMtA + q * 4096 + 2048, &A.tw[m.r], x, row0 + p.Fs + 16 * q,
+                                                &full[s], pol);
+                                }
                             }
-                            mbar_arrive_expect_tx(&R.full[sl], 2u * kBoxBytes + (uint32_t)nx * kBoxK * 8 * 2);
-                            unsigned char* dst = ring + sl * kMoeStageBytes;
-                            tma_load_3d_hint(dst, &A.tw[r], 0, st * (kBoxK / 64), rowa, &R.full[sl], pol);
-                            tma_load_3d_hint(dst + kBoxBytes, &A.tw[r], 0, st * (kBoxK / 64), rowb, &R.full[sl], pol);
-                            for (int g = 0; g < nx; ++g)
-                                tma_load_3d_keep(dst + 2 * kBoxBytes + g * kBoxK * 8 * 2, &A.tx[r], 0,
-                                                 st * (kBoxK / 64), off + ps + 8 * g, &R.full[sl]);
+                            for (int i = 0; i < nb; ++i)
+                                tma_load_2d_keep(sb + kb * kMtB + i * 1024, &A.tx[m.r], x, m.off + ps + 8 * i, &full[s]);
                         }
                     }
                 }
             }
             pdl_trigger();
-            if (!ok || *R.abort) producer_drain(R, it, kMoeStages);
+            // no copy may still be landing when the CTA exits
+            volatile int no_abort = 0;
+            for (uint32_t k = it > (uint32_t)kMtStages ? it - kMtStages : 0u; k < it; ++k)
+                mbar_wait(&full[k % kMtStages], (k / kMtStages) & 1, &no_abort, nullptr);
         }
-        return;
-    }
-
-    // ---- consumers
-    pdl_wait();
-    for (int i = tid; i <= p.E; i += kConsumers) s_off[i] = p.offsets[i];
-    consumer_sync(kConsumers);
-    const int wm = warp & 3, wk = warp >> 2;
-    const int g = lane >> 2, tq = lane & 3;
-    const int box = wm >> 1, brow = 16 * (wm & 1) + g;
-    uint32_t it = 0, ntile = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int tg = u % ngrp, le = (u / ngrp) % p.El, r = u / (ngrp * p.El);
-        const int e = p.ep ? r * p.El + le : le;
-        const int ntg = min(TG, tiles - tg * TG);
-        const int off = s_off[e], cnt = s_off[e + 1] - off;
-        for (int ps = 0; ps < cnt; ps += kMoeTokPass) {
-            const int ng = min(kMoeGroups, (cnt - ps + 7) / 8);
-            uint4 xr[2][2][kMoeGroups];                 // activation fragments (kept across a unit's tiles)
-            for (int i = 0; i < ntg; ++i) {
-                const int tb = tg * TG + i;
-                float c[kMoeGroups][4];
-#pragma unroll
-                for (int q = 0; q < kMoeGroups; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
-                for (int st = 0; st < spu; ++st, ++it) {
-                    const int sl = it % kMoeStages;
-                    mbar_wait(&R.full[sl], (it / kMoeStages) & 1, R.abort, p.status);
-                    __syncwarp();
-                    const int steps_here = min(kBoxK / kKStep, (K - st * kBoxK) / kKStep);
-                    // 128-byte-swizzled boxes: 16-byte unit u of the 128-byte row (row, chunk c)
-                    // sits at unit u ^ ((4 * row + c) & 7); every row a lane reads has parity g & 1
-                    const unsigned char* stage = ring + sl * kMoeStageBytes;
-                    const unsigned char* wA = stage + box * kBoxBytes + brow * (kBoxK * 2);
-                    const unsigned char* wB = wA + 8 * (kBoxK * 2);
-                    if (TG == 1 || i == 0) {
-#pragma unroll
-                        for (int s2 = 0; s2 < 2; ++s2)
-#pragma unroll
-                            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                                for (int q = 0; q < kMoeGroups; ++q)
-                                    if (wk + 2 * s2 < steps_here && q < ng) {
-                                        const int step = wk + 2 * s2;
-                                        xr[s2][h][q] = *reinterpret_cast<const uint4*>(
-                                            stage + 2 * kBoxBytes + q * kBoxK * 16 + g * (kBoxK * 2) + step * 128 +
-                                            ((h ^ (g & 1)) << 6) + ((tq ^ step) << 4));
-                                    }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, acc_i = 0;
+            bool ok = !*abort_flag;
+            for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+                const MoeUnit m = moe_unit(p, s_off, tiles, u);
+                for (int ps = 0; ps < m.cnt && ok; ps += kMtN, ++acc_i) {
+                    const int n16 = (min(kMtN, m.cnt - ps) + 15) & ~15;
+                    const uint32_t idesc = idesc_bf16(128, n16);
+                    const int buf = acc_i & 1;
+                    if (!mbar_wait(&acc_empty[buf], ((acc_i >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
                     }
-#pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int step = wk + 2 * s2;
-                        if (step < steps_here) {
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int off_w = step * 128 + ((h ^ (g & 1)) << 6) + ((tq ^ step) << 4);
-                                const uint4 a = *reinterpret_cast<const uint4*>(wA + off_w);
-                                const uint4 b = *reinterpret_cast<const uint4*>(wB + off_w);
-#pragma unroll
-                                for (int q = 0; q < kMoeGroups; ++q) {
-                                    if (q < ng) {
-                                        const uint4 xv = xr[s2][h][q];
-                                        mma_bf16_16816(c[q], a.x, b.x, a.y, b.y, xv.x, xv.y);
-                                        mma_bf16_16816(c[q], a.z, b.z, a.w, b.w, xv.z, xv.w);
-                                    }
-                                }
-                            }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(buf * kMtN);
+                    for (int st = 0; st < nst; ++st, ++it) {
+                        const int s = it % kMtStages;
+                        if (!mbar_wait(&full[s], (it / kMtStages) & 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(ring + s * kMtStage), b0 = a0 + kMtKB * kMtA;
+#pragma unroll
+                        for (int kb = 0; kb < kMtKB; ++kb)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma(d, smem_desc_sw128(a0 + kb * kMtA + k * 32), smem_desc_sw128(b0 + kb * kMtB + k * 32),
+                                       idesc, (st | kb | k) != 0);
+                        tc_commit(smem_u32(&empty[s]));
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&R.empty[sl]);
+                    if (ok) tc_commit(smem_u32(&acc_full[buf]));
                 }
-                if constexpr (DOWN) {
-                    // the second K half parks its sums in one of two tile buffers; after one barrier the
-                    // first half adds them (half 0 + half 1) and stores the expert's output rows from
-                    // registers: lanes g = 0..7 write 8 consecutive rows of one slot. The next tile
-                    // writes the other buffer, so no barrier is needed after the reads.
-                    float* tb2 = tile + (ntile & 1) * (kTileRows * kMoeTS);
-                    ++ntile;
-                    if (wk == 1) {
+            }
+            tc_commit(smem_u32(done));                  // fires when every issued MMA has completed
+        }
+    } else {
+        const int q = warp & 3;                         // tensor-memory lane quarter of this warp
+        uint32_t acc_i = 0;
+        bool ok = !*abort_flag;
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+            const MoeUnit m = moe_unit(p, s_off, tiles, u);
+            for (int ps = 0; ps < m.cnt && ok; ps += kMtN, ++acc_i) {
+                const int n = min(kMtN, m.cnt - ps), buf = acc_i & 1;
+                if (!mbar_wait(&acc_full[buf], (acc_i >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * kMtN), v);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);    // the buffer may take the next unit
+                const size_t slot0 = (size_t)m.r * nslot + m.off + ps;
+                if (DOWN) {
+                    // lane = output row 128 tb + 32 q + lane; 32 lanes store 128 consecutive bytes per slot
+                    float* o = p.o + slot0 * p.H + m.tb * 128 + 32 * q + lane;
 #pragma unroll
-                        for (int q = 0; q < kMoeGroups; ++q) {
-                            const int c0 = 8 * q + 2 * tq;
-                            const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
-                            tb2[i0] = c[q][0];
-                            tb2[i0 + 1] = c[q][1];
-                            tb2[i1] = c[q][2];
-                            tb2[i1 + 1] = c[q][3];
-                        }
-                    }
-                    consumer_sync(kConsumers);
-                    if (wk == 0) {
-                        const int nt = min(kMoeTokPass, cnt - ps);
-                        const int row0 = tb * kTileRows + 16 * wm + g;
-#pragma unroll
-                        for (int q = 0; q < kMoeGroups; ++q) {
-                            const int c0 = 8 * q + 2 * tq;
-                            const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
-#pragma unroll
-                            for (int e2 = 0; e2 < 2; ++e2) {
-                                if (c0 + e2 < nt) {
-                                    float* o = p.o + ((size_t)r * nslot + off + ps + c0 + e2) * p.H + row0;
-                                    o[0] = c[q][e2] + tb2[i0 + e2];
-                                    o[8] = c[q][2 + e2] + tb2[i1 + e2];
-                                }
-                            }
-                        }
-                    }
+                    for (int c = 0; c < kMtN; ++c)
+                        if (c < n) o[(size_t)c * p.H] = __uint_as_float(v[c]);
                 } else {
-                    // gate/up: tile[row][slot] = half 0 + half 1
+                    // lanes 0-15: gate rows j = 64 tb + 16 q + lane; lanes 16-31: the same rows' up values
+                    const float rl = lane < n ? p.rinv[m.off + ps + lane] : 0.f;
+                    bf16* act = reinterpret_cast<bf16*>(p.act) + slot0 * p.Fs + m.tb * 64 + 16 * q + lane;
 #pragma unroll
-                    for (int q = 0; q < kMoeGroups; ++q) {
-                        const int c0 = 8 * q + 2 * tq;
-                        const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
-                        if (wk == 0) {
-                            tile[i0] = c[q][0];
-                            tile[i0 + 1] = c[q][1];
-                            tile[i1] = c[q][2];
-                            tile[i1 + 1] = c[q][3];
+                    for (int c = 0; c < kMtN; ++c) {
+                        const float rv = __shfl_sync(0xffffffffu, rl, c);
+                        const float upv = __shfl_down_sync(0xffffffffu, __uint_as_float(v[c]), 16);
+                        if (c < n && lane < 16) {
+                            const float gt = __uint_as_float(v[c]) * rv, up = upv * rv;
+                            act[(size_t)c * p.Fs] = __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
                         }
                     }
-                    consumer_sync(kConsumers);
-#pragma unroll
-                    for (int q = 0; q < kMoeGroups; ++q) {
-                        const int c0 = 8 * q + 2 * tq;
-                        const int i0 = (16 * wm + g) * kMoeTS + c0, i1 = (16 * wm + g + 8) * kMoeTS + c0;
-                        if (wk == 1) {
-                            tile[i0] += c[q][0];
-                            tile[i0 + 1] += c[q][1];
-                            tile[i1] += c[q][2];
-                            tile[i1 + 1] += c[q][3];
-                        }
-                    }
-                    consumer_sync(kConsumers);
-                    {
-                        const int nt = min(kMoeTokPass, cnt - ps);
-                        bf16* act = reinterpret_cast<bf16*>(p.act);
-                        for (int i2 = tid; i2 < 32 * nt; i2 += kConsumers) {   // 32 consecutive outputs per slot
-                            const int q = i2 >> 5, j = i2 & 31;
-                            const int slot = off + ps + q;
-                            const float rv = p.rinv[slot];
-                            const float gt = tile[j * kMoeTS + q] * rv;
-                            const float up = tile[(j + 32) * kMoeTS + q] * rv;
-                            act[((size_t)r * nslot + slot) * p.Fs + tb * 32 + j] =
-                                __float2bfloat16_rn(gt / (1.0f + expf(-gt)) * up);
-                        }
-                    }
-                    consumer_sync(kConsumers);
                 }
             }
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        volatile int no_abort = 0;                      // every MMA has retired before the columns are freed
+        mbar_wait(done, 0, &no_abort, nullptr);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kMtCols);
+        tmem_relinquish();
     }
 }
 
@@ -498,10 +490,7 @@ __global__ void __launch_bounds__(kCombineCols / 4) moe_combine_kernel(const Moe
 
 // ---------------------------------------------------------------- launch sequence
 
-static size_t moe_gemm_smem(int E) {
-    return 1024 + (size_t)kMoeStages * kMoeStageBytes + (size_t)2 * kTileRows * kMoeTS * 4 +
-           (size_t)(E + 1) * 4 + 16;
-}
+static size_t moe_gemm_smem(int E) { return 1024 + (size_t)kMtStages * kMtStage + (size_t)(E + 1) * 4 + 16; }
 
 static cudaError_t launch_small(const void* fn, void* arg, int grid, int threads, cudaStream_t s) {
     void* args[] = {arg};
@@ -524,6 +513,8 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
     if (e == cudaSuccess) e = launch_small(reinterpret_cast<const void*>(moe_prep_kernel), &q, p.T, 256, s);
     if (e != cudaSuccess) return e;
     mark(1);
+    // the expert GEMMs take K in stages of 128 and weight tiles of 128 rows
+    if (p.H % 128 || p.Fs % 128 || p.E > kMaxBucketExperts) return cudaErrorInvalidValue;
     const size_t smem = moe_gemm_smem(p.E);
     static int set_bytes = -1;
     if ((int)smem > set_bytes) {
@@ -541,25 +532,23 @@ cudaError_t launch_moe(const MoeParams& p, cudaStream_t s, cudaEvent_t const* ma
         A.down = down;
         for (int r = 0; r < p.N; ++r) {
             if (down) {
-                e = step_stage_map(p.ed[r], p.Fs, p.El * p.H, 32, &A.tw[r]);
+                e = tensor_map_2d(p.ed[r], p.Fs, (long)p.El * p.H, 64, 128, 1, &A.tw[r]);
                 if (e == cudaSuccess)
-                    e = step_stage_map(static_cast<const bf16*>(p.act) + (size_t)r * nslot * p.Fs, p.Fs, (int)nslot, 8,
-                                       &A.tx[r]);
+                    e = tensor_map_2d(static_cast<const bf16*>(p.act) + (size_t)r * nslot * p.Fs, p.Fs, nslot, 64, 8, 1,
+                                      &A.tx[r]);
             } else {
-                e = step_stage_map(p.egu[r], p.H, p.El * 2 * p.Fs, 32, &A.tw[r]);
+                e = tensor_map_2d(p.egu[r], p.H, (long)p.El * 2 * p.Fs, 64, 16, 1, &A.tw[r]);
                 if (e == cudaSuccess)
-                    e = step_stage_map(static_cast<const bf16*>(p.xs) + (size_t)(q.xs_copies > 1 ? r : 0) * nslot * p.H,
-                                       p.H, (int)nslot, 8, &A.tx[r]);
+                    e = tensor_map_2d(static_cast<const bf16*>(p.xs) + (size_t)(q.xs_copies > 1 ? r : 0) * nslot * p.H,
+                                      p.H, nslot, 64, 8, 1, &A.tx[r]);
             }
             if (e != cudaSuccess) return e;
         }
-        const int tiles = down ? p.H / kTileRows : 2 * p.Fs / kTileRows;
-        const int TG = (down && (p.Fs + kBoxK - 1) / kBoxK == 1) ? kMoeTG : 1;
-        const int U = p.N * p.El * ((tiles + TG - 1) / TG);
+        const int U = p.N * p.El * (down ? p.H / 128 : p.Fs / 64);
         void* args[] = {&A};
         const void* fn = down ? reinterpret_cast<const void*>(moe_gemm_kernel<true>)
                               : reinterpret_cast<const void*>(moe_gemm_kernel<false>);
-        e = launch_pdl(fn, args, U < kSMs ? U : kSMs, smem, s, kStreamThreads);
+        e = launch_pdl(fn, args, U < kSMs ? U : kSMs, smem, s, kMtThreads);
         if (e != cudaSuccess) return e;
         mark(2 + down);
     }
