@@ -28,6 +28,21 @@ def _skewed(w, seed):
     return inp
 
 
+# per-expert slot counts around the expert GEMM's 8-slot boxes and 32-slot passes
+PASS_COUNTS = [1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65, 0, 2]
+
+
+def _counts(w, counts, seed):
+    """Top-1 inputs whose routing gives expert e exactly counts[e] tokens (in a
+    seeded random token order)."""
+    assert w.top_k == 1 and len(counts) == w.n_experts and sum(counts) == w.tokens
+    inp = synth.make_inputs(w)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    owner = rng.permutation(np.repeat(np.arange(w.n_experts), counts))
+    inp["router_logits"][np.arange(w.tokens), owner] += 20.0
+    return inp
+
+
 CASES = {
     "moe_expert_slice_tp4": lambda: synth.make_inputs(MOE),
     "moe_small_tp2_skewed_ragged": lambda: _skewed(
@@ -40,6 +55,13 @@ CASES = {
     "moe_ep_small_tp2_skewed_ragged": lambda: _skewed(
         synth.scaled(MOE, hidden=512, n_experts=16, top_k=2, expert_ffn=512, tp=2, batch=90, seed=44,
                      expert_parallel=1), 6),
+    # expert slot counts at and around the 8-slot box and 32-slot pass boundaries (and an empty expert)
+    "moe_pass_boundaries_tp2": lambda: _counts(
+        synth.scaled(MOE, hidden=256, n_experts=16, top_k=1, expert_ffn=512, tp=2, batch=sum(PASS_COUNTS), seed=46),
+        PASS_COUNTS, 7),
+    "moe_ep_pass_boundaries_tp2": lambda: _counts(
+        synth.scaled(MOE, hidden=256, n_experts=16, top_k=1, expert_ffn=256, tp=2, batch=sum(PASS_COUNTS), seed=47,
+                     expert_parallel=1), PASS_COUNTS, 8),
     # expert parallelism over 8 shards, 2 experts each
     "moe_ep_tp8": lambda: synth.make_inputs(
         synth.scaled(MOE, hidden=512, n_experts=16, top_k=4, expert_ffn=256, tp=8, batch=33, seed=45,
