@@ -360,6 +360,21 @@ def test_block_tpN_detects_a_wrong_shard_index():
     assert O.relerr(got, ref) > 1e-3
 
 
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_kv_cache_shards_are_the_kv_heads_of_the_shards_q_heads(N):
+    # The shards concatenate back to the cache along the head axis, and the KV
+    # heads a shard holds are exactly those its q heads read under GQA (q head
+    # j reads KV head j // (Hq / Hkv)), found here by brute force over the heads.
+    B, Hq, Hkv, Lk, d = 2, 16, 4, 5, 3
+    cache = rng(81).standard_normal((B, Hkv, Lk, d))
+    shards = O.shard_kv_cache(cache, N)
+    assert np.array_equal(np.concatenate(shards, axis=1), cache)
+    for r, sh in enumerate(shards):
+        q_heads = range(r * Hq // N, (r + 1) * Hq // N)
+        needed = sorted({j // (Hq // Hkv) for j in q_heads})
+        assert np.array_equal(sh, cache[:, needed])
+
+
 def test_divisibility_rule():
     with pytest.raises(ValueError):
         O.check_divisible(synth.WORKLOADS["qwen25_05b_decode_tp2"], 4)  # 14 heads, 2 kv heads
